@@ -1,0 +1,101 @@
+"""Draft-tree structure (oracle).
+
+Restates PTD (Progressive Tree Drafting, arXiv 2607.10661) §3.1 "tree construction":
+the draft is a tree T = (V, E); each node v may attend only to its observable prefix
+set pi(v) = {v} U pi(P(v)), P(v) its unique parent; the position encoding of v is fixed
+by |pi(v)| so that the tree input stays compatible with causal attention.
+
+Readings (the pages leave these open):
+  * node 0 is the root (the last committed token), parent[0] = -1, and every other
+    node has 0 <= parent[i] < i; a forest or a back edge is rejected;
+  * pi(root) = {root};
+  * position id = P + |pi(v)| - 1 (0-based, P = committed prefix length), i.e. the root
+    sits at position P, right after the prefix;
+  * children are ordered by node index.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def validate(parent) -> None:
+    parent = [int(x) for x in parent]
+    if len(parent) < 1:
+        raise ValueError("empty tree")
+    if parent[0] != -1:
+        raise ValueError("node 0 must be the root (parent -1)")
+    for i in range(1, len(parent)):
+        if not (0 <= parent[i] < i):
+            raise ValueError(f"parent[{i}] = {parent[i]} violates 0 <= parent[i] < i")
+
+
+def observable_set(parent, v: int) -> frozenset:
+    """pi(v) = {v} U pi(P(v)), written as the recursion it is."""
+    p = int(parent[v])
+    if p < 0:
+        return frozenset({v})
+    return frozenset({v}) | observable_set(parent, p)
+
+
+def root_path(parent, v: int) -> list:
+    """Nodes on the root -> v path, root first (the ancestor set in sequence order)."""
+    out = []
+    while v >= 0:
+        out.append(int(v))
+        v = int(parent[v])
+    return out[::-1]
+
+
+def depth(parent) -> np.ndarray:
+    """Edges from the root: |pi(v)| - 1."""
+    validate(parent)
+    return np.array([len(observable_set(parent, v)) - 1 for v in range(len(parent))], dtype=np.int32)
+
+
+def position_ids(parent, prefix_len: int) -> np.ndarray:
+    """0-based position of each node: P + |pi(v)| - 1."""
+    return (prefix_len + depth(parent)).astype(np.int32)
+
+
+def visibility(parent) -> np.ndarray:
+    """Boolean [N][N]: entry (i, j) is True iff j is in pi(i)."""
+    validate(parent)
+    n = len(parent)
+    vis = np.zeros((n, n), dtype=bool)
+    for i in range(n):
+        for j in observable_set(parent, i):
+            vis[i, j] = True
+    return vis
+
+
+def packed_mask(parent) -> np.ndarray:
+    """uint32 [N][ceil(N/32)]: bit (j % 32) of word j // 32 set iff j in pi(i)."""
+    vis = visibility(parent)
+    n = vis.shape[0]
+    w = (n + 31) // 32
+    out = np.zeros((n, w), dtype=np.uint32)
+    for i in range(n):
+        for j in range(n):
+            if vis[i, j]:
+                out[i, j // 32] |= np.uint32(1) << np.uint32(j % 32)
+    return out
+
+
+def children(parent) -> list:
+    """children[u] = nodes whose parent is u, in ascending node index."""
+    n = len(parent)
+    out = [[] for _ in range(n)]
+    for i in range(1, n):
+        out[int(parent[i])].append(i)
+    return out
+
+
+def child_csr(parent):
+    """(offsets [N+1], child index list) with each node's children in ascending order."""
+    ch = children(parent)
+    off = np.zeros(len(parent) + 1, dtype=np.int32)
+    idx = []
+    for u, cs in enumerate(ch):
+        off[u + 1] = off[u] + len(cs)
+        idx.extend(cs)
+    return off, np.array(idx, dtype=np.int32)
