@@ -1,0 +1,561 @@
+#!/usr/bin/env python3
+"""Throughput of one tree-verification round on GB300.
+
+A step = one pass of the hot path over one batch of seeded synthetic input:
+    tv_select_subtree (pool -> tree)  ->  tv_tree_attention  ->  tv_verify_greedy
+(the sampling workload runs tv_verify_sample instead of the greedy verify).
+Metric: verified tree nodes per second = B * N / step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and a device
+synchronise on both sides, timed with CUDA events on the launching stream.  Steps are
+CUDA-graph replays; the inputs rotate over enough copies that their total exceeds twice
+the L2, so no step reads its inputs from L2.  Under torchrun every rank runs its own
+replica (the path shards by independent sequences; there is no data-path collective),
+the max time over ranks is used and rank 0 prints one JSON line.
+
+``--impl reference`` times the CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified tree nodes/sec (attn+accept) and achieved HBM GB/s vs GB300 peak"
+UNIT = "nodes/s"
+DEFAULT_WORKLOAD = "qwen3_4b_layer"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-worker", type=float, default=None, help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------------
+# distributed plumbing (timing only: barrier and max over ranks)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_init(backend):
+    rank, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------
+# oracle sample (CPU baseline and the reference arm)
+
+def oracle_step_factory(workload: str):
+    """Build the oracle's inputs for ``workload`` (oracle selection + synthetic data of the
+    same recipe) and return (step, description).  One oracle step is a fixed slice of the
+    verification of sequence 0: the attention row of one (node, head) pair; the step that
+    completes a node's heads also takes that node's vocab row, and the step that completes
+    the tree also runs the subtree selection and the acceptance walk.  A step therefore
+    counts as 1/Hq of a verified node."""
+    import numpy as np
+
+    import synth
+    import synth.workloads as W
+    from oracle import attention, greedy, sampling, selection, vocab
+
+    cfg = W.WORKLOADS[workload]
+    g = synth.rng(cfg["seed"])
+    B, Hq, Hkv, D, P, V = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["P"], cfg["V"]
+    if "pool_d" in cfg:
+        N = cfg.get("N") or max(cfg["budgets"])
+        marg, ptok = W.pools(g, 1, cfg["pool_d"], cfg["pool_k"], V)
+        sel = selection.select_subtree(marg[0], ptok[0], N, 11)
+        par, tok = sel["parent"][None], sel["token"][None]
+    else:
+        N = cfg["N"]
+        marg = None
+        par, tok = W.trees(g, 1, N, cfg["depth_cap"], V)
+    bf16 = cfg["bf16"]
+    if cfg["mode"] == "sample":
+        tgt, drf, tok = W.sampling_logits(g, par, V, bf16, cfg["temperature"])
+        logits = tgt
+    else:
+        logits = W.planted_logits(g, par, tok, V, bf16)
+        _, _, argmax_all = vocab.vocab_stats(logits[0])  # set-up: lets the walk run every tree
+    q, k, v = (x.astype(np.float64) for x in W.qkv_host(g, 1, Hq, Hkv, D, P, N, bf16))
+
+    def step(i):
+        node = (i // Hq) % N
+        head = i % Hq
+        attention.tree_attention(q, k, v, par, P, nodes=[node], heads=[head])
+        if head == Hq - 1:
+            vocab.row_stats(logits[0][node])
+            if node == N - 1:
+                if marg is not None:
+                    selection.select_subtree(marg[0], ptok[0], N, 11)
+                if cfg["mode"] == "sample":
+                    sampling.sampling_walk(tgt[0], drf[0], par[0], tok[0], cfg["temperature"], 1, i, 0)
+                else:
+                    greedy.greedy_walk(par[0], tok[0], argmax_all)
+        return 1.0 / Hq
+
+    desc = (f"{workload}, sequence 0 (N={N}, Hq={Hq}, P={P}, V={V}): one oracle step = the float64 attention "
+            f"row of one (node, head) pair; every {Hq}th step adds that node's vocab row, every {N * Hq}th step "
+            f"the subtree selection and acceptance walk; a step counts as 1/{Hq} node")
+    return step, desc
+
+
+def oracle_worker(budget_s: float, workload: str):
+    step, desc = oracle_step_factory(workload)
+    nodes = 0
+    i = 0
+    t0 = time.perf_counter()
+    while True:
+        nodes += step(i)
+        i += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    print(json.dumps({"value": nodes / dt, "steps": i, "seconds": dt, "sample": desc}))
+
+
+def run_oracle_subprocess(budget_s: float, workload: str) -> dict:
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[var] = "1"
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    res = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker", str(budget_s), "--workload",
+                          workload], capture_output=True, text=True, env=env, timeout=900)
+    if res.returncode != 0:
+        raise RuntimeError("oracle worker failed:\n" + res.stderr[-2000:])
+    out = json.loads(res.stdout.strip().splitlines()[-1])
+    return {"value": out["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": out["sample"] + f"; {out['steps']} steps in {out['seconds']:.1f} s, single-threaded NumPy"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    step, desc = oracle_step_factory(args.workload)
+    for i in range(args.warmup):
+        step(i)
+    nodes = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        nodes += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = nodes / dt
+    import synth.workloads as W
+    cfg = W.WORKLOADS[args.workload]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.workload, cfg),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------
+# GPU arm
+
+
+def workload_config(name, cfg):
+    keys = ("B", "Hq", "Hkv", "D", "P", "N", "V", "mode")
+    c = {"workload": name}
+    c.update({k: cfg[k] for k in keys if k in cfg})
+    if "pool_d" in cfg:
+        c["pool"] = f"{cfg['pool_d']}x{cfg['pool_k']}"
+        c.setdefault("N", cfg.get("N"))
+    c["dtype"] = "bf16" if cfg["bf16"] else "f32"
+    return c
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", self.gpu_id, "-lms", "50"], stdout=self.tmp,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        lines = [ln.strip() for ln in self.tmp.read().splitlines() if ln.strip()]
+        self.tmp.close()
+        os.unlink(self.tmp.name)
+        sms, maxs, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxs.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": max(maxs) if maxs else None,
+                "reasons": sorted(reasons), "samples": len(sms), "power_w_max": max(power) if power else None}
+
+
+def gpu_identifier(torch, device_index):
+    try:
+        uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        if uuid:
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[device_index]
+    return str(device_index)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "tree_speculative_decoding_masked_gb300", "csrc", ent["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return ent["bytes_per_launch"] if h == ent["source_sha256_16"] else None
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import synth
+    import synth.workloads as W
+    import tree_speculative_decoding_masked_gb300 as tv
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # before any GPU work: the oracle runs in its own single-threaded process
+        cpu_base = run_oracle_subprocess(15.0, args.workload)
+    rank, world = dist_init("nccl")
+    tv.load_library()
+
+    cfg = W.WORKLOADS[args.workload]
+    bf16 = cfg["bf16"]
+    tdt = torch.bfloat16 if bf16 else torch.float32
+    B, Hq, Hkv, D, P, V = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["P"], cfg["V"]
+    sampling_mode = cfg["mode"] == "sample"
+    g = synth.rng(cfg["seed"] + rank)
+
+    def to_dev(x):
+        if bf16:
+            bits = synth.bf16_bits(x)
+            return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(x).to(dev)
+
+    # ---- inputs (one set on the host; device copies rotate)
+    use_pool = "pool_d" in cfg
+    if use_pool:
+        N = cfg.get("N") or max(cfg["budgets"])
+        marg, ptok = W.pools(g, B, cfg["pool_d"], cfg["pool_k"], V)
+        marg_d, ptok_d = torch.from_numpy(marg).to(dev), torch.from_numpy(ptok).to(dev)
+        root_d = torch.full((B,), 11, dtype=torch.int32, device=dev)
+        sel = tv.select_subtree(marg_d, ptok_d, N, root_d)
+        torch.cuda.synchronize()
+        par = sel["parent"].cpu().numpy()
+        tok = sel["tokens"].cpu().numpy()
+    else:
+        N = cfg["N"]
+        par, tok = W.trees(g, B, N, cfg["depth_cap"], V)
+    if sampling_mode:
+        tgt, drf, tok = W.sampling_logits(g, par, V, bf16, cfg["temperature"])
+    else:
+        tgt = W.planted_logits(g, par, tok, V, bf16)
+        drf = None
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, bf16)
+    host = {"q": q, "k": k, "v": v, "logits": tgt}
+    if drf is not None:
+        host["draft"] = drf
+    if use_pool:
+        host["marg"], host["ptok"] = marg, ptok
+
+    elt = 2 if bf16 else 4
+    bytes_attn = (B * Hkv * (P + N) * D * 2 + 2 * B * Hq * N * D) * elt
+    bytes_vocab = B * N * V * elt * (2 if sampling_mode else 1)
+    bytes_set = bytes_attn + bytes_vocab
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(2, -(-2 * l2 // bytes_set))
+    base = {kk: to_dev(vv) if kk in ("q", "k", "v", "logits", "draft") else torch.from_numpy(vv).to(dev)
+            for kk, vv in host.items()}
+    sets = [base] + [{kk: t.clone() for kk, t in base.items()} for _ in range(n_sets - 1)]
+    par_d = torch.from_numpy(par.astype(np.int32)).to(dev)
+    tok_d = torch.from_numpy(tok.astype(np.int32)).to(dev)
+    for s in sets:
+        s["out"] = torch.empty(B, Hq, N, D, dtype=tdt, device=dev)
+        s["root"] = torch.full((B,), 11, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_attn = torch.zeros(max(256, tv.tree_attention_workspace_size(B, Hq, Hkv, D, P, N, tdt)), dtype=torch.uint8,
+                          device=dev)
+    ws_ver = torch.zeros(tv.verify_workspace_size(B, N, V, tdt, sampling_mode), dtype=torch.uint8, device=dev)
+    sel_out = {"parent": par_d.clone(), "tokens": tok_d.clone(),
+               "depth": torch.empty(B, N, dtype=torch.int32, device=dev),
+               "score": torch.empty(B, N, dtype=torch.float32, device=dev),
+               "n_nodes": torch.empty(B, dtype=torch.int32, device=dev)}
+    ver_out = {"accepted_nodes": torch.empty(B, N, dtype=torch.int32, device=dev),
+               "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+               "bonus_token": torch.empty(B, dtype=torch.int32, device=dev),
+               "out_token": torch.empty(B, dtype=torch.int32, device=dev),
+               "p_draft": torch.empty(B, N, dtype=torch.float32, device=dev),
+               "q_draft": torch.empty(B, N, dtype=torch.float32, device=dev)}
+
+    def k_select(s):
+        if use_pool:
+            tv.select_subtree(s["marg"], s["ptok"], N, s["root"], dev_status=status, out=sel_out)
+
+    def k_attn(s):
+        tv.tree_attention(s["q"], s["k"], s["v"], sel_out["parent"], P, out=s["out"], workspace=ws_attn,
+                          dev_status=status)
+
+    def k_verify(s, rnd=0):
+        if sampling_mode:
+            tv.verify_sample(s["logits"], s["draft"], sel_out["parent"], sel_out["tokens"],
+                             temperature=cfg["temperature"], seed=cfg["seed"], round=rnd, workspace=ws_ver,
+                             dev_status=status, out=ver_out)
+        else:
+            tv.verify_greedy(s["logits"], sel_out["parent"], sel_out["tokens"], workspace=ws_ver, dev_status=status,
+                             out=ver_out)
+
+    def step(s):
+        k_select(s)
+        k_attn(s)
+        k_verify(s)
+
+    launches_per_step = (1 if use_pool else 0) + 1 + (2 if sampling_mode else 1)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(sets[i % n_sets])
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status {int(status.item())} after warm-up")
+
+    def capture(fn):
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph, stream=stream):
+            fn()
+        return gph
+
+    with torch.cuda.stream(stream):
+        g_all = capture(lambda: [step(s) for s in sets])          # one step per input set
+        g_one = [capture(lambda s=s: step(s)) for s in sets]
+        g_sel = [capture(lambda s=s: k_select(s)) for s in sets] if use_pool else None
+        g_att = [capture(lambda s=s: k_attn(s)) for s in sets]
+        g_ver = [capture(lambda s=s: k_verify(s)) for s in sets]
+    torch.cuda.synchronize()
+
+    def timed(fn, reps):
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        fn(reps)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return ev0.elapsed_time(ev1)  # ms
+
+    def run_steps(k):
+        with torch.cuda.stream(stream):
+            full, rest = divmod(k, n_sets)
+            for _ in range(full):
+                g_all.replay()
+            for i in range(rest):
+                g_one[i].replay()
+
+    # warm the graphs, then the timed region
+    run_steps(min(args.steps, 4 * n_sets))
+    sampler = ClockSampler(gpu_identifier(torch, local))
+    if rank == 0:
+        sampler.start()
+    ms = timed(run_steps, args.steps)
+    clocks = sampler.stop() if rank == 0 else None
+    ms = max_over_ranks(ms, world, dev)
+    ms_per_step = ms / args.steps
+    value = world * B * N / (ms_per_step / 1e3)
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status {int(status.item())} after the timed region")
+
+    # ---- per-kernel breakdown (same graphs, one kernel family at a time)
+    reps = max(n_sets, min(args.steps, 20000) // n_sets * n_sets)
+
+    def fam(gs):
+        def f(k):
+            with torch.cuda.stream(stream):
+                for i in range(k):
+                    gs[i % n_sets].replay()
+        return f
+
+    br = {"attention": timed(fam(g_att), reps) * 1e3 / reps, "verify": timed(fam(g_ver), reps) * 1e3 / reps}
+    if use_pool:
+        br["select"] = timed(fam(g_sel), reps) * 1e3 / reps
+    peak, peak_kind = measured_peaks()
+    fam_bytes = {"attention": bytes_attn, "verify": bytes_vocab}
+    dom = max(("attention", "verify"), key=lambda kk: br[kk])
+    achieved = fam_bytes[dom] / (br[dom] * 1e-6) / 1e9
+    kernel_names = {"attention": "attn_tc_kernel" if bf16 else "attn_simt_kernel", "verify": "vocab_pass_kernel"}
+    roofline = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": peak_kind,
+                "traffic": kernel_traffic(kernel_names[dom]),
+                "algorithmic_bytes_per_launch": fam_bytes[dom]}
+
+    # ---- end to end through the public API with host buffers (pinned), copies timed
+    pinned = {kk: (to_dev(vv) if kk in ("q", "k", "v", "logits", "draft") else torch.from_numpy(vv)).cpu()
+              .pin_memory() for kk, vv in host.items()}
+    res_host = {kk: torch.empty_like(ver_out[kk], device="cpu").pin_memory()
+                for kk in (("accepted_nodes", "accept_len", "out_token") if sampling_mode else
+                           ("accepted_nodes", "accept_len", "bonus_token"))}
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = sum(t.numel() * t.element_size() for t in res_host.values())
+    dst = sets[0]
+    e2e_steps = max(20, min(2000, args.steps // 20))
+
+    def e2e(k):
+        with torch.cuda.stream(stream):
+            for _ in range(k):
+                for kk, t in pinned.items():
+                    dst[kk].copy_(t, non_blocking=True)
+                step(dst)
+                for kk, t in res_host.items():
+                    t.copy_(ver_out[kk], non_blocking=True)
+
+    e2e(3)
+    ms_e2e = max_over_ranks(timed(e2e, e2e_steps), world, dev)
+    e2e_value = world * B * N / (ms_e2e / e2e_steps / 1e3)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
+            "config": dict(workload_config(args.workload, cfg),
+                           l2=f"inputs rotate over {n_sets} device copies, {n_sets * bytes_set / 1e6:.0f} MB "
+                              f"> 2 x L2 ({l2 / 1e6:.0f} MB)",
+                           step="select_subtree + tree_attention + " +
+                                ("verify_sample" if sampling_mode else "verify_greedy"),
+                           parallelism=f"replicas x{world}"),
+            "path_gbs": bytes_set / (ms_per_step * 1e-3) / 1e9,
+            "breakdown_us": br,
+            "roofline": roofline,
+            "cpu_baseline": cpu_base,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.oracle_worker is not None:
+        oracle_worker(args.oracle_worker, args.workload)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * treeverify.h - C ABI of the tree-verification library (libtreeverify.so), sm_103a.
+ *
+ * One verification round of tree speculative decoding, on one GPU:
+ *   tv_select_subtree   budgeted prefix-closed subtree from a block-marginal pool
+ *   tv_tree_prep        ancestor bitmask, depth / position ids, child lists
+ *   tv_tree_attention   tree-masked grouped-query attention over prefix KV + tree KV
+ *   tv_verify_greedy    fused vocab pass + greedy longest-match walk + bonus token
+ *   tv_verify_sample    fused vocab pass + min(1,p/q) walk + residual resampling
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless marked
+ *     "host".  The library never allocates device memory: calls that need scratch take
+ *     a caller-provided `workspace` of at least the size returned by the matching
+ *     tv_*_workspace_size() query.  A workspace must be zero-filled once before its
+ *     first use; every call leaves it ready for the next call (its counters return to
+ *     zero).  Calls that share one workspace must not overlap on the GPU.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns a tv_status.  TV_OK means the work was enqueued; argument
+ *     errors found on the host return a negative status and enqueue nothing.
+ *   - Problems that only the device can see (a malformed parent array, an
+ *     out-of-range token, a bounded wait that ran out) are OR-ed as TV_DEV_* bits into
+ *     the caller's `*dev_status` word (a device int32 the caller zeroes and reads back).
+ *     Outputs of an affected sequence are then unspecified but every kernel still
+ *     terminates.  Nothing throws across this ABI.
+ *   - Tree layout: per sequence b, `parent[b][0] = -1` (node 0 is the root = the last
+ *     committed token) and 0 <= parent[b][i] < i for i >= 1.  N counts all nodes,
+ *     root included.  Row u of a logits block is the target (or draft) distribution of
+ *     the token that follows node u, so draft node c is judged with row parent[c].
+ *   - Logits / activations are row-major and contiguous.  bf16 is IEEE bfloat16.
+ *
+ * Passages restated (the pages' titles):
+ *   TAPS (Target-Aware Prefix-tree Selection for diffusion-drafted speculative
+ *     decoding) §4.1-§4.2;  PTD (Progressive Tree Drafting) §3.1 tree construction;
+ *   TreeGraft (adaptive multi-drafter grafting) §3.1 cumulative path score;
+ *   "Speculative decoding principles" (blog): parallel verification, greedy
+ *     acceptance, sampling acceptance alpha = min(1, p/q), residual (p-q)+ correction.
+ */
+#ifndef TREEVERIFY_H
+#define TREEVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TV_API __attribute__((visibility("default")))
+#else
+#define TV_API
+#endif
+
+typedef struct CUstream_st* tv_stream_t; /* identical to cudaStream_t */
+
+typedef enum tv_dtype {
+  TV_F32 = 0,  /* IEEE float32 */
+  TV_BF16 = 1  /* bfloat16 (fp32 accumulation inside) */
+} tv_dtype;
+
+typedef enum tv_status {
+  TV_OK = 0,
+  TV_ERR_NULL = -1,        /* a required pointer is NULL */
+  TV_ERR_SHAPE = -2,       /* a size is out of the supported range */
+  TV_ERR_DTYPE = -3,       /* unknown or unsupported dtype for this call */
+  TV_ERR_WORKSPACE = -4,   /* workspace missing or smaller than the query says */
+  TV_ERR_ALIGN = -5,       /* a pointer or stride breaks an alignment rule */
+  TV_ERR_UNSUPPORTED = -6, /* a combination this build does not implement */
+  TV_ERR_CUDA = -7,        /* a CUDA runtime/driver call failed while enqueueing */
+  TV_ERR_VALUE = -8        /* a scalar argument is out of range (temperature, scale) */
+} tv_status;
+
+/* Bits OR-ed into *dev_status by device code. */
+#define TV_DEV_BAD_TREE 1   /* parent[] breaks parent[0] = -1, 0 <= parent[i] < i */
+#define TV_DEV_BAD_TOKEN 2  /* a draft token is outside [0, V) or pool token invalid */
+#define TV_DEV_TIMEOUT 4    /* a bounded wait inside a kernel ran out (pipeline stall) */
+
+/* Human-readable name of a tv_status value (static string, never NULL). */
+TV_API const char* tv_status_string(int status);
+
+/* Library ABI version: (major << 16) | minor. */
+TV_API int tv_version(void);
+
+/* ------------------------------------------------------------------------------------
+ * tv_tree_prep - tree structure for the attention mask and position encoding.
+ * PTD §3.1 "tree construction": node v observes pi(v) = {v} U pi(P(v)); its position
+ * encoding follows |pi(v)|.
+ *   parent     [B][N] int32
+ *   depth      [B][N] int32 out: |pi(v)| - 1                              (may be NULL)
+ *   pos        [B][N] int32 out: P + depth (0-based position ids)        (may be NULL)
+ *   anc_mask   [B][N][W] uint32 out, W = ceil(N/32): bit (j%32) of word j/32 of row i
+ *              is set iff j in pi(i)                                      (may be NULL)
+ *   child_off  [B][N+1] int32 out, child_idx [B][N] int32 out: per sequence, the
+ *              children of u are child_idx[child_off[u] .. child_off[u+1]) in
+ *              ascending node index (child_idx[b][N-1] is unused)  (both or neither)
+ * Limits: 1 <= N <= 1024, B >= 1.  Launches one CTA per sequence.
+ */
+TV_API tv_status tv_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* depth, int32_t* pos,
+                       uint32_t* anc_mask, int32_t* child_off, int32_t* child_idx,
+                       int32_t* dev_status, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * tv_tree_attention - tree-masked grouped-query attention of the draft tree.
+ * PTD §3.1 (a node attends only to its ancestors), blog "why target verification can
+ * be parallel" (all drafted positions are scored in one pass), TAPS §4.1 (the selected
+ * subtree is verified with tree attention).
+ *   out[b,h,i,:] = sum_j softmax_j(scale * q[b,h,i,:] . k[b,h/G,j,:]) v[b,h/G,j,:]
+ *   with j over the prefix rows [0, P) and the tree rows {P + t : t in pi(i)},
+ *   G = Hq / Hkv.
+ *   q, out        [B][Hq][N][D]             dtype
+ *   k_cache,
+ *   v_cache       [B][Hkv][kv_stride_tokens][D] dtype; rows 0..P-1 = committed prefix,
+ *                 row P + t = tree node t's key/value (already written by the caller;
+ *                 keys are post-RoPE).  kv_stride_tokens >= P + N.
+ *   parent        [B][N] int32
+ *   scale         softmax scale (> 0); pass 0 for 1/sqrt(D).
+ * Precision: fp32 in/out with fp32 math, or bf16 in/out with fp32 softmax and fp32
+ * accumulation (tensor cores).  Limits: N <= 1024, D in {64, 128} for bf16 tensor-core
+ * tiles (other D <= 256, D % 32 == 0 run the CUDA-core kernel), Hq % Hkv == 0.
+ * Alignment: q, k_cache, v_cache, out 16-byte aligned.
+ * Workspace: tv_tree_attention_workspace_size(...) bytes (split-KV partials).
+ */
+TV_API size_t tv_tree_attention_workspace_size(int B, int Hq, int Hkv, int D, int P, int N,
+                                        tv_dtype dtype);
+TV_API tv_status tv_tree_attention(const void* q, const void* k_cache, const void* v_cache, void* out,
+                            const int32_t* parent, int B, int Hq, int Hkv, int D, int P, int N,
+                            int kv_stride_tokens, float scale, tv_dtype dtype, void* workspace,
+                            size_t ws_bytes, int32_t* dev_status, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * tv_verify_greedy - greedy acceptance of a draft tree.
+ * Blog: "greedy decoding, intuitive version" and "accept a prefix and start the next
+ * round": drafts are kept while they equal the target's choice; the first disagreement
+ * is replaced by the target's token.
+ * One streaming pass over the target logits computes, per row u: the argmax (lowest
+ * index among equal raw values) and log-sum-exp of x/T with T = 1.  Then per sequence:
+ * cur = root; while some child c of cur has tokens[c] == argmax[cur]: accept c, cur = c.
+ *   logits        [B][N][V] dtype
+ *   tokens        [B][N] int32 draft token of every node (tokens[b][0] unused)
+ *   accepted_nodes[B][N] int32 out: accepted node ids in walk order, -1 padded
+ *   accept_len    [B] int32 out: number of accepted drafts L (root excluded)
+ *   bonus_token   [B] int32 out: argmax of the row where the walk stopped
+ *   p_draft       [B][N] float out (optional): softmax(x[parent(c)])[tokens[c]], NaN at c=0
+ *   row_lse       [B][N] float out (optional): log-sum-exp of each row
+ *   row_argmax    [B][N] int32 out (optional): argmax of each row
+ * Limits: 1 <= N <= 1024, 1 <= V < 2^31 / N.  Workspace: tv_verify_workspace_size().
+ */
+TV_API size_t tv_verify_workspace_size(int B, int N, int V, tv_dtype dtype, int sampling);
+TV_API tv_status tv_verify_greedy(const void* logits, const int32_t* parent, const int32_t* tokens, int B,
+                           int N, int V, tv_dtype dtype, int32_t* accepted_nodes,
+                           int32_t* accept_len, int32_t* bonus_token, float* p_draft,
+                           float* row_lse, int32_t* row_argmax, void* workspace, size_t ws_bytes,
+                           int32_t* dev_status, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * tv_verify_sample - stochastic acceptance down the draft tree.
+ * Blog "acceptance probability for sampling": draft token t at node u is kept with
+ * probability min(1, p_u(t)/q_u(t)); "how to correct after a rejection": the
+ * replacement is drawn from (p-q)+ / sum (p-q)+.
+ * p_u = softmax(target[u]/T), q_u = softmax(draft[u]/T).  At node u the children are
+ * tried in ascending index order with uniforms U(seed, round, b, u, k, 0), k = 1..m;
+ * after rejecting t_k: p <- (p-q)+ normalised (unchanged if the residual is 0) and
+ * q <- q without t_k, renormalised.  When all children are rejected or u is a leaf, the
+ * output token is the smallest v with U(seed, round, b, u, 0, 1) * sum(p) < p(0..v).
+ * U is Philox4x32-10 (Salmon et al., SC'11) with key = seed and counter =
+ * (round mod 2^32, b, u, 2k + kind), U = (x0 >> 8) * 2^-24.
+ *   target_logits, draft_logits [B][N][V] dtype
+ *   accepted_nodes [B][N], accept_len [B], out_token [B] int32 out
+ *   p_draft, q_draft [B][N] float out (optional): p_{parent(c)}(t_c), q_{parent(c)}(t_c)
+ * Limits as tv_verify_greedy; temperature > 0.  Workspace:
+ * tv_verify_workspace_size(B, N, V, dtype, 1).
+ */
+TV_API tv_status tv_verify_sample(const void* target_logits, const void* draft_logits,
+                           const int32_t* parent, const int32_t* tokens, int B, int N, int V,
+                           float temperature, uint64_t seed, uint64_t round, tv_dtype dtype,
+                           int32_t* accepted_nodes, int32_t* accept_len, int32_t* out_token,
+                           float* p_draft, float* q_draft, void* workspace, size_t ws_bytes,
+                           int32_t* dev_status, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * tv_select_subtree - budgeted prefix-closed subtree from a block-marginal pool.
+ * TAPS §4.1: d positions x top-K tokens form the candidate tree (a node at depth k is a
+ * rank path r_1..r_k with token pool_tokens[k-1][r_k]); TAPS §4.2: edge estimates are
+ * propagated to a path-level reach probability and a prefix-closed subtree is kept under
+ * a verification budget; TreeGraft §3.1: s(v) = product of the edge scores on the path.
+ * Edge score := the child's marginal.  s is formed in fp32 left to right along the path
+ * (correctly rounded multiplies).  The first budget-1 candidates in the order (s desc,
+ * depth asc, rank path lexicographic asc) are kept; this set is prefix-closed and has
+ * the largest sum of s among prefix-closed sets of its size.
+ *   marg          [B][d][K] float, each position sorted by (prob desc, token asc), >= 0
+ *   pool_tokens   [B][d][K] int32
+ *   root_token    [B] int32 (device)
+ *   parent, tokens, depth [B][budget] int32 out, score [B][budget] float out: nodes in
+ *                 selection order (parent < child), root = row 0 (score 1, depth 0);
+ *                 rows past n_nodes hold -1 (score 0)
+ *   n_nodes       [B] int32 out: 1 + number of selected candidates
+ * Limits: 1 <= d <= 16, 1 <= K <= 256, 1 <= budget <= 4096.
+ * Workspace: tv_select_workspace_size(...) bytes.
+ */
+TV_API size_t tv_select_workspace_size(int B, int d, int K, int budget);
+TV_API tv_status tv_select_subtree(const float* marg, const int32_t* pool_tokens, int B, int d, int K,
+                            int budget, const int32_t* root_token, int32_t* parent,
+                            int32_t* tokens, int32_t* depth, float* score, int32_t* n_nodes,
+                            void* workspace, size_t ws_bytes, int32_t* dev_status,
+                            tv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TREEVERIFY_H */

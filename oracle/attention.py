@@ -33,10 +33,12 @@ def _softmax_attend(qvec: np.ndarray, keys: np.ndarray, vals: np.ndarray, scale:
     return w @ vals
 
 
-def tree_attention(q, k_cache, v_cache, parent, prefix_len: int, scale: float | None = None) -> np.ndarray:
+def tree_attention(q, k_cache, v_cache, parent, prefix_len: int, scale: float | None = None,
+                   nodes=None, heads=None) -> np.ndarray:
     """out[b,h,i,:] = softmax over visible j of (q[b,h,i] . k[b,h//G,j]) * scale, applied to v.
 
-    ``parent`` is [B][N].  Everything is promoted to float64.
+    ``parent`` is [B][N].  Everything is promoted to float64.  ``nodes`` / ``heads``
+    optionally restrict the computation to those indices (other rows stay zero).
     """
     q = np.asarray(q, dtype=np.float64)
     k_cache = np.asarray(k_cache, dtype=np.float64)
@@ -51,10 +53,10 @@ def tree_attention(q, k_cache, v_cache, parent, prefix_len: int, scale: float | 
     out = np.zeros_like(q)
     for b in range(bsz):
         validate(parent[b])
-        for i in range(n):
+        for i in (range(n) if nodes is None else nodes):
             anc = sorted(observable_set(parent[b], i))
             rows = list(range(prefix_len)) + [prefix_len + t for t in anc]
-            for h in range(hq):
+            for h in (range(hq) if heads is None else heads):
                 kh = h // group
                 out[b, h, i] = _softmax_attend(q[b, h, i], k_cache[b, kh, rows], v_cache[b, kh, rows], scale)
     return out

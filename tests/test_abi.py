@@ -1,0 +1,111 @@
+"""CPU-side checks of the C ABI: the shared library builds, loads and exports every
+function that include/treeverify.h declares; host-side argument validation returns the
+documented status codes without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "treeverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from tree_speculative_decoding_masked_gb300 import build as b
+    import tree_speculative_decoding_masked_gb300 as tv
+    srcs = b.sources() + [HEADER]
+    stale = (not os.path.exists(b.LIB)) or max(os.path.getmtime(s) for s in srcs) > os.path.getmtime(b.LIB)
+    if stale:
+        b.build()
+    return tv.load_library()
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return re.findall(r"^TV_API\s+[\w\s\*]+?\b(tv_\w+)\s*\(", txt, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = set(_declared())
+    for n in ("tv_tree_attention", "tv_verify_greedy", "tv_verify_sample", "tv_select_subtree", "tv_tree_prep",
+              "tv_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import tree_speculative_decoding_masked_gb300 as tv
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) == set(tv.exported_symbols())
+
+
+def test_status_strings(lib):
+    assert lib.tv_status_string(0) == b"TV_OK"
+    for code in range(-8, 0):
+        assert lib.tv_status_string(code).startswith(b"TV_ERR_")
+    assert lib.tv_status_string(123) == b"unknown tv_status"
+    assert lib.tv_version() >> 16 == 1
+
+
+NULL = None
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+
+
+def test_attention_host_validation(lib):
+    f = lib.tv_tree_attention
+    # null pointer
+    assert f(NULL, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 8, 4, 12, 0.0, 0, NULL, 0, NULL, NULL) == -1
+    # Hq not a multiple of Hkv
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 6, 4, 64, 8, 4, 12, 0.0, 0, NULL, 0, NULL, NULL) == -2
+    # kv stride shorter than P + N
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 8, 4, 11, 0.0, 0, NULL, 0, NULL, NULL) == -2
+    # N above the limit
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 8, 1025, 2000, 0.0, 0, NULL, 0, NULL, NULL) == -2
+    # bad dtype
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 8, 4, 12, 0.0, 7, NULL, 0, NULL, NULL) == -3
+    # negative scale
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 8, 4, 12, -1.0, 0, NULL, 0, NULL, NULL) == -8
+    # misaligned pointer
+    odd = ctypes.c_void_p(0x1004)
+    assert f(odd, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 8, 4, 12, 0.0, 0, NULL, 0, NULL, NULL) == -5
+    # bf16 tensor-core shape without workspace
+    assert lib.tv_tree_attention_workspace_size(1, 32, 8, 128, 2048, 64, 1) > 0
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 128, 2048, 64, 2112, 0.0, 1, NULL, 0, NULL, NULL) == -4
+
+
+def test_verify_host_validation(lib):
+    g = lib.tv_verify_greedy
+    ws = lib.tv_verify_workspace_size(1, 16, 1024, 0, 0)
+    assert ws > 0
+    assert g(NULL, FAKE, FAKE, 1, 16, 1024, 0, FAKE, FAKE, FAKE, NULL, NULL, NULL, FAKE, ws, NULL, NULL) == -1
+    assert g(FAKE, FAKE, FAKE, 1, 0, 1024, 0, FAKE, FAKE, FAKE, NULL, NULL, NULL, FAKE, ws, NULL, NULL) == -2
+    assert g(FAKE, FAKE, FAKE, 1, 16, 1024, 0, FAKE, FAKE, FAKE, NULL, NULL, NULL, FAKE, ws - 1, NULL, NULL) == -4
+    s = lib.tv_verify_sample
+    wss = lib.tv_verify_workspace_size(1, 16, 1024, 0, 1)
+    assert wss > ws
+    assert s(FAKE, FAKE, FAKE, FAKE, 1, 16, 1024, 0.0, 1, 0, 0, FAKE, FAKE, FAKE, NULL, NULL, FAKE, wss, NULL,
+             NULL) == -8
+    assert s(FAKE, NULL, FAKE, FAKE, 1, 16, 1024, 1.0, 1, 0, 0, FAKE, FAKE, FAKE, NULL, NULL, FAKE, wss, NULL,
+             NULL) == -1
+
+
+def test_select_and_prep_host_validation(lib):
+    f = lib.tv_select_subtree
+    assert f(FAKE, FAKE, 1, 17, 4, 64, NULL, FAKE, FAKE, FAKE, FAKE, NULL, NULL, 0, NULL, NULL) == -2
+    assert f(FAKE, FAKE, 1, 16, 257, 64, NULL, FAKE, FAKE, FAKE, FAKE, NULL, NULL, 0, NULL, NULL) == -2
+    assert f(FAKE, FAKE, 1, 16, 4, 4097, NULL, FAKE, FAKE, FAKE, FAKE, NULL, NULL, 0, NULL, NULL) == -2
+    assert f(NULL, FAKE, 1, 16, 4, 64, NULL, FAKE, FAKE, FAKE, FAKE, NULL, NULL, 0, NULL, NULL) == -1
+    p = lib.tv_tree_prep
+    assert p(NULL, 1, 4, 0, NULL, NULL, NULL, NULL, NULL, NULL, NULL) == -1
+    assert p(FAKE, 1, 2000, 0, NULL, NULL, NULL, NULL, NULL, NULL, NULL) == -2
+    assert p(FAKE, 1, 4, 0, NULL, NULL, NULL, FAKE, NULL, NULL, NULL) == -1
+
+
+def test_binding_has_no_cpu_fallback(monkeypatch):
+    import tree_speculative_decoding_masked_gb300._binding as bnd
+    monkeypatch.setattr(bnd, "_lib", None)
+    monkeypatch.setattr(bnd, "_LIB_PATH", "/nonexistent/libtreeverify.so")
+    with pytest.raises(RuntimeError, match="not found"):
+        bnd.load_library()

@@ -1,0 +1,190 @@
+"""GPU parity: tv_tree_attention against the oracle (fp64).
+
+Tolerances: 1e-4 max-abs for fp32 inputs (CUDA-core kernel), 2e-2 max-abs for bf16
+inputs (tensor-core kernel: bf16 operands, fp32 accumulation and softmax, P rounded to
+bf16 for the second product).  Sizes span several 128-row tiles, several 64-key KV tiles
+with ragged tails, one and several KV splits, and the full workload shapes (sampled
+rows where the oracle would be slow)."""
+import math
+
+import numpy as np
+import pytest
+
+import synth
+import synth.workloads as W
+from oracle import attention, selection
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import tree_speculative_decoding_masked_gb300 as tv  # noqa: E402
+from gpu_util import dev, host, i32, to_dev  # noqa: E402
+
+
+def _run(q, k, v, par, P, bf16, stride_pad=0, pad_value=None):
+    qd = to_dev(q, bf16)
+    if stride_pad:
+        B, H, L, D = k.shape
+        kp = np.zeros((B, H, L + stride_pad, D), dtype=np.float32)
+        vp = np.zeros_like(kp)
+        kp[:, :, :L] = k
+        vp[:, :, :L] = v
+        kd, vd = to_dev(kp, bf16), to_dev(vp, bf16)
+        if pad_value is not None:
+            kd[:, :, L:] = pad_value
+            vd[:, :, L:] = pad_value
+    else:
+        kd, vd = to_dev(k, bf16), to_dev(v, bf16)
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    out = tv.tree_attention(qd, kd, vd, i32(par), P, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return host(out)
+
+
+def _check_all(q, k, v, par, P, bf16, **kw):
+    got = _run(q, k, v, par, P, bf16, **kw)
+    ref = attention.tree_attention(q, k, v, par, P)
+    err = float(np.max(np.abs(got - ref)))
+    assert np.isfinite(got).all()
+    assert err < (2e-2 if bf16 else 1e-4), err
+    return err
+
+
+def test_tiny_fp32_workload():
+    cfg = W.WORKLOADS["tiny_fp32"]
+    g = synth.rng(cfg["seed"])
+    par, _ = W.trees(g, cfg["B"], cfg["N"], cfg["depth_cap"], cfg["V"])
+    q, k, v = W.qkv_host(g, cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["P"], cfg["N"], False)
+    _check_all(q, k, v, par, cfg["P"], False)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("shape", [
+    # B, Hq, Hkv, D, P, N, depth cap
+    (2, 8, 2, 128, 300, 37, 5),     # one split, ragged tiles
+    (1, 8, 2, 128, 1000, 70, 8),    # several splits, two row tiles
+    (2, 4, 4, 64, 130, 129, 16),    # G = 1, D = 64, 2 row tiles
+    (1, 16, 2, 128, 200, 33, 4),    # G = 8 (16 nodes per row tile)
+    (1, 6, 2, 64, 77, 45, 3),       # G = 3 (40-node row tiles, 8 padding rows)
+    (1, 4, 1, 128, 0, 64, 6),       # empty prefix: tree keys only
+    (1, 4, 1, 128, 64, 16, 2),      # prefix ends on a tile boundary
+])
+def test_shapes(bf16, shape):
+    B, Hq, Hkv, D, P, N, cap = shape
+    g = synth.rng(sum(shape) + int(bf16))
+    par, _ = W.trees(g, B, N, cap, 100)
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, bf16)
+    _check_all(q, k, v, par, P, bf16)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_chain_tree_is_causal_attention(bf16):
+    B, Hq, Hkv, D, P, N = 1, 8, 2, 128, 500, 40
+    g = synth.rng(31)
+    par = synth.chain_parents(N)[None]
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, bf16)
+    got = _run(q, k, v, par, P, bf16)
+    for h in range(Hq):
+        ref = attention.causal_attention(q[0, h], k[0, h // 4, :P + N], v[0, h // 4, :P + N], 1 / math.sqrt(D))
+        assert np.max(np.abs(got[0, h] - ref)) < (2e-2 if bf16 else 1e-4)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_star_tree(bf16):
+    B, Hq, Hkv, D, P, N = 1, 4, 1, 64, 100, 100
+    g = synth.rng(32)
+    par = synth.star_parents(N)[None]
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, bf16)
+    _check_all(q, k, v, par, P, bf16)
+
+
+def test_cache_padding_rows_never_read():
+    # rows between P + N and the cache stride hold NaN; the output must not see them
+    B, Hq, Hkv, D, P, N = 1, 8, 2, 128, 190, 30
+    g = synth.rng(33)
+    par, _ = W.trees(g, B, N, 4, 100)
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, True)
+    got = _run(q, k, v, par, P, True, stride_pad=50, pad_value=float("nan"))
+    ref = attention.tree_attention(q, k, v, par, P)
+    assert np.isfinite(got).all() and np.max(np.abs(got - ref)) < 2e-2
+
+
+def test_large_scores_rescale_path():
+    # scores that grow along the key axis force the running-max rescale of O
+    B, Hq, Hkv, D, P, N = 1, 4, 1, 128, 1000, 32
+    g = synth.rng(34)
+    par, _ = W.trees(g, B, N, 4, 100)
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, False)
+    ramp = np.linspace(0.0, 6.0, P + N, dtype=np.float32)[None, None, :, None]
+    k = synth.round_to_bf16((k * 0.2 + ramp * np.sign(q.mean(axis=(0, 1, 2)))[None, None, None, :]).astype(np.float32))
+    q = synth.round_to_bf16(q)
+    v = synth.round_to_bf16(v)
+    _check_all(q, k, v, par, P, True)
+
+
+def test_qwen3_4b_layer_workload_all_rows():
+    cfg = W.WORKLOADS["qwen3_4b_layer"]
+    g = synth.rng(cfg["seed"])
+    marg, ptok = W.pools(g, 1, cfg["pool_d"], cfg["pool_k"], cfg["V"])
+    par = selection.select_subtree(marg[0], ptok[0], cfg["N"], 11)["parent"][None]
+    q, k, v = W.qkv_host(g, 1, cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["P"], cfg["N"], True)
+    _check_all(q, k, v, par, cfg["P"], True)
+
+
+def _sampled_rows(name, n_rows, seed_extra=0):
+    cfg = W.WORKLOADS[name]
+    B, Hq, Hkv, D, P = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["P"]
+    N = cfg.get("N", 1024)
+    g = synth.rng(cfg["seed"] + seed_extra)
+    par, _ = W.trees(g, B, N, cfg.get("depth_cap", 16), 100)
+    qd = W.device_normal((B, Hq, N, D), 1.0, cfg["seed"] + 1, torch.bfloat16, dev())
+    kd = W.device_normal((B, Hkv, P + N, D), 1.0, cfg["seed"] + 2, torch.bfloat16, dev())
+    vd = W.device_normal((B, Hkv, P + N, D), 1.0, cfg["seed"] + 3, torch.bfloat16, dev())
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    out = tv.tree_attention(qd, kd, vd, i32(par), P, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    G = Hq // Hkv
+    rows = [(int(g.integers(B)), int(g.integers(Hq)), int(g.integers(N))) for _ in range(n_rows)]
+    rows += [(0, 0, i) for i in range(0, N, max(1, N // 64))]  # a spread of nodes of one head
+    rows += [(B - 1, Hq - 1, N - 1)]
+    worst = 0.0
+    cache = {}
+    for b, h, i in rows:
+        key = (b, h // G)
+        if key not in cache:
+            cache[key] = (kd[b, h // G].float().cpu().numpy()[None, None], vd[b, h // G].float().cpu().numpy()[None, None])
+        kk, vv = cache[key]
+        qq = qd[b, h].float().cpu().numpy()[None, None]
+        ref = attention.per_node_bruteforce(qq, kk, vv, par[b:b + 1], P, 0, 0, i)
+        got = out[b, h, i].float().cpu().numpy()
+        worst = max(worst, float(np.max(np.abs(got - ref))))
+    assert worst < 2e-2, worst
+
+
+def test_long_context_workload_sampled():
+    _sampled_rows("long_context", 48)
+
+
+def test_sampling_workload_sampled():
+    _sampled_rows("sampling", 48)
+
+
+def test_budget_sweep_1024_nodes_sampled():
+    _sampled_rows("budget_sweep", 48)
+
+
+def test_bad_tree_flagged():
+    B, Hq, Hkv, D, P, N = 1, 8, 2, 128, 64, 8
+    g = synth.rng(35)
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, True)
+    par = np.array([[-1, 0, 1, 5, 2, 3, 4, 5]], dtype=np.int32)
+    for bf16 in (True, False):
+        st = torch.zeros(1, dtype=torch.int32, device=dev())
+        tv.tree_attention(to_dev(q, bf16), to_dev(k, bf16), to_dev(v, bf16), i32(par), P, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) & tv.TV_DEV_BAD_TREE

@@ -1,0 +1,265 @@
+"""ctypes binding of libtreeverify's C ABI (include/treeverify.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA kernels.
+Tensors must be CUDA tensors on the current device; calls are enqueued on torch's
+current stream and return immediately.  There is no CPU fallback: if the shared library
+is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libtreeverify.so")
+
+TV_F32 = 0
+TV_BF16 = 1
+
+TV_DEV_BAD_TREE = 1
+TV_DEV_BAD_TOKEN = 2
+TV_DEV_TIMEOUT = 4
+
+
+class TreeVerifyError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed with status {status}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+_U64 = ctypes.c_uint64
+
+_SIGS = {
+    "tv_status_string": (ctypes.c_char_p, [_I]),
+    "tv_version": (_I, []),
+    "tv_tree_prep": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "tv_tree_attention_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "tv_tree_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _P]),
+    "tv_verify_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "tv_verify_greedy": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "tv_verify_sample": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _U64, _U64, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "tv_select_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "tv_select_subtree": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+}
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libtreeverify.so (built by ``python -m tree_speculative_decoding_masked_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"libtreeverify.so not found at {_LIB_PATH}; build it with "
+                "`python -m tree_speculative_decoding_masked_gb300.build` (needs nvcc 13, sm_103a)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def exported_symbols() -> list:
+    return list(_SIGS)
+
+
+def status_string(status: int) -> str:
+    return load_library().tv_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise TreeVerifyError(fn, status, status_string(status))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return TV_BF16
+    if t.dtype == torch.float32:
+        return TV_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use torch.bfloat16 or torch.float32")
+
+
+def _need_cuda(**tensors):
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
+def _workspace(nbytes: int, device, workspace):
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace smaller than the library's query")
+        return workspace
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _out(o, key, shape, dtype, device):
+    t = o.get(key)
+    return t if t is not None else torch.empty(shape, dtype=dtype, device=device)
+
+
+def _status_tensor(dev_status, device):
+    return dev_status if dev_status is not None else torch.zeros(1, dtype=torch.int32, device=device)
+
+
+# ------------------------------------------------------------------------------------
+
+
+def tree_prep(parent: torch.Tensor, prefix_len: int, *, dev_status=None):
+    """Depth, position ids, packed ancestor mask and child CSR of ``parent`` [B][N]."""
+    _need_cuda(parent=parent)
+    lib = load_library()
+    B, N = parent.shape
+    dev = parent.device
+    W = (N + 31) // 32
+    depth = torch.empty(B, N, dtype=torch.int32, device=dev)
+    pos = torch.empty(B, N, dtype=torch.int32, device=dev)
+    mask = torch.empty(B, N, W, dtype=torch.int32, device=dev)
+    off = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    idx = torch.empty(B, N, dtype=torch.int32, device=dev)
+    st = _status_tensor(dev_status, dev)
+    _check("tv_tree_prep", lib.tv_tree_prep(_ptr(parent), B, N, int(prefix_len), _ptr(depth), _ptr(pos), _ptr(mask),
+                                            _ptr(off), _ptr(idx), _ptr(st), _stream()))
+    return {"depth": depth, "pos": pos, "anc_mask": mask, "child_off": off, "child_idx": idx, "dev_status": st}
+
+
+def tree_attention_workspace_size(B, Hq, Hkv, D, P, N, dtype) -> int:
+    code = TV_BF16 if dtype == torch.bfloat16 else TV_F32
+    return int(load_library().tv_tree_attention_workspace_size(B, Hq, Hkv, D, P, N, code))
+
+
+def tree_attention(q, k_cache, v_cache, parent, prefix_len: int, *, scale: float = 0.0, out=None, workspace=None,
+                   dev_status=None):
+    """Tree-masked GQA attention.  q [B][Hq][N][D]; k_cache, v_cache [B][Hkv][S][D]."""
+    _need_cuda(q=q, k_cache=k_cache, v_cache=v_cache, parent=parent, out=out)
+    lib = load_library()
+    B, Hq, N, D = q.shape
+    Hkv, S = k_cache.shape[1], k_cache.shape[2]
+    if v_cache.shape != k_cache.shape or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise ValueError("k_cache / v_cache must match each other and q's dtype")
+    code = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    ws_need = tree_attention_workspace_size(B, Hq, Hkv, D, prefix_len, N, q.dtype)
+    ws = _workspace(ws_need, q.device, workspace)
+    st = _status_tensor(dev_status, q.device)
+    _check("tv_tree_attention",
+           lib.tv_tree_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(parent), B, Hq, Hkv, D,
+                                 int(prefix_len), N, S, float(scale), code, _ptr(ws),
+                                 ws.numel() * ws.element_size(), _ptr(st), _stream()))
+    return out
+
+
+def verify_workspace_size(B, N, V, dtype, sampling: bool) -> int:
+    code = TV_BF16 if dtype == torch.bfloat16 else TV_F32
+    return int(load_library().tv_verify_workspace_size(B, N, V, code, 1 if sampling else 0))
+
+
+def verify_greedy(logits, parent, tokens, *, want_stats: bool = False, workspace=None, dev_status=None, out=None):
+    """Greedy acceptance.  logits [B][N][V]; returns dict of accepted_nodes [B][N],
+    accept_len [B], bonus_token [B], p_draft [B][N] (+ row_lse, row_argmax)."""
+    _need_cuda(logits=logits, parent=parent, tokens=tokens)
+    lib = load_library()
+    B, N, V = logits.shape
+    dev = logits.device
+    code = _dtype_code(logits)
+    o = out if out is not None else {}
+    acc = _out(o, "accepted_nodes", (B, N), torch.int32, dev)
+    alen = _out(o, "accept_len", (B), torch.int32, dev)
+    bonus = _out(o, "bonus_token", (B), torch.int32, dev)
+    pdr = _out(o, "p_draft", (B, N), torch.float32, dev)
+    lse = _out(o, "row_lse", (B, N), torch.float32, dev) if want_stats else None
+    am = _out(o, "row_argmax", (B, N), torch.int32, dev) if want_stats else None
+    ws = _workspace(verify_workspace_size(B, N, V, logits.dtype, False), dev, workspace)
+    st = _status_tensor(dev_status, dev)
+    _check("tv_verify_greedy",
+           lib.tv_verify_greedy(_ptr(logits), _ptr(parent), _ptr(tokens), B, N, V, code, _ptr(acc), _ptr(alen),
+                                _ptr(bonus), _ptr(pdr), _ptr(lse), _ptr(am), _ptr(ws), ws.numel() * ws.element_size(),
+                                _ptr(st), _stream()))
+    res = {"accepted_nodes": acc, "accept_len": alen, "bonus_token": bonus, "p_draft": pdr, "dev_status": st}
+    if want_stats:
+        res["row_lse"] = lse
+        res["row_argmax"] = am
+    return res
+
+
+def verify_sample(target_logits, draft_logits, parent, tokens, *, temperature: float, seed: int, round: int,
+                  workspace=None, dev_status=None, out=None):
+    """Sampling acceptance with residual resampling (Philox4x32-10 draws)."""
+    _need_cuda(target_logits=target_logits, draft_logits=draft_logits, parent=parent, tokens=tokens)
+    lib = load_library()
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    code = _dtype_code(target_logits)
+    if draft_logits.shape != target_logits.shape or draft_logits.dtype != target_logits.dtype:
+        raise ValueError("draft_logits must match target_logits")
+    o = out if out is not None else {}
+    acc = _out(o, "accepted_nodes", (B, N), torch.int32, dev)
+    alen = _out(o, "accept_len", (B), torch.int32, dev)
+    tok = _out(o, "out_token", (B), torch.int32, dev)
+    pdr = _out(o, "p_draft", (B, N), torch.float32, dev)
+    qdr = _out(o, "q_draft", (B, N), torch.float32, dev)
+    ws = _workspace(verify_workspace_size(B, N, V, target_logits.dtype, True), dev, workspace)
+    st = _status_tensor(dev_status, dev)
+    _check("tv_verify_sample",
+           lib.tv_verify_sample(_ptr(target_logits), _ptr(draft_logits), _ptr(parent), _ptr(tokens), B, N, V,
+                                float(temperature), int(seed) & (2**64 - 1), int(round) & (2**64 - 1), code, _ptr(acc),
+                                _ptr(alen), _ptr(tok), _ptr(pdr), _ptr(qdr), _ptr(ws), ws.numel() * ws.element_size(),
+                                _ptr(st), _stream()))
+    return {"accepted_nodes": acc, "accept_len": alen, "out_token": tok, "p_draft": pdr, "q_draft": qdr,
+            "dev_status": st}
+
+
+def select_workspace_size(B, d, K, budget) -> int:
+    return int(load_library().tv_select_workspace_size(B, d, K, budget))
+
+
+def select_subtree(marg, pool_tokens, budget: int, root_token, *, dev_status=None, out=None):
+    """TAPS-style budgeted prefix-closed subtree.  marg [B][d][K] float32 (sorted per
+    position), pool_tokens [B][d][K] int32, root_token [B] int32."""
+    _need_cuda(marg=marg, pool_tokens=pool_tokens, root_token=root_token)
+    if marg.dtype != torch.float32 or pool_tokens.dtype != torch.int32:
+        raise TypeError("marg must be float32 and pool_tokens int32")
+    lib = load_library()
+    B, d, K = marg.shape
+    dev = marg.device
+    o = out if out is not None else {}
+    par = _out(o, "parent", (B, budget), torch.int32, dev)
+    tok = _out(o, "tokens", (B, budget), torch.int32, dev)
+    dep = _out(o, "depth", (B, budget), torch.int32, dev)
+    sc = _out(o, "score", (B, budget), torch.float32, dev)
+    nn = _out(o, "n_nodes", (B), torch.int32, dev)
+    ws_need = select_workspace_size(B, d, K, budget)
+    ws = _workspace(ws_need, dev, None) if ws_need else None
+    st = _status_tensor(dev_status, dev)
+    _check("tv_select_subtree",
+           lib.tv_select_subtree(_ptr(marg), _ptr(pool_tokens), B, d, K, int(budget), _ptr(root_token), _ptr(par),
+                                 _ptr(tok), _ptr(dep), _ptr(sc), _ptr(nn), _ptr(ws),
+                                 0 if ws is None else ws.numel(), _ptr(st), _stream()))
+    return {"parent": par, "tokens": tok, "depth": dep, "score": sc, "n_nodes": nn, "dev_status": st}

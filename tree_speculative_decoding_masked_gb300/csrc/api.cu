@@ -1,0 +1,156 @@
+// C ABI of libtreeverify: host-side argument checks, workspace carving and launches.
+// Nothing here allocates device memory, synchronises the stream or throws.
+#include <math.h>
+
+#include "tv_kernels.cuh"
+
+using namespace tv;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool valid_dtype(tv_dtype d) { return d == TV_F32 || d == TV_BF16; }
+inline tv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TV_OK : TV_ERR_CUDA; }
+inline cudaStream_t st(tv_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* tv_status_string(int s) {
+  switch (s) {
+    case TV_OK:
+      return "TV_OK";
+    case TV_ERR_NULL:
+      return "TV_ERR_NULL: a required pointer is NULL";
+    case TV_ERR_SHAPE:
+      return "TV_ERR_SHAPE: a size is outside the supported range";
+    case TV_ERR_DTYPE:
+      return "TV_ERR_DTYPE: unsupported dtype";
+    case TV_ERR_WORKSPACE:
+      return "TV_ERR_WORKSPACE: workspace missing or too small";
+    case TV_ERR_ALIGN:
+      return "TV_ERR_ALIGN: pointer or stride misaligned";
+    case TV_ERR_UNSUPPORTED:
+      return "TV_ERR_UNSUPPORTED: combination not implemented";
+    case TV_ERR_CUDA:
+      return "TV_ERR_CUDA: CUDA call failed while enqueueing";
+    case TV_ERR_VALUE:
+      return "TV_ERR_VALUE: scalar argument out of range";
+    default:
+      return "unknown tv_status";
+  }
+}
+
+int tv_version(void) { return (1 << 16) | 0; }
+
+tv_status tv_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* depth, int32_t* pos, uint32_t* anc_mask,
+                       int32_t* child_off, int32_t* child_idx, int32_t* dev_status, tv_stream_t stream) {
+  if (!parent) return TV_ERR_NULL;
+  if (B < 1 || N < 1 || N > kMaxNodes || P < 0) return TV_ERR_SHAPE;
+  if ((child_off == nullptr) != (child_idx == nullptr)) return TV_ERR_NULL;
+  return cuda_status(launch_tree_prep(parent, B, N, P, depth, pos, anc_mask, child_off, child_idx, dev_status,
+                                      st(stream)));
+}
+
+size_t tv_tree_attention_workspace_size(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || P < 0 || N < 1) return 0;
+  AttnPlan p = attn_plan(B, Hq, Hkv, D, P, N, dtype);
+  return p.tc ? p.total : 0;
+}
+
+tv_status tv_tree_attention(const void* q, const void* k_cache, const void* v_cache, void* out,
+                            const int32_t* parent, int B, int Hq, int Hkv, int D, int P, int N, int kv_stride_tokens,
+                            float scale, tv_dtype dtype, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                            tv_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !out || !parent) return TV_ERR_NULL;
+  if (!valid_dtype(dtype)) return TV_ERR_DTYPE;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || N < 1 || N > kMaxNodes || P < 0) return TV_ERR_SHAPE;
+  if (D < 32 || D > 256 || D % 32) return TV_ERR_SHAPE;
+  if ((long long)kv_stride_tokens < (long long)P + N) return TV_ERR_SHAPE;
+  if ((long long)B * Hkv > 65535LL * 65535LL) return TV_ERR_SHAPE;
+  if (!(scale >= 0.f) || isinf(scale)) return TV_ERR_VALUE;
+  if (scale == 0.f) scale = 1.f / sqrtf((float)D);
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return TV_ERR_ALIGN;
+  AttnPlan p = attn_plan(B, Hq, Hkv, D, P, N, dtype);
+  if (p.tc) {
+    if (!workspace || ws_bytes < p.total) return TV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TV_ERR_ALIGN;
+    if (B > 65535 || Hkv > 65535) return TV_ERR_SHAPE;
+    return cuda_status(launch_attn_tc(q, k_cache, v_cache, out, parent, B, Hq, Hkv, D, P, N, kv_stride_tokens, scale,
+                                      p, reinterpret_cast<char*>(workspace), dev_status, st(stream)));
+  }
+  if ((long long)B * Hq * N / 4 + 1 > 0x7fffffffLL) return TV_ERR_SHAPE;
+  return cuda_status(launch_attn_simt(q, k_cache, v_cache, out, parent, B, Hq, Hkv, D, P, N, kv_stride_tokens, scale,
+                                      dtype, dev_status, st(stream)));
+}
+
+size_t tv_verify_workspace_size(int B, int N, int V, tv_dtype, int sampling) {
+  if (B < 1 || N < 1 || V < 1) return 0;
+  return verify_ws_layout(B, N, V, sampling ? 1 : 0, nullptr);
+}
+
+static tv_status verify_common_checks(const void* logits, const int32_t* parent, const int32_t* tokens, int B, int N,
+                                      int V, tv_dtype dtype, void* ws, size_t ws_bytes, int sampling) {
+  if (!logits || !parent || !tokens) return TV_ERR_NULL;
+  if (!valid_dtype(dtype)) return TV_ERR_DTYPE;
+  if (B < 1 || N < 1 || N > kMaxNodes || V < 1) return TV_ERR_SHAPE;
+  const long long rows = (long long)B * N;
+  const int splits = verify_splits((int)rows, V);
+  if (rows * splits > 0x7fffffffLL) return TV_ERR_SHAPE;
+  if ((long long)N * V > 0x7fffffffLL) return TV_ERR_SHAPE;
+  if (!ws || ws_bytes < verify_ws_layout(B, N, V, sampling, nullptr)) return TV_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TV_ERR_ALIGN;
+  return TV_OK;
+}
+
+tv_status tv_verify_greedy(const void* logits, const int32_t* parent, const int32_t* tokens, int B, int N, int V,
+                           tv_dtype dtype, int32_t* accepted_nodes, int32_t* accept_len, int32_t* bonus_token,
+                           float* p_draft, float* row_lse, int32_t* row_argmax, void* workspace, size_t ws_bytes,
+                           int32_t* dev_status, tv_stream_t stream) {
+  if (!accepted_nodes || !accept_len || !bonus_token) return TV_ERR_NULL;
+  tv_status s = verify_common_checks(logits, parent, tokens, B, N, V, dtype, workspace, ws_bytes, 0);
+  if (s != TV_OK) return s;
+  VerifyWs w;
+  verify_ws_layout(B, N, V, 0, &w);
+  return cuda_status(launch_vocab_pass(logits, nullptr, parent, tokens, B, N, V, dtype, 1.0f,
+                                       reinterpret_cast<char*>(workspace), w, accepted_nodes, accept_len, bonus_token,
+                                       p_draft, nullptr, row_lse, row_argmax, dev_status, 0, st(stream)));
+}
+
+tv_status tv_verify_sample(const void* target_logits, const void* draft_logits, const int32_t* parent,
+                           const int32_t* tokens, int B, int N, int V, float temperature, uint64_t seed,
+                           uint64_t round, tv_dtype dtype, int32_t* accepted_nodes, int32_t* accept_len,
+                           int32_t* out_token, float* p_draft, float* q_draft, void* workspace, size_t ws_bytes,
+                           int32_t* dev_status, tv_stream_t stream) {
+  if (!draft_logits || !accepted_nodes || !accept_len || !out_token) return TV_ERR_NULL;
+  if (!(temperature > 0.f) || isinf(temperature)) return TV_ERR_VALUE;
+  tv_status s = verify_common_checks(target_logits, parent, tokens, B, N, V, dtype, workspace, ws_bytes, 1);
+  if (s != TV_OK) return s;
+  VerifyWs w;
+  verify_ws_layout(B, N, V, 1, &w);
+  char* ws = reinterpret_cast<char*>(workspace);
+  cudaError_t e = launch_vocab_pass(target_logits, draft_logits, parent, tokens, B, N, V, dtype, temperature, ws, w,
+                                    nullptr, nullptr, nullptr, p_draft, q_draft, nullptr, nullptr, dev_status, 1,
+                                    st(stream));
+  if (e != cudaSuccess) return TV_ERR_CUDA;
+  return cuda_status(launch_sample_walk(target_logits, draft_logits, parent, tokens, B, N, V, dtype, temperature,
+                                        seed, round, ws, w, accepted_nodes, accept_len, out_token, dev_status,
+                                        st(stream)));
+}
+
+size_t tv_select_workspace_size(int B, int d, int K, int budget) { return select_ws_bytes(B, d, K, budget); }
+
+tv_status tv_select_subtree(const float* marg, const int32_t* pool_tokens, int B, int d, int K, int budget,
+                            const int32_t* root_token, int32_t* parent, int32_t* tokens, int32_t* depth, float* score,
+                            int32_t* n_nodes, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                            tv_stream_t stream) {
+  if (!marg || !pool_tokens || !parent || !tokens || !depth || !score) return TV_ERR_NULL;
+  if (B < 1 || d < 1 || d > kMaxDepth || K < 1 || K > kMaxRank || budget < 1 || budget > kMaxBudget)
+    return TV_ERR_SHAPE;
+  if (ws_bytes < select_ws_bytes(B, d, K, budget)) return TV_ERR_WORKSPACE;
+  return cuda_status(launch_select(marg, pool_tokens, B, d, K, budget, root_token, parent, tokens, depth, score,
+                                   n_nodes, reinterpret_cast<char*>(workspace), dev_status, st(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,566 @@
+// Tree-masked GQA attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// PTD §3.1: node i attends to the committed prefix and to its observable set pi(i);
+// TAPS §4.1: the selected subtree is verified by the target in one pass with tree
+// attention.  One CTA owns a tile of 128 query rows that share one KV head: the G query
+// heads of a GQA group times NT = 128/G consecutive tree nodes (head-major rows), so each
+// K/V tile fetched from HBM by TMA is used by every node and every head of the group.
+// The key range [0, P + last node of the tile) is cut into KV splits across CTAs.
+//
+// Per CTA, warp-specialised:
+//   warp 0      TMA producer: Q tile once, then K/V tiles of 64 keys into a 4-stage ring
+//   warp 1      TMEM owner; lane 0 issues tcgen05.mma:
+//                 S[t&1] = Q K_t^T         (M=128, N=64,  K=D,  fp32 in TMEM)
+//                 O     += P_t V_t         (M=128, N=D,   K=64, fp32 in TMEM)
+//   warps 2..5  softmax: one thread per row; read S from TMEM, apply the tree mask,
+//               keep a running reference max (rescale O only when the max grows by
+//               more than 2^8), write P (bf16) to shared memory for the second MMA.
+// With one split the epilogue normalises O and stores bf16; with several, rows are
+// written as fp32 partials (O, m, l) and the last CTA of the tile merges them.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "tv_kernels.cuh"
+#include "tv_ptx.cuh"
+
+namespace tv {
+
+constexpr int kRows = 128;     // MMA M: query rows per CTA
+constexpr int kBN = 64;        // keys per KV tile (MMA N of QK^T, K of PV)
+constexpr int kStages = 4;     // K/V ring depth
+constexpr int kThreads = 192;  // 6 warps
+constexpr float kRescaleLog2 = 8.f;
+
+template <int D>
+struct TcCfg {
+  static constexpr int kDB = D / 64;                  // 64-element (128-byte) column blocks
+  static constexpr int kQBlock = kRows * 128;         // bytes per column block of Q
+  static constexpr int kKVBlock = kBN * 128;          // bytes per column block of a K or V tile
+  static constexpr int kQBytes = kDB * kQBlock;
+  static constexpr int kStageBytes = 2 * kDB * kKVBlock;
+  static constexpr int kPBytes = kRows * kBN * 2;     // one P buffer (128 rows x 64 keys bf16)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kOffQ + kQBytes;
+  static constexpr int kOffP = kOffKV + kStages * kStageBytes;
+  static constexpr int kOffPar = kOffP + 2 * kPBytes;
+  static constexpr int kOffBar = kOffPar + kMaxNodes * 4;
+  static constexpr int kSmemUsed = kOffBar + 256;
+  static constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t kTmemCols = 256;           // S[0], S[1] (64 each) + O (D)
+  static constexpr uint32_t kColO = 2 * kBN;
+  static_assert(kColO + D <= kTmemCols, "TMEM budget");
+};
+
+struct TcArgs {
+  void* out;
+  const int32_t* parent;
+  int B, Hq, Hkv, N, P, G, NT, MT, splits;
+  float c;  // softmax scale * log2(e)
+  float* part;
+  float2* ml;
+  unsigned* cnt;
+  int32_t* dev_status;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full[2];
+  uint64_t p_free[2];
+  uint64_t o_done;
+  uint32_t tmem_base;
+  int abort;
+  int last;
+};
+
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// 64-bit visibility mask of keys [j0, j0 + 64) for tree node `node`.
+__device__ __forceinline__ uint64_t key_mask(int j0, int P, int N, int node, const int* s_par) {
+  if (j0 + kBN <= P) return ~0ull;
+  uint64_t vis = 0;
+  if (j0 < P) vis = (1ull << (P - j0)) - 1ull;
+  int a = node, guard = 0;
+  while (a >= 0 && guard <= N) {
+    const int j = P + a - j0;
+    if (j >= 0 && j < kBN) vis |= 1ull << j;
+    const int pa = s_par[a];
+    if (pa >= a) break;  // malformed (flagged when loaded)
+    a = pa;
+    ++guard;
+  }
+  return vis;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, TcArgs a) {
+  using C = TcCfg<D>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t mis = ptx::smem_addr(smem_raw) & 1023u;
+  unsigned char* sm = smem_raw + ((1024u - mis) & 1023u);
+  unsigned char* sQ = sm + C::kOffQ;
+  unsigned char* sKV = sm + C::kOffKV;
+  unsigned char* sP = sm + C::kOffP;
+  int* s_par = reinterpret_cast<int*>(sm + C::kOffPar);
+  Bars* bars = reinterpret_cast<Bars*>(sm + C::kOffBar);
+  volatile int* abort_flag = &bars->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x % a.MT, split = blockIdx.x / a.MT;
+  const int hk = blockIdx.y, b = blockIdx.z;
+  const int i0 = mt * a.NT;
+  const int nodes_hi = min(a.N, i0 + a.NT);
+  const int ltot = a.P + nodes_hi;
+  const int t_all = (ltot + kBN - 1) / kBN;
+  const int tps = (t_all + a.splits - 1) / a.splits;
+  const int t_begin = split * tps;
+  const int nt = max(0, min(t_all, t_begin + tps) - t_begin);
+  const int rows_used = a.G * a.NT;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&bars->kv_full[s], 1);
+      ptx::mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&bars->s_full[s], 1);
+      ptx::mbar_init(&bars->s_free[s], 4);
+      ptx::mbar_init(&bars->p_full[s], 4);
+      ptx::mbar_init(&bars->p_free[s], 1);
+    }
+    ptx::mbar_init(&bars->o_done, 1);
+    bars->abort = 0;
+    bars->last = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp >= 2) {
+    // parent array for the mask; zero the Q rows that no TMA box fills
+    const int t = threadIdx.x - 64;
+    int bad = 0;
+    for (int c = t; c < a.N; c += 128) {
+      const int p = a.parent[(size_t)b * a.N + c];
+      s_par[c] = p;
+      if (!((c == 0) ? (p == -1) : (p >= 0 && p < c))) bad = 1;
+    }
+    if (bad) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);
+    for (int r = rows_used + t; r < kRows; r += 128)
+      for (int db = 0; db < C::kDB; ++db) {
+        uint4* row = reinterpret_cast<uint4*>(sQ + db * C::kQBlock + r * 128);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) row[k] = make_uint4(0, 0, 0, 0);
+      }
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0 && nt > 0) {
+      int issued[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) issued[s] = 0;
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmK);
+      ptx::prefetch_tmap(&tmV);
+      ptx::mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(rows_used * 128 * C::kDB));
+      for (int g = 0; g < a.G; ++g)
+        for (int db = 0; db < C::kDB; ++db)
+          ptx::tma_load_3d(sQ + db * C::kQBlock + g * a.NT * 128, &tmQ, &bars->q_full, db * 64, i0,
+                           b * a.Hq + hk * a.G + g);
+      for (int t = 0; t < nt; ++t) {
+        const int st = t % kStages;
+        if (t >= kStages && !ptx::mbar_wait(&bars->kv_empty[st], ((t / kStages) - 1) & 1, abort_flag)) break;
+        unsigned char* sK = sKV + st * C::kStageBytes;
+        unsigned char* sV = sK + C::kDB * C::kKVBlock;
+        const int j0 = (t_begin + t) * kBN;
+        ptx::mbar_arrive_expect_tx(&bars->kv_full[st], (uint32_t)C::kStageBytes);
+        for (int db = 0; db < C::kDB; ++db) {
+          ptx::tma_load_3d(sK + db * C::kKVBlock, &tmK, &bars->kv_full[st], db * 64, j0, b * a.Hkv + hk);
+          ptx::tma_load_3d(sV + db * C::kKVBlock, &tmV, &bars->kv_full[st], db * 64, j0, b * a.Hkv + hk);
+        }
+        ++issued[st];
+      }
+      // never leave the CTA with copies in flight
+      ptx::mbar_wait(&bars->q_full, 0, abort_flag);
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s]) ptx::mbar_wait(&bars->kv_full[s], (issued[s] - 1) & 1, abort_flag);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      if (nt > 0 && ptx::mbar_wait(&bars->q_full, 0, abort_flag)) {
+        constexpr uint32_t idS = ptx::idesc_bf16(kRows, kBN, false, false);
+        constexpr uint32_t idO = ptx::idesc_bf16(kRows, D, false, true);
+        const uint32_t qaddr = ptx::smem_addr(sQ);
+        bool ok = true;
+        auto issue_s = [&](int t) -> bool {
+          const int st = t % kStages, sb = t & 1;
+          if (!ptx::mbar_wait(&bars->kv_full[st], (t / kStages) & 1, abort_flag)) return false;
+          if (t >= 2 && !ptx::mbar_wait(&bars->s_free[sb], ((t >> 1) - 1) & 1, abort_flag)) return false;
+          ptx::tc_fence_after();
+          const uint32_t kaddr = ptx::smem_addr(sKV + st * C::kStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk & 3) * 32;  // 16-element K step inside a 128-byte row
+            const uint64_t ad = ptx::sdesc_sw128(qaddr + (kk >> 2) * C::kQBlock + off, 16, 1024);
+            const uint64_t bd = ptx::sdesc_sw128(kaddr + (kk >> 2) * C::kKVBlock + off, 16, 1024);
+            ptx::mma_bf16_ss(tmem + sb * kBN, ad, bd, idS, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&bars->s_full[sb]);
+          return true;
+        };
+        auto issue_pv = [&](int t) -> bool {
+          const int st = t % kStages, sb = t & 1;
+          if (!ptx::mbar_wait(&bars->p_full[sb], (t >> 1) & 1, abort_flag)) return false;
+          ptx::tc_fence_after();
+          const uint32_t paddr = ptx::smem_addr(sP + sb * C::kPBytes);
+          const uint32_t vaddr = ptx::smem_addr(sKV + st * C::kStageBytes + C::kDB * C::kKVBlock);
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t ad = ptx::sdesc_sw128(paddr + kk * 32, 16, 1024);
+            const uint64_t bd = ptx::sdesc_sw128(vaddr + kk * 16 * 128, C::kKVBlock, 1024);
+            ptx::mma_bf16_ss(tmem + C::kColO, ad, bd, idO, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(&bars->kv_empty[st]);
+          ptx::mma_commit(&bars->p_free[sb]);
+          return true;
+        };
+        ok = issue_s(0);
+        for (int t = 0; ok && t < nt; ++t) {
+          if (t + 1 < nt) ok = issue_s(t + 1);
+          if (ok) ok = issue_pv(t);
+        }
+      }
+      ptx::mma_commit(&bars->o_done);
+      ptx::mbar_wait(&bars->o_done, 0, abort_flag);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax rows
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int g = r / a.NT, il = r % a.NT;
+    const int node = i0 + il;
+    const bool valid = (g < a.G) && (node < a.N) && (r < rows_used);
+    const int mnode = valid ? node : 0;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int t = 0; t < nt; ++t) {
+      const int sb = t & 1;
+      ok = ptx::mbar_wait(&bars->s_full[sb], (t >> 1) & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      float sv[kBN];
+      ptx::tmem_ld32(tmem + lane_base + sb * kBN, sv);
+      ptx::tmem_ld32(tmem + lane_base + sb * kBN + 32, sv + 32);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->s_free[sb]);
+
+      const int j0 = (t_begin + t) * kBN;
+      const uint64_t vis = key_mask(j0, a.P, a.N, mnode, s_par);
+      float tm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kBN; ++j)
+        if ((vis >> j) & 1ull) tm = fmaxf(tm, sv[j]);
+      const float tms = tm * a.c;
+      float alpha = 1.f;
+      bool need = false;
+      if (tms > m_run + kRescaleLog2) {
+        if (m_run != -INFINITY) {
+          alpha = exp2f(m_run - tms);
+          need = true;
+        }
+        m_run = tms;
+      }
+      if (__any_sync(0xffffffffu, need) && t > 0) {
+        // O already holds PV(t-1): wait for it, then scale this warp's rows
+        ok = ptx::mbar_wait(&bars->p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float ov[32];
+          ptx::tmem_ld32(tmem + lane_base + C::kColO + c0, ov);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] *= alpha;
+          ptx::tmem_st32(tmem + lane_base + C::kColO + c0, ov);
+        }
+        ptx::tmem_wait_st();
+      }
+      l_run *= alpha;
+      if (t >= 2) {
+        ok = ptx::mbar_wait(&bars->p_free[sb], ((t >> 1) - 1) & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      // P = 2^(S*c - m_run) on visible keys, bf16, 128-byte-swizzled K-major rows
+      unsigned char* prow = sP + sb * C::kPBytes + r * 128;
+      float lsum = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        float p[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int j = ch * 8 + k;
+          p[k] = (((vis >> j) & 1ull) && m_run != -INFINITY) ? exp2f(fmaf(sv[j], a.c, -m_run)) : 0.f;
+          lsum += p[k];
+        }
+        uint4 u;
+        u.x = pack_bf16x2(p[0], p[1]);
+        u.y = pack_bf16x2(p[2], p[3]);
+        u.z = pack_bf16x2(p[4], p[5]);
+        u.w = pack_bf16x2(p[6], p[7]);
+        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = u;
+      }
+      l_run += lsum;
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->p_full[sb]);
+    }
+    // ---- epilogue
+    bool have_o = false;
+    if (nt > 0) {
+      ok = ptx::mbar_wait(&bars->o_done, 0, abort_flag) && ok;
+      ok = __all_sync(0xffffffffu, ok);
+      have_o = ok;
+      if (ok) ptx::tc_fence_after();
+    }
+    const int h = hk * a.G + g;
+    const size_t orow = (((size_t)b * a.Hq + h) * a.N + node) * D;
+    const size_t slot = (((size_t)b * a.Hkv + hk) * a.MT + mt) * a.splits + split;
+    if (a.splits == 1) {
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float ov[32];
+        if (have_o) {
+          ptx::tmem_ld32(tmem + lane_base + C::kColO + c0, ov);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] = 0.f;
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow + c0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 u;
+            u.x = pack_bf16x2(ov[8 * k + 0] * inv, ov[8 * k + 1] * inv);
+            u.y = pack_bf16x2(ov[8 * k + 2] * inv, ov[8 * k + 3] * inv);
+            u.z = pack_bf16x2(ov[8 * k + 4] * inv, ov[8 * k + 5] * inv);
+            u.w = pack_bf16x2(ov[8 * k + 6] * inv, ov[8 * k + 7] * inv);
+            dst[k] = u;
+          }
+        }
+      }
+    } else {
+      float* prow = a.part + (slot * kRows + r) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float ov[32];
+        if (have_o) {
+          ptx::tmem_ld32(tmem + lane_base + C::kColO + c0, ov);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          reinterpret_cast<float4*>(prow + c0)[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+      }
+      a.ml[slot * kRows + r] = make_float2(have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
+      __threadfence();
+      softmax_sync();
+      const size_t tile = ((size_t)b * a.Hkv + hk) * a.MT + mt;
+      if (threadIdx.x == 64) {
+        const unsigned prev = atomicAdd(a.cnt + tile, 1u);
+        bars->last = (prev == (unsigned)(a.splits - 1));
+      }
+      softmax_sync();
+      if (bars->last) {
+        __threadfence();
+        if (valid) {
+          const size_t slot0 = tile * a.splits;
+          float M = -INFINITY;
+          for (int s = 0; s < a.splits; ++s) M = fmaxf(M, __ldcg(&a.ml[(slot0 + s) * kRows + r].x));
+          float L = 0.f;
+          for (int s = 0; s < a.splits; ++s) {
+            const float2 v = __ldcg(&a.ml[(slot0 + s) * kRows + r]);
+            if (v.x != -INFINITY) L += v.y * exp2f(v.x - M);
+          }
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          for (int c0 = 0; c0 < D; c0 += 8) {
+            float acc[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+            for (int s = 0; s < a.splits; ++s) {
+              const float mx = __ldcg(&a.ml[(slot0 + s) * kRows + r].x);
+              if (mx == -INFINITY) continue;
+              const float w = exp2f(mx - M);
+              const float4* src = reinterpret_cast<const float4*>(a.part + ((slot0 + s) * kRows + r) * D + c0);
+              const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+              acc[0] = fmaf(w, x0.x, acc[0]);
+              acc[1] = fmaf(w, x0.y, acc[1]);
+              acc[2] = fmaf(w, x0.z, acc[2]);
+              acc[3] = fmaf(w, x0.w, acc[3]);
+              acc[4] = fmaf(w, x1.x, acc[4]);
+              acc[5] = fmaf(w, x1.y, acc[5]);
+              acc[6] = fmaf(w, x1.z, acc[6]);
+              acc[7] = fmaf(w, x1.w, acc[7]);
+            }
+            uint4 u;
+            u.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            u.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+            u.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+            u.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+            *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow + c0) = u;
+          }
+        }
+        if (threadIdx.x == 64) a.cnt[tile] = 0;
+      }
+    }
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && bars->abort) set_dev_status(a.dev_status, TV_DEV_TIMEOUT);
+}
+
+// ------------------------------------------------------------------------------------
+// host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 3-D bf16 map {D, rows, planes} with a 64 x box_rows x 1 box, 128-byte swizzle.
+static bool encode_3d(CUtensorMap* m, const void* base, int D, int rows, long long planes, long long row_stride_elems,
+                      long long plane_stride_elems, int box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)row_stride_elems * 2, (cuuint64_t)plane_stride_elems * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) {
+  AttnPlan p{};
+  const int G = Hkv > 0 ? Hq / Hkv : 0;
+  p.tc = dtype == TV_BF16 && (D == 64 || D == 128) && G >= 1 && G <= 16 && (long long)G * N >= 64;
+  if (!p.tc) return p;
+  p.nt = (kRows / G) / 8 * 8;
+  p.mtiles = (N + p.nt - 1) / p.nt;
+  const long long base = (long long)B * Hkv * p.mtiles;
+  const int t_all = (P + N + kBN - 1) / kBN;
+  // pick the split count that fills 152 SMs (one CTA each) best; at least 4 KV tiles
+  // per split, and no more partial traffic than needed
+  int best = 1;
+  double best_eff = 0.0;
+  const int smax = std::max(1, std::min(32, t_all / 4));
+  for (int s = 1; s <= smax; ++s) {
+    const long long ctas = base * s;
+    const long long waves = (ctas + 151) / 152;
+    const double eff = (double)ctas / (double)(waves * 152);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  p.splits = best;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  };
+  const size_t slots = (size_t)base * p.splits;
+  p.ws_cnt = take((size_t)base * 4);
+  p.ws_ml = p.splits > 1 ? take(slots * kRows * sizeof(float2)) : 0;
+  p.ws_part = p.splits > 1 ? take(slots * kRows * D * sizeof(float)) : 0;
+  p.total = off;
+  return p;
+}
+
+template <int D>
+static cudaError_t launch_tc_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const TcArgs& a,
+                               int B, int Hkv, cudaStream_t stream) {
+  using C = TcCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.MT * a.splits, Hkv, B);
+  attn_tc_kernel<D><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* out, const int32_t* parent, int B,
+                           int Hq, int Hkv, int D, int P, int N, int S, float scale, const AttnPlan& plan, char* ws,
+                           int32_t* dev_status, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  if (!encode_3d(&mq, q, D, N, (long long)B * Hq, D, (long long)N * D, plan.nt)) return cudaErrorInvalidValue;
+  if (!encode_3d(&mk, k, D, P + N, (long long)B * Hkv, D, (long long)S * D, kBN)) return cudaErrorInvalidValue;
+  if (!encode_3d(&mv, v, D, P + N, (long long)B * Hkv, D, (long long)S * D, kBN)) return cudaErrorInvalidValue;
+  TcArgs a;
+  a.out = out;
+  a.parent = parent;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.P = P;
+  a.G = Hq / Hkv;
+  a.NT = plan.nt;
+  a.MT = plan.mtiles;
+  a.splits = plan.splits;
+  a.c = scale * kLog2e;
+  a.part = plan.splits > 1 ? reinterpret_cast<float*>(ws + plan.ws_part) : nullptr;
+  a.ml = plan.splits > 1 ? reinterpret_cast<float2*>(ws + plan.ws_ml) : nullptr;
+  a.cnt = reinterpret_cast<unsigned*>(ws + plan.ws_cnt);
+  a.dev_status = dev_status;
+  if (D == 64) return launch_tc_d<64>(mq, mk, mv, a, B, Hkv, stream);
+  return launch_tc_d<128>(mq, mk, mv, a, B, Hkv, stream);
+}
+
+}  // namespace tv

@@ -1,0 +1,109 @@
+// Tree structure: depth / position ids, ancestor bitmask and child lists.
+//
+// PTD (Progressive Tree Drafting) §3.1 "tree construction": node v may attend only to
+// its observable prefix set pi(v) = {v} U pi(P(v)); its position encoding is fixed by
+// |pi(v)|.  One CTA of 1024 threads per sequence; parent[] lives in shared memory.
+#include "tv_kernels.cuh"
+
+namespace tv {
+
+__global__ void __launch_bounds__(1024) tree_prep_kernel(const int32_t* __restrict__ parent, int N, int P,
+                                                         int32_t* depth, int32_t* pos, uint32_t* anc_mask,
+                                                         int32_t* child_off, int32_t* child_idx,
+                                                         int32_t* dev_status) {
+  __shared__ int s_par[kMaxNodes];
+  __shared__ int s_cnt[kMaxNodes + 1];
+  __shared__ int s_wsum[32];
+  __shared__ int s_bad;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int W = (N + 31) / 32;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  for (int i = tid; i < N; i += blockDim.x) {
+    const int p = parent[(size_t)b * N + i];
+    s_par[i] = p;
+    s_cnt[i] = 0;
+    if (!((i == 0) ? (p == -1) : (p >= 0 && p < i))) atomicOr(&s_bad, TV_DEV_BAD_TREE);
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) set_dev_status(dev_status, s_bad);
+    return;
+  }
+  for (int i = tid; i < N; i += blockDim.x) {
+    // walk i, parent(i), ..., root: indices strictly decrease, so words are visited
+    // from high to low and each mask word is written exactly once
+    int a = i, d = -1, cw = W - 1;
+    uint32_t bits = 0;
+    uint32_t* row = anc_mask ? anc_mask + ((size_t)b * N + i) * W : nullptr;
+    while (a >= 0) {
+      const int w = a >> 5;
+      while (cw > w) {
+        if (row) row[cw] = bits;
+        bits = 0;
+        --cw;
+      }
+      bits |= 1u << (a & 31);
+      a = s_par[a];
+      ++d;
+    }
+    while (cw >= 0) {
+      if (row) row[cw] = bits;
+      bits = 0;
+      --cw;
+    }
+    if (depth) depth[(size_t)b * N + i] = d;
+    if (pos) pos[(size_t)b * N + i] = P + d;
+    if (i > 0) atomicAdd(&s_cnt[s_par[i]], 1);
+  }
+  if (!child_off) return;
+  __syncthreads();
+  // exclusive scan of child counts (N <= 1024 = one element per thread)
+  const int x = tid < N ? s_cnt[tid] : 0;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_wsum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int v = s_wsum[lane];
+    int vi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, vi, o);
+      if (lane >= o) vi += y;
+    }
+    s_wsum[lane] = vi - v;
+  }
+  __syncthreads();
+  const int excl = s_wsum[wid] + incl - x;
+  __syncthreads();
+  if (tid < N) {
+    s_cnt[tid] = excl;
+    child_off[(size_t)b * (N + 1) + tid] = excl;
+  }
+  if (tid == 0) child_off[(size_t)b * (N + 1) + N] = N - 1;
+  __syncthreads();
+  for (int c = tid + 1; c < N; c += blockDim.x) {
+    if (c >= N) break;
+    const int u = s_par[c];
+    int rank = 0;
+    for (int j = u + 1; j < c; ++j) rank += (s_par[j] == u);
+    child_idx[(size_t)b * N + s_cnt[u] + rank] = c;
+  }
+  if (tid == 0 && N >= 1) child_idx[(size_t)b * N + N - 1] = -1;
+  // (slot N-1 is only used when N-1 children exist; a tree has N-1 edges, so the
+  // list fills slots 0..N-2 and the last slot is padding)
+}
+
+cudaError_t launch_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* depth, int32_t* pos,
+                             uint32_t* anc_mask, int32_t* child_off, int32_t* child_idx,
+                             int32_t* dev_status, cudaStream_t stream) {
+  tree_prep_kernel<<<B, 1024, 0, stream>>>(parent, N, P, depth, pos, anc_mask, child_off, child_idx, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace tv

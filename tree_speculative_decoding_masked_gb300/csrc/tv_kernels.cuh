@@ -1,0 +1,58 @@
+// Internal declarations shared between the kernel files and the C-ABI layer.
+#pragma once
+
+#include "tv_common.cuh"
+
+namespace tv {
+
+constexpr int kMaxNodes = 1024;  // N limit (tree nodes per sequence, root included)
+constexpr int kMaxDepth = 16;    // selection pool depth d
+constexpr int kMaxRank = 256;    // selection pool width K
+constexpr int kMaxBudget = 4096; // selection budget (rows)
+
+// ---- verify (vocab pass + walks)
+struct VerifyWs {
+  int splits;
+  size_t row_cnt, seq_cnt, part, part_q, lse2, lse2_q, amax, pc, qc, total;
+};
+int verify_splits(int rows, int V);
+size_t verify_ws_layout(int B, int N, int V, int sampling, VerifyWs* w);
+cudaError_t launch_vocab_pass(const void* logits, const void* draft, const int32_t* parent,
+                              const int32_t* tokens, int B, int N, int V, tv_dtype dtype, float temperature,
+                              char* ws, const VerifyWs& w, int32_t* accepted, int32_t* accept_len,
+                              int32_t* bonus, float* p_draft, float* q_draft, float* row_lse,
+                              int32_t* row_argmax, int32_t* dev_status, int sampling, cudaStream_t stream);
+cudaError_t launch_sample_walk(const void* target, const void* draft, const int32_t* parent,
+                               const int32_t* tokens, int B, int N, int V, tv_dtype dtype, float temperature,
+                               uint64_t seed, uint64_t round, char* ws, const VerifyWs& w,
+                               int32_t* accepted, int32_t* accept_len, int32_t* out_token,
+                               int32_t* dev_status, cudaStream_t stream);
+
+// ---- tree prep
+cudaError_t launch_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* depth, int32_t* pos,
+                             uint32_t* anc_mask, int32_t* child_off, int32_t* child_idx,
+                             int32_t* dev_status, cudaStream_t stream);
+
+// ---- selection
+size_t select_ws_bytes(int B, int d, int K, int budget);
+cudaError_t launch_select(const float* marg, const int32_t* ptok, int B, int d, int K, int budget,
+                          const int32_t* root_token, int32_t* parent, int32_t* tokens, int32_t* depth,
+                          float* score, int32_t* n_nodes, char* ws, int32_t* dev_status, cudaStream_t stream);
+
+// ---- attention
+struct AttnPlan {
+  bool tc;        // tensor-core (tcgen05) kernel
+  int nt;         // nodes per 128-row tile (tc)
+  int mtiles;     // row tiles per (b, kv head)
+  int splits;     // KV splits per row tile
+  size_t ws_part, ws_ml, ws_cnt, total;
+};
+AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype);
+cudaError_t launch_attn_simt(const void* q, const void* k, const void* v, void* out, const int32_t* parent,
+                             int B, int Hq, int Hkv, int D, int P, int N, int S, float scale, tv_dtype dtype,
+                             int32_t* dev_status, cudaStream_t stream);
+cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* out, const int32_t* parent,
+                           int B, int Hq, int Hkv, int D, int P, int N, int S, float scale, const AttnPlan& plan,
+                           char* ws, int32_t* dev_status, cudaStream_t stream);
+
+}  // namespace tv
