@@ -22,9 +22,10 @@ Readings (the pages state the rule for one draft per position only):
     child is rejected, or u is a leaf, the output token is drawn from the current p by
     inverse CDF with r = U(seed, round, b, u, 0, kind 1): the smallest v such that
     r * sum(p) < p(0) + ... + p(v).
-Every random decision is also returned with its margin (distance from r to the decision
-threshold, relative to the total mass for the inverse CDF) so that a float implementation
-can be compared decision by decision.
+Every random decision is also returned with its margin, as a (kind, margin) pair:
+("accept", |r - alpha|) for an acceptance test and ("icdf", distance from r * sum(p) to
+the nearest edge of the chosen bucket, relative to sum(p)) for the final draw, so that a
+float implementation can be compared decision by decision.
 """
 from __future__ import annotations
 
@@ -77,7 +78,7 @@ def sampling_walk(target_logits, draft_logits, parent, tokens, temperature: floa
             t = int(tokens[c])
             r = uniform(seed, rnd, b, u, k, 0)
             alpha = acceptance_prob(float(p[t]), float(q[t]))
-            margins.append(abs(r - alpha))
+            margins.append(("accept", abs(r - alpha)))
             if r < alpha:
                 accepted.append(c)
                 u = c
@@ -95,5 +96,5 @@ def sampling_walk(target_logits, draft_logits, parent, tokens, temperature: floa
             continue
         r = uniform(seed, rnd, b, u, 0, 1)
         v, m = inverse_cdf(p, r)
-        margins.append(m)
+        margins.append(("icdf", m))
         return accepted, v, margins, u

@@ -30,11 +30,20 @@ def validate(parent) -> None:
 
 
 def observable_set(parent, v: int) -> frozenset:
-    """pi(v) = {v} U pi(P(v)), written as the recursion it is."""
-    p = int(parent[v])
-    if p < 0:
-        return frozenset({v})
-    return frozenset({v}) | observable_set(parent, p)
+    """pi(v) = {v} U pi(P(v)), with pi(root) = {root}.
+
+    The recursion is unrolled into its sequence of steps: v, P(v), P(P(v)), ... are added
+    until the root's parent (-1) is reached (an explicit loop, so that trees deeper than
+    Python's recursion limit work).
+    """
+    out = set()
+    n = len(parent)
+    while v >= 0:
+        if v in out or len(out) > n:
+            raise ValueError("parent array has a cycle")
+        out.add(int(v))
+        v = int(parent[v])
+    return frozenset(out)
 
 
 def root_path(parent, v: int) -> list:

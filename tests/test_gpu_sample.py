@@ -1,9 +1,14 @@
 """GPU parity: tv_verify_sample against the oracle.
 
-Decisions are compared one by one: wherever every random decision on the oracle's path
-clears its threshold by more than 1e-5 (the fp32 vs fp64 error is ~1e-6), accepted path
-and output token must be identical; sequences whose path passes closer to a threshold are
-counted and must stay rare.  Drafted-token probabilities match within 1e-4 (fp32) /
+Decisions are compared one by one.  Wherever every random decision on the oracle's path
+clears its threshold by a safe margin, accepted path and output token must be identical;
+sequences whose path passes closer are counted and must stay rare.  Margins:
+  * acceptance tests r < min(1, p/q): |r - alpha| > 1e-5 (the GPU forms p and q in fp32
+    from fp32 log-sum-exps, alpha to a few 1e-6 relative);
+  * inverse-CDF draws: the target r * sum(p) lies more than 2e-7 * sum(p) from the
+    chosen bucket's edges (the GPU sums fp32 probabilities in fp64; a common scale error
+    of all p cancels between the target and the prefix sums, the per-element rounding
+    leaves ~1e-9 of the total).  Drafted-token probabilities match within 1e-4 (fp32) /
 2e-2 (bf16).  The distribution pin (the blog's promise that sampling verification keeps
 the target distribution) is re-run on the GPU with a chi-square test."""
 import math
@@ -25,7 +30,7 @@ if not torch.cuda.is_available():
 import tree_speculative_decoding_masked_gb300 as tv  # noqa: E402
 from gpu_util import i32, to_dev  # noqa: E402
 
-MARGIN = 1e-5
+MARGIN = {"accept": 1e-5, "icdf": 2e-7}
 
 
 def _run(tgt, drf, par, tok, bf16, T, seed, rnd, workspace=None):
@@ -48,7 +53,7 @@ def _compare(tgt, drf, par, tok, got, bf16, T, seed, rnd):
         assert np.max(np.abs(got["q_draft"][b][1:] - q[1:])) < tol
         acc, out_tok, margins, _ = sampling.sampling_walk(tgt[b], drf[b], par[b], tok[b], T, seed, rnd, b)
         L = int(got["accept_len"][b])
-        if min(margins) <= MARGIN:
+        if any(m <= MARGIN[kind] for kind, m in margins):
             close += 1
             continue
         assert got["accepted_nodes"][b][:L].tolist() == acc, b
@@ -79,7 +84,7 @@ def test_sampling_workload_full_vocab():
     par, _ = W.trees(g, B, cfg["N"], cfg["depth_cap"], cfg["V"])
     tgt, drf, tok = W.sampling_logits(g, par, cfg["V"], True, cfg["temperature"])
     got = _run(tgt, drf, par, tok, True, cfg["temperature"], cfg["seed"], 0)
-    assert _compare(tgt, drf, par, tok, got, True, cfg["temperature"], cfg["seed"], 0) == 0
+    assert _compare(tgt, drf, par, tok, got, True, cfg["temperature"], cfg["seed"], 0) <= 1
 
 
 def test_identical_distributions_accept_everything():
