@@ -154,6 +154,30 @@ TV_API tv_status tv_verify_greedy(const void* logits, const int32_t* parent, con
                            int32_t* dev_status, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * tv_verify_greedy_static - tv_verify_greedy for callers that cannot allocate.
+ * No counterpart in the paper: this is a packaging variant of tv_verify_greedy.  Some
+ * callers cannot provide a workspace at call time - a plugin whose host framework owns
+ * and plans all device memory, code running while a CUDA graph is being captured by a
+ * component that forbids allocations, or runtimes that disallow allocation after
+ * start-up.  This entry point takes the same inputs and outputs as tv_verify_greedy but
+ * keeps its scratch in a fixed 4 MiB array inside the library's device image (every
+ * GPU that loads the library holds it until exit).  It allocates nothing.
+ *   - The first call on a device looks up that array's device address and zero-fills it
+ *     synchronously; make that first call (per device) before any stream capture.
+ *   - Each call clears the completion counters on `stream` before the vocab pass.
+ *   - All calls share the array: calls that overlap on the GPU (other streams, other
+ *     host threads) race and give undefined results.
+ *   - Returns TV_ERR_WORKSPACE when the problem needs more scratch than the array holds
+ *     (about 40 bytes per logits row, i.e. B*N up to ~100k rows); other errors as
+ *     tv_verify_greedy.
+ */
+TV_API tv_status tv_verify_greedy_static(const void* logits, const int32_t* parent, const int32_t* tokens,
+                                         int B, int N, int V, tv_dtype dtype, int32_t* accepted_nodes,
+                                         int32_t* accept_len, int32_t* bonus_token, float* p_draft,
+                                         float* row_lse, int32_t* row_argmax, int32_t* dev_status,
+                                         tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * tv_verify_sample - stochastic acceptance down the draft tree.
  * Blog "acceptance probability for sampling": draft token t at node u is kept with
  * probability min(1, p_u(t)/q_u(t)); "how to correct after a rejection": the

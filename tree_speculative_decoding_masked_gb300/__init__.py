@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     tree_attention_workspace_size,
     tree_prep,
     verify_greedy,
+    verify_greedy_static,
     verify_sample,
     verify_workspace_size,
 )

@@ -45,6 +45,7 @@ _SIGS = {
     "tv_tree_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _P]),
     "tv_verify_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "tv_verify_greedy": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "tv_verify_greedy_static": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "tv_verify_sample": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _U64, _U64, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tv_select_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "tv_select_subtree": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
@@ -202,6 +203,35 @@ def verify_greedy(logits, parent, tokens, *, want_stats: bool = False, workspace
            lib.tv_verify_greedy(_ptr(logits), _ptr(parent), _ptr(tokens), B, N, V, code, _ptr(acc), _ptr(alen),
                                 _ptr(bonus), _ptr(pdr), _ptr(lse), _ptr(am), _ptr(ws), ws.numel() * ws.element_size(),
                                 _ptr(st), _stream()))
+    res = {"accepted_nodes": acc, "accept_len": alen, "bonus_token": bonus, "p_draft": pdr, "dev_status": st}
+    if want_stats:
+        res["row_lse"] = lse
+        res["row_argmax"] = am
+    return res
+
+
+def verify_greedy_static(logits, parent, tokens, *, want_stats: bool = False, dev_status=None, out=None):
+    """Greedy acceptance without a workspace, for callers that cannot allocate device
+    memory when they call the library: the scratch lives in a fixed 4 MiB array inside
+    the library.  The first call on a device sets that array up (call it once before any
+    stream capture); calls that overlap on the GPU race on the shared array.  Same
+    results as verify_greedy."""
+    _need_cuda(logits=logits, parent=parent, tokens=tokens)
+    lib = load_library()
+    B, N, V = logits.shape
+    dev = logits.device
+    code = _dtype_code(logits)
+    o = out if out is not None else {}
+    acc = _out(o, "accepted_nodes", (B, N), torch.int32, dev)
+    alen = _out(o, "accept_len", (B), torch.int32, dev)
+    bonus = _out(o, "bonus_token", (B), torch.int32, dev)
+    pdr = _out(o, "p_draft", (B, N), torch.float32, dev)
+    lse = _out(o, "row_lse", (B, N), torch.float32, dev) if want_stats else None
+    am = _out(o, "row_argmax", (B, N), torch.int32, dev) if want_stats else None
+    st = _status_tensor(dev_status, dev)
+    _check("tv_verify_greedy_static",
+           lib.tv_verify_greedy_static(_ptr(logits), _ptr(parent), _ptr(tokens), B, N, V, code, _ptr(acc),
+                                       _ptr(alen), _ptr(bonus), _ptr(pdr), _ptr(lse), _ptr(am), _ptr(st), _stream()))
     res = {"accepted_nodes": acc, "accept_len": alen, "bonus_token": bonus, "p_draft": pdr, "dev_status": st}
     if want_stats:
         res["row_lse"] = lse
