@@ -410,10 +410,21 @@ def run_ours(args):
             tv.verify_greedy(s["logits"], sel_out["parent"], sel_out["tokens"], workspace=ws_ver, dev_status=status,
                              out=ver_out)
 
+    side = torch.cuda.Stream(device=dev)
+
     def step(s):
+        # selection feeds both; tree attention and the vocab pass are independent of each
+        # other and run concurrently (fork after selection, join before the next step)
         k_select(s)
+        fork = torch.cuda.Event()
+        fork.record()
+        side.wait_event(fork)
         k_attn(s)
-        k_verify(s)
+        with torch.cuda.stream(side):
+            k_verify(s)
+            join = torch.cuda.Event()
+            join.record()
+        torch.cuda.current_stream().wait_event(join)
 
     launches_per_step = (1 if use_pool else 0) + 1 + (2 if sampling_mode else 1)
 
@@ -528,8 +539,8 @@ def run_ours(args):
             "config": dict(workload_config(args.workload, cfg),
                            l2=f"inputs rotate over {n_sets} device copies, {n_sets * bytes_set / 1e6:.0f} MB "
                               f"> 2 x L2 ({l2 / 1e6:.0f} MB)",
-                           step="select_subtree + tree_attention + " +
-                                ("verify_sample" if sampling_mode else "verify_greedy"),
+                           step="select_subtree, then tree_attention || " +
+                                ("verify_sample" if sampling_mode else "verify_greedy") + " (two streams)",
                            parallelism=f"replicas x{world}"),
             "path_gbs": bytes_set / (ms_per_step * 1e-3) / 1e9,
             "breakdown_us": br,

@@ -70,6 +70,17 @@ def test_max_sizes_and_single_rank():
     _check_select(marg1, ptok1, 40, roots, _gpu_select(marg1, ptok1, 40, roots))
 
 
+@pytest.mark.parametrize("budget", [40, 300, 2000])
+def test_uniform_pools_all_ties(budget):
+    # every path of a given depth ties: the order falls to depth, then the rank path;
+    # budget 2000 overflows the threshold expansion and exercises the exact fallback
+    d, k = 16, 8
+    marg = np.full((2, d, k), 0.125, dtype=np.float32)
+    ptok = np.tile(np.arange(d * k, dtype=np.int32).reshape(1, d, k), (2, 1, 1))
+    roots = np.array([1, 2], dtype=np.int32)
+    _check_select(marg, ptok, budget, roots, _gpu_select(marg, ptok, budget, roots))
+
+
 def test_unsorted_pool_is_flagged():
     marg = np.array([[[0.2, 0.7], [0.6, 0.4]]], dtype=np.float32)
     ptok = np.array([[[1, 2], [3, 4]]], dtype=np.int32)

@@ -74,8 +74,7 @@ tv_status tv_tree_attention(const void* q, const void* k_cache, const void* v_ca
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return TV_ERR_ALIGN;
   AttnPlan p = attn_plan(B, Hq, Hkv, D, P, N, dtype);
   if (p.tc) {
-    if (!workspace || ws_bytes < p.total) return TV_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return TV_ERR_ALIGN;
+    if (p.total > 0 && (!workspace || ws_bytes < p.total)) return TV_ERR_WORKSPACE;
     if (B > 65535 || Hkv > 65535) return TV_ERR_SHAPE;
     return cuda_status(launch_attn_tc(q, k_cache, v_cache, out, parent, B, Hq, Hkv, D, P, N, kv_stride_tokens, scale,
                                       p, reinterpret_cast<char*>(workspace), dev_status, st(stream)));

@@ -15,8 +15,10 @@
 //   warps 2..5  softmax: one thread per row; read S from TMEM, apply the tree mask,
 //               keep a running reference max (rescale O only when the max grows by
 //               more than 2^8), write P (bf16) to shared memory for the second MMA.
-// With one split the epilogue normalises O and stores bf16; with several, rows are
-// written as fp32 partials (O, m, l) and the last CTA of the tile merges them.
+// With one split the epilogue normalises O and stores bf16.  With several, the splits of
+// a row tile run as one thread-block cluster: each CTA parks its unnormalised O and
+// (m, l) in its own shared memory and, after a cluster barrier, merges a slice of the
+// rows by reading its peers' partials over distributed shared memory.
 #include <cuda.h>
 
 #include <algorithm>
@@ -31,6 +33,7 @@ constexpr int kBN = 64;        // keys per KV tile (MMA N of QK^T, K of PV)
 constexpr int kStages = 4;     // K/V ring depth
 constexpr int kThreads = 192;  // 6 warps
 constexpr float kRescaleLog2 = 8.f;
+constexpr int kMaxSplits = 8;  // KV splits of a row tile = one portable-size cluster
 
 template <int D>
 struct TcCfg {
@@ -57,9 +60,6 @@ struct TcArgs {
   const int32_t* parent;
   int B, Hq, Hkv, N, P, G, NT, MT, splits;
   float c;  // softmax scale * log2(e)
-  float* part;
-  float2* ml;
-  unsigned* cnt;
   int32_t* dev_status;
 };
 
@@ -74,10 +74,7 @@ struct Bars {
   uint64_t o_done;
   uint32_t tmem_base;
   int abort;
-  int last;
 };
-
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // 64-bit visibility mask of keys [j0, j0 + 64) for tree node `node`.
 __device__ __forceinline__ uint64_t key_mask(int j0, int P, int N, int node, const int* s_par) {
@@ -137,7 +134,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(&bars->o_done, 1);
     bars->abort = 0;
-    bars->last = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -348,7 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int h = hk * a.G + g;
     const size_t orow = (((size_t)b * a.Hq + h) * a.N + node) * D;
-    const size_t slot = (((size_t)b * a.Hkv + hk) * a.MT + mt) * a.splits + split;
     if (a.splits == 1) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
@@ -375,7 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      float* prow = a.part + (slot * kRows + r) * D;
+      // park this split's unnormalised O (column-major [D][128], conflict-free) and its
+      // (m, l) in the drained K/V ring for the cluster merge below
+      float* part = reinterpret_cast<float*>(sKV);
+      float2* ml = reinterpret_cast<float2*>(sKV + D * kRows * 4);
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         float ov[32];
@@ -387,61 +385,76 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 32; ++k) ov[k] = 0.f;
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          reinterpret_cast<float4*>(prow + c0)[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+        for (int k = 0; k < 32; ++k) part[(c0 + k) * kRows + r] = ov[k];
       }
-      a.ml[slot * kRows + r] = make_float2(have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
-      __threadfence();
-      softmax_sync();
-      const size_t tile = ((size_t)b * a.Hkv + hk) * a.MT + mt;
-      if (threadIdx.x == 64) {
-        const unsigned prev = atomicAdd(a.cnt + tile, 1u);
-        bars->last = (prev == (unsigned)(a.splits - 1));
-      }
-      softmax_sync();
-      if (bars->last) {
-        __threadfence();
-        if (valid) {
-          const size_t slot0 = tile * a.splits;
-          float M = -INFINITY;
-          for (int s = 0; s < a.splits; ++s) M = fmaxf(M, __ldcg(&a.ml[(slot0 + s) * kRows + r].x));
-          float L = 0.f;
-          for (int s = 0; s < a.splits; ++s) {
-            const float2 v = __ldcg(&a.ml[(slot0 + s) * kRows + r]);
-            if (v.x != -INFINITY) L += v.y * exp2f(v.x - M);
-          }
-          const float inv = L > 0.f ? 1.f / L : 0.f;
-          for (int c0 = 0; c0 < D; c0 += 8) {
-            float acc[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-            for (int s = 0; s < a.splits; ++s) {
-              const float mx = __ldcg(&a.ml[(slot0 + s) * kRows + r].x);
-              if (mx == -INFINITY) continue;
-              const float w = exp2f(mx - M);
-              const float4* src = reinterpret_cast<const float4*>(a.part + ((slot0 + s) * kRows + r) * D + c0);
-              const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
-              acc[0] = fmaf(w, x0.x, acc[0]);
-              acc[1] = fmaf(w, x0.y, acc[1]);
-              acc[2] = fmaf(w, x0.z, acc[2]);
-              acc[3] = fmaf(w, x0.w, acc[3]);
-              acc[4] = fmaf(w, x1.x, acc[4]);
-              acc[5] = fmaf(w, x1.y, acc[5]);
-              acc[6] = fmaf(w, x1.z, acc[6]);
-              acc[7] = fmaf(w, x1.w, acc[7]);
-            }
-            uint4 u;
-            u.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-            u.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-            u.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-            u.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-            *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow + c0) = u;
-          }
-        }
-        if (threadIdx.x == 64) a.cnt[tile] = 0;
-      }
+      ml[r] = make_float2(have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
     }
     ptx::tc_fence_before();
+  }
+  __syncwarp();
+  if (a.splits > 1) {
+    // The KV splits of this row tile form one thread-block cluster.  After every CTA has
+    // parked its partial, CTA `split` merges rows [split*R, split*R + R) by reading all
+    // peers' partials through distributed shared memory, then nobody leaves before every
+    // peer has finished reading.
+    ptx::cluster_sync();
+    if (warp >= 2) {
+      const int S = a.splits;
+      const int t = threadIdx.x - 64;
+      const int R = (kRows + S - 1) / S;
+      const int r0 = split * R, r1 = min(kRows, r0 + R);
+      const int nrows = r1 - r0;
+      const uint32_t part_local = ptx::smem_addr(sKV);
+      const uint32_t ml_local = ptx::smem_addr(sKV + D * kRows * 4);
+      for (int item = t; item < nrows * (D / 16); item += 128) {
+        const int rr = r0 + item % nrows;
+        const int chunk = item / nrows;
+        const int gg = rr / a.NT, ii = i0 + rr % a.NT;
+        if (gg >= a.G || ii >= a.N || rr >= rows_used) continue;
+        float ms[8], ls[8], w[8];
+        float M = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+          if (s2 < S) {
+            const uint32_t ra = ptx::map_cluster(ml_local + rr * 8, s2);
+            ms[s2] = ptx::ld_cluster_f32(ra);
+            ls[s2] = ptx::ld_cluster_f32(ra + 4);
+            M = fmaxf(M, ms[s2]);
+          }
+        }
+        float L = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+          w[s2] = (s2 < S && ms[s2] != -INFINITY) ? exp2f(ms[s2] - M) : 0.f;
+          if (s2 < S) L += ls[s2] * w[s2];
+        }
+        float acc[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+          if (s2 < S && w[s2] > 0.f) {
+            const uint32_t base = ptx::map_cluster(part_local, s2) + (uint32_t)((chunk * 16 * kRows + rr) * 4);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc[k] = fmaf(w[s2], ptx::ld_cluster_f32(base + k * kRows * 4), acc[k]);
+          }
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const size_t o2 = (((size_t)b * a.Hq + hk * a.G + gg) * a.N + ii) * D + chunk * 16;
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + o2);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          uint4 u;
+          u.x = pack_bf16x2(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
+          u.y = pack_bf16x2(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
+          u.z = pack_bf16x2(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
+          u.w = pack_bf16x2(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
+          dst[k] = u;
+        }
+      }
+    }
+    __syncwarp();
+    ptx::cluster_sync();
   }
   __syncthreads();
   if (warp == 1) {
@@ -499,7 +512,7 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) 
   // per split, and no more partial traffic than needed
   int best = 1;
   double best_eff = 0.0;
-  const int smax = std::max(1, std::min(32, t_all / 4));
+  const int smax = std::max(1, std::min(kMaxSplits, t_all / 4));
   for (int s = 1; s <= smax; ++s) {
     const long long ctas = base * s;
     const long long waves = (ctas + 151) / 152;
@@ -510,17 +523,7 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) 
     }
   }
   p.splits = best;
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    size_t o = off;
-    off += (bytes + 255) / 256 * 256;
-    return o;
-  };
-  const size_t slots = (size_t)base * p.splits;
-  p.ws_cnt = take((size_t)base * 4);
-  p.ws_ml = p.splits > 1 ? take(slots * kRows * sizeof(float2)) : 0;
-  p.ws_part = p.splits > 1 ? take(slots * kRows * D * sizeof(float)) : 0;
-  p.total = off;
+  p.total = 0;  // split partials live in the cluster's shared memory
   return p;
 }
 
@@ -530,8 +533,20 @@ static cudaError_t launch_tc_d(const CUtensorMap& mq, const CUtensorMap& mk, con
   using C = TcCfg<D>;
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.MT * a.splits, Hkv, B);
-  attn_tc_kernel<D><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.MT * a.splits, Hkv, B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)a.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, mq, mk, mv, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -555,9 +570,6 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* ou
   a.MT = plan.mtiles;
   a.splits = plan.splits;
   a.c = scale * kLog2e;
-  a.part = plan.splits > 1 ? reinterpret_cast<float*>(ws + plan.ws_part) : nullptr;
-  a.ml = plan.splits > 1 ? reinterpret_cast<float2*>(ws + plan.ws_ml) : nullptr;
-  a.cnt = reinterpret_cast<unsigned*>(ws + plan.ws_cnt);
   a.dev_status = dev_status;
   if (D == 64) return launch_tc_d<64>(mq, mk, mv, a, B, Hkv, stream);
   return launch_tc_d<128>(mq, mk, mv, a, B, Hkv, stream);

@@ -7,24 +7,26 @@
 // Edge score := the child's marginal; s is built with correctly rounded fp32 multiplies
 // from the root down, so the result is reproducible bit for bit.
 //
-// The first budget-1 candidates in the order (s desc, depth asc, rank path asc) are
-// found by best-first search over the first-child / next-sibling form of the candidate
-// tree, which is heap-ordered in that order.  One warp per sequence: the frontier lives
-// in shared memory; every pop is a warp-wide arg-min over the frontier keys.
+// Result: the first M = budget-1 candidates in the order (s desc, depth asc, rank path
+// lexicographic asc), numbered in that order.  One CTA per sequence:
+//   1. a lower bound tau on the M-th best score: the M-th best score among the
+//      "one-deviation" candidates (prefixes of the all-rank-0 path with at most one
+//      position replaced by a higher rank) - they are real candidates, so at least M
+//      candidates reach tau;
+//   2. expand the candidate tree level by level keeping every node with s >= tau (scores
+//      never grow along a path, so this set is prefix-closed and contains the answer);
+//   3. bitonic sort of that set in the selection order; keep the first M.
+// If the expanded set outgrows shared memory, tau is raised to the M-th best score
+// already found and the expansion is retried once; after that the kernel falls back to
+// an exact best-first search by one warp (first-child / next-sibling form of the
+// candidate tree, heap-ordered in the selection order).
 #include "tv_kernels.cuh"
 
 namespace tv {
 
-// Frontier key, compared lexicographically (k0, k1, k2) ascending:
-//   k0 = (~bits(s)) << 32 | depth      (s >= 0, so larger s -> smaller key)
-//   k1, k2 = rank path, one byte per level, level 0 in the top byte of k1
-struct FrontierSmem {
-  uint64_t* k0;
-  uint64_t* k1;
-  uint64_t* k2;
-  int* par;
-  float* psc;
-};
+constexpr int kSelThreads = 1024;
+constexpr int kSelCap = 4096;      // candidates held during the expansion
+constexpr int kSelDevRanks = 32;   // ranks 1..31 enumerated in the one-deviation family
 
 __device__ __forceinline__ bool key_less(uint64_t a0, uint64_t a1, uint64_t a2, uint64_t b0, uint64_t b1,
                                          uint64_t b2) {
@@ -33,64 +35,44 @@ __device__ __forceinline__ bool key_less(uint64_t a0, uint64_t a1, uint64_t a2, 
   return a2 < b2;
 }
 
+// Rank path packed one byte per level, level 0 in the top byte of k1, level 8 in k2.
 __device__ __forceinline__ int path_rank(uint64_t k1, uint64_t k2, int level) {
   return level < 8 ? (int)((k1 >> (8 * (7 - level))) & 0xFF) : (int)((k2 >> (8 * (15 - level))) & 0xFF);
 }
-
+__device__ __forceinline__ void path_set(uint64_t& k1, uint64_t& k2, int level, int r) {
+  if (level < 8)
+    k1 |= (uint64_t)r << (8 * (7 - level));
+  else
+    k2 |= (uint64_t)r << (8 * (15 - level));
+}
 __device__ __forceinline__ void path_bump(uint64_t& k1, uint64_t& k2, int level) {
   if (level < 8)
     k1 += 1ull << (8 * (7 - level));
   else
     k2 += 1ull << (8 * (15 - level));
 }
-
+// k0 = (~bits(s)) << 32 | depth: larger s (s >= 0) gives a smaller key
 __device__ __forceinline__ uint64_t make_k0(float s, int depth) {
   return ((uint64_t)(~__float_as_uint(s)) << 32) | (uint32_t)depth;
 }
+__device__ __forceinline__ float k0_score(uint64_t k0) { return __uint_as_float(~(uint32_t)(k0 >> 32)); }
 
-__global__ void __launch_bounds__(32) select_kernel(const float* __restrict__ marg, const int32_t* __restrict__ ptok,
-                                                    int d, int K, int budget, const int32_t* __restrict__ root_token,
-                                                    int32_t* out_parent, int32_t* out_tok, int32_t* out_depth,
-                                                    float* out_score, int32_t* n_nodes, int32_t* dev_status) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int b = blockIdx.x, lane = threadIdx.x;
+// ------------------------------------------------------------------------------------
+// exact best-first search by one warp (fallback)
+
+__device__ int select_heap_warp(const float* sm_marg, const int* sm_tok, int d, int K, int budget,
+                                unsigned char* work, int32_t* o_par, int32_t* o_tok, int32_t* o_dep, float* o_sc) {
+  const int lane = threadIdx.x & 31;
   const int cap = budget;  // frontier never exceeds 1 + pops <= budget
-  uint64_t* k0 = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* k0 = reinterpret_cast<uint64_t*>(work);
   uint64_t* k1 = k0 + cap;
   uint64_t* k2 = k1 + cap;
-  float* sm_marg = reinterpret_cast<float*>(k2 + cap);
-  int* sm_tok = reinterpret_cast<int*>(sm_marg + d * K);
-  int* par = sm_tok + d * K;
+  int* par = reinterpret_cast<int*>(k2 + cap);
   float* psc = reinterpret_cast<float*>(par + cap);
-
-  const float* mg = marg + (size_t)b * d * K;
-  const int32_t* tk = ptok + (size_t)b * d * K;
-  int bad = 0;
-  for (int i = lane; i < d * K; i += 32) {
-    const float m = mg[i];
-    sm_marg[i] = m;
-    sm_tok[i] = tk[i];
-    const bool sorted = (i % K == 0) || !(m > mg[i - 1]);
-    if (!(m >= 0.f && m <= 1.f) || !sorted) bad = 1;
-  }
-  if (__any_sync(0xffffffffu, bad) && lane == 0) set_dev_status(dev_status, TV_DEV_BAD_TOKEN);
-  __syncwarp();
-
-  int32_t* o_par = out_parent + (size_t)b * budget;
-  int32_t* o_tok = out_tok + (size_t)b * budget;
-  int32_t* o_dep = out_depth + (size_t)b * budget;
-  float* o_sc = out_score + (size_t)b * budget;
-  if (lane == 0) {
-    o_par[0] = -1;
-    o_tok[0] = root_token ? root_token[b] : -1;
-    o_dep[0] = 0;
-    o_sc[0] = 1.f;
-  }
   int F = 0;
   if (d >= 1 && K >= 1 && budget > 1) {
     if (lane == 0) {
-      const float s0 = __fmul_rn(1.f, sm_marg[0]);
-      k0[0] = make_k0(s0, 1);
+      k0[0] = make_k0(__fmul_rn(1.f, sm_marg[0]), 1);
       k1[0] = 0;
       k2[0] = 0;
       par[0] = 0;
@@ -101,7 +83,6 @@ __global__ void __launch_bounds__(32) select_kernel(const float* __restrict__ ma
   __syncwarp();
   int n = 1;
   while (F > 0 && n < budget) {
-    // warp arg-min over the frontier
     uint64_t b0 = ~0ull, b1 = ~0ull, b2 = ~0ull;
     int bi = -1;
     for (int i = lane; i < F; i += 32) {
@@ -128,7 +109,7 @@ __global__ void __launch_bounds__(32) select_kernel(const float* __restrict__ ma
     }
     if (lane == 0) {
       const int dep = (int)(b0 & 0xFFFFFFFFu);
-      const float s = __uint_as_float(~(uint32_t)(b0 >> 32));
+      const float s = k0_score(b0);
       const int p = par[bi];
       const float ps = psc[bi];
       const int r = path_rank(b1, b2, dep - 1);
@@ -136,7 +117,6 @@ __global__ void __launch_bounds__(32) select_kernel(const float* __restrict__ ma
       o_tok[n] = sm_tok[(dep - 1) * K + r];
       o_dep[n] = dep;
       o_sc[n] = s;
-      // remove the popped entry
       const int last = F - 1;
       k0[bi] = k0[last];
       k1[bi] = k1[last];
@@ -145,8 +125,7 @@ __global__ void __launch_bounds__(32) select_kernel(const float* __restrict__ ma
       psc[bi] = psc[last];
       int f = last;
       if (dep < d) {  // first child: rank 0 at the next position
-        const float sc = __fmul_rn(s, sm_marg[dep * K + 0]);
-        k0[f] = make_k0(sc, dep + 1);
+        k0[f] = make_k0(__fmul_rn(s, sm_marg[dep * K]), dep + 1);
         k1[f] = b1;
         k2[f] = b2;
         par[f] = n;
@@ -154,10 +133,9 @@ __global__ void __launch_bounds__(32) select_kernel(const float* __restrict__ ma
         ++f;
       }
       if (r + 1 < K) {  // next sibling under the same parent
-        const float ss = __fmul_rn(ps, sm_marg[(dep - 1) * K + r + 1]);
         uint64_t n1 = b1, n2 = b2;
         path_bump(n1, n2, dep - 1);
-        k0[f] = make_k0(ss, dep);
+        k0[f] = make_k0(__fmul_rn(ps, sm_marg[(dep - 1) * K + r + 1]), dep);
         k1[f] = n1;
         k2[f] = n2;
         par[f] = p;
@@ -170,17 +148,325 @@ __global__ void __launch_bounds__(32) select_kernel(const float* __restrict__ ma
     ++n;
     __syncwarp();
   }
-  for (int j = n + lane; j < budget; j += 32) {
+  return n;
+}
+
+// ------------------------------------------------------------------------------------
+// block helpers
+
+// k-th largest (1-based) of vals[0..n) by 8-bit radix select; all threads return it.
+__device__ uint32_t block_kth_largest(const uint32_t* vals, int n, int k, int* hist, int* bcast) {
+  uint32_t prefix = 0, mask = 0;
+  int want = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint32_t v = vals[i];
+      if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      // lane l owns digits 255-8l .. 248-8l (high digits first)
+      int cnt[8];
+      int tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cnt[j] = hist[255 - 8 * lane - j];
+        tot += cnt[j];
+      }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - tot;
+      const unsigned hit = __ballot_sync(0xffffffffu, excl < want && incl >= want);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        if (lane == src) {
+          int run = excl;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (run + cnt[j] >= want) {
+              bcast[0] = 255 - 8 * lane - j;
+              bcast[1] = want - run;
+              break;
+            }
+            run += cnt[j];
+          }
+        }
+      } else if (lane == 0) {  // fewer than k values: return the smallest possible
+        bcast[0] = 0;
+        bcast[1] = 1;
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)bcast[0] << shift;
+    mask |= 255u << shift;
+    want = bcast[1];
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// exclusive block scan of one int per thread; returns the exclusive prefix, *total set
+__device__ int block_excl_scan(int x, int* warp_tmp, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tmp[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int nw = blockDim.x >> 5;
+    const int v = lane < nw ? warp_tmp[lane] : 0;
+    int vi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, vi, o);
+      if (lane >= o) vi += y;
+    }
+    warp_tmp[lane] = vi - v;
+    if (lane == 31) warp_tmp[32] = vi;
+  }
+  __syncthreads();
+  const int r = warp_tmp[wid] + incl - x;
+  *total = warp_tmp[32];
+  __syncthreads();
+  return r;
+}
+
+struct SelSmem {
+  float* marg;
+  int* tok;
+  uint64_t* k0;
+  uint64_t* k1;
+  uint64_t* k2;
+  int* par;   // parent entry (-1: the root)
+  int* idx;   // sort permutation
+  int* pos;   // entry -> position in the sorted order
+};
+
+// Expand every candidate with s >= tau, level by level.  Returns the number of entries,
+// or -1 if more than kSelCap would be needed; *kept = entries written before stopping.
+__device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int* warp_tmp, int* kept) {
+  int lo = 0, hi = 0, n = 0;  // current level = entries [lo, hi); level 0 is the virtual root
+  for (int k = 1; k <= d; ++k) {
+    const int nparents = (k == 1) ? 1 : hi - lo;
+    if (nparents <= 0) break;
+    const float* mk = sm.marg + (k - 1) * K;
+    int new_n = n;
+    for (int base = 0; base < nparents; base += blockDim.x) {
+      const int pi = base + threadIdx.x;
+      int cnt = 0;
+      float ps = 1.f;
+      int pe = -1;
+      if (pi < nparents) {
+        pe = (k == 1) ? -1 : lo + pi;
+        ps = (k == 1) ? 1.f : k0_score(sm.k0[pe]);
+        while (cnt < K && __fmul_rn(ps, mk[cnt]) >= tau) ++cnt;
+      }
+      int total;
+      const int off = block_excl_scan(cnt, warp_tmp, &total);
+      if (new_n + total > kSelCap) {
+        *kept = new_n;
+        return -1;
+      }
+      if (pi < nparents) {
+        const uint64_t pk1 = (k == 1) ? 0ull : sm.k1[pe];
+        const uint64_t pk2 = (k == 1) ? 0ull : sm.k2[pe];
+        for (int j = 0; j < cnt; ++j) {
+          const int e = new_n + off + j;
+          uint64_t c1 = pk1, c2 = pk2;
+          path_set(c1, c2, k - 1, j);
+          sm.k0[e] = make_k0(__fmul_rn(ps, mk[j]), k);
+          sm.k1[e] = c1;
+          sm.k2[e] = c2;
+          sm.par[e] = pe;
+        }
+      }
+      new_n += total;
+      __syncthreads();
+    }
+    lo = n;
+    hi = new_n;
+    n = new_n;
+  }
+  return n;
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __restrict__ marg,
+                                                             const int32_t* __restrict__ ptok, int d, int K,
+                                                             int budget, const int32_t* __restrict__ root_token,
+                                                             int32_t* out_parent, int32_t* out_tok, int32_t* out_depth,
+                                                             float* out_score, int32_t* n_nodes, int32_t* dev_status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int warp_tmp[33];
+  __shared__ int hist[256];
+  __shared__ int bcast[2];
+  __shared__ int s_bad;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int M = budget - 1;
+  SelSmem sm;
+  sm.k0 = reinterpret_cast<uint64_t*>(smem);
+  sm.k1 = sm.k0 + kSelCap;
+  sm.k2 = sm.k1 + kSelCap;
+  sm.par = reinterpret_cast<int*>(sm.k2 + kSelCap);
+  sm.idx = sm.par + kSelCap;
+  sm.pos = sm.idx + kSelCap;
+  sm.marg = reinterpret_cast<float*>(sm.pos + kSelCap);
+  sm.tok = reinterpret_cast<int*>(sm.marg + d * K);
+
+  const float* mg = marg + (size_t)b * d * K;
+  const int32_t* tk = ptok + (size_t)b * d * K;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  for (int i = tid; i < d * K; i += blockDim.x) {
+    const float m = mg[i];
+    sm.marg[i] = m;
+    sm.tok[i] = tk[i];
+    const bool sorted = (i % K == 0) || !(m > mg[i - 1]);
+    if (!(m >= 0.f && m <= 1.f) || !sorted) s_bad = 1;
+  }
+  __syncthreads();
+  if (s_bad && tid == 0) set_dev_status(dev_status, TV_DEV_BAD_TOKEN);
+
+  int32_t* o_par = out_parent + (size_t)b * budget;
+  int32_t* o_tok = out_tok + (size_t)b * budget;
+  int32_t* o_dep = out_depth + (size_t)b * budget;
+  float* o_sc = out_score + (size_t)b * budget;
+  if (tid == 0) {
+    o_par[0] = -1;
+    o_tok[0] = root_token ? root_token[b] : -1;
+    o_dep[0] = 0;
+    o_sc[0] = 1.f;
+  }
+  int n_out = 1;
+  bool done = (M <= 0);
+  if (!done && M <= kSelCap / 2) {
+    // 1. tau = M-th best score among the one-deviation candidates (ranks < kSelDevRanks)
+    uint32_t* f1 = reinterpret_cast<uint32_t*>(sm.k1);  // 2 * kSelCap slots, free for now
+    const int rmax = min(K, kSelDevRanks);
+    const int ncombo = 1 + d * (rmax - 1);  // combo 0: no deviation; else (position j, rank r)
+    int nf1 = 0;
+    // counts per combo: no deviation -> d prefixes; deviation at j -> d - j prefixes
+    for (int c = tid; c < ncombo; c += blockDim.x) {
+      int j = -1, r = 0;
+      if (c > 0) {
+        j = (c - 1) / (rmax - 1);
+        r = 1 + (c - 1) % (rmax - 1);
+      }
+      // offset of this combo's prefixes: combo 0 -> 0; combo (j, r) -> d + sum_{j'<j} (rmax-1)(d-j') + (r-1)(d-j)
+      int off = 0;
+      if (c > 0) {
+        off = d;
+        for (int jj = 0; jj < j; ++jj) off += (rmax - 1) * (d - jj);
+        off += (r - 1) * (d - j);
+      }
+      float s = 1.f;
+      int w = 0;
+      for (int pos = 0; pos < d; ++pos) {
+        s = __fmul_rn(s, sm.marg[pos * K + (pos == j ? r : 0)]);
+        if (pos >= (j < 0 ? 0 : j)) {
+          const int slot = off + w++;
+          if (slot < 2 * kSelCap) f1[slot] = __float_as_uint(s);
+        }
+      }
+    }
+    {
+      int tot = d;
+      for (int jj = 0; jj < d; ++jj) tot += (rmax - 1) * (d - jj);
+      nf1 = min(tot, 2 * kSelCap);
+    }
+    __syncthreads();
+    float tau = 0.f;
+    if (nf1 >= M) tau = __uint_as_float(block_kth_largest(f1, nf1, M, hist, bcast));
+    __syncthreads();
+    // 2. expansion (one retry with a raised tau)
+    int kept = 0;
+    int n = expand_threshold(sm, d, K, tau, warp_tmp, &kept);
+    if (n < 0 && kept >= M) {
+      // raise tau to the M-th best score among the entries gathered before the overflow
+      uint32_t* sc = reinterpret_cast<uint32_t*>(sm.idx);  // idx + pos: 2 * kSelCap slots
+      for (int i = tid; i < kept; i += blockDim.x) sc[i] = __float_as_uint(k0_score(sm.k0[i]));
+      __syncthreads();
+      tau = __uint_as_float(block_kth_largest(sc, kept, M, hist, bcast));
+      __syncthreads();
+      n = expand_threshold(sm, d, K, tau, warp_tmp, &kept);
+    }
+    if (n >= 0) {
+      // 3. bitonic sort of entry indices in the selection order
+      int n2 = 1;
+      while (n2 < n) n2 <<= 1;
+      for (int i = tid; i < n2; i += blockDim.x) sm.idx[i] = i < n ? i : -1;
+      __syncthreads();
+      for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int i = tid; i < n2 / 2; i += blockDim.x) {
+            const int lo = 2 * stride * (i / stride) + (i % stride);
+            const int hi = lo + stride;
+            const bool asc = (lo & size) == 0;
+            const int a = sm.idx[lo], c = sm.idx[hi];
+            bool a_gt;  // key(a) > key(c), padding (-1) sorts last
+            if (a < 0)
+              a_gt = c >= 0;
+            else if (c < 0)
+              a_gt = false;
+            else
+              a_gt = key_less(sm.k0[c], sm.k1[c], sm.k2[c], sm.k0[a], sm.k1[a], sm.k2[a]);
+            if (a_gt == asc) {
+              sm.idx[lo] = c;
+              sm.idx[hi] = a;
+            }
+          }
+          __syncthreads();
+        }
+      }
+      const int take = min(n, M);
+      for (int i = tid; i < take; i += blockDim.x) sm.pos[sm.idx[i]] = i + 1;
+      __syncthreads();
+      for (int i = tid; i < take; i += blockDim.x) {
+        const int e = sm.idx[i];
+        const uint64_t k0 = sm.k0[e];
+        const int dep = (int)(k0 & 0xFFFFFFFFu);
+        const int r = path_rank(sm.k1[e], sm.k2[e], dep - 1);
+        o_par[i + 1] = sm.par[e] < 0 ? 0 : sm.pos[sm.par[e]];
+        o_tok[i + 1] = sm.tok[(dep - 1) * K + r];
+        o_dep[i + 1] = dep;
+        o_sc[i + 1] = k0_score(k0);
+      }
+      n_out = 1 + take;
+      done = true;
+    }
+    __syncthreads();
+  }
+  if (!done) {
+    // exact fallback: best-first search by warp 0 over the whole shared buffer
+    if (tid < 32) n_out = select_heap_warp(sm.marg, sm.tok, d, K, budget, smem, o_par, o_tok, o_dep, o_sc);
+    if (tid == 0) bcast[0] = n_out;
+    __syncthreads();
+    n_out = bcast[0];
+  }
+  for (int j = n_out + tid; j < budget; j += blockDim.x) {
     o_par[j] = -1;
     o_tok[j] = -1;
     o_dep[j] = -1;
     o_sc[j] = 0.f;
   }
-  if (lane == 0 && n_nodes) n_nodes[b] = n;
+  if (tid == 0 && n_nodes) n_nodes[b] = n_out;
 }
 
 static size_t select_smem_bytes(int d, int K, int budget) {
-  return (size_t)budget * (3 * 8 + 4 + 4) + (size_t)d * K * 8;
+  const size_t expand = (size_t)kSelCap * (3 * 8 + 3 * 4);
+  const size_t heap = (size_t)budget * (3 * 8 + 4 + 4);
+  // the heap fallback reuses the start of the buffer; marg/tok follow the expansion arrays
+  return (expand > heap ? expand : heap) + (size_t)d * K * 8;
 }
 
 size_t select_ws_bytes(int, int, int, int) { return 0; }
@@ -191,8 +477,8 @@ cudaError_t launch_select(const float* marg, const int32_t* ptok, int B, int d, 
   const size_t smem = select_smem_bytes(d, K, budget);
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  select_kernel<<<B, 32, smem, stream>>>(marg, ptok, d, K, budget, root_token, parent, tokens, depth, score,
-                                         n_nodes, dev_status);
+  select_kernel<<<B, kSelThreads, smem, stream>>>(marg, ptok, d, K, budget, root_token, parent, tokens, depth, score,
+                                                   n_nodes, dev_status);
   return cudaGetLastError();
 }
 

@@ -44,8 +44,8 @@ struct AttnPlan {
   bool tc;        // tensor-core (tcgen05) kernel
   int nt;         // nodes per 128-row tile (tc)
   int mtiles;     // row tiles per (b, kv head)
-  int splits;     // KV splits per row tile
-  size_t ws_part, ws_ml, ws_cnt, total;
+  int splits;     // KV splits per row tile (one cluster)
+  size_t total;   // workspace bytes (0: partials stay in the cluster's shared memory)
 };
 AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype);
 cudaError_t launch_attn_simt(const void* q, const void* k, const void* v, void* out, const int32_t* parent,

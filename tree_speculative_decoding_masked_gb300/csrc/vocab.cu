@@ -136,31 +136,32 @@ __device__ __forceinline__ VocabPartial block_merge(VocabPartial p, VocabPartial
   return r;
 }
 
-// Accumulate x[v0, v1) of one row into `acc` (16-byte loads when kVec).
+// Accumulate x[v0, v1) of one row into `acc`: 16-byte streaming loads, eight in flight
+// per thread, when kVec; scalar loads otherwise.
 template <typename T, bool kVec>
 __device__ __forceinline__ void scan_chunk(const T* __restrict__ row, int v0, int v1, float c2, RowAcc& acc) {
   if constexpr (kVec) {
     constexpr int kN = Vec16<T>::kN;
+    constexpr int kInFlight = 8;
     const int nvec = (v1 - v0) / kN;
     const uint4* p = reinterpret_cast<const uint4*>(row + v0);
-    int j = threadIdx.x;
     const int stride = blockDim.x;
-    for (; j + 3 * stride < nvec; j += 4 * stride) {
-      uint4 u[4];
+    for (int j = threadIdx.x; j < nvec; j += kInFlight * stride) {
+      uint4 u[kInFlight];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) u[k] = __ldcs(p + j + k * stride);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float x[kN];
-        unpack16<T>(u[k], x);
-        acc.template push<kN>(x, v0 + (j + k * stride) * kN, c2);
+      for (int k = 0; k < kInFlight; ++k) {
+        const int idx = j + k * stride;
+        if (idx < nvec) u[k] = __ldcs(p + idx);
       }
-    }
-    for (; j < nvec; j += stride) {
-      uint4 u = __ldcs(p + j);
-      float x[kN];
-      unpack16<T>(u, x);
-      acc.template push<kN>(x, v0 + j * kN, c2);
+#pragma unroll
+      for (int k = 0; k < kInFlight; ++k) {
+        const int idx = j + k * stride;
+        if (idx < nvec) {
+          float x[kN];
+          unpack16<T>(u[k], x);
+          acc.template push<kN>(x, v0 + idx * kN, c2);
+        }
+      }
     }
     for (int v = v0 + nvec * kN + threadIdx.x; v < v1; v += stride) acc.push1(to_f32(row[v]), v, c2);
   } else {
@@ -239,31 +240,34 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b) {
     if (a.q_draft) a.q_draft[(size_t)b * N + c] = qv;
   }
   if (a.sampling) return;  // the sampling walk runs in its own kernel
-  // greedy walk: one warp
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int cur = 0, len = 0, want = s_am[0];
+  // greedy walk: first find, in parallel, each node's child whose token equals the
+  // node's argmax (lowest index if several), then follow those links from the root
+  __shared__ int s_match[kMaxNodes];
+  __shared__ int s_path[kMaxNodes];
+  __shared__ int s_len, s_bonus;
+  for (int c = threadIdx.x; c < N; c += blockDim.x) s_match[c] = 0x7fffffff;
+  __syncthreads();
+  if (!bad)
+    for (int c = 1 + threadIdx.x; c < N; c += blockDim.x)
+      if (s_tok[c] == s_am[s_par[c]]) atomicMin(&s_match[s_par[c]], c);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int cur = 0, len = 0;
     if (!bad) {
-      for (;;) {
-        want = s_am[cur];
-        int found = -1;
-        for (int c0 = cur + 1; c0 < N && found < 0; c0 += 32) {
-          int c = c0 + lane;
-          bool hit = c < N && s_par[c] == cur && s_tok[c] == want;
-          unsigned m = __ballot_sync(0xffffffffu, hit);
-          if (m) found = c0 + __ffs(m) - 1;
-        }
-        if (found < 0) break;
-        if (lane == 0) a.accepted[(size_t)b * N + len] = found;
-        ++len;
-        cur = found;
+      for (int nxt = s_match[0]; nxt != 0x7fffffff; nxt = s_match[cur]) {
+        s_path[len++] = nxt;
+        cur = nxt;
       }
     }
-    for (int j = len + lane; j < N; j += 32) a.accepted[(size_t)b * N + j] = -1;
-    if (lane == 0) {
-      a.accept_len[b] = bad ? 0 : len;
-      a.bonus[b] = bad ? -1 : want;
-    }
+    s_len = len;
+    s_bonus = bad ? -1 : s_am[cur];
+  }
+  __syncthreads();
+  const int len = s_len;
+  for (int j = threadIdx.x; j < N; j += blockDim.x) a.accepted[(size_t)b * N + j] = j < len ? s_path[j] : -1;
+  if (threadIdx.x == 0) {
+    a.accept_len[b] = len;
+    a.bonus[b] = s_bonus;
   }
 }
 
@@ -298,30 +302,33 @@ __global__ void __launch_bounds__(256) vocab_pass_kernel(VocabArgs a) {
   }
   __syncthreads();
   if (!s_flag) return;
-  // last CTA of this row: merge the splits
-  if (threadIdx.x == 0) {
+  // last CTA of this row: warp 0 merges the splits (lane s takes split s, s + 32, ...)
+  if (threadIdx.x < 32) {
     __threadfence();
-    VocabPartial r{-INFINITY, 0.f, -INFINITY, 0x7fffffff}, rq = r;
-    for (int s = 0; s < a.splits; ++s) {
+    const VocabPartial none{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+    VocabPartial r = none, rq = none;
+    for (int s = threadIdx.x; s < a.splits; s += 32) {
       const VocabPartial* src = a.part + (size_t)row * a.splits + s;
-      VocabPartial x{__ldcg(&src->m), __ldcg(&src->s), __ldcg(&src->av), __ldcg(&src->ai)};
-      r = partial_merge(r, x);
+      r = partial_merge(r, {__ldcg(&src->m), __ldcg(&src->s), __ldcg(&src->av), __ldcg(&src->ai)});
       if (a.sampling) {
         const VocabPartial* sq = a.part_q + (size_t)row * a.splits + s;
-        VocabPartial y{__ldcg(&sq->m), __ldcg(&sq->s), __ldcg(&sq->av), __ldcg(&sq->ai)};
-        rq = partial_merge(rq, y);
+        rq = partial_merge(rq, {__ldcg(&sq->m), __ldcg(&sq->s), __ldcg(&sq->av), __ldcg(&sq->ai)});
       }
     }
-    float l2 = r.m + log2f(r.s);
-    a.lse2[row] = l2;
-    a.amax[row] = r.ai;
-    if (a.sampling) a.lse2_q[row] = rq.m + log2f(rq.s);
-    if (a.row_lse) a.row_lse[row] = l2 * kLn2;
-    if (a.row_argmax) a.row_argmax[row] = r.ai;
-    a.row_cnt[row] = 0;
-    __threadfence();
-    unsigned prev = atomicAdd(a.seq_cnt + b, 1u);
-    s_flag = (prev == (unsigned)(a.N - 1));
+    r = warp_merge(r);
+    if (a.sampling) rq = warp_merge(rq);
+    if (threadIdx.x == 0) {
+      const float l2 = r.m + log2f(r.s);
+      a.lse2[row] = l2;
+      a.amax[row] = r.ai;
+      if (a.sampling) a.lse2_q[row] = rq.m + log2f(rq.s);
+      if (a.row_lse) a.row_lse[row] = l2 * kLn2;
+      if (a.row_argmax) a.row_argmax[row] = r.ai;
+      a.row_cnt[row] = 0;
+      __threadfence();
+      const unsigned prev = atomicAdd(a.seq_cnt + b, 1u);
+      s_flag = (prev == (unsigned)(a.N - 1));
+    }
   }
   __syncthreads();
   if (!s_flag) return;
