@@ -109,7 +109,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x % a.MT, split = blockIdx.x / a.MT;
+  // the splits of one row tile are consecutive in x and form one cluster (rank = split)
+  const int mt = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
   const int hk = blockIdx.y, b = blockIdx.z;
   const int i0 = mt * a.NT;
   const int nodes_hi = min(a.N, i0 + a.NT);
