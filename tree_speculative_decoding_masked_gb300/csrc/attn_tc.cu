@@ -273,16 +273,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int j0 = (t_begin + t) * kBN;
       const uint64_t vis = key_mask(j0, a.P, a.N, mnode, s_par);
-      float tm = -INFINITY;
+      if (vis != ~0ull) {  // tree / tail tiles: hidden keys become -inf (exp -> 0)
 #pragma unroll
-      for (int j = 0; j < kBN; ++j)
-        if ((vis >> j) & 1ull) tm = fmaxf(tm, sv[j]);
+        for (int j = 0; j < kBN; ++j)
+          if (!((vis >> j) & 1ull)) sv[j] = -INFINITY;
+      }
+      // row max as eight independent chains, then a tree
+      float m8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8[k] = sv[k];
+#pragma unroll
+      for (int j = 8; j < kBN; j += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], sv[j + k]);
+      const float tm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float tms = tm * a.c;
       float alpha = 1.f;
       bool need = false;
       if (tms > m_run + kRescaleLog2) {
         if (m_run != -INFINITY) {
-          alpha = exp2f(m_run - tms);
+          alpha = ptx::ex2(m_run - tms);
           need = true;
         }
         m_run = tms;
@@ -312,23 +323,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P = 2^(S*c - m_run) on visible keys, bf16, 128-byte-swizzled K-major rows
       unsigned char* prow = sP + sb * C::kPBytes + r * 128;
-      float lsum = 0.f;
+      float ls8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls8[k] = 0.f;
+      const bool live = m_run != -INFINITY;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         float p[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const int j = ch * 8 + k;
-          p[k] = (((vis >> j) & 1ull) && m_run != -INFINITY) ? exp2f(fmaf(sv[j], a.c, -m_run)) : 0.f;
-          lsum += p[k];
+          p[k] = live ? ptx::ex2(fmaf(sv[ch * 8 + k], a.c, -m_run)) : 0.f;
+          ls8[k] += p[k];
         }
         uint4 u;
-        u.x = pack_bf16x2(p[0], p[1]);
-        u.y = pack_bf16x2(p[2], p[3]);
-        u.z = pack_bf16x2(p[4], p[5]);
-        u.w = pack_bf16x2(p[6], p[7]);
+        u.x = ptx::cvt_bf16x2(p[0], p[1]);
+        u.y = ptx::cvt_bf16x2(p[2], p[3]);
+        u.z = ptx::cvt_bf16x2(p[4], p[5]);
+        u.w = ptx::cvt_bf16x2(p[6], p[7]);
         *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = u;
       }
+      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       l_run += lsum;
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
@@ -362,18 +376,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             uint4 u;
-            u.x = pack_bf16x2(ov[8 * k + 0] * inv, ov[8 * k + 1] * inv);
-            u.y = pack_bf16x2(ov[8 * k + 2] * inv, ov[8 * k + 3] * inv);
-            u.z = pack_bf16x2(ov[8 * k + 4] * inv, ov[8 * k + 5] * inv);
-            u.w = pack_bf16x2(ov[8 * k + 6] * inv, ov[8 * k + 7] * inv);
+            u.x = ptx::cvt_bf16x2(ov[8 * k + 0] * inv, ov[8 * k + 1] * inv);
+            u.y = ptx::cvt_bf16x2(ov[8 * k + 2] * inv, ov[8 * k + 3] * inv);
+            u.z = ptx::cvt_bf16x2(ov[8 * k + 4] * inv, ov[8 * k + 5] * inv);
+            u.w = ptx::cvt_bf16x2(ov[8 * k + 6] * inv, ov[8 * k + 7] * inv);
             dst[k] = u;
           }
         }
       }
     } else {
-      // park this split's unnormalised O (column-major [D][128], conflict-free) and its
-      // (m, l) in the drained K/V ring for the cluster merge below
-      float* part = reinterpret_cast<float*>(sKV);
+      // park this split's unnormalised O as row-major [128][D] fp32 with the 16-byte chunks
+      // of row r XOR-swizzled by (r & 7) (conflict-free 16-byte stores), plus (m, l), in
+      // the drained K/V ring for the cluster merge below
+      unsigned char* part = sKV;
       float2* ml = reinterpret_cast<float2*>(sKV + D * kRows * 4);
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -386,7 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 32; ++k) ov[k] = 0.f;
         }
 #pragma unroll
-        for (int k = 0; k < 32; ++k) part[(c0 + k) * kRows + r] = ov[k];
+        for (int k = 0; k < 8; ++k) {
+          const int chunk = c0 / 4 + k;
+          *reinterpret_cast<float4*>(part + r * D * 4 + ((chunk ^ (r & 7)) << 4)) =
+              make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+        }
       }
       ml[r] = make_float2(have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
     }
@@ -399,57 +418,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     // peers' partials through distributed shared memory, then nobody leaves before every
     // peer has finished reading.
     ptx::cluster_sync();
-    if (warp >= 2) {
+    {
+      // all 192 threads: item = (row of this CTA's slice, group of 16 columns)
       const int S = a.splits;
-      const int t = threadIdx.x - 64;
       const int R = (kRows + S - 1) / S;
       const int r0 = split * R, r1 = min(kRows, r0 + R);
-      const int nrows = r1 - r0;
+      const int nrows = max(0, r1 - r0);
       const uint32_t part_local = ptx::smem_addr(sKV);
       const uint32_t ml_local = ptx::smem_addr(sKV + D * kRows * 4);
-      for (int item = t; item < nrows * (D / 16); item += 128) {
+      for (int item = threadIdx.x; item < nrows * (D / 16); item += kThreads) {
         const int rr = r0 + item % nrows;
-        const int chunk = item / nrows;
+        const int grp = item / nrows;  // columns [16 grp, 16 grp + 16) = chunks 4 grp .. 4 grp + 3
         const int gg = rr / a.NT, ii = i0 + rr % a.NT;
         if (gg >= a.G || ii >= a.N || rr >= rows_used) continue;
-        float ms[8], ls[8], w[8];
+        float2 mlv[8];
         float M = -INFINITY;
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2) {
           if (s2 < S) {
-            const uint32_t ra = ptx::map_cluster(ml_local + rr * 8, s2);
-            ms[s2] = ptx::ld_cluster_f32(ra);
-            ls[s2] = ptx::ld_cluster_f32(ra + 4);
-            M = fmaxf(M, ms[s2]);
+            mlv[s2] = ptx::ld_cluster_f32x2(ptx::map_cluster(ml_local + rr * 8, s2));
+            M = fmaxf(M, mlv[s2].x);
           }
         }
         float L = 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < 8; ++s2) {
-          w[s2] = (s2 < S && ms[s2] != -INFINITY) ? exp2f(ms[s2] - M) : 0.f;
-          if (s2 < S) L += ls[s2] * w[s2];
-        }
         float acc[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) acc[k] = 0.f;
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2) {
-          if (s2 < S && w[s2] > 0.f) {
-            const uint32_t base = ptx::map_cluster(part_local, s2) + (uint32_t)((chunk * 16 * kRows + rr) * 4);
+          if (s2 < S && mlv[s2].x != -INFINITY) {
+            const float w = ptx::ex2(mlv[s2].x - M);
+            L = fmaf(mlv[s2].y, w, L);
+            const uint32_t rowb = ptx::map_cluster(part_local, s2) + (uint32_t)(rr * D * 4);
+            float4 x[4];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) acc[k] = fmaf(w[s2], ptx::ld_cluster_f32(base + k * kRows * 4), acc[k]);
+            for (int q = 0; q < 4; ++q) x[q] = ptx::ld_cluster_f32x4(rowb + (((4 * grp + q) ^ (rr & 7)) << 4));
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[4 * q + 0] = fmaf(w, x[q].x, acc[4 * q + 0]);
+              acc[4 * q + 1] = fmaf(w, x[q].y, acc[4 * q + 1]);
+              acc[4 * q + 2] = fmaf(w, x[q].z, acc[4 * q + 2]);
+              acc[4 * q + 3] = fmaf(w, x[q].w, acc[4 * q + 3]);
+            }
           }
         }
         const float inv = L > 0.f ? 1.f / L : 0.f;
-        const size_t o2 = (((size_t)b * a.Hq + hk * a.G + gg) * a.N + ii) * D + chunk * 16;
+        const size_t o2 = (((size_t)b * a.Hq + hk * a.G + gg) * a.N + ii) * D + grp * 16;
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + o2);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           uint4 u;
-          u.x = pack_bf16x2(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
-          u.y = pack_bf16x2(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
-          u.z = pack_bf16x2(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
-          u.w = pack_bf16x2(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
+          u.x = ptx::cvt_bf16x2(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
+          u.y = ptx::cvt_bf16x2(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
+          u.z = ptx::cvt_bf16x2(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
+          u.w = ptx::cvt_bf16x2(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
           dst[k] = u;
         }
       }
@@ -507,25 +529,64 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) 
   if (!p.tc) return p;
   p.nt = (kRows / G) / 8 * 8;
   p.mtiles = (N + p.nt - 1) / p.nt;
-  const long long base = (long long)B * Hkv * p.mtiles;
-  const int t_all = (P + N + kBN - 1) / kBN;
-  // pick the split count that fills 152 SMs (one CTA each) best; at least 4 KV tiles
-  // per split, and no more partial traffic than needed
+  p.splits = 1;  // chosen at launch from the device's cluster occupancy
+  p.total = 0;   // split partials stay in the cluster's shared memory
+  return p;
+}
+
+// How many clusters of `s` CTAs of attn_tc_kernel<D> can be resident at once on the
+// current device (cached per device, D and s).
+template <int D>
+static int max_active_clusters(int s) {
+  static int cache[64][kMaxSplits + 1];
+  static bool init = false;
+  if (!init) {
+    for (auto& row : cache)
+      for (int& v : row) v = -1;
+    init = true;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev][s] >= 0) return cache[dev][s];
+  using C = TcCfg<D>;
+  int n = 0;
+  if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(s * 64, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemAlloc;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)s;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<D>, &cfg) != cudaSuccess) n = 0;
+  }
+  cache[dev][s] = n;
+  return n;
+}
+
+// KV splits per row tile: minimise (waves of clusters) x (KV tiles per CTA + a fixed
+// per-CTA cost for set-up and the cluster merge), counted in 64-key tiles.
+template <int D>
+static int choose_splits(long long row_tiles, int t_all) {
+  constexpr double kFixedTiles = 3.0;
   int best = 1;
-  double best_eff = 0.0;
-  const int smax = std::max(1, std::min(kMaxSplits, t_all / 4));
-  for (int s = 1; s <= smax; ++s) {
-    const long long ctas = base * s;
-    const long long waves = (ctas + 151) / 152;
-    const double eff = (double)ctas / (double)(waves * 152);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
+  double best_cost = 1e300;
+  for (int s = 1; s <= kMaxSplits && s <= t_all; ++s) {
+    const int act = max_active_clusters<D>(s);
+    if (act <= 0) continue;
+    const long long waves = (row_tiles + act - 1) / act;
+    const double cost = (double)waves * ((t_all + s - 1) / s + kFixedTiles);
+    if (cost < best_cost * 0.98) {
+      best_cost = cost;
       best = s;
     }
   }
-  p.splits = best;
-  p.total = 0;  // split partials live in the cluster's shared memory
-  return p;
+  return best;
 }
 
 template <int D>
@@ -569,9 +630,11 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* ou
   a.G = Hq / Hkv;
   a.NT = plan.nt;
   a.MT = plan.mtiles;
-  a.splits = plan.splits;
   a.c = scale * kLog2e;
   a.dev_status = dev_status;
+  const long long row_tiles = (long long)B * Hkv * plan.mtiles;
+  const int t_all = (P + N + kBN - 1) / kBN;
+  a.splits = D == 64 ? choose_splits<64>(row_tiles, t_all) : choose_splits<128>(row_tiles, t_all);
   if (D == 64) return launch_tc_d<64>(mq, mk, mv, a, B, Hkv, stream);
   return launch_tc_d<128>(mq, mk, mv, a, B, Hkv, stream);
 }

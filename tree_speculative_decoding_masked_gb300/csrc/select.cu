@@ -24,7 +24,7 @@
 
 namespace tv {
 
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 256;
 constexpr int kSelCap = 4096;      // candidates held during the expansion
 constexpr int kSelDevRanks = 32;   // ranks 1..31 enumerated in the one-deviation family
 
@@ -152,27 +152,72 @@ __device__ int select_heap_warp(const float* sm_marg, const int* sm_tok, int d, 
 }
 
 // ------------------------------------------------------------------------------------
-// block helpers
+// group-parallel helpers: a "group" is either warp 0 alone (kG = 32, __syncwarp) or the
+// whole block (kG = kSelThreads, __syncthreads); thread rank = threadIdx.x.
 
-// k-th largest (1-based) of vals[0..n) by 8-bit radix select; all threads return it.
-__device__ uint32_t block_kth_largest(const uint32_t* vals, int n, int k, int* hist, int* bcast) {
+template <int kG>
+__device__ __forceinline__ void gsync() {
+  if constexpr (kG == 32)
+    __syncwarp();
+  else
+    __syncthreads();
+}
+
+// exclusive scan of one int per group thread; *total = the sum
+template <int kG>
+__device__ int group_excl_scan(int x, int* warp_tmp, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if constexpr (kG == 32) {
+    *total = __shfl_sync(0xffffffffu, incl, 31);
+    return incl - x;
+  } else {
+    if (lane == 31) warp_tmp[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      const int v = lane < kG / 32 ? warp_tmp[lane] : 0;
+      int vi = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, vi, o);
+        if (lane >= o) vi += y;
+      }
+      warp_tmp[lane] = vi - v;
+      if (lane == 31) warp_tmp[32] = vi;
+    }
+    __syncthreads();
+    const int r = warp_tmp[wid] + incl - x;
+    *total = warp_tmp[32];
+    __syncthreads();
+    return r;
+  }
+}
+
+// k-th largest (1-based) of vals[0..n) by 8-bit radix select (k <= n); all group threads
+// return it.  The digit search runs in warp 0, which belongs to every group.
+template <int kG>
+__device__ uint32_t group_kth_largest(const uint32_t* vals, int n, int k, int* hist, int* bcast) {
   uint32_t prefix = 0, mask = 0;
   int want = k;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    for (int i = threadIdx.x; i < 256; i += kG) hist[i] = 0;
+    gsync<kG>();
+    for (int i = threadIdx.x; i < n; i += kG) {
       const uint32_t v = vals[i];
       if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1);
     }
-    __syncthreads();
+    gsync<kG>();
     if (threadIdx.x < 32) {
       const int lane = threadIdx.x;
-      // lane l owns digits 255-8l .. 248-8l (high digits first)
       int cnt[8];
       int tot = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 8; ++j) {  // lane l owns digits 255-8l .. 248-8l
         cnt[j] = hist[255 - 8 * lane - j];
         tot += cnt[j];
       }
@@ -184,62 +229,32 @@ __device__ uint32_t block_kth_largest(const uint32_t* vals, int n, int k, int* h
       }
       const int excl = incl - tot;
       const unsigned hit = __ballot_sync(0xffffffffu, excl < want && incl >= want);
-      if (hit) {
-        const int src = __ffs(hit) - 1;
-        if (lane == src) {
+      const int src = hit ? __ffs(hit) - 1 : 0;
+      if (lane == src) {
+        int dig = 0, rest = 1;
+        if (hit) {
           int run = excl;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             if (run + cnt[j] >= want) {
-              bcast[0] = 255 - 8 * lane - j;
-              bcast[1] = want - run;
+              dig = 255 - 8 * lane - j;
+              rest = want - run;
               break;
             }
             run += cnt[j];
           }
         }
-      } else if (lane == 0) {  // fewer than k values: return the smallest possible
-        bcast[0] = 0;
-        bcast[1] = 1;
+        bcast[0] = dig;
+        bcast[1] = rest;
       }
     }
-    __syncthreads();
+    gsync<kG>();
     prefix |= (uint32_t)bcast[0] << shift;
     mask |= 255u << shift;
     want = bcast[1];
-    __syncthreads();
+    gsync<kG>();
   }
   return prefix;
-}
-
-// exclusive block scan of one int per thread; returns the exclusive prefix, *total set
-__device__ int block_excl_scan(int x, int* warp_tmp, int* total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int incl = x;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tmp[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    const int nw = blockDim.x >> 5;
-    const int v = lane < nw ? warp_tmp[lane] : 0;
-    int vi = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, vi, o);
-      if (lane >= o) vi += y;
-    }
-    warp_tmp[lane] = vi - v;
-    if (lane == 31) warp_tmp[32] = vi;
-  }
-  __syncthreads();
-  const int r = warp_tmp[wid] + incl - x;
-  *total = warp_tmp[32];
-  __syncthreads();
-  return r;
 }
 
 struct SelSmem {
@@ -253,17 +268,18 @@ struct SelSmem {
   int* pos;   // entry -> position in the sorted order
 };
 
-// Expand every candidate with s >= tau, level by level.  Returns the number of entries,
-// or -1 if more than kSelCap would be needed; *kept = entries written before stopping.
-__device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int* warp_tmp, int* kept) {
+// Expand every candidate with s >= tau, level by level, into at most `cap` entries.
+// Returns the count, or -1 on overflow (*kept = entries written before stopping).
+template <int kG>
+__device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int cap, int* warp_tmp, int* kept) {
   int lo = 0, hi = 0, n = 0;  // current level = entries [lo, hi); level 0 is the virtual root
   for (int k = 1; k <= d; ++k) {
     const int nparents = (k == 1) ? 1 : hi - lo;
     if (nparents <= 0) break;
     const float* mk = sm.marg + (k - 1) * K;
     int new_n = n;
-    for (int base = 0; base < nparents; base += blockDim.x) {
-      const int pi = base + threadIdx.x;
+    for (int base = 0; base < nparents; base += kG) {
+      const int pi = base + (int)threadIdx.x;
       int cnt = 0;
       float ps = 1.f;
       int pe = -1;
@@ -273,8 +289,8 @@ __device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int*
         while (cnt < K && __fmul_rn(ps, mk[cnt]) >= tau) ++cnt;
       }
       int total;
-      const int off = block_excl_scan(cnt, warp_tmp, &total);
-      if (new_n + total > kSelCap) {
+      const int off = group_excl_scan<kG>(cnt, warp_tmp, &total);
+      if (new_n + total > cap) {
         *kept = new_n;
         return -1;
       }
@@ -292,7 +308,7 @@ __device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int*
         }
       }
       new_n += total;
-      __syncthreads();
+      gsync<kG>();
     }
     lo = n;
     hi = new_n;
@@ -300,6 +316,119 @@ __device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int*
   }
   return n;
 }
+
+// bitonic sort of sm.idx[0..n2) (entries, -1 = padding last) in the selection order
+template <int kG>
+__device__ void bitonic_sort_idx(const SelSmem& sm, int n2) {
+  for (int size = 2; size <= n2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n2 / 2; i += kG) {
+        const int lo = 2 * stride * (i / stride) + (i % stride);
+        const int hi = lo + stride;
+        const bool asc = (lo & size) == 0;
+        const int a = sm.idx[lo], c = sm.idx[hi];
+        bool a_gt;
+        if (a < 0)
+          a_gt = c >= 0;
+        else if (c < 0)
+          a_gt = false;
+        else
+          a_gt = key_less(sm.k0[c], sm.k1[c], sm.k2[c], sm.k0[a], sm.k1[a], sm.k2[a]);
+        if (a_gt == asc) {
+          sm.idx[lo] = c;
+          sm.idx[hi] = a;
+        }
+      }
+      gsync<kG>();
+    }
+  }
+}
+
+// Threshold selection by a group.  Returns 1 + number selected, or -1 if the candidate
+// set did not fit (caller falls back).  `sort_cap` bounds the tie group that is sorted.
+template <int kG>
+__device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int cap, int sort_cap, int* warp_tmp,
+                                int* hist, int* bcast, int32_t* o_par, int32_t* o_tok, int32_t* o_dep, float* o_sc) {
+  const int t = threadIdx.x;
+  // 1. tau = M-th best score among the one-deviation candidates (ranks < kSelDevRanks)
+  uint32_t* f1 = reinterpret_cast<uint32_t*>(sm.k1);  // 2 * kSelCap slots, free for now
+  const int rmax = min(K, kSelDevRanks);
+  const int ncombo = 1 + d * (rmax - 1);  // combo 0: no deviation; else (position j, rank r)
+  for (int c = t; c < ncombo; c += kG) {
+    int j = -1, r = 0, off = 0;
+    if (c > 0) {
+      j = (c - 1) / (rmax - 1);
+      r = 1 + (c - 1) % (rmax - 1);
+      // no deviation: d prefixes; deviation at j: d - j prefixes
+      off = d + (rmax - 1) * (j * d - j * (j - 1) / 2) + (r - 1) * (d - j);
+    }
+    float s = 1.f;
+    int w = 0;
+    for (int p = 0; p < d; ++p) {
+      s = __fmul_rn(s, sm.marg[p * K + (p == j ? r : 0)]);
+      if (p >= (j < 0 ? 0 : j)) {
+        const int slot = off + w++;
+        if (slot < 2 * kSelCap) f1[slot] = __float_as_uint(s);
+      }
+    }
+  }
+  const int nf1 = min(d + (rmax - 1) * (d * (d + 1) / 2), 2 * kSelCap);
+  gsync<kG>();
+  float tau = 0.f;
+  if (nf1 >= M) tau = __uint_as_float(group_kth_largest<kG>(f1, nf1, M, hist, bcast));
+  gsync<kG>();
+  // 2. expansion, one retry with tau raised to the M-th best entry found so far
+  int kept = 0;
+  int n = expand_threshold<kG>(sm, d, K, tau, cap, warp_tmp, &kept);
+  if (n < 0 && kept >= M) {
+    uint32_t* sc = reinterpret_cast<uint32_t*>(sm.idx);  // idx + pos: 2 * kSelCap slots
+    for (int i = t; i < kept; i += kG) sc[i] = __float_as_uint(k0_score(sm.k0[i]));
+    gsync<kG>();
+    tau = __uint_as_float(group_kth_largest<kG>(sc, kept, M, hist, bcast));
+    gsync<kG>();
+    n = expand_threshold<kG>(sm, d, K, tau, cap, warp_tmp, &kept);
+  }
+  if (n < 0) return -1;
+  const int take = min(n, M);
+  // 3. the M-th best score T; only entries with s >= T can be taken: sort just those
+  uint32_t* sc = reinterpret_cast<uint32_t*>(sm.pos);
+  for (int i = t; i < n; i += kG) sc[i] = __float_as_uint(k0_score(sm.k0[i]));
+  gsync<kG>();
+  const uint32_t T = take > 0 ? group_kth_largest<kG>(sc, n, take, hist, bcast) : 0u;
+  int cnt_ge = 0;
+  for (int base = 0; base < n; base += kG) {
+    const int i = base + t;
+    const int f = (i < n && sc[i] >= T) ? 1 : 0;
+    int total;
+    const int off = group_excl_scan<kG>(f, warp_tmp, &total);
+    if (f) sm.idx[cnt_ge + off] = i;
+    cnt_ge += total;
+    gsync<kG>();
+  }
+  if (cnt_ge > sort_cap) return -1;
+  int n2 = 1;
+  while (n2 < cnt_ge) n2 <<= 1;
+  for (int i = cnt_ge + t; i < n2; i += kG) sm.idx[i] = -1;
+  gsync<kG>();
+  bitonic_sort_idx<kG>(sm, n2);
+  for (int i = t; i < take; i += kG) sm.pos[sm.idx[i]] = i + 1;
+  gsync<kG>();
+  for (int i = t; i < take; i += kG) {
+    const int e = sm.idx[i];
+    const uint64_t k0 = sm.k0[e];
+    const int dep = (int)(k0 & 0xFFFFFFFFu);
+    const int r = path_rank(sm.k1[e], sm.k2[e], dep - 1);
+    o_par[i + 1] = sm.par[e] < 0 ? 0 : sm.pos[sm.par[e]];
+    o_tok[i + 1] = sm.tok[(dep - 1) * K + r];
+    o_dep[i + 1] = dep;
+    o_sc[i + 1] = k0_score(k0);
+  }
+  gsync<kG>();
+  return 1 + take;
+}
+
+constexpr int kWarpPathMaxM = 127;  // budgets up to 128 rows try the single-warp path
+constexpr int kWarpPathCap = 1024;
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __restrict__ marg,
                                                              const int32_t* __restrict__ ptok, int d, int K,
@@ -310,7 +439,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
   __shared__ int warp_tmp[33];
   __shared__ int hist[256];
   __shared__ int bcast[2];
-  __shared__ int s_bad;
+  __shared__ int s_bad, s_nout;
   const int b = blockIdx.x, tid = threadIdx.x;
   const int M = budget - 1;
   SelSmem sm;
@@ -325,7 +454,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
 
   const float* mg = marg + (size_t)b * d * K;
   const int32_t* tk = ptok + (size_t)b * d * K;
-  if (tid == 0) s_bad = 0;
+  if (tid == 0) {
+    s_bad = 0;
+    s_nout = -1;
+  }
   __syncthreads();
   for (int i = tid; i < d * K; i += blockDim.x) {
     const float m = mg[i];
@@ -347,112 +479,32 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
     o_dep[0] = 0;
     o_sc[0] = 1.f;
   }
-  int n_out = 1;
-  bool done = (M <= 0);
-  if (!done && M <= kSelCap / 2) {
-    // 1. tau = M-th best score among the one-deviation candidates (ranks < kSelDevRanks)
-    uint32_t* f1 = reinterpret_cast<uint32_t*>(sm.k1);  // 2 * kSelCap slots, free for now
-    const int rmax = min(K, kSelDevRanks);
-    const int ncombo = 1 + d * (rmax - 1);  // combo 0: no deviation; else (position j, rank r)
-    int nf1 = 0;
-    // counts per combo: no deviation -> d prefixes; deviation at j -> d - j prefixes
-    for (int c = tid; c < ncombo; c += blockDim.x) {
-      int j = -1, r = 0;
-      if (c > 0) {
-        j = (c - 1) / (rmax - 1);
-        r = 1 + (c - 1) % (rmax - 1);
-      }
-      // offset of this combo's prefixes: combo 0 -> 0; combo (j, r) -> d + sum_{j'<j} (rmax-1)(d-j') + (r-1)(d-j)
-      int off = 0;
-      if (c > 0) {
-        off = d;
-        for (int jj = 0; jj < j; ++jj) off += (rmax - 1) * (d - jj);
-        off += (r - 1) * (d - j);
-      }
-      float s = 1.f;
-      int w = 0;
-      for (int pos = 0; pos < d; ++pos) {
-        s = __fmul_rn(s, sm.marg[pos * K + (pos == j ? r : 0)]);
-        if (pos >= (j < 0 ? 0 : j)) {
-          const int slot = off + w++;
-          if (slot < 2 * kSelCap) f1[slot] = __float_as_uint(s);
-        }
-      }
+  if (M <= 0) {
+    if (tid == 0) s_nout = 1;
+  } else if (M <= kWarpPathMaxM) {
+    // small budgets: one warp, no block-wide barriers
+    if (tid < 32) {
+      const int r = select_threshold<32>(sm, d, K, M, kWarpPathCap, 128, warp_tmp, hist, bcast, o_par, o_tok,
+                                         o_dep, o_sc);
+      if (tid == 0) s_nout = r;
     }
-    {
-      int tot = d;
-      for (int jj = 0; jj < d; ++jj) tot += (rmax - 1) * (d - jj);
-      nf1 = min(tot, 2 * kSelCap);
-    }
-    __syncthreads();
-    float tau = 0.f;
-    if (nf1 >= M) tau = __uint_as_float(block_kth_largest(f1, nf1, M, hist, bcast));
-    __syncthreads();
-    // 2. expansion (one retry with a raised tau)
-    int kept = 0;
-    int n = expand_threshold(sm, d, K, tau, warp_tmp, &kept);
-    if (n < 0 && kept >= M) {
-      // raise tau to the M-th best score among the entries gathered before the overflow
-      uint32_t* sc = reinterpret_cast<uint32_t*>(sm.idx);  // idx + pos: 2 * kSelCap slots
-      for (int i = tid; i < kept; i += blockDim.x) sc[i] = __float_as_uint(k0_score(sm.k0[i]));
-      __syncthreads();
-      tau = __uint_as_float(block_kth_largest(sc, kept, M, hist, bcast));
-      __syncthreads();
-      n = expand_threshold(sm, d, K, tau, warp_tmp, &kept);
-    }
-    if (n >= 0) {
-      // 3. bitonic sort of entry indices in the selection order
-      int n2 = 1;
-      while (n2 < n) n2 <<= 1;
-      for (int i = tid; i < n2; i += blockDim.x) sm.idx[i] = i < n ? i : -1;
-      __syncthreads();
-      for (int size = 2; size <= n2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          for (int i = tid; i < n2 / 2; i += blockDim.x) {
-            const int lo = 2 * stride * (i / stride) + (i % stride);
-            const int hi = lo + stride;
-            const bool asc = (lo & size) == 0;
-            const int a = sm.idx[lo], c = sm.idx[hi];
-            bool a_gt;  // key(a) > key(c), padding (-1) sorts last
-            if (a < 0)
-              a_gt = c >= 0;
-            else if (c < 0)
-              a_gt = false;
-            else
-              a_gt = key_less(sm.k0[c], sm.k1[c], sm.k2[c], sm.k0[a], sm.k1[a], sm.k2[a]);
-            if (a_gt == asc) {
-              sm.idx[lo] = c;
-              sm.idx[hi] = a;
-            }
-          }
-          __syncthreads();
-        }
-      }
-      const int take = min(n, M);
-      for (int i = tid; i < take; i += blockDim.x) sm.pos[sm.idx[i]] = i + 1;
-      __syncthreads();
-      for (int i = tid; i < take; i += blockDim.x) {
-        const int e = sm.idx[i];
-        const uint64_t k0 = sm.k0[e];
-        const int dep = (int)(k0 & 0xFFFFFFFFu);
-        const int r = path_rank(sm.k1[e], sm.k2[e], dep - 1);
-        o_par[i + 1] = sm.par[e] < 0 ? 0 : sm.pos[sm.par[e]];
-        o_tok[i + 1] = sm.tok[(dep - 1) * K + r];
-        o_dep[i + 1] = dep;
-        o_sc[i + 1] = k0_score(k0);
-      }
-      n_out = 1 + take;
-      done = true;
-    }
+  }
+  __syncthreads();
+  if (s_nout < 0 && M <= kSelCap / 2) {
+    const int r = select_threshold<kSelThreads>(sm, d, K, M, kSelCap, kSelCap, warp_tmp, hist, bcast, o_par, o_tok,
+                                                o_dep, o_sc);
+    if (tid == 0) s_nout = r;
     __syncthreads();
   }
-  if (!done) {
+  if (s_nout < 0) {
     // exact fallback: best-first search by warp 0 over the whole shared buffer
-    if (tid < 32) n_out = select_heap_warp(sm.marg, sm.tok, d, K, budget, smem, o_par, o_tok, o_dep, o_sc);
-    if (tid == 0) bcast[0] = n_out;
+    if (tid < 32) {
+      const int r = select_heap_warp(sm.marg, sm.tok, d, K, budget, smem, o_par, o_tok, o_dep, o_sc);
+      if (tid == 0) s_nout = r;
+    }
     __syncthreads();
-    n_out = bcast[0];
   }
+  const int n_out = s_nout;
   for (int j = n_out + tid; j < budget; j += blockDim.x) {
     o_par[j] = -1;
     o_tok[j] = -1;

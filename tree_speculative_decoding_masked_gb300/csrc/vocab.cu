@@ -8,6 +8,7 @@
 // the partials, the last row of a sequence runs that sequence's epilogue (drafted-token
 // probabilities and, for greedy verification, the walk down the tree).
 #include "tv_kernels.cuh"
+#include "tv_ptx.cuh"
 
 namespace tv {
 
@@ -75,23 +76,23 @@ struct RowAcc {
       }
     if (bv > av) {
       float nmc = bv * c2;
-      s *= exp2f(mc - nmc);
+      s *= ptx::ex2(mc - nmc);
       av = bv;
       ai = bi;
       mc = nmc;
     }
 #pragma unroll
-    for (int k = 0; k < kN; ++k) s += exp2f(fmaf(x[k], c2, -mc));
+    for (int k = 0; k < kN; ++k) s += ptx::ex2(fmaf(x[k], c2, -mc));
   }
   __device__ __forceinline__ void push1(float x, int idx, float c2) {
     if (x > av) {
       float nmc = x * c2;
-      s *= exp2f(mc - nmc);
+      s *= ptx::ex2(mc - nmc);
       av = x;
       ai = idx;
       mc = nmc;
     }
-    s += exp2f(fmaf(x, c2, -mc));
+    s += ptx::ex2(fmaf(x, c2, -mc));
   }
 };
 
@@ -202,12 +203,13 @@ __device__ __forceinline__ float load_logit(const void* base, size_t idx) {
   return to_f32(reinterpret_cast<const T*>(base)[idx]);
 }
 
-// Per-sequence epilogue, run by the CTA that finished the sequence's last row.
+// Per-sequence epilogue, run by the CTA that finished the sequence's last partial.
+// s_lse2 / s_lse2q / s_am hold the merged row statistics of sequence b.
 template <typename T>
-__device__ void sequence_epilogue(const VocabArgs& a, int b) {
+__device__ void sequence_epilogue(const VocabArgs& a, int b, const float* s_lse2, const float* s_lse2q,
+                                  const int* s_am) {
   __shared__ int s_par[kMaxNodes];
   __shared__ int s_tok[kMaxNodes];
-  __shared__ int s_am[kMaxNodes];
   __shared__ int s_bad;
   const int N = a.N, V = a.V;
   if (threadIdx.x == 0) s_bad = 0;
@@ -217,7 +219,6 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b) {
     int t = a.tokens[(size_t)b * N + c];
     s_par[c] = p;
     s_tok[c] = t;
-    s_am[c] = __ldcg(a.amax + (size_t)b * N + c);
     bool ok = (c == 0) ? (p == -1) : (p >= 0 && p < c);
     if (!ok) atomicOr(&s_bad, TV_DEV_BAD_TREE);
     if (c > 0 && (t < 0 || t >= V)) atomicOr(&s_bad, TV_DEV_BAD_TOKEN);
@@ -231,8 +232,8 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b) {
     if (c > 0 && !bad) {
       int u = s_par[c];
       size_t idx = ((size_t)b * N + u) * (size_t)V + s_tok[c];
-      pv = exp2f(fmaf(load_logit<T>(a.logits, idx), a.c2, -__ldcg(a.lse2 + (size_t)b * N + u)));
-      if (a.sampling) qv = exp2f(fmaf(load_logit<T>(a.draft, idx), a.c2, -__ldcg(a.lse2_q + (size_t)b * N + u)));
+      pv = ptx::ex2(fmaf(load_logit<T>(a.logits, idx), a.c2, -s_lse2[u]));
+      if (a.sampling) qv = ptx::ex2(fmaf(load_logit<T>(a.draft, idx), a.c2, -s_lse2q[u]));
     }
     if (a.pc) a.pc[(size_t)b * N + c] = pv;
     if (a.qc) a.qc[(size_t)b * N + c] = qv;
@@ -272,9 +273,12 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b) {
 }
 
 template <typename T, bool kVec>
-__global__ void __launch_bounds__(256) vocab_pass_kernel(VocabArgs a) {
+__global__ void __launch_bounds__(256, 4) vocab_pass_kernel(VocabArgs a) {
   __shared__ VocabPartial red[32];
   __shared__ int s_flag;
+  __shared__ float s_lse2[kMaxNodes];
+  __shared__ float s_lse2q[kMaxNodes];
+  __shared__ int s_am[kMaxNodes];
   const int split = blockIdx.x % a.splits;
   const int row = blockIdx.x / a.splits;
   const int b = row / a.N;
@@ -297,57 +301,58 @@ __global__ void __launch_bounds__(256) vocab_pass_kernel(VocabArgs a) {
     a.part[(size_t)row * a.splits + split] = p;
     if (a.sampling) a.part_q[(size_t)row * a.splits + split] = pq;
     __threadfence();
-    unsigned prev = atomicAdd(a.row_cnt + row, 1u);
-    s_flag = (prev == (unsigned)(a.splits - 1));
+    // one completion counter per sequence: the CTA that writes its last partial merges
+    const unsigned prev = atomicAdd(a.seq_cnt + b, 1u);
+    s_flag = (prev == (unsigned)(a.N * a.splits - 1));
   }
   __syncthreads();
   if (!s_flag) return;
-  // last CTA of this row: warp 0 merges the splits (lane s takes split s, s + 32, ...)
-  if (threadIdx.x < 32) {
-    __threadfence();
-    const VocabPartial none{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+  __threadfence();
+  // merge the splits of every row of sequence b: one warp per row, lanes over splits
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const VocabPartial none{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+  for (int u = wid; u < a.N; u += nw) {
+    const size_t r2 = (size_t)b * a.N + u;
     VocabPartial r = none, rq = none;
-    for (int s = threadIdx.x; s < a.splits; s += 32) {
-      const VocabPartial* src = a.part + (size_t)row * a.splits + s;
+    for (int s2 = lane; s2 < a.splits; s2 += 32) {
+      const VocabPartial* src = a.part + r2 * a.splits + s2;
       r = partial_merge(r, {__ldcg(&src->m), __ldcg(&src->s), __ldcg(&src->av), __ldcg(&src->ai)});
       if (a.sampling) {
-        const VocabPartial* sq = a.part_q + (size_t)row * a.splits + s;
+        const VocabPartial* sq = a.part_q + r2 * a.splits + s2;
         rq = partial_merge(rq, {__ldcg(&sq->m), __ldcg(&sq->s), __ldcg(&sq->av), __ldcg(&sq->ai)});
       }
     }
-    r = warp_merge(r);
-    if (a.sampling) rq = warp_merge(rq);
-    if (threadIdx.x == 0) {
+    if (a.splits > 1) {
+      r = warp_merge(r);
+      if (a.sampling) rq = warp_merge(rq);
+    }
+    if (lane == 0) {
       const float l2 = r.m + log2f(r.s);
-      a.lse2[row] = l2;
-      a.amax[row] = r.ai;
-      if (a.sampling) a.lse2_q[row] = rq.m + log2f(rq.s);
-      if (a.row_lse) a.row_lse[row] = l2 * kLn2;
-      if (a.row_argmax) a.row_argmax[row] = r.ai;
-      a.row_cnt[row] = 0;
-      __threadfence();
-      const unsigned prev = atomicAdd(a.seq_cnt + b, 1u);
-      s_flag = (prev == (unsigned)(a.N - 1));
+      s_lse2[u] = l2;
+      s_am[u] = r.ai;
+      if (a.sampling) {
+        const float l2q = rq.m + log2f(rq.s);
+        s_lse2q[u] = l2q;
+        a.lse2[r2] = l2;  // the sampling walk kernel reads these
+        a.lse2_q[r2] = l2q;
+      }
+      if (a.row_lse) a.row_lse[r2] = l2 * kLn2;
+      if (a.row_argmax) a.row_argmax[r2] = r.ai;
     }
   }
+  if (threadIdx.x == 0) a.seq_cnt[b] = 0;
   __syncthreads();
-  if (!s_flag) return;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    a.seq_cnt[b] = 0;
-  }
-  __syncthreads();
-  sequence_epilogue<T>(a, b);
+  sequence_epilogue<T>(a, b, s_lse2, s_lse2q, s_am);
 }
 
 // ------------------------------------------------------------------------------------
 // host side
 
 int verify_splits(int rows, int V) {
-  // Aim for ~4 resident 256-thread CTAs per SM on 152 SMs, >= 8192 elements per CTA.
+  // One wave of 4 resident 256-thread CTAs per SM on 152 SMs, >= 4096 elements per CTA.
   const int target = 152 * 4;
-  int s = (target + rows - 1) / rows;
-  int max_by_len = V / 8192;
+  int s = target / rows;
+  int max_by_len = V / 4096;
   if (max_by_len < 1) max_by_len = 1;
   if (s > max_by_len) s = max_by_len;
   if (s > 64) s = 64;
