@@ -152,68 +152,30 @@ __device__ int select_heap_warp(const float* sm_marg, const int* sm_tok, int d, 
 }
 
 // ------------------------------------------------------------------------------------
-// group-parallel helpers: a "group" is either warp 0 alone (kG = 32, __syncwarp) or the
-// whole block (kG = kSelThreads, __syncthreads); thread rank = threadIdx.x.
+// block helpers (kSelThreads threads)
 
-template <int kG>
-__device__ __forceinline__ void gsync() {
-  if constexpr (kG == 32)
-    __syncwarp();
-  else
-    __syncthreads();
-}
-
-// exclusive scan of one int per group thread; *total = the sum
-template <int kG>
-__device__ int group_excl_scan(int x, int* warp_tmp, int* total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int incl = x;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if constexpr (kG == 32) {
-    *total = __shfl_sync(0xffffffffu, incl, 31);
-    return incl - x;
-  } else {
-    if (lane == 31) warp_tmp[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-      const int v = lane < kG / 32 ? warp_tmp[lane] : 0;
-      int vi = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, vi, o);
-        if (lane >= o) vi += y;
-      }
-      warp_tmp[lane] = vi - v;
-      if (lane == 31) warp_tmp[32] = vi;
-    }
-    __syncthreads();
-    const int r = warp_tmp[wid] + incl - x;
-    *total = warp_tmp[32];
-    __syncthreads();
-    return r;
-  }
-}
-
-// k-th largest (1-based) of vals[0..n) by 8-bit radix select (k <= n); all group threads
-// return it.  The digit search runs in warp 0, which belongs to every group.
-template <int kG>
-__device__ uint32_t group_kth_largest(const uint32_t* vals, int n, int k, int* hist, int* bcast) {
+// k-th largest (1-based, k <= n) of vals[0..n) by 8-bit radix select with warp-aggregated
+// histogram updates; every thread returns it.
+__device__ uint32_t block_kth_largest(const uint32_t* vals, int n, int k, int* hist, int* bcast) {
+  const int lane = threadIdx.x & 31;
   uint32_t prefix = 0, mask = 0;
   int want = k;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += kG) hist[i] = 0;
-    gsync<kG>();
-    for (int i = threadIdx.x; i < n; i += kG) {
-      const uint32_t v = vals[i];
-      if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1);
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += blockDim.x) {
+      const int i = base + threadIdx.x;
+      const uint32_t v = i < n ? vals[i] : 0u;
+      const bool act = i < n && (v & mask) == prefix;
+      const unsigned am = __ballot_sync(0xffffffffu, act);
+      if (act) {
+        const int dig = (int)((v >> shift) & 255u);
+        const unsigned peers = __match_any_sync(am, dig);
+        if (lane == __ffs(peers) - 1) atomicAdd(&hist[dig], __popc(peers));
+      }
     }
-    gsync<kG>();
+    __syncthreads();
     if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
       int cnt[8];
       int tot = 0;
 #pragma unroll
@@ -248,11 +210,11 @@ __device__ uint32_t group_kth_largest(const uint32_t* vals, int n, int k, int* h
         bcast[1] = rest;
       }
     }
-    gsync<kG>();
+    __syncthreads();
     prefix |= (uint32_t)bcast[0] << shift;
     mask |= 255u << shift;
     want = bcast[1];
-    gsync<kG>();
+    __syncthreads();
   }
   return prefix;
 }
@@ -265,21 +227,27 @@ struct SelSmem {
   uint64_t* k2;
   int* par;   // parent entry (-1: the root)
   int* idx;   // sort permutation
-  int* pos;   // entry -> position in the sorted order
+  int* pos;   // entry -> position in the output (0: not taken)
 };
 
-// Expand every candidate with s >= tau, level by level, into at most `cap` entries.
-// Returns the count, or -1 on overflow (*kept = entries written before stopping).
-template <int kG>
-__device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int cap, int* warp_tmp, int* kept) {
-  int lo = 0, hi = 0, n = 0;  // current level = entries [lo, hi); level 0 is the virtual root
+// Expand every candidate with s >= tau, level by level (one barrier per level; slots come
+// from one shared counter, one atomic per warp).  Returns the entry count, or -1 if more
+// than kSelCap would be needed; then *complete = entries of the fully expanded levels.
+__device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int* s_count, int* s_over,
+                                int* complete) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    *s_count = 0;
+    *s_over = 0;
+  }
+  __syncthreads();
+  int lo = 0, hi = 0;  // current level = entries [lo, hi); level 0 is the virtual root
   for (int k = 1; k <= d; ++k) {
     const int nparents = (k == 1) ? 1 : hi - lo;
     if (nparents <= 0) break;
     const float* mk = sm.marg + (k - 1) * K;
-    int new_n = n;
-    for (int base = 0; base < nparents; base += kG) {
-      const int pi = base + (int)threadIdx.x;
+    for (int base = 0; base < nparents; base += blockDim.x) {
+      const int pi = base + threadIdx.x;
       int cnt = 0;
       float ps = 1.f;
       int pe = -1;
@@ -288,41 +256,48 @@ __device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int 
         ps = (k == 1) ? 1.f : k0_score(sm.k0[pe]);
         while (cnt < K && __fmul_rn(ps, mk[cnt]) >= tau) ++cnt;
       }
-      int total;
-      const int off = group_excl_scan<kG>(cnt, warp_tmp, &total);
-      if (new_n + total > cap) {
-        *kept = new_n;
-        return -1;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-      if (pi < nparents) {
+      const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+      int wbase = 0;
+      if (lane == 31 && wtot > 0) wbase = atomicAdd(s_count, wtot);
+      wbase = __shfl_sync(0xffffffffu, wbase, 31);
+      if (wtot > 0 && wbase + wtot > kSelCap) {
+        if (lane == 0) *s_over = 1;
+      } else if (cnt > 0) {
         const uint64_t pk1 = (k == 1) ? 0ull : sm.k1[pe];
         const uint64_t pk2 = (k == 1) ? 0ull : sm.k2[pe];
+        const int e0 = wbase + incl - cnt;
         for (int j = 0; j < cnt; ++j) {
-          const int e = new_n + off + j;
           uint64_t c1 = pk1, c2 = pk2;
           path_set(c1, c2, k - 1, j);
-          sm.k0[e] = make_k0(__fmul_rn(ps, mk[j]), k);
-          sm.k1[e] = c1;
-          sm.k2[e] = c2;
-          sm.par[e] = pe;
+          sm.k0[e0 + j] = make_k0(__fmul_rn(ps, mk[j]), k);
+          sm.k1[e0 + j] = c1;
+          sm.k2[e0 + j] = c2;
+          sm.par[e0 + j] = pe;
         }
       }
-      new_n += total;
-      gsync<kG>();
     }
-    lo = n;
-    hi = new_n;
-    n = new_n;
+    __syncthreads();
+    if (*s_over) {
+      *complete = hi;
+      return -1;
+    }
+    lo = hi;
+    hi = *s_count;
   }
-  return n;
+  return *s_count;
 }
 
 // bitonic sort of sm.idx[0..n2) (entries, -1 = padding last) in the selection order
-template <int kG>
 __device__ void bitonic_sort_idx(const SelSmem& sm, int n2) {
   for (int size = 2; size <= n2; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < n2 / 2; i += kG) {
+      for (int i = threadIdx.x; i < n2 / 2; i += blockDim.x) {
         const int lo = 2 * stride * (i / stride) + (i % stride);
         const int hi = lo + stride;
         const bool asc = (lo & size) == 0;
@@ -339,22 +314,23 @@ __device__ void bitonic_sort_idx(const SelSmem& sm, int n2) {
           sm.idx[hi] = a;
         }
       }
-      gsync<kG>();
+      __syncthreads();
     }
   }
 }
 
-// Threshold selection by a group.  Returns 1 + number selected, or -1 if the candidate
-// set did not fit (caller falls back).  `sort_cap` bounds the tie group that is sorted.
-template <int kG>
-__device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int cap, int sort_cap, int* warp_tmp,
-                                int* hist, int* bcast, int32_t* o_par, int32_t* o_tok, int32_t* o_dep, float* o_sc) {
+constexpr int kRankDirect = 512;  // rank by direct comparison up to this many candidates
+
+// Threshold selection by the block.  Returns 1 + number selected, or -1 if the
+// candidate set did not fit (the caller falls back).
+__device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_count, int* s_over, int* hist,
+                                int* bcast, int32_t* o_par, int32_t* o_tok, int32_t* o_dep, float* o_sc) {
   const int t = threadIdx.x;
   // 1. tau = M-th best score among the one-deviation candidates (ranks < kSelDevRanks)
   uint32_t* f1 = reinterpret_cast<uint32_t*>(sm.k1);  // 2 * kSelCap slots, free for now
   const int rmax = min(K, kSelDevRanks);
   const int ncombo = 1 + d * (rmax - 1);  // combo 0: no deviation; else (position j, rank r)
-  for (int c = t; c < ncombo; c += kG) {
+  for (int c = t; c < ncombo; c += blockDim.x) {
     int j = -1, r = 0, off = 0;
     if (c > 0) {
       j = (c - 1) / (rmax - 1);
@@ -362,58 +338,65 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int cap,
       // no deviation: d prefixes; deviation at j: d - j prefixes
       off = d + (rmax - 1) * (j * d - j * (j - 1) / 2) + (r - 1) * (d - j);
     }
-    float s = 1.f;
+    float sc = 1.f;
     int w = 0;
     for (int p = 0; p < d; ++p) {
-      s = __fmul_rn(s, sm.marg[p * K + (p == j ? r : 0)]);
+      sc = __fmul_rn(sc, sm.marg[p * K + (p == j ? r : 0)]);
       if (p >= (j < 0 ? 0 : j)) {
         const int slot = off + w++;
-        if (slot < 2 * kSelCap) f1[slot] = __float_as_uint(s);
+        if (slot < 2 * kSelCap) f1[slot] = __float_as_uint(sc);
       }
     }
   }
   const int nf1 = min(d + (rmax - 1) * (d * (d + 1) / 2), 2 * kSelCap);
-  gsync<kG>();
+  __syncthreads();
   float tau = 0.f;
-  if (nf1 >= M) tau = __uint_as_float(group_kth_largest<kG>(f1, nf1, M, hist, bcast));
-  gsync<kG>();
-  // 2. expansion, one retry with tau raised to the M-th best entry found so far
-  int kept = 0;
-  int n = expand_threshold<kG>(sm, d, K, tau, cap, warp_tmp, &kept);
-  if (n < 0 && kept >= M) {
+  if (nf1 >= M) tau = __uint_as_float(block_kth_largest(f1, nf1, M, hist, bcast));
+  __syncthreads();
+  // 2. expansion; one retry with tau raised to the M-th best of the complete levels
+  int complete = 0;
+  int n = expand_threshold(sm, d, K, tau, s_count, s_over, &complete);
+  if (n < 0 && complete >= M) {
     uint32_t* sc = reinterpret_cast<uint32_t*>(sm.idx);  // idx + pos: 2 * kSelCap slots
-    for (int i = t; i < kept; i += kG) sc[i] = __float_as_uint(k0_score(sm.k0[i]));
-    gsync<kG>();
-    tau = __uint_as_float(group_kth_largest<kG>(sc, kept, M, hist, bcast));
-    gsync<kG>();
-    n = expand_threshold<kG>(sm, d, K, tau, cap, warp_tmp, &kept);
+    for (int i = t; i < complete; i += blockDim.x) sc[i] = __float_as_uint(k0_score(sm.k0[i]));
+    __syncthreads();
+    tau = __uint_as_float(block_kth_largest(sc, complete, M, hist, bcast));
+    __syncthreads();
+    n = expand_threshold(sm, d, K, tau, s_count, s_over, &complete);
   }
   if (n < 0) return -1;
   const int take = min(n, M);
-  // 3. the M-th best score T; only entries with s >= T can be taken: sort just those
-  uint32_t* sc = reinterpret_cast<uint32_t*>(sm.pos);
-  for (int i = t; i < n; i += kG) sc[i] = __float_as_uint(k0_score(sm.k0[i]));
-  gsync<kG>();
-  const uint32_t T = take > 0 ? group_kth_largest<kG>(sc, n, take, hist, bcast) : 0u;
-  int cnt_ge = 0;
-  for (int base = 0; base < n; base += kG) {
-    const int i = base + t;
-    const int f = (i < n && sc[i] >= T) ? 1 : 0;
-    int total;
-    const int off = group_excl_scan<kG>(f, warp_tmp, &total);
-    if (f) sm.idx[cnt_ge + off] = i;
-    cnt_ge += total;
-    gsync<kG>();
+  // 3. order: the output position of entry e is 1 + its rank in the selection order
+  if (n <= kRankDirect) {
+    for (int e = t; e < n; e += blockDim.x) {
+      const uint64_t a0 = sm.k0[e], a1 = sm.k1[e], a2 = sm.k2[e];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += key_less(sm.k0[j], sm.k1[j], sm.k2[j], a0, a1, a2) ? 1 : 0;
+      sm.pos[e] = rank < take ? rank + 1 : 0;
+      if (rank < take) sm.idx[rank] = e;
+    }
+  } else {
+    // only entries with s >= (M-th best score) can be taken: sort just those
+    uint32_t* sc = reinterpret_cast<uint32_t*>(sm.pos);
+    for (int i = t; i < n; i += blockDim.x) sc[i] = __float_as_uint(k0_score(sm.k0[i]));
+    __syncthreads();
+    const uint32_t T = block_kth_largest(sc, n, take, hist, bcast);
+    if (t == 0) *s_count = 0;
+    __syncthreads();
+    for (int i = t; i < n; i += blockDim.x)
+      if (sc[i] >= T) sm.idx[atomicAdd(s_count, 1)] = i;
+    __syncthreads();
+    const int cnt_ge = *s_count;
+    int n2 = 1;
+    while (n2 < cnt_ge) n2 <<= 1;
+    if (n2 > 2 * kSelCap) return -1;
+    for (int i = cnt_ge + t; i < n2; i += blockDim.x) sm.idx[i] = -1;
+    __syncthreads();
+    bitonic_sort_idx(sm, n2);
+    for (int i = t; i < take; i += blockDim.x) sm.pos[sm.idx[i]] = i + 1;
   }
-  if (cnt_ge > sort_cap) return -1;
-  int n2 = 1;
-  while (n2 < cnt_ge) n2 <<= 1;
-  for (int i = cnt_ge + t; i < n2; i += kG) sm.idx[i] = -1;
-  gsync<kG>();
-  bitonic_sort_idx<kG>(sm, n2);
-  for (int i = t; i < take; i += kG) sm.pos[sm.idx[i]] = i + 1;
-  gsync<kG>();
-  for (int i = t; i < take; i += kG) {
+  __syncthreads();
+  for (int i = t; i < take; i += blockDim.x) {
     const int e = sm.idx[i];
     const uint64_t k0 = sm.k0[e];
     const int dep = (int)(k0 & 0xFFFFFFFFu);
@@ -423,12 +406,9 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int cap,
     o_dep[i + 1] = dep;
     o_sc[i + 1] = k0_score(k0);
   }
-  gsync<kG>();
+  __syncthreads();
   return 1 + take;
 }
-
-constexpr int kWarpPathMaxM = 127;  // budgets up to 128 rows try the single-warp path
-constexpr int kWarpPathCap = 1024;
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __restrict__ marg,
                                                              const int32_t* __restrict__ ptok, int d, int K,
@@ -436,10 +416,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
                                                              int32_t* out_parent, int32_t* out_tok, int32_t* out_depth,
                                                              float* out_score, int32_t* n_nodes, int32_t* dev_status) {
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int warp_tmp[33];
   __shared__ int hist[256];
   __shared__ int bcast[2];
-  __shared__ int s_bad, s_nout;
+  __shared__ int s_bad, s_nout, s_count, s_over;
   const int b = blockIdx.x, tid = threadIdx.x;
   const int M = budget - 1;
   SelSmem sm;
@@ -481,21 +460,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
   }
   if (M <= 0) {
     if (tid == 0) s_nout = 1;
-  } else if (M <= kWarpPathMaxM) {
-    // small budgets: one warp, no block-wide barriers
-    if (tid < 32) {
-      const int r = select_threshold<32>(sm, d, K, M, kWarpPathCap, 128, warp_tmp, hist, bcast, o_par, o_tok,
-                                         o_dep, o_sc);
-      if (tid == 0) s_nout = r;
-    }
+  } else if (M <= kSelCap / 2) {
+    const int r = select_threshold(sm, d, K, M, &s_count, &s_over, hist, bcast, o_par, o_tok, o_dep, o_sc);
+    if (tid == 0) s_nout = r;
   }
   __syncthreads();
-  if (s_nout < 0 && M <= kSelCap / 2) {
-    const int r = select_threshold<kSelThreads>(sm, d, K, M, kSelCap, kSelCap, warp_tmp, hist, bcast, o_par, o_tok,
-                                                o_dep, o_sc);
-    if (tid == 0) s_nout = r;
-    __syncthreads();
-  }
   if (s_nout < 0) {
     // exact fallback: best-first search by warp 0 over the whole shared buffer
     if (tid < 32) {

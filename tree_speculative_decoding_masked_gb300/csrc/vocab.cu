@@ -12,6 +12,8 @@
 
 namespace tv {
 
+constexpr int kStagedParts = 640;  // split partials staged in shared memory by the merging CTA
+
 struct VocabPartial {
   float m;   // max of x * c2 over the chunk (base-2 scaled)
   float s;   // sum 2^(x*c2 - m)
@@ -279,6 +281,7 @@ __global__ void __launch_bounds__(256, 4) vocab_pass_kernel(VocabArgs a) {
   __shared__ float s_lse2[kMaxNodes];
   __shared__ float s_lse2q[kMaxNodes];
   __shared__ int s_am[kMaxNodes];
+  __shared__ float4 s_stage[kStagedParts];
   const int split = blockIdx.x % a.splits;
   const int row = blockIdx.x / a.splits;
   const int b = row / a.N;
@@ -308,37 +311,40 @@ __global__ void __launch_bounds__(256, 4) vocab_pass_kernel(VocabArgs a) {
   __syncthreads();
   if (!s_flag) return;
   __threadfence();
-  // merge the splits of every row of sequence b: one warp per row, lanes over splits
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  // merge the splits of every row of sequence b.  All partials are fetched at once (one
+  // round trip), staged in shared memory, then merged per row.
+  const int npart = a.N * a.splits;
+  const size_t pbase = (size_t)b * a.N * a.splits;
+  const bool staged = npart <= kStagedParts;
   const VocabPartial none{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
-  for (int u = wid; u < a.N; u += nw) {
-    const size_t r2 = (size_t)b * a.N + u;
-    VocabPartial r = none, rq = none;
-    for (int s2 = lane; s2 < a.splits; s2 += 32) {
-      const VocabPartial* src = a.part + r2 * a.splits + s2;
-      r = partial_merge(r, {__ldcg(&src->m), __ldcg(&src->s), __ldcg(&src->av), __ldcg(&src->ai)});
-      if (a.sampling) {
-        const VocabPartial* sq = a.part_q + r2 * a.splits + s2;
-        rq = partial_merge(rq, {__ldcg(&sq->m), __ldcg(&sq->s), __ldcg(&sq->av), __ldcg(&sq->ai)});
+  for (int pass = 0; pass < (a.sampling ? 2 : 1); ++pass) {
+    const VocabPartial* src = pass == 0 ? a.part : a.part_q;
+    if (staged) {
+      for (int i = threadIdx.x; i < npart; i += blockDim.x)
+        s_stage[i] = __ldcg(reinterpret_cast<const float4*>(src + pbase + i));
+      __syncthreads();
+    }
+    for (int u = threadIdx.x; u < a.N; u += blockDim.x) {
+      VocabPartial r = none;
+      for (int s2 = 0; s2 < a.splits; ++s2) {
+        const int i = u * a.splits + s2;
+        const float4 v = staged ? s_stage[i] : __ldcg(reinterpret_cast<const float4*>(src + pbase + i));
+        r = partial_merge(r, {v.x, v.y, v.z, __float_as_int(v.w)});
       }
-    }
-    if (a.splits > 1) {
-      r = warp_merge(r);
-      if (a.sampling) rq = warp_merge(rq);
-    }
-    if (lane == 0) {
+      const size_t r2 = (size_t)b * a.N + u;
       const float l2 = r.m + log2f(r.s);
-      s_lse2[u] = l2;
-      s_am[u] = r.ai;
-      if (a.sampling) {
-        const float l2q = rq.m + log2f(rq.s);
-        s_lse2q[u] = l2q;
-        a.lse2[r2] = l2;  // the sampling walk kernel reads these
-        a.lse2_q[r2] = l2q;
+      if (pass == 0) {
+        s_lse2[u] = l2;
+        s_am[u] = r.ai;
+        if (a.sampling) a.lse2[r2] = l2;  // the sampling walk kernel reads these
+        if (a.row_lse) a.row_lse[r2] = l2 * kLn2;
+        if (a.row_argmax) a.row_argmax[r2] = r.ai;
+      } else {
+        s_lse2q[u] = l2;
+        a.lse2_q[r2] = l2;
       }
-      if (a.row_lse) a.row_lse[r2] = l2 * kLn2;
-      if (a.row_argmax) a.row_argmax[r2] = r.ai;
     }
+    __syncthreads();
   }
   if (threadIdx.x == 0) a.seq_cnt[b] = 0;
   __syncthreads();
