@@ -144,7 +144,8 @@ TV_API tv_status tv_tree_attention(const void* q, const void* k_cache, const voi
  *   p_draft       [B][N] float out (optional): softmax(x[parent(c)])[tokens[c]], NaN at c=0
  *   row_lse       [B][N] float out (optional): log-sum-exp of each row
  *   row_argmax    [B][N] int32 out (optional): argmax of each row
- * Limits: 1 <= N <= 1024, 1 <= V < 2^31 / N.  Workspace: tv_verify_workspace_size().
+ * Limits: 1 <= N <= 1024, 1 <= V < 2^31 / N, B * N <= 131072.
+ * Workspace: tv_verify_workspace_size().
  */
 TV_API size_t tv_verify_workspace_size(int B, int N, int V, tv_dtype dtype, int sampling);
 TV_API tv_status tv_verify_greedy(const void* logits, const int32_t* parent, const int32_t* tokens, int B,

@@ -95,8 +95,7 @@ static tv_status verify_common_checks(const void* logits, const int32_t* parent,
   if (!valid_dtype(dtype)) return TV_ERR_DTYPE;
   if (B < 1 || N < 1 || N > kMaxNodes || V < 1) return TV_ERR_SHAPE;
   const long long rows = (long long)B * N;
-  const int splits = verify_splits((int)rows, V);
-  if (rows * splits > 0x7fffffffLL) return TV_ERR_SHAPE;
+  if (rows > kMaxVerifyRows) return TV_ERR_SHAPE;
   if ((long long)N * V > 0x7fffffffLL) return TV_ERR_SHAPE;
   if (!ws || ws_bytes < verify_ws_layout(B, N, V, sampling, nullptr)) return TV_ERR_WORKSPACE;
   if (!aligned16(ws)) return TV_ERR_ALIGN;

@@ -419,61 +419,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     // peer has finished reading.
     ptx::cluster_sync();
     {
-      // all 192 threads: item = (row of this CTA's slice, group of 16 columns)
+      // all 192 threads; item = (row of this CTA's slice, 16-byte chunk of 4 columns):
+      // a warp reads one contiguous row of each peer's partial, all loads issued first
       const int S = a.splits;
       const int R = (kRows + S - 1) / S;
       const int r0 = split * R, r1 = min(kRows, r0 + R);
       const int nrows = max(0, r1 - r0);
+      constexpr int kChunks = D / 4;
       const uint32_t part_local = ptx::smem_addr(sKV);
       const uint32_t ml_local = ptx::smem_addr(sKV + D * kRows * 4);
-      for (int item = threadIdx.x; item < nrows * (D / 16); item += kThreads) {
-        const int rr = r0 + item % nrows;
-        const int grp = item / nrows;  // columns [16 grp, 16 grp + 16) = chunks 4 grp .. 4 grp + 3
+      for (int item = threadIdx.x; item < nrows * kChunks; item += kThreads) {
+        const int rr = r0 + item / kChunks;
+        const int ch = item % kChunks;
         const int gg = rr / a.NT, ii = i0 + rr % a.NT;
         if (gg >= a.G || ii >= a.N || rr >= rows_used) continue;
-        float2 mlv[8];
-        float M = -INFINITY;
+        float2 mlv[kMaxSplits];
+        float4 x[kMaxSplits];
+        const uint32_t moff = (uint32_t)(rr * 8);
+        const uint32_t xoff = (uint32_t)(rr * D * 4 + ((ch ^ (rr & 7)) << 4));
 #pragma unroll
-        for (int s2 = 0; s2 < 8; ++s2) {
+        for (int s2 = 0; s2 < kMaxSplits; ++s2) {
           if (s2 < S) {
-            mlv[s2] = ptx::ld_cluster_f32x2(ptx::map_cluster(ml_local + rr * 8, s2));
-            M = fmaxf(M, mlv[s2].x);
+            mlv[s2] = ptx::ld_cluster_f32x2(ptx::map_cluster(ml_local, s2) + moff);
+            x[s2] = ptx::ld_cluster_f32x4(ptx::map_cluster(part_local, s2) + xoff);
           }
         }
+        float M = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxSplits; ++s2)
+          if (s2 < S) M = fmaxf(M, mlv[s2].x);
         float L = 0.f;
-        float acc[16];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < 8; ++s2) {
+        for (int s2 = 0; s2 < kMaxSplits; ++s2) {
           if (s2 < S && mlv[s2].x != -INFINITY) {
             const float w = ptx::ex2(mlv[s2].x - M);
             L = fmaf(mlv[s2].y, w, L);
-            const uint32_t rowb = ptx::map_cluster(part_local, s2) + (uint32_t)(rr * D * 4);
-            float4 x[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) x[q] = ptx::ld_cluster_f32x4(rowb + (((4 * grp + q) ^ (rr & 7)) << 4));
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              acc[4 * q + 0] = fmaf(w, x[q].x, acc[4 * q + 0]);
-              acc[4 * q + 1] = fmaf(w, x[q].y, acc[4 * q + 1]);
-              acc[4 * q + 2] = fmaf(w, x[q].z, acc[4 * q + 2]);
-              acc[4 * q + 3] = fmaf(w, x[q].w, acc[4 * q + 3]);
-            }
+            acc.x = fmaf(w, x[s2].x, acc.x);
+            acc.y = fmaf(w, x[s2].y, acc.y);
+            acc.z = fmaf(w, x[s2].z, acc.z);
+            acc.w = fmaf(w, x[s2].w, acc.w);
           }
         }
         const float inv = L > 0.f ? 1.f / L : 0.f;
-        const size_t o2 = (((size_t)b * a.Hq + hk * a.G + gg) * a.N + ii) * D + grp * 16;
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + o2);
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          uint4 u;
-          u.x = ptx::cvt_bf16x2(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
-          u.y = ptx::cvt_bf16x2(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
-          u.z = ptx::cvt_bf16x2(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
-          u.w = ptx::cvt_bf16x2(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
-          dst[k] = u;
-        }
+        const size_t o2 = (((size_t)b * a.Hq + hk * a.G + gg) * a.N + ii) * D + ch * 4;
+        uint2 u;
+        u.x = ptx::cvt_bf16x2(acc.x * inv, acc.y * inv);
+        u.y = ptx::cvt_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + o2) = u;
       }
     }
     __syncwarp();

@@ -254,7 +254,17 @@ __device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int*
       if (pi < nparents) {
         pe = (k == 1) ? -1 : lo + pi;
         ps = (k == 1) ? 1.f : k0_score(sm.k0[pe]);
-        while (cnt < K && __fmul_rn(ps, mk[cnt]) >= tau) ++cnt;
+        // marginals are sorted: the qualifying children are a prefix of the ranks
+        for (int j0 = 0; j0 < K; j0 += 4) {
+          float m4[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) m4[q] = j0 + q < K ? mk[j0 + q] : -1.f;
+          int c4 = 0;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) c4 += (m4[q] >= 0.f && __fmul_rn(ps, m4[q]) >= tau) ? 1 : 0;
+          cnt += c4;
+          if (c4 < 4) break;
+        }
       }
       int incl = cnt;
 #pragma unroll
@@ -338,13 +348,19 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_c
       // no deviation: d prefixes; deviation at j: d - j prefixes
       off = d + (rmax - 1) * (j * d - j * (j - 1) / 2) + (r - 1) * (d - j);
     }
+    float mv[kMaxDepth];
+#pragma unroll
+    for (int p = 0; p < kMaxDepth; ++p) mv[p] = p < d ? sm.marg[p * K + (p == j ? r : 0)] : 1.f;
     float sc = 1.f;
-    int w = 0;
-    for (int p = 0; p < d; ++p) {
-      sc = __fmul_rn(sc, sm.marg[p * K + (p == j ? r : 0)]);
-      if (p >= (j < 0 ? 0 : j)) {
-        const int slot = off + w++;
-        if (slot < 2 * kSelCap) f1[slot] = __float_as_uint(sc);
+    const int first = j < 0 ? 0 : j;
+#pragma unroll
+    for (int p = 0; p < kMaxDepth; ++p) {
+      if (p < d) {
+        sc = __fmul_rn(sc, mv[p]);
+        if (p >= first) {
+          const int slot = off + (p - first);
+          if (slot < 2 * kSelCap) f1[slot] = __float_as_uint(sc);
+        }
       }
     }
   }
@@ -371,7 +387,20 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_c
     for (int e = t; e < n; e += blockDim.x) {
       const uint64_t a0 = sm.k0[e], a1 = sm.k1[e], a2 = sm.k2[e];
       int rank = 0;
-      for (int j = 0; j < n; ++j) rank += key_less(sm.k0[j], sm.k1[j], sm.k2[j], a0, a1, a2) ? 1 : 0;
+      int j = 0;
+      for (; j + 8 <= n; j += 8) {
+        uint64_t c0[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) c0[q] = sm.k0[j + q];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (c0[q] < a0)
+            ++rank;
+          else if (c0[q] == a0 && key_less(c0[q], sm.k1[j + q], sm.k2[j + q], a0, a1, a2))
+            ++rank;
+        }
+      }
+      for (; j < n; ++j) rank += key_less(sm.k0[j], sm.k1[j], sm.k2[j], a0, a1, a2) ? 1 : 0;
       sm.pos[e] = rank < take ? rank + 1 : 0;
       if (rank < take) sm.idx[rank] = e;
     }

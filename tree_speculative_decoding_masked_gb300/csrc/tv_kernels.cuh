@@ -12,10 +12,11 @@ constexpr int kMaxBudget = 4096; // selection budget (rows)
 
 // ---- verify (vocab pass + walks)
 struct VerifyWs {
-  int splits;
-  size_t row_cnt, seq_cnt, part, part_q, lse2, lse2_q, amax, pc, qc, total;
+  int splits;  // partial slots per row
+  size_t row_cnt, seq_cnt, part, part_q, lse2, lse2_q, xc, pc, qc, yc, total;
 };
-int verify_splits(int rows, int V);
+constexpr long long kMaxVerifyRows = 131072;  // B * N limit of the verify calls
+int verify_slots_per_row(int rows);
 size_t verify_ws_layout(int B, int N, int V, int sampling, VerifyWs* w);
 cudaError_t launch_vocab_pass(const void* logits, const void* draft, const int32_t* parent,
                               const int32_t* tokens, int B, int N, int V, tv_dtype dtype, float temperature,

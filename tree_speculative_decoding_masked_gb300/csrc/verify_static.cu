@@ -65,7 +65,7 @@ extern "C" TV_API tv_status tv_verify_greedy_static(const void* logits, const in
   if (B < 1 || N < 1 || N > kMaxNodes || V < 1) return TV_ERR_SHAPE;
   const long long rows = (long long)B * N;
   if (rows > 0x7fffffffLL || (long long)N * V > 0x7fffffffLL) return TV_ERR_SHAPE;
-  if (rows * verify_splits((int)rows, V) > 0x7fffffffLL) return TV_ERR_SHAPE;
+  if (rows > kMaxVerifyRows) return TV_ERR_SHAPE;
   VerifyWs w;
   const size_t need = verify_ws_layout(B, N, V, 0, &w);
   if (need > kStaticScratchBytes) return TV_ERR_WORKSPACE;  // the fixed array is too small

@@ -3,12 +3,19 @@
 // Speculative-decoding blog, "greedy decoding, intuitive version" / "acceptance
 // probability for sampling": every drafted position needs the target's choice (argmax)
 // and the target probability of the drafted token p_u(t).  One streaming, vectorised
-// read of each logits row yields argmax (lowest index among equal raw values) and the
-// base-2 log-sum-exp of x/T; rows are split across CTAs and the last CTA of a row merges
-// the partials, the last row of a sequence runs that sequence's epilogue (drafted-token
-// probabilities and, for greedy verification, the walk down the tree).
+// read of the logits yields, per row, the argmax (lowest index among equal raw values)
+// and the base-2 log-sum-exp of x/T.
+//
+// Work split: the B*N*V logits are cut into equal contiguous ranges, one per resident CTA
+// (one full wave, identical bytes per CTA).  A CTA writes one partial (max, sum, argmax)
+// per row segment it covers and, on the way, the raw logit of every drafted token that
+// falls in its range.  The CTA that contributes the last partial of a sequence (one
+// atomic per sequence, against a closed-form count) merges that sequence's rows and runs
+// its epilogue: drafted-token probabilities and, for greedy verification, the walk.
 #include "tv_kernels.cuh"
 #include "tv_ptx.cuh"
+
+#include <algorithm>
 
 namespace tv {
 
@@ -145,7 +152,7 @@ template <typename T, bool kVec>
 __device__ __forceinline__ void scan_chunk(const T* __restrict__ row, int v0, int v1, float c2, RowAcc& acc) {
   if constexpr (kVec) {
     constexpr int kN = Vec16<T>::kN;
-    constexpr int kInFlight = 8;
+    constexpr int kInFlight = 4;
     const int nvec = (v1 - v0) / kN;
     const uint4* p = reinterpret_cast<const uint4*>(row + v0);
     const int stride = blockDim.x;
@@ -177,17 +184,21 @@ struct VocabArgs {
   const void* draft;  // sampling only
   const int32_t* parent;
   const int32_t* tokens;
-  int B, N, V, splits, chunk;
-  float c2;  // log2(e) / T
-  VocabPartial* part;
-  VocabPartial* part_q;
-  float* lse2;    // [rows] base-2 lse of x*c2
+  int B, N, V;
+  long long E;      // B * N * V elements
+  long long chunk;  // elements per CTA (multiple of 8)
+  long long L;      // chunk / gcd(V, chunk): row boundaries u*V on a chunk edge <=> L | u
+  int mc;           // partial slots per row (>= CTAs covering any row)
+  float c2;         // log2(e) / T
+  VocabPartial* part;    // [rows][mc]
+  VocabPartial* part_q;  // [rows][mc]
+  float* lse2;    // [rows] base-2 lse of x*c2 (sampling walk input)
   float* lse2_q;  // [rows]
-  int32_t* amax;  // [rows]
-  float* pc;      // [rows] p_{parent(c)}(t_c) (fp32), sampling scratch
+  float* xc;      // [rows] raw target logit of node c's token in its parent's row
+  float* yc;      // [rows] same for the draft logits
+  float* pc;      // [rows] p_{parent(c)}(t_c) (fp32), sampling walk input
   float* qc;
-  unsigned* row_cnt;  // [rows]
-  unsigned* seq_cnt;  // [B]
+  unsigned* seq_cnt;  // [B] completion counters
   // outputs
   int32_t* accepted;
   int32_t* accept_len;
@@ -200,180 +211,251 @@ struct VocabArgs {
   int sampling;
 };
 
+constexpr int kStage = 1024;   // float4 partials staged by a finishing CTA
+constexpr int kMaxFinish = 64; // sequences one CTA can finish
+
+__device__ __forceinline__ long long c_first(long long u, const VocabArgs& a) { return u * a.V / a.chunk; }
+__device__ __forceinline__ long long c_last(long long u, const VocabArgs& a) {
+  return ((u + 1) * a.V - 1) / a.chunk;
+}
+// number of (row, CTA) partials of sequence b
+__device__ __forceinline__ unsigned seq_total(int b, const VocabArgs& a) {
+  const long long r0 = (long long)b * a.N, r1 = r0 + a.N - 1;
+  const long long distinct = c_last(r1, a) - c_first(r0, a) + 1;
+  const long long on_edge = r1 / a.L - r0 / a.L;
+  return (unsigned)(distinct + (r1 - r0) - on_edge);
+}
+
+struct EpiSmem {
+  int* par;
+  int* tok;
+  float* lse2;
+  float* lse2q;
+  int* am;
+  float4* stage;  // merge staging, reused as match / path afterwards
+  float* xc;
+  float* yc;
+};
+
+// Epilogue of sequence b, run by the CTA that wrote its last partial.
+template <typename T>
+__device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) {
+  __shared__ int s_bad, s_len, s_bonus;
+  const int N = a.N, V = a.V, tid = threadIdx.x;
+  const long long r0 = (long long)b * N;
+  const int nstage = N * a.mc;
+  const bool staged = nstage <= kStage;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  // one round trip: tree, drafted-token logits and (if they fit) every partial
+  for (int c = tid; c < N; c += blockDim.x) {
+    const int p = a.parent[r0 + c];
+    const int t = a.tokens[r0 + c];
+    sm.par[c] = p;
+    sm.tok[c] = t;
+    sm.xc[c] = __ldcg(a.xc + r0 + c);
+    if (a.sampling) sm.yc[c] = __ldcg(a.yc + r0 + c);
+    const bool ok = (c == 0) ? (p == -1) : (p >= 0 && p < c);
+    if (!ok) atomicOr(&s_bad, TV_DEV_BAD_TREE);
+    if (c > 0 && (t < 0 || t >= V)) atomicOr(&s_bad, TV_DEV_BAD_TOKEN);
+  }
+  const VocabPartial none{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+  for (int pass = 0; pass < (a.sampling ? 2 : 1); ++pass) {
+    const VocabPartial* src = (pass == 0 ? a.part : a.part_q) + r0 * a.mc;
+    if (staged) {
+      for (int i = tid; i < nstage; i += blockDim.x) sm.stage[i] = __ldcg(reinterpret_cast<const float4*>(src + i));
+      __syncthreads();
+    }
+    for (int u = tid; u < N; u += blockDim.x) {
+      const long long ug = r0 + u;
+      const int cover = (int)(c_last(ug, a) - c_first(ug, a) + 1);
+      VocabPartial r = none;
+      for (int k = 0; k < cover; ++k) {
+        const int i = u * a.mc + k;
+        const float4 v = staged ? sm.stage[i] : __ldcg(reinterpret_cast<const float4*>(src + i));
+        r = partial_merge(r, {v.x, v.y, v.z, __float_as_int(v.w)});
+      }
+      const float l2 = r.m + log2f(r.s);
+      if (pass == 0) {
+        sm.lse2[u] = l2;
+        sm.am[u] = r.ai;
+        if (a.sampling) a.lse2[ug] = l2;  // the sampling walk kernel reads these
+        if (a.row_lse) a.row_lse[ug] = l2 * kLn2;
+        if (a.row_argmax) a.row_argmax[ug] = r.ai;
+      } else {
+        sm.lse2q[u] = l2;
+        a.lse2_q[ug] = l2;
+      }
+    }
+    __syncthreads();
+  }
+  const int bad = s_bad;
+  if (bad && tid == 0) set_dev_status(a.dev_status, bad);
+  // drafted-token probabilities p_c = 2^(x[parent(c)][t_c] * c2 - lse2[parent(c)])
+  for (int c = tid; c < N; c += blockDim.x) {
+    float pv = __int_as_float(0x7fc00000), qv = pv;
+    if (c > 0 && !bad) {
+      const int u = sm.par[c];
+      pv = ptx::ex2(fmaf(sm.xc[c], a.c2, -sm.lse2[u]));
+      if (a.sampling) qv = ptx::ex2(fmaf(sm.yc[c], a.c2, -sm.lse2q[u]));
+    }
+    if (a.pc) a.pc[r0 + c] = pv;
+    if (a.qc) a.qc[r0 + c] = qv;
+    if (a.p_draft) a.p_draft[r0 + c] = pv;
+    if (a.q_draft) a.q_draft[r0 + c] = qv;
+  }
+  if (a.sampling) {
+    __syncthreads();
+    return;  // the sampling walk runs in its own kernel
+  }
+  // greedy walk: each node's child whose token equals the node's argmax (lowest index if
+  // several) is found in parallel, then the links are followed from the root
+  int* match = reinterpret_cast<int*>(sm.stage);
+  int* path = match + kMaxNodes;
+  for (int c = tid; c < N; c += blockDim.x) match[c] = 0x7fffffff;
+  __syncthreads();
+  if (!bad)
+    for (int c = 1 + tid; c < N; c += blockDim.x)
+      if (sm.tok[c] == sm.am[sm.par[c]]) atomicMin(&match[sm.par[c]], c);
+  __syncthreads();
+  if (tid == 0) {
+    int cur = 0, len = 0;
+    if (!bad) {
+      for (int nxt = match[0]; nxt != 0x7fffffff; nxt = match[cur]) {
+        path[len++] = nxt;
+        cur = nxt;
+      }
+    }
+    s_len = len;
+    s_bonus = bad ? -1 : sm.am[cur];
+  }
+  __syncthreads();
+  const int len = s_len;
+  for (int j = tid; j < N; j += blockDim.x) a.accepted[r0 + j] = j < len ? path[j] : -1;
+  if (tid == 0) {
+    a.accept_len[b] = len;
+    a.bonus[b] = s_bonus;
+  }
+  __syncthreads();
+}
+
 template <typename T>
 __device__ __forceinline__ float load_logit(const void* base, size_t idx) {
   return to_f32(reinterpret_cast<const T*>(base)[idx]);
 }
 
-// Per-sequence epilogue, run by the CTA that finished the sequence's last partial.
-// s_lse2 / s_lse2q / s_am hold the merged row statistics of sequence b.
-template <typename T>
-__device__ void sequence_epilogue(const VocabArgs& a, int b, const float* s_lse2, const float* s_lse2q,
-                                  const int* s_am) {
+template <typename T, bool kVec>
+__global__ void __launch_bounds__(256, 3) vocab_pass_kernel(VocabArgs a) {
+  __shared__ VocabPartial red[32];
   __shared__ int s_par[kMaxNodes];
   __shared__ int s_tok[kMaxNodes];
-  __shared__ int s_bad;
-  const int N = a.N, V = a.V;
-  if (threadIdx.x == 0) s_bad = 0;
-  __syncthreads();
-  for (int c = threadIdx.x; c < N; c += blockDim.x) {
-    int p = a.parent[(size_t)b * N + c];
-    int t = a.tokens[(size_t)b * N + c];
-    s_par[c] = p;
-    s_tok[c] = t;
-    bool ok = (c == 0) ? (p == -1) : (p >= 0 && p < c);
-    if (!ok) atomicOr(&s_bad, TV_DEV_BAD_TREE);
-    if (c > 0 && (t < 0 || t >= V)) atomicOr(&s_bad, TV_DEV_BAD_TOKEN);
-  }
-  __syncthreads();
-  const int bad = s_bad;
-  if (bad && threadIdx.x == 0) set_dev_status(a.dev_status, bad);
-  // drafted-token probabilities p_c = 2^(x[parent(c)][t_c] * c2 - lse2[parent(c)])
-  for (int c = threadIdx.x; c < N; c += blockDim.x) {
-    float pv = __int_as_float(0x7fc00000), qv = pv;
-    if (c > 0 && !bad) {
-      int u = s_par[c];
-      size_t idx = ((size_t)b * N + u) * (size_t)V + s_tok[c];
-      pv = ptx::ex2(fmaf(load_logit<T>(a.logits, idx), a.c2, -s_lse2[u]));
-      if (a.sampling) qv = ptx::ex2(fmaf(load_logit<T>(a.draft, idx), a.c2, -s_lse2q[u]));
-    }
-    if (a.pc) a.pc[(size_t)b * N + c] = pv;
-    if (a.qc) a.qc[(size_t)b * N + c] = qv;
-    if (a.p_draft) a.p_draft[(size_t)b * N + c] = pv;
-    if (a.q_draft) a.q_draft[(size_t)b * N + c] = qv;
-  }
-  if (a.sampling) return;  // the sampling walk runs in its own kernel
-  // greedy walk: first find, in parallel, each node's child whose token equals the
-  // node's argmax (lowest index if several), then follow those links from the root
-  __shared__ int s_match[kMaxNodes];
-  __shared__ int s_path[kMaxNodes];
-  __shared__ int s_len, s_bonus;
-  for (int c = threadIdx.x; c < N; c += blockDim.x) s_match[c] = 0x7fffffff;
-  __syncthreads();
-  if (!bad)
-    for (int c = 1 + threadIdx.x; c < N; c += blockDim.x)
-      if (s_tok[c] == s_am[s_par[c]]) atomicMin(&s_match[s_par[c]], c);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int cur = 0, len = 0;
-    if (!bad) {
-      for (int nxt = s_match[0]; nxt != 0x7fffffff; nxt = s_match[cur]) {
-        s_path[len++] = nxt;
-        cur = nxt;
-      }
-    }
-    s_len = len;
-    s_bonus = bad ? -1 : s_am[cur];
-  }
-  __syncthreads();
-  const int len = s_len;
-  for (int j = threadIdx.x; j < N; j += blockDim.x) a.accepted[(size_t)b * N + j] = j < len ? s_path[j] : -1;
-  if (threadIdx.x == 0) {
-    a.accept_len[b] = len;
-    a.bonus[b] = s_bonus;
-  }
-}
-
-template <typename T, bool kVec>
-__global__ void __launch_bounds__(256, 4) vocab_pass_kernel(VocabArgs a) {
-  __shared__ VocabPartial red[32];
-  __shared__ int s_flag;
   __shared__ float s_lse2[kMaxNodes];
   __shared__ float s_lse2q[kMaxNodes];
   __shared__ int s_am[kMaxNodes];
-  __shared__ float4 s_stage[kStagedParts];
-  const int split = blockIdx.x % a.splits;
-  const int row = blockIdx.x / a.splits;
-  const int b = row / a.N;
-  const int v0 = split * a.chunk;
-  const int v1 = min(a.V, v0 + a.chunk);
-  const size_t roff = (size_t)row * a.V;
-
-  RowAcc acc;
-  acc.init();
-  if (v0 < v1) scan_chunk<T, kVec>(reinterpret_cast<const T*>(a.logits) + roff, v0, v1, a.c2, acc);
-  VocabPartial p = block_merge({acc.mc, acc.s, acc.av, acc.ai}, red);
-  VocabPartial pq{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
-  if (a.sampling) {
-    RowAcc accq;
-    accq.init();
-    if (v0 < v1) scan_chunk<T, kVec>(reinterpret_cast<const T*>(a.draft) + roff, v0, v1, a.c2, accq);
-    pq = block_merge({accq.mc, accq.s, accq.av, accq.ai}, red);
-  }
-  if (threadIdx.x == 0) {
-    a.part[(size_t)row * a.splits + split] = p;
-    if (a.sampling) a.part_q[(size_t)row * a.splits + split] = pq;
-    __threadfence();
-    // one completion counter per sequence: the CTA that writes its last partial merges
-    const unsigned prev = atomicAdd(a.seq_cnt + b, 1u);
-    s_flag = (prev == (unsigned)(a.N * a.splits - 1));
-  }
-  __syncthreads();
-  if (!s_flag) return;
-  __threadfence();
-  // merge the splits of every row of sequence b.  All partials are fetched at once (one
-  // round trip), staged in shared memory, then merged per row.
-  const int npart = a.N * a.splits;
-  const size_t pbase = (size_t)b * a.N * a.splits;
-  const bool staged = npart <= kStagedParts;
-  const VocabPartial none{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
-  for (int pass = 0; pass < (a.sampling ? 2 : 1); ++pass) {
-    const VocabPartial* src = pass == 0 ? a.part : a.part_q;
-    if (staged) {
-      for (int i = threadIdx.x; i < npart; i += blockDim.x)
-        s_stage[i] = __ldcg(reinterpret_cast<const float4*>(src + pbase + i));
+  __shared__ float4 s_stage[kStage];
+  __shared__ float s_xc[kMaxNodes];
+  __shared__ float s_yc[kMaxNodes];
+  __shared__ int s_finish[kMaxFinish];
+  __shared__ int s_nfinish;
+  const int tid = threadIdx.x;
+  const long long cta = blockIdx.x;
+  const long long e0 = cta * a.chunk;
+  const long long e1 = min(a.E, e0 + a.chunk);
+  const long long u_begin = e0 / a.V, u_end = (e1 - 1) / a.V;
+  const T* X = reinterpret_cast<const T*>(a.logits);
+  const T* Y = reinterpret_cast<const T*>(a.draft);
+  int cur_seq = -1;
+  for (long long u = u_begin; u <= u_end; ++u) {
+    const int b = (int)(u / a.N);
+    const int ul = (int)(u - (long long)b * a.N);
+    if (b != cur_seq) {  // tree of this sequence, to find the children of each row
       __syncthreads();
-    }
-    for (int u = threadIdx.x; u < a.N; u += blockDim.x) {
-      VocabPartial r = none;
-      for (int s2 = 0; s2 < a.splits; ++s2) {
-        const int i = u * a.splits + s2;
-        const float4 v = staged ? s_stage[i] : __ldcg(reinterpret_cast<const float4*>(src + pbase + i));
-        r = partial_merge(r, {v.x, v.y, v.z, __float_as_int(v.w)});
+      for (int c = tid; c < a.N; c += blockDim.x) {
+        s_par[c] = a.parent[(size_t)b * a.N + c];
+        s_tok[c] = a.tokens[(size_t)b * a.N + c];
       }
-      const size_t r2 = (size_t)b * a.N + u;
-      const float l2 = r.m + log2f(r.s);
-      if (pass == 0) {
-        s_lse2[u] = l2;
-        s_am[u] = r.ai;
-        if (a.sampling) a.lse2[r2] = l2;  // the sampling walk kernel reads these
-        if (a.row_lse) a.row_lse[r2] = l2 * kLn2;
-        if (a.row_argmax) a.row_argmax[r2] = r.ai;
-      } else {
-        s_lse2q[u] = l2;
-        a.lse2_q[r2] = l2;
+      __syncthreads();
+      cur_seq = b;
+    }
+    const long long rowbase = u * a.V;
+    const int v0 = (int)(max(e0, rowbase) - rowbase);
+    const int v1 = (int)(min(e1, rowbase + a.V) - rowbase);
+    RowAcc acc;
+    acc.init();
+    scan_chunk<T, kVec>(X + rowbase, v0, v1, a.c2, acc);
+    const VocabPartial p = block_merge({acc.mc, acc.s, acc.av, acc.ai}, red);
+    VocabPartial pq{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+    if (a.sampling) {
+      RowAcc accq;
+      accq.init();
+      scan_chunk<T, kVec>(Y + rowbase, v0, v1, a.c2, accq);
+      pq = block_merge({accq.mc, accq.s, accq.av, accq.ai}, red);
+    }
+    const size_t slot = (size_t)u * a.mc + (size_t)(cta - c_first(u, a));
+    if (tid == 0) {
+      a.part[slot] = p;
+      if (a.sampling) a.part_q[slot] = pq;
+    }
+    // raw logits of the drafted children of row u whose tokens fall in [v0, v1)
+    for (int c = 1 + tid; c < a.N; c += blockDim.x) {
+      const int t = s_tok[c];
+      if (s_par[c] == ul && t >= v0 && t < v1) {
+        a.xc[(size_t)b * a.N + c] = to_f32(X[rowbase + t]);
+        if (a.sampling) a.yc[(size_t)b * a.N + c] = to_f32(Y[rowbase + t]);
       }
     }
-    __syncthreads();
   }
-  if (threadIdx.x == 0) a.seq_cnt[b] = 0;
+  __threadfence();
   __syncthreads();
-  sequence_epilogue<T>(a, b, s_lse2, s_lse2q, s_am);
+  if (tid == 0) {
+    // one atomic per sequence this CTA touched; the CTA completing a sequence finishes it
+    int nf = 0;
+    const int b_first = (int)(u_begin / a.N), b_last = (int)(u_end / a.N);
+    for (int b = b_first; b <= b_last; ++b) {
+      const long long lo = max(u_begin, (long long)b * a.N), hi = min(u_end, (long long)b * a.N + a.N - 1);
+      const unsigned mine = (unsigned)(hi - lo + 1);
+      const unsigned prev = atomicAdd(a.seq_cnt + b, mine);
+      if (prev + mine == seq_total(b, a) && nf < kMaxFinish) s_finish[nf++] = b;
+    }
+    s_nfinish = nf;
+  }
+  __syncthreads();
+  const int nf = s_nfinish;
+  if (nf == 0) return;
+  __threadfence();
+  EpiSmem sm{s_par, s_tok, s_lse2, s_lse2q, s_am, s_stage, s_xc, s_yc};
+  for (int i = 0; i < nf; ++i) {
+    const int b = s_finish[i];
+    if (tid == 0) a.seq_cnt[b] = 0;
+    sequence_epilogue<T>(a, b, sm);
+  }
 }
 
 // ------------------------------------------------------------------------------------
 // host side
 
-int verify_splits(int rows, int V) {
-  // One wave of 4 resident 256-thread CTAs per SM on 152 SMs, >= 4096 elements per CTA.
-  const int target = 152 * 4;
-  int s = target / rows;
-  int max_by_len = V / 4096;
-  if (max_by_len < 1) max_by_len = 1;
-  if (s > max_by_len) s = max_by_len;
-  if (s > 64) s = 64;
-  if (s < 1) s = 1;
-  return s;
+constexpr int kVocabThreads = 256;
+constexpr long long kMinChunk = 2048;  // elements
+constexpr int kGridCap = 4096;         // CTAs (bounds the workspace)
+constexpr int kRowsPerCta = 32;        // at most this many rows (+1) per CTA
+
+static long long gcd_ll(long long x, long long y) {
+  while (y) {
+    const long long t = x % y;
+    x = y;
+    y = t;
+  }
+  return x;
 }
 
-static int verify_chunk(int V, int splits) {
-  int c = (V + splits - 1) / splits;
-  return (c + 7) / 8 * 8;
-}
+// partial slots per row for any grid of at most kGridCap CTAs
+static int ws_mc(long long rows) { return (int)((kGridCap + rows - 1) / rows) + 2; }
+
+int verify_slots_per_row(int rows) { return ws_mc(rows); }
 
 size_t verify_ws_layout(int B, int N, int V, int sampling, VerifyWs* w) {
   const size_t rows = (size_t)B * N;
-  const int splits = verify_splits((int)rows, V);
+  const int mc = ws_mc((long long)rows);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -381,19 +463,52 @@ size_t verify_ws_layout(int B, int N, int V, int sampling, VerifyWs* w) {
     return o;
   };
   VerifyWs l;
-  l.splits = splits;
-  l.row_cnt = take(rows * 4);
+  l.splits = mc;
+  l.row_cnt = 0;  // counter region: [row_cnt, part)
   l.seq_cnt = take((size_t)B * 4);
-  l.part = take(rows * splits * sizeof(VocabPartial));
-  l.part_q = sampling ? take(rows * splits * sizeof(VocabPartial)) : 0;
+  l.part = take(rows * mc * sizeof(VocabPartial));
+  l.part_q = sampling ? take(rows * mc * sizeof(VocabPartial)) : 0;
   l.lse2 = take(rows * 4);
   l.lse2_q = take(rows * 4);
-  l.amax = take(rows * 4);
+  l.xc = take(rows * 4);  // raw drafted-token logits (target)
   l.pc = take(rows * 4);
   l.qc = take(rows * 4);
+  l.yc = take(rows * 4);    // raw drafted-token logits (draft)
   l.total = off;
   if (w) *w = l;
+  (void)V;
   return off;
+}
+
+template <typename T, bool kVec>
+static int resident_ctas() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152 * 4;
+  if (!cache[dev]) {
+    int per_sm = 0, sms = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vocab_pass_kernel<T, kVec>, kVocabThreads, 0);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = per_sm > 0 && sms > 0 ? per_sm * sms : 152 * 4;
+  }
+  return cache[dev];
+}
+
+template <typename T, bool kVec>
+static cudaError_t launch_vocab_t(VocabArgs a, cudaStream_t stream) {
+  const int resident = resident_ctas<T, kVec>();
+  const long long rows = (long long)a.B * a.N;
+  long long G = std::min<long long>({(long long)resident, (long long)kGridCap, (a.E + kMinChunk - 1) / kMinChunk});
+  G = std::max<long long>(G, (rows + kRowsPerCta - 1) / kRowsPerCta);  // bounds sequences finished per CTA
+  if (G < 1) G = 1;
+  long long chunk = (a.E + G - 1) / G;
+  chunk = (chunk + 7) / 8 * 8;
+  G = (a.E + chunk - 1) / chunk;
+  a.chunk = chunk;
+  a.L = chunk / gcd_ll((long long)a.V, chunk);
+  a.mc = (int)((a.V + chunk - 1) / chunk) + 1;
+  vocab_pass_kernel<T, kVec><<<(unsigned)G, kVocabThreads, 0, stream>>>(a);
+  return cudaSuccess;
 }
 
 cudaError_t launch_vocab_pass(const void* logits, const void* draft, const int32_t* parent,
@@ -409,17 +524,16 @@ cudaError_t launch_vocab_pass(const void* logits, const void* draft, const int32
   a.B = B;
   a.N = N;
   a.V = V;
-  a.splits = w.splits;
-  a.chunk = verify_chunk(V, w.splits);
+  a.E = (long long)B * N * V;
   a.c2 = kLog2e / temperature;
   a.part = reinterpret_cast<VocabPartial*>(ws + w.part);
   a.part_q = sampling ? reinterpret_cast<VocabPartial*>(ws + w.part_q) : nullptr;
   a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
   a.lse2_q = reinterpret_cast<float*>(ws + w.lse2_q);
-  a.amax = reinterpret_cast<int32_t*>(ws + w.amax);
+  a.xc = reinterpret_cast<float*>(ws + w.xc);
+  a.yc = reinterpret_cast<float*>(ws + w.yc);
   a.pc = reinterpret_cast<float*>(ws + w.pc);
   a.qc = reinterpret_cast<float*>(ws + w.qc);
-  a.row_cnt = reinterpret_cast<unsigned*>(ws + w.row_cnt);
   a.seq_cnt = reinterpret_cast<unsigned*>(ws + w.seq_cnt);
   a.accepted = accepted;
   a.accept_len = accept_len;
@@ -431,20 +545,14 @@ cudaError_t launch_vocab_pass(const void* logits, const void* draft, const int32
   a.dev_status = dev_status;
   a.sampling = sampling;
   const size_t esz = dtype == TV_BF16 ? 2 : 4;
-  bool vec = ((size_t)V * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(logits) % 16) == 0 &&
-             (!sampling || (reinterpret_cast<uintptr_t>(draft) % 16) == 0);
-  const unsigned grid = (unsigned)((size_t)B * N * w.splits);
-  if (dtype == TV_BF16) {
-    if (vec)
-      vocab_pass_kernel<uint16_t, true><<<grid, 256, 0, stream>>>(a);
-    else
-      vocab_pass_kernel<uint16_t, false><<<grid, 256, 0, stream>>>(a);
-  } else {
-    if (vec)
-      vocab_pass_kernel<float, true><<<grid, 256, 0, stream>>>(a);
-    else
-      vocab_pass_kernel<float, false><<<grid, 256, 0, stream>>>(a);
-  }
+  const bool vec = ((size_t)V * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(logits) % 16) == 0 &&
+                   (!sampling || (reinterpret_cast<uintptr_t>(draft) % 16) == 0);
+  cudaError_t e;
+  if (dtype == TV_BF16)
+    e = vec ? launch_vocab_t<uint16_t, true>(a, stream) : launch_vocab_t<uint16_t, false>(a, stream);
+  else
+    e = vec ? launch_vocab_t<float, true>(a, stream) : launch_vocab_t<float, false>(a, stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
