@@ -8,7 +8,9 @@
 // from the root down, so the result is reproducible bit for bit.
 //
 // Result: the first M = budget-1 candidates in the order (s desc, depth asc, rank path
-// lexicographic asc), numbered in that order.  One CTA per sequence:
+// lexicographic asc), numbered in that order.  One CTA per sequence.  Budgets up to 128
+// rows: one warp runs the best-first search below with the whole frontier in registers
+// (a pop is a warp-wide redux minimum).  Larger budgets:
 //   1. a lower bound tau on the M-th best score: the M-th best score among the
 //      "one-deviation" candidates (prefixes of the all-rank-0 path with at most one
 //      position replaced by a higher rank) - they are real candidates, so at least M
@@ -152,15 +154,137 @@ __device__ int select_heap_warp(const float* sm_marg, const int* sm_tok, int d, 
 }
 
 // ------------------------------------------------------------------------------------
+// small budgets: best-first search by one warp with the frontier in registers
+// (slot g of the frontier lives in lane g % 32, register slot g / 32)
+
+constexpr int kRegSlots = 4;                 // frontier entries per lane
+constexpr int kRegMaxM = 32 * kRegSlots - 1;  // pops whose frontier fits (<= 1 + pops entries)
+
+__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+struct RegSlot {
+  uint64_t k0 = ~0ull, k1 = 0, k2 = 0;  // empty slot: the largest key
+  int par = 0;
+  float psc = 0.f;
+};
+
+__device__ __forceinline__ void slot_best(const RegSlot& sl, int j, int& bj, uint64_t& b0, uint64_t& b1, uint64_t& b2,
+                                          int& bpar, float& bpsc) {
+  if (key_less(sl.k0, sl.k1, sl.k2, b0, b1, b2)) {
+    bj = j;
+    b0 = sl.k0;
+    b1 = sl.k1;
+    b2 = sl.k2;
+    bpar = sl.par;
+    bpsc = sl.psc;
+  }
+}
+
+__device__ __forceinline__ void slot_put(RegSlot& sl, bool doit, uint64_t k0, uint64_t k1, uint64_t k2, int par,
+                                         float psc) {
+  if (doit) {
+    sl.k0 = k0;
+    sl.k1 = k1;
+    sl.k2 = k2;
+    sl.par = par;
+    sl.psc = psc;
+  }
+}
+
+__device__ int select_heap_regs(const float* sm_marg, const int* sm_tok, int d, int K, int budget, int32_t* o_par,
+                                int32_t* o_tok, int32_t* o_dep, float* o_sc) {
+  static_assert(kRegSlots == 4, "four named register slots");
+  const int lane = threadIdx.x & 31;
+  RegSlot q0, q1, q2, q3;
+  int nalloc = 0;
+  if (d >= 1 && K >= 1 && budget > 1) {
+    if (lane == 0) {
+      q0.k0 = make_k0(__fmul_rn(1.f, sm_marg[0]), 1);
+      q0.psc = 1.f;
+    }
+    nalloc = 1;
+  }
+  int n = 1;
+  while (n < budget) {
+    // lane-local best of the register slots
+    int bj = 0, bpar = q0.par;
+    uint64_t b0 = q0.k0, b1 = q0.k1, b2 = q0.k2;
+    float bpsc = q0.psc;
+    slot_best(q1, 1, bj, b0, b1, b2, bpar, bpsc);
+    slot_best(q2, 2, bj, b0, b1, b2, bpar, bpsc);
+    slot_best(q3, 3, bj, b0, b1, b2, bpar, bpsc);
+    // warp minimum: score word, then depth word, then (rare) the rank path
+    const uint32_t hi = (uint32_t)(b0 >> 32);
+    const uint32_t mhi = warp_min_u32(hi);
+    if (mhi == 0xFFFFFFFFu) break;  // frontier empty
+    const uint32_t lo = hi == mhi ? (uint32_t)b0 : 0xFFFFFFFFu;
+    const uint32_t mlo = warp_min_u32(lo);
+    const unsigned cand = __ballot_sync(0xffffffffu, hi == mhi && (uint32_t)b0 == mlo);
+    int win = __ffs(cand) - 1;
+    if (__popc(cand) > 1) {  // equal score and depth: smallest rank path among the candidates
+      for (unsigned rest = cand & (cand - 1); rest; rest &= rest - 1) {
+        const int other = __ffs(rest) - 1;
+        const uint64_t w1 = __shfl_sync(0xffffffffu, b1, win), w2 = __shfl_sync(0xffffffffu, b2, win);
+        const uint64_t o1 = __shfl_sync(0xffffffffu, b1, other), o2 = __shfl_sync(0xffffffffu, b2, other);
+        if (o1 < w1 || (o1 == w1 && o2 < w2)) win = other;
+      }
+    }
+    // the popped entry, broadcast from the winning lane
+    const uint64_t p0 = ((uint64_t)mhi << 32) | mlo;
+    const uint64_t p1 = __shfl_sync(0xffffffffu, b1, win);
+    const uint64_t p2 = __shfl_sync(0xffffffffu, b2, win);
+    const int ppar = __shfl_sync(0xffffffffu, bpar, win);
+    const float ppsc = __shfl_sync(0xffffffffu, bpsc, win);
+    const int pslot = __shfl_sync(0xffffffffu, bj, win);
+    const int dep = (int)(p0 & 0xFFFFFFFFu);
+    const float sc = k0_score(p0);
+    const int r = path_rank(p1, p2, dep - 1);
+    if (lane == 0) {
+      o_par[n] = ppar;
+      o_tok[n] = sm_tok[(dep - 1) * K + r];
+      o_dep[n] = dep;
+      o_sc[n] = sc;
+    }
+    // first child (rank 0 at the next position) replaces the popped slot
+    const uint64_t c0 = dep < d ? make_k0(__fmul_rn(sc, sm_marg[dep * K]), dep + 1) : ~0ull;
+    const bool mine = lane == win;
+    slot_put(q0, mine && pslot == 0, c0, p1, p2, n, sc);
+    slot_put(q1, mine && pslot == 1, c0, p1, p2, n, sc);
+    slot_put(q2, mine && pslot == 2, c0, p1, p2, n, sc);
+    slot_put(q3, mine && pslot == 3, c0, p1, p2, n, sc);
+    // next sibling under the same parent goes to a fresh slot
+    if (r + 1 < K) {
+      uint64_t s1 = p1, s2 = p2;
+      path_bump(s1, s2, dep - 1);
+      const uint64_t s0 = make_k0(__fmul_rn(ppsc, sm_marg[(dep - 1) * K + r + 1]), dep);
+      const int g = nalloc++;
+      const bool here = lane == (g & 31);
+      slot_put(q0, here && (g >> 5) == 0, s0, s1, s2, ppar, ppsc);
+      slot_put(q1, here && (g >> 5) == 1, s0, s1, s2, ppar, ppsc);
+      slot_put(q2, here && (g >> 5) == 2, s0, s1, s2, ppar, ppsc);
+      slot_put(q3, here && (g >> 5) == 3, s0, s1, s2, ppar, ppsc);
+    }
+    ++n;
+  }
+  return n;
+}
+
+// ------------------------------------------------------------------------------------
 // block helpers (kSelThreads threads)
 
-// k-th largest (1-based, k <= n) of vals[0..n) by 8-bit radix select with warp-aggregated
-// histogram updates; every thread returns it.
-__device__ uint32_t block_kth_largest(const uint32_t* vals, int n, int k, int* hist, int* bcast) {
+// Radix select of the k-th largest (1-based, k <= n) of vals[0..n) with warp-aggregated
+// histogram updates.  With min_shift = 0 the exact value is returned; with a larger
+// min_shift the passes stop early and the result is the k-th largest value with its low
+// min_shift bits cleared (a lower bound).  Every thread returns the result.
+__device__ uint32_t block_kth_largest(const uint32_t* vals, int n, int k, int* hist, int* bcast, int min_shift = 0) {
   const int lane = threadIdx.x & 31;
   uint32_t prefix = 0, mask = 0;
   int want = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  for (int shift = 24; shift >= min_shift; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     for (int base = 0; base < n; base += blockDim.x) {
@@ -230,65 +354,59 @@ struct SelSmem {
   int* pos;   // entry -> position in the output (0: not taken)
 };
 
-// Expand every candidate with s >= tau, level by level (one barrier per level; slots come
-// from one shared counter, one atomic per warp).  Returns the entry count, or -1 if more
-// than kSelCap would be needed; then *complete = entries of the fully expanded levels.
+// Expand every candidate with s >= tau.  Each candidate lies on exactly one "run": a node
+// reached by a rank >= 1 edge (or the root's rank-0 child), followed by its rank-0
+// descendants.  Step 0 starts the runs at the root's children; step i+1 starts runs at
+// the rank >= 1 children of every node made in step i.  A run is followed by one thread
+// (its scores are a running fp32 product, exactly the left-to-right path product), so the
+// number of steps is 1 + the largest number of rank >= 1 edges on a kept path.
+// Returns the entry count, or -1 if more than kSelCap would be needed; then *complete =
+// entries made by the steps that finished.
 __device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int* s_count, int* s_over,
                                 int* complete) {
-  const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     *s_count = 0;
     *s_over = 0;
   }
   __syncthreads();
-  int lo = 0, hi = 0;  // current level = entries [lo, hi); level 0 is the virtual root
-  for (int k = 1; k <= d; ++k) {
-    const int nparents = (k == 1) ? 1 : hi - lo;
-    if (nparents <= 0) break;
-    const float* mk = sm.marg + (k - 1) * K;
-    for (int base = 0; base < nparents; base += blockDim.x) {
-      const int pi = base + threadIdx.x;
-      int cnt = 0;
-      float ps = 1.f;
-      int pe = -1;
-      if (pi < nparents) {
-        pe = (k == 1) ? -1 : lo + pi;
-        ps = (k == 1) ? 1.f : k0_score(sm.k0[pe]);
-        // marginals are sorted: the qualifying children are a prefix of the ranks
-        for (int j0 = 0; j0 < K; j0 += 4) {
-          float m4[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) m4[q] = j0 + q < K ? mk[j0 + q] : -1.f;
-          int c4 = 0;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) c4 += (m4[q] >= 0.f && __fmul_rn(ps, m4[q]) >= tau) ? 1 : 0;
-          cnt += c4;
-          if (c4 < 4) break;
+  int lo = 0, hi = 0;  // entries made by the previous step; step 0 expands the virtual root
+  for (int step = 0;; ++step) {
+    const int nsrc = step == 0 ? 1 : hi - lo;
+    if (nsrc <= 0) break;
+    for (int i = threadIdx.x; i < nsrc; i += blockDim.x) {
+      const int pe = step == 0 ? -1 : lo + i;
+      const float ps = step == 0 ? 1.f : k0_score(sm.k0[pe]);
+      const int dep = step == 0 ? 0 : (int)(sm.k0[pe] & 0xFFFFFFFFu);  // children sit at position dep
+      if (dep >= d) continue;
+      const uint64_t pk1 = step == 0 ? 0ull : sm.k1[pe];
+      const uint64_t pk2 = step == 0 ? 0ull : sm.k2[pe];
+      const float* mrow = sm.marg + dep * K;
+      for (int r = step == 0 ? 0 : 1; r < K; ++r) {
+        const float s0 = __fmul_rn(ps, mrow[r]);
+        if (s0 < tau) break;  // ranks are sorted: no later rank qualifies
+        // run length: the rank-r child, then rank-0 descendants while s >= tau
+        int len = 1;
+        float sc = s0;
+        while (dep + len < d) {
+          const float nx = __fmul_rn(sc, sm.marg[(dep + len) * K]);
+          if (nx < tau) break;
+          sc = nx;
+          ++len;
         }
-      }
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int wtot = __shfl_sync(0xffffffffu, incl, 31);
-      int wbase = 0;
-      if (lane == 31 && wtot > 0) wbase = atomicAdd(s_count, wtot);
-      wbase = __shfl_sync(0xffffffffu, wbase, 31);
-      if (wtot > 0 && wbase + wtot > kSelCap) {
-        if (lane == 0) *s_over = 1;
-      } else if (cnt > 0) {
-        const uint64_t pk1 = (k == 1) ? 0ull : sm.k1[pe];
-        const uint64_t pk2 = (k == 1) ? 0ull : sm.k2[pe];
-        const int e0 = wbase + incl - cnt;
-        for (int j = 0; j < cnt; ++j) {
-          uint64_t c1 = pk1, c2 = pk2;
-          path_set(c1, c2, k - 1, j);
-          sm.k0[e0 + j] = make_k0(__fmul_rn(ps, mk[j]), k);
-          sm.k1[e0 + j] = c1;
-          sm.k2[e0 + j] = c2;
-          sm.par[e0 + j] = pe;
+        const int base = atomicAdd(s_count, len);
+        if (base + len > kSelCap) {
+          *s_over = 1;
+          break;
+        }
+        uint64_t c1 = pk1, c2 = pk2;
+        path_set(c1, c2, dep, r);
+        sc = s0;
+        for (int q = 0; q < len; ++q) {
+          if (q > 0) sc = __fmul_rn(sc, sm.marg[(dep + q) * K]);
+          sm.k0[base + q] = make_k0(sc, dep + q + 1);
+          sm.k1[base + q] = c1;
+          sm.k2[base + q] = c2;
+          sm.par[base + q] = q == 0 ? pe : base + q - 1;
         }
       }
     }
@@ -366,8 +484,9 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_c
   }
   const int nf1 = min(d + (rmax - 1) * (d * (d + 1) / 2), 2 * kSelCap);
   __syncthreads();
+  // a lower bound within 2^-7 (relative) of the M-th best one-deviation score
   float tau = 0.f;
-  if (nf1 >= M) tau = __uint_as_float(block_kth_largest(f1, nf1, M, hist, bcast));
+  if (nf1 >= M) tau = __uint_as_float(block_kth_largest(f1, nf1, M, hist, bcast, 16));
   __syncthreads();
   // 2. expansion; one retry with tau raised to the M-th best of the complete levels
   int complete = 0;
@@ -489,6 +608,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
   }
   if (M <= 0) {
     if (tid == 0) s_nout = 1;
+  } else if (M <= kRegMaxM) {
+    if (tid < 32) {
+      const int r = select_heap_regs(sm.marg, sm.tok, d, K, budget, o_par, o_tok, o_dep, o_sc);
+      if (tid == 0) s_nout = r;
+    }
   } else if (M <= kSelCap / 2) {
     const int r = select_threshold(sm, d, K, M, &s_count, &s_over, hist, bcast, o_par, o_tok, o_dep, o_sc);
     if (tid == 0) s_nout = r;

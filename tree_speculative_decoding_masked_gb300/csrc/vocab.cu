@@ -152,7 +152,7 @@ template <typename T, bool kVec>
 __device__ __forceinline__ void scan_chunk(const T* __restrict__ row, int v0, int v1, float c2, RowAcc& acc) {
   if constexpr (kVec) {
     constexpr int kN = Vec16<T>::kN;
-    constexpr int kInFlight = 4;
+    constexpr int kInFlight = 8;
     const int nvec = (v1 - v0) / kN;
     const uint4* p = reinterpret_cast<const uint4*>(row + v0);
     const int stride = blockDim.x;
@@ -345,7 +345,7 @@ __device__ __forceinline__ float load_logit(const void* base, size_t idx) {
 }
 
 template <typename T, bool kVec>
-__global__ void __launch_bounds__(256, 3) vocab_pass_kernel(VocabArgs a) {
+__global__ void __launch_bounds__(512, 1) vocab_pass_kernel(VocabArgs a) {
   __shared__ VocabPartial red[32];
   __shared__ int s_par[kMaxNodes];
   __shared__ int s_tok[kMaxNodes];
@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(256, 3) vocab_pass_kernel(VocabArgs a) {
 // ------------------------------------------------------------------------------------
 // host side
 
-constexpr int kVocabThreads = 256;
+constexpr int kVocabThreads = 512;
 constexpr long long kMinChunk = 2048;  // elements
 constexpr int kGridCap = 4096;         // CTAs (bounds the workspace)
 constexpr int kRowsPerCta = 32;        // at most this many rows (+1) per CTA
