@@ -8,9 +8,8 @@
 // from the root down, so the result is reproducible bit for bit.
 //
 // Result: the first M = budget-1 candidates in the order (s desc, depth asc, rank path
-// lexicographic asc), numbered in that order.  One CTA per sequence.  Budgets up to 128
-// rows: one warp runs the best-first search below with the whole frontier in registers
-// (a pop is a warp-wide redux minimum).  Larger budgets:
+// lexicographic asc), numbered in that order.  One CTA per sequence; the work is split
+// into a few block-wide phases rather than budget-many serial steps:
 //   1. a lower bound tau on the M-th best score: the M-th best score among the
 //      "one-deviation" candidates (prefixes of the all-rank-0 path with at most one
 //      position replaced by a higher rank) - they are real candidates, so at least M
@@ -149,126 +148,6 @@ __device__ int select_heap_warp(const float* sm_marg, const int* sm_tok, int d, 
     F = __shfl_sync(0xffffffffu, F, 0);
     ++n;
     __syncwarp();
-  }
-  return n;
-}
-
-// ------------------------------------------------------------------------------------
-// small budgets: best-first search by one warp with the frontier in registers
-// (slot g of the frontier lives in lane g % 32, register slot g / 32)
-
-constexpr int kRegSlots = 4;                 // frontier entries per lane
-constexpr int kRegMaxM = 32 * kRegSlots - 1;  // pops whose frontier fits (<= 1 + pops entries)
-
-__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
-  uint32_t r;
-  asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
-  return r;
-}
-
-struct RegSlot {
-  uint64_t k0 = ~0ull, k1 = 0, k2 = 0;  // empty slot: the largest key
-  int par = 0;
-  float psc = 0.f;
-};
-
-__device__ __forceinline__ void slot_best(const RegSlot& sl, int j, int& bj, uint64_t& b0, uint64_t& b1, uint64_t& b2,
-                                          int& bpar, float& bpsc) {
-  if (key_less(sl.k0, sl.k1, sl.k2, b0, b1, b2)) {
-    bj = j;
-    b0 = sl.k0;
-    b1 = sl.k1;
-    b2 = sl.k2;
-    bpar = sl.par;
-    bpsc = sl.psc;
-  }
-}
-
-__device__ __forceinline__ void slot_put(RegSlot& sl, bool doit, uint64_t k0, uint64_t k1, uint64_t k2, int par,
-                                         float psc) {
-  if (doit) {
-    sl.k0 = k0;
-    sl.k1 = k1;
-    sl.k2 = k2;
-    sl.par = par;
-    sl.psc = psc;
-  }
-}
-
-__device__ int select_heap_regs(const float* sm_marg, const int* sm_tok, int d, int K, int budget, int32_t* o_par,
-                                int32_t* o_tok, int32_t* o_dep, float* o_sc) {
-  static_assert(kRegSlots == 4, "four named register slots");
-  const int lane = threadIdx.x & 31;
-  RegSlot q0, q1, q2, q3;
-  int nalloc = 0;
-  if (d >= 1 && K >= 1 && budget > 1) {
-    if (lane == 0) {
-      q0.k0 = make_k0(__fmul_rn(1.f, sm_marg[0]), 1);
-      q0.psc = 1.f;
-    }
-    nalloc = 1;
-  }
-  int n = 1;
-  while (n < budget) {
-    // lane-local best of the register slots
-    int bj = 0, bpar = q0.par;
-    uint64_t b0 = q0.k0, b1 = q0.k1, b2 = q0.k2;
-    float bpsc = q0.psc;
-    slot_best(q1, 1, bj, b0, b1, b2, bpar, bpsc);
-    slot_best(q2, 2, bj, b0, b1, b2, bpar, bpsc);
-    slot_best(q3, 3, bj, b0, b1, b2, bpar, bpsc);
-    // warp minimum: score word, then depth word, then (rare) the rank path
-    const uint32_t hi = (uint32_t)(b0 >> 32);
-    const uint32_t mhi = warp_min_u32(hi);
-    if (mhi == 0xFFFFFFFFu) break;  // frontier empty
-    const uint32_t lo = hi == mhi ? (uint32_t)b0 : 0xFFFFFFFFu;
-    const uint32_t mlo = warp_min_u32(lo);
-    const unsigned cand = __ballot_sync(0xffffffffu, hi == mhi && (uint32_t)b0 == mlo);
-    int win = __ffs(cand) - 1;
-    if (__popc(cand) > 1) {  // equal score and depth: smallest rank path among the candidates
-      for (unsigned rest = cand & (cand - 1); rest; rest &= rest - 1) {
-        const int other = __ffs(rest) - 1;
-        const uint64_t w1 = __shfl_sync(0xffffffffu, b1, win), w2 = __shfl_sync(0xffffffffu, b2, win);
-        const uint64_t o1 = __shfl_sync(0xffffffffu, b1, other), o2 = __shfl_sync(0xffffffffu, b2, other);
-        if (o1 < w1 || (o1 == w1 && o2 < w2)) win = other;
-      }
-    }
-    // the popped entry, broadcast from the winning lane
-    const uint64_t p0 = ((uint64_t)mhi << 32) | mlo;
-    const uint64_t p1 = __shfl_sync(0xffffffffu, b1, win);
-    const uint64_t p2 = __shfl_sync(0xffffffffu, b2, win);
-    const int ppar = __shfl_sync(0xffffffffu, bpar, win);
-    const float ppsc = __shfl_sync(0xffffffffu, bpsc, win);
-    const int pslot = __shfl_sync(0xffffffffu, bj, win);
-    const int dep = (int)(p0 & 0xFFFFFFFFu);
-    const float sc = k0_score(p0);
-    const int r = path_rank(p1, p2, dep - 1);
-    if (lane == 0) {
-      o_par[n] = ppar;
-      o_tok[n] = sm_tok[(dep - 1) * K + r];
-      o_dep[n] = dep;
-      o_sc[n] = sc;
-    }
-    // first child (rank 0 at the next position) replaces the popped slot
-    const uint64_t c0 = dep < d ? make_k0(__fmul_rn(sc, sm_marg[dep * K]), dep + 1) : ~0ull;
-    const bool mine = lane == win;
-    slot_put(q0, mine && pslot == 0, c0, p1, p2, n, sc);
-    slot_put(q1, mine && pslot == 1, c0, p1, p2, n, sc);
-    slot_put(q2, mine && pslot == 2, c0, p1, p2, n, sc);
-    slot_put(q3, mine && pslot == 3, c0, p1, p2, n, sc);
-    // next sibling under the same parent goes to a fresh slot
-    if (r + 1 < K) {
-      uint64_t s1 = p1, s2 = p2;
-      path_bump(s1, s2, dep - 1);
-      const uint64_t s0 = make_k0(__fmul_rn(ppsc, sm_marg[(dep - 1) * K + r + 1]), dep);
-      const int g = nalloc++;
-      const bool here = lane == (g & 31);
-      slot_put(q0, here && (g >> 5) == 0, s0, s1, s2, ppar, ppsc);
-      slot_put(q1, here && (g >> 5) == 1, s0, s1, s2, ppar, ppsc);
-      slot_put(q2, here && (g >> 5) == 2, s0, s1, s2, ppar, ppsc);
-      slot_put(q3, here && (g >> 5) == 3, s0, s1, s2, ppar, ppsc);
-    }
-    ++n;
   }
   return n;
 }
@@ -484,9 +363,8 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_c
   }
   const int nf1 = min(d + (rmax - 1) * (d * (d + 1) / 2), 2 * kSelCap);
   __syncthreads();
-  // a lower bound within 2^-7 (relative) of the M-th best one-deviation score
   float tau = 0.f;
-  if (nf1 >= M) tau = __uint_as_float(block_kth_largest(f1, nf1, M, hist, bcast, 16));
+  if (nf1 >= M) tau = __uint_as_float(block_kth_largest(f1, nf1, M, hist, bcast));
   __syncthreads();
   // 2. expansion; one retry with tau raised to the M-th best of the complete levels
   int complete = 0;
@@ -608,11 +486,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
   }
   if (M <= 0) {
     if (tid == 0) s_nout = 1;
-  } else if (M <= kRegMaxM) {
-    if (tid < 32) {
-      const int r = select_heap_regs(sm.marg, sm.tok, d, K, budget, o_par, o_tok, o_dep, o_sc);
-      if (tid == 0) s_nout = r;
-    }
   } else if (M <= kSelCap / 2) {
     const int r = select_threshold(sm, d, K, M, &s_count, &s_over, hist, bcast, o_par, o_tok, o_dep, o_sc);
     if (tid == 0) s_nout = r;

@@ -146,32 +146,42 @@ __device__ __forceinline__ VocabPartial block_merge(VocabPartial p, VocabPartial
   return r;
 }
 
-// Accumulate x[v0, v1) of one row into `acc`: 16-byte streaming loads, eight in flight
-// per thread, when kVec; scalar loads otherwise.
+// Accumulate x[v0, v1) of one row into `acc`: 16-byte streaming loads in batches of six
+// per thread, the next batch issued before the current one is processed (kVec); scalar
+// loads otherwise.
 template <typename T, bool kVec>
 __device__ __forceinline__ void scan_chunk(const T* __restrict__ row, int v0, int v1, float c2, RowAcc& acc) {
   if constexpr (kVec) {
     constexpr int kN = Vec16<T>::kN;
-    constexpr int kInFlight = 8;
+    constexpr int kBatch = 6;  // 16-byte loads per batch; batches A and B alternate
     const int nvec = (v1 - v0) / kN;
     const uint4* p = reinterpret_cast<const uint4*>(row + v0);
     const int stride = blockDim.x;
-    for (int j = threadIdx.x; j < nvec; j += kInFlight * stride) {
-      uint4 u[kInFlight];
+    const int step = kBatch * stride;
+    uint4 A[kBatch], B[kBatch];
+    auto load = [&](uint4* buf, int j) {
 #pragma unroll
-      for (int k = 0; k < kInFlight; ++k) {
-        const int idx = j + k * stride;
-        if (idx < nvec) u[k] = __ldcs(p + idx);
-      }
+      for (int k = 0; k < kBatch; ++k)
+        if (j + k * stride < nvec) buf[k] = __ldcs(p + j + k * stride);
+    };
+    auto consume = [&](const uint4* buf, int j) {
 #pragma unroll
-      for (int k = 0; k < kInFlight; ++k) {
+      for (int k = 0; k < kBatch; ++k) {
         const int idx = j + k * stride;
         if (idx < nvec) {
           float x[kN];
-          unpack16<T>(u[k], x);
+          unpack16<T>(buf[k], x);
           acc.template push<kN>(x, v0 + idx * kN, c2);
         }
       }
+    };
+    int j = threadIdx.x;
+    load(A, j);
+    for (; j < nvec; j += 2 * step) {
+      load(B, j + step);
+      consume(A, j);
+      load(A, j + 2 * step);
+      consume(B, j + step);
     }
     for (int v = v0 + nvec * kN + threadIdx.x; v < v1; v += stride) acc.push1(to_f32(row[v]), v, c2);
   } else {
