@@ -382,22 +382,27 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_c
   // 3. order: the output position of entry e is 1 + its rank in the selection order
   if (n <= kRankDirect) {
     for (int e = t; e < n; e += blockDim.x) {
-      const uint64_t a0 = sm.k0[e], a1 = sm.k1[e], a2 = sm.k2[e];
-      int rank = 0;
+      // branch-free count on the (score, depth) word; exact ties are resolved on the
+      // rank path only when they occur
+      const uint64_t a0 = sm.k0[e];
+      int less = 0, eq = 0;
       int j = 0;
-      for (; j + 8 <= n; j += 8) {
-        uint64_t c0[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) c0[q] = sm.k0[j + q];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (c0[q] < a0)
-            ++rank;
-          else if (c0[q] == a0 && key_less(c0[q], sm.k1[j + q], sm.k2[j + q], a0, a1, a2))
-            ++rank;
-        }
+      const ulonglong2* k0v = reinterpret_cast<const ulonglong2*>(sm.k0);
+      for (; j + 2 <= n; j += 2) {
+        const ulonglong2 c = k0v[j >> 1];
+        less += (c.x < a0) + (c.y < a0);
+        eq += (c.x == a0) + (c.y == a0);
       }
-      for (; j < n; ++j) rank += key_less(sm.k0[j], sm.k1[j], sm.k2[j], a0, a1, a2) ? 1 : 0;
+      if (j < n) {
+        less += sm.k0[j] < a0;
+        eq += sm.k0[j] == a0;
+      }
+      int rank = less;
+      if (eq > 1) {
+        const uint64_t a1 = sm.k1[e], a2 = sm.k2[e];
+        for (int q = 0; q < n; ++q)
+          if (sm.k0[q] == a0 && key_less(a0, sm.k1[q], sm.k2[q], a0, a1, a2)) ++rank;
+      }
       sm.pos[e] = rank < take ? rank + 1 : 0;
       if (rank < take) sm.idx[rank] = e;
     }

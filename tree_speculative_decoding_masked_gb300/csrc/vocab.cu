@@ -442,6 +442,161 @@ __global__ void __launch_bounds__(512, 1) vocab_pass_kernel(VocabArgs a) {
 }
 
 // ------------------------------------------------------------------------------------
+// TMA variant (16-byte aligned rows): each CTA bulk-copies its contiguous byte range into
+// a ring of shared-memory stages (all stages in flight at once) and reduces from there.
+
+constexpr int kTmaThreads = 512;
+constexpr int kPieceBytes = 16384;  // per array per stage
+constexpr int kRingBytes = 196608;  // 12 stages (greedy) or 6 double stages (sampling)
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          ptx::smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(ptx::smem_addr(bar))
+      : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArgs a) {
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ VocabPartial red[32];
+  __shared__ uint64_t full[12];
+  __shared__ int s_par[kMaxNodes];
+  __shared__ int s_tok[kMaxNodes];
+  __shared__ int s_finish[kMaxFinish];
+  __shared__ int s_nfinish;
+  __shared__ int s_abort;
+  constexpr int kE = kPieceBytes / (int)sizeof(T);  // elements per piece
+  const int tid = threadIdx.x;
+  const int arrays = a.sampling ? 2 : 1;
+  const int nst = kRingBytes / (kPieceBytes * arrays);
+  const long long cta = blockIdx.x;
+  const long long e0 = cta * a.chunk;
+  const long long e1 = min(a.E, e0 + a.chunk);
+  const int npieces = (int)((e1 - e0 + kE - 1) / kE);
+  const T* X = reinterpret_cast<const T*>(a.logits);
+  const T* Y = reinterpret_cast<const T*>(a.draft);
+  auto issue = [&](int piece) {
+    const int st = piece % nst;
+    const long long q0 = e0 + (long long)piece * kE;
+    const uint32_t bytes = (uint32_t)((min(e1, q0 + kE) - q0) * (long long)sizeof(T));
+    ptx::mbar_arrive_expect_tx(&full[st], bytes * arrays);
+    unsigned char* dst = ring + (size_t)st * kPieceBytes * arrays;
+    bulk_g2s(dst, X + q0, bytes, &full[st]);
+    if (arrays == 2) bulk_g2s(dst + kPieceBytes, Y + q0, bytes, &full[st]);
+  };
+  if (tid == 0) {
+    for (int st = 0; st < nst; ++st) ptx::mbar_init(&full[st], 1);
+    s_abort = 0;
+    ptx::fence_mbar_init();
+    for (int pc = 0; pc < min(nst, npieces); ++pc) issue(pc);
+  }
+  __syncthreads();
+  RowAcc acc, accq;
+  acc.init();
+  accq.init();
+  int cur_seq = -1;
+  for (int pc = 0; pc < npieces; ++pc) {
+    const int st = pc % nst;
+    const long long q0 = e0 + (long long)pc * kE;
+    const long long q1 = min(e1, q0 + kE);
+    bool ok = ptx::mbar_wait(&full[st], (pc / nst) & 1, &s_abort);
+    (void)ok;
+    const unsigned char* stage = ring + (size_t)st * kPieceBytes * arrays;
+    const T* xs = reinterpret_cast<const T*>(stage);
+    const T* ys = reinterpret_cast<const T*>(stage + kPieceBytes);
+    for (long long u = q0 / a.V; u <= (q1 - 1) / a.V; ++u) {
+      const long long rowbase = u * a.V;
+      const long long x0 = max(q0, rowbase), x1 = min(q1, rowbase + a.V);
+      // 16-byte vectors of the segment [x0, x1) (both ends are multiples of 8 elements)
+      const int v_lo = (int)((x0 - q0) * (long long)sizeof(T) / 16);
+      const int v_hi = (int)((x1 - q0) * (long long)sizeof(T) / 16);
+      constexpr int kN = Vec16<T>::kN;
+      for (int j = v_lo + tid; j < v_hi; j += kTmaThreads) {
+        const int col = (int)(q0 - rowbase) + j * kN;  // column of the first element
+        float xv[kN];
+        unpack16<T>(reinterpret_cast<const uint4*>(stage)[j], xv);
+        acc.template push<kN>(xv, col, a.c2);
+        if (arrays == 2) {
+          float yv[kN];
+          unpack16<T>(reinterpret_cast<const uint4*>(ys)[j], yv);
+          accq.template push<kN>(yv, col, a.c2);
+        }
+      }
+      // drafted tokens of row u that fall in this segment: read them from the stage
+      const int b = (int)(u / a.N);
+      const int ul = (int)(u - (long long)b * a.N);
+      if (b != cur_seq) {
+        __syncthreads();
+        for (int c = tid; c < a.N; c += kTmaThreads) {
+          s_par[c] = a.parent[(size_t)b * a.N + c];
+          s_tok[c] = a.tokens[(size_t)b * a.N + c];
+        }
+        __syncthreads();
+        cur_seq = b;
+      }
+      const int c_lo = (int)(x0 - rowbase), c_hi = (int)(x1 - rowbase);
+      for (int c = 1 + tid; c < a.N; c += kTmaThreads) {
+        const int t = s_tok[c];
+        if (s_par[c] == ul && t >= c_lo && t < c_hi) {
+          const int off = (int)(rowbase + t - q0);
+          a.xc[(size_t)b * a.N + c] = to_f32(xs[off]);
+          if (arrays == 2) a.yc[(size_t)b * a.N + c] = to_f32(ys[off]);
+        }
+      }
+      // this CTA's share of row u ends here: one partial per row and array
+      if (x1 == min(e1, rowbase + a.V)) {
+        const VocabPartial p = block_merge({acc.mc, acc.s, acc.av, acc.ai}, red);
+        VocabPartial pq{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+        if (arrays == 2) pq = block_merge({accq.mc, accq.s, accq.av, accq.ai}, red);
+        if (tid == 0) {
+          const size_t slot = (size_t)u * a.mc + (size_t)(cta - c_first(u, a));
+          a.part[slot] = p;
+          if (arrays == 2) a.part_q[slot] = pq;
+        }
+        acc.init();
+        accq.init();
+      }
+    }
+    __syncthreads();  // stage consumed
+    if (tid == 0 && pc + nst < npieces) issue(pc + nst);
+  }
+  if (tid == 0 && s_abort) set_dev_status(a.dev_status, TV_DEV_TIMEOUT);
+  __threadfence();
+  __syncthreads();
+  const long long u_begin = e0 / a.V, u_end = (e1 - 1) / a.V;
+  if (tid == 0) {
+    int nf = 0;
+    const int b_first = (int)(u_begin / a.N), b_last = (int)(u_end / a.N);
+    for (int b = b_first; b <= b_last; ++b) {
+      const long long lo = max(u_begin, (long long)b * a.N), hi = min(u_end, (long long)b * a.N + a.N - 1);
+      const unsigned mine = (unsigned)(hi - lo + 1);
+      const unsigned prev = atomicAdd(a.seq_cnt + b, mine);
+      if (prev + mine == seq_total(b, a) && nf < kMaxFinish) s_finish[nf++] = b;
+    }
+    s_nfinish = nf;
+  }
+  __syncthreads();
+  const int nf = s_nfinish;
+  if (nf == 0) return;
+  __threadfence();
+  // the ring is drained: carve the epilogue's arrays from it
+  float* e_lse2 = reinterpret_cast<float*>(ring);
+  float* e_lse2q = e_lse2 + kMaxNodes;
+  int* e_am = reinterpret_cast<int*>(e_lse2q + kMaxNodes);
+  float* e_xc = reinterpret_cast<float*>(e_am + kMaxNodes);
+  float* e_yc = e_xc + kMaxNodes;
+  float4* e_stage = reinterpret_cast<float4*>(e_yc + kMaxNodes);
+  EpiSmem sm{s_par, s_tok, e_lse2, e_lse2q, e_am, e_stage, e_xc, e_yc};
+  for (int i = 0; i < nf; ++i) {
+    const int b = s_finish[i];
+    if (tid == 0) a.seq_cnt[b] = 0;
+    sequence_epilogue<T>(a, b, sm);
+  }
+}
+
+// ------------------------------------------------------------------------------------
 // host side
 
 constexpr int kVocabThreads = 512;
@@ -504,20 +659,41 @@ static int resident_ctas() {
   return cache[dev];
 }
 
-template <typename T, bool kVec>
-static cudaError_t launch_vocab_t(VocabArgs a, cudaStream_t stream) {
-  const int resident = resident_ctas<T, kVec>();
+static void plan_grid(VocabArgs& a, long long G) {
   const long long rows = (long long)a.B * a.N;
-  long long G = std::min<long long>({(long long)resident, (long long)kGridCap, (a.E + kMinChunk - 1) / kMinChunk});
+  G = std::min<long long>({G, (long long)kGridCap, (a.E + kMinChunk - 1) / kMinChunk});
   G = std::max<long long>(G, (rows + kRowsPerCta - 1) / kRowsPerCta);  // bounds sequences finished per CTA
   if (G < 1) G = 1;
   long long chunk = (a.E + G - 1) / G;
   chunk = (chunk + 7) / 8 * 8;
-  G = (a.E + chunk - 1) / chunk;
   a.chunk = chunk;
   a.L = chunk / gcd_ll((long long)a.V, chunk);
   a.mc = (int)((a.V + chunk - 1) / chunk) + 1;
+}
+
+template <typename T, bool kVec>
+static cudaError_t launch_vocab_t(VocabArgs a, cudaStream_t stream) {
+  plan_grid(a, resident_ctas<T, kVec>());
+  const long long G = (a.E + a.chunk - 1) / a.chunk;
   vocab_pass_kernel<T, kVec><<<(unsigned)G, kVocabThreads, 0, stream>>>(a);
+  return cudaSuccess;
+}
+
+template <typename T>
+static cudaError_t launch_vocab_tma(VocabArgs a, cudaStream_t stream) {
+  static bool attr_set[64] = {false};
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(vocab_pass_tma_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kRingBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  plan_grid(a, sms);  // one CTA per SM: the ring takes most of the shared memory
+  const long long G = (a.E + a.chunk - 1) / a.chunk;
+  vocab_pass_tma_kernel<T><<<(unsigned)G, kTmaThreads, kRingBytes, stream>>>(a);
   return cudaSuccess;
 }
 
@@ -559,9 +735,9 @@ cudaError_t launch_vocab_pass(const void* logits, const void* draft, const int32
                    (!sampling || (reinterpret_cast<uintptr_t>(draft) % 16) == 0);
   cudaError_t e;
   if (dtype == TV_BF16)
-    e = vec ? launch_vocab_t<uint16_t, true>(a, stream) : launch_vocab_t<uint16_t, false>(a, stream);
+    e = vec ? launch_vocab_tma<uint16_t>(a, stream) : launch_vocab_t<uint16_t, false>(a, stream);
   else
-    e = vec ? launch_vocab_t<float, true>(a, stream) : launch_vocab_t<float, false>(a, stream);
+    e = vec ? launch_vocab_tma<float>(a, stream) : launch_vocab_t<float, false>(a, stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
