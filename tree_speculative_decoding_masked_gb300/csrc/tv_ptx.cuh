@@ -48,6 +48,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Device-scope fetch-and-add with acquire-release semantics: after a CTA barrier, one
+// thread's call publishes the CTA's earlier writes and, if it observes the other CTAs'
+// contributions, makes their writes visible to the CTA after the next barrier.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ---- TMA
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int x, int y, int z) {
   asm volatile(

@@ -19,7 +19,6 @@
 
 namespace tv {
 
-constexpr int kStagedParts = 640;  // split partials staged in shared memory by the merging CTA
 
 struct VocabPartial {
   float m;   // max of x * c2 over the chunk (base-2 scaled)
@@ -27,6 +26,25 @@ struct VocabPartial {
   float av;  // raw max value
   int ai;    // its lowest index
 };
+
+// floor(x / d) for x >= 0 whose quotient is below 2^22, without a 64-bit integer
+// division: an fp32 estimate x * (1/d) has relative error below 3 * 2^-24, so it is off
+// by at most one, which one remainder check corrects.  Every quotient this file takes
+// (a row, a sequence, a CTA index) is below 2^18.
+struct DivQ {
+  long long d;
+  float r;
+  __device__ __forceinline__ long long operator()(long long x) const {
+    long long q = (long long)__float2int_rz(__ll2float_rn(x) * r);
+    const long long rem = x - q * d;
+    if (rem < 0)
+      --q;
+    else if (rem >= d)
+      ++q;
+    return q;
+  }
+};
+inline DivQ make_div(long long d) { return {d, (float)(1.0 / (double)d)}; }
 
 template <typename T>
 struct Vec16;
@@ -116,20 +134,25 @@ __device__ __forceinline__ VocabPartial partial_merge(VocabPartial a, VocabParti
   return r;
 }
 
+// Warp-wide merge of partials in three cheap reductions instead of five pairwise merges:
+// the common scaled max first, then every sum rescaled once to it and added, then the
+// lowest column among the lanes that hold the raw max.
 __device__ __forceinline__ VocabPartial warp_merge(VocabPartial p) {
+  float m = p.m, av = p.av;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    VocabPartial q;
-    q.m = __shfl_xor_sync(0xffffffffu, p.m, o);
-    q.s = __shfl_xor_sync(0xffffffffu, p.s, o);
-    q.av = __shfl_xor_sync(0xffffffffu, p.av, o);
-    q.ai = __shfl_xor_sync(0xffffffffu, p.ai, o);
-    p = partial_merge(p, q);
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    av = fmaxf(av, __shfl_xor_sync(0xffffffffu, av, o));
   }
-  return p;
+  float s = p.s > 0.f ? p.s * ptx::ex2(p.m - m) : 0.f;
+  int ai = p.av == av ? p.ai : 0x7fffffff;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    ai = min(ai, __shfl_xor_sync(0xffffffffu, ai, o));
+  }
+  return {m, s, av, ai};
 }
-
-// Block-wide merge; result valid in thread 0.  Uses `red` (>= 32 entries).
 __device__ __forceinline__ VocabPartial block_merge(VocabPartial p, VocabPartial* red) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   p = warp_merge(p);
@@ -199,6 +222,7 @@ struct VocabArgs {
   long long chunk;  // elements per CTA (multiple of 8)
   long long L;      // chunk / gcd(V, chunk): row boundaries u*V on a chunk edge <=> L | u
   int mc;           // partial slots per row (>= CTAs covering any row)
+  DivQ dV, dN, dC, dL;  // division by V, N, chunk and L
   float c2;         // log2(e) / T
   VocabPartial* part;    // [rows][mc]
   VocabPartial* part_q;  // [rows][mc]
@@ -224,15 +248,13 @@ struct VocabArgs {
 constexpr int kStage = 1024;   // float4 partials staged by a finishing CTA
 constexpr int kMaxFinish = 64; // sequences one CTA can finish
 
-__device__ __forceinline__ long long c_first(long long u, const VocabArgs& a) { return u * a.V / a.chunk; }
-__device__ __forceinline__ long long c_last(long long u, const VocabArgs& a) {
-  return ((u + 1) * a.V - 1) / a.chunk;
-}
+__device__ __forceinline__ long long c_first(long long u, const VocabArgs& a) { return a.dC(u * a.V); }
+__device__ __forceinline__ long long c_last(long long u, const VocabArgs& a) { return a.dC((u + 1) * a.V - 1); }
 // number of (row, CTA) partials of sequence b
 __device__ __forceinline__ unsigned seq_total(int b, const VocabArgs& a) {
   const long long r0 = (long long)b * a.N, r1 = r0 + a.N - 1;
   const long long distinct = c_last(r1, a) - c_first(r0, a) + 1;
-  const long long on_edge = r1 / a.L - r0 / a.L;
+  const long long on_edge = a.dL(r1) - a.dL(r0);
   return (unsigned)(distinct + (r1 - r0) - on_edge);
 }
 
@@ -242,9 +264,11 @@ struct EpiSmem {
   float* lse2;
   float* lse2q;
   int* am;
-  float4* stage;  // merge staging, reused as match / path afterwards
+  float4* stage;  // merge staging
   float* xc;
   float* yc;
+  int* match;  // greedy walk: lowest matching child of each node
+  int* path;
 };
 
 // Epilogue of sequence b, run by the CTA that wrote its last partial.
@@ -265,6 +289,7 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) 
     sm.tok[c] = t;
     sm.xc[c] = __ldcg(a.xc + r0 + c);
     if (a.sampling) sm.yc[c] = __ldcg(a.yc + r0 + c);
+    else sm.match[c] = 0x7fffffff;
     const bool ok = (c == 0) ? (p == -1) : (p >= 0 && p < c);
     if (!ok) atomicOr(&s_bad, TV_DEV_BAD_TREE);
     if (c > 0 && (t < 0 || t >= V)) atomicOr(&s_bad, TV_DEV_BAD_TOKEN);
@@ -272,10 +297,9 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) 
   const VocabPartial none{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
   for (int pass = 0; pass < (a.sampling ? 2 : 1); ++pass) {
     const VocabPartial* src = (pass == 0 ? a.part : a.part_q) + r0 * a.mc;
-    if (staged) {
+    if (staged)
       for (int i = tid; i < nstage; i += blockDim.x) sm.stage[i] = __ldcg(reinterpret_cast<const float4*>(src + i));
-      __syncthreads();
-    }
+    __syncthreads();
     for (int u = tid; u < N; u += blockDim.x) {
       const long long ug = r0 + u;
       const int cover = (int)(c_last(ug, a) - c_first(ug, a) + 1);
@@ -301,38 +325,32 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) 
   }
   const int bad = s_bad;
   if (bad && tid == 0) set_dev_status(a.dev_status, bad);
-  // drafted-token probabilities p_c = 2^(x[parent(c)][t_c] * c2 - lse2[parent(c)])
+  // drafted-token probabilities p_c = 2^(x[parent(c)][t_c] * c2 - lse2[parent(c)]); for
+  // greedy verification also each node's child whose token equals the node's argmax
+  // (lowest index if several)
   for (int c = tid; c < N; c += blockDim.x) {
     float pv = __int_as_float(0x7fc00000), qv = pv;
     if (c > 0 && !bad) {
       const int u = sm.par[c];
       pv = ptx::ex2(fmaf(sm.xc[c], a.c2, -sm.lse2[u]));
-      if (a.sampling) qv = ptx::ex2(fmaf(sm.yc[c], a.c2, -sm.lse2q[u]));
+      if (a.sampling)
+        qv = ptx::ex2(fmaf(sm.yc[c], a.c2, -sm.lse2q[u]));
+      else if (sm.tok[c] == sm.am[u])
+        atomicMin(&sm.match[u], c);
     }
     if (a.pc) a.pc[r0 + c] = pv;
     if (a.qc) a.qc[r0 + c] = qv;
     if (a.p_draft) a.p_draft[r0 + c] = pv;
     if (a.q_draft) a.q_draft[r0 + c] = qv;
   }
-  if (a.sampling) {
-    __syncthreads();
-    return;  // the sampling walk runs in its own kernel
-  }
-  // greedy walk: each node's child whose token equals the node's argmax (lowest index if
-  // several) is found in parallel, then the links are followed from the root
-  int* match = reinterpret_cast<int*>(sm.stage);
-  int* path = match + kMaxNodes;
-  for (int c = tid; c < N; c += blockDim.x) match[c] = 0x7fffffff;
   __syncthreads();
-  if (!bad)
-    for (int c = 1 + tid; c < N; c += blockDim.x)
-      if (sm.tok[c] == sm.am[sm.par[c]]) atomicMin(&match[sm.par[c]], c);
-  __syncthreads();
+  if (a.sampling) return;  // the sampling walk runs in its own kernel
+  // greedy walk: follow the matching links from the root
   if (tid == 0) {
     int cur = 0, len = 0;
     if (!bad) {
-      for (int nxt = match[0]; nxt != 0x7fffffff; nxt = match[cur]) {
-        path[len++] = nxt;
+      for (int nxt = sm.match[0]; nxt != 0x7fffffff; nxt = sm.match[cur]) {
+        sm.path[len++] = nxt;
         cur = nxt;
       }
     }
@@ -341,7 +359,7 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) 
   }
   __syncthreads();
   const int len = s_len;
-  for (int j = tid; j < N; j += blockDim.x) a.accepted[r0 + j] = j < len ? path[j] : -1;
+  for (int j = tid; j < N; j += blockDim.x) a.accepted[r0 + j] = j < len ? sm.path[j] : -1;
   if (tid == 0) {
     a.accept_len[b] = len;
     a.bonus[b] = s_bonus;
@@ -371,12 +389,12 @@ __global__ void __launch_bounds__(512, 1) vocab_pass_kernel(VocabArgs a) {
   const long long cta = blockIdx.x;
   const long long e0 = cta * a.chunk;
   const long long e1 = min(a.E, e0 + a.chunk);
-  const long long u_begin = e0 / a.V, u_end = (e1 - 1) / a.V;
+  const long long u_begin = a.dV(e0), u_end = a.dV(e1 - 1);
   const T* X = reinterpret_cast<const T*>(a.logits);
   const T* Y = reinterpret_cast<const T*>(a.draft);
   int cur_seq = -1;
   for (long long u = u_begin; u <= u_end; ++u) {
-    const int b = (int)(u / a.N);
+    const int b = (int)a.dN(u);
     const int ul = (int)(u - (long long)b * a.N);
     if (b != cur_seq) {  // tree of this sequence, to find the children of each row
       __syncthreads();
@@ -415,16 +433,15 @@ __global__ void __launch_bounds__(512, 1) vocab_pass_kernel(VocabArgs a) {
       }
     }
   }
-  __threadfence();
   __syncthreads();
   if (tid == 0) {
     // one atomic per sequence this CTA touched; the CTA completing a sequence finishes it
     int nf = 0;
-    const int b_first = (int)(u_begin / a.N), b_last = (int)(u_end / a.N);
+    const int b_first = (int)a.dN(u_begin), b_last = (int)a.dN(u_end);
     for (int b = b_first; b <= b_last; ++b) {
       const long long lo = max(u_begin, (long long)b * a.N), hi = min(u_end, (long long)b * a.N + a.N - 1);
       const unsigned mine = (unsigned)(hi - lo + 1);
-      const unsigned prev = atomicAdd(a.seq_cnt + b, mine);
+      const unsigned prev = ptx::atom_add_acq_rel_gpu(a.seq_cnt + b, mine);
       if (prev + mine == seq_total(b, a) && nf < kMaxFinish) s_finish[nf++] = b;
     }
     s_nfinish = nf;
@@ -432,8 +449,9 @@ __global__ void __launch_bounds__(512, 1) vocab_pass_kernel(VocabArgs a) {
   __syncthreads();
   const int nf = s_nfinish;
   if (nf == 0) return;
-  __threadfence();
-  EpiSmem sm{s_par, s_tok, s_lse2, s_lse2q, s_am, s_stage, s_xc, s_yc};
+  // the greedy walk's arrays reuse the sampling-only ones
+  EpiSmem sm{s_par, s_tok, s_lse2, s_lse2q, s_am, s_stage, s_xc, s_yc, reinterpret_cast<int*>(s_lse2q),
+             reinterpret_cast<int*>(s_yc)};
   for (int i = 0; i < nf; ++i) {
     const int b = s_finish[i];
     if (tid == 0) a.seq_cnt[b] = 0;
@@ -443,11 +461,14 @@ __global__ void __launch_bounds__(512, 1) vocab_pass_kernel(VocabArgs a) {
 
 // ------------------------------------------------------------------------------------
 // TMA variant (16-byte aligned rows): each CTA bulk-copies its contiguous byte range into
-// a ring of shared-memory stages (all stages in flight at once) and reduces from there.
+// a ring of shared-memory stages and reduces from there.  Warps run through the pieces
+// independently; the last warp to finish a stage refills it.
 
 constexpr int kTmaThreads = 512;
-constexpr int kPieceBytes = 16384;  // per array per stage
+constexpr int kTmaWarps = kTmaThreads / 32;
+constexpr int kPieceBytes = 16384;  // per array per stage: two 16-byte vectors per thread
 constexpr int kRingBytes = 196608;  // 12 stages (greedy) or 6 double stages (sampling)
+constexpr int kMaxStages = kRingBytes / kPieceBytes;
 
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -457,20 +478,114 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Per-thread running state over one row segment: raw max av, scaled max mc = av*c2 and
+// sum of 2^(x*c2 - mc) (two halves, so that packed fp32x2 arithmetic applies).  The
+// argmax column is not tracked element by element: the 16-byte vector that holds av and
+// its first column are kept, and the column is recovered once, when the segment ends.
 template <typename T>
+struct StreamAcc {
+  static constexpr int kN = Vec16<T>::kN;
+  float av;
+  float mc;
+  float2 s;
+  uint4 best;
+  int bcol;
+  __device__ __forceinline__ void init() {
+    av = -INFINITY;
+    mc = -INFINITY;
+    s = make_float2(0.f, 0.f);
+    bcol = -1;
+  }
+  template <int kM>
+  __device__ __forceinline__ void add_sums(const float (&x)[kM], float c2) {
+    const float2 cc = make_float2(c2, c2), nm = make_float2(-mc, -mc);
+    float2 e[kM / 2];
+#pragma unroll
+    for (int k = 0; k < kM / 2; ++k) {
+      const float2 t = __ffma2_rn(make_float2(x[2 * k], x[2 * k + 1]), cc, nm);
+      e[k] = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
+    }
+#pragma unroll
+    for (int w = 1; w < kM / 2; w *= 2)
+#pragma unroll
+      for (int k = 0; k + w < kM / 2; k += 2 * w) e[k] = __fadd2_rn(e[k], e[k + w]);
+    s = __fadd2_rn(s, e[0]);
+  }
+  __device__ __forceinline__ void raise(float bv, float c2) {
+    const float nmc = bv * c2;
+    const float r = ptx::ex2(mc - nmc);
+    s.x *= r;
+    s.y *= r;
+    av = bv;
+    mc = nmc;
+  }
+  // two vectors, at columns ca < cb
+  __device__ __forceinline__ void push2(const uint4& u0, const uint4& u1, int ca, int cb, float c2) {
+    float x[2 * kN];
+    unpack16<T>(u0, x);
+    unpack16<T>(u1, x + kN);
+    float b0 = x[0], b1 = x[kN];
+#pragma unroll
+    for (int k = 1; k < kN; ++k) {
+      b0 = fmaxf(b0, x[k]);
+      b1 = fmaxf(b1, x[kN + k]);
+    }
+    const float bv = fmaxf(b0, b1);
+    if (bv == -INFINITY) return;  // all -inf: nothing to add
+    if (bv > av) {
+      const bool first = b0 >= b1;
+      best = first ? u0 : u1;
+      bcol = first ? ca : cb;
+      raise(bv, c2);
+    }
+    add_sums<2 * kN>(x, c2);
+  }
+  __device__ __forceinline__ void push1(const uint4& u, int col, float c2) {
+    float x[kN];
+    unpack16<T>(u, x);
+    float bv = x[0];
+#pragma unroll
+    for (int k = 1; k < kN; ++k) bv = fmaxf(bv, x[k]);
+    if (bv == -INFINITY) return;
+    if (bv > av) {
+      best = u;
+      bcol = col;
+      raise(bv, c2);
+    }
+    add_sums<kN>(x, c2);
+  }
+  __device__ __forceinline__ VocabPartial partial() const {
+    int ai = 0x7fffffff;
+    if (bcol >= 0) {
+      float x[kN];
+      unpack16<T>(best, x);
+#pragma unroll
+      for (int k = kN - 1; k >= 0; --k)
+        if (x[k] == av) ai = bcol + k;
+    }
+    return {mc, s.x + s.y, av, ai};
+  }
+};
+
+template <typename T, int kArrays>
 __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArgs a) {
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ VocabPartial red[32];
-  __shared__ uint64_t full[12];
+  __shared__ uint64_t full[kMaxStages];
+  __shared__ int s_done[kMaxStages];
   __shared__ int s_par[kMaxNodes];
   __shared__ int s_tok[kMaxNodes];
   __shared__ int s_finish[kMaxFinish];
+  __shared__ unsigned s_total[kMaxFinish];
   __shared__ int s_nfinish;
   __shared__ int s_abort;
-  constexpr int kE = kPieceBytes / (int)sizeof(T);  // elements per piece
-  const int tid = threadIdx.x;
-  const int arrays = a.sampling ? 2 : 1;
-  const int nst = kRingBytes / (kPieceBytes * arrays);
+  constexpr int kE = kPieceBytes / (int)sizeof(T);  // elements per piece (a power of two)
+  constexpr int kN = Vec16<T>::kN;                  // elements per 16-byte vector
+  constexpr int kHalf = kPieceBytes / 32;           // vectors per thread-half of a piece
+  constexpr int nst = kMaxStages / kArrays;
+  static_assert(kHalf == kTmaThreads, "a piece is two vectors per thread");
+  static_assert(kMaxNodes <= 2 * kTmaThreads + 1, "each thread owns at most two children");
+  const int tid = threadIdx.x, lane = tid & 31;
   const long long cta = blockIdx.x;
   const long long e0 = cta * a.chunk;
   const long long e1 = min(a.E, e0 + a.chunk);
@@ -481,118 +596,176 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
     const int st = piece % nst;
     const long long q0 = e0 + (long long)piece * kE;
     const uint32_t bytes = (uint32_t)((min(e1, q0 + kE) - q0) * (long long)sizeof(T));
-    ptx::mbar_arrive_expect_tx(&full[st], bytes * arrays);
-    unsigned char* dst = ring + (size_t)st * kPieceBytes * arrays;
+    ptx::mbar_arrive_expect_tx(&full[st], bytes * kArrays);
+    unsigned char* dst = ring + (size_t)st * kPieceBytes * kArrays;
     bulk_g2s(dst, X + q0, bytes, &full[st]);
-    if (arrays == 2) bulk_g2s(dst + kPieceBytes, Y + q0, bytes, &full[st]);
+    if (kArrays == 2) bulk_g2s(dst + kPieceBytes, Y + q0, bytes, &full[st]);
   };
+  const long long u_begin = a.dV(e0), u_end = a.dV(e1 - 1);
+  const int b_first = (int)a.dN(u_begin), b_last = (int)a.dN(u_end);
+  // Drafted-token logits: the thread owning child c (c = 1 + tid + k * kTmaThreads) reads
+  // x[parent row][token] from the stage of the piece that holds it, if this CTA's range does.
+  int cap_pc[2], cap_off[2], tp[2], tt[2];
+  auto fetch_tree = [&](int bs) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int c = 1 + tid + k * kTmaThreads;
+      tp[k] = c < a.N ? a.parent[(size_t)bs * a.N + c] : -1;
+      tt[k] = c < a.N ? a.tokens[(size_t)bs * a.N + c] : -1;
+    }
+  };
+  auto make_caps = [&](int bs) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      cap_pc[k] = -1;
+      cap_off[k] = 0;
+      // malformed trees are reported by the epilogue
+      if (tp[k] >= 0 && tp[k] < a.N && tt[k] >= 0 && tt[k] < a.V) {
+        const long long g = ((long long)bs * a.N + tp[k]) * a.V + tt[k];
+        if (g >= e0 && g < e1) {
+          cap_pc[k] = (int)((g - e0) / kE);
+          cap_off[k] = (int)((g - e0) % kE);
+        }
+      }
+    }
+  };
+  auto capture = [&](int pc, int bs, const unsigned char* stage) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      if (cap_pc[k] == pc) {
+        const size_t c = (size_t)bs * a.N + 1 + tid + k * kTmaThreads;
+        a.xc[c] = to_f32(reinterpret_cast<const T*>(stage)[cap_off[k]]);
+        if (kArrays == 2) a.yc[c] = to_f32(reinterpret_cast<const T*>(stage + kPieceBytes)[cap_off[k]]);
+      }
+  };
+  fetch_tree(b_first);  // issued ahead of the bulk copies, so that it does not queue behind them
   if (tid == 0) {
-    for (int st = 0; st < nst; ++st) ptx::mbar_init(&full[st], 1);
+    for (int st = 0; st < nst; ++st) {
+      ptx::mbar_init(&full[st], 1);
+      s_done[st] = 0;
+    }
     s_abort = 0;
     ptx::fence_mbar_init();
     for (int pc = 0; pc < min(nst, npieces); ++pc) issue(pc);
+  } else if (tid >= 32 && tid < 64) {
+    for (int i = lane; i < min(b_last - b_first + 1, kMaxFinish); i += 32) s_total[i] = seq_total(b_first + i, a);
   }
   __syncthreads();
-  RowAcc acc, accq;
+  make_caps(b_first);
+  StreamAcc<T> acc, accq;
   acc.init();
   accq.init();
-  int cur_seq = -1;
-  for (int pc = 0; pc < npieces; ++pc) {
-    const int st = pc % nst;
-    const long long q0 = e0 + (long long)pc * kE;
+  // current row u: [rowbase, row_end) in flat element indices; rowbase <= q0 < row_end
+  // holds at the start of every piece
+  long long u = u_begin, rowbase = u_begin * a.V, row_end = rowbase + a.V;
+  int b = b_first, ul = (int)(u_begin - (long long)b_first * a.N);
+  long long slot = u_begin * a.mc + (cta - c_first(u_begin, a));
+  auto row_done = [&]() {  // this CTA's share of row u is complete: one partial per array
+    const VocabPartial p = block_merge(acc.partial(), red);
+    VocabPartial pq{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+    if (kArrays == 2) pq = block_merge(accq.partial(), red);
+    if (tid == 0) {
+      a.part[slot] = p;
+      if (kArrays == 2) a.part_q[slot] = pq;
+    }
+    acc.init();
+    accq.init();
+  };
+  auto next_row = [&]() {  // row u + 1 starts inside this CTA's range: its first partial slot
+    rowbase = row_end;
+    row_end += a.V;
+    ++u;
+    slot = u * a.mc;
+    if (++ul == a.N) {
+      ul = 0;
+      ++b;
+      fetch_tree(b);
+      make_caps(b);
+    }
+  };
+  int st = 0;
+  uint32_t phase = 0;
+  long long q0 = e0;
+  for (int pc = 0; pc < npieces; ++pc, q0 += kE) {
+    ptx::mbar_wait(&full[st], phase, &s_abort);
+    const unsigned char* stage = ring + (size_t)st * kPieceBytes * kArrays;
+    const uint4* xv4 = reinterpret_cast<const uint4*>(stage);
+    const uint4* yv4 = reinterpret_cast<const uint4*>(stage + kPieceBytes);
     const long long q1 = min(e1, q0 + kE);
-    bool ok = ptx::mbar_wait(&full[st], (pc / nst) & 1, &s_abort);
-    (void)ok;
-    const unsigned char* stage = ring + (size_t)st * kPieceBytes * arrays;
-    const T* xs = reinterpret_cast<const T*>(stage);
-    const T* ys = reinterpret_cast<const T*>(stage + kPieceBytes);
-    for (long long u = q0 / a.V; u <= (q1 - 1) / a.V; ++u) {
-      const long long rowbase = u * a.V;
-      const long long x0 = max(q0, rowbase), x1 = min(q1, rowbase + a.V);
-      // 16-byte vectors of the segment [x0, x1) (both ends are multiples of 8 elements)
-      const int v_lo = (int)((x0 - q0) * (long long)sizeof(T) / 16);
-      const int v_hi = (int)((x1 - q0) * (long long)sizeof(T) / 16);
-      constexpr int kN = Vec16<T>::kN;
-      for (int j = v_lo + tid; j < v_hi; j += kTmaThreads) {
-        const int col = (int)(q0 - rowbase) + j * kN;  // column of the first element
-        float xv[kN];
-        unpack16<T>(reinterpret_cast<const uint4*>(stage)[j], xv);
-        acc.template push<kN>(xv, col, a.c2);
-        if (arrays == 2) {
-          float yv[kN];
-          unpack16<T>(reinterpret_cast<const uint4*>(ys)[j], yv);
-          accq.template push<kN>(yv, col, a.c2);
-        }
+    if (q1 - q0 == kE && q1 <= row_end) {
+      // the whole piece lies in row u: vectors tid and tid + kHalf of every array
+      const int ca = (int)(q0 - rowbase) + tid * kN, cb = ca + kHalf * kN;
+      acc.push2(xv4[tid], xv4[tid + kHalf], ca, cb, a.c2);
+      if (kArrays == 2) accq.push2(yv4[tid], yv4[tid + kHalf], ca, cb, a.c2);
+      capture(pc, b, stage);
+      if (q1 == row_end) {
+        row_done();
+        if (q1 < e1) next_row();
       }
-      // drafted tokens of row u that fall in this segment: read them from the stage
-      const int b = (int)(u / a.N);
-      const int ul = (int)(u - (long long)b * a.N);
-      if (b != cur_seq) {
-        __syncthreads();
-        for (int c = tid; c < a.N; c += kTmaThreads) {
-          s_par[c] = a.parent[(size_t)b * a.N + c];
-          s_tok[c] = a.tokens[(size_t)b * a.N + c];
+    } else {
+      for (;;) {
+        const long long x0 = max(q0, rowbase), x1 = min(q1, row_end);
+        const int col0 = (int)(q0 - rowbase);
+        // 16-byte vectors of the segment [x0, x1) (both ends are multiples of 8 elements)
+        const int v_lo = (int)((x0 - q0) / kN), v_hi = (int)((x1 - q0) / kN);
+        for (int j = v_lo + tid; j < v_hi; j += kTmaThreads) {
+          acc.push1(xv4[j], col0 + j * kN, a.c2);
+          if (kArrays == 2) accq.push1(yv4[j], col0 + j * kN, a.c2);
         }
-        __syncthreads();
-        cur_seq = b;
-      }
-      const int c_lo = (int)(x0 - rowbase), c_hi = (int)(x1 - rowbase);
-      for (int c = 1 + tid; c < a.N; c += kTmaThreads) {
-        const int t = s_tok[c];
-        if (s_par[c] == ul && t >= c_lo && t < c_hi) {
-          const int off = (int)(rowbase + t - q0);
-          a.xc[(size_t)b * a.N + c] = to_f32(xs[off]);
-          if (arrays == 2) a.yc[(size_t)b * a.N + c] = to_f32(ys[off]);
-        }
-      }
-      // this CTA's share of row u ends here: one partial per row and array
-      if (x1 == min(e1, rowbase + a.V)) {
-        const VocabPartial p = block_merge({acc.mc, acc.s, acc.av, acc.ai}, red);
-        VocabPartial pq{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
-        if (arrays == 2) pq = block_merge({accq.mc, accq.s, accq.av, accq.ai}, red);
-        if (tid == 0) {
-          const size_t slot = (size_t)u * a.mc + (size_t)(cta - c_first(u, a));
-          a.part[slot] = p;
-          if (arrays == 2) a.part_q[slot] = pq;
-        }
-        acc.init();
-        accq.init();
+        capture(pc, b, stage);
+        if (x1 == min(e1, row_end)) row_done();
+        if (row_end > q1 || row_end >= e1) break;  // row u continues in the next piece
+        next_row();
       }
     }
-    __syncthreads();  // stage consumed
-    if (tid == 0 && pc + nst < npieces) issue(pc + nst);
+    // stage consumed by this warp; the last warp through refills it
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&s_done[st], 1) == kTmaWarps - 1) {
+        __threadfence_block();
+        s_done[st] = 0;
+        if (pc + nst < npieces) {
+          ptx::fence_proxy_async_smem();
+          issue(pc + nst);
+        }
+      }
+    }
+    if (++st == nst) {
+      st = 0;
+      phase ^= 1;
+    }
   }
-  if (tid == 0 && s_abort) set_dev_status(a.dev_status, TV_DEV_TIMEOUT);
-  __threadfence();
   __syncthreads();
-  const long long u_begin = e0 / a.V, u_end = (e1 - 1) / a.V;
   if (tid == 0) {
+    if (s_abort) set_dev_status(a.dev_status, TV_DEV_TIMEOUT);
     int nf = 0;
-    const int b_first = (int)(u_begin / a.N), b_last = (int)(u_end / a.N);
-    for (int b = b_first; b <= b_last; ++b) {
-      const long long lo = max(u_begin, (long long)b * a.N), hi = min(u_end, (long long)b * a.N + a.N - 1);
+    for (int bb = b_first; bb <= b_last; ++bb) {
+      const long long lo = max(u_begin, (long long)bb * a.N), hi = min(u_end, (long long)bb * a.N + a.N - 1);
       const unsigned mine = (unsigned)(hi - lo + 1);
-      const unsigned prev = atomicAdd(a.seq_cnt + b, mine);
-      if (prev + mine == seq_total(b, a) && nf < kMaxFinish) s_finish[nf++] = b;
+      const unsigned prev = ptx::atom_add_acq_rel_gpu(a.seq_cnt + bb, mine);
+      const int i = bb - b_first;
+      if (i < kMaxFinish && prev + mine == s_total[i] && nf < kMaxFinish) s_finish[nf++] = bb;
     }
     s_nfinish = nf;
   }
   __syncthreads();
   const int nf = s_nfinish;
   if (nf == 0) return;
-  __threadfence();
   // the ring is drained: carve the epilogue's arrays from it
   float* e_lse2 = reinterpret_cast<float*>(ring);
   float* e_lse2q = e_lse2 + kMaxNodes;
   int* e_am = reinterpret_cast<int*>(e_lse2q + kMaxNodes);
   float* e_xc = reinterpret_cast<float*>(e_am + kMaxNodes);
   float* e_yc = e_xc + kMaxNodes;
-  float4* e_stage = reinterpret_cast<float4*>(e_yc + kMaxNodes);
-  EpiSmem sm{s_par, s_tok, e_lse2, e_lse2q, e_am, e_stage, e_xc, e_yc};
+  int* e_match = reinterpret_cast<int*>(e_yc + kMaxNodes);
+  int* e_path = e_match + kMaxNodes;
+  float4* e_stage = reinterpret_cast<float4*>(e_path + kMaxNodes);
+  EpiSmem sm{s_par, s_tok, e_lse2, e_lse2q, e_am, e_stage, e_xc, e_yc, e_match, e_path};
   for (int i = 0; i < nf; ++i) {
-    const int b = s_finish[i];
-    if (tid == 0) a.seq_cnt[b] = 0;
-    sequence_epilogue<T>(a, b, sm);
+    const int bs = s_finish[i];
+    if (tid == 0) a.seq_cnt[bs] = 0;
+    sequence_epilogue<T>(a, bs, sm);
   }
 }
 
@@ -669,6 +842,10 @@ static void plan_grid(VocabArgs& a, long long G) {
   a.chunk = chunk;
   a.L = chunk / gcd_ll((long long)a.V, chunk);
   a.mc = (int)((a.V + chunk - 1) / chunk) + 1;
+  a.dV = make_div(a.V);
+  a.dN = make_div(a.N);
+  a.dC = make_div(a.chunk);
+  a.dL = make_div(a.L);
 }
 
 template <typename T, bool kVec>
@@ -679,22 +856,27 @@ static cudaError_t launch_vocab_t(VocabArgs a, cudaStream_t stream) {
   return cudaSuccess;
 }
 
-template <typename T>
+template <typename T, int kArrays>
 static cudaError_t launch_vocab_tma(VocabArgs a, cudaStream_t stream) {
   static bool attr_set[64] = {false};
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(vocab_pass_tma_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kRingBytes);
+    cudaError_t e = cudaFuncSetAttribute(vocab_pass_tma_kernel<T, kArrays>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   plan_grid(a, sms);  // one CTA per SM: the ring takes most of the shared memory
   const long long G = (a.E + a.chunk - 1) / a.chunk;
-  vocab_pass_tma_kernel<T><<<(unsigned)G, kTmaThreads, kRingBytes, stream>>>(a);
+  vocab_pass_tma_kernel<T, kArrays><<<(unsigned)G, kTmaThreads, kRingBytes, stream>>>(a);
   return cudaSuccess;
+}
+
+template <typename T>
+static cudaError_t launch_vocab_tma(VocabArgs a, cudaStream_t stream) {
+  return a.sampling ? launch_vocab_tma<T, 2>(a, stream) : launch_vocab_tma<T, 1>(a, stream);
 }
 
 cudaError_t launch_vocab_pass(const void* logits, const void* draft, const int32_t* parent,
