@@ -10,24 +10,32 @@
 // Result: the first M = budget-1 candidates in the order (s desc, depth asc, rank path
 // lexicographic asc), numbered in that order.  One CTA per sequence; the work is split
 // into a few block-wide phases rather than budget-many serial steps:
-//   1. a lower bound tau on the M-th best score: the M-th best score among the
-//      "one-deviation" candidates (prefixes of the all-rank-0 path with at most one
-//      position replaced by a higher rank) - they are real candidates, so at least M
-//      candidates reach tau;
-//   2. expand the candidate tree level by level keeping every node with s >= tau (scores
-//      never grow along a path, so this set is prefix-closed and contains the answer);
-//   3. bitonic sort of that set in the selection order; keep the first M.
-// If the expanded set outgrows shared memory, tau is raised to the M-th best score
-// already found and the expansion is retried once; after that the kernel falls back to
-// an exact best-first search by one warp (first-child / next-sibling form of the
-// candidate tree, heap-ordered in the selection order).
+//   1. a lower bound tau on the M-th best score, from the "one-deviation" candidates
+//      (prefixes of the all-rank-0 path with at most one position replaced by a higher
+//      rank): they are real candidates, so if at least M of them reach tau, so do at
+//      least M candidates.  tau is the lower edge of the coarse score class (8 exponent
+//      and 3 mantissa bits) in which their count from the top reaches M: one histogram.
+//   2. expand the candidate tree keeping every node with s >= tau (scores never grow
+//      along a path, so this set is prefix-closed and contains the answer), in parallel
+//      over (node, rank) pairs.  If the set outgrows shared memory, tau is raised to the
+//      M-th best score among the candidates already stored (again a valid bound) and the
+//      expansion restarts;
+//   3. order the set in the selection order (direct ranking when small, else an exact
+//      cut at the M-th best score and a bitonic sort) and keep the first M.
+// After a few failed restarts the kernel falls back to an exact best-first search by one
+// warp (first-child / next-sibling form of the candidate tree, heap-ordered in the
+// selection order).
 #include "tv_kernels.cuh"
 
 namespace tv {
 
-constexpr int kSelThreads = 256;
+constexpr int kSelThreads = 512;
 constexpr int kSelCap = 4096;      // candidates held during the expansion
 constexpr int kSelDevRanks = 32;   // ranks 1..31 enumerated in the one-deviation family
+constexpr int kSelBins = 512;      // coarse score classes of [2^-63, 1]: 8 per octave, the lowest takes the rest
+constexpr int kSelRetries = 4;     // expansions with a raised bound before the fallback
+static_assert(kSelBins == kSelThreads, "one coarse class per thread");
+static_assert(32 * kSelBins * 4 <= 2 * kSelCap * 8, "per-lane histogram columns fit in two key arrays");
 
 __device__ __forceinline__ bool key_less(uint64_t a0, uint64_t a1, uint64_t a2, uint64_t b0, uint64_t b1,
                                          uint64_t b2) {
@@ -233,71 +241,145 @@ struct SelSmem {
   int* pos;   // entry -> position in the output (0: not taken)
 };
 
+// Coarse score class of s in [0, 1]: 8 exponent and 3 mantissa bits (8 classes per
+// octave), offset so that class 1 starts at 2^-63; class 0 holds everything below.
+__device__ __forceinline__ int score_class(float s) {
+  return min(max((int)(__float_as_uint(s) >> 20) - 512, 0), kSelBins - 1);
+}
+__device__ __forceinline__ float class_floor(int c) { return c <= 0 ? 0.f : __uint_as_float((uint32_t)(c + 512) << 20); }
+
+// Lower edge of the highest class c such that the histogram's count in classes >= c
+// reaches M; 0 if the total is below M.  One class per thread (kSelBins == blockDim.x).
+__device__ float coarse_bound(const int* hist, int M, int* wsum, float* s_tau) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int c = kSelBins - 1 - t;  // this thread's class, in descending score order
+  const int h = hist[c];
+  int incl = h;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[w] = incl;
+  if (t == 0) *s_tau = 0.f;
+  __syncthreads();
+  int before = 0;
+  for (int k = 0; k < w; ++k) before += wsum[k];
+  const int excl = before + incl - h;
+  if (excl < M && excl + h >= M) *s_tau = class_floor(c);
+  __syncthreads();
+  return *s_tau;
+}
+
 // Expand every candidate with s >= tau.  Each candidate lies on exactly one "run": a node
-// reached by a rank >= 1 edge (or the root's rank-0 child), followed by its rank-0
+// reached by a rank >= 1 edge (or a child of the root), followed by its rank-0
 // descendants.  Step 0 starts the runs at the root's children; step i+1 starts runs at
-// the rank >= 1 children of every node made in step i.  A run is followed by one thread
-// (its scores are a running fp32 product, exactly the left-to-right path product), so the
-// number of steps is 1 + the largest number of rank >= 1 edges on a kept path.
-// Returns the entry count, or -1 if more than kSelCap would be needed; then *complete =
-// entries made by the steps that finished.
-__device__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int* s_count, int* s_over,
-                                int* complete) {
-  if (threadIdx.x == 0) {
+// the rank >= 1 children of every node made in step i.  Per step, the nodes with at
+// least one qualifying child are listed first; then one thread per (listed node, rank)
+// pair follows a run (its scores are a running fp32 product, exactly the left-to-right
+// path product).  The number of steps is 1 + the largest number of rank >= 1 edges on a
+// kept path.  Returns the entry count, or -(stored + 1) if more than kSelCap entries would
+// be needed; then entries [0, stored) are complete (runs are allocated in increasing
+// order, so the first run that did not fit ends the stored prefix) and prefix-closed.
+__device__ __forceinline__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int* s_count,
+                                                int* s_fail, int* s_live) {
+  const int t = threadIdx.x, lane = t & 31;
+  int* live = sm.idx;  // sources with a qualifying child, this step
+  if (t == 0) {
     *s_count = 0;
-    *s_over = 0;
+    *s_fail = 0x7fffffff;
+    *s_live = 0;
   }
   __syncthreads();
   int lo = 0, hi = 0;  // entries made by the previous step; step 0 expands the virtual root
   for (int step = 0;; ++step) {
     const int nsrc = step == 0 ? 1 : hi - lo;
     if (nsrc <= 0) break;
-    for (int i = threadIdx.x; i < nsrc; i += blockDim.x) {
-      const int pe = step == 0 ? -1 : lo + i;
-      const float ps = step == 0 ? 1.f : k0_score(sm.k0[pe]);
-      const int dep = step == 0 ? 0 : (int)(sm.k0[pe] & 0xFFFFFFFFu);  // children sit at position dep
-      if (dep >= d) continue;
-      const uint64_t pk1 = step == 0 ? 0ull : sm.k1[pe];
-      const uint64_t pk2 = step == 0 ? 0ull : sm.k2[pe];
-      const float* mrow = sm.marg + dep * K;
-      for (int r = step == 0 ? 0 : 1; r < K; ++r) {
-        const float s0 = __fmul_rn(ps, mrow[r]);
-        if (s0 < tau) break;  // ranks are sorted: no later rank qualifies
-        // run length: the rank-r child, then rank-0 descendants while s >= tau
-        int len = 1;
-        float sc = s0;
-        while (dep + len < d) {
-          const float nx = __fmul_rn(sc, sm.marg[(dep + len) * K]);
-          if (nx < tau) break;
-          sc = nx;
-          ++len;
+    const int r0 = step == 0 ? 0 : 1;
+    const int nr = K - r0;
+    if (nr <= 0) break;
+    // 1. sources whose best rank >= r0 child reaches tau (ranks are sorted)
+    for (int ib = t - lane; ib < nsrc; ib += blockDim.x) {
+      const int i = ib + lane;
+      bool ok = false;
+      if (i < nsrc) {
+        const uint64_t pk0 = step == 0 ? make_k0(1.f, 0) : sm.k0[lo + i];
+        const int dep = (int)(pk0 & 0xFFFFFFFFu);
+        ok = dep < d && __fmul_rn(k0_score(pk0), sm.marg[dep * K + r0]) >= tau;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, ok);
+      if (m == 0) continue;
+      int wb = 0;
+      if (lane == 0) wb = atomicAdd(s_live, __popc(m));
+      wb = __shfl_sync(0xffffffffu, wb, 0);
+      if (ok) live[wb + __popc(m & ((1u << lane) - 1))] = step == 0 ? -1 : lo + i;
+    }
+    __syncthreads();
+    const int nlive = *s_live;
+    __syncthreads();
+    if (t == 0) *s_live = 0;
+    // 2. one thread per (listed source, rank): the run from that child
+    const int items = nlive * nr;
+    for (int ib = t - lane; ib < items; ib += blockDim.x) {  // warp-uniform trip count
+      const int it = ib + lane;
+      int len = 0, pe = -1, dep = 0, r = 0;
+      float s0 = 0.f;
+      if (it < items) {
+        const int i = it / nr;
+        r = r0 + (it - i * nr);
+        pe = live[i];
+        const uint64_t pk0 = pe < 0 ? make_k0(1.f, 0) : sm.k0[pe];
+        dep = (int)(pk0 & 0xFFFFFFFFu);  // children sit at position dep
+        s0 = __fmul_rn(k0_score(pk0), sm.marg[dep * K + r]);
+        if (s0 >= tau) {
+          // run length: the rank-r child, then rank-0 descendants while s >= tau
+          len = 1;
+          float sc = s0;
+          for (int p = dep + 1; p < d; ++p) {
+            const float nx = __fmul_rn(sc, sm.marg[p * K]);
+            if (!(nx >= tau)) break;
+            sc = nx;
+            ++len;
+          }
         }
-        const int base = atomicAdd(s_count, len);
-        if (base + len > kSelCap) {
-          *s_over = 1;
-          break;
-        }
-        uint64_t c1 = pk1, c2 = pk2;
-        path_set(c1, c2, dep, r);
-        sc = s0;
-        for (int q = 0; q < len; ++q) {
-          if (q > 0) sc = __fmul_rn(sc, sm.marg[(dep + q) * K]);
-          sm.k0[base + q] = make_k0(sc, dep + q + 1);
-          sm.k1[base + q] = c1;
-          sm.k2[base + q] = c2;
-          sm.par[base + q] = q == 0 ? pe : base + q - 1;
-        }
+      }
+      // one allocation per warp: lanes take consecutive slots in lane order
+      int incl = len;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      if (total == 0) continue;
+      int wbase = 0;
+      if (lane == 31) wbase = atomicAdd(s_count, total);
+      const int base = __shfl_sync(0xffffffffu, wbase, 31) + incl - len;
+      if (len == 0) continue;
+      if (base + len > kSelCap) {
+        atomicMin(s_fail, base);
+        continue;
+      }
+      uint64_t c1 = pe < 0 ? 0ull : sm.k1[pe], c2 = pe < 0 ? 0ull : sm.k2[pe];
+      path_set(c1, c2, dep, r);
+      float sc = s0;
+      for (int q = 0; q < len; ++q) {
+        if (q > 0) sc = __fmul_rn(sc, sm.marg[(dep + q) * K]);
+        const int e = base + q;
+        sm.k0[e] = make_k0(sc, dep + q + 1);
+        sm.k1[e] = c1;
+        sm.k2[e] = c2;
+        sm.par[e] = q == 0 ? pe : e - 1;
       }
     }
     __syncthreads();
-    if (*s_over) {
-      *complete = hi;
-      return -1;
-    }
+    const int fail = *s_fail, cnt = *s_count;
+    __syncthreads();  // every thread has read the counters before the next step moves them
+    if (fail != 0x7fffffff) return -fail - 1;
     lo = hi;
-    hi = *s_count;
+    hi = cnt;
   }
-  return *s_count;
+  return hi;
 }
 
 // bitonic sort of sm.idx[0..n2) (entries, -1 = padding last) in the selection order
@@ -330,52 +412,63 @@ constexpr int kRankDirect = 512;  // rank by direct comparison up to this many c
 
 // Threshold selection by the block.  Returns 1 + number selected, or -1 if the
 // candidate set did not fit (the caller falls back).
-__device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_count, int* s_over, int* hist,
-                                int* bcast, int32_t* o_par, int32_t* o_tok, int32_t* o_dep, float* o_sc) {
+__device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_count, int* s_fail, int* hist,
+                                int* bcast, float* s_tau, int32_t* o_par, int32_t* o_tok, int32_t* o_dep,
+                                float* o_sc) {
   const int t = threadIdx.x;
-  // 1. tau = M-th best score among the one-deviation candidates (ranks < kSelDevRanks)
-  uint32_t* f1 = reinterpret_cast<uint32_t*>(sm.k1);  // 2 * kSelCap slots, free for now
+  // 1. coarse histogram of the one-deviation candidates (ranks < kSelDevRanks)
+  // per-lane histogram columns (lane-major, in the expansion buffers, free for now): the
+  // atomics of a warp never collide
+  int* hcol = reinterpret_cast<int*>(sm.k1);
+  for (int i = t; i < 32 * kSelBins / 4; i += blockDim.x) reinterpret_cast<int4*>(hcol)[i] = make_int4(0, 0, 0, 0);
+  float m0[kMaxDepth];  // rank-0 factors, in registers for the run loops
+#pragma unroll
+  for (int p = 0; p < kMaxDepth; ++p) m0[p] = p < d ? sm.marg[p * K] : 1.f;
+  __syncthreads();
   const int rmax = min(K, kSelDevRanks);
-  const int ncombo = 1 + d * (rmax - 1);  // combo 0: no deviation; else (position j, rank r)
-  for (int c = t; c < ncombo; c += blockDim.x) {
-    int j = -1, r = 0, off = 0;
+  const int nchain = 1 + d * (rmax - 1);  // chain 0: no deviation; else (position j, rank r)
+  const int lane = t & 31;
+  int* mycol = hcol + lane * kSelBins;
+  for (int c = t; c < nchain; c += blockDim.x) {
+    int j = -1, r = 0;
     if (c > 0) {
       j = (c - 1) / (rmax - 1);
-      r = 1 + (c - 1) % (rmax - 1);
-      // no deviation: d prefixes; deviation at j: d - j prefixes
-      off = d + (rmax - 1) * (j * d - j * (j - 1) / 2) + (r - 1) * (d - j);
+      r = 1 + (c - 1) - j * (rmax - 1);
     }
-    float mv[kMaxDepth];
-#pragma unroll
-    for (int p = 0; p < kMaxDepth; ++p) mv[p] = p < d ? sm.marg[p * K + (p == j ? r : 0)] : 1.f;
+    const float mj = j >= 0 ? sm.marg[j * K + r] : 1.f;
     float sc = 1.f;
-    const int first = j < 0 ? 0 : j;
 #pragma unroll
     for (int p = 0; p < kMaxDepth; ++p) {
       if (p < d) {
-        sc = __fmul_rn(sc, mv[p]);
-        if (p >= first) {
-          const int slot = off + (p - first);
-          if (slot < 2 * kSelCap) f1[slot] = __float_as_uint(sc);
-        }
+        sc = __fmul_rn(sc, p == j ? mj : m0[p]);
+        if (p >= j) atomicAdd(&mycol[score_class(sc)], 1);  // prefixes that contain the deviation
       }
     }
   }
-  const int nf1 = min(d + (rmax - 1) * (d * (d + 1) / 2), 2 * kSelCap);
   __syncthreads();
-  float tau = 0.f;
-  if (nf1 >= M) tau = __uint_as_float(block_kth_largest(f1, nf1, M, hist, bcast));
+  {
+    int h = 0;
+#pragma unroll 8
+    for (int l = 0; l < 32; ++l) h += hcol[l * kSelBins + t];
+    hist[t] = h;
+  }
   __syncthreads();
-  // 2. expansion; one retry with tau raised to the M-th best of the complete levels
-  int complete = 0;
-  int n = expand_threshold(sm, d, K, tau, s_count, s_over, &complete);
-  if (n < 0 && complete >= M) {
-    uint32_t* sc = reinterpret_cast<uint32_t*>(sm.idx);  // idx + pos: 2 * kSelCap slots
-    for (int i = t; i < complete; i += blockDim.x) sc[i] = __float_as_uint(k0_score(sm.k0[i]));
+  float tau = coarse_bound(hist, M, bcast + 2, s_tau);
+  // 2. expansion; restarts with tau raised to the M-th best stored score
+  int n = -1;
+  for (int attempt = 0; attempt <= kSelRetries; ++attempt) {
+    n = expand_threshold(sm, d, K, tau, s_count, s_fail, bcast + 2 + kSelThreads / 32);
+    if (n >= 0) break;
+    const int stored = -n - 1;
+    n = -1;
+    if (stored < M || attempt == kSelRetries) break;
+    uint32_t* sc = reinterpret_cast<uint32_t*>(sm.idx);
+    for (int i = t; i < stored; i += blockDim.x) sc[i] = __float_as_uint(k0_score(sm.k0[i]));
     __syncthreads();
-    tau = __uint_as_float(block_kth_largest(sc, complete, M, hist, bcast));
+    const float raised = __uint_as_float(block_kth_largest(sc, stored, M, hist, bcast));
     __syncthreads();
-    n = expand_threshold(sm, d, K, tau, s_count, s_over, &complete);
+    if (!(raised > tau)) break;  // ties at the bound: no progress possible
+    tau = raised;
   }
   if (n < 0) return -1;
   const int take = min(n, M);
@@ -388,6 +481,7 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_c
       int less = 0, eq = 0;
       int j = 0;
       const ulonglong2* k0v = reinterpret_cast<const ulonglong2*>(sm.k0);
+#pragma unroll 4
       for (; j + 2 <= n; j += 2) {
         const ulonglong2 c = k0v[j >> 1];
         less += (c.x < a0) + (c.y < a0);
@@ -447,9 +541,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
                                                              int32_t* out_parent, int32_t* out_tok, int32_t* out_depth,
                                                              float* out_score, int32_t* n_nodes, int32_t* dev_status) {
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int hist[256];
-  __shared__ int bcast[2];
-  __shared__ int s_bad, s_nout, s_count, s_over;
+  __shared__ int hist[kSelBins > 256 ? kSelBins : 256];
+  __shared__ int bcast[3 + kSelThreads / 32];
+  __shared__ float s_tau;
+  __shared__ int s_bad, s_nout, s_count, s_fail;
   const int b = blockIdx.x, tid = threadIdx.x;
   const int M = budget - 1;
   SelSmem sm;
@@ -464,6 +559,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
 
   const float* mg = marg + (size_t)b * d * K;
   const int32_t* tk = ptok + (size_t)b * d * K;
+  const int root = (tid == 0 && root_token) ? root_token[b] : -1;  // in flight with the pool loads
   if (tid == 0) {
     s_bad = 0;
     s_nout = -1;
@@ -485,14 +581,14 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
   float* o_sc = out_score + (size_t)b * budget;
   if (tid == 0) {
     o_par[0] = -1;
-    o_tok[0] = root_token ? root_token[b] : -1;
+    o_tok[0] = root;
     o_dep[0] = 0;
     o_sc[0] = 1.f;
   }
   if (M <= 0) {
     if (tid == 0) s_nout = 1;
   } else if (M <= kSelCap / 2) {
-    const int r = select_threshold(sm, d, K, M, &s_count, &s_over, hist, bcast, o_par, o_tok, o_dep, o_sc);
+    const int r = select_threshold(sm, d, K, M, &s_count, &s_fail, hist, bcast, &s_tau, o_par, o_tok, o_dep, o_sc);
     if (tid == 0) s_nout = r;
   }
   __syncthreads();
