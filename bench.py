@@ -501,7 +501,7 @@ def run_ours(args):
     fam_bytes = {"attention": bytes_attn, "verify": bytes_vocab}
     dom = max(("attention", "verify"), key=lambda kk: br[kk])
     achieved = fam_bytes[dom] / (br[dom] * 1e-6) / 1e9
-    kernel_names = {"attention": "attn_tc_kernel" if bf16 else "attn_simt_kernel", "verify": "vocab_pass_kernel"}
+    kernel_names = {"attention": "attn_tc_kernel" if bf16 else "attn_simt_kernel", "verify": "vocab_pass_tma_kernel"}
     roofline = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": kernel_traffic(kernel_names[dom]),

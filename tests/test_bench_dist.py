@@ -1,0 +1,75 @@
+"""Host logic of bench.py's multi-rank launch, on CPU with the gloo backend and two ranks:
+rendezvous, the barrier around the timed region, the max-over-ranks time, and the
+reference arm's rank-0-only rule.  The GPU path itself runs replicas only (no data-path
+collective), so these are the only cross-rank steps."""
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+    r, w = bench.dist_init("gloo")
+    bench.barrier(w)
+    # each rank reports a different time; every rank must see the largest
+    slowest = bench.max_over_ranks(1.5 + rank, w, device="cpu")
+    bench.barrier(w)
+    with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+        json.dump({"rank": r, "world": w, "env": list(bench.dist_env()), "max": slowest}, f)
+    dist.destroy_process_group()
+
+
+def test_two_rank_barrier_and_max_over_ranks(tmp_path):
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True,
+                       start_method="spawn")
+    res = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(world)]
+    for r, x in enumerate(res):
+        assert x["rank"] == r and x["world"] == world
+        assert x["env"] == [r, world, r]
+        assert x["max"] == pytest.approx(1.5 + world - 1)
+
+
+def test_single_rank_needs_no_process_group(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.dist_env() == (0, 1, 0)
+    assert bench.dist_init("gloo") == (0, 1)
+    bench.barrier(1)
+    assert bench.max_over_ranks(3.25, 1) == 3.25
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    args = bench.parse_args(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0"])
+    bench.run_reference(args)  # a non-zero rank returns without work or output
+    assert capsys.readouterr().out == ""
+
+
+def test_defaults_are_one_gpu_and_the_headline_workload():
+    sys.path.insert(0, ROOT)
+    import bench
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.impl == "ours" and a.warmup >= 3
+    assert a.workload == bench.DEFAULT_WORKLOAD
