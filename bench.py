@@ -44,6 +44,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=60000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--budget", type=int, default=None,
+                    help="rows per tree for pool workloads (default: the workload's largest budget)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-worker", type=float, default=None, help=argparse.SUPPRESS)
@@ -341,7 +343,7 @@ def run_ours(args):
     # ---- inputs (one set on the host; device copies rotate)
     use_pool = "pool_d" in cfg
     if use_pool:
-        N = cfg.get("N") or max(cfg["budgets"])
+        N = args.budget or cfg.get("N") or max(cfg["budgets"])
         marg, ptok = W.pools(g, B, cfg["pool_d"], cfg["pool_k"], V)
         marg_d, ptok_d = torch.from_numpy(marg).to(dev), torch.from_numpy(ptok).to(dev)
         root_d = torch.full((B,), 11, dtype=torch.int32, device=dev)
@@ -536,7 +538,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
-            "config": dict(workload_config(args.workload, cfg),
+            "config": dict(workload_config(args.workload, cfg), N=N,
                            l2=f"inputs rotate over {n_sets} device copies, {n_sets * bytes_set / 1e6:.0f} MB "
                               f"> 2 x L2 ({l2 / 1e6:.0f} MB)",
                            step="select_subtree, then tree_attention || " +

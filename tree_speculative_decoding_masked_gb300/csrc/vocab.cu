@@ -247,6 +247,8 @@ struct VocabArgs {
 
 constexpr int kStage = 1024;   // float4 partials staged by a finishing CTA
 constexpr int kMaxFinish = 64; // sequences one CTA can finish
+constexpr int kRowsPerCta = 32;                // the host plan gives a CTA at most this many rows (+ 2 partial)
+constexpr int kMaxSeg = kRowsPerCta + 4;       // row segments one CTA can cover
 
 __device__ __forceinline__ long long c_first(long long u, const VocabArgs& a) { return a.dC(u * a.V); }
 __device__ __forceinline__ long long c_last(long long u, const VocabArgs& a) { return a.dC((u + 1) * a.V - 1); }
@@ -466,8 +468,9 @@ __global__ void __launch_bounds__(512, 1) vocab_pass_kernel(VocabArgs a) {
 
 constexpr int kTmaThreads = 512;
 constexpr int kTmaWarps = kTmaThreads / 32;
-constexpr int kPieceBytes = 16384;  // per array per stage: two 16-byte vectors per thread
-constexpr int kRingBytes = 196608;  // 12 stages (greedy) or 6 double stages (sampling)
+constexpr int kPieceBytes = 32768;  // per array per stage: four 16-byte vectors per thread
+constexpr int kRingBytes = 196608;  // 6 stages (greedy) or 3 double stages (sampling)
+constexpr int kVpt = kPieceBytes / 16 / kTmaThreads;  // vectors per thread per piece
 constexpr int kMaxStages = kRingBytes / kPieceBytes;
 
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -519,26 +522,34 @@ struct StreamAcc {
     av = bv;
     mc = nmc;
   }
-  // two vectors, at columns ca < cb
-  __device__ __forceinline__ void push2(const uint4& u0, const uint4& u1, int ca, int cb, float c2) {
-    float x[2 * kN];
-    unpack16<T>(u0, x);
-    unpack16<T>(u1, x + kN);
-    float b0 = x[0], b1 = x[kN];
+  // kV vectors; vector v starts at column col0 + v * cstride
+  template <int kV>
+  __device__ __forceinline__ void pushv(const uint4 (&u)[kV], int col0, int cstride, float c2) {
+    float x[kV * kN];
+    float bm[kV];
 #pragma unroll
-    for (int k = 1; k < kN; ++k) {
-      b0 = fmaxf(b0, x[k]);
-      b1 = fmaxf(b1, x[kN + k]);
+    for (int v = 0; v < kV; ++v) {
+      unpack16<T>(u[v], x + v * kN);
+      bm[v] = x[v * kN];
+#pragma unroll
+      for (int k = 1; k < kN; ++k) bm[v] = fmaxf(bm[v], x[v * kN + k]);
     }
-    const float bv = fmaxf(b0, b1);
+    float bv = bm[0];
+#pragma unroll
+    for (int v = 1; v < kV; ++v) bv = fmaxf(bv, bm[v]);
     if (bv == -INFINITY) return;  // all -inf: nothing to add
-    if (bv > av) {
-      const bool first = b0 >= b1;
-      best = first ? u0 : u1;
-      bcol = first ? ca : cb;
+    if (bv > av) {                // rare: keep the first vector that holds the new max
+      bool found = false;
+#pragma unroll
+      for (int v = 0; v < kV; ++v)
+        if (!found && bm[v] == bv) {
+          found = true;
+          best = u[v];
+          bcol = col0 + v * cstride;
+        }
       raise(bv, c2);
     }
-    add_sums<2 * kN>(x, c2);
+    add_sums<kV * kN>(x, c2);
   }
   __device__ __forceinline__ void push1(const uint4& u, int col, float c2) {
     float x[kN];
@@ -570,22 +581,20 @@ struct StreamAcc {
 template <typename T, int kArrays>
 __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArgs a) {
   extern __shared__ __align__(128) unsigned char ring[];
-  __shared__ VocabPartial red[32];
   __shared__ uint64_t full[kMaxStages];
   __shared__ int s_done[kMaxStages];
-  __shared__ int s_par[kMaxNodes];
-  __shared__ int s_tok[kMaxNodes];
+  __shared__ VocabPartial s_wp[kArrays][kMaxSeg][kTmaWarps];  // per-warp partials of each row segment
+  __shared__ long long s_segslot[kMaxSeg];
   __shared__ int s_finish[kMaxFinish];
   __shared__ unsigned s_total[kMaxFinish];
   __shared__ int s_nfinish;
   __shared__ int s_abort;
   constexpr int kE = kPieceBytes / (int)sizeof(T);  // elements per piece (a power of two)
   constexpr int kN = Vec16<T>::kN;                  // elements per 16-byte vector
-  constexpr int kHalf = kPieceBytes / 32;           // vectors per thread-half of a piece
   constexpr int nst = kMaxStages / kArrays;
-  static_assert(kHalf == kTmaThreads, "a piece is two vectors per thread");
+  static_assert(kVpt * 16 * kTmaThreads == kPieceBytes, "a piece is kVpt vectors per thread");
   static_assert(kMaxNodes <= 2 * kTmaThreads + 1, "each thread owns at most two children");
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const long long cta = blockIdx.x;
   const long long e0 = cta * a.chunk;
   const long long e1 = min(a.E, e0 + a.chunk);
@@ -660,14 +669,21 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
   long long u = u_begin, rowbase = u_begin * a.V, row_end = rowbase + a.V;
   int b = b_first, ul = (int)(u_begin - (long long)b_first * a.N);
   long long slot = u_begin * a.mc + (cta - c_first(u_begin, a));
-  auto row_done = [&]() {  // this CTA's share of row u is complete: one partial per array
-    const VocabPartial p = block_merge(acc.partial(), red);
-    VocabPartial pq{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
-    if (kArrays == 2) pq = block_merge(accq.partial(), red);
-    if (tid == 0) {
-      a.part[slot] = p;
-      if (kArrays == 2) a.part_q[slot] = pq;
+  // Where this CTA's share of row u ends, every warp parks its merged partial in shared
+  // memory (no block barrier in the streaming loop); the segments are merged at the end.
+  int seg = 0;
+  auto row_done = [&]() {
+    const VocabPartial p = warp_merge(acc.partial());
+    VocabPartial pq{};
+    if (kArrays == 2) pq = warp_merge(accq.partial());
+    if (seg < kMaxSeg) {
+      if (lane == 0) {
+        s_wp[0][seg][wid] = p;
+        if (kArrays == 2) s_wp[kArrays - 1][seg][wid] = pq;
+      }
+      if (tid == 0) s_segslot[seg] = slot;
     }
+    ++seg;
     acc.init();
     accq.init();
   };
@@ -686,23 +702,38 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
   int st = 0;
   uint32_t phase = 0;
   long long q0 = e0;
+  // fast-path bookkeeping in 32 bits: elements from the piece start to the end of row u
+  int rem = (int)(row_end - q0);
+  const bool last_full = (e1 - e0) % kE == 0;
+  int next_cap = min((unsigned)cap_pc[0], (unsigned)cap_pc[1]);  // -1 (none) sorts last
   for (int pc = 0; pc < npieces; ++pc, q0 += kE) {
     ptx::mbar_wait(&full[st], phase, &s_abort);
     const unsigned char* stage = ring + (size_t)st * kPieceBytes * kArrays;
     const uint4* xv4 = reinterpret_cast<const uint4*>(stage);
     const uint4* yv4 = reinterpret_cast<const uint4*>(stage + kPieceBytes);
-    const long long q1 = min(e1, q0 + kE);
-    if (q1 - q0 == kE && q1 <= row_end) {
-      // the whole piece lies in row u: vectors tid and tid + kHalf of every array
-      const int ca = (int)(q0 - rowbase) + tid * kN, cb = ca + kHalf * kN;
-      acc.push2(xv4[tid], xv4[tid + kHalf], ca, cb, a.c2);
-      if (kArrays == 2) accq.push2(yv4[tid], yv4[tid + kHalf], ca, cb, a.c2);
-      capture(pc, b, stage);
-      if (q1 == row_end) {
+    if (rem >= kE && (pc + 1 < npieces || last_full)) {
+      // the whole piece lies in row u: vectors tid + v * kTmaThreads of every array
+      const int col0 = (a.V - rem) + tid * kN;
+      uint4 u[kVpt];
+#pragma unroll
+      for (int v = 0; v < kVpt; ++v) u[v] = xv4[tid + v * kTmaThreads];
+      acc.template pushv<kVpt>(u, col0, kTmaThreads * kN, a.c2);
+      if (kArrays == 2) {
+#pragma unroll
+        for (int v = 0; v < kVpt; ++v) u[v] = yv4[tid + v * kTmaThreads];
+        accq.template pushv<kVpt>(u, col0, kTmaThreads * kN, a.c2);
+      }
+      if (pc == next_cap) capture(pc, b, stage);
+      rem -= kE;
+      if (rem == 0) {
         row_done();
-        if (q1 < e1) next_row();
+        if (q0 + kE < e1) {
+          next_row();
+          rem = a.V;
+        }
       }
     } else {
+      const long long q1 = min(e1, q0 + kE);
       for (;;) {
         const long long x0 = max(q0, rowbase), x1 = min(q1, row_end);
         const int col0 = (int)(q0 - rowbase);
@@ -717,7 +748,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
         if (row_end > q1 || row_end >= e1) break;  // row u continues in the next piece
         next_row();
       }
+      rem = (int)(row_end - (q0 + kE));
     }
+    next_cap = min((unsigned)cap_pc[0], (unsigned)cap_pc[1]);
     // stage consumed by this warp; the last warp through refills it
     __syncwarp();
     if (lane == 0) {
@@ -737,8 +770,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
     }
   }
   __syncthreads();
+  // one partial per (row segment, array): merge the warps' partials
+  for (int sg = wid; sg < min(seg, kMaxSeg); sg += kTmaWarps) {
+#pragma unroll
+    for (int ar = 0; ar < kArrays; ++ar) {
+      VocabPartial q = lane < kTmaWarps ? s_wp[ar][sg][lane] : VocabPartial{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+      q = warp_merge(q);
+      if (lane == 0) (ar == 0 ? a.part : a.part_q)[s_segslot[sg]] = q;
+    }
+  }
+  __syncthreads();
   if (tid == 0) {
     if (s_abort) set_dev_status(a.dev_status, TV_DEV_TIMEOUT);
+    if (seg > kMaxSeg) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);  // excluded by the host plan
     int nf = 0;
     for (int bb = b_first; bb <= b_last; ++bb) {
       const long long lo = max(u_begin, (long long)bb * a.N), hi = min(u_end, (long long)bb * a.N + a.N - 1);
@@ -753,7 +797,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
   const int nf = s_nfinish;
   if (nf == 0) return;
   // the ring is drained: carve the epilogue's arrays from it
-  float* e_lse2 = reinterpret_cast<float*>(ring);
+  int* e_par = reinterpret_cast<int*>(ring);
+  int* e_tok = e_par + kMaxNodes;
+  float* e_lse2 = reinterpret_cast<float*>(e_tok + kMaxNodes);
   float* e_lse2q = e_lse2 + kMaxNodes;
   int* e_am = reinterpret_cast<int*>(e_lse2q + kMaxNodes);
   float* e_xc = reinterpret_cast<float*>(e_am + kMaxNodes);
@@ -761,7 +807,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
   int* e_match = reinterpret_cast<int*>(e_yc + kMaxNodes);
   int* e_path = e_match + kMaxNodes;
   float4* e_stage = reinterpret_cast<float4*>(e_path + kMaxNodes);
-  EpiSmem sm{s_par, s_tok, e_lse2, e_lse2q, e_am, e_stage, e_xc, e_yc, e_match, e_path};
+  EpiSmem sm{e_par, e_tok, e_lse2, e_lse2q, e_am, e_stage, e_xc, e_yc, e_match, e_path};
   for (int i = 0; i < nf; ++i) {
     const int bs = s_finish[i];
     if (tid == 0) a.seq_cnt[bs] = 0;
@@ -775,7 +821,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
 constexpr int kVocabThreads = 512;
 constexpr long long kMinChunk = 2048;  // elements
 constexpr int kGridCap = 4096;         // CTAs (bounds the workspace)
-constexpr int kRowsPerCta = 32;        // at most this many rows (+1) per CTA
 
 static long long gcd_ll(long long x, long long y) {
   while (y) {
