@@ -1,4 +1,4 @@
-// Stochastic acceptance walk down the draft tree (one CTA of 1024 threads per sequence).
+// Stochastic acceptance walk down the draft tree (one cluster of CTAs per sequence).
 //
 // Speculative-decoding blog, "acceptance probability for sampling": draft token t of
 // node c is kept with probability min(1, p(t)/q(t)); "how to correct after a
@@ -7,9 +7,18 @@
 // t_k the target side moves to the normalised residual and the draft side drops t_k and
 // renormalises (the drafts at one node are distinct tokens).  Each residual needs one
 // pass over the vocabulary (its normaliser Z); the final draw needs one more pass
-// (an inverse-CDF scan).  Sums run in fp64.
+// (an inverse-CDF scan).
+//
+// Every CTA of the cluster runs the same control flow (same tree, same Philox draws, same
+// sums, hence the same decisions) and takes an equal share of the vocabulary in each
+// pass.
+// Sums are exact: each term in [0, 1] is rounded once to a multiple of 2^-56 and added as
+// a 64-bit integer, so a total does not depend on the order of the additions and every
+// CTA, after reading the others' partial sums through distributed shared memory, holds
+// the same value.
 #include "philox.cuh"
 #include "tv_kernels.cuh"
+#include "tv_ptx.cuh"
 
 namespace tv {
 
@@ -32,6 +41,7 @@ struct WalkArgs {
   int32_t* accept_len;
   int32_t* out_token;
   int32_t* dev_status;
+  int csize;  // CTAs per cluster (one cluster per sequence)
 };
 
 template <typename T>
@@ -62,20 +72,53 @@ __device__ __forceinline__ void eval_pq(const Residual& r, int v, float p, float
   Q = removed ? 0.f : q * r.invd[r.nrej];
 }
 
-__device__ double block_sum_d(double v, double* red) {
+constexpr int kWalkClusterMax = 16;  // CTAs per sequence where the device allows it, else 8
+constexpr int kBatch = 5;            // vocabulary elements per thread whose loads are issued together
+constexpr float kFixScale = 72057594037927936.0f;  // 2^56
+
+__device__ __forceinline__ unsigned long long to_fix(float x) { return __float2ull_rn(x * kFixScale); }
+
+__device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t addr) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Block-wide exclusive scan of 64-bit values; returns this thread's exclusive prefix and
+// sets *total.  red holds at least 33 entries.
+__device__ unsigned long long block_scan_u64(unsigned long long v, unsigned long long* red,
+                                             unsigned long long* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  v = warp_sum_d(v);
-  if (lane == 0) red[wid] = v;
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) red[wid] = incl;
   __syncthreads();
   if (wid == 0) {
-    double x = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.0;
-    x = warp_sum_d(x);
-    if (lane == 0) red[32] = x;
+    const unsigned long long x = lane < (int)(blockDim.x >> 5) ? red[lane] : 0ull;
+    unsigned long long xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, xi, o);
+      if (lane >= o) xi += y;
+    }
+    red[lane] = xi - x;
+    if (lane == 31) red[32] = xi;
   }
   __syncthreads();
-  double r = red[32];
+  const unsigned long long excl = red[wid] + (incl - v);
+  *total = red[32];
   __syncthreads();
-  return r;
+  return excl;
 }
 
 template <typename T>
@@ -85,12 +128,49 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
   __shared__ int s_kids[kMaxNodes];
   __shared__ int s_wcnt[32];
   __shared__ int s_nkids, s_bad, s_found;
-  __shared__ double red[33];
+  __shared__ unsigned long long red[33];
+  __shared__ unsigned long long s_part[2];  // this CTA's sum in a pass (alternating slots)
+  __shared__ unsigned long long s_sum[2];   // cluster total and the sum of the lower ranks
+  __shared__ float s_pc[kMaxNodes], s_qc[kMaxNodes], s_l2p[kMaxNodes], s_l2q[kMaxNodes];
   __shared__ Residual res;
   __shared__ int s_dec;  // broadcast of a decision
-  const int b = blockIdx.x;
+  const uint32_t crank = cluster_rank();
+  const int csize = a.csize;
+  const int b = blockIdx.x / csize;
   const int N = a.N, V = a.V;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  // this CTA's share of the vocabulary in every pass
+  const int span = (V + csize - 1) / csize;
+  const int vlo = min(V, (int)crank * span), vhi = min(V, vlo + span);
+  int npass = 0;
+  // Sum of `mine` over the cluster: every CTA gets the same total; *below = the sum over
+  // the lower-ranked CTAs
+  auto cluster_total = [&](unsigned long long mine, unsigned long long* below) {
+    const int slot = npass & 1;
+    if (tid == 0) s_part[slot] = mine;
+    ptx::cluster_sync();
+    if (tid < 32) {  // lane r reads CTA r's partial; the 16 remote loads overlap
+      const uint32_t r = (uint32_t)lane;
+      const unsigned long long x =
+          r < (uint32_t)csize ? ld_cluster_u64(ptx::map_cluster(ptx::smem_addr(&s_part[slot]), r)) : 0ull;
+      unsigned long long tot = x, lower = r < crank ? x : 0ull;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        lower += __shfl_xor_sync(0xffffffffu, lower, o);
+      }
+      if (lane == 0) {
+        s_sum[0] = tot;
+        s_sum[1] = lower;
+      }
+    }
+    __syncthreads();
+    const unsigned long long tot = s_sum[0];
+    *below = s_sum[1];
+    __syncthreads();
+    ++npass;
+    return tot;
+  };
   if (tid == 0) s_bad = 0;
   __syncthreads();
   for (int c = tid; c < N; c += blockDim.x) {
@@ -98,18 +178,26 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
     const int t = a.tokens[(size_t)b * N + c];
     s_par[c] = p;
     s_tok[c] = t;
+    // per-node inputs of the decisions, in the same round trip
+    s_pc[c] = a.pc[(size_t)b * N + c];
+    s_qc[c] = a.qc[(size_t)b * N + c];
+    s_l2p[c] = a.lse2[(size_t)b * N + c];
+    s_l2q[c] = a.lse2_q[(size_t)b * N + c];
     const bool ok = (c == 0) ? (p == -1) : (p >= 0 && p < c);
     if (!ok) atomicOr(&s_bad, TV_DEV_BAD_TREE);
     if (c > 0 && (t < 0 || t >= V)) atomicOr(&s_bad, TV_DEV_BAD_TOKEN);
   }
   __syncthreads();
   if (s_bad) {
-    if (tid == 0) {
-      set_dev_status(a.dev_status, s_bad);
-      a.accept_len[b] = 0;
-      a.out_token[b] = -1;
+    if (crank == 0) {
+      if (tid == 0) {
+        set_dev_status(a.dev_status, s_bad);
+        a.accept_len[b] = 0;
+        a.out_token[b] = -1;
+      }
+      for (int j = tid; j < N; j += blockDim.x) a.accepted[(size_t)b * N + j] = -1;
     }
-    for (int j = tid; j < N; j += blockDim.x) a.accepted[(size_t)b * N + j] = -1;
+    ptx::cluster_sync();
     return;
   }
   int u = 0, len = 0;
@@ -143,19 +231,19 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
     }
     const int m = s_nkids;
     const size_t rowp = ((size_t)b * N + u) * (size_t)V;
-    const float l2p = a.lse2[(size_t)b * N + u];
-    const float l2q = a.lse2_q[(size_t)b * N + u];
+    const float l2p = s_l2p[u];
+    const float l2q = s_l2q[u];
     for (int k = 1; k <= m; ++k) {
       const int c = s_kids[k - 1];
       if (tid == 0) {
         const int t = s_tok[c];
         float pt, qt;
         if (res.nrej == 0) {
-          pt = a.pc[(size_t)b * N + c];
-          qt = a.qc[(size_t)b * N + c];
+          pt = s_pc[c];
+          qt = s_qc[c];
         } else {
-          const float p0 = exp2f(fmaf(ld_logit<T>(a.target, rowp + t), a.c2, -l2p));
-          const float q0 = exp2f(fmaf(ld_logit<T>(a.draft, rowp + t), a.c2, -l2q));
+          const float p0 = ptx::ex2(fmaf(ld_logit<T>(a.target, rowp + t), a.c2, -l2p));
+          const float q0 = ptx::ex2(fmaf(ld_logit<T>(a.draft, rowp + t), a.c2, -l2q));
           eval_pq(res, t, p0, q0, pt, qt);
         }
         const float r = philox_uniform(a.seed, a.round, b, u, k, 0);
@@ -166,19 +254,33 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
       __syncthreads();
       if (s_dec) break;
       // rejection of t_k: Z = sum_v (P(v) - Q(v))+ with the current (P, Q)
-      double zs = 0.0;
-      for (int v = tid; v < V; v += blockDim.x) {
-        const float p0 = exp2f(fmaf(ld_logit<T>(a.target, rowp + v), a.c2, -l2p));
-        const float q0 = exp2f(fmaf(ld_logit<T>(a.draft, rowp + v), a.c2, -l2q));
-        float P, Q;
-        eval_pq(res, v, p0, q0, P, Q);
-        zs += (double)fmaxf(P - Q, 0.f);
+      unsigned long long zs = 0;
+      for (int vb = vlo + tid; vb < vhi; vb += kBatch * blockDim.x) {
+        float xs[kBatch], ys[kBatch];  // all loads of a batch in flight together
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int v = vb + i * blockDim.x;
+          xs[i] = v < vhi ? ld_logit<T>(a.target, rowp + v) : 0.f;
+          ys[i] = v < vhi ? ld_logit<T>(a.draft, rowp + v) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int v = vb + i * blockDim.x;
+          if (v < vhi) {
+            float P, Q;
+            eval_pq(res, v, ptx::ex2(fmaf(xs[i], a.c2, -l2p)), ptx::ex2(fmaf(ys[i], a.c2, -l2q)), P, Q);
+            zs += to_fix(fmaxf(P - Q, 0.f));
+          }
+        }
       }
-      const double z = block_sum_d(zs, red);
+      unsigned long long ztot = 0, dummy;
+      block_scan_u64(zs, red, &ztot);
+      const unsigned long long zall = cluster_total(ztot, &dummy);
       if (tid == 0) {
+        const double z = (double)zall * 0x1p-56;
         const int j = res.nrej;
         const int t = s_tok[c];
-        const float q0 = exp2f(fmaf(ld_logit<T>(a.draft, rowp + t), a.c2, -l2q));
+        const float q0 = ptx::ex2(fmaf(ld_logit<T>(a.draft, rowp + t), a.c2, -l2q));
         res.tok[j] = t;
         res.invz[j] = z > 0.0 ? (float)(1.0 / z) : 0.f;
         const float dprev = res.invd[j] > 0.f ? 1.f / res.invd[j] : 0.f;
@@ -190,79 +292,81 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
     }
     if (s_found >= 0) {
       const int c = s_found;
-      if (tid == 0) a.accepted[(size_t)b * N + len] = c;
+      if (tid == 0 && crank == 0) a.accepted[(size_t)b * N + len] = c;
       ++len;
       u = c;
       __syncthreads();
       continue;
     }
-    // ---- final draw from the current P by inverse CDF (blocked fp64 scan)
-    const int per = (V + blockDim.x - 1) / blockDim.x;
-    const int v0 = min(V, tid * per), v1 = min(V, v0 + per);
-    double loc = 0.0;
-    for (int v = v0; v < v1; ++v) {
-      const float p0 = exp2f(fmaf(ld_logit<T>(a.target, rowp + v), a.c2, -l2p));
-      const float q0 = res.nrej ? exp2f(fmaf(ld_logit<T>(a.draft, rowp + v), a.c2, -l2q)) : 0.f;
-      float P, Q;
-      eval_pq(res, v, p0, q0, P, Q);
-      loc += (double)P;
-    }
-    // exclusive scan of `loc` across the block
-    double incl = loc;
+    // ---- final draw from the current P by inverse CDF: smallest v with
+    // target < prefix(v), target = floor(r * total), all in exact 2^-56 units
+    const int per = (vhi - vlo + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int v0 = min(vhi, vlo + tid * per), v1 = min(vhi, v0 + per);
+    // fixed-point terms P(v) of v0 + i, i < kBatch (below v1), loads issued together
+    auto terms = [&](int vb, unsigned long long* out) {
+      float xs[kBatch], ys[kBatch];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      double y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) red[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-      double x = red[lane];
-      double xi = x;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        double y = __shfl_up_sync(0xffffffffu, xi, o);
-        if (lane >= o) xi += y;
+      for (int i = 0; i < kBatch; ++i) {
+        const int v = vb + i;
+        xs[i] = v < v1 ? ld_logit<T>(a.target, rowp + v) : 0.f;
+        ys[i] = (v < v1 && res.nrej) ? ld_logit<T>(a.draft, rowp + v) : 0.f;
       }
-      red[lane] = xi - x;
-      if (lane == 31) red[32] = xi;
-    }
-    __syncthreads();
-    const double excl = red[wid] + (incl - loc);
-    const double total = red[32];
-    const float r = philox_uniform(a.seed, a.round, b, u, 0, 1);
-    const double target = (double)r * total;
-    if (tid == 0) s_found = 0x7fffffff;
-    __syncthreads();
-    if (target >= excl && target < excl + loc) {
-      // this thread's slice holds the crossing: smallest v with target < prefix(v)
-      double run = excl;
-      int pick = -1, last_pos = -1;
-      for (int v = v0; v < v1; ++v) {
-        const float p0 = exp2f(fmaf(ld_logit<T>(a.target, rowp + v), a.c2, -l2p));
-        const float q0 = res.nrej ? exp2f(fmaf(ld_logit<T>(a.draft, rowp + v), a.c2, -l2q)) : 0.f;
-        float P, Q;
-        eval_pq(res, v, p0, q0, P, Q);
-        if (P > 0.f) last_pos = v;
-        run += (double)P;
-        if (target < run) {
-          pick = v;
-          break;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int v = vb + i;
+        out[i] = 0;
+        if (v < v1) {
+          float P, Q;
+          eval_pq(res, v, ptx::ex2(fmaf(xs[i], a.c2, -l2p)), res.nrej ? ptx::ex2(fmaf(ys[i], a.c2, -l2q)) : 0.f,
+                  P, Q);
+          out[i] = to_fix(P);
         }
       }
-      if (pick < 0) pick = last_pos;
-      if (pick >= 0) atomicMin(&s_found, pick);
+    };
+    unsigned long long loc = 0;
+    for (int vb = v0; vb < v1; vb += kBatch) {
+      unsigned long long tb[kBatch];
+      terms(vb, tb);
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) loc += tb[i];
     }
-    __syncthreads();
-    if (tid == 0 && s_found == 0x7fffffff) s_found = V - 1;
-    __syncthreads();
-    if (tid == 0) {
-      a.out_token[b] = s_found;
-      a.accept_len[b] = len;
+    unsigned long long mine = 0, below = 0;
+    const unsigned long long excl = block_scan_u64(loc, red, &mine);
+    const unsigned long long total = cluster_total(mine, &below);
+    const float r = philox_uniform(a.seed, a.round, b, u, 0, 1);
+    const unsigned long long r24 = (unsigned long long)(r * 16777216.0f);  // r = k * 2^-24 exactly
+    const unsigned long long target = (total >> 24) * r24 + (((total & 0xFFFFFFull) * r24) >> 24);
+    if (total > 0) {
+      const unsigned long long lo = below + excl;
+      if (target >= lo && target < lo + loc) {
+        // this thread's slice holds the crossing
+        unsigned long long run = lo;
+        int pick = v1 - 1;
+        bool done = false;
+        for (int vb = v0; vb < v1 && !done; vb += kBatch) {
+          unsigned long long tb[kBatch];
+          terms(vb, tb);
+#pragma unroll
+          for (int i = 0; i < kBatch; ++i) {
+            run += tb[i];
+            if (!done && vb + i < v1 && target < run) {
+              pick = vb + i;
+              done = true;
+            }
+          }
+        }
+        a.out_token[b] = pick;
+      }
+    } else if (tid == 0 && crank == 0) {
+      a.out_token[b] = V - 1;
     }
-    for (int j = len + tid; j < N; j += blockDim.x) a.accepted[(size_t)b * N + j] = -1;
-    return;
+    if (crank == 0) {
+      if (tid == 0) a.accept_len[b] = len;
+      for (int j = len + tid; j < N; j += blockDim.x) a.accepted[(size_t)b * N + j] = -1;
+    }
+    break;
   }
+  ptx::cluster_sync();  // the other CTAs may still read this CTA's partial sums
 }
 
 cudaError_t launch_sample_walk(const void* target, const void* draft, const int32_t* parent,
@@ -288,10 +392,49 @@ cudaError_t launch_sample_walk(const void* target, const void* draft, const int3
   a.accept_len = accept_len;
   a.out_token = out_token;
   a.dev_status = dev_status;
-  if (dtype == TV_BF16)
-    sample_walk_kernel<uint16_t><<<B, kWalkThreads, 0, stream>>>(a);
-  else
-    sample_walk_kernel<float><<<B, kWalkThreads, 0, stream>>>(a);
+  // 16 CTAs per cluster where the device can co-schedule them, else the portable 8
+  static int csize_cache[64][2] = {};  // per device and element type (each kernel has its own attribute)
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int ti = dtype == TV_BF16 ? 1 : 0;
+  int csize = (dev >= 0 && dev < 64) ? csize_cache[dev][ti] : 0;
+  if (csize == 0) {
+    csize = 8;
+    auto kern = dtype == TV_BF16 ? sample_walk_kernel<uint16_t> : sample_walk_kernel<float>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(kWalkClusterMax);
+      q.blockDim = dim3(kWalkThreads);
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = kWalkClusterMax;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      int nclusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &q) == cudaSuccess && nclusters > 0)
+        csize = kWalkClusterMax;
+    }
+    cudaGetLastError();  // a refused query leaves the portable size
+    if (dev >= 0 && dev < 64) csize_cache[dev][ti] = csize;
+  }
+  a.csize = csize;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)B * csize);
+  cfg.blockDim = dim3(kWalkThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = dtype == TV_BF16 ? cudaLaunchKernelEx(&cfg, sample_walk_kernel<uint16_t>, a)
+                                   : cudaLaunchKernelEx(&cfg, sample_walk_kernel<float>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -34,16 +34,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase with the given parity.  Gives up (returns false) after
-// TV_WAIT_NS nanoseconds or as soon as *abort is set by another thread of the CTA.
+// TV_WAIT_NS nanoseconds or as soon as *abort is set by another thread of the CTA.  The
+// flag and the clock are looked at only every 64 polls, so a completed phase is seen
+// within one poll.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > TV_WAIT_NS) {
-      *abort = 1;
-      return false;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > TV_WAIT_NS) {
+        *abort = 1;
+        return false;
+      }
     }
   }
 }
