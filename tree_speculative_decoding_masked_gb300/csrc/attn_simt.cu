@@ -85,9 +85,15 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(const T* __r
     if (j < total) {
       krow = j < P ? j : P + s_anc[warp][j - P];
       const T* kr = k + kvbase + (size_t)krow * D;
-      float dot = 0.f;
-      for (int d = 0; d < D; ++d) dot = fmaf(s_q[warp][d], ldx(kr, d), dot);
-      s = dot * scale;
+      // eight independent partial dot products, so that the row's loads overlap
+      float dot[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) dot[u] = 0.f;
+      for (int d0 = 0; d0 < D; d0 += 8)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (d0 + u < D) dot[u] = fmaf(s_q[warp][d0 + u], ldx(kr, d0 + u), dot[u]);
+      s = (((dot[0] + dot[1]) + (dot[2] + dot[3])) + ((dot[4] + dot[5]) + (dot[6] + dot[7]))) * scale;
     }
     const float mnew = fmaxf(m, warp_max(s));
     const float corr = exp2f((m - mnew) * kLog2e);
@@ -96,12 +102,22 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(const T* __r
 #pragma unroll
     for (int t = 0; t < kDPL; ++t) acc[t] *= corr;
     const int cnt = min(32, total - j0);
-    for (int jj = 0; jj < cnt; ++jj) {
-      const float pj = __shfl_sync(0xffffffffu, p, jj);
-      const int rj = __shfl_sync(0xffffffffu, krow, jj);
-      const T* vr = v + kvbase + (size_t)rj * D;
+    for (int jb = 0; jb < cnt; jb += 4) {
+      // four value rows at a time: all their loads are issued before the FMAs
+      float vv[4][kDPL], pj[4];
 #pragma unroll
-      for (int t = 0; t < kDPL; ++t) acc[t] = fmaf(pj, ldx(vr, lane + 32 * t), acc[t]);
+      for (int u = 0; u < 4; ++u) {
+        const int jj = min(jb + u, cnt - 1);
+        pj[u] = jb + u < cnt ? __shfl_sync(0xffffffffu, p, jj) : 0.f;
+        const int rj = __shfl_sync(0xffffffffu, krow, jj);
+        const T* vr = v + kvbase + (size_t)rj * D;
+#pragma unroll
+        for (int t = 0; t < kDPL; ++t) vv[u][t] = lane + 32 * t < D ? ldx(vr, lane + 32 * t) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int t = 0; t < kDPL; ++t) acc[t] = fmaf(pj[u], vv[u][t], acc[t]);
     }
     m = mnew;
   }
