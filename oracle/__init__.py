@@ -23,6 +23,8 @@ sampling   blog, "acceptance probability for sampling" (alpha = min(1, p/q)) and
            "how to correct after a rejection" ((p - q)+ normalised).
 selection  TAPS §4.1-§4.2 (candidate pool from per-position top-K marginals, budgeted
            prefix-closed subtree) and TreeGraft §3.1 (cumulative path score s(v)).
+kvcommit   blog, "KV cache handling": keep the accepted tokens' cache entries, drop the
+           rejected candidates' (the accepted root path laid out as a plain sequence).
 
 Readings taken where the pages are silent are listed in each module's docstring.
 Parity status: every function is pinned by tests under ``tests/test_oracle_*.py``
