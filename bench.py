@@ -412,6 +412,10 @@ def run_ours(args):
             tv.verify_greedy(s["logits"], sel_out["parent"], sel_out["tokens"], workspace=ws_ver, dev_status=status,
                              out=ver_out)
 
+    def k_commit(s):
+        # keep the accepted path's KV rows (timed in the breakdown, not part of the step)
+        tv.commit_accepted_kv(s["k"], s["v"], ver_out["accepted_nodes"], ver_out["accept_len"], P, dev_status=status)
+
     side = torch.cuda.Stream(device=dev)
 
     def step(s):
@@ -450,6 +454,7 @@ def run_ours(args):
         g_sel = [capture(lambda s=s: k_select(s)) for s in sets] if use_pool else None
         g_att = [capture(lambda s=s: k_attn(s)) for s in sets]
         g_ver = [capture(lambda s=s: k_verify(s)) for s in sets]
+        g_com = [capture(lambda s=s: k_commit(s)) for s in sets]
     torch.cuda.synchronize()
 
     def timed(fn, reps):
@@ -499,6 +504,8 @@ def run_ours(args):
     br = {"attention": timed(fam(g_att), reps) * 1e3 / reps, "verify": timed(fam(g_ver), reps) * 1e3 / reps}
     if use_pool:
         br["select"] = timed(fam(g_sel), reps) * 1e3 / reps
+    br["commit"] = timed(fam(g_com), reps) * 1e3 / reps
+    commit_bytes = int(ver_out["accept_len"].sum().item()) * Hkv * D * elt * 2 * 2  # K and V rows, read + write
     peak, peak_kind = measured_peaks()
     fam_bytes = {"attention": bytes_attn, "verify": bytes_vocab}
     dom = max(("attention", "verify"), key=lambda kk: br[kk])
@@ -546,6 +553,7 @@ def run_ours(args):
                            parallelism=f"replicas x{world}"),
             "path_gbs": bytes_set / (ms_per_step * 1e-3) / 1e9,
             "breakdown_us": br,
+            "commit_bytes_per_launch": commit_bytes,
             "roofline": roofline,
             "cpu_baseline": cpu_base,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

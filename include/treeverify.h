@@ -7,6 +7,7 @@
  *   tv_tree_attention   tree-masked grouped-query attention over prefix KV + tree KV
  *   tv_verify_greedy    fused vocab pass + greedy longest-match walk + bonus token
  *   tv_verify_sample    fused vocab pass + min(1,p/q) walk + residual resampling
+ *   tv_commit_accepted_kv  keep the accepted path's cache rows (contiguous), drop the rest
  *
  * Conventions shared by every call
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless marked
@@ -202,6 +203,26 @@ TV_API tv_status tv_verify_sample(const void* target_logits, const void* draft_l
                            int32_t* accepted_nodes, int32_t* accept_len, int32_t* out_token,
                            float* p_draft, float* q_draft, void* workspace, size_t ws_bytes,
                            int32_t* dev_status, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * tv_commit_accepted_kv - keep the accepted root path's keys and values.
+ * Blog, "KV cache handling": after verification only the accepted tokens' cache entries
+ * stay in the target cache.  The tree's rows sit at P + t (root at P); for each sequence
+ * b with L = accept_len[b] accepted nodes a_1..a_L (accepted_nodes[b][0..L-1], as
+ * written by tv_verify_greedy / tv_verify_sample), row P + a_k of every KV head of both
+ * caches is copied to row P + k, in place, so rows [0, P + L] become the cache of the
+ * plain sequence prefix, root, a_1..a_L.  Other rows are left as they are.
+ *   k_cache, v_cache [B][Hkv][kv_stride_tokens][D] (in/out), kv_stride_tokens >= P + N
+ *   accepted_nodes [B][N] int32, accept_len [B] int32
+ * Device checks: a_1 > 0, increasing, < N, and 0 <= L < N (TV_DEV_BAD_TREE otherwise;
+ * that sequence's cache is then partly or not updated).  Host errors: NULL pointers,
+ * sizes, D * element size not a multiple of 16 bytes or misaligned caches.
+ * No workspace.
+ */
+TV_API tv_status tv_commit_accepted_kv(void* k_cache, void* v_cache, const int32_t* accepted_nodes,
+                                const int32_t* accept_len, int B, int Hkv, int D, int P, int N,
+                                int kv_stride_tokens, tv_dtype dtype, int32_t* dev_status,
+                                tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * tv_select_subtree - budgeted prefix-closed subtree from a block-marginal pool.

@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     TV_DEV_TIMEOUT,
     TV_F32,
     TreeVerifyError,
+    commit_accepted_kv,
     exported_symbols,
     library_path,
     load_library,

@@ -47,6 +47,7 @@ _SIGS = {
     "tv_verify_greedy": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tv_verify_greedy_static": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "tv_verify_sample": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _U64, _U64, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "tv_commit_accepted_kv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "tv_select_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "tv_select_subtree": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
 }
@@ -175,6 +176,23 @@ def tree_attention(q, k_cache, v_cache, parent, prefix_len: int, *, scale: float
                                  int(prefix_len), N, S, float(scale), code, _ptr(ws),
                                  ws.numel() * ws.element_size(), _ptr(st), _stream()))
     return out
+
+
+def commit_accepted_kv(k_cache, v_cache, accepted_nodes, accept_len, prefix_len: int, *, dev_status=None):
+    """Move the accepted root path's cache rows P + a_k to P + k, in place, for every KV
+    head of k_cache and v_cache [B][Hkv][S][D].  accepted_nodes [B][N], accept_len [B]
+    as returned by verify_greedy / verify_sample."""
+    _need_cuda(k_cache=k_cache, v_cache=v_cache, accepted_nodes=accepted_nodes, accept_len=accept_len)
+    lib = load_library()
+    B, Hkv, S, D = k_cache.shape
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache must match")
+    N = accepted_nodes.shape[1]
+    st = _status_tensor(dev_status, k_cache.device)
+    _check("tv_commit_accepted_kv",
+           lib.tv_commit_accepted_kv(_ptr(k_cache), _ptr(v_cache), _ptr(accepted_nodes), _ptr(accept_len), B, Hkv,
+                                     D, int(prefix_len), N, S, _dtype_code(k_cache), _ptr(st), _stream()))
+    return k_cache, v_cache
 
 
 def verify_workspace_size(B, N, V, dtype, sampling: bool) -> int:

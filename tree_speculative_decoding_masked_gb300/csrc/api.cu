@@ -137,6 +137,21 @@ tv_status tv_verify_sample(const void* target_logits, const void* draft_logits, 
                                         st(stream)));
 }
 
+tv_status tv_commit_accepted_kv(void* k_cache, void* v_cache, const int32_t* accepted_nodes,
+                                const int32_t* accept_len, int B, int Hkv, int D, int P, int N, int kv_stride_tokens,
+                                tv_dtype dtype, int32_t* dev_status, tv_stream_t stream) {
+  if (!k_cache || !v_cache || !accepted_nodes || !accept_len) return TV_ERR_NULL;
+  if (!valid_dtype(dtype)) return TV_ERR_DTYPE;
+  if (B < 1 || Hkv < 1 || D < 1 || P < 0 || N < 1 || N > kMaxNodes) return TV_ERR_SHAPE;
+  if ((long long)kv_stride_tokens < (long long)P + N) return TV_ERR_SHAPE;
+  const long long row_bytes = (long long)D * (dtype == TV_BF16 ? 2 : 4);
+  if (row_bytes % 16) return TV_ERR_ALIGN;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return TV_ERR_ALIGN;
+  if ((long long)B * Hkv * 2 * (row_bytes / 16) > 0x7fffffffLL * 256) return TV_ERR_SHAPE;
+  return cuda_status(launch_kv_commit(k_cache, v_cache, accepted_nodes, accept_len, B, Hkv, D, P, N,
+                                      kv_stride_tokens, dtype, dev_status, st(stream)));
+}
+
 size_t tv_select_workspace_size(int B, int d, int K, int budget) { return select_ws_bytes(B, d, K, budget); }
 
 tv_status tv_select_subtree(const float* marg, const int32_t* pool_tokens, int B, int d, int K, int budget,

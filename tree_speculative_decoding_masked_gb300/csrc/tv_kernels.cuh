@@ -34,6 +34,11 @@ cudaError_t launch_tree_prep(const int32_t* parent, int B, int N, int P, int32_t
                              uint32_t* anc_mask, int32_t* child_off, int32_t* child_idx,
                              int32_t* dev_status, cudaStream_t stream);
 
+// ---- accepted-path KV commit
+cudaError_t launch_kv_commit(void* k_cache, void* v_cache, const int32_t* accepted, const int32_t* accept_len,
+                             int B, int Hkv, int D, int P, int N, int S, tv_dtype dtype, int32_t* dev_status,
+                             cudaStream_t stream);
+
 // ---- selection
 size_t select_ws_bytes(int B, int d, int K, int budget);
 cudaError_t launch_select(const float* marg, const int32_t* ptok, int B, int d, int K, int budget,
