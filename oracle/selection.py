@@ -82,3 +82,58 @@ def select_subtree(marg, pool_tokens, budget: int, root_token: int):
             heapq.heappush(heap, (-float(ss), dep, path[:-1] + (r + 1,), par, par_s))
     return {"parent": parent, "token": token, "depth": depth, "score": score,
             "paths": paths, "n_nodes": n}
+
+
+# ------------------------------------------------------------------------------------
+# Cost-aware size of the verified tree.
+#
+# TAPS §3.1 (limitation 2): verification latency grows with the number of selected
+# nodes (64 -> 512 nodes took 33 -> 81 ms in the paper's figure) while each round still
+# commits one prefix; §3.2: the selector should pick a compact prefix-closed subtree
+# that maximises expected accepted tokens per unit of verification cost rather than
+# fill the budget.
+#
+# Readings
+#   * Expected tokens of a round with the first n rows of the selection order (root
+#     included) = 1 + sum of s over its n - 1 drafts: under the edge-score reading s(v)
+#     is the probability that v is accepted, and every round also yields one token from
+#     the target (the bonus or corrected token).
+#   * Verification cost of n rows = cost_base + cost_per_row * n, a line fitted to the
+#     measured step time against the tree size.
+#   * n* = the smallest n in [1, available rows] that maximises
+#     (1 + sum_{i<n} s_i) / (cost_base + cost_per_row * n).  For a result that does not
+#     depend on the order of additions, every score is first rounded to a multiple of
+#     2^-40 (round half to even) and the sums are exact integers; numerator, denominator
+#     and quotient are then single IEEE double operations.
+FIX_BITS = 40
+
+
+def adaptive_rows(scores, cost_base: float, cost_per_row: float) -> int:
+    """scores: the selected rows' scores in selection order, root first (any value)."""
+    cost_base = float(np.float32(cost_base))
+    cost_per_row = float(np.float32(cost_per_row))
+    unit = 2 ** FIX_BITS
+    best_n, best = 1, None
+    acc = 0  # exact sum of the rounded draft scores so far
+    for n in range(1, len(scores) + 1):
+        if n > 1:
+            acc += round(float(np.float32(scores[n - 1])) * unit)
+        num = float(unit + acc)
+        den = cost_base + cost_per_row * float(n)
+        val = num / den
+        if best is None or val > best:
+            best, best_n = val, n
+    return best_n
+
+
+def select_subtree_adaptive(marg, pool_tokens, budget: int, root_token: int, cost_base: float,
+                            cost_per_row: float):
+    """select_subtree(budget) cut to its cost-aware prefix of n* rows (rows beyond it
+    become -1 / score 0, like rows past the available candidates)."""
+    res = select_subtree(marg, pool_tokens, budget, root_token)
+    n_avail = int(res["n_nodes"])
+    n = adaptive_rows(res["score"][:n_avail], cost_base, cost_per_row)
+    for key, fill in (("parent", -1), ("token", -1), ("depth", -1), ("score", 0.0)):
+        res[key][n:] = fill
+    res["n_nodes"] = n
+    return res

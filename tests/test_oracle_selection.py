@@ -114,3 +114,63 @@ def test_budget_beyond_pool_takes_whole_tree():
     got = selection.select_subtree(marg, ptok, 100, 0)
     assert got["n_nodes"] == 1 + 3 + 9 + 27
     assert sorted(got["paths"][1:]) == sorted(_all_paths(3, 3))
+
+
+# ---- cost-aware row count (TAPS §3.1 limitation 2, §3.2)
+from fractions import Fraction  # noqa: E402
+
+import synth.workloads as W  # noqa: E402
+
+
+def _exact_best(scores, a, b):
+    """Independent restatement with exact rationals of the 2^-40-rounded scores."""
+    unit = 2 ** selection.FIX_BITS
+    best, best_n, acc = None, 1, Fraction(0)
+    for n in range(1, len(scores) + 1):
+        if n > 1:
+            acc += Fraction(round(float(np.float32(scores[n - 1])) * unit), unit)
+        val = (1 + acc) / (Fraction(float(np.float32(a))) + Fraction(float(np.float32(b))) * n)
+        if best is None or val > best:
+            best, best_n = val, n
+    return best_n
+
+
+@pytest.mark.parametrize("s,a,b,expect_all", [
+    (0.5, 8.0, 1.0, True),    # s*a = 4 > b*(1-s) = 0.5: every row pays
+    (0.5, 0.5, 1.0, False),   # 0.25 < 0.5: the root alone is best
+    (0.25, 4.0, 2.0, False),  # 1.0 < 1.5
+    (0.75, 4.0, 2.0, True),   # 3.0 > 0.5
+])
+def test_adaptive_equal_scores_closed_form(s, a, b, expect_all):
+    # (1 + (n-1)s) / (a + bn) is monotone in n, increasing iff s*a > b*(1-s)
+    scores = [1.0] + [s] * 30
+    n = selection.adaptive_rows(scores, a, b)
+    assert n == (31 if expect_all else 1)
+
+
+def test_adaptive_flat_cost_takes_everything_and_zero_base_takes_the_root():
+    scores = [1.0, 0.9, 0.5, 0.3, 0.2, 0.05]
+    assert selection.adaptive_rows(scores, 1.0, 2.0 ** -30) == len(scores)
+    assert selection.adaptive_rows(scores, 0.0, 1.0) == 1  # average score per row only falls
+
+
+def test_adaptive_matches_exact_rationals():
+    g = synth.rng(77)
+    for _ in range(200):
+        n = int(g.integers(1, 40))
+        scores = [1.0] + sorted(g.random(n - 1).astype(np.float32).tolist(), reverse=True)
+        a = float(np.float32(g.uniform(0.0, 20.0)))
+        b = float(np.float32(g.uniform(0.01, 2.0)))
+        assert selection.adaptive_rows(scores, a, b) == _exact_best(scores, a, b)
+
+
+def test_adaptive_selection_is_a_prefix():
+    g = synth.rng(78)
+    marg, ptok = W.pools(g, 1, 8, 6, 5000)
+    full = selection.select_subtree(marg[0], ptok[0], 40, 3)
+    cut = selection.select_subtree_adaptive(marg[0], ptok[0], 40, 3, 6.0, 0.25)
+    n = cut["n_nodes"]
+    assert 1 <= n <= full["n_nodes"]
+    for key in ("parent", "token", "depth", "score"):
+        assert np.array_equal(cut[key][:n], full[key][:n])
+        assert np.all(cut[key][n:] == (0 if key == "score" else -1))
