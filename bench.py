@@ -412,6 +412,15 @@ def run_ours(args):
             tv.verify_greedy(s["logits"], sel_out["parent"], sel_out["tokens"], workspace=ws_ver, dev_status=status,
                              out=ver_out)
 
+    # cost line for the cost-aware selection: step time against tree rows, fitted to this
+    # bench's own budget_sweep runs (attention + verify, B=16): ~38 us + 3.09 us per row
+    cost_line = (38.0, 3.09)
+    sel_ad_out = {kk: torch.empty_like(t) for kk, t in sel_out.items()}
+
+    def k_select_adaptive(s):
+        if use_pool:
+            tv.select_subtree(s["marg"], s["ptok"], N, s["root"], dev_status=status, out=sel_ad_out, cost=cost_line)
+
     def k_commit(s):
         # keep the accepted path's KV rows (timed in the breakdown, not part of the step)
         tv.commit_accepted_kv(s["k"], s["v"], ver_out["accepted_nodes"], ver_out["accept_len"], P, dev_status=status)
@@ -452,6 +461,7 @@ def run_ours(args):
         g_all = capture(lambda: [step(s) for s in sets])          # one step per input set
         g_one = [capture(lambda s=s: step(s)) for s in sets]
         g_sel = [capture(lambda s=s: k_select(s)) for s in sets] if use_pool else None
+        g_sad = [capture(lambda s=s: k_select_adaptive(s)) for s in sets] if use_pool else None
         g_att = [capture(lambda s=s: k_attn(s)) for s in sets]
         g_ver = [capture(lambda s=s: k_verify(s)) for s in sets]
         g_com = [capture(lambda s=s: k_commit(s)) for s in sets]
@@ -504,6 +514,7 @@ def run_ours(args):
     br = {"attention": timed(fam(g_att), reps) * 1e3 / reps, "verify": timed(fam(g_ver), reps) * 1e3 / reps}
     if use_pool:
         br["select"] = timed(fam(g_sel), reps) * 1e3 / reps
+        br["select_adaptive"] = timed(fam(g_sad), reps) * 1e3 / reps
     br["commit"] = timed(fam(g_com), reps) * 1e3 / reps
     commit_bytes = int(ver_out["accept_len"].sum().item()) * Hkv * D * elt * 2 * 2  # K and V rows, read + write
     peak, peak_kind = measured_peaks()

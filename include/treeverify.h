@@ -3,6 +3,7 @@
  *
  * One verification round of tree speculative decoding, on one GPU:
  *   tv_select_subtree   budgeted prefix-closed subtree from a block-marginal pool
+ *   tv_select_subtree_adaptive  the same, cut where expected tokens per unit cost peak
  *   tv_tree_prep        ancestor bitmask, depth / position ids, child lists
  *   tv_tree_attention   tree-masked grouped-query attention over prefix KV + tree KV
  *   tv_verify_greedy    fused vocab pass + greedy longest-match walk + bonus token
@@ -250,6 +251,27 @@ TV_API tv_status tv_select_subtree(const float* marg, const int32_t* pool_tokens
                             int32_t* tokens, int32_t* depth, float* score, int32_t* n_nodes,
                             void* workspace, size_t ws_bytes, int32_t* dev_status,
                             tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * tv_select_subtree_adaptive - tv_select_subtree cut to its cost-aware prefix.
+ * TAPS §3.1 (limitation 2: verification latency grows with the selected node count)
+ * and §3.2 (choose the compact prefix-closed subtree that maximises expected accepted
+ * tokens per unit of verification cost instead of filling the budget).  Of the rows
+ * tv_select_subtree(budget) would return, keeps the first n*, the smallest n in
+ * [1, rows available] maximising
+ *     (1 + sum_{i=1}^{n-1} score[i]) / (cost_base + cost_per_row * n)
+ * where every score is first rounded to a multiple of 2^-40 and summed exactly, and
+ * the ratio is an IEEE double division (so the choice does not depend on summation
+ * order).  cost_base, cost_per_row: a line fitted to measured verification time
+ * against tree rows (any unit, same for both).  Rows past n* hold -1 (score 0) and
+ * n_nodes[b] = n*.  Other arguments, limits and workspace as tv_select_subtree.
+ * Host errors: cost_base < 0, cost_per_row <= 0 or not finite -> TV_ERR_VALUE.
+ */
+TV_API tv_status tv_select_subtree_adaptive(const float* marg, const int32_t* pool_tokens, int B, int d,
+                                     int K, int budget, float cost_base, float cost_per_row,
+                                     const int32_t* root_token, int32_t* parent, int32_t* tokens,
+                                     int32_t* depth, float* score, int32_t* n_nodes, void* workspace,
+                                     size_t ws_bytes, int32_t* dev_status, tv_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -112,3 +112,37 @@ def test_tree_prep_flags_bad_parent():
     out = tv.tree_prep(i32(par), 0)
     torch.cuda.synchronize()
     assert int(out["dev_status"][0]) & tv.TV_DEV_BAD_TREE
+
+
+# ---- cost-aware tree size (tv_select_subtree_adaptive), bit-exact against the oracle
+@pytest.mark.parametrize("B,d,k,budget,cost", [
+    (1, 16, 4, 64, (20.0, 0.25)),     # a qwen3-like pool: the cut falls inside the budget
+    (3, 8, 6, 40, (6.0, 0.25)),
+    (16, 16, 32, 1024, (60.0, 0.05)),  # thousands of rows: several rows per thread in the scan
+    (2, 4, 3, 30, (1.0, 2.0 ** -20)),  # nearly flat cost: every available row
+    (2, 6, 5, 50, (0.0, 1.0)),         # no base cost: the root alone
+])
+def test_adaptive_budget_matches_oracle(B, d, k, budget, cost):
+    g = synth.rng(5000 + budget + k)
+    marg, ptok = W.pools(g, B, d, k, 3000)
+    roots = np.arange(B, dtype=np.int32) + 5
+    out = tv.select_subtree(torch.from_numpy(marg).to(dev()), i32(ptok), budget, i32(roots), cost=cost)
+    torch.cuda.synchronize()
+    got = {kk: v.cpu().numpy() for kk, v in out.items()}
+    for b in range(B):
+        ref = selection.select_subtree_adaptive(marg[b], ptok[b], budget, int(roots[b]), *cost)
+        assert int(got["n_nodes"][b]) == ref["n_nodes"]
+        assert np.array_equal(got["parent"][b], ref["parent"])
+        assert np.array_equal(got["tokens"][b], ref["token"])
+        assert np.array_equal(got["depth"][b], ref["depth"])
+        assert np.array_equal(got["score"][b].view(np.uint32), ref["score"].view(np.uint32))
+    assert int(got["dev_status"][0]) == 0
+
+
+def test_adaptive_budget_rejects_bad_costs():
+    g = synth.rng(5100)
+    marg, ptok = W.pools(g, 1, 4, 3, 100)
+    m, p, r = torch.from_numpy(marg).to(dev()), i32(ptok), i32(np.array([1]))
+    for cost in ((1.0, 0.0), (-1.0, 1.0), (float("inf"), 1.0)):
+        with pytest.raises(tv.TreeVerifyError):
+            tv.select_subtree(m, p, 10, r, cost=cost)

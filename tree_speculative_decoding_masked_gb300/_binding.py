@@ -50,6 +50,7 @@ _SIGS = {
     "tv_commit_accepted_kv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "tv_select_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "tv_select_subtree": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "tv_select_subtree_adaptive": (_I, [_P, _P, _I, _I, _I, _I, _F, _F, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
 }
 
 
@@ -288,9 +289,11 @@ def select_workspace_size(B, d, K, budget) -> int:
     return int(load_library().tv_select_workspace_size(B, d, K, budget))
 
 
-def select_subtree(marg, pool_tokens, budget: int, root_token, *, dev_status=None, out=None):
+def select_subtree(marg, pool_tokens, budget: int, root_token, *, dev_status=None, out=None, cost=None):
     """TAPS-style budgeted prefix-closed subtree.  marg [B][d][K] float32 (sorted per
-    position), pool_tokens [B][d][K] int32, root_token [B] int32."""
+    position), pool_tokens [B][d][K] int32, root_token [B] int32.  With
+    cost=(cost_base, cost_per_row) the tree is cut where expected tokens per unit of
+    verification cost peak (tv_select_subtree_adaptive)."""
     _need_cuda(marg=marg, pool_tokens=pool_tokens, root_token=root_token)
     if marg.dtype != torch.float32 or pool_tokens.dtype != torch.int32:
         raise TypeError("marg must be float32 and pool_tokens int32")
@@ -306,8 +309,15 @@ def select_subtree(marg, pool_tokens, budget: int, root_token, *, dev_status=Non
     ws_need = select_workspace_size(B, d, K, budget)
     ws = _workspace(ws_need, dev, None) if ws_need else None
     st = _status_tensor(dev_status, dev)
-    _check("tv_select_subtree",
-           lib.tv_select_subtree(_ptr(marg), _ptr(pool_tokens), B, d, K, int(budget), _ptr(root_token), _ptr(par),
-                                 _ptr(tok), _ptr(dep), _ptr(sc), _ptr(nn), _ptr(ws),
-                                 0 if ws is None else ws.numel(), _ptr(st), _stream()))
+    if cost is None:
+        _check("tv_select_subtree",
+               lib.tv_select_subtree(_ptr(marg), _ptr(pool_tokens), B, d, K, int(budget), _ptr(root_token),
+                                     _ptr(par), _ptr(tok), _ptr(dep), _ptr(sc), _ptr(nn), _ptr(ws),
+                                     0 if ws is None else ws.numel(), _ptr(st), _stream()))
+    else:
+        _check("tv_select_subtree_adaptive",
+               lib.tv_select_subtree_adaptive(_ptr(marg), _ptr(pool_tokens), B, d, K, int(budget), float(cost[0]),
+                                              float(cost[1]), _ptr(root_token), _ptr(par), _ptr(tok), _ptr(dep),
+                                              _ptr(sc), _ptr(nn), _ptr(ws), 0 if ws is None else ws.numel(),
+                                              _ptr(st), _stream()))
     return {"parent": par, "tokens": tok, "depth": dep, "score": sc, "n_nodes": nn, "dev_status": st}

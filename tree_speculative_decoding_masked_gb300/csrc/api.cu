@@ -163,7 +163,21 @@ tv_status tv_select_subtree(const float* marg, const int32_t* pool_tokens, int B
     return TV_ERR_SHAPE;
   if (ws_bytes < select_ws_bytes(B, d, K, budget)) return TV_ERR_WORKSPACE;
   return cuda_status(launch_select(marg, pool_tokens, B, d, K, budget, root_token, parent, tokens, depth, score,
-                                   n_nodes, reinterpret_cast<char*>(workspace), dev_status, st(stream)));
+                                   n_nodes, reinterpret_cast<char*>(workspace), dev_status, 0.f, 0.f, st(stream)));
+}
+
+tv_status tv_select_subtree_adaptive(const float* marg, const int32_t* pool_tokens, int B, int d, int K, int budget,
+                                     float cost_base, float cost_per_row, const int32_t* root_token, int32_t* parent,
+                                     int32_t* tokens, int32_t* depth, float* score, int32_t* n_nodes,
+                                     void* workspace, size_t ws_bytes, int32_t* dev_status, tv_stream_t stream) {
+  if (!marg || !pool_tokens || !parent || !tokens || !depth || !score || !n_nodes) return TV_ERR_NULL;
+  if (B < 1 || d < 1 || d > kMaxDepth || K < 1 || K > kMaxRank || budget < 1 || budget > kMaxBudget)
+    return TV_ERR_SHAPE;
+  if (!(cost_base >= 0.f) || isinf(cost_base) || !(cost_per_row > 0.f) || isinf(cost_per_row)) return TV_ERR_VALUE;
+  if (ws_bytes < select_ws_bytes(B, d, K, budget)) return TV_ERR_WORKSPACE;
+  return cuda_status(launch_select(marg, pool_tokens, B, d, K, budget, root_token, parent, tokens, depth, score,
+                                   n_nodes, reinterpret_cast<char*>(workspace), dev_status, cost_base, cost_per_row,
+                                   st(stream)));
 }
 
 }  // extern "C"

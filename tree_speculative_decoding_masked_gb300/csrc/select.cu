@@ -535,11 +535,86 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_c
   return 1 + take;
 }
 
+// TAPS §3.1 (limitation 2) and §3.2: verify the prefix of the selection order that
+// maximises expected tokens per unit of verification cost.  Expected tokens of the first
+// n rows = 1 + sum of the drafts' s (each s(v) is v's acceptance probability under the
+// edge-score reading, plus the round's bonus token); cost = cost_base + cost_per_row * n.
+// Scores are rounded to multiples of 2^-40 and summed exactly (64-bit integers), the
+// ratio is one IEEE double division; n* is the smallest maximiser.  Needs the CTA's
+// output writes to be complete (called after a barrier).
+constexpr float kFixUnit = 1099511627776.0f;  // 2^40
+
+__device__ int cost_aware_rows(const float* o_sc, int n_out, float cost_base, float cost_per_row) {
+  __shared__ unsigned long long red[33];
+  __shared__ double s_obj[32];
+  __shared__ int s_n[32];
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  const int T = blockDim.x;
+  __syncthreads();
+  // rows 1 .. n_out-1 in contiguous slices
+  const int nd = n_out - 1;
+  const int per = (nd + T - 1) / T;
+  const int r0 = 1 + t * per, r1 = min(n_out, r0 + per);
+  unsigned long long loc = 0;
+  for (int r = r0; r < r1; ++r) loc += __float2ull_rn(o_sc[r] * kFixUnit);
+  unsigned long long tot;
+  unsigned long long acc = block_scan_u64(loc, red, &tot);
+  const double a = (double)cost_base, bcost = (double)cost_per_row;
+  auto objective = [&](unsigned long long sum, int n) {
+    const double num = (double)(1099511627776ull + sum);
+    return __ddiv_rn(num, __dadd_rn(a, __dmul_rn(bcost, (double)n)));
+  };
+  double best = t == 0 ? objective(0ull, 1) : -1.0;
+  int best_n = t == 0 ? 1 : 0x7fffffff;
+  for (int r = r0; r < r1; ++r) {
+    acc += __float2ull_rn(o_sc[r] * kFixUnit);
+    const double v = objective(acc, r + 1);
+    if (v > best) {  // rows grow within the slice: a later row wins only if strictly better
+      best = v;
+      best_n = r + 1;
+    }
+  }
+  // largest objective, smallest n among equals
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const double ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int on = __shfl_xor_sync(0xffffffffu, best_n, o);
+    if (ov > best || (ov == best && on < best_n)) {
+      best = ov;
+      best_n = on;
+    }
+  }
+  if (lane == 0) {
+    s_obj[wid] = best;
+    s_n[wid] = best_n;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    best = lane < (T >> 5) ? s_obj[lane] : -1.0;
+    best_n = lane < (T >> 5) ? s_n[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const double ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int on = __shfl_xor_sync(0xffffffffu, best_n, o);
+      if (ov > best || (ov == best && on < best_n)) {
+        best = ov;
+        best_n = on;
+      }
+    }
+    if (lane == 0) s_n[0] = best_n;
+  }
+  __syncthreads();
+  const int n = s_n[0];
+  __syncthreads();
+  return n;
+}
+
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __restrict__ marg,
                                                              const int32_t* __restrict__ ptok, int d, int K,
                                                              int budget, const int32_t* __restrict__ root_token,
                                                              int32_t* out_parent, int32_t* out_tok, int32_t* out_depth,
-                                                             float* out_score, int32_t* n_nodes, int32_t* dev_status) {
+                                                             float* out_score, int32_t* n_nodes, int32_t* dev_status,
+                                                             float cost_base, float cost_per_row) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int hist[kSelBins > 256 ? kSelBins : 256];
   __shared__ int bcast[3 + kSelThreads / 32];
@@ -600,7 +675,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
     }
     __syncthreads();
   }
-  const int n_out = s_nout;
+  int n_out = s_nout;
+  if (cost_per_row > 0.f && n_out > 1) n_out = cost_aware_rows(o_sc, n_out, cost_base, cost_per_row);
   for (int j = n_out + tid; j < budget; j += blockDim.x) {
     o_par[j] = -1;
     o_tok[j] = -1;
@@ -621,12 +697,13 @@ size_t select_ws_bytes(int, int, int, int) { return 0; }
 
 cudaError_t launch_select(const float* marg, const int32_t* ptok, int B, int d, int K, int budget,
                           const int32_t* root_token, int32_t* parent, int32_t* tokens, int32_t* depth,
-                          float* score, int32_t* n_nodes, char*, int32_t* dev_status, cudaStream_t stream) {
+                          float* score, int32_t* n_nodes, char*, int32_t* dev_status, float cost_base,
+                          float cost_per_row, cudaStream_t stream) {
   const size_t smem = select_smem_bytes(d, K, budget);
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   select_kernel<<<B, kSelThreads, smem, stream>>>(marg, ptok, d, K, budget, root_token, parent, tokens, depth, score,
-                                                   n_nodes, dev_status);
+                                                   n_nodes, dev_status, cost_base, cost_per_row);
   return cudaGetLastError();
 }
 

@@ -81,4 +81,35 @@ __device__ __forceinline__ ArgMax argmax_merge(ArgMax a, ArgMax b) {
   return a;
 }
 
+// Block-wide exclusive scan of 64-bit values; returns this thread's exclusive prefix and
+// sets *total.  red holds at least 33 entries.
+static __device__ unsigned long long block_scan_u64(unsigned long long v, unsigned long long* red,
+                                                    unsigned long long* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) red[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const unsigned long long x = lane < (int)(blockDim.x >> 5) ? red[lane] : 0ull;
+    unsigned long long xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, xi, o);
+      if (lane >= o) xi += y;
+    }
+    red[lane] = xi - x;
+    if (lane == 31) red[32] = xi;
+  }
+  __syncthreads();
+  const unsigned long long excl = red[wid] + (incl - v);
+  *total = red[32];
+  __syncthreads();
+  return excl;
+}
+
 }  // namespace tv

@@ -43,7 +43,8 @@ cudaError_t launch_kv_commit(void* k_cache, void* v_cache, const int32_t* accept
 size_t select_ws_bytes(int B, int d, int K, int budget);
 cudaError_t launch_select(const float* marg, const int32_t* ptok, int B, int d, int K, int budget,
                           const int32_t* root_token, int32_t* parent, int32_t* tokens, int32_t* depth,
-                          float* score, int32_t* n_nodes, char* ws, int32_t* dev_status, cudaStream_t stream);
+                          float* score, int32_t* n_nodes, char* ws, int32_t* dev_status, float cost_base,
+                          float cost_per_row, cudaStream_t stream);
 
 // ---- attention
 struct AttnPlan {
