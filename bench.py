@@ -421,6 +421,16 @@ def run_ours(args):
         if use_pool:
             tv.select_subtree(s["marg"], s["ptok"], N, s["root"], dev_status=status, out=sel_ad_out, cost=cost_line)
 
+    Wm = (N + 31) // 32
+    prep_out = {"depth": torch.empty(B, N, dtype=torch.int32, device=dev),
+                "pos": torch.empty(B, N, dtype=torch.int32, device=dev),
+                "anc_mask": torch.empty(B, N, Wm, dtype=torch.int32, device=dev),
+                "child_off": torch.empty(B, N + 1, dtype=torch.int32, device=dev),
+                "child_idx": torch.empty(B, N, dtype=torch.int32, device=dev)}
+
+    def k_prep(s):
+        tv.tree_prep(sel_out["parent"], P, dev_status=status, out=prep_out)
+
     def k_commit(s):
         # keep the accepted path's KV rows (timed in the breakdown, not part of the step)
         tv.commit_accepted_kv(s["k"], s["v"], ver_out["accepted_nodes"], ver_out["accept_len"], P, dev_status=status)
@@ -465,6 +475,7 @@ def run_ours(args):
         g_att = [capture(lambda s=s: k_attn(s)) for s in sets]
         g_ver = [capture(lambda s=s: k_verify(s)) for s in sets]
         g_com = [capture(lambda s=s: k_commit(s)) for s in sets]
+        g_prep = [capture(lambda s=s: k_prep(s)) for s in sets]
     torch.cuda.synchronize()
 
     def timed(fn, reps):
@@ -516,6 +527,7 @@ def run_ours(args):
         br["select"] = timed(fam(g_sel), reps) * 1e3 / reps
         br["select_adaptive"] = timed(fam(g_sad), reps) * 1e3 / reps
     br["commit"] = timed(fam(g_com), reps) * 1e3 / reps
+    br["tree_prep"] = timed(fam(g_prep), reps) * 1e3 / reps
     commit_bytes = int(ver_out["accept_len"].sum().item()) * Hkv * D * elt * 2 * 2  # K and V rows, read + write
     peak, peak_kind = measured_peaks()
     fam_bytes = {"attention": bytes_attn, "verify": bytes_vocab}

@@ -134,18 +134,19 @@ def _status_tensor(dev_status, device):
 # ------------------------------------------------------------------------------------
 
 
-def tree_prep(parent: torch.Tensor, prefix_len: int, *, dev_status=None):
+def tree_prep(parent: torch.Tensor, prefix_len: int, *, dev_status=None, out=None):
     """Depth, position ids, packed ancestor mask and child CSR of ``parent`` [B][N]."""
     _need_cuda(parent=parent)
     lib = load_library()
     B, N = parent.shape
     dev = parent.device
     W = (N + 31) // 32
-    depth = torch.empty(B, N, dtype=torch.int32, device=dev)
-    pos = torch.empty(B, N, dtype=torch.int32, device=dev)
-    mask = torch.empty(B, N, W, dtype=torch.int32, device=dev)
-    off = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
-    idx = torch.empty(B, N, dtype=torch.int32, device=dev)
+    o = out if out is not None else {}
+    depth = _out(o, "depth", (B, N), torch.int32, dev)
+    pos = _out(o, "pos", (B, N), torch.int32, dev)
+    mask = _out(o, "anc_mask", (B, N, W), torch.int32, dev)
+    off = _out(o, "child_off", (B, N + 1), torch.int32, dev)
+    idx = _out(o, "child_idx", (B, N), torch.int32, dev)
     st = _status_tensor(dev_status, dev)
     _check("tv_tree_prep", lib.tv_tree_prep(_ptr(parent), B, N, int(prefix_len), _ptr(depth), _ptr(pos), _ptr(mask),
                                             _ptr(off), _ptr(idx), _ptr(st), _stream()))
