@@ -25,6 +25,8 @@ selection  TAPS §4.1-§4.2 (candidate pool from per-position top-K marginals, b
            prefix-closed subtree) and TreeGraft §3.1 (cumulative path score s(v)).
 kvcommit   blog, "KV cache handling": keep the accepted tokens' cache entries, drop the
            rejected candidates' (the accepted root path laid out as a plain sequence).
+frontier   TreeGraft §3.1 single-drafter expansion: frontier Top_W by s(v), the top-m
+           tokens of each frontier node's drafter distribution attached as children.
 
 Readings taken where the pages are silent are listed in each module's docstring.
 Parity status: every function is pinned by tests under ``tests/test_oracle_*.py``
