@@ -431,6 +431,20 @@ def run_ours(args):
     def k_prep(s):
         tv.tree_prep(sel_out["parent"], P, dev_status=status, out=prep_out)
 
+    # one TreeGraft-style expansion step: 8 frontier rows per sequence, top-8 children each;
+    # the first rows of the set's logits stand in for the drafter's next-token rows
+    exp_rows = min(B * 8, B * N)
+    exp_m = 8
+    exp_ps = torch.full((exp_rows,), 0.5, dtype=torch.float32, device=dev)
+    exp_ws = torch.zeros(tv.expand_workspace_size(exp_rows, V, exp_m), dtype=torch.uint8, device=dev)
+    exp_out = {"token": torch.empty(exp_rows, exp_m, dtype=torch.int32, device=dev),
+               "p": torch.empty(exp_rows, exp_m, dtype=torch.float32, device=dev),
+               "score": torch.empty(exp_rows, exp_m, dtype=torch.float32, device=dev)}
+
+    def k_expand(s):
+        tv.expand_children(s["logits"].view(B * N, V)[:exp_rows], exp_ps, exp_m, workspace=exp_ws,
+                           dev_status=status, out=exp_out)
+
     def k_commit(s):
         # keep the accepted path's KV rows (timed in the breakdown, not part of the step)
         tv.commit_accepted_kv(s["k"], s["v"], ver_out["accepted_nodes"], ver_out["accept_len"], P, dev_status=status)
@@ -475,6 +489,7 @@ def run_ours(args):
         g_att = [capture(lambda s=s: k_attn(s)) for s in sets]
         g_ver = [capture(lambda s=s: k_verify(s)) for s in sets]
         g_com = [capture(lambda s=s: k_commit(s)) for s in sets]
+        g_exp = [capture(lambda s=s: k_expand(s)) for s in sets]
         g_prep = [capture(lambda s=s: k_prep(s)) for s in sets]
     torch.cuda.synchronize()
 
@@ -528,6 +543,8 @@ def run_ours(args):
         br["select_adaptive"] = timed(fam(g_sad), reps) * 1e3 / reps
     br["commit"] = timed(fam(g_com), reps) * 1e3 / reps
     br["tree_prep"] = timed(fam(g_prep), reps) * 1e3 / reps
+    br["expand"] = timed(fam(g_exp), reps) * 1e3 / reps
+    expand_bytes = exp_rows * V * elt
     commit_bytes = int(ver_out["accept_len"].sum().item()) * Hkv * D * elt * 2 * 2  # K and V rows, read + write
     peak, peak_kind = measured_peaks()
     fam_bytes = {"attention": bytes_attn, "verify": bytes_vocab}
@@ -577,6 +594,8 @@ def run_ours(args):
             "path_gbs": bytes_set / (ms_per_step * 1e-3) / 1e9,
             "breakdown_us": br,
             "commit_bytes_per_launch": commit_bytes,
+            "expand": {"rows": exp_rows, "m": exp_m, "bytes_per_launch": expand_bytes,
+                       "gbs": expand_bytes / (br["expand"] * 1e-6) / 1e9},
             "roofline": roofline,
             "cpu_baseline": cpu_base,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -9,6 +9,7 @@
  *   tv_verify_greedy    fused vocab pass + greedy longest-match walk + bonus token
  *   tv_verify_sample    fused vocab pass + min(1,p/q) walk + residual resampling
  *   tv_commit_accepted_kv  keep the accepted path's cache rows (contiguous), drop the rest
+ *   tv_frontier_topw / tv_expand_children  one single-drafter tree-expansion step
  *
  * Conventions shared by every call
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless marked
@@ -224,6 +225,34 @@ TV_API tv_status tv_commit_accepted_kv(void* k_cache, void* v_cache, const int32
                                 const int32_t* accept_len, int B, int Hkv, int D, int P, int N,
                                 int kv_stride_tokens, tv_dtype dtype, int32_t* dev_status,
                                 tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * One single-drafter tree-expansion step (TreeGraft §3.1): the drafter ranks its
+ * candidate pool by the cumulative path score s(v) and expands the frontier
+ * F = Top_W(pool, s); each frontier node's next-token distribution contributes its
+ * top-m tokens as children, with edge score p = the drafter's probability of the token
+ * and path score s(child) = s(parent) * p.
+ *
+ * tv_frontier_topw: for each sequence b, the positions (into scores[b][0..count[b]-1])
+ * of the W highest scores, highest first; ties go to the lower position.
+ *   scores [B][C] float, count [B] int32 (<= C), out_idx [B][W] int32 (-1 past count).
+ *   Limits: 1 <= C <= 4096, 1 <= W <= C.  count outside [0, C] -> TV_DEV_BAD_TREE.
+ *
+ * tv_expand_children: for each of R drafter rows (the next-token logits after a
+ * frontier node), the top-m tokens (highest logit first, ties to the lower token id),
+ * p = softmax(logits / temperature)[token] and s = fl32(parent_score[r] * p).
+ *   draft_logits [R][V] (bf16 or fp32), parent_score [R] float,
+ *   child_token [R][m] int32, child_p, child_score [R][m] float (token -1, p = s = 0
+ *   where m > V).  Limits: 1 <= m <= 32.  temperature > 0.
+ *   Workspace: tv_expand_workspace_size(R, V, m) bytes, zero-filled before first use.
+ */
+TV_API tv_status tv_frontier_topw(const float* scores, const int32_t* count, int B, int C, int W,
+                           int32_t* out_idx, int32_t* dev_status, tv_stream_t stream);
+TV_API size_t tv_expand_workspace_size(int R, int V, int m);
+TV_API tv_status tv_expand_children(const void* draft_logits, const float* parent_score, int R, int V,
+                             int m, float temperature, tv_dtype dtype, int32_t* child_token,
+                             float* child_p, float* child_score, void* workspace, size_t ws_bytes,
+                             int32_t* dev_status, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * tv_select_subtree - budgeted prefix-closed subtree from a block-marginal pool.

@@ -12,7 +12,10 @@ from ._binding import (  # noqa: F401
     TV_F32,
     TreeVerifyError,
     commit_accepted_kv,
+    expand_children,
+    expand_workspace_size,
     exported_symbols,
+    frontier_topw,
     library_path,
     load_library,
     select_subtree,

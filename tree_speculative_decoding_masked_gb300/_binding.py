@@ -48,6 +48,9 @@ _SIGS = {
     "tv_verify_greedy_static": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "tv_verify_sample": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _U64, _U64, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tv_commit_accepted_kv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "tv_frontier_topw": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "tv_expand_workspace_size": (_SZ, [_I, _I, _I]),
+    "tv_expand_children": (_I, [_P, _P, _I, _I, _I, _F, _I, _P, _P, _P, _P, _SZ, _P, _P]),
     "tv_select_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "tv_select_subtree": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tv_select_subtree_adaptive": (_I, [_P, _P, _I, _I, _I, _I, _F, _F, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
@@ -195,6 +198,44 @@ def commit_accepted_kv(k_cache, v_cache, accepted_nodes, accept_len, prefix_len:
            lib.tv_commit_accepted_kv(_ptr(k_cache), _ptr(v_cache), _ptr(accepted_nodes), _ptr(accept_len), B, Hkv,
                                      D, int(prefix_len), N, S, _dtype_code(k_cache), _ptr(st), _stream()))
     return k_cache, v_cache
+
+
+def frontier_topw(scores, count, width: int, *, dev_status=None, out=None):
+    """TreeGraft §3.1 frontier: positions of the `width` highest of scores[b][:count[b]]
+    (scores [B][C] float32, count [B] int32); ties to the lower position."""
+    _need_cuda(scores=scores, count=count)
+    lib = load_library()
+    B, C = scores.shape
+    idx = out if out is not None else torch.empty(B, width, dtype=torch.int32, device=scores.device)
+    st = _status_tensor(dev_status, scores.device)
+    _check("tv_frontier_topw", lib.tv_frontier_topw(_ptr(scores), _ptr(count), B, C, int(width), _ptr(idx), _ptr(st),
+                                                    _stream()))
+    return idx
+
+
+def expand_workspace_size(R, V, m) -> int:
+    return int(load_library().tv_expand_workspace_size(R, V, m))
+
+
+def expand_children(draft_logits, parent_score, m: int, *, temperature: float = 1.0, workspace=None,
+                    dev_status=None, out=None):
+    """TreeGraft §3.1 children: the top-m tokens of every drafter row [R][V] with their
+    probability p and path score s = parent_score * p.  Returns dict token/p/score [R][m]."""
+    _need_cuda(draft_logits=draft_logits, parent_score=parent_score)
+    lib = load_library()
+    R, V = draft_logits.shape
+    dev = draft_logits.device
+    o = out if out is not None else {}
+    tok = _out(o, "token", (R, m), torch.int32, dev)
+    p = _out(o, "p", (R, m), torch.float32, dev)
+    sc = _out(o, "score", (R, m), torch.float32, dev)
+    ws = _workspace(expand_workspace_size(R, V, m), dev, workspace)
+    st = _status_tensor(dev_status, dev)
+    _check("tv_expand_children",
+           lib.tv_expand_children(_ptr(draft_logits), _ptr(parent_score), R, V, int(m), float(temperature),
+                                  _dtype_code(draft_logits), _ptr(tok), _ptr(p), _ptr(sc), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _ptr(st), _stream()))
+    return {"token": tok, "p": p, "score": sc, "dev_status": st}
 
 
 def verify_workspace_size(B, N, V, dtype, sampling: bool) -> int:

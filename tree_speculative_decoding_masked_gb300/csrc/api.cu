@@ -152,6 +152,30 @@ tv_status tv_commit_accepted_kv(void* k_cache, void* v_cache, const int32_t* acc
                                       kv_stride_tokens, dtype, dev_status, st(stream)));
 }
 
+tv_status tv_frontier_topw(const float* scores, const int32_t* count, int B, int C, int W, int32_t* out_idx,
+                           int32_t* dev_status, tv_stream_t stream) {
+  if (!scores || !count || !out_idx) return TV_ERR_NULL;
+  if (B < 1 || C < 1 || C > 4096 || W < 1 || W > C) return TV_ERR_SHAPE;
+  return cuda_status(launch_frontier_topw(scores, count, B, C, W, out_idx, dev_status, st(stream)));
+}
+
+size_t tv_expand_workspace_size(int R, int V, int m) { return expand_ws_bytes(R, V, m); }
+
+tv_status tv_expand_children(const void* draft_logits, const float* parent_score, int R, int V, int m,
+                             float temperature, tv_dtype dtype, int32_t* child_token, float* child_p,
+                             float* child_score, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                             tv_stream_t stream) {
+  if (!draft_logits || !parent_score || !child_token || !child_p || !child_score) return TV_ERR_NULL;
+  if (!valid_dtype(dtype)) return TV_ERR_DTYPE;
+  if (R < 1 || V < 1 || m < 1 || m > 32) return TV_ERR_SHAPE;
+  if ((long long)R * 32 > 0x7fffffffLL) return TV_ERR_SHAPE;
+  if (!(temperature > 0.f) || isinf(temperature)) return TV_ERR_VALUE;
+  if (!workspace || ws_bytes < expand_ws_bytes(R, V, m)) return TV_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return TV_ERR_ALIGN;
+  return cuda_status(launch_expand(draft_logits, parent_score, R, V, m, temperature, dtype, child_token, child_p,
+                                   child_score, reinterpret_cast<char*>(workspace), dev_status, st(stream)));
+}
+
 size_t tv_select_workspace_size(int B, int d, int K, int budget) { return select_ws_bytes(B, d, K, budget); }
 
 tv_status tv_select_subtree(const float* marg, const int32_t* pool_tokens, int B, int d, int K, int budget,

@@ -39,6 +39,14 @@ cudaError_t launch_kv_commit(void* k_cache, void* v_cache, const int32_t* accept
                              int B, int Hkv, int D, int P, int N, int S, tv_dtype dtype, int32_t* dev_status,
                              cudaStream_t stream);
 
+// ---- single-drafter expansion step
+cudaError_t launch_frontier_topw(const float* scores, const int32_t* count, int B, int C, int W, int32_t* out_idx,
+                                 int32_t* dev_status, cudaStream_t stream);
+size_t expand_ws_bytes(int R, int V, int m);
+cudaError_t launch_expand(const void* logits, const float* parent_score, int R, int V, int m, float temperature,
+                          tv_dtype dtype, int32_t* child_token, float* child_p, float* child_score, char* ws,
+                          int32_t* dev_status, cudaStream_t stream);
+
 // ---- selection
 size_t select_ws_bytes(int B, int d, int K, int budget);
 cudaError_t launch_select(const float* marg, const int32_t* ptok, int B, int d, int K, int budget,
