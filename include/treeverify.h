@@ -86,6 +86,17 @@ TV_API const char* tv_status_string(int status);
 TV_API int tv_version(void);
 
 /* ------------------------------------------------------------------------------------
+ * tv_set_sm_partition - SM shares for running tv_tree_attention and tv_verify_* at the
+ * same time on two streams.  The vocab pass then launches at most verify_sms CTAs (one
+ * per SM) and the tensor-core attention plans its KV splits for attention_sms SMs, so
+ * that the two grids can be resident together instead of queueing behind each other.
+ * 0 (the default) means the whole device.  Process-wide, host-side; affects launches
+ * made after the call.  Results do not depend on it beyond fp32 summation order.
+ * Errors: a negative count -> TV_ERR_VALUE.
+ */
+TV_API tv_status tv_set_sm_partition(int verify_sms, int attention_sms);
+
+/* ------------------------------------------------------------------------------------
  * tv_tree_prep - tree structure for the attention mask and position encoding.
  * PTD §3.1 "tree construction": node v observes pi(v) = {v} U pi(P(v)); its position
  * encoding follows |pi(v)|.

@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     load_library,
     select_subtree,
     select_workspace_size,
+    set_sm_partition,
     status_string,
     tree_attention,
     tree_attention_workspace_size,

@@ -6,6 +6,14 @@
 
 using namespace tv;
 
+// SM shares for running the vocab pass and the tree attention concurrently (0 = all SMs)
+static int g_sm_verify = 0, g_sm_attention = 0;
+
+namespace tv {
+int sm_share_verify() { return g_sm_verify; }
+int sm_share_attention() { return g_sm_attention; }
+}  // namespace tv
+
 namespace {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -43,6 +51,13 @@ const char* tv_status_string(int s) {
 }
 
 int tv_version(void) { return (1 << 16) | 0; }
+
+tv_status tv_set_sm_partition(int verify_sms, int attention_sms) {
+  if (verify_sms < 0 || attention_sms < 0) return TV_ERR_VALUE;
+  g_sm_verify = verify_sms;
+  g_sm_attention = attention_sms;
+  return TV_OK;
+}
 
 tv_status tv_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* depth, int32_t* pos, uint32_t* anc_mask,
                        int32_t* child_off, int32_t* child_idx, int32_t* dev_status, tv_stream_t stream) {

@@ -567,11 +567,16 @@ static int max_active_clusters(int s) {
 template <int D>
 static int choose_splits(long long row_tiles, int t_all) {
   constexpr double kFixedTiles = 3.0;
+  // with an SM share set for concurrent kernels, plan for that part of the device
+  const int share = sm_share_attention();
+  int nsm = 152, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   int best = 1;
   double best_cost = 1e300;
   for (int s = 1; s <= kMaxSplits && s <= t_all; ++s) {
-    const int act = max_active_clusters<D>(s);
+    int act = max_active_clusters<D>(s);
     if (act <= 0) continue;
+    if (share > 0 && share < nsm) act = std::max(1, (int)((long long)act * share / nsm));
     const long long waves = (row_tiles + act - 1) / act;
     const double cost = (double)waves * ((t_all + s - 1) / s + kFixedTiles);
     if (cost < best_cost * 0.98) {

@@ -202,8 +202,28 @@ __global__ void __launch_bounds__(kExpThreads) expand_kernel(ExpArgs a) {
         if (j < nvec) {
           float xv[kN];
           unpack8<T>(u[q], xv);
+          // whole-vector fast path: one max, one rare rescale, a tree of exponentials,
+          // and the list touched only if the vector's max beats its last entry
+          float vm = xv[0];
 #pragma unroll
-          for (int e = 0; e < kN; ++e) push(xv[e], v0 + j * kN + e);
+          for (int e = 1; e < kN; ++e) vm = fmaxf(vm, xv[e]);
+          if (vm * a.c2 > mc) {
+            const float nm = vm * a.c2;
+            sum *= ptx::ex2(mc - nm);
+            mc = nm;
+          }
+          float ex[kN];
+#pragma unroll
+          for (int e = 0; e < kN; ++e) ex[e] = ptx::ex2(fmaf(xv[e], a.c2, -mc));
+#pragma unroll
+          for (int w = 1; w < kN; w *= 2)
+#pragma unroll
+            for (int e = 0; e + w < kN; e += 2 * w) ex[e] += ex[e + w];
+          sum += ex[0];
+          if (vm > lv[kM - 1]) {
+#pragma unroll
+            for (int e = 0; e < kN; ++e) list_insert<kM>(lv, li, xv[e], v0 + j * kN + e);
+          }
         }
       }
     }
@@ -285,8 +305,9 @@ __global__ void __launch_bounds__(kExpThreads) expand_kernel(ExpArgs a) {
 static int exp_km(int m) { return m <= 4 ? 4 : m <= 8 ? 8 : m <= 16 ? 16 : 32; }
 
 static void exp_plan(int R, int V, int& S, int& chunk) {
-  // about four CTAs per SM of the 152, at least 4096 elements per slice
-  const long long want = (4LL * 152 + R - 1) / R;
+  // about two CTAs per SM of the 152 (the per-slice merges are not free), at least 4096
+  // elements per slice
+  const long long want = (2LL * 152 + R - 1) / R;
   S = (int)std::min<long long>(std::max<long long>(1, want), kExpMaxSplits);
   S = std::min(S, std::max(1, V / 4096));
   chunk = (V + S - 1) / S;

@@ -47,6 +47,10 @@ cudaError_t launch_expand(const void* logits, const float* parent_score, int R, 
                           tv_dtype dtype, int32_t* child_token, float* child_p, float* child_score, char* ws,
                           int32_t* dev_status, cudaStream_t stream);
 
+// ---- SM shares set by tv_set_sm_partition (0 = the whole device)
+int sm_share_verify();
+int sm_share_attention();
+
 // ---- selection
 size_t select_ws_bytes(int B, int d, int K, int budget);
 cudaError_t launch_select(const float* marg, const int32_t* ptok, int B, int d, int K, int budget,

@@ -913,6 +913,7 @@ static cudaError_t launch_vocab_tma(VocabArgs a, cudaStream_t stream) {
     attr_set[dev] = true;
   }
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sm_share_verify() > 0) sms = std::min(sms, sm_share_verify());
   plan_grid(a, sms);  // one CTA per SM: the ring takes most of the shared memory
   const long long G = (a.E + a.chunk - 1) / a.chunk;
   vocab_pass_tma_kernel<T, kArrays><<<(unsigned)G, kTmaThreads, kRingBytes, stream>>>(a);
