@@ -8,13 +8,15 @@
 // The key range [0, P + last node of the tile) is cut into KV splits across CTAs.
 //
 // Per CTA, warp-specialised:
-//   warp 0      TMA producer: Q tile once, then K/V tiles of 64 keys into a 4-stage ring
-//   warp 1      TMEM owner; lane 0 issues tcgen05.mma:
-//                 S[t&1] = Q K_t^T         (M=128, N=64,  K=D,  fp32 in TMEM)
-//                 O     += P_t V_t         (M=128, N=D,   K=64, fp32 in TMEM)
-//   warps 2..5  softmax: one thread per row; read S from TMEM, apply the tree mask,
-//               keep a running reference max (rescale O only when the max grows by
-//               more than 2^8), write P (bf16) to shared memory for the second MMA.
+//   warp 0      TMA producer: Q tile once, then K/V tiles of 128 keys into a 2-stage ring
+//   warp 1      TMEM owner; lane 0 issues S[t&1] = Q K_t^T (M=128, N=128, K=D, fp32
+//               in TMEM) as soon as a K tile and an S buffer are free
+//   warp 10     lane 0 issues O += P_t V_t (M=128, N=D, K=128, fp32 in TMEM) as soon as
+//               the softmax has written P_t
+//   warps 2..9  softmax: two threads per row (each half of a tile's 128 keys); read S
+//               from TMEM, apply the tree mask, agree on the row max with the partner
+//               thread, keep a running reference max (rescale O only when the max grows
+//               by more than 2^8), write P (bf16) to shared memory for the second MMA.
 // With one split the epilogue normalises O and stores bf16.  With several, the splits of
 // a row tile run as one thread-block cluster: each CTA parks its unnormalised O and
 // (m, l) in its own shared memory and, after a cluster barrier, merges a slice of the
@@ -29,9 +31,9 @@
 namespace tv {
 
 constexpr int kRows = 128;     // MMA M: query rows per CTA
-constexpr int kBN = 64;        // keys per KV tile (MMA N of QK^T, K of PV)
-constexpr int kStages = 4;     // K/V ring depth
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kBN = 128;       // keys per KV tile (MMA N of QK^T, K of PV)
+constexpr int kStages = 2;     // K/V ring depth (tiles of 128 keys)
+constexpr int kThreads = 352;  // 11 warps: TMA producer, S issuer, 8 softmax warps, PV issuer
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxSplits = 8;  // KV splits of a row tile = one portable-size cluster
 
@@ -42,15 +44,16 @@ struct TcCfg {
   static constexpr int kKVBlock = kBN * 128;          // bytes per column block of a K or V tile
   static constexpr int kQBytes = kDB * kQBlock;
   static constexpr int kStageBytes = 2 * kDB * kKVBlock;
-  static constexpr int kPBytes = kRows * kBN * 2;     // one P buffer (128 rows x 64 keys bf16)
+  static constexpr int kPBlock = kRows * 128;         // bytes per 64-key column block of P
+  static constexpr int kPBytes = kRows * kBN * 2;     // the P buffer (128 rows x 128 keys bf16)
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kQBytes;
   static constexpr int kOffP = kOffKV + kStages * kStageBytes;
-  static constexpr int kOffPar = kOffP + 2 * kPBytes;
+  static constexpr int kOffPar = kOffP + kPBytes;
   static constexpr int kOffBar = kOffPar + kMaxNodes * 4;
   static constexpr int kSmemUsed = kOffBar + 256;
   static constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack for 1024-byte alignment
-  static constexpr uint32_t kTmemCols = 256;           // S[0], S[1] (64 each) + O (D)
+  static constexpr uint32_t kTmemCols = 512;           // S[0], S[1] (128 each) + O (D)
   static constexpr uint32_t kColO = 2 * kBN;
   static_assert(kColO + D <= kTmemCols, "TMEM budget");
 };
@@ -69,22 +72,23 @@ struct Bars {
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t p_full[2];
-  uint64_t p_free[2];
+  uint64_t p_full;
+  uint64_t p_free;
   uint64_t o_done;
+  uint64_t s_done;
   uint32_t tmem_base;
   int abort;
 };
 
-// 64-bit visibility mask of keys [j0, j0 + 64) for tree node `node`.
+// 64-bit visibility mask of keys [j0, j0 + 64) for tree node `node` (half a KV tile).
 __device__ __forceinline__ uint64_t key_mask(int j0, int P, int N, int node, const int* s_par) {
-  if (j0 + kBN <= P) return ~0ull;
+  if (j0 + 64 <= P) return ~0ull;
   uint64_t vis = 0;
   if (j0 < P) vis = (1ull << (P - j0)) - 1ull;
   int a = node, guard = 0;
   while (a >= 0 && guard <= N) {
     const int j = P + a - j0;
-    if (j >= 0 && j < kBN) vis |= 1ull << j;
+    if (j >= 0 && j < 64) vis |= 1ull << j;
     const int pa = s_par[a];
     if (pa >= a) break;  // malformed (flagged when loaded)
     a = pa;
@@ -99,6 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmV, TcArgs a) {
   using C = TcCfg<D>;
   extern __shared__ unsigned char smem_raw[];
+  __shared__ float s_xmax[2][2][kRows];  // [tile parity][half][row] partial row maxima
+  __shared__ float s_xl[2][kRows];       // [half][row] partial row sums
   const uint32_t mis = ptx::smem_addr(smem_raw) & 1023u;
   unsigned char* sm = smem_raw + ((1024u - mis) & 1023u);
   unsigned char* sQ = sm + C::kOffQ;
@@ -129,11 +135,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&bars->s_full[s], 1);
-      ptx::mbar_init(&bars->s_free[s], 4);
-      ptx::mbar_init(&bars->p_full[s], 4);
-      ptx::mbar_init(&bars->p_free[s], 1);
+      ptx::mbar_init(&bars->s_free[s], 8);
     }
+    ptx::mbar_init(&bars->p_full, 8);
+    ptx::mbar_init(&bars->p_free, 1);
     ptx::mbar_init(&bars->o_done, 1);
+    ptx::mbar_init(&bars->s_done, 1);
     bars->abort = 0;
     ptx::fence_mbar_init();
   }
@@ -145,13 +152,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // parent array for the mask; zero the Q rows that no TMA box fills
     const int t = threadIdx.x - 64;
     int bad = 0;
-    for (int c = t; c < a.N; c += 128) {
+    for (int c = t; c < a.N; c += kThreads - 64) {
       const int p = a.parent[(size_t)b * a.N + c];
       s_par[c] = p;
       if (!((c == 0) ? (p == -1) : (p >= 0 && p < c))) bad = 1;
     }
     if (bad) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);
-    for (int r = rows_used + t; r < kRows; r += 128)
+    for (int r = rows_used + t; r < kRows; r += kThreads - 64)
       for (int db = 0; db < C::kDB; ++db) {
         uint4* row = reinterpret_cast<uint4*>(sQ + db * C::kQBlock + r * 128);
 #pragma unroll
@@ -220,26 +227,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_commit(&bars->s_full[sb]);
           return true;
         };
-        auto issue_pv = [&](int t) -> bool {
-          const int st = t % kStages, sb = t & 1;
-          if (!ptx::mbar_wait(&bars->p_full[sb], (t >> 1) & 1, abort_flag)) return false;
+        // S = QK^T tiles run ahead of the softmax (bounded by the two S buffers); the PV
+        // products are issued by warp 10, so neither waits behind the other's issue
+        for (int t = 0; ok && t < nt; ++t) ok = issue_s(t);
+      }
+      ptx::mma_commit(&bars->s_done);
+      ptx::mbar_wait(&bars->s_done, 0, abort_flag);
+    }
+    __syncwarp();
+  } else if (warp == kThreads / 32 - 1) {
+    // ------------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      if (nt > 0) {
+        constexpr uint32_t idO = ptx::idesc_bf16(kRows, D, false, true);
+        for (int t = 0; t < nt; ++t) {
+          const int st = t % kStages;
+          if (!ptx::mbar_wait(&bars->p_full, t & 1, abort_flag)) break;
           ptx::tc_fence_after();
-          const uint32_t paddr = ptx::smem_addr(sP + sb * C::kPBytes);
+          const uint32_t paddr = ptx::smem_addr(sP);
           const uint32_t vaddr = ptx::smem_addr(sKV + st * C::kStageBytes + C::kDB * C::kKVBlock);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t ad = ptx::sdesc_sw128(paddr + kk * 32, 16, 1024);
+            const uint64_t ad = ptx::sdesc_sw128(paddr + (kk >> 2) * C::kPBlock + (kk & 3) * 32, 16, 1024);
             const uint64_t bd = ptx::sdesc_sw128(vaddr + kk * 16 * 128, C::kKVBlock, 1024);
             ptx::mma_bf16_ss(tmem + C::kColO, ad, bd, idO, (t > 0 || kk > 0) ? 1u : 0u);
           }
           ptx::mma_commit(&bars->kv_empty[st]);
-          ptx::mma_commit(&bars->p_free[sb]);
-          return true;
-        };
-        ok = issue_s(0);
-        for (int t = 0; ok && t < nt; ++t) {
-          if (t + 1 < nt) ok = issue_s(t + 1);
-          if (ok) ok = issue_pv(t);
+          ptx::mma_commit(&bars->p_free);
         }
       }
       ptx::mma_commit(&bars->o_done);
@@ -248,46 +262,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ softmax rows
+    // two threads per row: warps 2-5 take keys [0, 64) of each tile, warps 6-9 keys
+    // [64, 128) (warp w and w + 4 read the same TMEM lane quarter); the halves agree on the
+    // row max through shared memory and a barrier of the warp pair once per tile
     const int q4 = warp & 3;
+    const int h = (warp - 2) >> 2;
     const int r = q4 * 32 + lane;
     const int g = r / a.NT, il = r % a.NT;
     const int node = i0 + il;
     const bool valid = (g < a.G) && (node < a.N) && (r < rows_used);
     const int mnode = valid ? node : 0;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const int c_lo = h * (kBN / 2);  // this thread's key columns in a tile
+    const int d_lo = h * (D / 2);    // and its O columns
+    const uint32_t pair_bar = 1 + q4;
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
+    // after a failed wait the loop keeps running without waiting or computing, so that
+    // both threads of a row still meet at every pair barrier
     for (int t = 0; t < nt; ++t) {
       const int sb = t & 1;
-      ok = ptx::mbar_wait(&bars->s_full[sb], (t >> 1) & 1, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      float sv[kBN];
-      ptx::tmem_ld32(tmem + lane_base + sb * kBN, sv);
-      ptx::tmem_ld32(tmem + lane_base + sb * kBN + 32, sv + 32);
-      ptx::tmem_wait_ld();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->s_free[sb]);
+      if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->s_full[sb], (t >> 1) & 1, abort_flag));
+      float sv[kBN / 2];
+      if (ok) {
+        ptx::tc_fence_after();
+        ptx::tmem_ld32(tmem + lane_base + sb * kBN + c_lo, sv);
+        ptx::tmem_ld32(tmem + lane_base + sb * kBN + c_lo + 32, sv + 32);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->s_free[sb]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kBN / 2; ++j) sv[j] = -INFINITY;
+      }
 
       const int j0 = (t_begin + t) * kBN;
-      const uint64_t vis = key_mask(j0, a.P, a.N, mnode, s_par);
+      const uint64_t vis = key_mask(j0 + c_lo, a.P, a.N, mnode, s_par);
       if (vis != ~0ull) {  // tree / tail tiles: hidden keys become -inf (exp -> 0)
 #pragma unroll
-        for (int j = 0; j < kBN; ++j)
+        for (int j = 0; j < kBN / 2; ++j)
           if (!((vis >> j) & 1ull)) sv[j] = -INFINITY;
       }
-      // row max as eight independent chains, then a tree
       float m8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) m8[k] = sv[k];
 #pragma unroll
-      for (int j = 8; j < kBN; j += 8)
+      for (int j = 8; j < kBN / 2; j += 8)
 #pragma unroll
         for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], sv[j + k]);
-      const float tm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      float tm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      s_xmax[t & 1][h][r] = tm;
+      pair_sync();
+      tm = fmaxf(tm, s_xmax[t & 1][h ^ 1][r]);
       const float tms = tm * a.c;
       float alpha = 1.f;
       bool need = false;
@@ -298,58 +326,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         m_run = tms;
       }
-      if (__any_sync(0xffffffffu, need) && t > 0) {
-        // O already holds PV(t-1): wait for it, then scale this warp's rows
-        ok = ptx::mbar_wait(&bars->p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
+      if (__any_sync(0xffffffffu, need) && t > 0 && ok) {
+        // O already holds PV(t-1): wait for it, then scale this thread's half of the row
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->p_free, (t - 1) & 1, abort_flag));
+      }
+      if (__any_sync(0xffffffffu, need) && t > 0 && ok) {
         ptx::tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
           float ov[32];
-          ptx::tmem_ld32(tmem + lane_base + C::kColO + c0, ov);
+          ptx::tmem_ld32(tmem + lane_base + C::kColO + d_lo + c0, ov);
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) ov[k] *= alpha;
-          ptx::tmem_st32(tmem + lane_base + C::kColO + c0, ov);
+          ptx::tmem_st32(tmem + lane_base + C::kColO + d_lo + c0, ov);
         }
         ptx::tmem_wait_st();
       }
       l_run *= alpha;
-      if (t >= 2) {
-        ok = ptx::mbar_wait(&bars->p_free[sb], ((t >> 1) - 1) & 1, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
+      // the single P buffer is free once PV(t-1) has completed
+      if (t >= 1 && ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->p_free, (t - 1) & 1, abort_flag));
+      if (!ok) continue;  // nothing more to compute or signal for this tile
       // P = 2^(S*c - m_run) on visible keys, bf16, 128-byte-swizzled K-major rows
-      unsigned char* prow = sP + sb * C::kPBytes + r * 128;
+      unsigned char* prow = sP + h * C::kPBlock + r * 128;  // this half's 64-key column block
       float ls8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) ls8[k] = 0.f;
       const bool live = m_run != -INFINITY;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        float p[8];
+      for (int cc = 0; cc < 8; ++cc) {
+        const int ch = cc;  // 16-byte chunk of the row
+        float pv[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          p[k] = live ? ptx::ex2(fmaf(sv[ch * 8 + k], a.c, -m_run)) : 0.f;
-          ls8[k] += p[k];
+          pv[k] = live ? ptx::ex2(fmaf(sv[cc * 8 + k], a.c, -m_run)) : 0.f;
+          ls8[k] += pv[k];
         }
         uint4 u;
-        u.x = ptx::cvt_bf16x2(p[0], p[1]);
-        u.y = ptx::cvt_bf16x2(p[2], p[3]);
-        u.z = ptx::cvt_bf16x2(p[4], p[5]);
-        u.w = ptx::cvt_bf16x2(p[6], p[7]);
+        u.x = ptx::cvt_bf16x2(pv[0], pv[1]);
+        u.y = ptx::cvt_bf16x2(pv[2], pv[3]);
+        u.z = ptx::cvt_bf16x2(pv[4], pv[5]);
+        u.w = ptx::cvt_bf16x2(pv[6], pv[7]);
         *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = u;
       }
-      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-      l_run += lsum;
+      l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->p_full[sb]);
+      if (lane == 0) ptx::mbar_arrive(&bars->p_full);
     }
-    // ---- epilogue
+    // ---- epilogue: the row's sum is the two halves' sums
+    s_xl[h][r] = l_run;
+    pair_sync();
+    l_run += s_xl[h ^ 1][r];
     bool have_o = false;
     if (nt > 0) {
       ok = ptx::mbar_wait(&bars->o_done, 0, abort_flag) && ok;
@@ -357,22 +386,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       have_o = ok;
       if (ok) ptx::tc_fence_after();
     }
-    const int h = hk * a.G + g;
-    const size_t orow = (((size_t)b * a.Hq + h) * a.N + node) * D;
+    const int hh = hk * a.G + g;
+    const size_t orow = (((size_t)b * a.Hq + hh) * a.N + node) * D;
     if (a.splits == 1) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
         float ov[32];
         if (have_o) {
-          ptx::tmem_ld32(tmem + lane_base + C::kColO + c0, ov);
+          ptx::tmem_ld32(tmem + lane_base + C::kColO + d_lo + c0, ov);
           ptx::tmem_wait_ld();
         } else {
 #pragma unroll
           for (int k = 0; k < 32; ++k) ov[k] = 0.f;
         }
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow + c0);
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow + d_lo + c0);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             uint4 u;
@@ -391,10 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned char* part = sKV;
       float2* ml = reinterpret_cast<float2*>(sKV + D * kRows * 4);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
         float ov[32];
         if (have_o) {
-          ptx::tmem_ld32(tmem + lane_base + C::kColO + c0, ov);
+          ptx::tmem_ld32(tmem + lane_base + C::kColO + d_lo + c0, ov);
           ptx::tmem_wait_ld();
         } else {
 #pragma unroll
@@ -402,12 +431,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const int chunk = c0 / 4 + k;
+          const int chunk = (d_lo + c0) / 4 + k;
           *reinterpret_cast<float4*>(part + r * D * 4 + ((chunk ^ (r & 7)) << 4)) =
               make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
         }
       }
-      ml[r] = make_float2(have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
+      if (h == 0) ml[r] = make_float2(have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
     }
     ptx::tc_fence_before();
   }
@@ -419,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // peer has finished reading.
     ptx::cluster_sync();
     {
-      // all 192 threads; item = (row of this CTA's slice, 16-byte chunk of 4 columns):
+      // every thread; item = (row of this CTA's slice, 16-byte chunk of 4 columns):
       // a warp reads one contiguous row of each peer's partial, all loads issued first
       const int S = a.splits;
       const int R = (kRows + S - 1) / S;
@@ -566,7 +595,7 @@ static int max_active_clusters(int s) {
 // per-CTA cost for set-up and the cluster merge), counted in 64-key tiles.
 template <int D>
 static int choose_splits(long long row_tiles, int t_all) {
-  constexpr double kFixedTiles = 3.0;
+  constexpr double kFixedTiles = 1.5;
   // with an SM share set for concurrent kernels, plan for that part of the device
   const int share = sm_share_attention();
   int nsm = 152, dev = 0;
