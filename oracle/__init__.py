@@ -27,6 +27,8 @@ kvcommit   blog, "KV cache handling": keep the accepted tokens' cache entries, d
            rejected candidates' (the accepted root path laid out as a plain sequence).
 frontier   TreeGraft §3.1 single-drafter expansion: frontier Top_W by s(v), the top-m
            tokens of each frontier node's drafter distribution attached as children.
+prune      PTD §3.1 "overhead constraints": a per-parent child cap and the sliding-window
+           stepping of the root when the tree gets too deep (page truncated there).
 
 Readings taken where the pages are silent are listed in each module's docstring.
 Parity status: every function is pinned by tests under ``tests/test_oracle_*.py``
