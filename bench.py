@@ -445,6 +445,16 @@ def run_ours(args):
         tv.expand_children(s["logits"].view(B * N, V)[:exp_rows], exp_ps, exp_m, workspace=exp_ws,
                            dev_status=status, out=exp_out)
 
+    # PTD width / depth control on the step's tree: at most 2 children per node, 8 levels
+    prune_conf = sel_out["score"] if use_pool else torch.ones(B, N, dtype=torch.float32, device=dev)
+    prune_out = {"old_to_new": torch.empty(B, N, dtype=torch.int32, device=dev),
+                 "new_parent": torch.empty(B, N, dtype=torch.int32, device=dev),
+                 "n_kept": torch.empty(B, dtype=torch.int32, device=dev),
+                 "new_root": torch.empty(B, dtype=torch.int32, device=dev)}
+
+    def k_prune(s):
+        tv.prune_tree(sel_out["parent"], prune_conf, 2, 8, dev_status=status, out=prune_out)
+
     def k_commit(s):
         # keep the accepted path's KV rows (timed in the breakdown, not part of the step)
         tv.commit_accepted_kv(s["k"], s["v"], ver_out["accepted_nodes"], ver_out["accept_len"], P, dev_status=status)
@@ -515,7 +525,8 @@ def run_ours(args):
                       "verify": capture(lambda: [k_verify(s) for s in sets]),
                       "commit": capture(lambda: [k_commit(s) for s in sets]),
                       "tree_prep": capture(lambda: [k_prep(s) for s in sets]),
-                      "expand": capture(lambda: [k_expand(s) for s in sets])}
+                      "expand": capture(lambda: [k_expand(s) for s in sets]),
+                      "prune": capture(lambda: [k_prune(s) for s in sets])}
         if use_pool:
             fam_graphs["select"] = capture(lambda: [k_select(s) for s in sets])
             fam_graphs["select_adaptive"] = capture(lambda: [k_select_adaptive(s) for s in sets])

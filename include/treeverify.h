@@ -10,6 +10,7 @@
  *   tv_verify_sample    fused vocab pass + min(1,p/q) walk + residual resampling
  *   tv_commit_accepted_kv  keep the accepted path's cache rows (contiguous), drop the rest
  *   tv_frontier_topw / tv_expand_children  one single-drafter tree-expansion step
+ *   tv_prune_tree       per-parent child cap and depth-window re-rooting of a tree
  *
  * Conventions shared by every call
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless marked
@@ -113,6 +114,25 @@ TV_API tv_status tv_set_sm_partition(int verify_sms, int attention_sms);
 TV_API tv_status tv_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* depth, int32_t* pos,
                        uint32_t* anc_mask, int32_t* child_off, int32_t* child_idx,
                        int32_t* dev_status, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * tv_prune_tree - width and depth control of a draft tree.
+ * PTD §3.1 "overhead constraints": every parent keeps at most max_children children,
+ * the most confident ones (conf descending, ties to the lower index), and loses the
+ * others with their subtrees; then, while the kept tree is more than depth_limit edges
+ * deep, the root's lowest-index kept child becomes the root and everything outside its
+ * subtree is pruned (the page's sliding-window stepping; nodes are numbered in the
+ * order they were added).  Survivors are renumbered in their original order.
+ *   parent [B][N] int32 (tree layout as above), conf [B][N] float (finite)
+ *   old_to_new [B][N] out: new index of each node or -1
+ *   new_parent [B][N] out: rows < n_kept[b] hold the new tree (-1 at its root), the
+ *                 rest -1
+ *   n_kept [B], new_root [B] out: count and the old index of the new root
+ * Limits: 1 <= N <= 1024, max_children >= 1, depth_limit >= 1.  No workspace.
+ */
+TV_API tv_status tv_prune_tree(const int32_t* parent, const float* conf, int B, int N, int max_children,
+                        int depth_limit, int32_t* old_to_new, int32_t* new_parent, int32_t* n_kept,
+                        int32_t* new_root, int32_t* dev_status, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * tv_tree_attention - tree-masked grouped-query attention of the draft tree.

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     frontier_topw,
     library_path,
     load_library,
+    prune_tree,
     select_subtree,
     select_workspace_size,
     set_sm_partition,

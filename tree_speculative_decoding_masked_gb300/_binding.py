@@ -42,6 +42,7 @@ _SIGS = {
     "tv_version": (_I, []),
     "tv_set_sm_partition": (_I, [_I, _I]),
     "tv_tree_prep": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "tv_prune_tree": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "tv_tree_attention_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "tv_tree_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _P]),
     "tv_verify_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
@@ -160,6 +161,24 @@ def tree_prep(parent: torch.Tensor, prefix_len: int, *, dev_status=None, out=Non
     _check("tv_tree_prep", lib.tv_tree_prep(_ptr(parent), B, N, int(prefix_len), _ptr(depth), _ptr(pos), _ptr(mask),
                                             _ptr(off), _ptr(idx), _ptr(st), _stream()))
     return {"depth": depth, "pos": pos, "anc_mask": mask, "child_off": off, "child_idx": idx, "dev_status": st}
+
+
+def prune_tree(parent, conf, max_children: int, depth_limit: int, *, dev_status=None, out=None):
+    """PTD width / depth control of parent [B][N] with confidences conf [B][N] float32.
+    Returns dict old_to_new, new_parent [B][N], n_kept, new_root [B]."""
+    _need_cuda(parent=parent, conf=conf)
+    lib = load_library()
+    B, N = parent.shape
+    dev = parent.device
+    o = out if out is not None else {}
+    o2n = _out(o, "old_to_new", (B, N), torch.int32, dev)
+    npar = _out(o, "new_parent", (B, N), torch.int32, dev)
+    nk = _out(o, "n_kept", (B,), torch.int32, dev)
+    nr = _out(o, "new_root", (B,), torch.int32, dev)
+    st = _status_tensor(dev_status, dev)
+    _check("tv_prune_tree", lib.tv_prune_tree(_ptr(parent), _ptr(conf), B, N, int(max_children), int(depth_limit),
+                                              _ptr(o2n), _ptr(npar), _ptr(nk), _ptr(nr), _ptr(st), _stream()))
+    return {"old_to_new": o2n, "new_parent": npar, "n_kept": nk, "new_root": nr, "dev_status": st}
 
 
 def tree_attention_workspace_size(B, Hq, Hkv, D, P, N, dtype) -> int:

@@ -68,6 +68,16 @@ tv_status tv_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* dept
                                       st(stream)));
 }
 
+tv_status tv_prune_tree(const int32_t* parent, const float* conf, int B, int N, int max_children, int depth_limit,
+                        int32_t* old_to_new, int32_t* new_parent, int32_t* n_kept, int32_t* new_root,
+                        int32_t* dev_status, tv_stream_t stream) {
+  if (!parent || !conf || !old_to_new || !new_parent || !n_kept || !new_root) return TV_ERR_NULL;
+  if (B < 1 || N < 1 || N > kMaxNodes) return TV_ERR_SHAPE;
+  if (max_children < 1 || depth_limit < 1) return TV_ERR_VALUE;
+  return cuda_status(launch_prune(parent, conf, B, N, max_children, depth_limit, old_to_new, new_parent, n_kept,
+                                  new_root, dev_status, st(stream)));
+}
+
 size_t tv_tree_attention_workspace_size(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) {
   if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || P < 0 || N < 1) return 0;
   AttnPlan p = attn_plan(B, Hq, Hkv, D, P, N, dtype);

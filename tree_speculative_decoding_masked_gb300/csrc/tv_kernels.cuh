@@ -47,6 +47,11 @@ cudaError_t launch_expand(const void* logits, const float* parent_score, int R, 
                           tv_dtype dtype, int32_t* child_token, float* child_p, float* child_score, char* ws,
                           int32_t* dev_status, cudaStream_t stream);
 
+// ---- width / depth control
+cudaError_t launch_prune(const int32_t* parent, const float* conf, int B, int N, int max_children, int depth_limit,
+                         int32_t* old_to_new, int32_t* new_parent, int32_t* n_kept, int32_t* new_root,
+                         int32_t* dev_status, cudaStream_t stream);
+
 // ---- SM shares set by tv_set_sm_partition (0 = the whole device)
 int sm_share_verify();
 int sm_share_attention();
