@@ -9,11 +9,12 @@
 //   scores by direct comparison (s desc, position asc) and keeps the first W.
 // expand_kernel: the drafter rows [R][V] are split over CTAs; each CTA streams its
 //   slice once (16-byte loads, several in flight per thread) keeping a running
-//   (max, sum 2^(x*c - max)) and a per-thread top-kM list in registers (insertion only
-//   when a value beats the list's last entry: rare after the first elements).  Lists are
-//   merged warp by warp (kM rounds of a warp arg-max over the lists' heads), the slice's
-//   top-m and (max, sum) go to the workspace, and the CTA that completes a row (one
-//   acquire-release atomic) merges the row's slices and writes tokens, p and s.
+//   (max, sum 2^(x*c - max)) per thread and a sorted top-m list per warp (lane k holds
+//   the k-th best): a vector touches the list only if its max reaches the list's m-th
+//   entry, and each qualifying element is inserted by the whole warp (ballot for the
+//   position, one shuffle to shift the tail).  Warp 0 merges the warps' lists, the
+//   slice's top-m and (max, sum) go to the workspace, and the CTA that completes a row
+//   (one acquire-release atomic) merges the row's slices and writes tokens, p and s.
 #include <algorithm>
 
 #include "tv_kernels.cuh"
@@ -73,8 +74,8 @@ struct ExpArgs {
   int R, V, m, S;       // rows, vocabulary, children per row, slices per row
   int chunk;            // elements per slice (a multiple of 8)
   float c2;             // log2(e) / T
-  float* part_v;        // [R][S][kM] raw logits of the slice's top list
-  int* part_i;          // [R][S][kM] their tokens
+  float* part_v;        // [R][S][32] raw logits of the slice's top list
+  int* part_i;          // [R][S][32] their tokens
   float2* part_ms;      // [R][S] (scaled max, sum)
   unsigned* row_cnt;    // [R]
   int32_t* child_token; // [R][m]
@@ -82,59 +83,6 @@ struct ExpArgs {
   float* child_score;
   int32_t* dev_status;
 };
-
-// insert (x, i) into the descending list (v, id) of length kM if it beats the last entry;
-// equal values keep the earlier entry in front
-template <int kM>
-__device__ __forceinline__ void list_insert(float (&v)[kM], int (&id)[kM], float x, int i) {
-  if (!(x > v[kM - 1])) return;
-#pragma unroll
-  for (int k = kM - 1; k >= 0; --k) {
-    if (k > 0 && v[k - 1] < x) {
-      v[k] = v[k - 1];
-      id[k] = id[k - 1];
-    } else if (v[k] < x) {
-      v[k] = x;
-      id[k] = i;
-    }
-  }
-}
-
-// kM rounds of a warp arg-max over the lanes' list heads (value desc, token asc); round r's
-// winner lands in out_v[r], out_i[r] (written by lane 0)
-template <int kM>
-__device__ __forceinline__ void warp_merge_lists(float (&v)[kM], int (&id)[kM], float* out_v, int* out_i) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll 1
-  for (int r = 0; r < kM; ++r) {
-    float bv = v[0];
-    int bi = id[0], bl = lane;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
-      if (ov > bv || (ov == bv && (oi < bi || (oi == bi && ol < bl)))) {
-        bv = ov;
-        bi = oi;
-        bl = ol;
-      }
-    }
-    if (lane == 0) {
-      out_v[r] = bv;
-      out_i[r] = bi;
-    }
-    if (lane == bl) {  // pop the winner's head
-#pragma unroll
-      for (int k = 0; k + 1 < kM; ++k) {
-        v[k] = v[k + 1];
-        id[k] = id[k + 1];
-      }
-      v[kM - 1] = -INFINITY;
-      id[kM - 1] = 0x7fffffff;
-    }
-  }
-}
 
 template <typename T>
 __device__ __forceinline__ void unpack8(const uint4& u, float* x);
@@ -155,58 +103,156 @@ __device__ __forceinline__ void unpack8<float>(const uint4& u, float* x) {
   x[3] = __uint_as_float(u.w);
 }
 
-template <typename T, int kM, bool kVec>
+// A warp-wide sorted list of the best (value, token) pairs seen so far: lane k holds the
+// k-th best (value descending, token ascending), lanes >= m hold nothing.  An insertion
+// is warp-collective: every lane compares its entry with the candidate, the lanes behind
+// it shift down by one.
+struct WarpList {
+  float v;
+  int i;
+  __device__ __forceinline__ void init() {
+    v = -INFINITY;
+    i = 0x7fffffff;
+  }
+  __device__ __forceinline__ static bool better(float xa, int ia, float xb, int ib) {
+    return xa > xb || (xa == xb && ia < ib);
+  }
+  // the m-th best entry (the bar a candidate must beat)
+  __device__ __forceinline__ void bar(int m, float& bv, int& bi) const {
+    bv = __shfl_sync(0xffffffffu, v, m - 1);
+    bi = __shfl_sync(0xffffffffu, i, m - 1);
+  }
+  // warp-uniform candidate (x, ix)
+  __device__ __forceinline__ void insert(float x, int ix, int m) {
+    const int lane = threadIdx.x & 31;
+    const unsigned ahead = __ballot_sync(0xffffffffu, lane < m && better(v, i, x, ix));
+    const int pos = __popc(ahead);
+    const float pv = __shfl_up_sync(0xffffffffu, v, 1);
+    const int pi = __shfl_up_sync(0xffffffffu, i, 1);
+    if (pos < m) {
+      if (lane == pos) {
+        v = x;
+        i = ix;
+      } else if (lane > pos && lane < m) {
+        v = pv;
+        i = pi;
+      }
+    }
+  }
+  // merge another sorted list (lane k holds its k-th best) and keep the best 32: the
+  // concatenation of this list and the other reversed is bitonic, so one comparison with
+  // the mirrored lane keeps the better half and five shuffle stages sort it
+  __device__ __forceinline__ void merge(float ov, int oi) {
+    const int lane = threadIdx.x & 31;
+    const float rv = __shfl_sync(0xffffffffu, ov, 31 - lane);
+    const int ri = __shfl_sync(0xffffffffu, oi, 31 - lane);
+    if (better(rv, ri, v, i)) {
+      v = rv;
+      i = ri;
+    }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+      const float pv = __shfl_xor_sync(0xffffffffu, v, d);
+      const int pi = __shfl_xor_sync(0xffffffffu, i, d);
+      const bool pb = better(pv, pi, v, i);
+      if (((lane & d) == 0) == pb) {
+        v = pv;
+        i = pi;
+      }
+    }
+  }
+  // become the sorted list of the lanes' (x, ix): a bitonic sort across the warp
+  __device__ __forceinline__ void sort_from(float x, int ix) {
+    const int lane = threadIdx.x & 31;
+    v = x;
+    i = ix;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const float pv = __shfl_xor_sync(0xffffffffu, v, j);
+        const int pi = __shfl_xor_sync(0xffffffffu, i, j);
+        const bool lower = (lane & j) == 0, desc = (lane & k) == 0;
+        const bool pb = better(pv, pi, v, i);
+        if ((lower == desc) == pb) {
+          v = pv;
+          i = pi;
+        }
+      }
+  }
+  // offer each lane's (x, ix) (per-lane candidates, in lane order)
+  __device__ __forceinline__ void offer(float x, int ix, bool want, int m) {
+    float bv;
+    int bi;
+    bar(m, bv, bi);
+    unsigned cand = __ballot_sync(0xffffffffu, want && better(x, ix, bv, bi));
+    while (cand) {
+      const int src = __ffs(cand) - 1;
+      cand &= cand - 1;
+      const float cx = __shfl_sync(0xffffffffu, x, src);
+      const int ci = __shfl_sync(0xffffffffu, ix, src);
+      float b2;
+      int i2;
+      bar(m, b2, i2);
+      if (better(cx, ci, b2, i2)) insert(cx, ci, m);
+    }
+  }
+};
+
+template <typename T, bool kVec>
 __global__ void __launch_bounds__(kExpThreads) expand_kernel(ExpArgs a) {
-  __shared__ float s_v[kExpThreads / 32][kM];
-  __shared__ int s_i[kExpThreads / 32][kM];
+  __shared__ float s_v[kExpThreads / 32][32];
+  __shared__ int s_i[kExpThreads / 32][32];
   __shared__ float2 s_ms[kExpThreads / 32];
-  __shared__ float s_fv[kM];
-  __shared__ int s_fi[kM];
   __shared__ int s_last;
   const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  const int m = a.m;
   const int row = blockIdx.x / a.S, slice = blockIdx.x % a.S;
   const int v0 = min(a.V, slice * a.chunk), v1 = min(a.V, v0 + a.chunk);
   const T* x = reinterpret_cast<const T*>(a.logits) + (size_t)row * a.V;
-  float lv[kM];
-  int li[kM];
-#pragma unroll
-  for (int k = 0; k < kM; ++k) {
-    lv[k] = -INFINITY;
-    li[k] = 0x7fffffff;
-  }
+  WarpList wl;
+  wl.init();
   float mc = -INFINITY, sum = 0.f;
-  auto push = [&](float xv, int i) {
-    if (xv * a.c2 > mc) {
-      const float nm = xv * a.c2;
-      sum *= ptx::ex2(mc - nm);
-      mc = nm;
+  auto scalar = [&](int i, bool ok) {  // one element per lane (tails and unaligned rows)
+    const float xv = ok ? to_f32_any<T>(x[i]) : -INFINITY;
+    if (ok) {
+      if (xv * a.c2 > mc) {
+        const float nm = xv * a.c2;
+        sum *= ptx::ex2(mc - nm);
+        mc = nm;
+      }
+      sum += ptx::ex2(fmaf(xv, a.c2, -mc));
     }
-    sum += ptx::ex2(fmaf(xv, a.c2, -mc));
-    list_insert<kM>(lv, li, xv, i);
+    wl.offer(xv, i, ok, m);
   };
   if constexpr (kVec) {
     constexpr int kN = 16 / sizeof(T);
     const uint4* p = reinterpret_cast<const uint4*>(x + v0);
     const int nvec = (v1 - v0) / kN;
     constexpr int kB = 4;  // 16-byte loads in flight per thread
-    for (int jb = t; jb < nvec; jb += kB * kExpThreads) {
+    for (int jb = t - lane; jb < nvec; jb += kB * kExpThreads) {  // warp-uniform trip count
       uint4 u[kB];
 #pragma unroll
       for (int q = 0; q < kB; ++q) {
-        const int j = jb + q * kExpThreads;
+        const int j = jb + lane + q * kExpThreads;
         u[q] = j < nvec ? __ldcs(p + j) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int q = 0; q < kB; ++q) {
-        const int j = jb + q * kExpThreads;
-        if (j < nvec) {
-          float xv[kN];
-          unpack8<T>(u[q], xv);
-          // whole-vector fast path: one max, one rare rescale, a tree of exponentials,
-          // and the list touched only if the vector's max beats its last entry
-          float vm = xv[0];
+        const int j = jb + lane + q * kExpThreads;
+        const bool ok = j < nvec;
+        float xv[kN];
+        unpack8<T>(u[q], xv);
+        float vm = -INFINITY;
+        int em = 0;  // position of the vector's max (first one on ties)
+        if (ok) {
+          vm = xv[0];
 #pragma unroll
-          for (int e = 1; e < kN; ++e) vm = fmaxf(vm, xv[e]);
+          for (int e = 1; e < kN; ++e)
+            if (xv[e] > vm) {
+              vm = xv[e];
+              em = e;
+            }
           if (vm * a.c2 > mc) {
             const float nm = vm * a.c2;
             sum *= ptx::ex2(mc - nm);
@@ -220,18 +266,35 @@ __global__ void __launch_bounds__(kExpThreads) expand_kernel(ExpArgs a) {
 #pragma unroll
             for (int e = 0; e + w < kN; e += 2 * w) ex[e] += ex[e + w];
           sum += ex[0];
-          if (vm > lv[kM - 1]) {
+        }
+        if (jb == t - lane && q == 0) {
+          // first vectors of the warp: the lanes' maxima, sorted, seed the list in one go
+          // (real elements, so its m-th entry is a valid bar from the start)
+          wl.sort_from(vm, ok ? v0 + j * kN + em : 0x7fffffff);
+          if (lane >= m) wl.init();
+          float bv;
+          int bi;
+          wl.bar(m, bv, bi);
 #pragma unroll
-            for (int e = 0; e < kN; ++e) list_insert<kM>(lv, li, xv[e], v0 + j * kN + e);
+          for (int e = 0; e < kN; ++e) wl.offer(xv[e], v0 + j * kN + e, ok && e != em && vm >= bv, m);
+        } else {
+          // the list is touched only by vectors whose max reaches the warp's m-th entry
+          float bv;
+          int bi;
+          wl.bar(m, bv, bi);
+          if (__any_sync(0xffffffffu, ok && vm >= bv)) {
+#pragma unroll
+            for (int e = 0; e < kN; ++e) wl.offer(xv[e], v0 + j * kN + e, ok && vm >= bv, m);
           }
         }
       }
     }
-    for (int i = v0 + nvec * kN + t; i < v1; i += kExpThreads) push(to_f32_any<T>(x[i]), i);
+    const int tail0 = v0 + nvec * kN;
+    for (int ib = tail0 + t - lane; ib < v1; ib += kExpThreads) scalar(ib + lane, ib + lane < v1);
   } else {
-    for (int i = v0 + t; i < v1; i += kExpThreads) push(to_f32_any<T>(x[i]), i);
+    for (int ib = v0 + t - lane; ib < v1; ib += kExpThreads) scalar(ib + lane, ib + lane < v1);
   }
-  // slice (max, sum): warp then CTA
+  // slice (max, sum): warp then CTA; slice list: the warps' lists merged by warp 0
   float wm = mc;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
@@ -239,28 +302,22 @@ __global__ void __launch_bounds__(kExpThreads) expand_kernel(ExpArgs a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
   if (lane == 0) s_ms[wid] = make_float2(wm, ws);
-  // slice top list: per warp, then across warps
-  warp_merge_lists<kM>(lv, li, s_v[wid], s_i[wid]);
+  s_v[wid][lane] = wl.v;
+  s_i[wid][lane] = wl.i;
   __syncthreads();
   const size_t slot = (size_t)row * a.S + slice;
   if (wid == 0) {
-    float cm = lane < kExpThreads / 32 ? s_ms[lane].x : -INFINITY;
+    const float cm = lane < kExpThreads / 32 ? s_ms[lane].x : -INFINITY;
     float cmax = cm;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
     float cs = (lane < kExpThreads / 32 && s_ms[lane].y > 0.f) ? s_ms[lane].y * ptx::ex2(cm - cmax) : 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
-#pragma unroll
-    for (int k = 0; k < kM; ++k) {
-      lv[k] = lane < kExpThreads / 32 ? s_v[lane][k] : -INFINITY;
-      li[k] = lane < kExpThreads / 32 ? s_i[lane][k] : 0x7fffffff;
-    }
-    warp_merge_lists<kM>(lv, li, s_fv, s_fi);
-    __syncwarp();
-    for (int k = lane; k < kM; k += 32) {
-      a.part_v[slot * kM + k] = s_fv[k];
-      a.part_i[slot * kM + k] = s_fi[k];
+    for (int w2 = 1; w2 < kExpThreads / 32; ++w2) wl.merge(s_v[w2][lane], s_i[w2][lane]);
+    if (lane < m) {
+      a.part_v[slot * 32 + lane] = wl.v;
+      a.part_i[slot * 32 + lane] = wl.i;
     }
     if (lane == 0) a.part_ms[slot] = make_float2(cmax, cs);
   }
@@ -272,9 +329,21 @@ __global__ void __launch_bounds__(kExpThreads) expand_kernel(ExpArgs a) {
     if (s_last) a.row_cnt[row] = 0;
   }
   __syncthreads();
-  if (!s_last || wid != 0) return;
+  if (!s_last) return;
   const size_t base = (size_t)row * a.S;
-  float2 ms = lane < a.S ? __ldcg(a.part_ms + base + lane) : make_float2(-INFINITY, 0.f);
+  // every warp merges a share of the row's slice lists, then warp 0 merges the warps'
+  wl.init();
+  for (int sl = wid; sl < a.S; sl += kExpThreads / 32) {
+    const float pv = lane < m ? __ldcg(a.part_v + (base + sl) * 32 + lane) : -INFINITY;
+    const int pi = lane < m ? __ldcg(a.part_i + (base + sl) * 32 + lane) : 0x7fffffff;
+    wl.merge(pv, pi);
+  }
+  s_v[wid][lane] = wl.v;
+  s_i[wid][lane] = wl.i;
+  __syncthreads();
+  if (wid != 0) return;
+  for (int w2 = 1; w2 < kExpThreads / 32; ++w2) wl.merge(s_v[w2][lane], s_i[w2][lane]);
+  const float2 ms = lane < a.S ? __ldcg(a.part_ms + base + lane) : make_float2(-INFINITY, 0.f);
   float rmax = ms.x;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, o));
@@ -282,34 +351,27 @@ __global__ void __launch_bounds__(kExpThreads) expand_kernel(ExpArgs a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
   const float lse2 = rmax + log2f(rs);
-#pragma unroll
-  for (int k = 0; k < kM; ++k) {
-    lv[k] = lane < a.S ? __ldcg(a.part_v + (base + lane) * kM + k) : -INFINITY;
-    li[k] = lane < a.S ? __ldcg(a.part_i + (base + lane) * kM + k) : 0x7fffffff;
-  }
-  warp_merge_lists<kM>(lv, li, s_fv, s_fi);
-  __syncwarp();
   const float ps = a.parent_score[row];
-  for (int k = lane; k < a.m; k += 32) {
-    const bool ok = k < a.V;
-    const float p = ok ? ptx::ex2(fmaf(s_fv[k], a.c2, -lse2)) : 0.f;
-    a.child_token[(size_t)row * a.m + k] = ok ? s_fi[k] : -1;
-    a.child_p[(size_t)row * a.m + k] = p;
-    a.child_score[(size_t)row * a.m + k] = ok ? __fmul_rn(ps, p) : 0.f;
+  if (lane < m) {
+    const bool ok = lane < a.V;
+    const float pr = ok ? ptx::ex2(fmaf(wl.v, a.c2, -lse2)) : 0.f;
+    a.child_token[(size_t)row * m + lane] = ok ? wl.i : -1;
+    a.child_p[(size_t)row * m + lane] = pr;
+    a.child_score[(size_t)row * m + lane] = ok ? __fmul_rn(ps, pr) : 0.f;
   }
 }
 
 // ------------------------------------------------------------------------------------
 // host side
 
-static int exp_km(int m) { return m <= 4 ? 4 : m <= 8 ? 8 : m <= 16 ? 16 : 32; }
+static int exp_km(int) { return 32; }  // slice lists are stored with 32 slots
 
 static void exp_plan(int R, int V, int& S, int& chunk) {
-  // about two CTAs per SM of the 152 (the per-slice merges are not free), at least 4096
-  // elements per slice
+  // about two CTAs per SM of the 152, but at least 16384 elements per slice: every slice
+  // pays a list seed, a CTA merge and a share of the row merge
   const long long want = (2LL * 152 + R - 1) / R;
   S = (int)std::min<long long>(std::max<long long>(1, want), kExpMaxSplits);
-  S = std::min(S, std::max(1, V / 4096));
+  S = std::min(S, std::max(1, V / 16384));
   chunk = (V + S - 1) / S;
   chunk = (chunk + 7) / 8 * 8;
   S = (V + chunk - 1) / chunk;
@@ -335,28 +397,14 @@ cudaError_t launch_frontier_topw(const float* scores, const int32_t* count, int 
   return cudaGetLastError();
 }
 
-template <typename T, int kM>
+template <typename T>
 static cudaError_t launch_expand_t(const ExpArgs& a, bool vec, cudaStream_t stream) {
   const unsigned grid = (unsigned)((long long)a.R * a.S);
   if (vec)
-    expand_kernel<T, kM, true><<<grid, kExpThreads, 0, stream>>>(a);
+    expand_kernel<T, true><<<grid, kExpThreads, 0, stream>>>(a);
   else
-    expand_kernel<T, kM, false><<<grid, kExpThreads, 0, stream>>>(a);
+    expand_kernel<T, false><<<grid, kExpThreads, 0, stream>>>(a);
   return cudaGetLastError();
-}
-
-template <typename T>
-static cudaError_t launch_expand_m(const ExpArgs& a, bool vec, cudaStream_t stream) {
-  switch (exp_km(a.m)) {
-    case 4:
-      return launch_expand_t<T, 4>(a, vec, stream);
-    case 8:
-      return launch_expand_t<T, 8>(a, vec, stream);
-    case 16:
-      return launch_expand_t<T, 16>(a, vec, stream);
-    default:
-      return launch_expand_t<T, 32>(a, vec, stream);
-  }
 }
 
 cudaError_t launch_expand(const void* logits, const float* parent_score, int R, int V, int m, float temperature,
@@ -387,7 +435,7 @@ cudaError_t launch_expand(const void* logits, const float* parent_score, int R, 
   const size_t esz = dtype == TV_BF16 ? 2 : 4;
   const bool vec = ((size_t)V * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(logits) % 16) == 0 &&
                    ((size_t)a.chunk * esz) % 16 == 0;
-  return dtype == TV_BF16 ? launch_expand_m<uint16_t>(a, vec, stream) : launch_expand_m<float>(a, vec, stream);
+  return dtype == TV_BF16 ? launch_expand_t<uint16_t>(a, vec, stream) : launch_expand_t<float>(a, vec, stream);
 }
 
 }  // namespace tv
