@@ -10,8 +10,6 @@
 
 namespace tv {
 
-constexpr int kSimtWarps = 4;
-constexpr int kSimtMaxD = 256;
 
 template <typename T>
 __device__ __forceinline__ float ldx(const T* p, size_t i) {
@@ -29,119 +27,182 @@ __device__ __forceinline__ void stx(T* p, size_t i, float v) {
     p[i] = v;
 }
 
+// One CTA per (b, kv head, block of kRowsCta query rows of that head's G x N rows).
+// Keys are walked in tiles of 32: the CTA stages the tile's K and V rows in shared memory
+// (K rows padded by one word so that 32 lanes reading 32 different rows hit 32 banks),
+// then every warp updates its rows: lane j scores key j of the tile, the warp keeps an
+// online softmax and accumulates p_j v_j with lanes split over D.
+constexpr int kSimtWarpsT = 8;
+constexpr int kRowsPerWarp = 4;
+constexpr int kRowsCta = kSimtWarpsT * kRowsPerWarp;
+constexpr int kKeyTile = 32;
+
 template <typename T, int kDPL>  // kDPL = D / 32 output dims per lane
-__global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
-                                                                   const T* __restrict__ v, T* __restrict__ out,
-                                                                   const int32_t* __restrict__ parent, int B, int Hq,
-                                                                   int Hkv, int D, int P, int N, int S, float scale,
-                                                                   int32_t* dev_status) {
-  __shared__ float s_q[kSimtWarps][kSimtMaxD];
-  __shared__ int s_anc[kSimtWarps][kMaxNodes];
+__global__ void __launch_bounds__(kSimtWarpsT * 32) attn_simt_kernel(const T* __restrict__ q,
+                                                                    const T* __restrict__ k,
+                                                                    const T* __restrict__ v, T* __restrict__ out,
+                                                                    const int32_t* __restrict__ parent, int B,
+                                                                    int Hq, int Hkv, int D, int P, int N, int S,
+                                                                    float scale, int32_t* dev_status) {
+  constexpr int kD = kDPL * 32;
+  extern __shared__ float simt_smem[];
+  // dynamic layout: K tile (rows padded by one word), V tile, the rows' queries, their
+  // visible-tree-node masks, the parent array
+  float(*s_k)[kD + 1] = reinterpret_cast<float(*)[kD + 1]>(simt_smem);
+  float(*s_v)[kD] = reinterpret_cast<float(*)[kD]>(simt_smem + kKeyTile * (kD + 1));
+  float(*s_q)[kD] = reinterpret_cast<float(*)[kD]>(simt_smem + kKeyTile * (kD + 1) + kKeyTile * kD);
+  uint32_t(*s_vis)[kMaxNodes / 32] = reinterpret_cast<uint32_t(*)[kMaxNodes / 32]>(
+      simt_smem + kKeyTile * (kD + 1) + kKeyTile * kD + kRowsCta * kD);
+  int* s_par = reinterpret_cast<int*>(simt_smem + kKeyTile * (kD + 1) + kKeyTile * kD + kRowsCta * kD +
+                                      kRowsCta * (kMaxNodes / 32));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * kSimtWarps + warp;
-  const long long rows = (long long)B * Hq * N;
-  if (row >= rows) return;
-  const int i = (int)(row % N);
-  const int h = (int)((row / N) % Hq);
-  const int b = (int)(row / ((long long)N * Hq));
   const int G = Hq / Hkv;
-  const int kh = h / G;
+  const int blocks_per_head = (G * N + kRowsCta - 1) / kRowsCta;
+  const int kh = (blockIdx.x / blocks_per_head) % Hkv;
+  const int b = blockIdx.x / (blocks_per_head * Hkv);
+  const int r0 = (blockIdx.x % blocks_per_head) * kRowsCta;
+  const int W = (N + 31) / 32;
   const int32_t* par = parent + (size_t)b * N;
-  // ancestors of i (root ... i), validated: each step must go to a smaller index
-  int na = 0;
-  if (lane == 0) {
-    int a = i, cnt = 0;
-    bool ok = true;
-    while (a >= 0) {
-      s_anc[warp][cnt++] = a;
-      const int pa = par[a];
-      if (!(pa < a) || (a == 0 && pa != -1) || (a > 0 && pa < 0)) {
-        ok = false;
-        break;
+  for (int c = threadIdx.x; c < N; c += blockDim.x) s_par[c] = par[c];
+  __syncthreads();
+  // rows of this CTA: query, visible-node mask (validated ancestor walk)
+  for (int rr = warp; rr < kRowsCta; rr += kSimtWarpsT) {
+    const int row = r0 + rr;
+    const bool live = row < G * N;
+    const int g = live ? row / N : 0, i = live ? row % N : 0;
+    const size_t qoff = (((size_t)b * Hq + kh * G + g) * N + i) * D;
+    for (int d = lane; d < kD; d += 32) s_q[rr][d] = live ? ldx(q, qoff + d) * scale : 0.f;
+    for (int w = lane; w < W; w += 32) s_vis[rr][w] = 0u;
+    __syncwarp();
+    if (lane == 0 && live) {
+      int a = i, guard = 0;
+      bool ok = true;
+      while (a >= 0 && guard <= N) {
+        s_vis[rr][a >> 5] |= 1u << (a & 31);
+        const int pa = s_par[a];
+        if (!(pa < a) || (a == 0 && pa != -1) || (a > 0 && pa < 0)) {
+          ok = false;
+          break;
+        }
+        a = pa;
+        ++guard;
       }
-      a = pa;
+      if (!ok) {
+        set_dev_status(dev_status, TV_DEV_BAD_TREE);
+        for (int w = 0; w < W; ++w) s_vis[rr][w] = 0u;
+        s_vis[rr][i >> 5] = 1u << (i & 31);
+      }
     }
-    if (!ok) {
-      set_dev_status(dev_status, TV_DEV_BAD_TREE);
-      cnt = 1;
-      s_anc[warp][0] = i;
-    }
-    na = cnt;
   }
-  na = __shfl_sync(0xffffffffu, na, 0);
-  const size_t qoff = (((size_t)b * Hq + h) * N + i) * D;
-  for (int d = lane; d < D; d += 32) s_q[warp][d] = ldx(q, qoff + d);
-  __syncwarp();
+  float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kDPL];
+#pragma unroll
+  for (int rw = 0; rw < kRowsPerWarp; ++rw) {
+    m[rw] = -INFINITY;
+    l[rw] = 0.f;
+#pragma unroll
+    for (int t = 0; t < kDPL; ++t) acc[rw][t] = 0.f;
+  }
   const size_t kvbase = ((size_t)b * Hkv + kh) * (size_t)S * D;
-  const int total = P + na;
-  float m = -INFINITY, l = 0.f;
-  float acc[kDPL];
+  const int total = P + N;
+  for (int j0 = 0; j0 < total; j0 += kKeyTile) {
+    __syncthreads();  // the previous tile is consumed
+    // all of a thread's tile loads are issued before any of them is stored
+    constexpr int kPer = kKeyTile * kD / (kSimtWarpsT * 32);
+    float kx[kPer], vx[kPer];
 #pragma unroll
-  for (int t = 0; t < kDPL; ++t) acc[t] = 0.f;
-  for (int j0 = 0; j0 < total; j0 += 32) {
+    for (int it = 0; it < kPer; ++it) {
+      const int e = threadIdx.x + it * kSimtWarpsT * 32;
+      const int jj = e / kD, d = e - jj * kD;
+      const bool in = j0 + jj < total;
+      const size_t off = kvbase + (size_t)(j0 + jj) * D + d;
+      kx[it] = in ? ldx(k, off) : 0.f;
+      vx[it] = in ? ldx(v, off) : 0.f;
+    }
+#pragma unroll
+    for (int it = 0; it < kPer; ++it) {
+      const int e = threadIdx.x + it * kSimtWarpsT * 32;
+      const int jj = e / kD, d = e - jj * kD;
+      s_k[jj][d] = kx[it];
+      s_v[jj][d] = vx[it];
+    }
+    __syncthreads();
     const int j = j0 + lane;
-    int krow = 0;
-    float s = -INFINITY;
-    if (j < total) {
-      krow = j < P ? j : P + s_anc[warp][j - P];
-      const T* kr = k + kvbase + (size_t)krow * D;
-      // eight independent partial dot products, so that the row's loads overlap
-      float dot[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) dot[u] = 0.f;
-      for (int d0 = 0; d0 < D; d0 += 8)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (d0 + u < D) dot[u] = fmaf(s_q[warp][d0 + u], ldx(kr, d0 + u), dot[u]);
-      s = (((dot[0] + dot[1]) + (dot[2] + dot[3])) + ((dot[4] + dot[5]) + (dot[6] + dot[7]))) * scale;
-    }
-    const float mnew = fmaxf(m, warp_max(s));
-    const float corr = exp2f((m - mnew) * kLog2e);
-    const float p = j < total ? exp2f((s - mnew) * kLog2e) : 0.f;
-    l = l * corr + warp_sum(p);
-#pragma unroll
-    for (int t = 0; t < kDPL; ++t) acc[t] *= corr;
-    const int cnt = min(32, total - j0);
-    for (int jb = 0; jb < cnt; jb += 4) {
-      // four value rows at a time: all their loads are issued before the FMAs
-      float vv[4][kDPL], pj[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int jj = min(jb + u, cnt - 1);
-        pj[u] = jb + u < cnt ? __shfl_sync(0xffffffffu, p, jj) : 0.f;
-        const int rj = __shfl_sync(0xffffffffu, krow, jj);
-        const T* vr = v + kvbase + (size_t)rj * D;
-#pragma unroll
-        for (int t = 0; t < kDPL; ++t) vv[u][t] = lane + 32 * t < D ? ldx(vr, lane + 32 * t) : 0.f;
+    for (int rw = 0; rw < kRowsPerWarp; ++rw) {
+      const int rr = warp + rw * kSimtWarpsT;
+      const int row = r0 + rr;
+      if (row >= G * N) continue;  // warp-uniform
+      bool vis = j < P;
+      if (j >= P && j < total) {
+        const int t = j - P;
+        vis = (s_vis[rr][t >> 5] >> (t & 31)) & 1u;
       }
+      float dot[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+      for (int d = 0; d < kD; d += 4) {
+        dot[0] = fmaf(s_q[rr][d], s_k[lane][d], dot[0]);
+        dot[1] = fmaf(s_q[rr][d + 1], s_k[lane][d + 1], dot[1]);
+        dot[2] = fmaf(s_q[rr][d + 2], s_k[lane][d + 2], dot[2]);
+        dot[3] = fmaf(s_q[rr][d + 3], s_k[lane][d + 3], dot[3]);
+      }
+      const float sc = vis ? (dot[0] + dot[1]) + (dot[2] + dot[3]) : -INFINITY;
+      const float mt = warp_max(sc);
+      if (mt == -INFINITY) continue;  // nothing visible in this tile for this row
+      const float mnew = fmaxf(m[rw], mt);
+      const float corr = exp2f((m[rw] - mnew) * kLog2e);
+      const float pj = vis ? exp2f((sc - mnew) * kLog2e) : 0.f;
+      l[rw] = l[rw] * corr + warp_sum(pj);
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int t = 0; t < kDPL; ++t) acc[rw][t] *= corr;
+#pragma unroll 4
+      for (int jj = 0; jj < kKeyTile; ++jj) {
+        const float pv = __shfl_sync(0xffffffffu, pj, jj);
 #pragma unroll
-        for (int t = 0; t < kDPL; ++t) acc[t] = fmaf(pj[u], vv[u][t], acc[t]);
+        for (int t = 0; t < kDPL; ++t) acc[rw][t] = fmaf(pv, s_v[jj][lane + 32 * t], acc[rw][t]);
+      }
+      m[rw] = mnew;
     }
-    m = mnew;
   }
-  const float inv = 1.f / l;
 #pragma unroll
-  for (int t = 0; t < kDPL; ++t) stx(out, qoff + lane + 32 * t, acc[t] * inv);
+  for (int rw = 0; rw < kRowsPerWarp; ++rw) {
+    const int rr = warp + rw * kSimtWarpsT;
+    const int row = r0 + rr;
+    if (row >= G * N) continue;
+    const int g = row / N, i = row % N;
+    const size_t ooff = (((size_t)b * Hq + kh * G + g) * N + i) * D;
+    const float inv = l[rw] > 0.f ? 1.f / l[rw] : 0.f;
+#pragma unroll
+    for (int t = 0; t < kDPL; ++t) stx(out, ooff + lane + 32 * t, acc[rw][t] * inv);
+  }
+}
+
+static size_t simt_smem_bytes(int d) {
+  return sizeof(float) * ((size_t)kKeyTile * (d + 1) + (size_t)kKeyTile * d + (size_t)kRowsCta * d +
+                          (size_t)kRowsCta * (kMaxNodes / 32) + kMaxNodes);
 }
 
 template <typename T>
 static void launch_simt_t(const void* q, const void* k, const void* v, void* out, const int32_t* parent, int B,
                           int Hq, int Hkv, int D, int P, int N, int S, float scale, int32_t* dev_status,
                           cudaStream_t stream) {
-  const long long rows = (long long)B * Hq * N;
-  const unsigned grid = (unsigned)((rows + kSimtWarps - 1) / kSimtWarps);
+  const int G = Hq / Hkv;
+  const long long blocks_per_head = ((long long)G * N + kRowsCta - 1) / kRowsCta;
+  const unsigned grid = (unsigned)(blocks_per_head * Hkv * B);
   const T* qq = reinterpret_cast<const T*>(q);
   const T* kk = reinterpret_cast<const T*>(k);
   const T* vv = reinterpret_cast<const T*>(v);
   T* oo = reinterpret_cast<T*>(out);
   switch (D / 32) {
 #define TV_SIMT_CASE(n)                                                                                        \
-  case n:                                                                                                      \
-    attn_simt_kernel<T, n><<<grid, kSimtWarps * 32, 0, stream>>>(qq, kk, vv, oo, parent, B, Hq, Hkv, D, P, N, S, \
-                                                                 scale, dev_status);                           \
-    break;
+  case n: {                                                                                                    \
+    const size_t smem = simt_smem_bytes(n * 32);                                                               \
+    if (cudaFuncSetAttribute(attn_simt_kernel<T, n>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != \
+        cudaSuccess)                                                                                           \
+      return;                                                                                                  \
+    attn_simt_kernel<T, n><<<grid, kSimtWarpsT * 32, smem, stream>>>(qq, kk, vv, oo, parent, B, Hq, Hkv, D, P, N, \
+                                                                    S, scale, dev_status);                     \
+    break;                                                                                                     \
+  }
     TV_SIMT_CASE(1)
     TV_SIMT_CASE(2)
     TV_SIMT_CASE(3)
