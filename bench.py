@@ -283,28 +283,44 @@ def gpu_identifier(torch, device_index):
 
 
 def measured_peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s burst, 'measured' | 'fallback')."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return d.get("hbm_gbs"), "measured"
-    return 6800.0, "fallback"
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
 
 
-def kernel_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source; else None."""
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of ``kernel`` on ``workload`` from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     ent = d.get(kernel)
-    if not ent:
+    if not ent or workload not in ent.get("workloads", {}):
         return None
     src = os.path.join(ROOT, "tree_speculative_decoding_masked_gb300", "csrc", ent["source"])
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return ent["bytes_per_launch"] if h == ent["source_sha256_16"] else None
+    return ent["workloads"][workload]["bytes_per_launch"] if h == ent["source_sha256_16"] else None
+
+
+def roofline_entry(kernel, bytes_per_launch, flops_per_launch, seconds, workload):
+    """Roofline of one kernel: HBM-bound unless its arithmetic intensity is above the
+    ridge point of the measured peaks, then bf16 tensor-bound."""
+    hbm, tflops, kind = measured_peaks()
+    tensor = flops_per_launch > 0 and flops_per_launch / bytes_per_launch > tflops * 1e12 / (hbm * 1e9)
+    if tensor:
+        achieved, peak, unit = flops_per_launch / seconds / 1e12, tflops, "TFLOP/s"
+    else:
+        achieved, peak, unit = bytes_per_launch / seconds / 1e9, hbm, "GB/s"
+    return {"bound": "tensor" if tensor else "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
+            "unit": unit, "frac": achieved / peak, "peak_kind": kind,
+            "traffic": kernel_traffic(kernel, workload), "algorithmic_bytes_per_launch": bytes_per_launch,
+            "algorithmic_flops_per_launch": flops_per_launch}
 
 
 def run_ours(args):
@@ -579,15 +595,14 @@ def run_ours(args):
     br = {name: timed(fam(name), fam_reps) * 1e3 / (fam_reps * n_sets) for name in fam_graphs}
     expand_bytes = exp_rows * V * elt
     commit_bytes = int(ver_out["accept_len"].sum().item()) * Hkv * D * elt * 2 * 2  # K and V rows, read + write
-    peak, peak_kind = measured_peaks()
     fam_bytes = {"attention": bytes_attn, "verify": bytes_vocab}
+    # dense-equivalent attention FLOPs: QK^T and PV over every (node row, key) pair of
+    # the prefix and the tree block, as the kernel computes them
+    fam_flops = {"attention": 4 * B * Hq * N * (P + N) * D, "verify": 0}
     dom = max(("attention", "verify"), key=lambda kk: br[kk])
-    achieved = fam_bytes[dom] / (br[dom] * 1e-6) / 1e9
     kernel_names = {"attention": "attn_tc_kernel" if bf16 else "attn_simt_kernel", "verify": "vocab_pass_tma_kernel"}
-    roofline = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_kind": peak_kind,
-                "traffic": kernel_traffic(kernel_names[dom]),
-                "algorithmic_bytes_per_launch": fam_bytes[dom]}
+    roofline = roofline_entry(kernel_names[dom], fam_bytes[dom], fam_flops[dom] if bf16 else 0, br[dom] * 1e-6,
+                              args.workload)
 
     # ---- end to end through the public API with host buffers (pinned), copies timed
     pinned = {kk: (to_dev(vv) if kk in ("q", "k", "v", "logits", "draft") else torch.from_numpy(vv)).cpu()

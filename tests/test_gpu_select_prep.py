@@ -81,6 +81,32 @@ def test_uniform_pools_all_ties(budget):
     _check_select(marg, ptok, budget, roots, _gpu_select(marg, ptok, budget, roots))
 
 
+@pytest.mark.parametrize("k,budget", [(8, 500), (9, 500), (8, 1500), (12, 3000)])
+def test_dyadic_pools_many_exact_ties(k, budget):
+    # marginals from {1/2, 1/4, 1/8, 1/16}: products are exact powers of two, so whole
+    # score classes tie across depths and rank paths; k = 8 and 9 sit on either side of
+    # the chain count at which the bound's histogram switches layout
+    g = synth.rng(500 + k + budget)
+    d = 16
+    marg = np.sort(2.0 ** -g.integers(1, 5, size=(2, d, k)), axis=2)[:, :, ::-1].astype(np.float32)
+    ptok = g.integers(0, 5000, size=(2, d, k)).astype(np.int32)
+    roots = np.array([3, 4], dtype=np.int32)
+    _check_select(marg, ptok, budget, roots, _gpu_select(marg, ptok, budget, roots))
+
+
+@pytest.mark.parametrize("budget", [200, 1200])
+def test_tiny_marginals_past_the_counting_range(budget):
+    # every edge scores about 2^-11, so paths of depth >= 3 fall below 2^-32, past the
+    # range of the quantised-log counting bound; the larger budget needs those paths and
+    # takes the one-deviation bound instead
+    g = synth.rng(900 + budget)
+    d, k = 16, 8
+    marg = np.sort(g.uniform(2.0 ** -12, 2.0 ** -10, size=(2, d, k)), axis=2)[:, :, ::-1].astype(np.float32)
+    ptok = g.integers(0, 5000, size=(2, d, k)).astype(np.int32)
+    roots = np.array([5, 6], dtype=np.int32)
+    _check_select(marg, ptok, budget, roots, _gpu_select(marg, ptok, budget, roots))
+
+
 def test_unsorted_pool_is_flagged():
     marg = np.array([[[0.2, 0.7], [0.6, 0.4]]], dtype=np.float32)
     ptok = np.array([[[1, 2], [3, 4]]], dtype=np.int32)

@@ -8,15 +8,18 @@
 // The key range [0, P + last node of the tile) is cut into KV splits across CTAs.
 //
 // Per CTA, warp-specialised:
-//   warp 0      TMA producer: Q tile once, then K/V tiles of 128 keys into a 2-stage ring
+//   warp 0      TMA producers: lane 0 loads the Q tile once, then K tiles of 128 keys
+//               into a 3-slot ring; lane 1 loads the V tiles into a 2-slot ring
 //   warp 1      TMEM owner; lane 0 issues S[t&1] = Q K_t^T (M=128, N=128, K=D, fp32
 //               in TMEM) as soon as a K tile and an S buffer are free
-//   warp 10     lane 0 issues O += P_t V_t (M=128, N=D, K=128, fp32 in TMEM) as soon as
-//               the softmax has written P_t
+//   warp 10     lane 0 issues O += P_t V_t (M=128, N=D, K=128, fp32 in TMEM, P_t read
+//               from TMEM) as soon as the softmax has written P_t
 //   warps 2..9  softmax: two threads per row (each half of a tile's 128 keys); read S
 //               from TMEM, apply the tree mask, agree on the row max with the partner
 //               thread, keep a running reference max (rescale O only when the max grows
-//               by more than 2^8), write P (bf16) to shared memory for the second MMA.
+//               by more than 2^8), write P (bf16) into one of two TMEM buffers, so the
+//               exponentials of tile t overlap the PV product of tile t-1.
+// TMEM columns: S[0] 0..127, S[1] 128..255, O 256..256+D, P[0] 384..447, P[1] 448..511.
 // With one split the epilogue normalises O and stores bf16.  With several, the splits of
 // a row tile run as one thread-block cluster: each CTA parks its unnormalised O and
 // (m, l) in its own shared memory and, after a cluster barrier, merges a slice of the
@@ -32,8 +35,9 @@ namespace tv {
 
 constexpr int kRows = 128;     // MMA M: query rows per CTA
 constexpr int kBN = 128;       // keys per KV tile (MMA N of QK^T, K of PV)
-constexpr int kStages = 2;     // K/V ring depth (tiles of 128 keys)
-constexpr int kThreads = 352;  // 11 warps: TMA producer, S issuer, 8 softmax warps, PV issuer
+constexpr int kKSlots = 3;     // K ring depth (tiles of 128 keys)
+constexpr int kVSlots = 2;     // V ring depth
+constexpr int kThreads = 352;  // 11 warps: TMA producers, S issuer, 8 softmax warps, PV issuer
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxSplits = 8;  // KV splits of a row tile = one portable-size cluster
 
@@ -43,19 +47,19 @@ struct TcCfg {
   static constexpr int kQBlock = kRows * 128;         // bytes per column block of Q
   static constexpr int kKVBlock = kBN * 128;          // bytes per column block of a K or V tile
   static constexpr int kQBytes = kDB * kQBlock;
-  static constexpr int kStageBytes = 2 * kDB * kKVBlock;
-  static constexpr int kPBlock = kRows * 128;         // bytes per 64-key column block of P
-  static constexpr int kPBytes = kRows * kBN * 2;     // the P buffer (128 rows x 128 keys bf16)
+  static constexpr int kTileBytes = kDB * kKVBlock;   // one K or V tile
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = kOffQ + kQBytes;
-  static constexpr int kOffP = kOffKV + kStages * kStageBytes;
-  static constexpr int kOffPar = kOffP + kPBytes;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffV = kOffK + kKSlots * kTileBytes;
+  static constexpr int kOffPar = kOffV + kVSlots * kTileBytes;
   static constexpr int kOffBar = kOffPar + kMaxNodes * 4;
   static constexpr int kSmemUsed = kOffBar + 256;
   static constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack for 1024-byte alignment
-  static constexpr uint32_t kTmemCols = 512;           // S[0], S[1] (128 each) + O (D)
-  static constexpr uint32_t kColO = 2 * kBN;
-  static_assert(kColO + D <= kTmemCols, "TMEM budget");
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 2 * kBN;           // after S[0], S[1]
+  static constexpr uint32_t kColP = 384;               // P[0], P[1]: 64 columns each
+  static_assert(kColO + D <= kColP && kColP + 2 * (kBN / 2) <= kTmemCols, "TMEM budget");
+  static_assert(kOffV - kOffK >= D * kRows * 4 + kRows * 8, "split partials fit in the drained K ring");
 };
 
 struct TcArgs {
@@ -68,12 +72,14 @@ struct TcArgs {
 
 struct Bars {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t k_full[kKSlots];
+  uint64_t k_empty[kKSlots];
+  uint64_t v_full[kVSlots];
+  uint64_t v_empty[kVSlots];
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t p_full;
-  uint64_t p_free;
+  uint64_t p_full[2];
+  uint64_t pv_done[2];  // PV(t) complete, on barrier t & 1
   uint64_t o_done;
   uint64_t s_done;
   uint32_t tmem_base;
@@ -108,8 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t mis = ptx::smem_addr(smem_raw) & 1023u;
   unsigned char* sm = smem_raw + ((1024u - mis) & 1023u);
   unsigned char* sQ = sm + C::kOffQ;
-  unsigned char* sKV = sm + C::kOffKV;
-  unsigned char* sP = sm + C::kOffP;
+  unsigned char* sK = sm + C::kOffK;
+  unsigned char* sV = sm + C::kOffV;
   int* s_par = reinterpret_cast<int*>(sm + C::kOffPar);
   Bars* bars = reinterpret_cast<Bars*>(sm + C::kOffBar);
   volatile int* abort_flag = &bars->abort;
@@ -129,16 +135,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(&bars->kv_full[s], 1);
-      ptx::mbar_init(&bars->kv_empty[s], 1);
+    for (int s = 0; s < kKSlots; ++s) {
+      ptx::mbar_init(&bars->k_full[s], 1);
+      ptx::mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < kVSlots; ++s) {
+      ptx::mbar_init(&bars->v_full[s], 1);
+      ptx::mbar_init(&bars->v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&bars->s_full[s], 1);
       ptx::mbar_init(&bars->s_free[s], 8);
+      ptx::mbar_init(&bars->p_full[s], 8);
+      ptx::mbar_init(&bars->pv_done[s], 1);
     }
-    ptx::mbar_init(&bars->p_full, 8);
-    ptx::mbar_init(&bars->p_free, 1);
     ptx::mbar_init(&bars->o_done, 1);
     ptx::mbar_init(&bars->s_done, 1);
     bars->abort = 0;
@@ -172,51 +182,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ producer
+    // ------------------------------------------------------------------ producers
     if (lane == 0 && nt > 0) {
-      int issued[kStages];
+      // Q once, then the K tiles; a slot is refilled once S of its previous tile is done
+      int issued[kKSlots];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s) issued[s] = 0;
+      for (int s = 0; s < kKSlots; ++s) issued[s] = 0;
       ptx::prefetch_tmap(&tmQ);
       ptx::prefetch_tmap(&tmK);
-      ptx::prefetch_tmap(&tmV);
       ptx::mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(rows_used * 128 * C::kDB));
       for (int g = 0; g < a.G; ++g)
         for (int db = 0; db < C::kDB; ++db)
           ptx::tma_load_3d(sQ + db * C::kQBlock + g * a.NT * 128, &tmQ, &bars->q_full, db * 64, i0,
                            b * a.Hq + hk * a.G + g);
       for (int t = 0; t < nt; ++t) {
-        const int st = t % kStages;
-        if (t >= kStages && !ptx::mbar_wait(&bars->kv_empty[st], ((t / kStages) - 1) & 1, abort_flag)) break;
-        unsigned char* sK = sKV + st * C::kStageBytes;
-        unsigned char* sV = sK + C::kDB * C::kKVBlock;
+        const int ks = t % kKSlots;
+        if (t >= kKSlots && !ptx::mbar_wait(&bars->k_empty[ks], ((t / kKSlots) - 1) & 1, abort_flag)) break;
+        unsigned char* dst = sK + ks * C::kTileBytes;
         const int j0 = (t_begin + t) * kBN;
-        ptx::mbar_arrive_expect_tx(&bars->kv_full[st], (uint32_t)C::kStageBytes);
-        for (int db = 0; db < C::kDB; ++db) {
-          ptx::tma_load_3d(sK + db * C::kKVBlock, &tmK, &bars->kv_full[st], db * 64, j0, b * a.Hkv + hk);
-          ptx::tma_load_3d(sV + db * C::kKVBlock, &tmV, &bars->kv_full[st], db * 64, j0, b * a.Hkv + hk);
-        }
-        ++issued[st];
+        ptx::mbar_arrive_expect_tx(&bars->k_full[ks], (uint32_t)C::kTileBytes);
+        for (int db = 0; db < C::kDB; ++db)
+          ptx::tma_load_3d(dst + db * C::kKVBlock, &tmK, &bars->k_full[ks], db * 64, j0, b * a.Hkv + hk);
+        ++issued[ks];
       }
       // never leave the CTA with copies in flight
       ptx::mbar_wait(&bars->q_full, 0, abort_flag);
-      for (int s = 0; s < kStages; ++s)
-        if (issued[s]) ptx::mbar_wait(&bars->kv_full[s], (issued[s] - 1) & 1, abort_flag);
+      for (int s = 0; s < kKSlots; ++s)
+        if (issued[s]) ptx::mbar_wait(&bars->k_full[s], (issued[s] - 1) & 1, abort_flag);
+    } else if (lane == 1 && nt > 0) {
+      // the V tiles; a slot is refilled once PV of its previous tile is done
+      int issued[kVSlots];
+#pragma unroll
+      for (int s = 0; s < kVSlots; ++s) issued[s] = 0;
+      ptx::prefetch_tmap(&tmV);
+      for (int t = 0; t < nt; ++t) {
+        const int vs = t % kVSlots;
+        if (t >= kVSlots && !ptx::mbar_wait(&bars->v_empty[vs], ((t / kVSlots) - 1) & 1, abort_flag)) break;
+        unsigned char* dst = sV + vs * C::kTileBytes;
+        const int j0 = (t_begin + t) * kBN;
+        ptx::mbar_arrive_expect_tx(&bars->v_full[vs], (uint32_t)C::kTileBytes);
+        for (int db = 0; db < C::kDB; ++db)
+          ptx::tma_load_3d(dst + db * C::kKVBlock, &tmV, &bars->v_full[vs], db * 64, j0, b * a.Hkv + hk);
+        ++issued[vs];
+      }
+      for (int s = 0; s < kVSlots; ++s)
+        if (issued[s]) ptx::mbar_wait(&bars->v_full[s], (issued[s] - 1) & 1, abort_flag);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       if (nt > 0 && ptx::mbar_wait(&bars->q_full, 0, abort_flag)) {
         constexpr uint32_t idS = ptx::idesc_bf16(kRows, kBN, false, false);
-        constexpr uint32_t idO = ptx::idesc_bf16(kRows, D, false, true);
         const uint32_t qaddr = ptx::smem_addr(sQ);
         bool ok = true;
         auto issue_s = [&](int t) -> bool {
-          const int st = t % kStages, sb = t & 1;
-          if (!ptx::mbar_wait(&bars->kv_full[st], (t / kStages) & 1, abort_flag)) return false;
+          const int ks = t % kKSlots, sb = t & 1;
+          if (!ptx::mbar_wait(&bars->k_full[ks], (t / kKSlots) & 1, abort_flag)) return false;
           if (t >= 2 && !ptx::mbar_wait(&bars->s_free[sb], ((t >> 1) - 1) & 1, abort_flag)) return false;
           ptx::tc_fence_after();
-          const uint32_t kaddr = ptx::smem_addr(sKV + st * C::kStageBytes);
+          const uint32_t kaddr = ptx::smem_addr(sK + ks * C::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk & 3) * 32;  // 16-element K step inside a 128-byte row
@@ -225,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_bf16_ss(tmem + sb * kBN, ad, bd, idS, kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit(&bars->s_full[sb]);
+          ptx::mma_commit(&bars->k_empty[ks]);
           return true;
         };
         // S = QK^T tiles run ahead of the softmax (bounded by the two S buffers); the PV
@@ -241,19 +267,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nt > 0) {
         constexpr uint32_t idO = ptx::idesc_bf16(kRows, D, false, true);
         for (int t = 0; t < nt; ++t) {
-          const int st = t % kStages;
-          if (!ptx::mbar_wait(&bars->p_full, t & 1, abort_flag)) break;
+          const int vs = t % kVSlots, pb = t & 1;
+          if (!ptx::mbar_wait(&bars->p_full[pb], (t >> 1) & 1, abort_flag)) break;
+          if (!ptx::mbar_wait(&bars->v_full[vs], (t / kVSlots) & 1, abort_flag)) break;
           ptx::tc_fence_after();
-          const uint32_t paddr = ptx::smem_addr(sP);
-          const uint32_t vaddr = ptx::smem_addr(sKV + st * C::kStageBytes + C::kDB * C::kKVBlock);
+          const uint32_t vaddr = ptx::smem_addr(sV + vs * C::kTileBytes);
+          const uint32_t paddr = tmem + C::kColP + pb * (kBN / 2);  // 16 keys = 8 columns
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t ad = ptx::sdesc_sw128(paddr + (kk >> 2) * C::kPBlock + (kk & 3) * 32, 16, 1024);
             const uint64_t bd = ptx::sdesc_sw128(vaddr + kk * 16 * 128, C::kKVBlock, 1024);
-            ptx::mma_bf16_ss(tmem + C::kColO, ad, bd, idO, (t > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_bf16_ts(tmem + C::kColO, paddr + kk * 8, bd, idO, (t > 0 || kk > 0) ? 1u : 0u);
           }
-          ptx::mma_commit(&bars->kv_empty[st]);
-          ptx::mma_commit(&bars->p_free);
+          ptx::mma_commit(&bars->v_empty[vs]);
+          ptx::mma_commit(&bars->pv_done[pb]);
         }
       }
       ptx::mma_commit(&bars->o_done);
@@ -328,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (__any_sync(0xffffffffu, need) && t > 0 && ok) {
         // O already holds PV(t-1): wait for it, then scale this thread's half of the row
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->p_free, (t - 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag));
       }
       if (__any_sync(0xffffffffu, need) && t > 0 && ok) {
         ptx::tc_fence_after();
@@ -344,36 +370,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_wait_st();
       }
       l_run *= alpha;
-      // the single P buffer is free once PV(t-1) has completed
-      if (t >= 1 && ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->p_free, (t - 1) & 1, abort_flag));
+      // P buffer t & 1 is free once PV(t-2) has completed
+      if (t >= 2 && ok)
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->pv_done[sb], ((t >> 1) - 1) & 1, abort_flag));
       if (!ok) continue;  // nothing more to compute or signal for this tile
-      // P = 2^(S*c - m_run) on visible keys, bf16, 128-byte-swizzled K-major rows
-      unsigned char* prow = sP + h * C::kPBlock + r * 128;  // this half's 64-key column block
+      // P = 2^(S*c - m_run) on visible keys, bf16 pairs along the key axis, into this
+      // thread's 32 columns of the TMEM P buffer (its row's lane)
       float ls8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) ls8[k] = 0.f;
       const bool live = m_run != -INFINITY;
+      uint32_t pw[kBN / 4];
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
-        const int ch = cc;  // 16-byte chunk of the row
         float pv[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           pv[k] = live ? ptx::ex2(fmaf(sv[cc * 8 + k], a.c, -m_run)) : 0.f;
           ls8[k] += pv[k];
         }
-        uint4 u;
-        u.x = ptx::cvt_bf16x2(pv[0], pv[1]);
-        u.y = ptx::cvt_bf16x2(pv[2], pv[3]);
-        u.z = ptx::cvt_bf16x2(pv[4], pv[5]);
-        u.w = ptx::cvt_bf16x2(pv[6], pv[7]);
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) pw[cc * 4 + k] = ptx::cvt_bf16x2(pv[2 * k], pv[2 * k + 1]);
       }
       l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-      ptx::fence_proxy_async_smem();
+      ptx::tmem_st32u(tmem + lane_base + C::kColP + sb * (kBN / 2) + h * (kBN / 4), pw);
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->p_full);
+      if (lane == 0) ptx::mbar_arrive(&bars->p_full[sb]);
     }
     // ---- epilogue: the row's sum is the two halves' sums
     s_xl[h][r] = l_run;
@@ -417,8 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // park this split's unnormalised O as row-major [128][D] fp32 with the 16-byte chunks
       // of row r XOR-swizzled by (r & 7) (conflict-free 16-byte stores), plus (m, l), in
       // the drained K/V ring for the cluster merge below
-      unsigned char* part = sKV;
-      float2* ml = reinterpret_cast<float2*>(sKV + D * kRows * 4);
+      unsigned char* part = sK;
+      float2* ml = reinterpret_cast<float2*>(sK + D * kRows * 4);
 #pragma unroll
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
         float ov[32];
@@ -455,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r0 = split * R, r1 = min(kRows, r0 + R);
       const int nrows = max(0, r1 - r0);
       constexpr int kChunks = D / 4;
-      const uint32_t part_local = ptx::smem_addr(sKV);
-      const uint32_t ml_local = ptx::smem_addr(sKV + D * kRows * 4);
+      const uint32_t part_local = ptx::smem_addr(sK);
+      const uint32_t ml_local = ptx::smem_addr(sK + D * kRows * 4);
       for (int item = threadIdx.x; item < nrows * kChunks; item += kThreads) {
         const int rr = r0 + item / kChunks;
         const int ch = item % kChunks;

@@ -31,6 +31,9 @@ namespace tv {
 
 constexpr int kSelThreads = 512;
 constexpr int kSelCap = 4096;      // candidates held during the expansion
+constexpr int kSelSlots = kSelCap + 32;  // + one spare slot per lane for masked-off stores
+static_assert((size_t)kSelSlots * 28 + (size_t)kSelCap * 8 >= (size_t)kMaxBudget * 36,
+              "the heap fallback fits below the pool copy");
 constexpr int kSelDevRanks = 32;   // ranks 1..31 enumerated in the one-deviation family
 constexpr int kSelBins = 512;      // coarse score classes of [2^-63, 1]: 8 per octave, the lowest takes the rest
 constexpr int kSelRetries = 4;     // expansions with a raised bound before the fallback
@@ -271,76 +274,185 @@ __device__ float coarse_bound(const int* hist, int M, int* wsum, float* s_tau) {
   return *s_tau;
 }
 
+// A second lower bound on the M-th best score, for large budgets, where the one-deviation
+// family is sparse next to the whole candidate tree: count every candidate by its
+// quantised log score.  Edge weight w = ceil(-16 log2 m + slack) >= -16 log2 m (16 bins
+// per octave, 32 octaves; m = 0 or weights past the range are left out), so a path whose
+// weights sum to <= v has an exact product >= 2^(-v/16); its fp32 product is within 16
+// roundings of that, which the final scale covers.  H_l[v] = number of depth-l paths of
+// weight v, built level by level (H_{l+1}[v] = sum over ranks of H_l[v - w]; counts
+// saturate at 2^40).  The bound is 2^(-v*/16) (slightly shrunk) for the smallest v* whose
+// paths of weight <= v* number at least M; 0 if the range holds fewer.
+constexpr int kLogBins = kSelThreads;  // one weight bin per thread
+constexpr int kCountMinRows = 128;     // smaller budgets use the one-deviation bound alone
+
+__device__ float counting_bound(const SelSmem& sm, int d, int K, int M, unsigned long long* red, float* s_tau) {
+  const int t = threadIdx.x;
+  const int Kp = (K + 7) & ~7;                                            // ranks padded to whole groups of 8
+  int* wts = sm.idx;                                                      // [d][Kp] weights
+  unsigned long long* H = reinterpret_cast<unsigned long long*>(sm.pos);  // [2][kLogBins]
+  for (int i = t; i < d * Kp; i += blockDim.x) {
+    const int l = i / Kp, r = i - l * Kp;
+    const float m = r < K ? sm.marg[l * K + r] : 0.f;
+    int w = kLogBins;
+    if (m > 0.f) {
+      const float x = -16.f * log2f(m) + 1e-3f;
+      if (x < (float)kLogBins) w = max((int)ceilf(x), 0);
+    }
+    wts[i] = w;
+  }
+  H[t] = t == 0 ? 1ull : 0ull;
+  __syncthreads();
+  unsigned long long acc = 0;
+  for (int l = 0; l < d; ++l) {
+    const unsigned long long* cur = H + (l & 1) * kLogBins;
+    const int* wl = wts + l * Kp;
+    unsigned long long h = 0;
+    // weights grow with the rank: groups of 8 independent gathers until the first
+    // weight past the range (the same for every thread)
+    for (int r0 = 0; r0 < Kp && wl[r0] < kLogBins; r0 += 8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int w = wl[r0 + q];
+        const unsigned long long x = cur[max(t - w, 0)];
+        h += w <= t ? x : 0ull;
+      }
+    }
+    h = min(h, 1ull << 40);
+    H[((l + 1) & 1) * kLogBins + t] = h;
+    acc += h;
+    __syncthreads();
+  }
+  unsigned long long tot;
+  const unsigned long long excl = block_scan_u64(acc, red, &tot);
+  if (t == 0) *s_tau = 0.f;
+  __syncthreads();
+  if (excl < (unsigned long long)M && excl + acc >= (unsigned long long)M)
+    *s_tau = exp2f(-(float)t / 16.f) * (1.f - 1.f / 65536.f);
+  __syncthreads();
+  return *s_tau;
+}
+
 // Expand every candidate with s >= tau.  Each candidate lies on exactly one "run": a node
 // reached by a rank >= 1 edge (or a child of the root), followed by its rank-0
 // descendants.  Step 0 starts the runs at the root's children; step i+1 starts runs at
-// the rank >= 1 children of every node made in step i.  Per step, the nodes with at
-// least one qualifying child are listed first; then one thread per (listed node, rank)
-// pair follows a run (its scores are a running fp32 product, exactly the left-to-right
-// path product).  The number of steps is 1 + the largest number of rank >= 1 edges on a
-// kept path.  Returns the entry count, or -(stored + 1) if more than kSelCap entries would
-// be needed; then entries [0, stored) are complete (runs are allocated in increasing
-// order, so the first run that did not fit ends the stored prefix) and prefix-closed.
-__device__ __forceinline__ int expand_threshold(const SelSmem& sm, int d, int K, float tau, int* s_count,
-                                                int* s_fail, int* s_live) {
+// the rank >= 1 children of every node made in step i.  One thread per (source node,
+// rank) pair follows a run (its scores are a running fp32 product, exactly the
+// left-to-right path product; the rank-0 factors m0 sit in registers); when the pairs
+// outnumber the block, only the qualifying pairs are listed first (found per source by
+// bisection over its sorted ranks).
+// The number of steps is 1 + the largest number of rank >= 1 edges on a kept path.
+// Step i counts its allocations in the set (i mod 3) of the counters: a set is cleared
+// one step before its use and read by every thread one step after, so one barrier per
+// step (two with the listing) orders everything.  Returns the entry count, or
+// -(stored + 1) if more than kSelCap entries would be needed; then entries [0, stored)
+// are complete (runs are allocated in increasing order, so the first run that did not
+// fit ends the stored prefix) and prefix-closed.
+struct ExpandCounters {
+  int count[3];  // entries allocated by the step
+  int fail[3];   // lowest offset that did not fit
+  int live[3];   // (source, rank) pairs listed by the step
+};
+
+__device__ __forceinline__ int expand_threshold(const SelSmem& sm, const float (&m0)[kMaxDepth], int d, int K,
+                                                float tau, ExpandCounters* ec) {
   const int t = threadIdx.x, lane = t & 31;
-  int* live = sm.idx;  // sources with a qualifying child, this step
-  if (t == 0) {
-    *s_count = 0;
-    *s_fail = 0x7fffffff;
-    *s_live = 0;
+  if (t < 3) {
+    ec->count[t] = 0;
+    ec->fail[t] = 0x7fffffff;
+    ec->live[t] = 0;
   }
   __syncthreads();
   int lo = 0, hi = 0;  // entries made by the previous step; step 0 expands the virtual root
-  for (int step = 0;; ++step) {
+  for (int step = 0, b = 0;; ++step, b = b == 2 ? 0 : b + 1) {
     const int nsrc = step == 0 ? 1 : hi - lo;
-    if (nsrc <= 0) break;
     const int r0 = step == 0 ? 0 : 1;
     const int nr = K - r0;
-    if (nr <= 0) break;
-    // 1. sources whose best rank >= r0 child reaches tau (ranks are sorted)
-    for (int ib = t - lane; ib < nsrc; ib += blockDim.x) {
-      const int i = ib + lane;
-      bool ok = false;
-      if (i < nsrc) {
-        const uint64_t pk0 = step == 0 ? make_k0(1.f, 0) : sm.k0[lo + i];
-        const int dep = (int)(pk0 & 0xFFFFFFFFu);
-        ok = dep < d && __fmul_rn(k0_score(pk0), sm.marg[dep * K + r0]) >= tau;
-      }
-      const unsigned m = __ballot_sync(0xffffffffu, ok);
-      if (m == 0) continue;
-      int wb = 0;
-      if (lane == 0) wb = atomicAdd(s_live, __popc(m));
-      wb = __shfl_sync(0xffffffffu, wb, 0);
-      if (ok) live[wb + __popc(m & ((1u << lane) - 1))] = step == 0 ? -1 : lo + i;
+    if (nsrc <= 0 || nr <= 0) break;
+    if (t == 0) {  // the set for step + 1 was last read before the previous barrier
+      const int nb = b == 2 ? 0 : b + 1;
+      ec->count[nb] = 0;
+      ec->fail[nb] = 0x7fffffff;
+      ec->live[nb] = 0;
     }
-    __syncthreads();
-    const int nlive = *s_live;
-    __syncthreads();
-    if (t == 0) *s_live = 0;
-    // 2. one thread per (listed source, rank): the run from that child
-    const int items = nlive * nr;
-    for (int ib = t - lane; ib < items; ib += blockDim.x) {  // warp-uniform trip count
+    int nitems = nsrc * nr;
+    const bool listed = nitems > (int)blockDim.x;
+    bool dropped = false;
+    int* item = sm.pos;  // listed (source, rank) pairs, (entry + 1) << 8 | rank
+    if (listed) {
+      // per source the qualifying ranks form a prefix of [r0, K) (ranks are sorted and the
+      // rounded product is monotone): count them by bisection, list every pair.  Each
+      // pair makes at least one entry, so pairs past the free space are dropped and the
+      // step then reports the overflow after storing what fits.
+      for (int ib = t - lane; ib < nsrc; ib += blockDim.x) {
+        const int i = ib + lane;
+        int nq = 0, pe = -1;
+        if (i < nsrc) {
+          pe = step == 0 ? -1 : lo + i;
+          const uint64_t pk0 = pe < 0 ? make_k0(1.f, 0) : sm.k0[pe];
+          const int dep = (int)(pk0 & 0xFFFFFFFFu);
+          if (dep < d) {
+            const float ps = k0_score(pk0);
+            const float* row = sm.marg + dep * K;
+            int a = r0, z = K;  // the first rank in [r0, K] whose child misses tau
+            while (a < z) {
+              const int mid = (a + z) >> 1;
+              if (__fmul_rn(ps, row[mid]) >= tau)
+                a = mid + 1;
+              else
+                z = mid;
+            }
+            nq = a - r0;
+          }
+        }
+        int incl = nq;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total == 0) continue;
+        int wb = 0;
+        if (lane == 31) wb = atomicAdd(&ec->live[b], total);
+        const int base = __shfl_sync(0xffffffffu, wb, 31) + incl - nq;
+        for (int q = 0; q < nq && base + q < kSelCap - hi; ++q) item[base + q] = (pe + 1) << 8 | (r0 + q);
+      }
+      __syncthreads();
+      nitems = ec->live[b];
+      dropped = nitems > kSelCap - hi;
+      if (dropped) nitems = kSelCap - hi;
+    }
+    // one thread per (source, rank): the run from that child
+    for (int ib = t - lane; ib < nitems; ib += blockDim.x) {  // warp-uniform trip count
       const int it = ib + lane;
       int len = 0, pe = -1, dep = 0, r = 0;
       float s0 = 0.f;
-      if (it < items) {
-        const int i = it / nr;
-        r = r0 + (it - i * nr);
-        pe = live[i];
+      if (it < nitems) {
+        if (listed) {
+          const int v = item[it];
+          pe = (v >> 8) - 1;
+          r = v & 255;
+        } else {
+          const int i = it / nr;
+          r = r0 + (it - i * nr);
+          pe = step == 0 ? -1 : lo + i;
+        }
         const uint64_t pk0 = pe < 0 ? make_k0(1.f, 0) : sm.k0[pe];
         dep = (int)(pk0 & 0xFFFFFFFFu);  // children sit at position dep
-        s0 = __fmul_rn(k0_score(pk0), sm.marg[dep * K + r]);
-        if (s0 >= tau) {
-          // run length: the rank-r child, then rank-0 descendants while s >= tau
-          len = 1;
+        if (dep < d) {
+          s0 = __fmul_rn(k0_score(pk0), sm.marg[dep * K + r]);
+          // run length: the rank-r child, then rank-0 descendants while s >= tau.  The
+          // products along a run never grow, so this is the count of its products that
+          // reach tau; the multiply chain carries no compare.
+          int cnt = 1;
           float sc = s0;
-          for (int p = dep + 1; p < d; ++p) {
-            const float nx = __fmul_rn(sc, sm.marg[p * K]);
-            if (!(nx >= tau)) break;
-            sc = nx;
-            ++len;
+#pragma unroll
+          for (int p = 1; p < kMaxDepth; ++p) {
+            sc = __fmul_rn(sc, p > dep ? m0[p] : 1.f);
+            cnt += (p > dep && p < d && sc >= tau) ? 1 : 0;
           }
+          len = s0 >= tau ? cnt : 0;
         }
       }
       // one allocation per warp: lanes take consecutive slots in lane order
@@ -352,84 +464,82 @@ __device__ __forceinline__ int expand_threshold(const SelSmem& sm, int d, int K,
       }
       const int total = __shfl_sync(0xffffffffu, incl, 31);
       if (total == 0) continue;
+      const int wmax = __reduce_max_sync(0xffffffffu, len);
       int wbase = 0;
-      if (lane == 31) wbase = atomicAdd(s_count, total);
-      const int base = __shfl_sync(0xffffffffu, wbase, 31) + incl - len;
+      if (lane == 31) wbase = atomicAdd(&ec->count[b], total);
+      const int base = hi + __shfl_sync(0xffffffffu, wbase, 31) + incl - len;
       if (len == 0) continue;
       if (base + len > kSelCap) {
-        atomicMin(s_fail, base);
+        atomicMin(&ec->fail[b], base);
         continue;
       }
       uint64_t c1 = pe < 0 ? 0ull : sm.k1[pe], c2 = pe < 0 ? 0ull : sm.k2[pe];
       path_set(c1, c2, dep, r);
+      // branch-free stores: entries outside the run go to the lane's spare slot.  Short
+      // runs (every run of the warp within 4) walk 4 positions with the factors read
+      // from shared memory; longer ones walk all positions with the factors in registers.
       float sc = s0;
-      for (int q = 0; q < len; ++q) {
-        if (q > 0) sc = __fmul_rn(sc, sm.marg[(dep + q) * K]);
-        const int e = base + q;
-        sm.k0[e] = make_k0(sc, dep + q + 1);
-        sm.k1[e] = c1;
-        sm.k2[e] = c2;
-        sm.par[e] = q == 0 ? pe : e - 1;
+      if (wmax <= 4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q > 0) sc = __fmul_rn(sc, sm.marg[min(dep + q, d - 1) * K]);
+          const int e = q < len ? base + q : kSelCap + lane;
+          sm.k0[e] = make_k0(sc, dep + q + 1);
+          sm.k1[e] = c1;
+          sm.k2[e] = c2;
+          sm.par[e] = q == 0 ? pe : e - 1;
+        }
+      } else {
+#pragma unroll
+        for (int p = 0; p < kMaxDepth; ++p) {
+          const int q = p - dep;
+          sc = __fmul_rn(sc, p > dep ? m0[p] : 1.f);
+          const int e = (unsigned)q < (unsigned)len ? base + q : kSelCap + lane;
+          sm.k0[e] = make_k0(sc, p + 1);
+          sm.k1[e] = c1;
+          sm.k2[e] = c2;
+          sm.par[e] = q == 0 ? pe : e - 1;
+        }
       }
     }
     __syncthreads();
-    const int fail = *s_fail, cnt = *s_count;
-    __syncthreads();  // every thread has read the counters before the next step moves them
-    if (fail != 0x7fffffff) return -fail - 1;
+    const int cnt = ec->count[b];
+    int fail = ec->fail[b];
+    if (dropped && fail == 0x7fffffff) fail = hi + cnt;  // everything allocated is stored
+    if (fail != 0x7fffffff) {
+      __syncthreads();  // every thread has read the set before a restart clears it
+      return -fail - 1;
+    }
     lo = hi;
-    hi = cnt;
+    hi += cnt;
   }
+  __syncthreads();  // every thread has read the last set before a restart clears it
   return hi;
 }
 
-// bitonic sort of sm.idx[0..n2) (entries, -1 = padding last) in the selection order
-__device__ void bitonic_sort_idx(const SelSmem& sm, int n2) {
-  for (int size = 2; size <= n2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < n2 / 2; i += blockDim.x) {
-        const int lo = 2 * stride * (i / stride) + (i % stride);
-        const int hi = lo + stride;
-        const bool asc = (lo & size) == 0;
-        const int a = sm.idx[lo], c = sm.idx[hi];
-        bool a_gt;
-        if (a < 0)
-          a_gt = c >= 0;
-        else if (c < 0)
-          a_gt = false;
-        else
-          a_gt = key_less(sm.k0[c], sm.k1[c], sm.k2[c], sm.k0[a], sm.k1[a], sm.k2[a]);
-        if (a_gt == asc) {
-          sm.idx[lo] = c;
-          sm.idx[hi] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
+constexpr int kFewChains = 128;  // up to this many chains share one histogram
 
-constexpr int kRankDirect = 512;  // rank by direct comparison up to this many candidates
-
-// Threshold selection by the block.  Returns 1 + number selected, or -1 if the
-// candidate set did not fit (the caller falls back).
-__device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_count, int* s_fail, int* hist,
-                                int* bcast, float* s_tau, int32_t* o_par, int32_t* o_tok, int32_t* o_dep,
-                                float* o_sc) {
-  const int t = threadIdx.x;
-  // 1. coarse histogram of the one-deviation candidates (ranks < kSelDevRanks)
-  // per-lane histogram columns (lane-major, in the expansion buffers, free for now): the
-  // atomics of a warp never collide
-  int* hcol = reinterpret_cast<int*>(sm.k1);
-  for (int i = t; i < 32 * kSelBins / 4; i += blockDim.x) reinterpret_cast<int4*>(hcol)[i] = make_int4(0, 0, 0, 0);
-  float m0[kMaxDepth];  // rank-0 factors, in registers for the run loops
-#pragma unroll
-  for (int p = 0; p < kMaxDepth; ++p) m0[p] = p < d ? sm.marg[p * K] : 1.f;
-  __syncthreads();
+// The one-deviation bound (see the top of this file): one coarse class histogram.
+__device__ float family_bound(const SelSmem& sm, const float (&m0)[kMaxDepth], int d, int K, int M, int* hist,
+                              int* bcast, float* s_tau) {
+  const int t = threadIdx.x, lane = t & 31;
+  // coarse histogram of the one-deviation candidates (ranks < kSelDevRanks).  Few
+  // chains: spread over the warps (a few lanes each) into one shared histogram.  Many:
+  // per-lane histogram columns (lane-major, in the expansion buffers, free for now), so
+  // the atomics of a warp never collide.
   const int rmax = min(K, kSelDevRanks);
   const int nchain = 1 + d * (rmax - 1);  // chain 0: no deviation; else (position j, rank r)
-  const int lane = t & 31;
-  int* mycol = hcol + lane * kSelBins;
-  for (int c = t; c < nchain; c += blockDim.x) {
+  const bool few = nchain <= kFewChains;
+  int* hcol = reinterpret_cast<int*>(sm.k1);
+  if (few)
+    hist[t] = 0;
+  else
+    for (int i = t; i < 32 * kSelBins / 4; i += blockDim.x) reinterpret_cast<int4*>(hcol)[i] = make_int4(0, 0, 0, 0);
+  __syncthreads();
+  int* mycol = few ? hist : hcol + lane * kSelBins;
+  const int nw = blockDim.x >> 5;
+  // few: chain c on lane c / nw of warp c % nw
+  for (int c = few ? (lane * nw + (t >> 5)) : t; c < nchain; c += blockDim.x) {
     int j = -1, r = 0;
     if (c > 0) {
       j = (c - 1) / (rmax - 1);
@@ -437,27 +547,46 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_c
     }
     const float mj = j >= 0 ? sm.marg[j * K + r] : 1.f;
     float sc = 1.f;
+    // the prefixes that contain the deviation are counted; the other positions add to
+    // the lane's spare bin (branch-free)
 #pragma unroll
     for (int p = 0; p < kMaxDepth; ++p) {
-      if (p < d) {
-        sc = __fmul_rn(sc, p == j ? mj : m0[p]);
-        if (p >= j) atomicAdd(&mycol[score_class(sc)], 1);  // prefixes that contain the deviation
-      }
+      sc = __fmul_rn(sc, p == j ? mj : m0[p]);
+      atomicAdd(p < d && p >= j ? &mycol[score_class(sc)] : &hist[kSelBins + lane], 1);
     }
   }
   __syncthreads();
-  {
+  if (!few) {
     int h = 0;
 #pragma unroll 8
     for (int l = 0; l < 32; ++l) h += hcol[l * kSelBins + t];
     hist[t] = h;
+    __syncthreads();
   }
-  __syncthreads();
-  float tau = coarse_bound(hist, M, bcast + 2, s_tau);
+  return coarse_bound(hist, M, bcast + 2, s_tau);
+}
+
+constexpr int kRankDirect = 512;  // rank by direct comparison up to this many candidates
+
+// Threshold selection by the block.  Returns 1 + number selected, or -1 if the
+// candidate set did not fit (the caller falls back).
+__device__ int select_threshold(const SelSmem& sm, int d, int K, int M, ExpandCounters* ec, int* s_count, int* hist,
+                                int* bcast, float* s_tau, int32_t* o_par, int32_t* o_tok, int32_t* o_dep,
+                                float* o_sc) {
+  const int t = threadIdx.x;
+  float m0[kMaxDepth];  // rank-0 factors, in registers for the run loops
+#pragma unroll
+  for (int p = 0; p < kMaxDepth; ++p) m0[p] = p < d ? sm.marg[p * K] : 1.f;
+  // 1. a lower bound on the M-th best score: for small budgets the one-deviation bound
+  // (cheap, and tight enough); for large ones the counting bound, which stays within a
+  // few percent of M candidates where the one-deviation family is far too sparse
+  float tau = M >= kCountMinRows ? counting_bound(sm, d, K, M, reinterpret_cast<unsigned long long*>(hist), s_tau)
+                                 : 0.f;
+  if (!(tau > 0.f)) tau = family_bound(sm, m0, d, K, M, hist, bcast, s_tau);
   // 2. expansion; restarts with tau raised to the M-th best stored score
   int n = -1;
   for (int attempt = 0; attempt <= kSelRetries; ++attempt) {
-    n = expand_threshold(sm, d, K, tau, s_count, s_fail, bcast + 2 + kSelThreads / 32);
+    n = expand_threshold(sm, m0, d, K, tau, ec);
     if (n >= 0) break;
     const int stored = -n - 1;
     n = -1;
@@ -474,51 +603,105 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, int* s_c
   const int take = min(n, M);
   // 3. order: the output position of entry e is 1 + its rank in the selection order
   if (n <= kRankDirect) {
-    for (int e = t; e < n; e += blockDim.x) {
-      // branch-free count on the (score, depth) word; exact ties are resolved on the
-      // rank path only when they occur
-      const uint64_t a0 = sm.k0[e];
-      int less = 0, eq = 0;
-      int j = 0;
-      const ulonglong2* k0v = reinterpret_cast<const ulonglong2*>(sm.k0);
+    // L lanes per entry (a power of two, L * n <= blockDim): a branch-free count on the
+    // (score, depth) word; exact ties are resolved on the rank path only when they occur
+    int L = 1;
+    while (L < 32 && 2 * L * n <= (int)blockDim.x) L <<= 1;
+    const int e = t / L, sub = t & (L - 1);
+    const bool own = e < n;
+    const uint64_t a0 = own ? sm.k0[e] : 0ull;
+    int less = 0, eq = 0;
+    if (own) {
+      int j = sub;
 #pragma unroll 4
-      for (; j + 2 <= n; j += 2) {
-        const ulonglong2 c = k0v[j >> 1];
-        less += (c.x < a0) + (c.y < a0);
-        eq += (c.x == a0) + (c.y == a0);
+      for (; j < n; j += L) {
+        const uint64_t c = sm.k0[j];
+        less += c < a0;
+        eq += c == a0;
       }
-      if (j < n) {
-        less += sm.k0[j] < a0;
-        eq += sm.k0[j] == a0;
-      }
-      int rank = less;
-      if (eq > 1) {
-        const uint64_t a1 = sm.k1[e], a2 = sm.k2[e];
-        for (int q = 0; q < n; ++q)
-          if (sm.k0[q] == a0 && key_less(a0, sm.k1[q], sm.k2[q], a0, a1, a2)) ++rank;
-      }
+    }
+    for (int o = 1; o < L; o <<= 1) {
+      less += __shfl_xor_sync(0xffffffffu, less, o);
+      eq += __shfl_xor_sync(0xffffffffu, eq, o);
+    }
+    int tied_before = 0;
+    if (own && eq > 1) {
+      const uint64_t a1 = sm.k1[e], a2 = sm.k2[e];
+      for (int q = sub; q < n; q += L)
+        if (sm.k0[q] == a0 && key_less(a0, sm.k1[q], sm.k2[q], a0, a1, a2)) ++tied_before;
+    }
+    if (__any_sync(0xffffffffu, tied_before != 0))
+      for (int o = 1; o < L; o <<= 1) tied_before += __shfl_xor_sync(0xffffffffu, tied_before, o);
+    if (own && sub == 0) {
+      const int rank = less + tied_before;
       sm.pos[e] = rank < take ? rank + 1 : 0;
       if (rank < take) sm.idx[rank] = e;
     }
   } else {
-    // only entries with s >= (M-th best score) can be taken: sort just those
-    uint32_t* sc = reinterpret_cast<uint32_t*>(sm.pos);
-    for (int i = t; i < n; i += blockDim.x) sc[i] = __float_as_uint(k0_score(sm.k0[i]));
+    // counting sort on the score bits: kSelCap bins over [tau, 1] (bin 0 = the highest
+    // scores), then the exact order inside each bin by direct comparison
+    static_assert(kSelCap % kSelThreads == 0, "whole bins per thread");
+    constexpr int kPer = kSelCap / kSelThreads;
+    int* cnt = sm.pos;   // bin counts, then bin ends
+    int* list = sm.idx;  // entries grouped by bin
+    const uint32_t u_hi = __float_as_uint(1.f), u_lo = __float_as_uint(tau);
+    int shift = 0;
+    while (((u_hi - u_lo) >> shift) >= (uint32_t)kSelCap) ++shift;
+    auto bin_of = [&](uint64_t k0) {  // clamped, so out-of-range scores keep the order
+      const uint32_t u = __float_as_uint(k0_score(k0));
+      return u >= u_hi ? 0 : (int)((u_hi - max(u, u_lo)) >> shift);
+    };
+    for (int i = t; i < kSelCap; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
-    const uint32_t T = block_kth_largest(sc, n, take, hist, bcast);
-    if (t == 0) *s_count = 0;
+    for (int e = t; e < n; e += blockDim.x) atomicAdd(&cnt[bin_of(sm.k0[e])], 1);
     __syncthreads();
-    for (int i = t; i < n; i += blockDim.x)
-      if (sc[i] >= T) sm.idx[atomicAdd(s_count, 1)] = i;
+    {  // exclusive scan: thread t owns bins [kPer t, kPer t + kPer)
+      int c[kPer];
+      unsigned long long own = 0;
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        c[q] = cnt[kPer * t + q];
+        own += c[q];
+      }
+      unsigned long long tot;
+      int run = (int)block_scan_u64(own, reinterpret_cast<unsigned long long*>(hist), &tot);
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        cnt[kPer * t + q] = run;
+        run += c[q];
+      }
+    }
     __syncthreads();
-    const int cnt_ge = *s_count;
-    int n2 = 1;
-    while (n2 < cnt_ge) n2 <<= 1;
-    if (n2 > 2 * kSelCap) return -1;
-    for (int i = cnt_ge + t; i < n2; i += blockDim.x) sm.idx[i] = -1;
-    __syncthreads();
-    bitonic_sort_idx(sm, n2);
-    for (int i = t; i < take; i += blockDim.x) sm.pos[sm.idx[i]] = i + 1;
+    for (int e = t; e < n; e += blockDim.x) list[atomicAdd(&cnt[bin_of(sm.k0[e])], 1)] = e;
+    __syncthreads();  // cnt[b] is now the end of bin b
+    int rk[kPer], en[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int j = t + q * kSelThreads;
+      en[q] = -1;
+      rk[q] = 0;
+      if (j < n) {
+        const int e = list[j];
+        const uint64_t a0 = sm.k0[e], a1 = sm.k1[e], a2 = sm.k2[e];
+        const int bn = bin_of(a0);
+        const int lo = bn > 0 ? cnt[bn - 1] : 0, hi = cnt[bn];
+        int rank = lo;
+        for (int x = lo; x < hi; ++x) {
+          const int f = list[x];
+          const uint64_t c0 = sm.k0[f];
+          rank += c0 < a0 || (c0 == a0 && key_less(c0, sm.k1[f], sm.k2[f], a0, a1, a2));
+        }
+        en[q] = e;
+        rk[q] = rank;
+      }
+    }
+    __syncthreads();  // the bins and the list are read; positions overwrite them
+#pragma unroll
+    for (int q = 0; q < kPer; ++q)
+      if (en[q] >= 0) {
+        sm.pos[en[q]] = rk[q] < take ? rk[q] + 1 : 0;
+        if (rk[q] < take) sm.idx[rk[q]] = en[q];
+      }
   }
   __syncthreads();
   for (int i = t; i < take; i += blockDim.x) {
@@ -616,18 +799,19 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
                                                              float* out_score, int32_t* n_nodes, int32_t* dev_status,
                                                              float cost_base, float cost_per_row) {
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int hist[kSelBins > 256 ? kSelBins : 256];
+  __shared__ __align__(16) int hist[kSelBins + 32];  // + one spare bin per lane
   __shared__ int bcast[3 + kSelThreads / 32];
   __shared__ float s_tau;
-  __shared__ int s_bad, s_nout, s_count, s_fail;
+  __shared__ int s_bad, s_nout, s_count;
+  __shared__ ExpandCounters s_ec;
   const int b = blockIdx.x, tid = threadIdx.x;
   const int M = budget - 1;
   SelSmem sm;
   sm.k0 = reinterpret_cast<uint64_t*>(smem);
-  sm.k1 = sm.k0 + kSelCap;
-  sm.k2 = sm.k1 + kSelCap;
-  sm.par = reinterpret_cast<int*>(sm.k2 + kSelCap);
-  sm.idx = sm.par + kSelCap;
+  sm.k1 = sm.k0 + kSelSlots;
+  sm.k2 = sm.k1 + kSelSlots;
+  sm.par = reinterpret_cast<int*>(sm.k2 + kSelSlots);
+  sm.idx = sm.par + kSelSlots;
   sm.pos = sm.idx + kSelCap;
   sm.marg = reinterpret_cast<float*>(sm.pos + kSelCap);
   sm.tok = reinterpret_cast<int*>(sm.marg + d * K);
@@ -663,7 +847,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
   if (M <= 0) {
     if (tid == 0) s_nout = 1;
   } else if (M <= kSelCap / 2) {
-    const int r = select_threshold(sm, d, K, M, &s_count, &s_fail, hist, bcast, &s_tau, o_par, o_tok, o_dep, o_sc);
+    const int r = select_threshold(sm, d, K, M, &s_ec, &s_count, hist, bcast, &s_tau, o_par, o_tok, o_dep, o_sc);
     if (tid == 0) s_nout = r;
   }
   __syncthreads();
@@ -687,7 +871,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
 }
 
 static size_t select_smem_bytes(int d, int K, int budget) {
-  const size_t expand = (size_t)kSelCap * (3 * 8 + 3 * 4);
+  const size_t expand = (size_t)kSelSlots * (3 * 8 + 4) + (size_t)kSelCap * 2 * 4;
   const size_t heap = (size_t)budget * (3 * 8 + 4 + 4);
   // the heap fallback reuses the start of the buffer; marg/tok follow the expansion arrays
   return (expand > heap ? expand : heap) + (size_t)d * K * 8;
