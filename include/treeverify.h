@@ -98,6 +98,18 @@ TV_API int tv_version(void);
 TV_API tv_status tv_set_sm_partition(int verify_sms, int attention_sms);
 
 /* ------------------------------------------------------------------------------------
+ * tv_set_attention_variant - which tensor-core kernel tv_tree_attention uses for bf16.
+ *   0  automatic (default): paired row tiles when a (sequence, KV head) has more than
+ *      one 128-row tile of query rows (G * N > 128), else one tile per CTA
+ *   1  one 128-row tile per CTA
+ *   2  paired row tiles: one CTA streams the KV range once for two 128-row tiles
+ * Both compute the same result (up to fp32 summation order); the switch exists to
+ * compare and test them.  Process-wide, host-side; affects launches made after the call.
+ * Errors: a value outside 0..2 -> TV_ERR_VALUE.
+ */
+TV_API tv_status tv_set_attention_variant(int variant);
+
+/* ------------------------------------------------------------------------------------
  * tv_tree_prep - tree structure for the attention mask and position encoding.
  * PTD §3.1 "tree construction": node v observes pi(v) = {v} U pi(P(v)); its position
  * encoding follows |pi(v)|.

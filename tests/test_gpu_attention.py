@@ -188,3 +188,58 @@ def test_bad_tree_flagged():
         tv.tree_attention(to_dev(q, bf16), to_dev(k, bf16), to_dev(v, bf16), i32(par), P, dev_status=st)
         torch.cuda.synchronize()
         assert int(st.item()) & tv.TV_DEV_BAD_TREE
+
+
+@pytest.fixture(params=[1, 2], ids=["one_tile_per_cta", "paired_tiles"])
+def variant(request):
+    tv.set_attention_variant(request.param)
+    yield request.param
+    tv.set_attention_variant(0)
+
+
+@pytest.mark.parametrize("shape", [
+    # B, Hq, Hkv, D, P, N, depth cap
+    (1, 8, 2, 128, 1000, 70, 8),    # three row tiles: one full pair and a pair with no second tile
+    (1, 8, 2, 128, 96, 64, 6),      # the pair's second tile needs one KV tile more than the first
+    (2, 4, 4, 64, 130, 129, 16),    # G = 1, D = 64, two row tiles
+    (1, 6, 2, 64, 77, 45, 3),       # G = 3, padding rows in every tile
+    (1, 4, 1, 128, 0, 300, 16),     # empty prefix, three row tiles of tree keys only
+    (2, 32, 8, 128, 2048, 64, 8),   # the qwen3 layer shape, two sequences (KV splits in clusters)
+    (1, 4, 1, 128, 5000, 96, 12),   # many KV tiles per split, the last split shorter
+])
+def test_shapes_both_variants(variant, shape):
+    B, Hq, Hkv, D, P, N, cap = shape
+    g = synth.rng(sum(shape) + 7)
+    par, _ = W.trees(g, B, N, cap, 100)
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, True)
+    _check_all(q, k, v, par, P, True)
+
+
+def test_rescale_path_both_variants(variant):
+    # scores growing along the key axis force O rescales in either kernel
+    B, Hq, Hkv, D, P, N = 1, 4, 1, 128, 3000, 200
+    g = synth.rng(36)
+    par, _ = W.trees(g, B, N, 8, 100)
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, False)
+    ramp = np.linspace(0.0, 6.0, P + N, dtype=np.float32)[None, None, :, None]
+    k = synth.round_to_bf16((k * 0.2 + ramp * np.sign(q.mean(axis=(0, 1, 2)))[None, None, None, :]).astype(np.float32))
+    _check_all(synth.round_to_bf16(q), k, synth.round_to_bf16(v), par, P, True)
+
+
+def test_chain_and_star_both_variants(variant):
+    B, Hq, Hkv, D, P, N = 1, 8, 2, 128, 700, 100
+    g = synth.rng(37)
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, True)
+    got = _run(q, k, v, synth.chain_parents(N)[None], P, True)
+    for h in range(Hq):
+        ref = attention.causal_attention(q[0, h], k[0, h // 4, :P + N], v[0, h // 4, :P + N], 1 / math.sqrt(D))
+        assert np.max(np.abs(got[0, h] - ref)) < 2e-2
+    _check_all(q, k, v, synth.star_parents(N)[None], P, True)
+
+
+def test_long_context_workload_sampled_one_tile_per_cta():
+    tv.set_attention_variant(1)
+    try:
+        _sampled_rows("long_context", 24, seed_extra=5)
+    finally:
+        tv.set_attention_variant(0)

@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     prune_tree,
     select_subtree,
     select_workspace_size,
+    set_attention_variant,
     set_sm_partition,
     status_string,
     tree_attention,

@@ -41,6 +41,7 @@ _SIGS = {
     "tv_status_string": (ctypes.c_char_p, [_I]),
     "tv_version": (_I, []),
     "tv_set_sm_partition": (_I, [_I, _I]),
+    "tv_set_attention_variant": (_I, [_I]),
     "tv_tree_prep": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "tv_prune_tree": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "tv_tree_attention_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
@@ -142,6 +143,11 @@ def _status_tensor(dev_status, device):
 def set_sm_partition(verify_sms: int, attention_sms: int):
     """SM shares for running tree_attention and verify_* concurrently (0, 0 = whole device)."""
     _check("tv_set_sm_partition", load_library().tv_set_sm_partition(int(verify_sms), int(attention_sms)))
+
+
+def set_attention_variant(variant: int):
+    """Tensor-core attention kernel: 0 automatic, 1 one 128-row tile per CTA, 2 paired tiles."""
+    _check("tv_set_attention_variant", load_library().tv_set_attention_variant(int(variant)))
 
 
 def tree_prep(parent: torch.Tensor, prefix_len: int, *, dev_status=None, out=None):

@@ -8,10 +8,13 @@ using namespace tv;
 
 // SM shares for running the vocab pass and the tree attention concurrently (0 = all SMs)
 static int g_sm_verify = 0, g_sm_attention = 0;
+// tensor-core attention kernel: 0 automatic, 1 one row tile per CTA, 2 paired row tiles
+static int g_attn_variant = 0;
 
 namespace tv {
 int sm_share_verify() { return g_sm_verify; }
 int sm_share_attention() { return g_sm_attention; }
+int attention_variant() { return g_attn_variant; }
 }  // namespace tv
 
 namespace {
@@ -56,6 +59,12 @@ tv_status tv_set_sm_partition(int verify_sms, int attention_sms) {
   if (verify_sms < 0 || attention_sms < 0) return TV_ERR_VALUE;
   g_sm_verify = verify_sms;
   g_sm_attention = attention_sms;
+  return TV_OK;
+}
+
+tv_status tv_set_attention_variant(int variant) {
+  if (variant < 0 || variant > 2) return TV_ERR_VALUE;
+  g_attn_variant = variant;
   return TV_OK;
 }
 

@@ -86,6 +86,47 @@ struct Bars {
   int abort;
 };
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// max of `init` and 64 scores: four independent chains of three-input maxima
+__device__ __forceinline__ float max64(const float (&sv)[64], float init) {
+  float c0 = init, c1 = -INFINITY, c2 = -INFINITY, c3 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 64; j += 8) {
+    c0 = fmax3(c0, sv[j], sv[j + 1]);
+    c1 = fmax3(c1, sv[j + 2], sv[j + 3]);
+    c2 = fmax3(c2, sv[j + 4], sv[j + 5]);
+    c3 = fmax3(c3, sv[j + 6], sv[j + 7]);
+  }
+  return fmaxf(fmax3(c0, c1, c2), c3);
+}
+
+// P = 2^(s * c - m) of 64 scores as 32 bf16 pairs (key 2k in the low half of pw[k]);
+// returns the fp32 sum of the unrounded values.  m = -inf means every score seen so far
+// is masked (-inf): the offset is then 0 and every P is 2^-inf = 0.  Packed fp32x2 FMA
+// and add halve their instruction count.
+__device__ __forceinline__ float exp_p64(const float (&sv)[64], float c, float m, uint32_t (&pw)[32]) {
+  const float nm = m == -INFINITY ? 0.f : -m;
+  const float2 cc = make_float2(c, c), nm2 = make_float2(nm, nm);
+  float2 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const float2 t = __ffma2_rn(make_float2(sv[2 * k], sv[2 * k + 1]), cc, nm2);
+    const float e0 = ptx::ex2(t.x), e1 = ptx::ex2(t.y);
+    acc[k & 3] = __fadd2_rn(acc[k & 3], make_float2(e0, e1));
+    pw[k] = ptx::cvt_bf16x2(e0, e1);
+  }
+  const float2 s2 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  return s2.x + s2.y;
+}
+
 // 64-bit visibility mask of keys [j0, j0 + 64) for tree node `node` (half a KV tile).
 __device__ __forceinline__ uint64_t key_mask(int j0, int P, int N, int node, const int* s_par) {
   if (j0 + 64 <= P) return ~0ull;
@@ -331,14 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < kBN / 2; ++j)
           if (!((vis >> j) & 1ull)) sv[j] = -INFINITY;
       }
-      float m8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) m8[k] = sv[k];
-#pragma unroll
-      for (int j = 8; j < kBN / 2; j += 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], sv[j + k]);
-      float tm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      float tm = max64(sv, -INFINITY);
       s_xmax[t & 1][h][r] = tm;
       pair_sync();
       tm = fmaxf(tm, s_xmax[t & 1][h ^ 1][r]);
@@ -376,23 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) continue;  // nothing more to compute or signal for this tile
       // P = 2^(S*c - m_run) on visible keys, bf16 pairs along the key axis, into this
       // thread's 32 columns of the TMEM P buffer (its row's lane)
-      float ls8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) ls8[k] = 0.f;
-      const bool live = m_run != -INFINITY;
       uint32_t pw[kBN / 4];
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        float pv[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          pv[k] = live ? ptx::ex2(fmaf(sv[cc * 8 + k], a.c, -m_run)) : 0.f;
-          ls8[k] += pv[k];
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) pw[cc * 4 + k] = ptx::cvt_bf16x2(pv[2 * k], pv[2 * k + 1]);
-      }
-      l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      l_run += exp_p64(sv, a.c, m_run, pw);
       ptx::tmem_st32u(tmem + lane_base + C::kColP + sb * (kBN / 2) + h * (kBN / 4), pw);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -534,6 +553,482 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------
+// Paired row tiles.  One CTA owns two 128-row tiles A and B of the same (b, kv head)
+// (tiles 2m and 2m + 1) and streams the KV range once for both: every K/V tile fetched
+// serves 256 query rows.  The two tiles ping-pong on the tensor core: while the softmax
+// warps of tile A turn S_A into probabilities, the tensor core runs S_B and PV_B, and
+// the other way round.
+//   warp 0      TMA producers: lane 0 loads Q_A, Q_B once, then K tiles into a 2-slot
+//               ring; lane 1 loads the V tiles into a 2-slot ring
+//   warp 1      TMEM owner; lane 0 issues S_X = Q_X K_t^T for X = A, B
+//   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B: one thread per row
+//               (TMEM lane), 128 keys per tile, no partner thread to wait for
+//   warp 10     lane 0 issues O_X += P_X V_t
+// TMEM columns: S_A 0..127, S_B 128..255, O_A 256.., O_B 384...  P_X (bf16) is written
+// over S_X by its own row's thread: keys 64..127 into columns 64..95 (S values already
+// in registers), then keys 0..63 into columns 0..31 after they have been read again.
+// S_X of the next KV tile is issued only once PV_X of the current one has completed, so
+// it never overwrites P_X early, and O_X is quiescent whenever its softmax runs.
+constexpr int kPairSlots = 2;  // K ring and V ring depth
+
+template <int D>
+struct PairCfg {
+  static constexpr int kDB = D / 64;
+  static constexpr int kQBlock = kRows * 128;       // bytes per column block of one Q tile
+  static constexpr int kQTile = kDB * kQBlock;      // one Q tile
+  static constexpr int kKVBlock = kBN * 128;        // bytes per column block of a K or V tile
+  static constexpr int kTileBytes = kDB * kKVBlock; // one K or V tile
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kQTile;
+  static constexpr int kOffV = kOffK + kPairSlots * kTileBytes;
+  static constexpr int kOffPar = kOffV + kPairSlots * kTileBytes;
+  static constexpr int kOffBar = kOffPar + kMaxNodes * 4;
+  static constexpr int kSmemUsed = kOffBar + 256;
+  static constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 2 * kBN;           // O_X at kColO + X * 128
+  static_assert(kColO + kBN + D <= kTmemCols, "TMEM budget");
+  static_assert(2 * kPairSlots * kTileBytes >= 2 * kRows * D * 4, "split partials fit in the drained rings");
+  static_assert(2 * kQTile >= 2 * kRows * 8, "(m, l) of both tiles fit in the drained Q tiles");
+  static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
+};
+
+struct PairBars {
+  uint64_t q_full;
+  uint64_t k_full[kPairSlots];
+  uint64_t k_empty[kPairSlots];
+  uint64_t v_full[kPairSlots];
+  uint64_t v_empty[kPairSlots];
+  uint64_t s_full[2];   // S_X(t) complete
+  uint64_t p_full[2];   // P_X(t) written (4 warps)
+  uint64_t pv_done[2];  // PV_X(t) complete
+  uint64_t o_done;
+  uint64_t s_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, TcArgs a) {
+  using C = PairCfg<D>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t mis = ptx::smem_addr(smem_raw) & 1023u;
+  unsigned char* sm = smem_raw + ((1024u - mis) & 1023u);
+  unsigned char* sQ = sm + C::kOffQ;
+  unsigned char* sK = sm + C::kOffK;
+  unsigned char* sV = sm + C::kOffV;
+  int* s_par = reinterpret_cast<int*>(sm + C::kOffPar);
+  PairBars* bars = reinterpret_cast<PairBars*>(sm + C::kOffBar);
+  volatile int* abort_flag = &bars->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the splits of one tile pair are consecutive in x and form one cluster (rank = split)
+  const int mp = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
+  const int hk = blockIdx.y, b = blockIdx.z;
+  int i0[2], t_allx[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    i0[x] = (2 * mp + x) * a.NT;
+    t_allx[x] = i0[x] < a.N ? (a.P + min(a.N, i0[x] + a.NT) + kBN - 1) / kBN : 0;
+  }
+  const int t_all = max(t_allx[0], t_allx[1]);
+  const int tps = (t_all + a.splits - 1) / a.splits;
+  const int t_begin = split * tps;
+  int ntx[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) ntx[x] = max(0, min(t_allx[x], t_begin + tps) - t_begin);
+  const int nt = max(ntx[0], ntx[1]);
+  const int rows_used = a.G * a.NT;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kPairSlots; ++s) {
+      ptx::mbar_init(&bars->k_full[s], 1);
+      ptx::mbar_init(&bars->k_empty[s], 1);
+      ptx::mbar_init(&bars->v_full[s], 1);
+      ptx::mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      ptx::mbar_init(&bars->s_full[x], 1);
+      ptx::mbar_init(&bars->p_full[x], 4);
+      ptx::mbar_init(&bars->pv_done[x], 1);
+    }
+    ptx::mbar_init(&bars->o_done, 1);
+    ptx::mbar_init(&bars->s_done, 1);
+    bars->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp >= 2) {
+    // parent array for the mask; zero the Q rows that no TMA box fills
+    const int t = threadIdx.x - 64;
+    int bad = 0;
+    for (int c = t; c < a.N; c += kThreads - 64) {
+      const int p = a.parent[(size_t)b * a.N + c];
+      s_par[c] = p;
+      if (!((c == 0) ? (p == -1) : (p >= 0 && p < c))) bad = 1;
+    }
+    if (bad) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);
+    for (int r = rows_used + t; r < 2 * kRows; r += kThreads - 64) {
+      const int x = r >= kRows ? 1 : 0, rr = r - x * kRows;
+      if (rr < rows_used) continue;
+      for (int db = 0; db < C::kDB; ++db) {
+        uint4* row = reinterpret_cast<uint4*>(sQ + x * C::kQTile + db * C::kQBlock + rr * 128);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) row[k] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producers
+    if (lane == 0 && nt > 0) {
+      int issued[kPairSlots] = {0, 0};
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmK);
+      uint32_t qbytes = 0;
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+        if (ntx[x] > 0) qbytes += (uint32_t)(rows_used * 128 * C::kDB);
+      ptx::mbar_arrive_expect_tx(&bars->q_full, qbytes);
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+        if (ntx[x] > 0)
+          for (int g = 0; g < a.G; ++g)
+            for (int db = 0; db < C::kDB; ++db)
+              ptx::tma_load_3d(sQ + x * C::kQTile + db * C::kQBlock + g * a.NT * 128, &tmQ, &bars->q_full, db * 64,
+                               i0[x], b * a.Hq + hk * a.G + g);
+      for (int t = 0; t < nt; ++t) {
+        const int ks = t % kPairSlots;
+        if (t >= kPairSlots && !ptx::mbar_wait(&bars->k_empty[ks], ((t / kPairSlots) - 1) & 1, abort_flag)) break;
+        unsigned char* dst = sK + ks * C::kTileBytes;
+        const int j0 = (t_begin + t) * kBN;
+        ptx::mbar_arrive_expect_tx(&bars->k_full[ks], (uint32_t)C::kTileBytes);
+        for (int db = 0; db < C::kDB; ++db)
+          ptx::tma_load_3d(dst + db * C::kKVBlock, &tmK, &bars->k_full[ks], db * 64, j0, b * a.Hkv + hk);
+        ++issued[ks];
+      }
+      // never leave the CTA with copies in flight
+      ptx::mbar_wait(&bars->q_full, 0, abort_flag);
+      for (int s = 0; s < kPairSlots; ++s)
+        if (issued[s]) ptx::mbar_wait(&bars->k_full[s], (issued[s] - 1) & 1, abort_flag);
+    } else if (lane == 1 && nt > 0) {
+      int issued[kPairSlots] = {0, 0};
+      ptx::prefetch_tmap(&tmV);
+      for (int t = 0; t < nt; ++t) {
+        const int vs = t % kPairSlots;
+        if (t >= kPairSlots && !ptx::mbar_wait(&bars->v_empty[vs], ((t / kPairSlots) - 1) & 1, abort_flag)) break;
+        unsigned char* dst = sV + vs * C::kTileBytes;
+        const int j0 = (t_begin + t) * kBN;
+        ptx::mbar_arrive_expect_tx(&bars->v_full[vs], (uint32_t)C::kTileBytes);
+        for (int db = 0; db < C::kDB; ++db)
+          ptx::tma_load_3d(dst + db * C::kKVBlock, &tmV, &bars->v_full[vs], db * 64, j0, b * a.Hkv + hk);
+        ++issued[vs];
+      }
+      for (int s = 0; s < kPairSlots; ++s)
+        if (issued[s]) ptx::mbar_wait(&bars->v_full[s], (issued[s] - 1) & 1, abort_flag);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ S issuer
+    if (lane == 0) {
+      if (nt > 0 && ptx::mbar_wait(&bars->q_full, 0, abort_flag)) {
+        constexpr uint32_t idS = ptx::idesc_bf16(kRows, kBN, false, false);
+        bool ok = true;
+        for (int t = 0; ok && t < nt; ++t) {
+          const int ks = t % kPairSlots;
+          if (!ptx::mbar_wait(&bars->k_full[ks], (t / kPairSlots) & 1, abort_flag)) break;
+          const uint32_t kaddr = ptx::smem_addr(sK + ks * C::kTileBytes);
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (t >= ntx[x]) continue;
+            // S_X(t) overwrites P_X(t - 1): wait for PV_X(t - 1)
+            if (t >= 1 && !ptx::mbar_wait(&bars->pv_done[x], (t - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t qaddr = ptx::smem_addr(sQ + x * C::kQTile);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk & 3) * 32;  // 16-element K step inside a 128-byte row
+              const uint64_t ad = ptx::sdesc_sw128(qaddr + (kk >> 2) * C::kQBlock + off, 16, 1024);
+              const uint64_t bd = ptx::sdesc_sw128(kaddr + (kk >> 2) * C::kKVBlock + off, 16, 1024);
+              ptx::mma_bf16_ss(tmem + x * kBN, ad, bd, idS, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(&bars->s_full[x]);
+          }
+          if (ok) ptx::mma_commit(&bars->k_empty[ks]);
+        }
+      }
+      ptx::mma_commit(&bars->s_done);
+      ptx::mbar_wait(&bars->s_done, 0, abort_flag);
+    }
+    __syncwarp();
+  } else if (warp == kThreads / 32 - 1) {
+    // ------------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t idO = ptx::idesc_bf16(kRows, D, false, true);
+      bool ok = true;
+      for (int t = 0; ok && t < nt; ++t) {
+        const int vs = t % kPairSlots;
+        if (!ptx::mbar_wait(&bars->v_full[vs], (t / kPairSlots) & 1, abort_flag)) break;
+        const uint32_t vaddr = ptx::smem_addr(sV + vs * C::kTileBytes);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (t >= ntx[x]) continue;
+          if (!ptx::mbar_wait(&bars->p_full[x], t & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t pcol = tmem + x * kBN;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            // keys 0..63 in columns 0..31, keys 64..127 in columns 64..95 (8 columns per 16 keys)
+            const uint32_t pa = pcol + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+            const uint64_t bd = ptx::sdesc_sw128(vaddr + kk * 16 * 128, C::kKVBlock, 1024);
+            ptx::mma_bf16_ts(tmem + C::kColO + x * kBN, pa, bd, idO, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(&bars->pv_done[x]);
+        }
+        if (ok) ptx::mma_commit(&bars->v_empty[vs]);
+      }
+      ptx::mma_commit(&bars->o_done);
+      ptx::mbar_wait(&bars->o_done, 0, abort_flag);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax rows
+    const int x = (warp - 2) >> 2;  // tile
+    const int q4 = warp & 3;        // TMEM lane quarter of this warp
+    const int r = q4 * 32 + lane;
+    const int g = r / a.NT, il = r % a.NT;
+    const int node = i0[x] + il;
+    const bool valid = (g < a.G) && (node < a.N) && (r < rows_used);
+    const int mnode = valid ? node : 0;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const uint32_t colS = tmem + lane_base + x * kBN;
+    const uint32_t colO = tmem + lane_base + C::kColO + x * kBN;
+    const int ntm = ntx[x];
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int t = 0; t < ntm; ++t) {
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->s_full[x], t & 1, abort_flag));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int j0 = (t_begin + t) * kBN;
+      const uint64_t vis_lo = key_mask(j0, a.P, a.N, mnode, s_par);
+      const uint64_t vis_hi = key_mask(j0 + 64, a.P, a.N, mnode, s_par);
+      float sv[64];
+      // row max over the tile: keys 0..63, then keys 64..127 (kept in registers)
+      ptx::tmem_ld32(colS, sv);
+      ptx::tmem_ld32(colS + 32, sv + 32);
+      ptx::tmem_wait_ld();
+      if (vis_lo != ~0ull) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (!((vis_lo >> j) & 1ull)) sv[j] = -INFINITY;
+      }
+      float tm = max64(sv, -INFINITY);
+      ptx::tmem_ld32(colS + 64, sv);
+      ptx::tmem_ld32(colS + 96, sv + 32);
+      ptx::tmem_wait_ld();
+      if (vis_hi != ~0ull) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (!((vis_hi >> j) & 1ull)) sv[j] = -INFINITY;
+      }
+      tm = max64(sv, tm);
+      const float tms = tm * a.c;
+      float alpha = 1.f;
+      bool need = false;
+      if (tms > m_run + kRescaleLog2) {
+        if (m_run != -INFINITY) {
+          alpha = ptx::ex2(m_run - tms);
+          need = true;
+        }
+        m_run = tms;
+      }
+      if (__any_sync(0xffffffffu, need)) {
+        // O_X holds PV_X(t - 1), complete (S_X(t) was issued after it); the wait returns
+        // at once and orders the TMEM reads after the MMA's writes
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->pv_done[x], (t - 1) & 1, abort_flag));
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float ov[32];
+          ptx::tmem_ld32(colO + c0, ov);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] *= alpha;
+          ptx::tmem_st32(colO + c0, ov);
+        }
+        ptx::tmem_wait_st();
+      }
+      l_run *= alpha;
+      uint32_t pw[32];
+      // P for keys 64..127 over their own S columns 64..95
+      float lsum = exp_p64(sv, a.c, m_run, pw);
+      ptx::tmem_st32u(colS + 64, pw);
+      // keys 0..63 again, then P over columns 0..31
+      ptx::tmem_ld32(colS, sv);
+      ptx::tmem_ld32(colS + 32, sv + 32);
+      ptx::tmem_wait_ld();
+      if (vis_lo != ~0ull) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (!((vis_lo >> j) & 1ull)) sv[j] = -INFINITY;
+      }
+      lsum += exp_p64(sv, a.c, m_run, pw);
+      ptx::tmem_st32u(colS, pw);
+      l_run += lsum;
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->p_full[x]);
+    }
+    // ---- epilogue: every MMA of the CTA (both tiles) is complete at o_done, so the
+    // rings may be reused for the split partials
+    bool have_o = false;
+    if (nt > 0) {
+      const bool done = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->o_done, 0, abort_flag));
+      have_o = done && ok && ntm > 0;
+      if (done) ptx::tc_fence_after();
+    }
+    const int hh = hk * a.G + g;
+    const size_t orow = (((size_t)b * a.Hq + hh) * a.N + node) * D;
+    if (a.splits == 1) {
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float ov[32];
+        if (have_o) {
+          ptx::tmem_ld32(colO + c0, ov);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] = 0.f;
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow + c0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 u;
+            u.x = ptx::cvt_bf16x2(ov[8 * k + 0] * inv, ov[8 * k + 1] * inv);
+            u.y = ptx::cvt_bf16x2(ov[8 * k + 2] * inv, ov[8 * k + 3] * inv);
+            u.z = ptx::cvt_bf16x2(ov[8 * k + 4] * inv, ov[8 * k + 5] * inv);
+            u.w = ptx::cvt_bf16x2(ov[8 * k + 6] * inv, ov[8 * k + 7] * inv);
+            dst[k] = u;
+          }
+        }
+      }
+    } else {
+      // park the unnormalised O of row R = x * 128 + r as row-major [256][D] fp32 with
+      // the 16-byte chunks XOR-swizzled by (R & 7), over the drained K and V rings, and
+      // (m, l) over the drained Q tiles
+      const int R = x * kRows + r;
+      unsigned char* part = sK;
+      float2* ml = reinterpret_cast<float2*>(sQ);
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float ov[32];
+        if (have_o) {
+          ptx::tmem_ld32(colO + c0, ov);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int chunk = c0 / 4 + k;
+          *reinterpret_cast<float4*>(part + (size_t)R * D * 4 + ((chunk ^ (R & 7)) << 4)) =
+              make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+        }
+      }
+      ml[R] = make_float2(have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
+    }
+    ptx::tc_fence_before();
+  }
+  __syncwarp();
+  if (a.splits > 1) {
+    // merge as in attn_tc_kernel, over the 256 rows of the pair
+    ptx::cluster_sync();
+    {
+      const int S = a.splits;
+      constexpr int kPRows = 2 * kRows;
+      const int R = (kPRows + S - 1) / S;
+      const int r0 = split * R, r1 = min(kPRows, r0 + R);
+      const int nrows = max(0, r1 - r0);
+      constexpr int kChunks = D / 4;
+      const uint32_t part_local = ptx::smem_addr(sK);
+      const uint32_t ml_local = ptx::smem_addr(sQ);
+      for (int item = threadIdx.x; item < nrows * kChunks; item += kThreads) {
+        const int rr = r0 + item / kChunks;
+        const int ch = item % kChunks;
+        const int xx = rr >= kRows ? 1 : 0, rt = rr - xx * kRows;
+        const int gg = rt / a.NT, ii = i0[xx] + rt % a.NT;
+        if (gg >= a.G || ii >= a.N || rt >= rows_used) continue;
+        float2 mlv[kMaxSplits];
+        float4 xv[kMaxSplits];
+        const uint32_t moff = (uint32_t)(rr * 8);
+        const uint32_t xoff = (uint32_t)(rr * D * 4 + ((ch ^ (rr & 7)) << 4));
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+          if (s2 < S) {
+            mlv[s2] = ptx::ld_cluster_f32x2(ptx::map_cluster(ml_local, s2) + moff);
+            xv[s2] = ptx::ld_cluster_f32x4(ptx::map_cluster(part_local, s2) + xoff);
+          }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxSplits; ++s2)
+          if (s2 < S) M = fmaxf(M, mlv[s2].x);
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+          if (s2 < S && mlv[s2].x != -INFINITY) {
+            const float w = ptx::ex2(mlv[s2].x - M);
+            L = fmaf(mlv[s2].y, w, L);
+            acc.x = fmaf(w, xv[s2].x, acc.x);
+            acc.y = fmaf(w, xv[s2].y, acc.y);
+            acc.z = fmaf(w, xv[s2].z, acc.z);
+            acc.w = fmaf(w, xv[s2].w, acc.w);
+          }
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const size_t o2 = (((size_t)b * a.Hq + hk * a.G + gg) * a.N + ii) * D + ch * 4;
+        uint2 u;
+        u.x = ptx::cvt_bf16x2(acc.x * inv, acc.y * inv);
+        u.y = ptx::cvt_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + o2) = u;
+      }
+    }
+    __syncwarp();
+    ptx::cluster_sync();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && bars->abort) set_dev_status(a.dev_status, TV_DEV_TIMEOUT);
+}
+
+// ------------------------------------------------------------------------------------
 // host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -575,16 +1070,19 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) 
   if (!p.tc) return p;
   p.nt = (kRows / G) / 8 * 8;
   p.mtiles = (N + p.nt - 1) / p.nt;
+  // paired tiles wherever there are two row tiles to pair (or when forced)
+  const int variant = attention_variant();
+  p.pair = variant == 2 || (variant == 0 && p.mtiles >= 2);
   p.splits = 1;  // chosen at launch from the device's cluster occupancy
   p.total = 0;   // split partials stay in the cluster's shared memory
   return p;
 }
 
-// How many clusters of `s` CTAs of attn_tc_kernel<D> can be resident at once on the
-// current device (cached per device, D and s).
-template <int D>
+// How many clusters of `s` CTAs of attn_tc_kernel<D> (kPair: attn_pair_kernel<D>) can be
+// resident at once on the current device (cached per device, kernel and s).
+template <int D, bool kPair>
 static int max_active_clusters(int s) {
-  static int cache[64][kMaxSplits + 1];
+  static int cache[64][kMaxSplits + 1];  // one table per template instance
   static bool init = false;
   if (!init) {
     for (auto& row : cache)
@@ -594,14 +1092,15 @@ static int max_active_clusters(int s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (cache[dev][s] >= 0) return cache[dev][s];
-  using C = TcCfg<D>;
+  const void* fn = kPair ? reinterpret_cast<const void*>(attn_pair_kernel<D>)
+                         : reinterpret_cast<const void*>(attn_tc_kernel<D>);
+  const int smem = kPair ? PairCfg<D>::kSmemAlloc : TcCfg<D>::kSmemAlloc;
   int n = 0;
-  if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc) ==
-      cudaSuccess) {
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(s * 64, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmemAlloc;
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)s;
@@ -609,7 +1108,7 @@ static int max_active_clusters(int s) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<D>, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
   }
   cache[dev][s] = n;
   return n;
@@ -617,7 +1116,7 @@ static int max_active_clusters(int s) {
 
 // KV splits per row tile: minimise (waves of clusters) x (KV tiles per CTA + a fixed
 // per-CTA cost for set-up and the cluster merge), counted in 64-key tiles.
-template <int D>
+template <int D, bool kPair>
 static int choose_splits(long long row_tiles, int t_all) {
   constexpr double kFixedTiles = 1.5;
   // with an SM share set for concurrent kernels, plan for that part of the device
@@ -627,7 +1126,7 @@ static int choose_splits(long long row_tiles, int t_all) {
   int best = 1;
   double best_cost = 1e300;
   for (int s = 1; s <= kMaxSplits && s <= t_all; ++s) {
-    int act = max_active_clusters<D>(s);
+    int act = max_active_clusters<D, kPair>(s);
     if (act <= 0) continue;
     if (share > 0 && share < nsm) act = std::max(1, (int)((long long)act * share / nsm));
     const long long waves = (row_tiles + act - 1) / act;
@@ -640,16 +1139,18 @@ static int choose_splits(long long row_tiles, int t_all) {
   return best;
 }
 
-template <int D>
+template <int D, bool kPair>
 static cudaError_t launch_tc_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const TcArgs& a,
                                int B, int Hkv, cudaStream_t stream) {
-  using C = TcCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+  const int smem = kPair ? PairCfg<D>::kSmemAlloc : TcCfg<D>::kSmemAlloc;
+  cudaError_t e = kPair ? cudaFuncSetAttribute(attn_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                        : cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.MT * a.splits, Hkv, B);
+  const int units = kPair ? (a.MT + 1) / 2 : a.MT;  // CTAs per (b, kv head) and split
+  cfg.gridDim = dim3(units * a.splits, Hkv, B);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemAlloc;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -658,7 +1159,8 @@ static cudaError_t launch_tc_d(const CUtensorMap& mq, const CUtensorMap& mk, con
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, mq, mk, mv, a);
+  e = kPair ? cudaLaunchKernelEx(&cfg, attn_pair_kernel<D>, mq, mk, mv, a)
+            : cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, mq, mk, mv, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -683,11 +1185,17 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* ou
   a.MT = plan.mtiles;
   a.c = scale * kLog2e;
   a.dev_status = dev_status;
-  const long long row_tiles = (long long)B * Hkv * plan.mtiles;
   const int t_all = (P + N + kBN - 1) / kBN;
-  a.splits = D == 64 ? choose_splits<64>(row_tiles, t_all) : choose_splits<128>(row_tiles, t_all);
-  if (D == 64) return launch_tc_d<64>(mq, mk, mv, a, B, Hkv, stream);
-  return launch_tc_d<128>(mq, mk, mv, a, B, Hkv, stream);
+  if (plan.pair) {
+    const long long units = (long long)B * Hkv * ((plan.mtiles + 1) / 2);
+    a.splits = D == 64 ? choose_splits<64, true>(units, t_all) : choose_splits<128, true>(units, t_all);
+    if (D == 64) return launch_tc_d<64, true>(mq, mk, mv, a, B, Hkv, stream);
+    return launch_tc_d<128, true>(mq, mk, mv, a, B, Hkv, stream);
+  }
+  const long long row_tiles = (long long)B * Hkv * plan.mtiles;
+  a.splits = D == 64 ? choose_splits<64, false>(row_tiles, t_all) : choose_splits<128, false>(row_tiles, t_all);
+  if (D == 64) return launch_tc_d<64, false>(mq, mk, mv, a, B, Hkv, stream);
+  return launch_tc_d<128, false>(mq, mk, mv, a, B, Hkv, stream);
 }
 
 }  // namespace tv

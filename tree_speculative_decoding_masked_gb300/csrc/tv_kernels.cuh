@@ -55,6 +55,8 @@ cudaError_t launch_prune(const int32_t* parent, const float* conf, int B, int N,
 // ---- SM shares set by tv_set_sm_partition (0 = the whole device)
 int sm_share_verify();
 int sm_share_attention();
+// ---- tensor-core attention kernel set by tv_set_attention_variant (0 = automatic)
+int attention_variant();
 
 // ---- selection
 size_t select_ws_bytes(int B, int d, int K, int budget);
@@ -68,6 +70,7 @@ struct AttnPlan {
   bool tc;        // tensor-core (tcgen05) kernel
   int nt;         // nodes per 128-row tile (tc)
   int mtiles;     // row tiles per (b, kv head)
+  int pair;       // one CTA per two row tiles (attn_pair_kernel)
   int splits;     // KV splits per row tile (one cluster)
   size_t total;   // workspace bytes (0: partials stay in the cluster's shared memory)
 };
