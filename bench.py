@@ -600,7 +600,9 @@ def run_ours(args):
     # the prefix and the tree block, as the kernel computes them
     fam_flops = {"attention": 4 * B * Hq * N * (P + N) * D, "verify": 0}
     dom = max(("attention", "verify"), key=lambda kk: br[kk])
-    kernel_names = {"attention": "attn_tc_kernel" if bf16 else "attn_simt_kernel", "verify": "vocab_pass_tma_kernel"}
+    attn_kernel, attn_splits = tv.tree_attention_plan(B, Hq, Hkv, D, P, N, tdt)
+    kernel_names = {"attention": ("attn_simt_kernel", "attn_tc_kernel", "attn_pair_kernel")[attn_kernel],
+                    "verify": "vocab_pass_tma_kernel"}
     roofline = roofline_entry(kernel_names[dom], fam_bytes[dom], fam_flops[dom] if bf16 else 0, br[dom] * 1e-6,
                               args.workload)
 
@@ -639,7 +641,8 @@ def run_ours(args):
                            step="select_subtree, then tree_attention || " +
                                 ("verify_sample" if sampling_mode else "verify_greedy") + " (two streams)",
                            parallelism=f"replicas x{world}",
-                           sm_partition={"verify": sm_partition[0] or n_sm, "attention": sm_partition[1] or n_sm}),
+                           sm_partition={"verify": sm_partition[0] or n_sm, "attention": sm_partition[1] or n_sm},
+                           attention_kernel=kernel_names["attention"], attention_kv_splits=attn_splits),
             "path_gbs": bytes_set / (ms_per_step * 1e-3) / 1e9,
             "breakdown_us": br,
             "commit_bytes_per_launch": commit_bytes,

@@ -99,8 +99,8 @@ TV_API tv_status tv_set_sm_partition(int verify_sms, int attention_sms);
 
 /* ------------------------------------------------------------------------------------
  * tv_set_attention_variant - which tensor-core kernel tv_tree_attention uses for bf16.
- *   0  automatic (default): paired row tiles when a (sequence, KV head) has more than
- *      one 128-row tile of query rows (G * N > 128), else one tile per CTA
+ *   0  automatic (default): the variant and KV split count that minimise a wave model
+ *      of the run time (see tv_tree_attention_plan); paired tiles need G * N > 128
  *   1  one 128-row tile per CTA
  *   2  paired row tiles: one CTA streams the KV range once for two 128-row tiles
  * Both compute the same result (up to fp32 summation order); the switch exists to
@@ -108,6 +108,16 @@ TV_API tv_status tv_set_sm_partition(int verify_sms, int attention_sms);
  * Errors: a value outside 0..2 -> TV_ERR_VALUE.
  */
 TV_API tv_status tv_set_attention_variant(int variant);
+
+/* ------------------------------------------------------------------------------------
+ * tv_set_attention_splits - KV splits of the tensor-core attention, for measurement and
+ * tuning.  0 (default): chosen per launch from the device's cluster occupancy and the
+ * KV length.  1..8: every (sequence, KV head, row tile group) is cut into that many KV
+ * ranges (at most one per 128-key tile), merged inside one thread-block cluster.
+ * Results do not depend on it beyond fp32 summation order.  Process-wide, host-side.
+ * Errors: a value outside 0..8 -> TV_ERR_VALUE.
+ */
+TV_API tv_status tv_set_attention_splits(int splits);
 
 /* ------------------------------------------------------------------------------------
  * tv_tree_prep - tree structure for the attention mask and position encoding.
@@ -169,6 +179,20 @@ TV_API tv_status tv_prune_tree(const int32_t* parent, const float* conf, int B, 
  */
 TV_API size_t tv_tree_attention_workspace_size(int B, int Hq, int Hkv, int D, int P, int N,
                                         tv_dtype dtype);
+/* tv_tree_attention_plan - the kernel and KV split count that tv_tree_attention would use
+ * for these sizes on the current device with the current settings
+ * (tv_set_attention_variant, tv_set_attention_splits, tv_set_sm_partition):
+ *   *kernel  0 CUDA-core kernel (fp32, or shapes the tensor-core kernels do not take),
+ *            1 tensor-core kernel with one 128-row tile per CTA, 2 paired row tiles
+ *   *splits  KV ranges per tile group, merged in one thread-block cluster
+ * Automatic choice: the variant and split count that minimise a wave model of the run
+ * time (waves of resident clusters x (KV tiles per CTA + fixed per-CTA and merge costs))
+ * fitted to GB300 measurements.  Queries the device's cluster occupancy (needs a
+ * current CUDA device); launches nothing.
+ * Errors: NULL outputs -> TV_ERR_NULL; bad dtype -> TV_ERR_DTYPE; sizes -> TV_ERR_SHAPE.
+ */
+TV_API tv_status tv_tree_attention_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype,
+                                        int* kernel, int* splits);
 TV_API tv_status tv_tree_attention(const void* q, const void* k_cache, const void* v_cache, void* out,
                             const int32_t* parent, int B, int Hq, int Hkv, int D, int P, int N,
                             int kv_stride_tokens, float scale, tv_dtype dtype, void* workspace,

@@ -243,3 +243,18 @@ def test_long_context_workload_sampled_one_tile_per_cta():
         _sampled_rows("long_context", 24, seed_extra=5)
     finally:
         tv.set_attention_variant(0)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 8])
+def test_forced_splits_both_variants(variant, splits):
+    # every split count merges to the same result, including more splits than a short
+    # KV range has tiles (the last CTAs of a cluster then own no keys)
+    B, Hq, Hkv, D, P, N = 2, 8, 2, 128, 600, 90
+    g = synth.rng(38 + splits)
+    par, _ = W.trees(g, B, N, 7, 100)
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, True)
+    tv.set_attention_splits(splits)
+    try:
+        _check_all(q, k, v, par, P, True)
+    finally:
+        tv.set_attention_splits(0)

@@ -21,10 +21,12 @@ from ._binding import (  # noqa: F401
     prune_tree,
     select_subtree,
     select_workspace_size,
+    set_attention_splits,
     set_attention_variant,
     set_sm_partition,
     status_string,
     tree_attention,
+    tree_attention_plan,
     tree_attention_workspace_size,
     tree_prep,
     verify_greedy,

@@ -42,9 +42,11 @@ _SIGS = {
     "tv_version": (_I, []),
     "tv_set_sm_partition": (_I, [_I, _I]),
     "tv_set_attention_variant": (_I, [_I]),
+    "tv_set_attention_splits": (_I, [_I]),
     "tv_tree_prep": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "tv_prune_tree": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "tv_tree_attention_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "tv_tree_attention_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "tv_tree_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _P]),
     "tv_verify_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "tv_verify_greedy": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
@@ -150,6 +152,11 @@ def set_attention_variant(variant: int):
     _check("tv_set_attention_variant", load_library().tv_set_attention_variant(int(variant)))
 
 
+def set_attention_splits(splits: int):
+    """KV splits of the tensor-core attention: 0 automatic, 1..8 forced (measurement)."""
+    _check("tv_set_attention_splits", load_library().tv_set_attention_splits(int(splits)))
+
+
 def tree_prep(parent: torch.Tensor, prefix_len: int, *, dev_status=None, out=None):
     """Depth, position ids, packed ancestor mask and child CSR of ``parent`` [B][N]."""
     _need_cuda(parent=parent)
@@ -190,6 +197,16 @@ def prune_tree(parent, conf, max_children: int, depth_limit: int, *, dev_status=
 def tree_attention_workspace_size(B, Hq, Hkv, D, P, N, dtype) -> int:
     code = TV_BF16 if dtype == torch.bfloat16 else TV_F32
     return int(load_library().tv_tree_attention_workspace_size(B, Hq, Hkv, D, P, N, code))
+
+
+def tree_attention_plan(B, Hq, Hkv, D, P, N, dtype):
+    """(kernel, splits) that tree_attention would launch: kernel 0 CUDA cores, 1 one
+    128-row tile per CTA, 2 paired row tiles (tensor cores)."""
+    code = TV_BF16 if dtype == torch.bfloat16 else TV_F32
+    kern, spl = ctypes.c_int(0), ctypes.c_int(0)
+    _check("tv_tree_attention_plan", load_library().tv_tree_attention_plan(
+        B, Hq, Hkv, D, P, N, code, ctypes.addressof(kern), ctypes.addressof(spl)))
+    return kern.value, spl.value
 
 
 def tree_attention(q, k_cache, v_cache, parent, prefix_len: int, *, scale: float = 0.0, out=None, workspace=None,

@@ -10,11 +10,15 @@ using namespace tv;
 static int g_sm_verify = 0, g_sm_attention = 0;
 // tensor-core attention kernel: 0 automatic, 1 one row tile per CTA, 2 paired row tiles
 static int g_attn_variant = 0;
+// KV splits per tensor-core attention CTA group: 0 automatic, else forced (capped at the
+// KV tile count and the cluster limit)
+static int g_attn_splits = 0;
 
 namespace tv {
 int sm_share_verify() { return g_sm_verify; }
 int sm_share_attention() { return g_sm_attention; }
 int attention_variant() { return g_attn_variant; }
+int attention_splits() { return g_attn_splits; }
 }  // namespace tv
 
 namespace {
@@ -68,6 +72,12 @@ tv_status tv_set_attention_variant(int variant) {
   return TV_OK;
 }
 
+tv_status tv_set_attention_splits(int splits) {
+  if (splits < 0 || splits > 8) return TV_ERR_VALUE;
+  g_attn_splits = splits;
+  return TV_OK;
+}
+
 tv_status tv_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* depth, int32_t* pos, uint32_t* anc_mask,
                        int32_t* child_off, int32_t* child_idx, int32_t* dev_status, tv_stream_t stream) {
   if (!parent) return TV_ERR_NULL;
@@ -116,6 +126,23 @@ tv_status tv_tree_attention(const void* q, const void* k_cache, const void* v_ca
   if ((long long)B * Hq * N / 4 + 1 > 0x7fffffffLL) return TV_ERR_SHAPE;
   return cuda_status(launch_attn_simt(q, k_cache, v_cache, out, parent, B, Hq, Hkv, D, P, N, kv_stride_tokens, scale,
                                       dtype, dev_status, st(stream)));
+}
+
+tv_status tv_tree_attention_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype, int* kernel,
+                                 int* splits) {
+  if (!kernel || !splits) return TV_ERR_NULL;
+  if (!valid_dtype(dtype)) return TV_ERR_DTYPE;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || N < 1 || N > kMaxNodes || P < 0) return TV_ERR_SHAPE;
+  AttnPlan p = attn_plan(B, Hq, Hkv, D, P, N, dtype);
+  if (!p.tc) {
+    *kernel = 0;
+    *splits = 1;
+    return TV_OK;
+  }
+  int pair = 0;
+  attn_tc_choice(B, Hkv, D, P, N, p, &pair, splits);
+  *kernel = pair ? 2 : 1;
+  return TV_OK;
 }
 
 size_t tv_verify_workspace_size(int B, int N, int V, tv_dtype, int sampling) {

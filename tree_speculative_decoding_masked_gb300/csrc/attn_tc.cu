@@ -1070,10 +1070,8 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) 
   if (!p.tc) return p;
   p.nt = (kRows / G) / 8 * 8;
   p.mtiles = (N + p.nt - 1) / p.nt;
-  // paired tiles wherever there are two row tiles to pair (or when forced)
-  const int variant = attention_variant();
-  p.pair = variant == 2 || (variant == 0 && p.mtiles >= 2);
-  p.splits = 1;  // chosen at launch from the device's cluster occupancy
+  p.pair = 0;    // kernel variant and KV splits are chosen at launch (choose_plan)
+  p.splits = 1;
   p.total = 0;   // split partials stay in the cluster's shared memory
   return p;
 }
@@ -1114,29 +1112,51 @@ static int max_active_clusters(int s) {
   return n;
 }
 
-// KV splits per row tile: minimise (waves of clusters) x (KV tiles per CTA + a fixed
-// per-CTA cost for set-up and the cluster merge), counted in 64-key tiles.
+// Launch plan: kernel variant and KV splits minimising a wave model of the run time,
+// (waves of clusters) x (KV tiles per CTA + a fixed per-CTA cost + the cluster merge when
+// split) x (tile cost), in units of one 128-row x 128-key tile of attn_tc_kernel.  The
+// constants are fitted to GB300 measurements over the qwen3 layer, sampling,
+// long-context and budget-sweep shapes (every split count of both kernels): a CTA's
+// set-up, pipeline fill and epilogue cost about 6 tiles, a cluster merge about 4.4, and a
+// tile pair of attn_pair_kernel about 1.85 single tiles.
+constexpr double kFixedTiles = 6.0;
+constexpr double kMergeTiles = 4.4;
+constexpr double kPairTileCost = 1.85;
+
 template <int D, bool kPair>
-static int choose_splits(long long row_tiles, int t_all) {
-  constexpr double kFixedTiles = 1.5;
-  // with an SM share set for concurrent kernels, plan for that part of the device
-  const int share = sm_share_attention();
+static double plan_cost(long long units, int t_all, int s) {
+  const int share = sm_share_attention();  // an SM share set for concurrent kernels
   int nsm = 152, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  int best = 1;
+  int act = max_active_clusters<D, kPair>(s);
+  if (act <= 0) return 1e300;
+  if (share > 0 && share < nsm) act = std::max(1, (int)((long long)act * share / nsm));
+  const long long waves = (units + act - 1) / act;
+  return (double)waves * ((t_all + s - 1) / s + kFixedTiles + (s > 1 ? kMergeTiles : 0.0)) *
+         (kPair ? kPairTileCost : 1.0);
+}
+
+template <int D>
+static void choose_plan(int B, int Hkv, int mtiles, int t_all, bool* pair, int* splits) {
+  const int variant = attention_variant();
+  const int forced = attention_splits();
   double best_cost = 1e300;
-  for (int s = 1; s <= kMaxSplits && s <= t_all; ++s) {
-    int act = max_active_clusters<D, kPair>(s);
-    if (act <= 0) continue;
-    if (share > 0 && share < nsm) act = std::max(1, (int)((long long)act * share / nsm));
-    const long long waves = (row_tiles + act - 1) / act;
-    const double cost = (double)waves * ((t_all + s - 1) / s + kFixedTiles);
-    if (cost < best_cost * 0.98) {
-      best_cost = cost;
-      best = s;
+  *pair = false;
+  *splits = 1;
+  for (int v = 1; v <= 2; ++v) {
+    if (variant != 0 && v != variant) continue;
+    if (variant == 0 && v == 2 && mtiles < 2) continue;  // nothing to pair
+    const long long units = (long long)B * Hkv * (v == 2 ? (mtiles + 1) / 2 : mtiles);
+    for (int s = 1; s <= kMaxSplits && s <= t_all; ++s) {
+      if (forced > 0 && s != std::min(forced, t_all)) continue;
+      const double c = v == 2 ? plan_cost<D, true>(units, t_all, s) : plan_cost<D, false>(units, t_all, s);
+      if (c < best_cost * 0.98) {  // prefer fewer splits and the single-tile kernel on near ties
+        best_cost = c;
+        *pair = v == 2;
+        *splits = s;
+      }
     }
   }
-  return best;
 }
 
 template <int D, bool kPair>
@@ -1165,6 +1185,16 @@ static cudaError_t launch_tc_d(const CUtensorMap& mq, const CUtensorMap& mk, con
   return cudaGetLastError();
 }
 
+void attn_tc_choice(int B, int Hkv, int D, int P, int N, const AttnPlan& plan, int* pair, int* splits) {
+  const int t_all = (P + N + kBN - 1) / kBN;
+  bool pr = false;
+  if (D == 64)
+    choose_plan<64>(B, Hkv, plan.mtiles, t_all, &pr, splits);
+  else
+    choose_plan<128>(B, Hkv, plan.mtiles, t_all, &pr, splits);
+  *pair = pr ? 1 : 0;
+}
+
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* out, const int32_t* parent, int B,
                            int Hq, int Hkv, int D, int P, int N, int S, float scale, const AttnPlan& plan, char* ws,
                            int32_t* dev_status, cudaStream_t stream) {
@@ -1186,16 +1216,15 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* ou
   a.c = scale * kLog2e;
   a.dev_status = dev_status;
   const int t_all = (P + N + kBN - 1) / kBN;
-  if (plan.pair) {
-    const long long units = (long long)B * Hkv * ((plan.mtiles + 1) / 2);
-    a.splits = D == 64 ? choose_splits<64, true>(units, t_all) : choose_splits<128, true>(units, t_all);
-    if (D == 64) return launch_tc_d<64, true>(mq, mk, mv, a, B, Hkv, stream);
-    return launch_tc_d<128, true>(mq, mk, mv, a, B, Hkv, stream);
-  }
-  const long long row_tiles = (long long)B * Hkv * plan.mtiles;
-  a.splits = D == 64 ? choose_splits<64, false>(row_tiles, t_all) : choose_splits<128, false>(row_tiles, t_all);
-  if (D == 64) return launch_tc_d<64, false>(mq, mk, mv, a, B, Hkv, stream);
-  return launch_tc_d<128, false>(mq, mk, mv, a, B, Hkv, stream);
+  bool pair = false;
+  if (D == 64)
+    choose_plan<64>(B, Hkv, plan.mtiles, t_all, &pair, &a.splits);
+  else
+    choose_plan<128>(B, Hkv, plan.mtiles, t_all, &pair, &a.splits);
+  if (pair) return D == 64 ? launch_tc_d<64, true>(mq, mk, mv, a, B, Hkv, stream)
+                           : launch_tc_d<128, true>(mq, mk, mv, a, B, Hkv, stream);
+  return D == 64 ? launch_tc_d<64, false>(mq, mk, mv, a, B, Hkv, stream)
+                 : launch_tc_d<128, false>(mq, mk, mv, a, B, Hkv, stream);
 }
 
 }  // namespace tv

@@ -57,6 +57,8 @@ int sm_share_verify();
 int sm_share_attention();
 // ---- tensor-core attention kernel set by tv_set_attention_variant (0 = automatic)
 int attention_variant();
+// ---- forced KV split count set by tv_set_attention_splits (0 = automatic)
+int attention_splits();
 
 // ---- selection
 size_t select_ws_bytes(int B, int d, int K, int budget);
@@ -70,14 +72,16 @@ struct AttnPlan {
   bool tc;        // tensor-core (tcgen05) kernel
   int nt;         // nodes per 128-row tile (tc)
   int mtiles;     // row tiles per (b, kv head)
-  int pair;       // one CTA per two row tiles (attn_pair_kernel)
-  int splits;     // KV splits per row tile (one cluster)
+  int pair;       // unused at plan time: the variant is chosen at launch
+  int splits;     // unused at plan time: the KV splits are chosen at launch
   size_t total;   // workspace bytes (0: partials stay in the cluster's shared memory)
 };
 AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype);
 cudaError_t launch_attn_simt(const void* q, const void* k, const void* v, void* out, const int32_t* parent,
                              int B, int Hq, int Hkv, int D, int P, int N, int S, float scale, tv_dtype dtype,
                              int32_t* dev_status, cudaStream_t stream);
+// kernel variant (1 = attn_pair_kernel) and KV splits the next launch would use
+void attn_tc_choice(int B, int Hkv, int D, int P, int N, const AttnPlan& plan, int* pair, int* splits);
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* out, const int32_t* parent,
                            int B, int Hq, int Hkv, int D, int P, int N, int S, float scale, const AttnPlan& plan,
                            char* ws, int32_t* dev_status, cudaStream_t stream);
