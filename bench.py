@@ -476,17 +476,21 @@ def run_ours(args):
         tv.commit_accepted_kv(s["k"], s["v"], ver_out["accepted_nodes"], ver_out["accept_len"], P, dev_status=status)
 
     side = torch.cuda.Stream(device=dev)
+    order = {"verify_on_main": False}
 
     def step(s):
         # selection feeds both; tree attention and the vocab pass are independent of each
-        # other and run concurrently (fork after selection, join before the next step)
+        # other and run concurrently (fork after selection, join before the next step).
+        # The kernel on selection's own stream starts its CTAs while selection finishes
+        # (programmatic dependent launch); the other one waits for an event.
+        first, second = (k_verify, k_attn) if order["verify_on_main"] else (k_attn, k_verify)
         k_select(s)
         fork = torch.cuda.Event()
         fork.record()
         side.wait_event(fork)
-        k_attn(s)
+        first(s)
         with torch.cuda.stream(side):
-            k_verify(s)
+            second(s)
             join = torch.cuda.Event()
             join.record()
         torch.cuda.current_stream().wait_event(join)
@@ -511,10 +515,13 @@ def run_ours(args):
     # fastest step (the whole device for both, or disjoint parts so both grids are
     # resident together)
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    candidates = [(0, 0)] + [(v, n_sm - v) for v in (n_sm // 4, n_sm // 3, n_sm // 2, 2 * n_sm // 3)]
+    candidates = [(part, vm) for part in [(0, 0)] + [(v, n_sm - v) for v in
+                                                      (n_sm // 4, n_sm // 3, n_sm // 2, 2 * n_sm // 3)]
+                  for vm in (False, True)]
     trial = {}
     for cand in candidates:
-        tv.set_sm_partition(*cand)
+        tv.set_sm_partition(*cand[0])
+        order["verify_on_main"] = cand[1]
         with torch.cuda.stream(stream):
             g_try = capture(lambda: [step(s) for s in sets])
             for _ in range(3):
@@ -529,8 +536,9 @@ def run_ours(args):
         torch.cuda.synchronize()
         trial[cand] = ev0.elapsed_time(ev1)
         del g_try
-    sm_partition = min(trial, key=trial.get)
+    sm_partition, verify_on_main = min(trial, key=trial.get)
     tv.set_sm_partition(*sm_partition)
+    order["verify_on_main"] = verify_on_main
 
     with torch.cuda.stream(stream):
         g_all = capture(lambda: [step(s) for s in sets])          # one step per input set
@@ -639,7 +647,9 @@ def run_ours(args):
                            l2=f"inputs rotate over {n_sets} device copies, {n_sets * bytes_set / 1e6:.0f} MB "
                               f"> 2 x L2 ({l2 / 1e6:.0f} MB)",
                            step="select_subtree, then tree_attention || " +
-                                ("verify_sample" if sampling_mode else "verify_greedy") + " (two streams)",
+                                ("verify_sample" if sampling_mode else "verify_greedy") +
+                                " (two streams; " + ("verify" if verify_on_main else "attention") +
+                                " on selection's stream with programmatic dependent launch)",
                            parallelism=f"replicas x{world}",
                            sm_partition={"verify": sm_partition[0] or n_sm, "attention": sm_partition[1] or n_sm},
                            attention_kernel=kernel_names["attention"], attention_kv_splits=attn_splits),

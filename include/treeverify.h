@@ -32,6 +32,13 @@
  *     root included.  Row u of a logits block is the target (or draft) distribution of
  *     the token that follows node u, so draft node c is judged with row parent[c].
  *   - Logits / activations are row-major and contiguous.  bf16 is IEEE bfloat16.
+ *   - The kernels of tv_select_subtree*, tv_tree_attention (tensor-core path) and
+ *     tv_verify_* are launched with programmatic stream serialization: their CTAs may
+ *     become resident while the previous kernel of the stream is still finishing, and
+ *     each waits (griddepcontrol.wait) for that kernel to complete, with its memory
+ *     visible, before it reads or writes any global memory.  Stream order and results
+ *     are those of an ordinary launch; only the launch latency between dependent
+ *     kernels is hidden (and the selection kernel lets its successor start early).
  *
  * Passages restated (the pages' titles):
  *   TAPS (Target-Aware Prefix-tree Selection for diffusion-drafted speculative

@@ -148,6 +148,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, TcArgs a) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();  // before any global read or write
   using C = TcCfg<D>;
   extern __shared__ unsigned char smem_raw[];
   __shared__ float s_xmax[2][2][kRows];  // [tile parity][half][row] partial row maxima
@@ -612,6 +614,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, TcArgs a) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();  // before any global read or write
   using C = PairCfg<D>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t mis = ptx::smem_addr(smem_raw) & 1023u;
@@ -1177,10 +1181,8 @@ static cudaError_t launch_tc_d(const CUtensorMap& mq, const CUtensorMap& mk, con
   attr[0].val.clusterDim.x = (unsigned)a.splits;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = kPair ? cudaLaunchKernelEx(&cfg, attn_pair_kernel<D>, mq, mk, mv, a)
-            : cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, mq, mk, mv, a);
+  e = kPair ? launch_pdl(attn_pair_kernel<D>, cfg.gridDim, cfg.blockDim, smem, stream, attr, 1, mq, mk, mv, a)
+            : launch_pdl(attn_tc_kernel<D>, cfg.gridDim, cfg.blockDim, smem, stream, attr, 1, mq, mk, mv, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -92,6 +92,8 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 
 template <typename T>
 __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   __shared__ int s_par[kMaxNodes];
   __shared__ int s_tok[kMaxNodes];
   __shared__ int s_kids[kMaxNodes];
@@ -399,10 +401,9 @@ cudaError_t launch_sample_walk(const void* target, const void* draft, const int3
   attr[0].val.clusterDim.x = csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = dtype == TV_BF16 ? cudaLaunchKernelEx(&cfg, sample_walk_kernel<uint16_t>, a)
-                                   : cudaLaunchKernelEx(&cfg, sample_walk_kernel<float>, a);
+  cudaError_t e = dtype == TV_BF16
+                      ? launch_pdl(sample_walk_kernel<uint16_t>, cfg.gridDim, cfg.blockDim, 0, stream, attr, 1, a)
+                      : launch_pdl(sample_walk_kernel<float>, cfg.gridDim, cfg.blockDim, 0, stream, attr, 1, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

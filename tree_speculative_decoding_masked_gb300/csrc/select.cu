@@ -26,6 +26,7 @@
 // warp (first-child / next-sibling form of the candidate tree, heap-ordered in the
 // selection order).
 #include "tv_kernels.cuh"
+#include "tv_ptx.cuh"
 
 namespace tv {
 
@@ -276,21 +277,24 @@ __device__ float coarse_bound(const int* hist, int M, int* wsum, float* s_tau) {
 
 // A second lower bound on the M-th best score, for large budgets, where the one-deviation
 // family is sparse next to the whole candidate tree: count every candidate by its
-// quantised log score.  Edge weight w = ceil(-16 log2 m + slack) >= -16 log2 m (16 bins
+// quantised log score.  (On a 16 x 4 pool at budget 64 it leaves 75 candidates instead
+// of 238, but its 16 barrier-separated levels cost more than the expansion and ranking
+// they save.)  Edge weight w = ceil(-16 log2 m + slack) >= -16 log2 m (16 bins
 // per octave, 32 octaves; m = 0 or weights past the range are left out), so a path whose
 // weights sum to <= v has an exact product >= 2^(-v/16); its fp32 product is within 16
 // roundings of that, which the final scale covers.  H_l[v] = number of depth-l paths of
 // weight v, built level by level (H_{l+1}[v] = sum over ranks of H_l[v - w]; counts
-// saturate at 2^40).  The bound is 2^(-v*/16) (slightly shrunk) for the smallest v* whose
+// saturate at 2^30).  The bound is 2^(-v*/16) (slightly shrunk) for the smallest v* whose
 // paths of weight <= v* number at least M; 0 if the range holds fewer.
 constexpr int kLogBins = kSelThreads;  // one weight bin per thread
 constexpr int kCountMinRows = 128;     // smaller budgets use the one-deviation bound alone
+constexpr unsigned kCountSat = 1u << 30;  // saturation of the per-bin path counts
 
 __device__ float counting_bound(const SelSmem& sm, int d, int K, int M, unsigned long long* red, float* s_tau) {
   const int t = threadIdx.x;
   const int Kp = (K + 7) & ~7;                                            // ranks padded to whole groups of 8
-  int* wts = sm.idx;                                                      // [d][Kp] weights
-  unsigned long long* H = reinterpret_cast<unsigned long long*>(sm.pos);  // [2][kLogBins]
+  int* wts = sm.idx;                                  // [d][Kp] weights
+  unsigned* H = reinterpret_cast<unsigned*>(sm.pos);  // [2][kLogBins] path counts, saturated
   for (int i = t; i < d * Kp; i += blockDim.x) {
     const int l = i / Kp, r = i - l * Kp;
     const float m = r < K ? sm.marg[l * K + r] : 0.f;
@@ -301,26 +305,26 @@ __device__ float counting_bound(const SelSmem& sm, int d, int K, int M, unsigned
     }
     wts[i] = w;
   }
-  H[t] = t == 0 ? 1ull : 0ull;
+  H[t] = t == 0 ? 1u : 0u;
   __syncthreads();
   unsigned long long acc = 0;
   for (int l = 0; l < d; ++l) {
-    const unsigned long long* cur = H + (l & 1) * kLogBins;
+    const unsigned* cur = H + (l & 1) * kLogBins;
     const int* wl = wts + l * Kp;
     unsigned long long h = 0;
     // weights grow with the rank: groups of 8 independent gathers until the first
-    // weight past the range (the same for every thread)
-    for (int r0 = 0; r0 < Kp && wl[r0] < kLogBins; r0 += 8) {
+    // weight past this thread's bin (no heavier edge can reach it)
+    for (int r0 = 0; r0 < Kp && wl[r0] <= t; r0 += 8) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const int w = wl[r0 + q];
-        const unsigned long long x = cur[max(t - w, 0)];
-        h += w <= t ? x : 0ull;
+        const unsigned x = cur[max(t - w, 0)];
+        h += w <= t ? x : 0u;
       }
     }
-    h = min(h, 1ull << 40);
-    H[((l + 1) & 1) * kLogBins + t] = h;
-    acc += h;
+    const unsigned hs = (unsigned)min(h, (unsigned long long)kCountSat);
+    H[((l + 1) & 1) * kLogBins + t] = hs;
+    acc += hs;
     __syncthreads();
   }
   unsigned long long tot;
@@ -805,6 +809,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
   __shared__ int s_bad, s_nout, s_count;
   __shared__ ExpandCounters s_ec;
   const int b = blockIdx.x, tid = threadIdx.x;
+  ptx::griddep_launch_dependents();  // the verification kernels may start their set-up
+  ptx::griddep_wait();
   const int M = budget - 1;
   SelSmem sm;
   sm.k0 = reinterpret_cast<uint64_t*>(smem);
@@ -886,8 +892,9 @@ cudaError_t launch_select(const float* marg, const int32_t* ptok, int B, int d, 
   const size_t smem = select_smem_bytes(d, K, budget);
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  select_kernel<<<B, kSelThreads, smem, stream>>>(marg, ptok, d, K, budget, root_token, parent, tokens, depth, score,
-                                                   n_nodes, dev_status, cost_base, cost_per_row);
+  e = launch_pdl(select_kernel, dim3(B), dim3(kSelThreads), smem, stream, nullptr, 0, marg, ptok, d, K, budget,
+                 root_token, parent, tokens, depth, score, n_nodes, dev_status, cost_base, cost_per_row);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -112,4 +112,27 @@ static __device__ unsigned long long block_scan_u64(unsigned long long v, unsign
   return excl;
 }
 
+// Launch with programmatic stream serialization: the kernel's CTAs may start while the
+// previous kernel of the stream is finishing (after it calls griddep_launch_dependents)
+// and wait in griddep_wait() for its completion, which hides the launch latency between
+// dependent kernels.  Optional extra attributes (e.g. a cluster shape) come first.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              const cudaLaunchAttribute* extra, int n_extra, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[4];
+  int n = 0;
+  for (int i = 0; i < n_extra && n < 3; ++i) attr[n++] = extra[i];
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  cfg.attrs = attr;
+  cfg.numAttrs = (unsigned)n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace tv

@@ -64,6 +64,18 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v
   return old;
 }
 
+// ---- programmatic dependent launch
+// Let the next kernel of the stream (if launched with programmatic stream serialization)
+// start its CTAs now; they block in griddep_wait() until this grid has completed.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until every grid this one depends on has completed and its memory operations are
+// visible (returns at once when the kernel was launched without a programmatic
+// dependency).  Every kernel launched with launch_pdl calls it before its first global
+// read or write.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- TMA
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int x, int y, int z) {
   asm volatile(

@@ -388,6 +388,8 @@ __global__ void __launch_bounds__(512, 1) vocab_pass_kernel(VocabArgs a) {
   __shared__ int s_finish[kMaxFinish];
   __shared__ int s_nfinish;
   const int tid = threadIdx.x;
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const long long cta = blockIdx.x;
   const long long e0 = cta * a.chunk;
   const long long e1 = min(a.E, e0 + a.chunk);
@@ -595,6 +597,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
   static_assert(kVpt * 16 * kTmaThreads == kPieceBytes, "a piece is kVpt vectors per thread");
   static_assert(kMaxNodes <= 2 * kTmaThreads + 1, "each thread owns at most two children");
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const long long cta = blockIdx.x;
   const long long e0 = cta * a.chunk;
   const long long e1 = min(a.E, e0 + a.chunk);
@@ -897,8 +901,7 @@ template <typename T, bool kVec>
 static cudaError_t launch_vocab_t(VocabArgs a, cudaStream_t stream) {
   plan_grid(a, resident_ctas<T, kVec>());
   const long long G = (a.E + a.chunk - 1) / a.chunk;
-  vocab_pass_kernel<T, kVec><<<(unsigned)G, kVocabThreads, 0, stream>>>(a);
-  return cudaSuccess;
+  return launch_pdl(vocab_pass_kernel<T, kVec>, dim3((unsigned)G), dim3(kVocabThreads), 0, stream, nullptr, 0, a);
 }
 
 template <typename T, int kArrays>
@@ -916,8 +919,8 @@ static cudaError_t launch_vocab_tma(VocabArgs a, cudaStream_t stream) {
   if (sm_share_verify() > 0) sms = std::min(sms, sm_share_verify());
   plan_grid(a, sms);  // one CTA per SM: the ring takes most of the shared memory
   const long long G = (a.E + a.chunk - 1) / a.chunk;
-  vocab_pass_tma_kernel<T, kArrays><<<(unsigned)G, kTmaThreads, kRingBytes, stream>>>(a);
-  return cudaSuccess;
+  return launch_pdl(vocab_pass_tma_kernel<T, kArrays>, dim3((unsigned)G), dim3(kTmaThreads), kRingBytes, stream,
+                    nullptr, 0, a);
 }
 
 template <typename T>
