@@ -172,3 +172,16 @@ def test_adaptive_budget_rejects_bad_costs():
     for cost in ((1.0, 0.0), (-1.0, 1.0), (float("inf"), 1.0)):
         with pytest.raises(tv.TreeVerifyError):
             tv.select_subtree(m, p, 10, r, cost=cost)
+
+
+@pytest.mark.parametrize("k,budget", [(2, 100), (3, 120), (4, 127), (32, 60)])
+def test_uniform_pools_small_budgets(k, budget):
+    # with all paths of a depth tied, the one-deviation bound of a small budget lies far
+    # below the M-th best score: for K = 2, 3 the kept set outgrows the expansion buffer
+    # and the bound-raising restarts take over; for K = 4, 32 the ranking cuts a large
+    # tied set down to the coarse class that holds the M-th score
+    d = 16
+    marg = np.full((2, d, k), np.float32(1.0 / k), dtype=np.float32)
+    ptok = np.tile(np.arange(d * k, dtype=np.int32).reshape(1, d, k), (2, 1, 1))
+    roots = np.array([3, 4], dtype=np.int32)
+    _check_select(marg, ptok, budget, roots, _gpu_select(marg, ptok, budget, roots))

@@ -607,19 +607,39 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, ExpandCo
   const int take = min(n, M);
   // 3. order: the output position of entry e is 1 + its rank in the selection order
   if (n <= kRankDirect) {
-    // L lanes per entry (a power of two, L * n <= blockDim): a branch-free count on the
+    // With many more entries than places, rank only those at or above the coarse score
+    // class where the count from the top reaches `take` (one histogram): at least `take`
+    // entries lie above that class edge, so nothing below it is placed, and an entry's
+    // rank among the listed ones is its rank among all.
+    int nr = n;
+    const int* list = nullptr;
+    if (n > 2 * take && n > 64) {
+      int* lst = reinterpret_cast<int*>(sm.k1 + (kSelCap - kRankDirect / 2));  // past every entry
+      hist[t] = 0;
+      if (t == 0) bcast[0] = 0;
+      __syncthreads();
+      if (t < n) atomicAdd(&hist[score_class(k0_score(sm.k0[t]))], 1);
+      __syncthreads();
+      const float edge = coarse_bound(hist, take, bcast + 2, s_tau);
+      if (t < n && k0_score(sm.k0[t]) >= edge) lst[atomicAdd(&bcast[0], 1)] = t;
+      __syncthreads();
+      nr = bcast[0];
+      list = lst;
+    }
+    // L lanes per entry (a power of two, L * nr <= blockDim): a branch-free count on the
     // (score, depth) word; exact ties are resolved on the rank path only when they occur
     int L = 1;
-    while (L < 32 && 2 * L * n <= (int)blockDim.x) L <<= 1;
-    const int e = t / L, sub = t & (L - 1);
-    const bool own = e < n;
+    while (L < 32 && 2 * L * nr <= (int)blockDim.x) L <<= 1;
+    const int i_own = t / L, sub = t & (L - 1);
+    const bool own = i_own < nr;
+    const int e = own ? (list ? list[i_own] : i_own) : 0;
     const uint64_t a0 = own ? sm.k0[e] : 0ull;
     int less = 0, eq = 0;
     if (own) {
       int j = sub;
 #pragma unroll 4
-      for (; j < n; j += L) {
-        const uint64_t c = sm.k0[j];
+      for (; j < nr; j += L) {
+        const uint64_t c = sm.k0[list ? list[j] : j];
         less += c < a0;
         eq += c == a0;
       }
@@ -631,8 +651,10 @@ __device__ int select_threshold(const SelSmem& sm, int d, int K, int M, ExpandCo
     int tied_before = 0;
     if (own && eq > 1) {
       const uint64_t a1 = sm.k1[e], a2 = sm.k2[e];
-      for (int q = sub; q < n; q += L)
+      for (int q0 = sub; q0 < nr; q0 += L) {
+        const int q = list ? list[q0] : q0;
         if (sm.k0[q] == a0 && key_less(a0, sm.k1[q], sm.k2[q], a0, a1, a2)) ++tied_before;
+      }
     }
     if (__any_sync(0xffffffffu, tied_before != 0))
       for (int o = 1; o < L; o <<= 1) tied_before += __shfl_xor_sync(0xffffffffu, tied_before, o);
