@@ -515,9 +515,18 @@ def run_ours(args):
     # fastest step (the whole device for both, or disjoint parts so both grids are
     # resident together)
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    candidates = [(part, vm) for part in [(0, 0)] + [(v, n_sm - v) for v in
-                                                      (n_sm // 4, n_sm // 3, n_sm // 2, 2 * n_sm // 3)]
-                  for vm in (False, True)]
+    parts = [(0, 0)] + [(v, n_sm - v) for v in (n_sm // 4, n_sm // 3, n_sm // 2, 2 * n_sm // 3)]
+    if bf16:
+        # when the whole-device attention grid leaves SMs free, give exactly those to verify
+        tv.set_sm_partition(0, 0)
+        kern, spl = tv.tree_attention_plan(B, Hq, Hkv, D, P, N, tdt)
+        G = Hq // Hkv
+        nt = (128 // G) // 8 * 8
+        mtiles = -(-N // nt)
+        ctas = B * Hkv * (-(-mtiles // 2) if kern == 2 else mtiles) * spl
+        if kern and ctas < n_sm:
+            parts.append((n_sm - ctas, ctas))
+    candidates = [(part, vm) for part in parts for vm in (False, True)]
     trial = {}
     for cand in candidates:
         tv.set_sm_partition(*cand[0])

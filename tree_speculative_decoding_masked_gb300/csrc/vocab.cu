@@ -283,23 +283,38 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) 
   const bool staged = nstage <= kStage;
   if (tid == 0) s_bad = 0;
   __syncthreads();
-  // one round trip: tree, drafted-token logits and (if they fit) every partial
-  for (int c = tid; c < N; c += blockDim.x) {
-    const int p = a.parent[r0 + c];
-    const int t = a.tokens[r0 + c];
-    sm.par[c] = p;
-    sm.tok[c] = t;
-    sm.xc[c] = __ldcg(a.xc + r0 + c);
-    if (a.sampling) sm.yc[c] = __ldcg(a.yc + r0 + c);
-    else sm.match[c] = 0x7fffffff;
-    const bool ok = (c == 0) ? (p == -1) : (p >= 0 && p < c);
-    if (!ok) atomicOr(&s_bad, TV_DEV_BAD_TREE);
-    if (c > 0 && (t < 0 || t >= V)) atomicOr(&s_bad, TV_DEV_BAD_TOKEN);
+  // one round trip: tree, drafted-token logits and (if they fit) every target partial,
+  // all loads of a thread issued before any of them is used
+  const VocabPartial* src0 = a.part + r0 * a.mc;
+  for (int base = 0; base < max(N, staged ? nstage : 0); base += blockDim.x) {
+    const int c = base + tid;
+    const bool tree_item = c < N, stage_item = staged && c < nstage;
+    int p = 0, t = 0;
+    float x = 0.f, y = 0.f;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tree_item) {
+      p = a.parent[r0 + c];
+      t = a.tokens[r0 + c];
+      x = __ldcg(a.xc + r0 + c);
+      if (a.sampling) y = __ldcg(a.yc + r0 + c);
+    }
+    if (stage_item) v = __ldcg(reinterpret_cast<const float4*>(src0 + c));
+    if (tree_item) {
+      sm.par[c] = p;
+      sm.tok[c] = t;
+      sm.xc[c] = x;
+      if (a.sampling) sm.yc[c] = y;
+      else sm.match[c] = 0x7fffffff;
+      const bool ok = (c == 0) ? (p == -1) : (p >= 0 && p < c);
+      if (!ok) atomicOr(&s_bad, TV_DEV_BAD_TREE);
+      if (c > 0 && (t < 0 || t >= V)) atomicOr(&s_bad, TV_DEV_BAD_TOKEN);
+    }
+    if (stage_item) sm.stage[c] = v;
   }
   const VocabPartial none{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
   for (int pass = 0; pass < (a.sampling ? 2 : 1); ++pass) {
     const VocabPartial* src = (pass == 0 ? a.part : a.part_q) + r0 * a.mc;
-    if (staged)
+    if (staged && pass == 1)
       for (int i = tid; i < nstage; i += blockDim.x) sm.stage[i] = __ldcg(reinterpret_cast<const float4*>(src + i));
     __syncthreads();
     for (int u = tid; u < N; u += blockDim.x) {
