@@ -79,6 +79,13 @@ __device__ __forceinline__ void unpack16<float>(const uint4& u, float* out) {
   out[3] = __uint_as_float(u.w);
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float vmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Running state of one thread over its share of a row.
 struct RowAcc {
   float av;  // raw max
@@ -547,13 +554,21 @@ struct StreamAcc {
 #pragma unroll
     for (int v = 0; v < kV; ++v) {
       unpack16<T>(u[v], x + v * kN);
-      bm[v] = x[v * kN];
+      // vector maximum with three-input max instructions
+      float m = x[v * kN];
+      int k = 1;
 #pragma unroll
-      for (int k = 1; k < kN; ++k) bm[v] = fmaxf(bm[v], x[v * kN + k]);
+      for (; k + 1 < kN; k += 2) m = vmax3(m, x[v * kN + k], x[v * kN + k + 1]);
+      if (k < kN) m = fmaxf(m, x[v * kN + k]);
+      bm[v] = m;
     }
     float bv = bm[0];
+    {
+      int v = 1;
 #pragma unroll
-    for (int v = 1; v < kV; ++v) bv = fmaxf(bv, bm[v]);
+      for (; v + 1 < kV; v += 2) bv = vmax3(bv, bm[v], bm[v + 1]);
+      if (v < kV) bv = fmaxf(bv, bm[v]);
+    }
     if (bv == -INFINITY) return;  // all -inf: nothing to add
     if (bv > av) {                // rare: keep the first vector that holds the new max
       bool found = false;
