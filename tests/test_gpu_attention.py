@@ -258,3 +258,13 @@ def test_forced_splits_both_variants(variant, splits):
         _check_all(q, k, v, par, P, True)
     finally:
         tv.set_attention_splits(0)
+
+
+def test_fp32_many_rows_four_rows_per_warp():
+    # more than 4096 query rows: the CUDA-core kernel gives each warp four rows (small
+    # problems get one row per warp); fp32 within 1e-4
+    B, Hq, Hkv, D, P, N = 2, 32, 8, 64, 100, 80
+    g = synth.rng(39)
+    par, _ = W.trees(g, B, N, 6, 100)
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, False)
+    _check_all(q, k, v, par, P, False)

@@ -31,13 +31,14 @@ __device__ __forceinline__ void stx(T* p, size_t i, float v) {
 // Keys are walked in tiles of 32: the CTA stages the tile's K and V rows in shared memory
 // (K rows padded by one word so that 32 lanes reading 32 different rows hit 32 banks),
 // then every warp updates its rows: lane j scores key j of the tile, the warp keeps an
-// online softmax and accumulates p_j v_j with lanes split over D.
+// online softmax and accumulates p_j v_j with lanes split over D.  A warp owns
+// kRowsPerWarp rows: 4 where there are many rows (fewer K/V tile loads per row), 1 for
+// small problems, which are latency-bound and need the CTAs spread over the device.
 constexpr int kSimtWarpsT = 8;
-constexpr int kRowsPerWarp = 4;
-constexpr int kRowsCta = kSimtWarpsT * kRowsPerWarp;
 constexpr int kKeyTile = 32;
+constexpr long long kSimtFewRows = 4096;  // up to this many query rows: one row per warp
 
-template <typename T, int kDPL>  // kDPL = D / 32 output dims per lane
+template <typename T, int kDPL, int kRowsPerWarp>  // kDPL = D / 32 output dims per lane
 __global__ void __launch_bounds__(kSimtWarpsT * 32) attn_simt_kernel(const T* __restrict__ q,
                                                                     const T* __restrict__ k,
                                                                     const T* __restrict__ v, T* __restrict__ out,
@@ -45,6 +46,7 @@ __global__ void __launch_bounds__(kSimtWarpsT * 32) attn_simt_kernel(const T* __
                                                                     int Hq, int Hkv, int D, int P, int N, int S,
                                                                     float scale, int32_t* dev_status) {
   constexpr int kD = kDPL * 32;
+  constexpr int kRowsCta = kSimtWarpsT * kRowsPerWarp;
   extern __shared__ float simt_smem[];
   // dynamic layout: K tile (rows padded by one word), V tile, the rows' queries, their
   // visible-tree-node masks, the parent array
@@ -176,15 +178,16 @@ __global__ void __launch_bounds__(kSimtWarpsT * 32) attn_simt_kernel(const T* __
   }
 }
 
-static size_t simt_smem_bytes(int d) {
-  return sizeof(float) * ((size_t)kKeyTile * (d + 1) + (size_t)kKeyTile * d + (size_t)kRowsCta * d +
-                          (size_t)kRowsCta * (kMaxNodes / 32) + kMaxNodes);
+static size_t simt_smem_bytes(int d, int rows_cta) {
+  return sizeof(float) * ((size_t)kKeyTile * (d + 1) + (size_t)kKeyTile * d + (size_t)rows_cta * d +
+                          (size_t)rows_cta * (kMaxNodes / 32) + kMaxNodes);
 }
 
-template <typename T>
+template <typename T, int kRPW>
 static void launch_simt_t(const void* q, const void* k, const void* v, void* out, const int32_t* parent, int B,
                           int Hq, int Hkv, int D, int P, int N, int S, float scale, int32_t* dev_status,
                           cudaStream_t stream) {
+  constexpr int kRowsCta = kSimtWarpsT * kRPW;
   const int G = Hq / Hkv;
   const long long blocks_per_head = ((long long)G * N + kRowsCta - 1) / kRowsCta;
   const unsigned grid = (unsigned)(blocks_per_head * Hkv * B);
@@ -195,12 +198,12 @@ static void launch_simt_t(const void* q, const void* k, const void* v, void* out
   switch (D / 32) {
 #define TV_SIMT_CASE(n)                                                                                        \
   case n: {                                                                                                    \
-    const size_t smem = simt_smem_bytes(n * 32);                                                               \
-    if (cudaFuncSetAttribute(attn_simt_kernel<T, n>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != \
-        cudaSuccess)                                                                                           \
+    const size_t smem = simt_smem_bytes(n * 32, kRowsCta);                                                     \
+    if (cudaFuncSetAttribute(attn_simt_kernel<T, n, kRPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,         \
+                             (int)smem) != cudaSuccess)                                                        \
       return;                                                                                                  \
-    attn_simt_kernel<T, n><<<grid, kSimtWarpsT * 32, smem, stream>>>(qq, kk, vv, oo, parent, B, Hq, Hkv, D, P, N, \
-                                                                    S, scale, dev_status);                     \
+    attn_simt_kernel<T, n, kRPW><<<grid, kSimtWarpsT * 32, smem, stream>>>(qq, kk, vv, oo, parent, B, Hq, Hkv, D, \
+                                                                          P, N, S, scale, dev_status);         \
     break;                                                                                                     \
   }
     TV_SIMT_CASE(1)
@@ -220,10 +223,18 @@ static void launch_simt_t(const void* q, const void* k, const void* v, void* out
 cudaError_t launch_attn_simt(const void* q, const void* k, const void* v, void* out, const int32_t* parent,
                              int B, int Hq, int Hkv, int D, int P, int N, int S, float scale, tv_dtype dtype,
                              int32_t* dev_status, cudaStream_t stream) {
-  if (dtype == TV_BF16)
-    launch_simt_t<uint16_t>(q, k, v, out, parent, B, Hq, Hkv, D, P, N, S, scale, dev_status, stream);
-  else
-    launch_simt_t<float>(q, k, v, out, parent, B, Hq, Hkv, D, P, N, S, scale, dev_status, stream);
+  const bool few = (long long)B * Hq * N <= kSimtFewRows;
+  if (dtype == TV_BF16) {
+    if (few)
+      launch_simt_t<uint16_t, 1>(q, k, v, out, parent, B, Hq, Hkv, D, P, N, S, scale, dev_status, stream);
+    else
+      launch_simt_t<uint16_t, 4>(q, k, v, out, parent, B, Hq, Hkv, D, P, N, S, scale, dev_status, stream);
+  } else {
+    if (few)
+      launch_simt_t<float, 1>(q, k, v, out, parent, B, Hq, Hkv, D, P, N, S, scale, dev_status, stream);
+    else
+      launch_simt_t<float, 4>(q, k, v, out, parent, B, Hq, Hkv, D, P, N, S, scale, dev_status, stream);
+  }
   return cudaGetLastError();
 }
 
