@@ -106,11 +106,11 @@ __global__ void __launch_bounds__(kSimtWarpsT * 32) attn_simt_kernel(const T* __
   }
   const size_t kvbase = ((size_t)b * Hkv + kh) * (size_t)S * D;
   const int total = P + N;
-  for (int j0 = 0; j0 < total; j0 += kKeyTile) {
-    __syncthreads();  // the previous tile is consumed
-    // all of a thread's tile loads are issued before any of them is stored
-    constexpr int kPer = kKeyTile * kD / (kSimtWarpsT * 32);
-    float kx[kPer], vx[kPer];
+  // K/V tiles go through registers: the next tile's loads are issued before the current
+  // tile is computed on, so their latency overlaps the compute
+  constexpr int kPer = kKeyTile * kD / (kSimtWarpsT * 32);
+  float kx[kPer], vx[kPer];
+  auto load_tile = [&](int j0) {
 #pragma unroll
     for (int it = 0; it < kPer; ++it) {
       const int e = threadIdx.x + it * kSimtWarpsT * 32;
@@ -120,6 +120,10 @@ __global__ void __launch_bounds__(kSimtWarpsT * 32) attn_simt_kernel(const T* __
       kx[it] = in ? ldx(k, off) : 0.f;
       vx[it] = in ? ldx(v, off) : 0.f;
     }
+  };
+  load_tile(0);
+  for (int j0 = 0; j0 < total; j0 += kKeyTile) {
+    __syncthreads();  // the previous tile is consumed
 #pragma unroll
     for (int it = 0; it < kPer; ++it) {
       const int e = threadIdx.x + it * kSimtWarpsT * 32;
@@ -128,6 +132,7 @@ __global__ void __launch_bounds__(kSimtWarpsT * 32) attn_simt_kernel(const T* __
       s_v[jj][d] = vx[it];
     }
     __syncthreads();
+    if (j0 + kKeyTile < total) load_tile(j0 + kKeyTile);
     const int j = j0 + lane;
 #pragma unroll
     for (int rw = 0; rw < kRowsPerWarp; ++rw) {
