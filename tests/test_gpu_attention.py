@@ -268,3 +268,23 @@ def test_fp32_many_rows_four_rows_per_warp():
     par, _ = W.trees(g, B, N, 6, 100)
     q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, False)
     _check_all(q, k, v, par, P, False)
+
+
+def test_attention_plan_query_and_overrides():
+    # the plan query names a tensor-core kernel for bf16 tile shapes and the CUDA-core one
+    # for fp32; forced variants and split counts are what the query then reports
+    assert tv.tree_attention_plan(1, 4, 1, 64, 128, 16, torch.float32) == (0, 1)
+    k, s = tv.tree_attention_plan(8, 32, 8, 128, 32768, 128, torch.bfloat16)
+    assert k in (1, 2) and 1 <= s <= 8
+    try:
+        tv.set_attention_variant(1)
+        tv.set_attention_splits(3)
+        assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16) == (1, 3)
+        tv.set_attention_variant(2)
+        tv.set_attention_splits(0)
+        assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16)[0] == 2
+    finally:
+        tv.set_attention_variant(0)
+        tv.set_attention_splits(0)
+    with pytest.raises(Exception):
+        tv.set_attention_splits(9)
