@@ -380,6 +380,7 @@ __device__ __forceinline__ int expand_threshold(const SelSmem& sm, const float (
       ec->live[nb] = 0;
     }
     int nitems = nsrc * nr;
+    const float inv_nr = nr > 0 ? 1.f / (float)nr : 0.f;
     const bool listed = nitems > (int)blockDim.x;
     bool dropped = false;
     int* item = sm.pos;  // listed (source, rank) pairs, (entry + 1) << 8 | rank
@@ -438,7 +439,11 @@ __device__ __forceinline__ int expand_threshold(const SelSmem& sm, const float (
           pe = (v >> 8) - 1;
           r = v & 255;
         } else {
-          const int i = it / nr;
+          int i = (int)((float)it * inv_nr);  // it / nr: the estimate is off by at most one
+          if ((i + 1) * nr <= it)
+            ++i;
+          else if (i * nr > it)
+            --i;
           r = r0 + (it - i * nr);
           pe = step == 0 ? -1 : lo + i;
         }
@@ -480,13 +485,20 @@ __device__ __forceinline__ int expand_threshold(const SelSmem& sm, const float (
       uint64_t c1 = pe < 0 ? 0ull : sm.k1[pe], c2 = pe < 0 ? 0ull : sm.k2[pe];
       path_set(c1, c2, dep, r);
       // branch-free stores: entries outside the run go to the lane's spare slot.  Short
-      // runs (every run of the warp within 4) walk 4 positions with the factors read
-      // from shared memory; longer ones walk all positions with the factors in registers.
+      // runs (every run of the warp within 4 or 8) walk 4 or 8 positions with the factors
+      // read from shared memory up front; longer ones walk all positions with the factors
+      // in registers.
       float sc = s0;
-      if (wmax <= 4) {
+      if (wmax <= 8) {
+        // the rank-0 factors of the next positions, loaded independently of each other;
+        // 4 or 8 positions (warp-uniform)
+        float f[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (q > 0) sc = __fmul_rn(sc, sm.marg[min(dep + q, d - 1) * K]);
+        for (int q = 1; q < 8; ++q) f[q] = sm.marg[min(dep + q, d - 1) * K];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (q == 4 && wmax <= 4) break;
+          if (q > 0) sc = __fmul_rn(sc, f[q]);
           const int e = q < len ? base + q : kSelCap + lane;
           sm.k0[e] = make_k0(sc, dep + q + 1);
           sm.k1[e] = c1;
