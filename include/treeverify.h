@@ -93,6 +93,16 @@ TV_API const char* tv_status_string(int status);
 /* Library ABI version: (major << 16) | minor. */
 TV_API int tv_version(void);
 
+/* tv_selftest_bounded_wait - exercise the failure path of the in-kernel bounded waits.
+ * (No counterpart in the pages: it checks this library's own failure detection.)  One
+ * warp waits on an mbarrier phase that nothing completes, through the same bounded wait
+ * the attention and vocab pipelines use but with a limit of wait_us microseconds; the
+ * wait gives up, the kernel ORs TV_DEV_TIMEOUT into *dev_status and returns, and the CUDA
+ * context stays usable.  Nothing faults, traps or hangs.
+ * Errors: dev_status NULL -> TV_ERR_NULL; wait_us outside 1..1000000 -> TV_ERR_VALUE.
+ */
+TV_API tv_status tv_selftest_bounded_wait(int wait_us, int32_t* dev_status, tv_stream_t stream);
+
 /* ------------------------------------------------------------------------------------
  * tv_set_sm_partition - SM shares for running tv_tree_attention and tv_verify_* at the
  * same time on two streams.  The vocab pass then launches at most verify_sms CTAs (one

@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     prune_tree,
     select_subtree,
     select_workspace_size,
+    selftest_bounded_wait,
     set_attention_splits,
     set_attention_variant,
     set_sm_partition,

@@ -40,6 +40,7 @@ _U64 = ctypes.c_uint64
 _SIGS = {
     "tv_status_string": (ctypes.c_char_p, [_I]),
     "tv_version": (_I, []),
+    "tv_selftest_bounded_wait": (_I, [_I, _P, _P]),
     "tv_set_sm_partition": (_I, [_I, _I]),
     "tv_set_attention_variant": (_I, [_I]),
     "tv_set_attention_splits": (_I, [_I]),
@@ -145,6 +146,14 @@ def _status_tensor(dev_status, device):
 def set_sm_partition(verify_sms: int, attention_sms: int):
     """SM shares for running tree_attention and verify_* concurrently (0, 0 = whole device)."""
     _check("tv_set_sm_partition", load_library().tv_set_sm_partition(int(verify_sms), int(attention_sms)))
+
+
+def selftest_bounded_wait(wait_us: int, dev_status):
+    """Wait on an mbarrier that nothing completes, giving up after wait_us; the kernel
+    sets TV_DEV_TIMEOUT in dev_status (a CUDA int32 tensor) and returns."""
+    _need_cuda(dev_status=dev_status)
+    _check("tv_selftest_bounded_wait", load_library().tv_selftest_bounded_wait(int(wait_us), _ptr(dev_status),
+                                                                               _stream()))
 
 
 def set_attention_variant(variant: int):

@@ -59,6 +59,12 @@ const char* tv_status_string(int s) {
 
 int tv_version(void) { return (1 << 16) | 0; }
 
+tv_status tv_selftest_bounded_wait(int wait_us, int32_t* dev_status, tv_stream_t stream) {
+  if (!dev_status) return TV_ERR_NULL;
+  if (wait_us < 1 || wait_us > 1000000) return TV_ERR_VALUE;
+  return cuda_status(launch_wait_selftest((uint64_t)wait_us * 1000ull, dev_status, st(stream)));
+}
+
 tv_status tv_set_sm_partition(int verify_sms, int attention_sms) {
   if (verify_sms < 0 || attention_sms < 0) return TV_ERR_VALUE;
   g_sm_verify = verify_sms;

@@ -4,6 +4,7 @@
 // its observable prefix set pi(v) = {v} U pi(P(v)); its position encoding is fixed by
 // |pi(v)|.  One CTA of 1024 threads per sequence; parent[] lives in shared memory.
 #include "tv_kernels.cuh"
+#include "tv_ptx.cuh"
 
 namespace tv {
 
@@ -103,6 +104,29 @@ cudaError_t launch_tree_prep(const int32_t* parent, int B, int N, int P, int32_t
                              uint32_t* anc_mask, int32_t* child_off, int32_t* child_idx,
                              int32_t* dev_status, cudaStream_t stream) {
   tree_prep_kernel<<<B, 1024, 0, stream>>>(parent, N, P, depth, pos, anc_mask, child_off, child_idx, dev_status);
+  return cudaGetLastError();
+}
+
+// Self-test of the bounded waits: one warp waits on an mbarrier that nothing arrives on,
+// through the same bounded wait every pipeline uses but with the caller's limit; it must
+// give up, report TV_DEV_TIMEOUT and return.  (Every other lane of the warp waits on the
+// abort flag the first one sets.)
+__global__ void wait_selftest_kernel(uint64_t limit_ns, int32_t* dev_status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = ptx::mbar_wait_limit(&bar, 0, &abort_flag, limit_ns);
+  __syncthreads();
+  if (threadIdx.x == 0 && (!ok || abort_flag)) set_dev_status(dev_status, TV_DEV_TIMEOUT);
+}
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* dev_status, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, dev_status);
   return cudaGetLastError();
 }
 

@@ -29,6 +29,9 @@ cudaError_t launch_sample_walk(const void* target, const void* draft, const int3
                                int32_t* accepted, int32_t* accept_len, int32_t* out_token,
                                int32_t* dev_status, cudaStream_t stream);
 
+// ---- bounded-wait self-test
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* dev_status, cudaStream_t stream);
+
 // ---- tree prep
 cudaError_t launch_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* depth, int32_t* pos,
                              uint32_t* anc_mask, int32_t* child_off, int32_t* child_idx,

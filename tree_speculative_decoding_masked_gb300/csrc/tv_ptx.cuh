@@ -37,7 +37,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // TV_WAIT_NS nanoseconds or as soon as *abort is set by another thread of the CTA.  The
 // flag and the clock are looked at only every 64 polls, so a completed phase is seen
 // within one poll.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
@@ -47,12 +48,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       const uint64_t now = globaltimer_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > TV_WAIT_NS) {
+      } else if (now - t0 > limit_ns) {
         *abort = 1;
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return mbar_wait_limit(bar, parity, abort, TV_WAIT_NS);
 }
 
 // Device-scope fetch-and-add with acquire-release semantics: after a CTA barrier, one
