@@ -523,7 +523,7 @@ def run_ours(args):
         G = Hq // Hkv
         nt = (128 // G) // 8 * 8
         mtiles = -(-N // nt)
-        ctas = B * Hkv * (-(-mtiles // 2) if kern == 2 else mtiles) * spl
+        ctas = B * Hkv * (-(-mtiles // 2) if kern >= 2 else mtiles) * spl
         if kern and ctas < n_sm:
             parts.append((n_sm - ctas, ctas))
     candidates = [(part, vm) for part in parts for vm in (False, True)]
@@ -629,7 +629,8 @@ def run_ours(args):
     fam_flops = {"attention": 4 * B * Hq * N * (P + N) * D, "verify": 0}
     dom = max(("attention", "verify"), key=lambda kk: br[kk])
     attn_kernel, attn_splits = tv.tree_attention_plan(B, Hq, Hkv, D, P, N, tdt)
-    kernel_names = {"attention": ("attn_simt_kernel", "attn_tc_kernel", "attn_pair_kernel")[attn_kernel],
+    kernel_names = {"attention": ("attn_simt_kernel", "attn_tc_kernel", "attn_pair_kernel",
+                                  "attn_pair2_kernel")[attn_kernel],
                     "verify": "vocab_pass_tma_kernel"}
     roofline = roofline_entry(kernel_names[dom], fam_bytes[dom], fam_flops[dom] if bf16 else 0, br[dom] * 1e-6,
                               args.workload)

@@ -116,13 +116,16 @@ TV_API tv_status tv_set_sm_partition(int verify_sms, int attention_sms);
 
 /* ------------------------------------------------------------------------------------
  * tv_set_attention_variant - which tensor-core kernel tv_tree_attention uses for bf16.
- *   0  automatic (default): the variant and KV split count that minimise a wave model
- *      of the run time (see tv_tree_attention_plan); paired tiles need G * N > 128
+ *   0  automatic (default): the variant (1 or 3) and KV split count that minimise a
+ *      wave model of the run time (see tv_tree_attention_plan); paired tiles need
+ *      G * N > 128
  *   1  one 128-row tile per CTA
  *   2  paired row tiles: one CTA streams the KV range once for two 128-row tiles
+ *   3  paired row tiles with 64-key KV tiles and two S buffers per row tile, so S of
+ *      the next KV tile is computed while the softmax of the current one runs
  * Both compute the same result (up to fp32 summation order); the switch exists to
  * compare and test them.  Process-wide, host-side; affects launches made after the call.
- * Errors: a value outside 0..2 -> TV_ERR_VALUE.
+ * Errors: a value outside 0..3 -> TV_ERR_VALUE.
  */
 TV_API tv_status tv_set_attention_variant(int variant);
 
@@ -200,7 +203,8 @@ TV_API size_t tv_tree_attention_workspace_size(int B, int Hq, int Hkv, int D, in
  * for these sizes on the current device with the current settings
  * (tv_set_attention_variant, tv_set_attention_splits, tv_set_sm_partition):
  *   *kernel  0 CUDA-core kernel (fp32, or shapes the tensor-core kernels do not take),
- *            1 tensor-core kernel with one 128-row tile per CTA, 2 paired row tiles
+ *            1 tensor-core kernel with one 128-row tile per CTA, 2 paired row tiles,
+ *            3 paired row tiles with 64-key KV tiles and double-buffered S
  *   *splits  KV ranges per tile group, merged in one thread-block cluster
  * Automatic choice: the variant and split count that minimise a wave model of the run
  * time (waves of resident clusters x (KV tiles per CTA + fixed per-CTA and merge costs))

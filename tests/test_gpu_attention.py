@@ -190,7 +190,7 @@ def test_bad_tree_flagged():
         assert int(st.item()) & tv.TV_DEV_BAD_TREE
 
 
-@pytest.fixture(params=[1, 2], ids=["one_tile_per_cta", "paired_tiles"])
+@pytest.fixture(params=[1, 2, 3], ids=["one_tile_per_cta", "paired_tiles", "paired_tiles_64key_double_s"])
 def variant(request):
     tv.set_attention_variant(request.param)
     yield request.param
@@ -245,6 +245,15 @@ def test_long_context_workload_sampled_one_tile_per_cta():
         tv.set_attention_variant(0)
 
 
+@pytest.mark.parametrize("name", ["long_context", "sampling", "budget_sweep"])
+def test_workloads_sampled_64key_double_s(name):
+    tv.set_attention_variant(3)
+    try:
+        _sampled_rows(name, 24, seed_extra=6)
+    finally:
+        tv.set_attention_variant(0)
+
+
 @pytest.mark.parametrize("splits", [1, 3, 8])
 def test_forced_splits_both_variants(variant, splits):
     # every split count merges to the same result, including more splits than a short
@@ -275,7 +284,7 @@ def test_attention_plan_query_and_overrides():
     # for fp32; forced variants and split counts are what the query then reports
     assert tv.tree_attention_plan(1, 4, 1, 64, 128, 16, torch.float32) == (0, 1)
     k, s = tv.tree_attention_plan(8, 32, 8, 128, 32768, 128, torch.bfloat16)
-    assert k in (1, 2) and 1 <= s <= 8
+    assert k in (1, 3) and 1 <= s <= 8
     try:
         tv.set_attention_variant(1)
         tv.set_attention_splits(3)
@@ -283,6 +292,8 @@ def test_attention_plan_query_and_overrides():
         tv.set_attention_variant(2)
         tv.set_attention_splits(0)
         assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16)[0] == 2
+        tv.set_attention_variant(3)
+        assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16)[0] == 3
     finally:
         tv.set_attention_variant(0)
         tv.set_attention_splits(0)

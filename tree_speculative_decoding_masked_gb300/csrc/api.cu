@@ -8,7 +8,8 @@ using namespace tv;
 
 // SM shares for running the vocab pass and the tree attention concurrently (0 = all SMs)
 static int g_sm_verify = 0, g_sm_attention = 0;
-// tensor-core attention kernel: 0 automatic, 1 one row tile per CTA, 2 paired row tiles
+// tensor-core attention kernel: 0 automatic, 1 one row tile per CTA, 2 paired row tiles,
+// 3 paired row tiles with 64-key KV tiles and double-buffered S
 static int g_attn_variant = 0;
 // KV splits per tensor-core attention CTA group: 0 automatic, else forced (capped at the
 // KV tile count and the cluster limit)
@@ -73,7 +74,7 @@ tv_status tv_set_sm_partition(int verify_sms, int attention_sms) {
 }
 
 tv_status tv_set_attention_variant(int variant) {
-  if (variant < 0 || variant > 2) return TV_ERR_VALUE;
+  if (variant < 0 || variant > 3) return TV_ERR_VALUE;
   g_attn_variant = variant;
   return TV_OK;
 }
@@ -145,9 +146,7 @@ tv_status tv_tree_attention_plan(int B, int Hq, int Hkv, int D, int P, int N, tv
     *splits = 1;
     return TV_OK;
   }
-  int pair = 0;
-  attn_tc_choice(B, Hkv, D, P, N, p, &pair, splits);
-  *kernel = pair ? 2 : 1;
+  attn_tc_choice(B, Hkv, D, P, N, p, kernel, splits);
   return TV_OK;
 }
 

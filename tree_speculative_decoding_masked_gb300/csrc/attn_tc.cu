@@ -1033,6 +1033,447 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------
+// Paired row tiles with 64-key KV tiles and two S buffers per row tile.  The same roles
+// as attn_pair_kernel, but with 64-key tiles each tile's S takes 64 TMEM columns, so both
+// row tiles get two S buffers next to their O accumulators: S_X of KV tile t + 1 is
+// computed while the softmax of tile t runs, and the tensor core no longer waits for the
+// serial S -> softmax -> PV chain of each tile.  P_X(t) (bf16, 32 columns) is written over
+// the first half of its own S buffer by its row's thread; S_X(t + 2) reuses that buffer
+// once PV_X(t) has completed.
+// TMEM columns: S_A[0] 0..63, S_A[1] 64..127, S_B[0] 128..191, S_B[1] 192..255,
+// O_A 256.., O_B 384...
+constexpr int kBN2 = 64;       // keys per KV tile
+constexpr int kPair2Slots = 4; // K ring and V ring depth
+
+template <int D>
+struct Pair2Cfg {
+  static constexpr int kDB = D / 64;
+  static constexpr int kQBlock = kRows * 128;        // bytes per column block of one Q tile
+  static constexpr int kQTile = kDB * kQBlock;
+  static constexpr int kKVBlock = kBN2 * 128;        // bytes per column block of a K or V tile
+  static constexpr int kTileBytes = kDB * kKVBlock;  // one K or V tile
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kQTile;
+  static constexpr int kOffV = kOffK + kPair2Slots * kTileBytes;
+  static constexpr int kOffPar = kOffV + kPair2Slots * kTileBytes;
+  static constexpr int kOffBar = kOffPar + kMaxNodes * 4;
+  static constexpr int kSmemUsed = kOffBar + 512;
+  static constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 256;               // O_X at kColO + X * 128
+  static_assert(kColO + kRows + D <= kTmemCols, "TMEM budget");
+  static_assert(2 * kPair2Slots * kTileBytes >= 2 * kRows * D * 4, "split partials fit in the drained rings");
+  static_assert(2 * kQTile >= 2 * kRows * 8, "(m, l) of both tiles fit in the drained Q tiles");
+  static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
+};
+
+struct Pair2Bars {
+  uint64_t q_full;
+  uint64_t k_full[kPair2Slots];
+  uint64_t k_empty[kPair2Slots];
+  uint64_t v_full[kPair2Slots];
+  uint64_t v_empty[kPair2Slots];
+  uint64_t s_full[2][2];   // [row tile][S buffer]: S_X(t) complete, t & 1 == buffer
+  uint64_t p_full[2][2];   // P_X(t) written (4 warps)
+  uint64_t pv_done[2][2];  // PV_X(t) complete
+  uint64_t o_done;
+  uint64_t s_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_pair2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, TcArgs a) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();  // before any global read or write
+  using C = Pair2Cfg<D>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t mis = ptx::smem_addr(smem_raw) & 1023u;
+  unsigned char* sm = smem_raw + ((1024u - mis) & 1023u);
+  unsigned char* sQ = sm + C::kOffQ;
+  unsigned char* sK = sm + C::kOffK;
+  unsigned char* sV = sm + C::kOffV;
+  int* s_par = reinterpret_cast<int*>(sm + C::kOffPar);
+  Pair2Bars* bars = reinterpret_cast<Pair2Bars*>(sm + C::kOffBar);
+  volatile int* abort_flag = &bars->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mp = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
+  const int hk = blockIdx.y, b = blockIdx.z;
+  int i0[2], t_allx[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    i0[x] = (2 * mp + x) * a.NT;
+    t_allx[x] = i0[x] < a.N ? (a.P + min(a.N, i0[x] + a.NT) + kBN2 - 1) / kBN2 : 0;
+  }
+  const int t_all = max(t_allx[0], t_allx[1]);
+  const int tps = (t_all + a.splits - 1) / a.splits;
+  const int t_begin = split * tps;
+  int ntx[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) ntx[x] = max(0, min(t_allx[x], t_begin + tps) - t_begin);
+  const int nt = max(ntx[0], ntx[1]);
+  const int rows_used = a.G * a.NT;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kPair2Slots; ++s) {
+      ptx::mbar_init(&bars->k_full[s], 1);
+      ptx::mbar_init(&bars->k_empty[s], 1);
+      ptx::mbar_init(&bars->v_full[s], 1);
+      ptx::mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x)
+      for (int u = 0; u < 2; ++u) {
+        ptx::mbar_init(&bars->s_full[x][u], 1);
+        ptx::mbar_init(&bars->p_full[x][u], 4);
+        ptx::mbar_init(&bars->pv_done[x][u], 1);
+      }
+    ptx::mbar_init(&bars->o_done, 1);
+    ptx::mbar_init(&bars->s_done, 1);
+    bars->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp >= 2) {
+    const int t = threadIdx.x - 64;
+    int bad = 0;
+    for (int c = t; c < a.N; c += kThreads - 64) {
+      const int p = a.parent[(size_t)b * a.N + c];
+      s_par[c] = p;
+      if (!((c == 0) ? (p == -1) : (p >= 0 && p < c))) bad = 1;
+    }
+    if (bad) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);
+    for (int r = rows_used + t; r < 2 * kRows; r += kThreads - 64) {
+      const int x = r >= kRows ? 1 : 0, rr = r - x * kRows;
+      if (rr < rows_used) continue;
+      for (int db = 0; db < C::kDB; ++db) {
+        uint4* row = reinterpret_cast<uint4*>(sQ + x * C::kQTile + db * C::kQBlock + rr * 128);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) row[k] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producers
+    if (lane == 0 && nt > 0) {
+      int issued[kPair2Slots] = {0, 0, 0, 0};
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmK);
+      uint32_t qbytes = 0;
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+        if (ntx[x] > 0) qbytes += (uint32_t)(rows_used * 128 * C::kDB);
+      ptx::mbar_arrive_expect_tx(&bars->q_full, qbytes);
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+        if (ntx[x] > 0)
+          for (int g = 0; g < a.G; ++g)
+            for (int db = 0; db < C::kDB; ++db)
+              ptx::tma_load_3d(sQ + x * C::kQTile + db * C::kQBlock + g * a.NT * 128, &tmQ, &bars->q_full, db * 64,
+                               i0[x], b * a.Hq + hk * a.G + g);
+      for (int t = 0; t < nt; ++t) {
+        const int ks = t % kPair2Slots;
+        if (t >= kPair2Slots && !ptx::mbar_wait(&bars->k_empty[ks], ((t / kPair2Slots) - 1) & 1, abort_flag))
+          break;
+        unsigned char* dst = sK + ks * C::kTileBytes;
+        const int j0 = (t_begin + t) * kBN2;
+        ptx::mbar_arrive_expect_tx(&bars->k_full[ks], (uint32_t)C::kTileBytes);
+        for (int db = 0; db < C::kDB; ++db)
+          ptx::tma_load_3d(dst + db * C::kKVBlock, &tmK, &bars->k_full[ks], db * 64, j0, b * a.Hkv + hk);
+        ++issued[ks];
+      }
+      ptx::mbar_wait(&bars->q_full, 0, abort_flag);
+      for (int s = 0; s < kPair2Slots; ++s)
+        if (issued[s]) ptx::mbar_wait(&bars->k_full[s], (issued[s] - 1) & 1, abort_flag);
+    } else if (lane == 1 && nt > 0) {
+      int issued[kPair2Slots] = {0, 0, 0, 0};
+      ptx::prefetch_tmap(&tmV);
+      for (int t = 0; t < nt; ++t) {
+        const int vs = t % kPair2Slots;
+        if (t >= kPair2Slots && !ptx::mbar_wait(&bars->v_empty[vs], ((t / kPair2Slots) - 1) & 1, abort_flag))
+          break;
+        unsigned char* dst = sV + vs * C::kTileBytes;
+        const int j0 = (t_begin + t) * kBN2;
+        ptx::mbar_arrive_expect_tx(&bars->v_full[vs], (uint32_t)C::kTileBytes);
+        for (int db = 0; db < C::kDB; ++db)
+          ptx::tma_load_3d(dst + db * C::kKVBlock, &tmV, &bars->v_full[vs], db * 64, j0, b * a.Hkv + hk);
+        ++issued[vs];
+      }
+      for (int s = 0; s < kPair2Slots; ++s)
+        if (issued[s]) ptx::mbar_wait(&bars->v_full[s], (issued[s] - 1) & 1, abort_flag);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ S issuer
+    if (lane == 0) {
+      if (nt > 0 && ptx::mbar_wait(&bars->q_full, 0, abort_flag)) {
+        constexpr uint32_t idS = ptx::idesc_bf16(kRows, kBN2, false, false);
+        bool ok = true;
+        for (int t = 0; ok && t < nt; ++t) {
+          const int ks = t % kPair2Slots, buf = t & 1;
+          if (!ptx::mbar_wait(&bars->k_full[ks], (t / kPair2Slots) & 1, abort_flag)) break;
+          const uint32_t kaddr = ptx::smem_addr(sK + ks * C::kTileBytes);
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (t >= ntx[x]) continue;
+            // S_X(t) overwrites P_X(t - 2) in this buffer: wait for PV_X(t - 2)
+            if (t >= 2 && !ptx::mbar_wait(&bars->pv_done[x][buf], ((t - 2) >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t qaddr = ptx::smem_addr(sQ + x * C::kQTile);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk & 3) * 32;  // 16-element K step inside a 128-byte row
+              const uint64_t ad = ptx::sdesc_sw128(qaddr + (kk >> 2) * C::kQBlock + off, 16, 1024);
+              const uint64_t bd = ptx::sdesc_sw128(kaddr + (kk >> 2) * C::kKVBlock + off, 16, 1024);
+              ptx::mma_bf16_ss(tmem + x * kRows + buf * kBN2, ad, bd, idS, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(&bars->s_full[x][buf]);
+          }
+          if (ok) ptx::mma_commit(&bars->k_empty[ks]);
+        }
+      }
+      ptx::mma_commit(&bars->s_done);
+      ptx::mbar_wait(&bars->s_done, 0, abort_flag);
+    }
+    __syncwarp();
+  } else if (warp == kThreads / 32 - 1) {
+    // ------------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t idO = ptx::idesc_bf16(kRows, D, false, true);
+      bool ok = true;
+      for (int t = 0; ok && t < nt; ++t) {
+        const int vs = t % kPair2Slots, buf = t & 1;
+        if (!ptx::mbar_wait(&bars->v_full[vs], (t / kPair2Slots) & 1, abort_flag)) break;
+        const uint32_t vaddr = ptx::smem_addr(sV + vs * C::kTileBytes);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (t >= ntx[x]) continue;
+          if (!ptx::mbar_wait(&bars->p_full[x][buf], (t >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t pcol = tmem + x * kRows + buf * kBN2;  // P: 8 columns per 16 keys
+#pragma unroll
+          for (int kk = 0; kk < kBN2 / 16; ++kk) {
+            const uint64_t bd = ptx::sdesc_sw128(vaddr + kk * 16 * 128, C::kKVBlock, 1024);
+            ptx::mma_bf16_ts(tmem + C::kColO + x * kRows, pcol + kk * 8, bd, idO, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(&bars->pv_done[x][buf]);
+        }
+        if (ok) ptx::mma_commit(&bars->v_empty[vs]);
+      }
+      ptx::mma_commit(&bars->o_done);
+      ptx::mbar_wait(&bars->o_done, 0, abort_flag);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax rows
+    const int x = (warp - 2) >> 2;
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int g = r / a.NT, il = r % a.NT;
+    const int node = i0[x] + il;
+    const bool valid = (g < a.G) && (node < a.N) && (r < rows_used);
+    const int mnode = valid ? node : 0;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const uint32_t colS = tmem + lane_base + x * kRows;
+    const uint32_t colO = tmem + lane_base + C::kColO + x * kRows;
+    const int ntm = ntx[x];
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int t = 0; t < ntm; ++t) {
+      const int buf = t & 1;
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->s_full[x][buf], (t >> 1) & 1, abort_flag));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int j0 = (t_begin + t) * kBN2;
+      const uint64_t vis = key_mask(j0, a.P, a.N, mnode, s_par);
+      float sv[64];
+      ptx::tmem_ld32(colS + buf * kBN2, sv);
+      ptx::tmem_ld32(colS + buf * kBN2 + 32, sv + 32);
+      ptx::tmem_wait_ld();
+      if (vis != ~0ull) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (!((vis >> j) & 1ull)) sv[j] = -INFINITY;
+      }
+      const float tms = max64(sv, -INFINITY) * a.c;
+      float alpha = 1.f;
+      bool need = false;
+      if (tms > m_run + kRescaleLog2) {
+        if (m_run != -INFINITY) {
+          alpha = ptx::ex2(m_run - tms);
+          need = true;
+        }
+        m_run = tms;
+      }
+      uint32_t pw[32];
+      const float lsum = exp_p64(sv, a.c, m_run, pw);
+      ptx::tmem_st32u(colS + buf * kBN2, pw);  // P over the first half of this S buffer
+      if (__any_sync(0xffffffffu, need) && t > 0) {
+        // O_X must hold all of PV_X(t - 1) before it is rescaled (S_X(t) may have been
+        // computed while PV_X(t - 1) was still running); PV_X(t) waits for P_X(t)
+        ok = __all_sync(0xffffffffu,
+                        ptx::mbar_wait(&bars->pv_done[x][(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag));
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float ov[32];
+          ptx::tmem_ld32(colO + c0, ov);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] *= alpha;
+          ptx::tmem_st32(colO + c0, ov);
+        }
+      }
+      l_run = l_run * alpha + lsum;
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->p_full[x][buf]);
+    }
+    // ---- epilogue (as in attn_pair_kernel): every MMA is complete at o_done
+    bool have_o = false;
+    if (nt > 0) {
+      const bool done = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->o_done, 0, abort_flag));
+      have_o = done && ok && ntm > 0;
+      if (done) ptx::tc_fence_after();
+    }
+    const int hh = hk * a.G + g;
+    const size_t orow = (((size_t)b * a.Hq + hh) * a.N + node) * D;
+    if (a.splits == 1) {
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float ov[32];
+        if (have_o) {
+          ptx::tmem_ld32(colO + c0, ov);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] = 0.f;
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow + c0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 u;
+            u.x = ptx::cvt_bf16x2(ov[8 * k + 0] * inv, ov[8 * k + 1] * inv);
+            u.y = ptx::cvt_bf16x2(ov[8 * k + 2] * inv, ov[8 * k + 3] * inv);
+            u.z = ptx::cvt_bf16x2(ov[8 * k + 4] * inv, ov[8 * k + 5] * inv);
+            u.w = ptx::cvt_bf16x2(ov[8 * k + 6] * inv, ov[8 * k + 7] * inv);
+            dst[k] = u;
+          }
+        }
+      }
+    } else {
+      const int R = x * kRows + r;
+      unsigned char* part = sK;
+      float2* ml = reinterpret_cast<float2*>(sQ);
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float ov[32];
+        if (have_o) {
+          ptx::tmem_ld32(colO + c0, ov);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int chunk = c0 / 4 + k;
+          *reinterpret_cast<float4*>(part + (size_t)R * D * 4 + ((chunk ^ (R & 7)) << 4)) =
+              make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+        }
+      }
+      ml[R] = make_float2(have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
+    }
+    ptx::tc_fence_before();
+  }
+  __syncwarp();
+  if (a.splits > 1) {
+    ptx::cluster_sync();
+    {
+      const int S = a.splits;
+      constexpr int kPRows = 2 * kRows;
+      const int R = (kPRows + S - 1) / S;
+      const int r0 = split * R, r1 = min(kPRows, r0 + R);
+      const int nrows = max(0, r1 - r0);
+      constexpr int kChunks = D / 4;
+      const uint32_t part_local = ptx::smem_addr(sK);
+      const uint32_t ml_local = ptx::smem_addr(sQ);
+      for (int item = threadIdx.x; item < nrows * kChunks; item += kThreads) {
+        const int rr = r0 + item / kChunks;
+        const int ch = item % kChunks;
+        const int xx = rr >= kRows ? 1 : 0, rt = rr - xx * kRows;
+        const int gg = rt / a.NT, ii = i0[xx] + rt % a.NT;
+        if (gg >= a.G || ii >= a.N || rt >= rows_used) continue;
+        float2 mlv[kMaxSplits];
+        float4 xv[kMaxSplits];
+        const uint32_t moff = (uint32_t)(rr * 8);
+        const uint32_t xoff = (uint32_t)(rr * D * 4 + ((ch ^ (rr & 7)) << 4));
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+          if (s2 < S) {
+            mlv[s2] = ptx::ld_cluster_f32x2(ptx::map_cluster(ml_local, s2) + moff);
+            xv[s2] = ptx::ld_cluster_f32x4(ptx::map_cluster(part_local, s2) + xoff);
+          }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxSplits; ++s2)
+          if (s2 < S) M = fmaxf(M, mlv[s2].x);
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+          if (s2 < S && mlv[s2].x != -INFINITY) {
+            const float w = ptx::ex2(mlv[s2].x - M);
+            L = fmaf(mlv[s2].y, w, L);
+            acc.x = fmaf(w, xv[s2].x, acc.x);
+            acc.y = fmaf(w, xv[s2].y, acc.y);
+            acc.z = fmaf(w, xv[s2].z, acc.z);
+            acc.w = fmaf(w, xv[s2].w, acc.w);
+          }
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const size_t o2 = (((size_t)b * a.Hq + hk * a.G + gg) * a.N + ii) * D + ch * 4;
+        uint2 u;
+        u.x = ptx::cvt_bf16x2(acc.x * inv, acc.y * inv);
+        u.y = ptx::cvt_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + o2) = u;
+      }
+    }
+    __syncwarp();
+    ptx::cluster_sync();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && bars->abort) set_dev_status(a.dev_status, TV_DEV_TIMEOUT);
+}
+
+// ------------------------------------------------------------------------------------
 // host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1080,9 +1521,24 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) 
   return p;
 }
 
-// How many clusters of `s` CTAs of attn_tc_kernel<D> (kPair: attn_pair_kernel<D>) can be
-// resident at once on the current device (cached per device, kernel and s).
-template <int D, bool kPair>
+// Kernel variants: 1 attn_tc_kernel (one 128-row tile per CTA, 128-key KV tiles),
+// 2 attn_pair_kernel (two row tiles, 128-key KV tiles), 3 attn_pair2_kernel (two row
+// tiles, 64-key KV tiles, two S buffers per row tile).
+template <int D, int kVar>
+static const void* tc_kernel_fn() {
+  if constexpr (kVar == 1) return reinterpret_cast<const void*>(attn_tc_kernel<D>);
+  else if constexpr (kVar == 2) return reinterpret_cast<const void*>(attn_pair_kernel<D>);
+  else return reinterpret_cast<const void*>(attn_pair2_kernel<D>);
+}
+template <int D, int kVar>
+static constexpr int tc_smem() {
+  return kVar == 1 ? TcCfg<D>::kSmemAlloc : kVar == 2 ? PairCfg<D>::kSmemAlloc : Pair2Cfg<D>::kSmemAlloc;
+}
+constexpr int tc_keys(int var) { return var == 3 ? kBN2 : kBN; }  // keys per KV tile
+
+// How many clusters of `s` CTAs of variant kVar can be resident at once on the current
+// device (cached per device, variant and s).
+template <int D, int kVar>
 static int max_active_clusters(int s) {
   static int cache[64][kMaxSplits + 1];  // one table per template instance
   static bool init = false;
@@ -1094,9 +1550,8 @@ static int max_active_clusters(int s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (cache[dev][s] >= 0) return cache[dev][s];
-  const void* fn = kPair ? reinterpret_cast<const void*>(attn_pair_kernel<D>)
-                         : reinterpret_cast<const void*>(attn_tc_kernel<D>);
-  const int smem = kPair ? PairCfg<D>::kSmemAlloc : TcCfg<D>::kSmemAlloc;
+  const void* fn = tc_kernel_fn<D, kVar>();
+  const int smem = tc_smem<D, kVar>();
   int n = 0;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
@@ -1121,89 +1576,90 @@ static int max_active_clusters(int s) {
 // split) x (tile cost), in units of one 128-row x 128-key tile of attn_tc_kernel.  The
 // constants are fitted to GB300 measurements over the qwen3 layer, sampling,
 // long-context and budget-sweep shapes (every split count of both kernels): a CTA's
-// set-up, pipeline fill and epilogue cost about 6 tiles, a cluster merge about 4.4, and a
-// tile pair of attn_pair_kernel about 1.85 single tiles.
+// set-up, pipeline fill and epilogue cost about 6 tiles, a cluster merge about 4.4, and
+// 128 keys of a tile pair about 1.85 single tiles for attn_pair_kernel and 1.78 for
+// attn_pair2_kernel (1.69-1.83 over the workloads).
 constexpr double kFixedTiles = 6.0;
 constexpr double kMergeTiles = 4.4;
 constexpr double kPairTileCost = 1.85;
+constexpr double kPair2TileCost = 1.78;
 
-template <int D, bool kPair>
-static double plan_cost(long long units, int t_all, int s) {
+template <int D, int kVar>
+static double plan_cost(long long units, int t_all128, int s) {
   const int share = sm_share_attention();  // an SM share set for concurrent kernels
   int nsm = 152, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  int act = max_active_clusters<D, kPair>(s);
+  int act = max_active_clusters<D, kVar>(s);
   if (act <= 0) return 1e300;
   if (share > 0 && share < nsm) act = std::max(1, (int)((long long)act * share / nsm));
   const long long waves = (units + act - 1) / act;
-  return (double)waves * ((t_all + s - 1) / s + kFixedTiles + (s > 1 ? kMergeTiles : 0.0)) *
-         (kPair ? kPairTileCost : 1.0);
+  const double tile = kVar == 1 ? 1.0 : kVar == 2 ? kPairTileCost : kPair2TileCost;
+  return (double)waves * ((t_all128 + s - 1) / s + kFixedTiles + (s > 1 ? kMergeTiles : 0.0)) * tile;
 }
 
+// *var: 1, 2 or 3 (see tc_kernel_fn).  The automatic choice considers variants 1 and 3:
+// variant 3 was faster than variant 2 on every workload measured (3-8 %); 2 stays
+// available when forced.
 template <int D>
-static void choose_plan(int B, int Hkv, int mtiles, int t_all, bool* pair, int* splits) {
+static void choose_plan(int B, int Hkv, int mtiles, int P, int N, int* var, int* splits) {
   const int variant = attention_variant();
   const int forced = attention_splits();
+  const int t_all128 = (P + N + kBN - 1) / kBN;
   double best_cost = 1e300;
-  *pair = false;
+  *var = 1;
   *splits = 1;
-  for (int v = 1; v <= 2; ++v) {
+  for (int v = 1; v <= 3; ++v) {
     if (variant != 0 && v != variant) continue;
-    if (variant == 0 && v == 2 && mtiles < 2) continue;  // nothing to pair
-    const long long units = (long long)B * Hkv * (v == 2 ? (mtiles + 1) / 2 : mtiles);
+    if (variant == 0 && (v == 2 || (v == 3 && mtiles < 2))) continue;
+    const long long units = (long long)B * Hkv * (v >= 2 ? (mtiles + 1) / 2 : mtiles);
+    const int t_all = (P + N + tc_keys(v) - 1) / tc_keys(v);
     for (int s = 1; s <= kMaxSplits && s <= t_all; ++s) {
       if (forced > 0 && s != std::min(forced, t_all)) continue;
-      const double c = v == 2 ? plan_cost<D, true>(units, t_all, s) : plan_cost<D, false>(units, t_all, s);
+      const double c = v == 1   ? plan_cost<D, 1>(units, t_all128, s)
+                       : v == 2 ? plan_cost<D, 2>(units, t_all128, s)
+                                : plan_cost<D, 3>(units, t_all128, s);
       if (c < best_cost * 0.98) {  // prefer fewer splits and the single-tile kernel on near ties
         best_cost = c;
-        *pair = v == 2;
+        *var = v;
         *splits = s;
       }
     }
   }
 }
 
-template <int D, bool kPair>
+template <int D, int kVar>
 static cudaError_t launch_tc_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const TcArgs& a,
                                int B, int Hkv, cudaStream_t stream) {
-  const int smem = kPair ? PairCfg<D>::kSmemAlloc : TcCfg<D>::kSmemAlloc;
-  cudaError_t e = kPair ? cudaFuncSetAttribute(attn_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                        : cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int smem = tc_smem<D, kVar>();
+  cudaError_t e = cudaFuncSetAttribute(tc_kernel_fn<D, kVar>(), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  const int units = kPair ? (a.MT + 1) / 2 : a.MT;  // CTAs per (b, kv head) and split
-  cfg.gridDim = dim3(units * a.splits, Hkv, B);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
+  const int units = kVar >= 2 ? (a.MT + 1) / 2 : a.MT;  // CTAs per (b, kv head) and split
+  const dim3 grid(units * a.splits, Hkv, B), block(kThreads, 1, 1);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)a.splits;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  e = kPair ? launch_pdl(attn_pair_kernel<D>, cfg.gridDim, cfg.blockDim, smem, stream, attr, 1, mq, mk, mv, a)
-            : launch_pdl(attn_tc_kernel<D>, cfg.gridDim, cfg.blockDim, smem, stream, attr, 1, mq, mk, mv, a);
+  if constexpr (kVar == 1)
+    e = launch_pdl(attn_tc_kernel<D>, grid, block, smem, stream, attr, 1, mq, mk, mv, a);
+  else if constexpr (kVar == 2)
+    e = launch_pdl(attn_pair_kernel<D>, grid, block, smem, stream, attr, 1, mq, mk, mv, a);
+  else
+    e = launch_pdl(attn_pair2_kernel<D>, grid, block, smem, stream, attr, 1, mq, mk, mv, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-void attn_tc_choice(int B, int Hkv, int D, int P, int N, const AttnPlan& plan, int* pair, int* splits) {
-  const int t_all = (P + N + kBN - 1) / kBN;
-  bool pr = false;
+void attn_tc_choice(int B, int Hkv, int D, int P, int N, const AttnPlan& plan, int* var, int* splits) {
   if (D == 64)
-    choose_plan<64>(B, Hkv, plan.mtiles, t_all, &pr, splits);
+    choose_plan<64>(B, Hkv, plan.mtiles, P, N, var, splits);
   else
-    choose_plan<128>(B, Hkv, plan.mtiles, t_all, &pr, splits);
-  *pair = pr ? 1 : 0;
+    choose_plan<128>(B, Hkv, plan.mtiles, P, N, var, splits);
 }
 
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* out, const int32_t* parent, int B,
                            int Hq, int Hkv, int D, int P, int N, int S, float scale, const AttnPlan& plan, char* ws,
                            int32_t* dev_status, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
-  if (!encode_3d(&mq, q, D, N, (long long)B * Hq, D, (long long)N * D, plan.nt)) return cudaErrorInvalidValue;
-  if (!encode_3d(&mk, k, D, P + N, (long long)B * Hkv, D, (long long)S * D, kBN)) return cudaErrorInvalidValue;
-  if (!encode_3d(&mv, v, D, P + N, (long long)B * Hkv, D, (long long)S * D, kBN)) return cudaErrorInvalidValue;
   TcArgs a;
   a.out = out;
   a.parent = parent;
@@ -1217,16 +1673,21 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* ou
   a.MT = plan.mtiles;
   a.c = scale * kLog2e;
   a.dev_status = dev_status;
-  const int t_all = (P + N + kBN - 1) / kBN;
-  bool pair = false;
-  if (D == 64)
-    choose_plan<64>(B, Hkv, plan.mtiles, t_all, &pair, &a.splits);
-  else
-    choose_plan<128>(B, Hkv, plan.mtiles, t_all, &pair, &a.splits);
-  if (pair) return D == 64 ? launch_tc_d<64, true>(mq, mk, mv, a, B, Hkv, stream)
-                           : launch_tc_d<128, true>(mq, mk, mv, a, B, Hkv, stream);
-  return D == 64 ? launch_tc_d<64, false>(mq, mk, mv, a, B, Hkv, stream)
-                 : launch_tc_d<128, false>(mq, mk, mv, a, B, Hkv, stream);
+  int var = 1;
+  attn_tc_choice(B, Hkv, D, P, N, plan, &var, &a.splits);
+  const int keys = tc_keys(var);  // KV tile rows of the chosen variant
+  CUtensorMap mq, mk, mv;
+  if (!encode_3d(&mq, q, D, N, (long long)B * Hq, D, (long long)N * D, plan.nt)) return cudaErrorInvalidValue;
+  if (!encode_3d(&mk, k, D, P + N, (long long)B * Hkv, D, (long long)S * D, keys)) return cudaErrorInvalidValue;
+  if (!encode_3d(&mv, v, D, P + N, (long long)B * Hkv, D, (long long)S * D, keys)) return cudaErrorInvalidValue;
+  if (D == 64) {
+    if (var == 1) return launch_tc_d<64, 1>(mq, mk, mv, a, B, Hkv, stream);
+    if (var == 2) return launch_tc_d<64, 2>(mq, mk, mv, a, B, Hkv, stream);
+    return launch_tc_d<64, 3>(mq, mk, mv, a, B, Hkv, stream);
+  }
+  if (var == 1) return launch_tc_d<128, 1>(mq, mk, mv, a, B, Hkv, stream);
+  if (var == 2) return launch_tc_d<128, 2>(mq, mk, mv, a, B, Hkv, stream);
+  return launch_tc_d<128, 3>(mq, mk, mv, a, B, Hkv, stream);
 }
 
 }  // namespace tv

@@ -83,8 +83,9 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype);
 cudaError_t launch_attn_simt(const void* q, const void* k, const void* v, void* out, const int32_t* parent,
                              int B, int Hq, int Hkv, int D, int P, int N, int S, float scale, tv_dtype dtype,
                              int32_t* dev_status, cudaStream_t stream);
-// kernel variant (1 = attn_pair_kernel) and KV splits the next launch would use
-void attn_tc_choice(int B, int Hkv, int D, int P, int N, const AttnPlan& plan, int* pair, int* splits);
+// kernel variant (1 attn_tc_kernel, 2 attn_pair_kernel, 3 attn_pair2_kernel) and KV
+// splits the next launch would use
+void attn_tc_choice(int B, int Hkv, int D, int P, int N, const AttnPlan& plan, int* var, int* splits);
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* out, const int32_t* parent,
                            int B, int Hq, int Hkv, int D, int P, int N, int S, float scale, const AttnPlan& plan,
                            char* ws, int32_t* dev_status, cudaStream_t stream);
