@@ -492,10 +492,17 @@ __global__ void __launch_bounds__(512, 1) vocab_pass_kernel(VocabArgs a) {
 
 constexpr int kTmaThreads = 512;
 constexpr int kTmaWarps = kTmaThreads / 32;
-constexpr int kPieceBytes = 32768;  // per array per stage: four 16-byte vectors per thread
-constexpr int kRingBytes = 196608;  // 6 stages (greedy) or 3 double stages (sampling)
-constexpr int kVpt = kPieceBytes / 16 / kTmaThreads;  // vectors per thread per piece
-constexpr int kMaxStages = kRingBytes / kPieceBytes;
+constexpr int kRingBytes = 196608;  // 3 stages of 64 KB (one array) or 3 double stages of 32 KB (two)
+constexpr int kGroupVec = 4;        // 16-byte vectors per thread reduced in one group
+// per array per stage: 64 KB (two groups of four vectors per thread) with one logits
+// array, 32 KB (one group) with target and draft arrays; three stages either way
+template <int kArrays>
+struct Pieces {
+  static constexpr int kBytes = kArrays == 1 ? 65536 : 32768;
+  static constexpr int kVpt = kBytes / 16 / kTmaThreads;  // vectors per thread per piece
+  static constexpr int kStages = kRingBytes / (kBytes * kArrays);
+};
+constexpr int kMaxStages = 3;
 
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -613,6 +620,9 @@ struct StreamAcc {
 template <typename T, int kArrays>
 __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArgs a) {
   extern __shared__ __align__(128) unsigned char ring[];
+  constexpr int kPieceBytes = Pieces<kArrays>::kBytes;
+  constexpr int kVpt = Pieces<kArrays>::kVpt;
+  static_assert(Pieces<kArrays>::kStages == kMaxStages, "three stages");
   __shared__ uint64_t full[kMaxStages];
   __shared__ int s_done[kMaxStages];
   __shared__ VocabPartial s_wp[kArrays][kMaxSeg][kTmaWarps];  // per-warp partials of each row segment
@@ -623,7 +633,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
   __shared__ int s_abort;
   constexpr int kE = kPieceBytes / (int)sizeof(T);  // elements per piece (a power of two)
   constexpr int kN = Vec16<T>::kN;                  // elements per 16-byte vector
-  constexpr int nst = kMaxStages / kArrays;
+  constexpr int nst = kMaxStages;
   static_assert(kVpt * 16 * kTmaThreads == kPieceBytes, "a piece is kVpt vectors per thread");
   static_assert(kMaxNodes <= 2 * kTmaThreads + 1, "each thread owns at most two children");
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -748,14 +758,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
     if (rem >= kE && (pc + 1 < npieces || last_full)) {
       // the whole piece lies in row u: vectors tid + v * kTmaThreads of every array
       const int col0 = (a.V - rem) + tid * kN;
-      uint4 u[kVpt];
+      // groups of four vectors per thread: vectors tid + v * kTmaThreads
 #pragma unroll
-      for (int v = 0; v < kVpt; ++v) u[v] = xv4[tid + v * kTmaThreads];
-      acc.template pushv<kVpt>(u, col0, kTmaThreads * kN, a.c2);
-      if (kArrays == 2) {
+      for (int g0 = 0; g0 < kVpt; g0 += kGroupVec) {
+        uint4 u[kGroupVec];
 #pragma unroll
-        for (int v = 0; v < kVpt; ++v) u[v] = yv4[tid + v * kTmaThreads];
-        accq.template pushv<kVpt>(u, col0, kTmaThreads * kN, a.c2);
+        for (int v = 0; v < kGroupVec; ++v) u[v] = xv4[tid + (g0 + v) * kTmaThreads];
+        acc.template pushv<kGroupVec>(u, col0 + g0 * kTmaThreads * kN, kTmaThreads * kN, a.c2);
+        if (kArrays == 2) {
+#pragma unroll
+          for (int v = 0; v < kGroupVec; ++v) u[v] = yv4[tid + (g0 + v) * kTmaThreads];
+          accq.template pushv<kGroupVec>(u, col0 + g0 * kTmaThreads * kN, kTmaThreads * kN, a.c2);
+        }
       }
       if (pc == next_cap) capture(pc, b, stage);
       rem -= kE;
