@@ -77,7 +77,7 @@ typedef enum tv_status {
   TV_ERR_DTYPE = -3,       /* unknown or unsupported dtype for this call */
   TV_ERR_WORKSPACE = -4,   /* workspace missing or smaller than the query says */
   TV_ERR_ALIGN = -5,       /* a pointer or stride breaks an alignment rule */
-  TV_ERR_UNSUPPORTED = -6, /* a combination this build does not implement */
+  TV_ERR_UNSUPPORTED = -6, /* a combination the library does not implement */
   TV_ERR_CUDA = -7,        /* a CUDA runtime/driver call failed while enqueueing */
   TV_ERR_VALUE = -8        /* a scalar argument is out of range (temperature, scale) */
 } tv_status;

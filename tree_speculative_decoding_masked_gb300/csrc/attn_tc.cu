@@ -2,7 +2,11 @@
 //
 // PTD §3.1: node i attends to the committed prefix and to its observable set pi(i);
 // TAPS §4.1: the selected subtree is verified by the target in one pass with tree
-// attention.  One CTA owns a tile of 128 query rows that share one KV head: the G query
+// attention.  Three kernels share this file: attn_tc_kernel (one 128-row tile per CTA,
+// described here), attn_pair_kernel (two row tiles per CTA) and attn_pair2_kernel (two
+// row tiles, 64-key KV tiles, two S buffers per row tile), each described where it is
+// defined; the host side at the end picks one per launch from a wave model.
+// attn_tc_kernel: one CTA owns a tile of 128 query rows that share one KV head: the G query
 // heads of a GQA group times NT = 128/G consecutive tree nodes (head-major rows), so each
 // K/V tile fetched from HBM by TMA is used by every node and every head of the group.
 // The key range [0, P + last node of the tile) is cut into KV splits across CTAs.
