@@ -204,6 +204,10 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
     const size_t rowp = ((size_t)b * N + u) * (size_t)V;
     const float l2p = s_l2p[u];
     const float l2q = s_l2q[u];
+    // thread 0: raw logits of the next child's token, loaded while the rejection pass
+    // before its decision runs (off the decision's critical path)
+    float pre_x = 0.f, pre_y = 0.f;
+    bool pre_ok = false;
     for (int k = 1; k <= m; ++k) {
       const int c = s_kids[k - 1];
       if (tid == 0) {
@@ -213,8 +217,10 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
           pt = s_pc[c];
           qt = s_qc[c];
         } else {
-          const float p0 = ptx::ex2(fmaf(ld_logit<T>(a.target, rowp + t), a.c2, -l2p));
-          const float q0 = ptx::ex2(fmaf(ld_logit<T>(a.draft, rowp + t), a.c2, -l2q));
+          const float xt = pre_ok ? pre_x : ld_logit<T>(a.target, rowp + t);
+          const float yt = pre_ok ? pre_y : ld_logit<T>(a.draft, rowp + t);
+          const float p0 = ptx::ex2(fmaf(xt, a.c2, -l2p));
+          const float q0 = ptx::ex2(fmaf(yt, a.c2, -l2q));
           eval_pq(res, t, p0, q0, pt, qt);
         }
         const float r = philox_uniform(a.seed, a.round, b, u, k, 0);
@@ -224,6 +230,18 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
       }
       __syncthreads();
       if (s_dec) break;
+      // loads thread 0 needs after the pass, issued before it: the rejected token's draft
+      // logit and the next child's two logits
+      float rej_y = 0.f;
+      if (tid == 0) {
+        rej_y = ld_logit<T>(a.draft, rowp + s_tok[c]);
+        pre_ok = k < m;
+        if (pre_ok) {
+          const int tn = s_tok[s_kids[k]];
+          pre_x = ld_logit<T>(a.target, rowp + tn);
+          pre_y = ld_logit<T>(a.draft, rowp + tn);
+        }
+      }
       // rejection of t_k: Z = sum_v (P(v) - Q(v))+ with the current (P, Q)
       unsigned long long zs = 0;
       for (int vb = vlo + tid; vb < vhi; vb += kBatch * blockDim.x) {
@@ -251,7 +269,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
         const double z = (double)zall * 0x1p-56;
         const int j = res.nrej;
         const int t = s_tok[c];
-        const float q0 = ptx::ex2(fmaf(ld_logit<T>(a.draft, rowp + t), a.c2, -l2q));
+        const float q0 = ptx::ex2(fmaf(rej_y, a.c2, -l2q));
         res.tok[j] = t;
         res.invz[j] = z > 0.0 ? (float)(1.0 / z) : 0.f;
         const float dprev = res.invd[j] > 0.f ? 1.f / res.invd[j] : 0.f;
