@@ -515,7 +515,8 @@ def run_ours(args):
     # fastest step (the whole device for both, or disjoint parts so both grids are
     # resident together)
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    parts = [(0, 0)] + [(v, n_sm - v) for v in (n_sm // 4, n_sm // 3, n_sm // 2, 2 * n_sm // 3)]
+    parts = [(0, 0)] + [(v, n_sm - v) for v in (n_sm // 4, n_sm // 3, 5 * n_sm // 12, n_sm // 2,
+                                                   7 * n_sm // 12, 2 * n_sm // 3)]
     if bf16:
         # when the whole-device attention grid leaves SMs free, give exactly those to verify
         tv.set_sm_partition(0, 0)
