@@ -93,6 +93,18 @@ TV_API const char* tv_status_string(int status);
 /* Library ABI version: (major << 16) | minor. */
 TV_API int tv_version(void);
 
+/* tv_philox4x32_10 - the counter-based generator that tv_verify_sample draws its
+ * uniforms from: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers:
+ * as easy as 1, 2, 3", SC'11), key = seed split into (low, high) 32-bit words.
+ *   counters [n][4] uint32 (device), out [n][4] uint32 (device): the four output words of
+ *   each counter.  The sampling walk's draw k of kind `kind` at node u of sequence b in
+ *   round r uses counter (r mod 2^32, b, u, 2k + kind) and the uniform (x0 >> 8) * 2^-24.
+ * Errors: n < 0 -> TV_ERR_SHAPE; NULL arrays with n > 0 -> TV_ERR_NULL; arrays not 16-byte
+ * aligned -> TV_ERR_ALIGN.
+ */
+TV_API tv_status tv_philox4x32_10(uint64_t seed, const uint32_t* counters, int n, uint32_t* out,
+                                  tv_stream_t stream);
+
 /* tv_selftest_bounded_wait - exercise the failure path of the in-kernel bounded waits.
  * (No counterpart in the pages: it checks this library's own failure detection.)  One
  * warp waits on an mbarrier phase that nothing completes, through the same bounded wait

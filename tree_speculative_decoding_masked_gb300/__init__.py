@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     frontier_topw,
     library_path,
     load_library,
+    philox4x32_10,
     prune_tree,
     select_subtree,
     select_workspace_size,

@@ -41,6 +41,7 @@ _SIGS = {
     "tv_status_string": (ctypes.c_char_p, [_I]),
     "tv_version": (_I, []),
     "tv_selftest_bounded_wait": (_I, [_I, _P, _P]),
+    "tv_philox4x32_10": (_I, [_U64, _P, _I, _P, _P]),
     "tv_set_sm_partition": (_I, [_I, _I]),
     "tv_set_attention_variant": (_I, [_I]),
     "tv_set_attention_splits": (_I, [_I]),
@@ -146,6 +147,17 @@ def _status_tensor(dev_status, device):
 def set_sm_partition(verify_sms: int, attention_sms: int):
     """SM shares for running tree_attention and verify_* concurrently (0, 0 = whole device)."""
     _check("tv_set_sm_partition", load_library().tv_set_sm_partition(int(verify_sms), int(attention_sms)))
+
+
+def philox4x32_10(seed: int, counters):
+    """Philox4x32-10 words of counters [n][4] (CUDA int32 tensor, read as uint32) under
+    the 64-bit key `seed`: the sampling walk's generator.  Returns [n][4] int32 (bits)."""
+    _need_cuda(counters=counters)
+    n = counters.shape[0]
+    out = torch.empty_like(counters)
+    _check("tv_philox4x32_10", load_library().tv_philox4x32_10(ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF),
+                                                               _ptr(counters), n, _ptr(out), _stream()))
+    return out
 
 
 def selftest_bounded_wait(wait_us: int, dev_status):

@@ -60,6 +60,13 @@ const char* tv_status_string(int s) {
 
 int tv_version(void) { return (1 << 16) | 0; }
 
+tv_status tv_philox4x32_10(uint64_t seed, const uint32_t* counters, int n, uint32_t* out, tv_stream_t stream) {
+  if (n < 0) return TV_ERR_SHAPE;
+  if (n > 0 && (!counters || !out)) return TV_ERR_NULL;
+  if (!aligned16(counters) || !aligned16(out)) return TV_ERR_ALIGN;
+  return cuda_status(launch_philox_words(seed, counters, n, out, st(stream)));
+}
+
 tv_status tv_selftest_bounded_wait(int wait_us, int32_t* dev_status, tv_stream_t stream) {
   if (!dev_status) return TV_ERR_NULL;
   if (wait_us < 1 || wait_us > 1000000) return TV_ERR_VALUE;

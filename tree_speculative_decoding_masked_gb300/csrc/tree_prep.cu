@@ -3,6 +3,7 @@
 // PTD (Progressive Tree Drafting) §3.1 "tree construction": node v may attend only to
 // its observable prefix set pi(v) = {v} U pi(P(v)); its position encoding is fixed by
 // |pi(v)|.  One CTA of 1024 threads per sequence; parent[] lives in shared memory.
+#include "philox.cuh"
 #include "tv_kernels.cuh"
 #include "tv_ptx.cuh"
 
@@ -127,6 +128,21 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns, int32_t* dev_status) {
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* dev_status, cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, dev_status);
+  return cudaGetLastError();
+}
+
+// Philox4x32-10 words of caller-given counters under one 64-bit key: the generator the
+// sampling walk draws its uniforms from, exposed so that draws can be reproduced.
+__global__ void philox_words_kernel(uint64_t seed, const uint32_t* __restrict__ ctr, int n, uint32_t* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint4 c = reinterpret_cast<const uint4*>(ctr)[i];
+  const Philox4 r = philox4x32_10(c.x, c.y, c.z, c.w, (uint32_t)seed, (uint32_t)(seed >> 32));
+  reinterpret_cast<uint4*>(out)[i] = make_uint4(r.x[0], r.x[1], r.x[2], r.x[3]);
+}
+
+cudaError_t launch_philox_words(uint64_t seed, const uint32_t* ctr, int n, uint32_t* out, cudaStream_t stream) {
+  if (n > 0) philox_words_kernel<<<(n + 255) / 256, 256, 0, stream>>>(seed, ctr, n, out);
   return cudaGetLastError();
 }
 

@@ -29,6 +29,9 @@ cudaError_t launch_sample_walk(const void* target, const void* draft, const int3
                                int32_t* accepted, int32_t* accept_len, int32_t* out_token,
                                int32_t* dev_status, cudaStream_t stream);
 
+// ---- Philox4x32-10 words (the sampling walk's generator)
+cudaError_t launch_philox_words(uint64_t seed, const uint32_t* ctr, int n, uint32_t* out, cudaStream_t stream);
+
 // ---- bounded-wait self-test
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* dev_status, cudaStream_t stream);
 
