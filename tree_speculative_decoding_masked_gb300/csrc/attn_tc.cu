@@ -1519,8 +1519,7 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) 
   if (!p.tc) return p;
   p.nt = (kRows / G) / 8 * 8;
   p.mtiles = (N + p.nt - 1) / p.nt;
-  p.pair = 0;    // kernel variant and KV splits are chosen at launch (choose_plan)
-  p.splits = 1;
+  // the kernel variant and the KV splits are chosen at launch (choose_plan)
   p.total = 0;   // split partials stay in the cluster's shared memory
   return p;
 }

@@ -78,8 +78,6 @@ struct AttnPlan {
   bool tc;        // tensor-core (tcgen05) kernel
   int nt;         // nodes per 128-row tile (tc)
   int mtiles;     // row tiles per (b, kv head)
-  int pair;       // unused at plan time: the variant is chosen at launch
-  int splits;     // unused at plan time: the KV splits are chosen at launch
   size_t total;   // workspace bytes (0: partials stay in the cluster's shared memory)
 };
 AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype);
