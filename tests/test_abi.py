@@ -108,3 +108,27 @@ def test_binding_has_no_cpu_fallback(monkeypatch):
     monkeypatch.setattr(bnd, "_LIB_PATH", "/nonexistent/libtreeverify.so")
     with pytest.raises(RuntimeError, match="not found"):
         bnd.load_library()
+
+
+def test_settings_and_utility_host_validation(lib):
+    # process-wide settings: out-of-range values are refused, valid ones accepted
+    assert lib.tv_set_attention_variant(4) == -8
+    assert lib.tv_set_attention_variant(-1) == -8
+    assert lib.tv_set_attention_splits(9) == -8
+    assert lib.tv_set_sm_partition(-1, 0) == -8
+    for v in (3, 0):
+        assert lib.tv_set_attention_variant(v) == 0
+    assert lib.tv_set_attention_splits(0) == 0
+    # the attention plan query checks its arguments before asking the device anything
+    out = ctypes.c_int(0)
+    assert lib.tv_tree_attention_plan(1, 32, 8, 128, 2048, 64, 1, NULL, ctypes.byref(out)) == -1
+    assert lib.tv_tree_attention_plan(1, 32, 8, 128, 2048, 64, 9, ctypes.byref(out), ctypes.byref(out)) == -3
+    assert lib.tv_tree_attention_plan(1, 30, 8, 128, 2048, 64, 1, ctypes.byref(out), ctypes.byref(out)) == -2
+    # Philox words: sizes, pointers, alignment
+    assert lib.tv_philox4x32_10(1, FAKE, -1, FAKE, NULL) == -2
+    assert lib.tv_philox4x32_10(1, NULL, 4, FAKE, NULL) == -1
+    assert lib.tv_philox4x32_10(1, ctypes.c_void_p(0x1004), 4, FAKE, NULL) == -5
+    # bounded-wait self-test: a status word is required and the limit is bounded
+    assert lib.tv_selftest_bounded_wait(1000, NULL, NULL) == -1
+    assert lib.tv_selftest_bounded_wait(0, FAKE, NULL) == -8
+    assert lib.tv_selftest_bounded_wait(1000001, FAKE, NULL) == -8
