@@ -135,3 +135,68 @@ def test_inverse_cdf_boundaries():
     assert sampling.inverse_cdf(p, 0.7499)[0] == 2
     assert sampling.inverse_cdf(p, 0.75)[0] == 3
     assert sampling.inverse_cdf(p, 1.0 - 2 ** -24)[0] == 3
+
+
+def _two_token_hist(p1_logits, p2_logits, q1_logits, q2_logits, m1, m2, n_rounds, seed):
+    """Root with m1 drafted children, each with m2 drafted children; the target and draft
+    rows of a depth-1 node depend on its token.  Returns the joint histogram of the first
+    two tokens of the generated text: the round's accepted tokens and its final token,
+    topped up, when the round ends after one token, by one plain target step from the
+    context that token makes."""
+    g = synth.rng(seed)
+    v = len(p1_logits)
+    parent = [-1] + [0] * m1
+    for c in range(1, m1 + 1):
+        parent += [c] * m2
+    parent = np.array(parent, dtype=np.int32)
+    n = len(parent)
+
+    def probs(logits):
+        z = logits.astype(np.float64)
+        w = np.exp(z - z.max())
+        return w / w.sum()
+
+    hist = np.zeros((v, v), dtype=np.int64)
+    for rnd in range(n_rounds):
+        tok = np.zeros(n, dtype=np.int32)
+        tok[1:m1 + 1] = g.choice(v, size=m1, replace=False, p=probs(q1_logits))
+        rows_t = np.empty((n, v), dtype=np.float32)
+        rows_d = np.empty((n, v), dtype=np.float32)
+        rows_t[0], rows_d[0] = p1_logits, q1_logits
+        for c in range(1, m1 + 1):
+            rows_t[c], rows_d[c] = p2_logits[tok[c]], q2_logits[tok[c]]
+            kids = np.flatnonzero(parent == c)
+            tok[kids] = g.choice(v, size=m2, replace=False, p=probs(q2_logits[tok[c]]))
+            for k in kids:
+                # Depth-2 rows are never read for a decision about the first two tokens.
+                rows_t[k], rows_d[k] = p1_logits, q1_logits
+        acc, last, _, _ = sampling.sampling_walk(rows_t, rows_d, parent, tok, 1.0, seed, rnd, 0)
+        out = [int(tok[c]) for c in acc] + [int(last)]
+        if len(out) == 1:
+            out.append(int(g.choice(v, p=probs(p2_logits[out[0]]))))
+        hist[out[0], out[1]] += 1
+    return hist
+
+
+def test_first_two_tokens_follow_the_target_joint():
+    # Losslessness one level down the tree: after an acceptance the walk restarts at the
+    # accepted child with that child's rows, so the first two generated tokens follow
+    # p1(x1) p2(x2 | x1) whatever the drafter does at either level.
+    v, n = 4, 16000
+    g = synth.rng(41)
+    p1 = synth.normal(g, v, std=1.0)
+    p2 = np.stack([synth.normal(g, v, std=1.0) for _ in range(v)])
+    q1 = (p1 + synth.normal(g, v, std=1.0)).astype(np.float32)
+    q2 = (p2 + np.stack([synth.normal(g, v, std=1.0) for _ in range(v)])).astype(np.float32)
+    hist = _two_token_hist(p1, p2, q1, q2, 2, 2, n, seed=43)
+    sp1 = sampling.softmax_row(p1, 1.0)
+    joint = np.stack([sp1[a] * sampling.softmax_row(p2[a], 1.0) for a in range(v)])
+    expect = n * joint
+    assert expect.min() >= 5.0
+    crit = stats.chi2.ppf(1 - 1e-3, df=v * v - 1)
+    chi2 = float(np.sum((hist - expect) ** 2 / expect))
+    assert chi2 < crit, (chi2, crit, hist, expect)
+    # Power of the check: the same counts fail against a joint whose second token
+    # ignores the first (every context's row replaced by the first context's row).
+    wrong = n * np.outer(sp1, sampling.softmax_row(p2[0], 1.0))
+    assert float(np.sum((hist - wrong) ** 2 / wrong)) > crit
