@@ -204,10 +204,19 @@ TV_API tv_status tv_prune_tree(const int32_t* parent, const float* conf, int B, 
  *   parent        [B][N] int32
  *   scale         softmax scale (> 0); pass 0 for 1/sqrt(D).
  * Precision: fp32 in/out with fp32 math, or bf16 in/out with fp32 softmax and fp32
- * accumulation (tensor cores).  Limits: N <= 1024, D in {64, 128} for bf16 tensor-core
- * tiles (other D <= 256, D % 32 == 0 run the CUDA-core kernel), Hq % Hkv == 0.
+ * accumulation.  Limits: 1 <= N <= 1024, 32 <= D <= 256 with D % 32 == 0, Hq % Hkv == 0.
+ * bf16 with D in {64, 128}, G <= 16 and G * N >= 64 runs on the tensor cores; every
+ * other case (fp32, other D, small trees) runs on the CUDA-core kernel.
  * Alignment: q, k_cache, v_cache, out 16-byte aligned.
- * Workspace: tv_tree_attention_workspace_size(...) bytes (split-KV partials).
+ * Workspace: tv_tree_attention_workspace_size(...) bytes; that is 0 for every shape the
+ * library takes today (split-KV partials are merged through the thread-block cluster's
+ * distributed shared memory), and workspace may then be NULL.
+ * Errors: NULL pointers -> TV_ERR_NULL; dtype -> TV_ERR_DTYPE; sizes, B * Hkv or the
+ * grid outside the launch limits -> TV_ERR_SHAPE; scale < 0, NaN or infinite ->
+ * TV_ERR_VALUE; misaligned pointers -> TV_ERR_ALIGN; a workspace smaller than the
+ * query -> TV_ERR_WORKSPACE; a failed launch -> TV_ERR_CUDA.  Tree structure problems
+ * found on the device (node 0 not a root, or a parent index not below its node) and a
+ * bounded wait that ran out are written to *dev_status.
  */
 TV_API size_t tv_tree_attention_workspace_size(int B, int Hq, int Hkv, int D, int P, int N,
                                         tv_dtype dtype);
