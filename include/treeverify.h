@@ -375,13 +375,18 @@ TV_API tv_status tv_expand_children(const void* draft_logits, const float* paren
  * the largest sum of s among prefix-closed sets of its size.
  *   marg          [B][d][K] float, each position sorted by (prob desc, token asc), >= 0
  *   pool_tokens   [B][d][K] int32
- *   root_token    [B] int32 (device)
+ *   root_token    [B] int32 (device; may be NULL, the root's token is then -1)
  *   parent, tokens, depth [B][budget] int32 out, score [B][budget] float out: nodes in
  *                 selection order (parent < child), root = row 0 (score 1, depth 0);
  *                 rows past n_nodes hold -1 (score 0)
- *   n_nodes       [B] int32 out: 1 + number of selected candidates
+ *   n_nodes       [B] int32 out: 1 + number of selected candidates (may be NULL)
  * Limits: 1 <= d <= 16, 1 <= K <= 256, 1 <= budget <= 4096.
- * Workspace: tv_select_workspace_size(...) bytes.
+ * Workspace: tv_select_workspace_size(...) bytes (0 today: the kernel works in shared
+ * memory; workspace may then be NULL).
+ * Errors: NULL marg, pool_tokens or outputs -> TV_ERR_NULL; sizes -> TV_ERR_SHAPE;
+ * ws_bytes below the query -> TV_ERR_WORKSPACE; a failed launch -> TV_ERR_CUDA.  A
+ * marginal outside [0, 1] (NaN included) or a position not sorted by descending
+ * marginal sets TV_DEV_BAD_TOKEN; pool tokens are copied to the output unchecked.
  */
 TV_API size_t tv_select_workspace_size(int B, int d, int K, int budget);
 TV_API tv_status tv_select_subtree(const float* marg, const int32_t* pool_tokens, int B, int d, int K,
@@ -402,7 +407,8 @@ TV_API tv_status tv_select_subtree(const float* marg, const int32_t* pool_tokens
  * the ratio is an IEEE double division (so the choice does not depend on summation
  * order).  cost_base, cost_per_row: a line fitted to measured verification time
  * against tree rows (any unit, same for both).  Rows past n* hold -1 (score 0) and
- * n_nodes[b] = n*.  Other arguments, limits and workspace as tv_select_subtree.
+ * n_nodes[b] = n*.  Other arguments, limits and workspace as tv_select_subtree, except
+ * that n_nodes is required.
  * Host errors: cost_base < 0, cost_per_row <= 0 or not finite -> TV_ERR_VALUE.
  */
 TV_API tv_status tv_select_subtree_adaptive(const float* marg, const int32_t* pool_tokens, int B, int d,
