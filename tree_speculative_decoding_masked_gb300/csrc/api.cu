@@ -2,24 +2,28 @@
 // Nothing here allocates device memory, synchronises the stream or throws.
 #include <math.h>
 
+#include <atomic>
+
 #include "tv_kernels.cuh"
 
 using namespace tv;
 
+// Process-wide settings, read at every launch (atomics: another host thread may change
+// them while launches are being made).
 // SM shares for running the vocab pass and the tree attention concurrently (0 = all SMs)
-static int g_sm_verify = 0, g_sm_attention = 0;
+static std::atomic<int> g_sm_verify{0}, g_sm_attention{0};
 // tensor-core attention kernel: 0 automatic, 1 one row tile per CTA, 2 paired row tiles,
 // 3 paired row tiles with 64-key KV tiles and double-buffered S
-static int g_attn_variant = 0;
+static std::atomic<int> g_attn_variant{0};
 // KV splits per tensor-core attention CTA group: 0 automatic, else forced (capped at the
 // KV tile count and the cluster limit)
-static int g_attn_splits = 0;
+static std::atomic<int> g_attn_splits{0};
 
 namespace tv {
-int sm_share_verify() { return g_sm_verify; }
-int sm_share_attention() { return g_sm_attention; }
-int attention_variant() { return g_attn_variant; }
-int attention_splits() { return g_attn_splits; }
+int sm_share_verify() { return g_sm_verify.load(std::memory_order_relaxed); }
+int sm_share_attention() { return g_sm_attention.load(std::memory_order_relaxed); }
+int attention_variant() { return g_attn_variant.load(std::memory_order_relaxed); }
+int attention_splits() { return g_attn_splits.load(std::memory_order_relaxed); }
 }  // namespace tv
 
 namespace {
@@ -75,20 +79,20 @@ tv_status tv_selftest_bounded_wait(int wait_us, int32_t* dev_status, tv_stream_t
 
 tv_status tv_set_sm_partition(int verify_sms, int attention_sms) {
   if (verify_sms < 0 || attention_sms < 0) return TV_ERR_VALUE;
-  g_sm_verify = verify_sms;
-  g_sm_attention = attention_sms;
+  g_sm_verify.store(verify_sms, std::memory_order_relaxed);
+  g_sm_attention.store(attention_sms, std::memory_order_relaxed);
   return TV_OK;
 }
 
 tv_status tv_set_attention_variant(int variant) {
   if (variant < 0 || variant > 3) return TV_ERR_VALUE;
-  g_attn_variant = variant;
+  g_attn_variant.store(variant, std::memory_order_relaxed);
   return TV_OK;
 }
 
 tv_status tv_set_attention_splits(int splits) {
   if (splits < 0 || splits > 8) return TV_ERR_VALUE;
-  g_attn_splits = splits;
+  g_attn_splits.store(splits, std::memory_order_relaxed);
   return TV_OK;
 }
 

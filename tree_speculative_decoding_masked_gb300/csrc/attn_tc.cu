@@ -31,6 +31,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "tv_kernels.cuh"
 #include "tv_ptx.cuh"
@@ -1543,16 +1544,13 @@ constexpr int tc_keys(int var) { return var == 3 ? kBN2 : kBN; }  // keys per KV
 // device (cached per device, variant and s).
 template <int D, int kVar>
 static int max_active_clusters(int s) {
-  static int cache[64][kMaxSplits + 1];  // one table per template instance
-  static bool init = false;
-  if (!init) {
-    for (auto& row : cache)
-      for (int& v : row) v = -1;
-    init = true;
-  }
+  // one table per template instance: 0 = not queried yet, else the count + 1; threads that
+  // query at the same time store the same value
+  static std::atomic<int> cache[64][kMaxSplits + 1];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev][s] >= 0) return cache[dev][s];
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || s < 1 || s > kMaxSplits) return 0;
+  const int known = cache[dev][s].load(std::memory_order_relaxed);
+  if (known > 0) return known - 1;
   const void* fn = tc_kernel_fn<D, kVar>();
   const int smem = tc_smem<D, kVar>();
   int n = 0;
@@ -1570,7 +1568,7 @@ static int max_active_clusters(int s) {
     cfg.numAttrs = 1;
     if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
   }
-  cache[dev][s] = n;
+  cache[dev][s].store(n + 1, std::memory_order_relaxed);
   return n;
 }
 

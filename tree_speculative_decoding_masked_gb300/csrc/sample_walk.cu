@@ -16,6 +16,8 @@
 // a 64-bit integer, so a total does not depend on the order of the additions and every
 // CTA, after reading the others' partial sums through distributed shared memory, holds
 // the same value.
+#include <atomic>
+
 #include "philox.cuh"
 #include "tv_kernels.cuh"
 #include "tv_ptx.cuh"
@@ -382,11 +384,14 @@ cudaError_t launch_sample_walk(const void* target, const void* draft, const int3
   a.out_token = out_token;
   a.dev_status = dev_status;
   // 16 CTAs per cluster where the device can co-schedule them, else the portable 8
-  static int csize_cache[64][2] = {};  // per device and element type (each kernel has its own attribute)
+  // per device and element type (each kernel has its own attribute); 0 = not queried yet.
+  // The release store follows the attribute change, so a thread that reads 16 launches
+  // after the attribute is in place.
+  static std::atomic<int> csize_cache[64][2];
   int dev = 0;
   cudaGetDevice(&dev);
   const int ti = dtype == TV_BF16 ? 1 : 0;
-  int csize = (dev >= 0 && dev < 64) ? csize_cache[dev][ti] : 0;
+  int csize = (dev >= 0 && dev < 64) ? csize_cache[dev][ti].load(std::memory_order_acquire) : 0;
   if (csize == 0) {
     csize = 8;
     auto kern = dtype == TV_BF16 ? sample_walk_kernel<uint16_t> : sample_walk_kernel<float>;
@@ -406,7 +411,7 @@ cudaError_t launch_sample_walk(const void* target, const void* draft, const int3
         csize = kWalkClusterMax;
     }
     cudaGetLastError();  // a refused query leaves the portable size
-    if (dev >= 0 && dev < 64) csize_cache[dev][ti] = csize;
+    if (dev >= 0 && dev < 64) csize_cache[dev][ti].store(csize, std::memory_order_release);
   }
   a.csize = csize;
   cudaLaunchConfig_t cfg = {};

@@ -16,6 +16,7 @@
 #include "tv_ptx.cuh"
 
 #include <algorithm>
+#include <atomic>
 
 namespace tv {
 
@@ -913,16 +914,18 @@ size_t verify_ws_layout(int B, int N, int V, int sampling, VerifyWs* w) {
 
 template <typename T, bool kVec>
 static int resident_ctas() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];  // 0 = not queried yet
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152 * 4;
-  if (!cache[dev]) {
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (!n) {
     int per_sm = 0, sms = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vocab_pass_kernel<T, kVec>, kVocabThreads, 0);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cache[dev] = per_sm > 0 && sms > 0 ? per_sm * sms : 152 * 4;
+    n = per_sm > 0 && sms > 0 ? per_sm * sms : 152 * 4;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 static void plan_grid(VocabArgs& a, long long G) {
@@ -950,14 +953,14 @@ static cudaError_t launch_vocab_t(VocabArgs a, cudaStream_t stream) {
 
 template <typename T, int kArrays>
 static cudaError_t launch_vocab_tma(VocabArgs a, cudaStream_t stream) {
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // false until the attribute is set on that device
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(vocab_pass_tma_kernel<T, kArrays>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sm_share_verify() > 0) sms = std::min(sms, sm_share_verify());
