@@ -73,3 +73,32 @@ def test_defaults_are_one_gpu_and_the_headline_workload():
     a = bench.parse_args([])
     assert a.gpus == 1 and a.impl == "ours" and a.warmup >= 3
     assert a.workload == bench.DEFAULT_WORKLOAD
+
+
+@pytest.mark.parametrize("workload", [None, "tiny_fp32", "budget_sweep"])
+def test_reference_arm_prints_one_complete_json_line(monkeypatch, capsys, workload):
+    # The oracle arm's line carries every key of the bench contract, with its own value
+    # repeated as cpu_baseline and e2e and no host<->device bytes.
+    sys.path.insert(0, ROOT)
+    import bench
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    argv = ["--impl", "reference", "--steps", "2", "--warmup", "0"]
+    if workload:
+        argv += ["--workload", workload]
+    bench.run_reference(bench.parse_args(argv))
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 0
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
+    assert d["config"]["workload"] == (workload or bench.DEFAULT_WORKLOAD)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert cb["unit"] == d["unit"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
