@@ -411,10 +411,11 @@ TV_API tv_status tv_select_subtree(const float* marg, const int32_t* pool_tokens
  * that n_nodes is required.
  * Handing the tree on: tv_tree_prep, tv_tree_attention and tv_verify_* take one N for
  * every sequence of a call and flag a parent of -1 below row 0 as TV_DEV_BAD_TREE, so
- * the padded rows past n_nodes[b] are not passed on: call them with N = n_nodes[b]
- * (one call per group of sequences with equal n_nodes, the leading N rows of each
- * output array, row stride N).  The same holds for tv_select_subtree whenever the
- * candidate tree holds fewer than budget - 1 nodes.
+ * the padded rows past n_nodes[b] are not passed on: call them with N = n_nodes[b].
+ * A call for one sequence can pass the first N rows of its output rows directly; a call
+ * for several sequences with equal n_nodes needs their first N rows packed with row
+ * stride N.  The same holds for tv_select_subtree whenever the candidate tree holds
+ * fewer than budget - 1 nodes.
  * Host errors: cost_base < 0, cost_per_row <= 0 or not finite -> TV_ERR_VALUE.
  */
 TV_API tv_status tv_select_subtree_adaptive(const float* marg, const int32_t* pool_tokens, int B, int d,
