@@ -33,6 +33,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+# BLAS / OpenMP pool sizes of the oracle runs: one host core, as their lines report
+ORACLE_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS")
+if __name__ == "__main__" and ("--impl=reference" in sys.argv[1:] or any(
+        a == "--impl" and b == "reference" for a, b in zip(sys.argv[1:], sys.argv[2:]))):
+    for _var in ORACLE_THREAD_VARS:  # before NumPy is first imported
+        os.environ[_var] = "1"
+
 METRIC = "verified tree nodes/sec (attn+accept) and achieved HBM GB/s vs GB300 peak"
 UNIT = "nodes/s"
 DEFAULT_WORKLOAD = "qwen3_4b_layer"
@@ -160,7 +167,7 @@ def oracle_worker(budget_s: float, workload: str):
 
 def run_oracle_subprocess(budget_s: float, workload: str) -> dict:
     env = dict(os.environ)
-    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+    for var in ORACLE_THREAD_VARS:
         env[var] = "1"
     env.pop("RANK", None)
     env.pop("WORLD_SIZE", None)
