@@ -132,3 +132,58 @@ def test_settings_and_utility_host_validation(lib):
     assert lib.tv_selftest_bounded_wait(1000, NULL, NULL) == -1
     assert lib.tv_selftest_bounded_wait(0, FAKE, NULL) == -8
     assert lib.tv_selftest_bounded_wait(1000001, FAKE, NULL) == -8
+
+
+class _FakeCuda:
+    """Stands in for a CUDA tensor so that the binding's checks of caller-supplied
+    outputs can be reached on a machine without a GPU (nothing is launched)."""
+
+    def __init__(self, shape, dtype):
+        import torch
+        self.shape = shape
+        self.dtype = dtype
+        self.is_cuda = True
+        self.device = torch.device("cpu")
+
+    def is_contiguous(self):
+        return True
+
+    def numel(self):
+        n = 1
+        for x in self.shape:
+            n *= x
+        return n
+
+    def element_size(self):
+        import torch
+        return torch.empty((), dtype=self.dtype).element_size()
+
+
+def test_binding_refuses_host_tensors_everywhere(lib):
+    # No CPU fallback: host tensors are refused as inputs, outputs, status words and
+    # workspaces before anything reaches the library.
+    import torch
+    import tree_speculative_decoding_masked_gb300 as tv
+    cpu_i32 = torch.zeros((1, 4), dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        tv.verify_greedy(torch.zeros((1, 4, 8)), cpu_i32, cpu_i32)
+    with pytest.raises(ValueError, match="CUDA"):
+        tv.tree_prep(cpu_i32, 0)
+    with pytest.raises(ValueError, match="CUDA"):
+        tv.select_subtree(torch.zeros((1, 2, 2)), torch.zeros((1, 2, 2), dtype=torch.int32), 4,
+                          torch.zeros(1, dtype=torch.int32))
+    logits = _FakeCuda((1, 4, 8), torch.float32)
+    par, tok = _FakeCuda((1, 4), torch.int32), _FakeCuda((1, 4), torch.int32)
+    with pytest.raises(ValueError, match=r"out\['accept_len'\] must be a CUDA tensor"):
+        tv.verify_greedy(logits, par, tok, out={"accept_len": torch.zeros(1, dtype=torch.int32)})
+    with pytest.raises(ValueError, match="workspace must be a CUDA tensor"):
+        tv.verify_greedy(logits, par, tok, out={k: _FakeCuda((1, 4), torch.int32) for k in
+                                                 ("accepted_nodes", "accept_len", "bonus_token", "p_draft")},
+                         workspace=torch.zeros(1 << 20, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="dev_status must be a CUDA tensor"):
+        tv.verify_greedy(logits, par, tok, out={k: _FakeCuda((1, 4), torch.int32) for k in
+                                                 ("accepted_nodes", "accept_len", "bonus_token", "p_draft")},
+                         workspace=_FakeCuda((1 << 20,), torch.uint8), dev_status=torch.zeros(1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        tv.frontier_topw(_FakeCuda((1, 8), torch.float32), _FakeCuda((1,), torch.int32), 2,
+                         out=torch.zeros((1, 2), dtype=torch.int32))

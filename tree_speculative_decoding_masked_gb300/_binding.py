@@ -126,6 +126,8 @@ def _need_cuda(**tensors):
 
 def _workspace(nbytes: int, device, workspace):
     if workspace is not None:
+        if not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA tensor")
         if workspace.numel() * workspace.element_size() < nbytes:
             raise ValueError("workspace smaller than the library's query")
         return workspace
@@ -134,11 +136,19 @@ def _workspace(nbytes: int, device, workspace):
 
 def _out(o, key, shape, dtype, device):
     t = o.get(key)
-    return t if t is not None else torch.empty(shape, dtype=dtype, device=device)
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    if not t.is_cuda:
+        raise ValueError(f"out[{key!r}] must be a CUDA tensor")
+    return t
 
 
 def _status_tensor(dev_status, device):
-    return dev_status if dev_status is not None else torch.zeros(1, dtype=torch.int32, device=device)
+    if dev_status is None:
+        return torch.zeros(1, dtype=torch.int32, device=device)
+    if not dev_status.is_cuda:
+        raise ValueError("dev_status must be a CUDA tensor")
+    return dev_status
 
 
 # ------------------------------------------------------------------------------------
@@ -274,7 +284,7 @@ def commit_accepted_kv(k_cache, v_cache, accepted_nodes, accept_len, prefix_len:
 def frontier_topw(scores, count, width: int, *, dev_status=None, out=None):
     """TreeGraft §3.1 frontier: positions of the `width` highest of scores[b][:count[b]]
     (scores [B][C] float32, count [B] int32); ties to the lower position."""
-    _need_cuda(scores=scores, count=count)
+    _need_cuda(scores=scores, count=count, out=out)
     lib = load_library()
     B, C = scores.shape
     idx = out if out is not None else torch.empty(B, width, dtype=torch.int32, device=scores.device)
