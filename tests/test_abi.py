@@ -174,15 +174,19 @@ def test_binding_refuses_host_tensors_everywhere(lib):
                           torch.zeros(1, dtype=torch.int32))
     logits = _FakeCuda((1, 4, 8), torch.float32)
     par, tok = _FakeCuda((1, 4), torch.int32), _FakeCuda((1, 4), torch.int32)
+    outs = {"accepted_nodes": _FakeCuda((1, 4), torch.int32), "accept_len": _FakeCuda((1,), torch.int32),
+            "bonus_token": _FakeCuda((1,), torch.int32), "p_draft": _FakeCuda((1, 4), torch.float32)}
+    with pytest.raises(ValueError, match=r"out\['p_draft'\] must be a contiguous torch.float32"):
+        tv.verify_greedy(logits, par, tok, out=dict(outs, p_draft=_FakeCuda((1, 4), torch.int32)))
+    with pytest.raises(ValueError, match=r"at least 4 elements"):
+        tv.verify_greedy(logits, par, tok, out=dict(outs, accepted_nodes=_FakeCuda((1, 3), torch.int32)))
     with pytest.raises(ValueError, match=r"out\['accept_len'\] must be a CUDA tensor"):
         tv.verify_greedy(logits, par, tok, out={"accept_len": torch.zeros(1, dtype=torch.int32)})
     with pytest.raises(ValueError, match="workspace must be a CUDA tensor"):
-        tv.verify_greedy(logits, par, tok, out={k: _FakeCuda((1, 4), torch.int32) for k in
-                                                 ("accepted_nodes", "accept_len", "bonus_token", "p_draft")},
+        tv.verify_greedy(logits, par, tok, out=outs,
                          workspace=torch.zeros(1 << 20, dtype=torch.uint8))
     with pytest.raises(ValueError, match="dev_status must be a CUDA tensor"):
-        tv.verify_greedy(logits, par, tok, out={k: _FakeCuda((1, 4), torch.int32) for k in
-                                                 ("accepted_nodes", "accept_len", "bonus_token", "p_draft")},
+        tv.verify_greedy(logits, par, tok, out=outs,
                          workspace=_FakeCuda((1 << 20,), torch.uint8), dev_status=torch.zeros(1, dtype=torch.int32))
     with pytest.raises(ValueError, match="must be a CUDA tensor"):
         tv.frontier_topw(_FakeCuda((1, 8), torch.float32), _FakeCuda((1,), torch.int32), 2,

@@ -8,6 +8,7 @@ is missing the first call raises.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 import torch
@@ -140,6 +141,9 @@ def _out(o, key, shape, dtype, device):
         return torch.empty(shape, dtype=dtype, device=device)
     if not t.is_cuda:
         raise ValueError(f"out[{key!r}] must be a CUDA tensor")
+    need = shape if isinstance(shape, int) else math.prod(shape)
+    if t.dtype != dtype or not t.is_contiguous() or t.numel() < need:
+        raise ValueError(f"out[{key!r}] must be a contiguous {dtype} tensor of at least {need} elements")
     return t
 
 
@@ -254,6 +258,8 @@ def tree_attention(q, k_cache, v_cache, parent, prefix_len: int, *, scale: float
     code = _dtype_code(q)
     if out is None:
         out = torch.empty_like(q)
+    elif out.dtype != q.dtype or out.shape != q.shape:
+        raise ValueError("out must have q's shape and dtype")
     ws_need = tree_attention_workspace_size(B, Hq, Hkv, D, prefix_len, N, q.dtype)
     ws = _workspace(ws_need, q.device, workspace)
     st = _status_tensor(dev_status, q.device)
