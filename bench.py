@@ -241,6 +241,10 @@ class ClockSampler:
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            if self.tmp is not None:  # no sampler: drop the empty sample file
+                self.tmp.close()
+                os.unlink(self.tmp.name)
+                self.tmp = None
         time.sleep(0.3)
 
     def stop(self):

@@ -102,3 +102,35 @@ def test_reference_arm_prints_one_complete_json_line(monkeypatch, capsys, worklo
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_clock_sampler_reads_clocks_and_throttle_reasons(tmp_path, monkeypatch):
+    # A stand-in nvidia-smi on PATH prints three samples and then idles like the real
+    # looping query; the sampler must report the median SM clock, the largest maximum
+    # clock and every throttle reason seen Active in any sample.
+    sys.path.insert(0, ROOT)
+    import bench
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "printf '0, 2070, 2070, 700.5, Active, Not Active, Not Active, Not Active, Not Active\\n'\n"
+                    "printf '0, 1980, 2070, 720.0, Active, Active, Not Active, Not Active, Active\\n'\n"
+                    "printf '0, 2070, 2070, 710.0, Not Active, Not Active, Not Active, Not Active, Not Active\\n'\n"
+                    "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", str(tmp_path) + os.pathsep + os.environ.get("PATH", ""))
+    s = bench.ClockSampler("0")
+    s.start()
+    c = s.stop()
+    assert c["sm_mhz"] == 2070.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert c["samples"] == 3 and c["power_w_max"] == 720.0
+
+
+def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("PATH", str(tmp_path))
+    s = bench.ClockSampler("0")
+    s.start()
+    assert s.tmp is None  # the sample file is not left behind
+    assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
