@@ -191,3 +191,32 @@ def test_binding_refuses_host_tensors_everywhere(lib):
     with pytest.raises(ValueError, match="must be a CUDA tensor"):
         tv.frontier_topw(_FakeCuda((1, 8), torch.float32), _FakeCuda((1,), torch.int32), 2,
                          out=torch.zeros((1, 2), dtype=torch.int32))
+
+
+def test_header_is_plain_c_and_links_from_c(lib, tmp_path):
+    # The boundary is a C ABI: the header compiles as strict C99 and a C program links
+    # against the shared library and gets host-side answers from it (no GPU involved).
+    import shutil
+    import subprocess
+    from tree_speculative_decoding_masked_gb300 import build as b
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "abi_check.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "treeverify.h"\n'
+        "int main(void) {\n"
+        "  int kernel = -1, splits = -1;\n"
+        '  printf("%d %d %d %d\\n", tv_version() >> 16, (int)tv_set_attention_variant(9),\n'
+        "         (int)tv_tree_attention_plan(1, 4, 1, 64, 0, 16, TV_F32, NULL, &splits),\n"
+        "         (int)tv_verify_workspace_size(0, 1, 1, TV_BF16, 0));\n"
+        '  printf("%s\\n", tv_status_string(TV_ERR_VALUE));\n'
+        "  return kernel != -1;\n}\n")
+    libdir = os.path.dirname(b.LIB)
+    exe = tmp_path / "abi_check"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-l:" + os.path.basename(b.LIB),
+                    "-Wl,-rpath," + libdir], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    assert out[0].split() == ["1", str(-8), str(-1), "0"]
+    assert out[1].startswith("TV_ERR_VALUE")
