@@ -138,12 +138,12 @@ class _FakeCuda:
     """Stands in for a CUDA tensor so that the binding's checks of caller-supplied
     outputs can be reached on a machine without a GPU (nothing is launched)."""
 
-    def __init__(self, shape, dtype):
+    def __init__(self, shape, dtype, device="cpu"):
         import torch
-        self.shape = shape
+        self.shape = tuple(shape)
         self.dtype = dtype
         self.is_cuda = True
-        self.device = torch.device("cpu")
+        self.device = torch.device(device)
 
     def is_contiguous(self):
         return True
@@ -191,6 +191,63 @@ def test_binding_refuses_host_tensors_everywhere(lib):
     with pytest.raises(ValueError, match="must be a CUDA tensor"):
         tv.frontier_topw(_FakeCuda((1, 8), torch.float32), _FakeCuda((1,), torch.int32), 2,
                          out=torch.zeros((1, 2), dtype=torch.int32))
+
+
+def test_binding_refuses_inputs_the_kernels_would_misread(lib):
+    # Index inputs must be int32 of exactly [B][N] (kernels read B * N entries), KV caches
+    # must match the queries' batch and head size and hold P + N rows, and every tensor
+    # of a call must sit on one device.  All refused before the library is called.
+    import torch
+    import tree_speculative_decoding_masked_gb300 as tv
+    F = _FakeCuda
+    logits = F((2, 4, 8), torch.float32)
+    par, tok = F((2, 4), torch.int32), F((2, 4), torch.int32)
+    with pytest.raises(ValueError, match="parent must be torch.int32"):
+        tv.verify_greedy(logits, F((2, 4), torch.int64), tok)
+    with pytest.raises(ValueError, match=r"tokens must have shape \(2, 4\)"):
+        tv.verify_greedy(logits, par, F((2, 3), torch.int32))
+    with pytest.raises(ValueError, match=r"parent must have shape \(2, 4\)"):
+        tv.verify_greedy_static(logits, F((1, 4), torch.int32), tok)
+    with pytest.raises(ValueError, match="logits must have 3 dimensions"):
+        tv.verify_greedy(F((8, 8), torch.float32), par, tok)
+    with pytest.raises(ValueError, match="one device per call"):
+        tv.verify_greedy(F((2, 4, 8), torch.float32, "cuda:0"), F((2, 4), torch.int32, "cuda:1"),
+                         F((2, 4), torch.int32, "cuda:0"))
+    with pytest.raises(ValueError, match="parent must be torch.int32"):
+        tv.verify_sample(logits, F((2, 4, 8), torch.float32), F((2, 4), torch.int64), tok, temperature=1.0, seed=1,
+                         round=0)
+    with pytest.raises(ValueError, match="dev_status must be an int32 tensor"):
+        tv.verify_greedy(logits, par, tok, workspace=F((1 << 20,), torch.uint8),
+                         dev_status=F((1,), torch.int64))
+    q = F((2, 8, 4, 128), torch.bfloat16)
+    kv = F((2, 2, 100, 128), torch.bfloat16)
+    with pytest.raises(ValueError, match=r"k_cache must be \[B=2\]"):
+        tv.tree_attention(q, F((1, 2, 100, 128), torch.bfloat16), F((1, 2, 100, 128), torch.bfloat16), par, 10)
+    with pytest.raises(ValueError, match="prefix_len \\+ N must fit the cache rows"):
+        tv.tree_attention(q, kv, kv, par, 97)
+    with pytest.raises(ValueError, match="parent must be torch.int32"):
+        tv.tree_attention(q, kv, kv, F((2, 4), torch.int64), 10)
+    with pytest.raises(ValueError, match="one device per call"):
+        tv.tree_attention(F((2, 8, 4, 128), torch.bfloat16, "cuda:0"), F((2, 2, 100, 128), torch.bfloat16, "cuda:0"),
+                          F((2, 2, 100, 128), torch.bfloat16, "cuda:1"), F((2, 4), torch.int32, "cuda:0"), 10)
+    with pytest.raises(ValueError, match=r"accept_len must have shape \(2,\)"):
+        tv.commit_accepted_kv(kv, kv, par, F((3,), torch.int32), 10)
+    with pytest.raises(ValueError, match="accepted_nodes must be torch.int32"):
+        tv.commit_accepted_kv(kv, kv, F((2, 4), torch.int64), F((2,), torch.int32), 10)
+    with pytest.raises(ValueError, match="root_token must have shape"):
+        tv.select_subtree(F((2, 4, 4), torch.float32), F((2, 4, 4), torch.int32), 8, F((1,), torch.int32))
+    with pytest.raises(ValueError, match="pool_tokens must have shape"):
+        tv.select_subtree(F((2, 4, 4), torch.float32), F((2, 4, 3), torch.int32), 8, F((2,), torch.int32))
+    with pytest.raises(ValueError, match="count must be torch.int32"):
+        tv.frontier_topw(F((2, 16), torch.float32), F((2,), torch.int64), 4)
+    with pytest.raises(ValueError, match="conf must be torch.float32"):
+        tv.prune_tree(par, F((2, 4), torch.float64), 2, 4)
+    with pytest.raises(ValueError, match="parent must be torch.int32"):
+        tv.tree_prep(F((2, 4), torch.int16), 0)
+    with pytest.raises(ValueError, match="parent_score must have shape"):
+        tv.expand_children(F((3, 64), torch.float32), F((2,), torch.float32), 4)
+    with pytest.raises(ValueError, match=r"counters must have shape \(5, 4\)"):
+        tv.philox4x32_10(1, F((5, 3), torch.int32))
 
 
 def test_header_is_plain_c_and_links_from_c(lib, tmp_path):
