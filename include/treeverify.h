@@ -8,6 +8,7 @@
  *   tv_tree_attention   tree-masked grouped-query attention over prefix KV + tree KV
  *   tv_verify_greedy    fused vocab pass + greedy longest-match walk + bonus token
  *   tv_verify_sample    fused vocab pass + min(1,p/q) walk + residual resampling
+ *   tv_vocab_stats      the fused vocab pass alone (row argmax / lse, drafted-token p, q)
  *   tv_commit_accepted_kv  keep the accepted path's cache rows (contiguous), drop the rest
  *   tv_frontier_topw / tv_expand_children  one single-drafter tree-expansion step
  *   tv_prune_tree       per-parent child cap and depth-window re-rooting of a tree
@@ -280,15 +281,47 @@ TV_API tv_status tv_verify_greedy(const void* logits, const int32_t* parent, con
  *   - Each call clears the completion counters on `stream` before the vocab pass.
  *   - All calls share the array: calls that overlap on the GPU (other streams, other
  *     host threads) race and give undefined results.
- *   - Returns TV_ERR_WORKSPACE when the problem needs more scratch than the array holds
- *     (about 40 bytes per logits row, i.e. B*N up to ~100k rows); other errors as
- *     tv_verify_greedy.
+ *   - Returns TV_ERR_WORKSPACE when the problem needs more scratch than the array holds:
+ *     exactly when tv_verify_workspace_size(B, N, V, dtype, 0) exceeds 4194304 bytes.
+ *     That size is about 72 bytes per logits row once B*N reaches 4096 rows (three
+ *     16-byte partial slots plus six 4-byte per-row values), so B*N up to about 58,000
+ *     rows fits; other errors as tv_verify_greedy.
  */
 TV_API tv_status tv_verify_greedy_static(const void* logits, const int32_t* parent, const int32_t* tokens,
                                          int B, int N, int V, tv_dtype dtype, int32_t* accepted_nodes,
                                          int32_t* accept_len, int32_t* bonus_token, float* p_draft,
                                          float* row_lse, int32_t* row_argmax, int32_t* dev_status,
                                          tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * tv_vocab_stats - the fused vocabulary pass on its own, without an acceptance walk.
+ * Blog "greedy decoding" and "acceptance probability for sampling": verification needs,
+ * per node row u, the target's choice and the target (and draft) probability of each
+ * drafted token.  One streaming read of the logits (and of the draft logits, when given)
+ * computes, per row u of x/T: the argmax (lowest index among equal raw values) and the
+ * natural-log log-sum-exp; per node c >= 1 the drafted token's probability in its
+ * parent's row.  It is the pass that tv_verify_greedy and tv_verify_sample run before
+ * their walks, exposed for callers that only want the statistics (acceptance rates,
+ * their own walk) and to time the pass alone.
+ *   logits        [B][N][V] dtype; draft_logits [B][N][V] dtype or NULL
+ *   parent, tokens [B][N] int32 (tree layout above; tokens[b][0] unused)
+ *   temperature   > 0; divides both logits arrays (argmax compares raw values)
+ *   row_lse       [B][N] float out (optional): log-sum-exp of x/T per row
+ *   row_argmax    [B][N] int32 out (optional): argmax per row
+ *   p_draft       [B][N] float out (optional): softmax(x[parent(c)]/T)[tokens[c]], NaN at c=0
+ *   draft_row_lse [B][N] float out (optional, needs draft_logits): lse of the draft rows
+ *   q_draft       [B][N] float out (optional, needs draft_logits): the same gather in the
+ *                 draft rows
+ * Limits as tv_verify_greedy.  Workspace: tv_verify_workspace_size(B, N, V, dtype,
+ * draft_logits != NULL), zero-filled once; the call leaves it ready for the next one.
+ * Errors: draft outputs without draft_logits -> TV_ERR_NULL; temperature <= 0 or not
+ * finite -> TV_ERR_VALUE; others as tv_verify_greedy.
+ */
+TV_API tv_status tv_vocab_stats(const void* logits, const void* draft_logits, const int32_t* parent,
+                                const int32_t* tokens, int B, int N, int V, float temperature, tv_dtype dtype,
+                                float* row_lse, int32_t* row_argmax, float* p_draft, float* draft_row_lse,
+                                float* q_draft, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * tv_verify_sample - stochastic acceptance down the draft tree.
