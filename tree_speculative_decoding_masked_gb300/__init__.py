@@ -35,4 +35,5 @@ from ._binding import (  # noqa: F401
     verify_greedy_static,
     verify_sample,
     verify_workspace_size,
+    vocab_stats,
 )

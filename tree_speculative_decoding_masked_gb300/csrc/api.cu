@@ -190,7 +190,24 @@ tv_status tv_verify_greedy(const void* logits, const int32_t* parent, const int3
   verify_ws_layout(B, N, V, 0, &w);
   return cuda_status(launch_vocab_pass(logits, nullptr, parent, tokens, B, N, V, dtype, 1.0f,
                                        reinterpret_cast<char*>(workspace), w, accepted_nodes, accept_len, bonus_token,
-                                       p_draft, nullptr, row_lse, row_argmax, dev_status, 0, st(stream)));
+                                       p_draft, nullptr, row_lse, row_argmax, nullptr, dev_status, 0,
+                                       st(stream)));
+}
+
+tv_status tv_vocab_stats(const void* logits, const void* draft_logits, const int32_t* parent,
+                         const int32_t* tokens, int B, int N, int V, float temperature, tv_dtype dtype,
+                         float* row_lse, int32_t* row_argmax, float* p_draft, float* draft_row_lse, float* q_draft,
+                         void* workspace, size_t ws_bytes, int32_t* dev_status, tv_stream_t stream) {
+  if (!draft_logits && (draft_row_lse || q_draft)) return TV_ERR_NULL;
+  if (!(temperature > 0.f) || isinf(temperature)) return TV_ERR_VALUE;
+  const int two = draft_logits ? 1 : 0;
+  tv_status s = verify_common_checks(logits, parent, tokens, B, N, V, dtype, workspace, ws_bytes, two);
+  if (s != TV_OK) return s;
+  VerifyWs w;
+  verify_ws_layout(B, N, V, two, &w);
+  return cuda_status(launch_vocab_pass(logits, draft_logits, parent, tokens, B, N, V, dtype, temperature,
+                                       reinterpret_cast<char*>(workspace), w, nullptr, nullptr, nullptr, p_draft,
+                                       q_draft, row_lse, row_argmax, draft_row_lse, dev_status, two, st(stream)));
 }
 
 tv_status tv_verify_sample(const void* target_logits, const void* draft_logits, const int32_t* parent,
@@ -206,8 +223,8 @@ tv_status tv_verify_sample(const void* target_logits, const void* draft_logits, 
   verify_ws_layout(B, N, V, 1, &w);
   char* ws = reinterpret_cast<char*>(workspace);
   cudaError_t e = launch_vocab_pass(target_logits, draft_logits, parent, tokens, B, N, V, dtype, temperature, ws, w,
-                                    nullptr, nullptr, nullptr, p_draft, q_draft, nullptr, nullptr, dev_status, 1,
-                                    st(stream));
+                                    nullptr, nullptr, nullptr, p_draft, q_draft, nullptr, nullptr, nullptr,
+                                    dev_status, 1, st(stream));
   if (e != cudaSuccess) return TV_ERR_CUDA;
   return cuda_status(launch_sample_walk(target_logits, draft_logits, parent, tokens, B, N, V, dtype, temperature,
                                         seed, round, ws, w, accepted_nodes, accept_len, out_token, dev_status,

@@ -22,7 +22,8 @@ cudaError_t launch_vocab_pass(const void* logits, const void* draft, const int32
                               const int32_t* tokens, int B, int N, int V, tv_dtype dtype, float temperature,
                               char* ws, const VerifyWs& w, int32_t* accepted, int32_t* accept_len,
                               int32_t* bonus, float* p_draft, float* q_draft, float* row_lse,
-                              int32_t* row_argmax, int32_t* dev_status, int sampling, cudaStream_t stream);
+                              int32_t* row_argmax, float* row_lse_q, int32_t* dev_status, int sampling,
+                              cudaStream_t stream);
 cudaError_t launch_sample_walk(const void* target, const void* draft, const int32_t* parent,
                                const int32_t* tokens, int B, int N, int V, tv_dtype dtype, float temperature,
                                uint64_t seed, uint64_t round, char* ws, const VerifyWs& w,

@@ -76,7 +76,8 @@ extern "C" TV_API tv_status tv_verify_greedy_static(const void* logits, const in
   // the completion counters must start at zero; clear them on the caller's stream
   if (cudaMemsetAsync(ws + w.row_cnt, 0, w.part - w.row_cnt, s) != cudaSuccess) return TV_ERR_CUDA;
   return launch_vocab_pass(logits, nullptr, parent, tokens, B, N, V, dtype, 1.0f, ws, w, accepted_nodes, accept_len,
-                           bonus_token, p_draft, nullptr, row_lse, row_argmax, dev_status, 0, s) == cudaSuccess
+                           bonus_token, p_draft, nullptr, row_lse, row_argmax, nullptr, dev_status, 0,
+                           s) == cudaSuccess
              ? TV_OK
              : TV_ERR_CUDA;
 }

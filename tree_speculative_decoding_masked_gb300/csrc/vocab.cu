@@ -249,6 +249,7 @@ struct VocabArgs {
   float* q_draft;
   float* row_lse;
   int32_t* row_argmax;
+  float* row_lse_q;   // draft rows' natural-log lse (optional)
   int32_t* dev_status;
   int sampling;
 };
@@ -344,6 +345,7 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) 
       } else {
         sm.lse2q[u] = l2;
         a.lse2_q[ug] = l2;
+        if (a.row_lse_q) a.row_lse_q[ug] = l2 * kLn2;
       }
     }
     __syncthreads();
@@ -369,7 +371,8 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) 
     if (a.q_draft) a.q_draft[r0 + c] = qv;
   }
   __syncthreads();
-  if (a.sampling) return;  // the sampling walk runs in its own kernel
+  // the sampling walk runs in its own kernel; the plain statistics call has no walk
+  if (a.sampling || !a.accepted) return;
   // greedy walk: follow the matching links from the root
   if (tid == 0) {
     int cur = 0, len = 0;
@@ -979,7 +982,8 @@ cudaError_t launch_vocab_pass(const void* logits, const void* draft, const int32
                               const int32_t* tokens, int B, int N, int V, tv_dtype dtype, float temperature,
                               char* ws, const VerifyWs& w, int32_t* accepted, int32_t* accept_len,
                               int32_t* bonus, float* p_draft, float* q_draft, float* row_lse,
-                              int32_t* row_argmax, int32_t* dev_status, int sampling, cudaStream_t stream) {
+                              int32_t* row_argmax, float* row_lse_q, int32_t* dev_status, int sampling,
+                              cudaStream_t stream) {
   VocabArgs a;
   a.logits = logits;
   a.draft = draft;
@@ -1006,6 +1010,7 @@ cudaError_t launch_vocab_pass(const void* logits, const void* draft, const int32
   a.q_draft = q_draft;
   a.row_lse = row_lse;
   a.row_argmax = row_argmax;
+  a.row_lse_q = row_lse_q;
   a.dev_status = dev_status;
   a.sampling = sampling;
   const size_t esz = dtype == TV_BF16 ? 2 : 4;
