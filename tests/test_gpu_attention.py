@@ -135,7 +135,23 @@ def test_qwen3_4b_layer_workload_all_rows():
     _check_all(q, k, v, par, cfg["P"], True)
 
 
-def _sampled_rows(name, n_rows, seed_extra=0):
+def _tree_dominated(qd, kd, P, N, seed, gamma=13.0):
+    """Add gamma * u (u a seeded unit vector) to every query and to the tree's key rows
+    P..P+N-1: a node's tree keys then score about gamma^2 / sqrt(D) ~ 15 above the
+    prefix keys, more than ln(P) + a margin, so the ancestors carry most of the softmax
+    mass and a wrong ancestor set or a wrong tile boundary at P moves the output by O(1)."""
+    D = qd.shape[-1]
+    gen = torch.Generator(device=qd.device)
+    gen.manual_seed(int(seed))
+    u = torch.randn(D, generator=gen, device=qd.device, dtype=torch.float32)
+    u /= u.norm()
+    qd = (qd.float() + gamma * u).to(qd.dtype)
+    kd = kd.clone()
+    kd[:, :, P:P + N] = (kd[:, :, P:P + N].float() + gamma * u).to(kd.dtype)
+    return qd, kd
+
+
+def _sampled_rows(name, n_rows, seed_extra=0, tree_dominated=False):
     cfg = W.WORKLOADS[name]
     B, Hq, Hkv, D, P = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["P"]
     N = cfg.get("N", 1024)
@@ -144,6 +160,8 @@ def _sampled_rows(name, n_rows, seed_extra=0):
     qd = W.device_normal((B, Hq, N, D), 1.0, cfg["seed"] + 1, torch.bfloat16, dev())
     kd = W.device_normal((B, Hkv, P + N, D), 1.0, cfg["seed"] + 2, torch.bfloat16, dev())
     vd = W.device_normal((B, Hkv, P + N, D), 1.0, cfg["seed"] + 3, torch.bfloat16, dev())
+    if tree_dominated:
+        qd, kd = _tree_dominated(qd, kd, P, N, cfg["seed"] + 4)
     st = torch.zeros(1, dtype=torch.int32, device=dev())
     out = tv.tree_attention(qd, kd, vd, i32(par), P, dev_status=st)
     torch.cuda.synchronize()
@@ -154,6 +172,7 @@ def _sampled_rows(name, n_rows, seed_extra=0):
     rows += [(B - 1, Hq - 1, N - 1)]
     worst = 0.0
     cache = {}
+    tree_mass = []
     for b, h, i in rows:
         key = (b, h // G)
         if key not in cache:
@@ -163,7 +182,14 @@ def _sampled_rows(name, n_rows, seed_extra=0):
         ref = attention.per_node_bruteforce(qq, kk, vv, par[b:b + 1], P, 0, 0, i)
         got = out[b, h, i].float().cpu().numpy()
         worst = max(worst, float(np.max(np.abs(got - ref))))
+        if tree_dominated:  # share of the softmax mass on the node's tree keys (test power)
+            path = [P + t for t in _root_path(par[b], i)]
+            sc = (kk[0, 0, :P + N].astype(np.float64) @ qq[0, 0, i].astype(np.float64)) / math.sqrt(D)
+            w = np.exp(sc[:P] - sc[path].max())
+            tree_mass.append(np.exp(sc[path] - sc[path].max()).sum() / (w.sum() + np.exp(sc[path] - sc[path].max()).sum()))
     assert worst < 2e-2, worst
+    if tree_dominated:
+        assert np.median(tree_mass) > 0.9, np.median(tree_mass)
 
 
 def test_long_context_workload_sampled():
@@ -176,6 +202,22 @@ def test_sampling_workload_sampled():
 
 def test_budget_sweep_1024_nodes_sampled():
     _sampled_rows("budget_sweep", 48)
+
+
+def _root_path(parent, i):
+    path = []
+    while i >= 0:
+        path.append(int(i))
+        i = int(parent[i])
+    return path[::-1]
+
+
+@pytest.mark.parametrize("name", ["long_context", "budget_sweep"])
+def test_full_size_tree_dominated(name):
+    # prefix 32768 / 128-node trees and prefix 4096 / 1024-node trees with the softmax
+    # mass on each node's ancestors: the mask and the KV tile and split boundaries at P
+    # decide the output at full size
+    _sampled_rows(name, 48, seed_extra=9, tree_dominated=True)
 
 
 def test_bad_tree_flagged():
