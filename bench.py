@@ -2,9 +2,11 @@
 """Throughput of one tree-verification round on GB300.
 
 A step = one pass of the hot path over one batch of seeded synthetic input:
-    tv_select_subtree (pool -> tree)  ->  tv_tree_attention  ->  tv_verify_greedy
+    tv_select_subtree (pool -> tree)  ->  tv_tree_attention  ||  tv_verify_greedy
 (the sampling workload runs tv_verify_sample instead of the greedy verify).
-Metric: verified tree nodes per second = B * N / step time.
+Metric: verified tree nodes per second = B * N / step time.  The default workload is
+long_context (B=8, prefix 32768, 128-node trees, V=151936): the largest one that fits a
+single GPU.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -14,6 +16,11 @@ CUDA-graph replays; the inputs rotate over enough copies that their total exceed
 the L2, so no step reads its inputs from L2.  Under torchrun every rank runs its own
 replica (the path shards by independent sequences; there is no data-path collective),
 the max time over ranks is used and rank 0 prints one JSON line.
+
+The line's roofline is that of the dominant kernel (algorithmic bytes or FLOPs per
+launch over its CUDA-event time, against MEASURED_PEAKS.json); "e2e" repeats the step
+through the Python API with the round's inputs copied in from pinned host memory and the
+outcome copied back; "cpu_baseline" is the CPU oracle on every host core.
 
 ``--impl reference`` times the CPU oracle on the host cores instead (rank 0 only).
 """
@@ -33,7 +40,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-# BLAS / OpenMP pool sizes of the oracle runs: one host core, as their lines report
+# BLAS / OpenMP pool sizes of the oracle processes: one thread each (one process per core)
 ORACLE_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS")
 if __name__ == "__main__" and ("--impl=reference" in sys.argv[1:] or any(
         a == "--impl" and b == "reference" for a, b in zip(sys.argv[1:], sys.argv[2:]))):
@@ -42,7 +49,7 @@ if __name__ == "__main__" and ("--impl=reference" in sys.argv[1:] or any(
 
 METRIC = "verified tree nodes/sec (attn+accept) and achieved HBM GB/s vs GB300 peak"
 UNIT = "nodes/s"
-DEFAULT_WORKLOAD = "qwen3_4b_layer"
+DEFAULT_WORKLOAD = "long_context"  # the largest workload that fits one GPU
 
 
 def parse_args(argv=None):
@@ -94,75 +101,156 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
 
 
 # ------------------------------------------------------------------------------------
-# oracle sample (CPU baseline and the reference arm)
+# oracle sample (CPU baseline and the reference arm), run on every host core
+#
+# One oracle unit is a fixed slice of the verification of sequence 0 of the workload: the
+# float64 attention row of one (node, head) pair; the unit that completes a node's heads
+# also takes that node's vocab row, and the unit that completes the tree also runs the
+# subtree selection and the acceptance walk.  A unit counts as 1/Hq of a verified node.
+# The inputs are built once, stored as float64 .npy files and memory-mapped by a pool of
+# spawned worker processes (one per core the process may run on), each single-threaded.
 
-def oracle_step_factory(workload: str):
-    """Build the oracle's inputs for ``workload`` (oracle selection + synthetic data of the
-    same recipe) and return (step, description).  One oracle step is a fixed slice of the
-    verification of sequence 0: the attention row of one (node, head) pair; the step that
-    completes a node's heads also takes that node's vocab row, and the step that completes
-    the tree also runs the subtree selection and the acceptance walk.  A step therefore
-    counts as 1/Hq of a verified node."""
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_inputs(workload: str, dirpath: str) -> dict:
+    """Build sequence 0 of ``workload`` for the oracle (oracle selection + the bench's
+    synthetic recipe) and store it under ``dirpath``; returns the metadata."""
     import numpy as np
 
     import synth
     import synth.workloads as W
-    from oracle import attention, greedy, sampling, selection, vocab
+    from oracle import selection, vocab
 
     cfg = W.WORKLOADS[workload]
     g = synth.rng(cfg["seed"])
-    B, Hq, Hkv, D, P, V = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["P"], cfg["V"]
+    Hq, Hkv, D, P, V = cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["P"], cfg["V"]
+    arrays = {}
     if "pool_d" in cfg:
         N = cfg.get("N") or max(cfg["budgets"])
         marg, ptok = W.pools(g, 1, cfg["pool_d"], cfg["pool_k"], V)
         sel = selection.select_subtree(marg[0], ptok[0], N, 11)
         par, tok = sel["parent"][None], sel["token"][None]
+        arrays["marg"], arrays["ptok"] = marg, ptok
     else:
         N = cfg["N"]
-        marg = None
         par, tok = W.trees(g, 1, N, cfg["depth_cap"], V)
     bf16 = cfg["bf16"]
     if cfg["mode"] == "sample":
         tgt, drf, tok = W.sampling_logits(g, par, V, bf16, cfg["temperature"])
-        logits = tgt
+        arrays["draft"] = drf
     else:
-        logits = W.planted_logits(g, par, tok, V, bf16)
-        _, _, argmax_all = vocab.vocab_stats(logits[0])  # set-up: lets the walk run every tree
-    q, k, v = (x.astype(np.float64) for x in W.qkv_host(g, 1, Hq, Hkv, D, P, N, bf16))
+        tgt = W.planted_logits(g, par, tok, V, bf16)
+        _, _, argmax_all = vocab.vocab_stats(tgt[0])  # set-up: lets the walk run every tree
+        arrays["argmax"] = argmax_all
+    arrays["logits"] = tgt
+    q, k, v = W.qkv_host(g, 1, Hq, Hkv, D, P, N, bf16)
+    arrays.update(q=q.astype(np.float64), k=k.astype(np.float64), v=v.astype(np.float64), par=par, tok=tok)
+    for name, arr in arrays.items():
+        np.save(os.path.join(dirpath, name + ".npy"), arr)
+    meta = {"workload": workload, "N": int(N), "Hq": Hq, "P": P, "V": V, "mode": cfg["mode"],
+            "temperature": cfg.get("temperature", 1.0), "pool": "pool_d" in cfg}
+    with open(os.path.join(dirpath, "meta.json"), "w") as f:
+        json.dump(meta, f)
+    return meta
 
-    def step(i):
+
+def oracle_sample_desc(meta: dict) -> str:
+    N, Hq = meta["N"], meta["Hq"]
+    return (f"{meta['workload']}, sequence 0 (N={N}, Hq={Hq}, P={meta['P']}, V={meta['V']}): one oracle unit = "
+            f"the float64 attention row of one (node, head) pair; every {Hq}th unit adds that node's vocab row, "
+            f"every {N * Hq}th unit the subtree selection and acceptance walk; a unit counts as 1/{Hq} node")
+
+
+_ORACLE = {}  # per-process state of an oracle worker
+
+
+def oracle_worker_init(dirpath: str):
+    """Memory-map the stored inputs and build the unit function (pool initializer)."""
+    import numpy as np
+
+    from oracle import attention, greedy, sampling, selection, vocab
+
+    with open(os.path.join(dirpath, "meta.json")) as f:
+        meta = json.load(f)
+    A = {name[:-4]: np.load(os.path.join(dirpath, name), mmap_mode="r")
+         for name in os.listdir(dirpath) if name.endswith(".npy")}
+    N, Hq, P = meta["N"], meta["Hq"], meta["P"]
+    par, tok = np.asarray(A["par"]), np.asarray(A["tok"])
+
+    def unit(i):
         node = (i // Hq) % N
         head = i % Hq
-        attention.tree_attention(q, k, v, par, P, nodes=[node], heads=[head])
+        attention.tree_attention(A["q"], A["k"], A["v"], par, P, nodes=[node], heads=[head])
         if head == Hq - 1:
-            vocab.row_stats(logits[0][node])
+            vocab.row_stats(A["logits"][0][node])
             if node == N - 1:
-                if marg is not None:
-                    selection.select_subtree(marg[0], ptok[0], N, 11)
-                if cfg["mode"] == "sample":
-                    sampling.sampling_walk(tgt[0], drf[0], par[0], tok[0], cfg["temperature"], 1, i, 0)
+                if meta["pool"]:
+                    selection.select_subtree(A["marg"][0], A["ptok"][0], N, 11)
+                if meta["mode"] == "sample":
+                    sampling.sampling_walk(A["logits"][0], A["draft"][0], par[0], tok[0], meta["temperature"], 1, i, 0)
                 else:
-                    greedy.greedy_walk(par[0], tok[0], argmax_all)
+                    greedy.greedy_walk(par[0], tok[0], A["argmax"])
         return 1.0 / Hq
 
-    desc = (f"{workload}, sequence 0 (N={N}, Hq={Hq}, P={P}, V={V}): one oracle step = the float64 attention "
-            f"row of one (node, head) pair; every {Hq}th step adds that node's vocab row, every {N * Hq}th step "
-            f"the subtree selection and acceptance walk; a step counts as 1/{Hq} node")
-    return step, desc
+    _ORACLE["unit"] = unit
+    _ORACLE["meta"] = meta
+
+
+def oracle_run_units(job):
+    """Run units start, start + stride, ... (count of them); returns (nodes, seconds)."""
+    start, count, stride = job
+    unit = _ORACLE["unit"]
+    t0 = time.perf_counter()
+    nodes = 0.0
+    for j in range(count):
+        nodes += unit(start + j * stride)
+    return nodes, time.perf_counter() - t0
+
+
+def oracle_run_for(job):
+    """Run units start, start + stride, ... for ``seconds``; returns (nodes, units, seconds)."""
+    start, stride, seconds = job
+    unit = _ORACLE["unit"]
+    t0 = time.perf_counter()
+    nodes, i = 0.0, 0
+    while True:
+        nodes += unit(start + i * stride)
+        i += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return nodes, i, time.perf_counter() - t0
+
+
+def oracle_pool(dirpath: str, cores: int):
+    import multiprocessing as mp
+    for var in ORACLE_THREAD_VARS:  # spawned workers inherit one-thread BLAS pools
+        os.environ[var] = "1"
+    return mp.get_context("spawn").Pool(cores, initializer=oracle_worker_init, initargs=(dirpath,))
 
 
 def oracle_worker(budget_s: float, workload: str):
-    step, desc = oracle_step_factory(workload)
-    nodes = 0
-    i = 0
-    t0 = time.perf_counter()
-    while True:
-        nodes += step(i)
-        i += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    print(json.dumps({"value": nodes / dt, "steps": i, "seconds": dt, "sample": desc}))
+    """CPU baseline: the oracle on every host core for ``budget_s`` seconds of wall time
+    (each worker runs its own interleaved units), then on one core for a quarter of it."""
+    cores = host_cores()
+    with tempfile.TemporaryDirectory() as d:
+        meta = oracle_inputs(workload, d)
+        with oracle_pool(d, cores) as pool:
+            pool.map(oracle_run_units, [(k, 1, cores) for k in range(cores)])  # warm every worker
+            res = pool.map(oracle_run_for, [(k, cores, budget_s) for k in range(cores)])
+        nodes = sum(r[0] for r in res)
+        units = sum(r[1] for r in res)
+        wall = max(r[2] for r in res)
+        oracle_worker_init(d)
+        n1, u1, t1 = oracle_run_for((0, 1, max(2.0, budget_s / 4)))
+    print(json.dumps({"value": nodes / wall, "units": units, "seconds": wall, "cores": cores,
+                      "single_core_value": n1 / t1, "single_core_units": u1, "single_core_seconds": t1,
+                      "sample": oracle_sample_desc(meta)}))
 
 
 def run_oracle_subprocess(budget_s: float, workload: str) -> dict:
@@ -172,35 +260,57 @@ def run_oracle_subprocess(budget_s: float, workload: str) -> dict:
     env.pop("RANK", None)
     env.pop("WORLD_SIZE", None)
     res = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker", str(budget_s), "--workload",
-                          workload], capture_output=True, text=True, env=env, timeout=900)
+                          workload], capture_output=True, text=True, env=env, timeout=1800)
     if res.returncode != 0:
         raise RuntimeError("oracle worker failed:\n" + res.stderr[-2000:])
     out = json.loads(res.stdout.strip().splitlines()[-1])
-    return {"value": out["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": out["sample"] + f"; {out['steps']} steps in {out['seconds']:.1f} s, single-threaded NumPy"}
+    return {"value": out["value"], "unit": UNIT, "cores": out["cores"], "kind": "oracle",
+            "sample": out["sample"] + f"; {out['units']} units in {out['seconds']:.1f} s over {out['cores']} "
+                      f"single-threaded NumPy processes (one per host core)",
+            "single_core": {"value": out["single_core_value"], "unit": UNIT, "cores": 1,
+                            "sample": f"{out['single_core_units']} units in {out['single_core_seconds']:.1f} s "
+                                      f"in one process"}}
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    step, desc = oracle_step_factory(args.workload)
-    for i in range(args.warmup):
-        step(i)
-    nodes = 0
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        nodes += step(args.warmup + i)
-    dt = time.perf_counter() - t0
-    value = nodes / dt
     import synth.workloads as W
     cfg = W.WORKLOADS[args.workload]
+    cores = host_cores()
+    with tempfile.TemporaryDirectory() as d:
+        meta = oracle_inputs(args.workload, d)
+        with oracle_pool(d, cores) as pool:
+            # a step = the same number of units on every worker, sized so that the whole
+            # run takes about two minutes (at most 0.25 s per step)
+            probe = pool.map(oracle_run_units, [(k, 2, cores) for k in range(cores)])
+            per_unit = max(1e-6, max(t for _, t in probe) / 2)
+            step_s = min(0.25, max(0.002, 120.0 / max(1, args.steps + args.warmup)))
+            per_worker = max(1, int(round(step_s / per_unit)))
+            base = [2 * cores]
+
+            def step():
+                jobs = [(base[0] + k, per_worker, cores) for k in range(cores)]
+                base[0] += cores * per_worker
+                return sum(n for n, _ in pool.map(oracle_run_units, jobs))
+
+            for _ in range(args.warmup):
+                step()
+            nodes = 0.0
+            t0 = time.perf_counter()
+            for _ in range(args.steps):
+                nodes += step()
+            dt = time.perf_counter() - t0
+    value = nodes / dt
+    sample = (oracle_sample_desc(meta) + f"; a step = {per_worker} units on each of {cores} single-threaded NumPy "
+              f"processes (one per host core), {args.steps} steps timed in {dt:.2f} s")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(args.workload, cfg),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -349,8 +459,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # before any GPU work: the oracle runs in its own single-threaded process
-        cpu_base = run_oracle_subprocess(15.0, args.workload)
+        # before any GPU work: the oracle runs in its own processes, one per host core
+        cpu_base = run_oracle_subprocess(10.0, args.workload)
     rank, world = dist_init("nccl")
     tv.load_library()
 
@@ -438,6 +548,17 @@ def run_ours(args):
         else:
             tv.verify_greedy(s["logits"], sel_out["parent"], sel_out["tokens"], workspace=ws_ver, dev_status=status,
                              out=ver_out)
+
+    vocab_out = {"row_lse": torch.empty(B, N, dtype=torch.float32, device=dev),
+                 "row_argmax": torch.empty(B, N, dtype=torch.int32, device=dev),
+                 "p_draft": torch.empty(B, N, dtype=torch.float32, device=dev),
+                 "draft_row_lse": torch.empty(B, N, dtype=torch.float32, device=dev),
+                 "q_draft": torch.empty(B, N, dtype=torch.float32, device=dev)}
+
+    def k_vocab(s):
+        # the vocab pass alone (the first kernel of either verify call)
+        tv.vocab_stats(s["logits"], sel_out["parent"], sel_out["tokens"], draft_logits=s.get("draft"),
+                       temperature=cfg.get("temperature", 1.0), workspace=ws_ver, dev_status=status, out=vocab_out)
 
     # cost line for the cost-aware selection: step time against tree rows, fitted to this
     # bench's own budget_sweep runs (attention + verify, B=16): ~38 us + 3.09 us per row
@@ -579,6 +700,7 @@ def run_ours(args):
         # the same way as in the step graph)
         fam_graphs = {"attention": capture(lambda: [k_attn(s) for s in sets]),
                       "verify": capture(lambda: [k_verify(s) for s in sets]),
+                      "vocab": capture(lambda: [k_vocab(s) for s in sets]),
                       "commit": capture(lambda: [k_commit(s) for s in sets]),
                       "tree_prep": capture(lambda: [k_prep(s) for s in sets]),
                       "expand": capture(lambda: [k_expand(s) for s in sets]),
@@ -633,43 +755,100 @@ def run_ours(args):
         return f
 
     br = {name: timed(fam(name), fam_reps) * 1e3 / (fam_reps * n_sets) for name in fam_graphs}
+    if sampling_mode:
+        br["walk"] = br["verify"] - br["vocab"]  # the sampling walk kernel after the vocab pass
     expand_bytes = exp_rows * V * elt
     commit_bytes = int(ver_out["accept_len"].sum().item()) * Hkv * D * elt * 2 * 2  # K and V rows, read + write
-    fam_bytes = {"attention": bytes_attn, "verify": bytes_vocab}
-    # dense-equivalent attention FLOPs: QK^T and PV over every (node row, key) pair of
-    # the prefix and the tree block, as the kernel computes them
-    fam_flops = {"attention": 4 * B * Hq * N * (P + N) * D, "verify": 0}
-    dom = max(("attention", "verify"), key=lambda kk: br[kk])
+    # algorithmic attention FLOPs: QK^T and PV over each node's visible keys only, the
+    # prefix plus its |pi(i)| = depth + 1 tree keys; the dense bound counts every
+    # (node, key) pair of the prefix and the tree block, as the tile kernels compute them
+    depth = np.zeros((B, N), dtype=np.int64)
+    for i in range(1, N):
+        depth[:, i] = depth[np.arange(B), par[:, i]] + 1
+    visible = int(B * N * P + (depth + 1).sum())
+    flops_alg = 4 * Hq * D * visible
+    flops_dense = 4 * B * Hq * N * (P + N) * D
     attn_kernel, attn_splits = tv.tree_attention_plan(B, Hq, Hkv, D, P, N, tdt)
-    kernel_names = {"attention": ("attn_simt_kernel", "attn_tc_kernel", "attn_pair_kernel",
-                                  "attn_pair2_kernel")[attn_kernel],
-                    "verify": "vocab_pass_tma_kernel"}
-    roofline = roofline_entry(kernel_names[dom], fam_bytes[dom], fam_flops[dom] if bf16 else 0, br[dom] * 1e-6,
-                              args.workload)
+    attn_name = ("attn_simt_kernel", "attn_tc_kernel", "attn_pair_kernel", "attn_pair2_kernel")[attn_kernel]
+    rooflines = {
+        attn_name: roofline_entry(attn_name, bytes_attn, flops_alg if bf16 else 0, br["attention"] * 1e-6,
+                                  args.workload),
+        "vocab_pass_tma_kernel": roofline_entry("vocab_pass_tma_kernel", bytes_vocab, 0, br["vocab"] * 1e-6,
+                                                args.workload),
+    }
+    rooflines[attn_name]["dense_flops_per_launch"] = flops_dense
+    rooflines["vocab_pass_tma_kernel"]["timed"] = "tv_vocab_stats alone (the vocab pass without a walk)"
+    dom = attn_name if br["attention"] >= br["vocab"] else "vocab_pass_tma_kernel"
+    roofline = rooflines[dom]
 
-    # ---- end to end through the public API with host buffers (pinned), copies timed
-    pinned = {kk: (to_dev(vv) if kk in ("q", "k", "v", "logits", "draft") else torch.from_numpy(vv)).cpu()
-              .pin_memory() for kk, vv in host.items()}
+    # ---- end to end through the public API with host buffers (pinned), copies timed.
+    # A decoding loop keeps the committed prefix KV cache (rows 0..P-1) on the device
+    # across rounds; what a round brings is the tree's queries, the tree's own K/V rows
+    # (written into cache rows P..P+N-1), the target (and draft) logits and the
+    # candidate pool.  Those are copied in from pinned host memory every step, and the
+    # accept outcome is copied back.
+    round_in = {"q": (host["q"], lambda d: d["q"]),
+                "k_tree": (np.ascontiguousarray(host["k"][:, :, P:P + N]), lambda d: d["k"][:, :, P:P + N]),
+                "v_tree": (np.ascontiguousarray(host["v"][:, :, P:P + N]), lambda d: d["v"][:, :, P:P + N]),
+                "logits": (host["logits"], lambda d: d["logits"])}
+    if "draft" in host:
+        round_in["draft"] = (host["draft"], lambda d: d["draft"])
+    if use_pool:
+        round_in["marg"] = (host["marg"], lambda d: d["marg"])
+        round_in["ptok"] = (host["ptok"], lambda d: d["ptok"])
+    pinned = {kk: ((to_dev(vv) if kk not in ("marg", "ptok") else torch.from_numpy(vv)).cpu().pin_memory(), where)
+              for kk, (vv, where) in round_in.items()}
     res_host = {kk: torch.empty_like(ver_out[kk], device="cpu").pin_memory()
                 for kk in (("accepted_nodes", "accept_len", "out_token") if sampling_mode else
                            ("accepted_nodes", "accept_len", "bonus_token"))}
-    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    h2d = sum(t.numel() * t.element_size() for t, _ in pinned.values())
     d2h = sum(t.numel() * t.element_size() for t in res_host.values())
     dst = sets[0]
+    dst_views = {kk: where(dst) for kk, (_, where) in pinned.items()}
     e2e_steps = max(20, min(2000, args.steps // 20))
+
+    def copies_in():
+        for kk, (t, _) in pinned.items():
+            dst_views[kk].copy_(t, non_blocking=True)
+
+    def copies_out():
+        for kk, t in res_host.items():
+            t.copy_(ver_out[kk], non_blocking=True)
 
     def e2e(k):
         with torch.cuda.stream(stream):
             for _ in range(k):
-                for kk, t in pinned.items():
-                    dst[kk].copy_(t, non_blocking=True)
+                copies_in()
                 step(dst)
-                for kk, t in res_host.items():
-                    t.copy_(ver_out[kk], non_blocking=True)
+                copies_out()
+
+    def copies_only(k):
+        with torch.cuda.stream(stream):
+            for _ in range(k):
+                copies_in()
+                copies_out()
 
     e2e(3)
     ms_e2e = max_over_ranks(timed(e2e, e2e_steps), world, dev)
     e2e_value = world * B * N / (ms_e2e / e2e_steps / 1e3)
+    copies_only(2)
+    ms_copy = timed(copies_only, e2e_steps) / e2e_steps
+
+    # pinned host <-> device copy ceiling: one 256 MiB copy each way, best of three
+    probe_bytes = 1 << 28
+    hbuf = torch.empty(probe_bytes, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(probe_bytes, dtype=torch.uint8, device=dev)
+    best = {"h2d": float("inf"), "d2h": float("inf")}
+    for _ in range(3):
+        for way in ("h2d", "d2h"):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                (dbuf.copy_(hbuf, non_blocking=True) if way == "h2d" else hbuf.copy_(dbuf, non_blocking=True))
+            e1.record(stream)
+            torch.cuda.synchronize()
+            best[way] = min(best[way], e0.elapsed_time(e1))
+    del hbuf, dbuf
 
     if rank == 0:
         line = {
@@ -685,16 +864,21 @@ def run_ours(args):
                                 " on selection's stream with programmatic dependent launch)",
                            parallelism=f"replicas x{world}",
                            sm_partition={"verify": sm_partition[0] or n_sm, "attention": sm_partition[1] or n_sm},
-                           attention_kernel=kernel_names["attention"], attention_kv_splits=attn_splits),
+                           attention_kernel=attn_name, attention_kv_splits=attn_splits),
             "path_gbs": bytes_set / (ms_per_step * 1e-3) / 1e9,
             "breakdown_us": br,
             "commit_bytes_per_launch": commit_bytes,
             "expand": {"rows": exp_rows, "m": exp_m, "bytes_per_launch": expand_bytes,
                        "gbs": expand_bytes / (br["expand"] * 1e-6) / 1e9},
             "roofline": roofline,
+            "rooflines": rooflines,
             "cpu_baseline": cpu_base,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps},
+                    "steps": e2e_steps, "ms_per_step": ms_e2e / e2e_steps,
+                    "copied": "per round: " + ", ".join(pinned) + "; the prefix KV cache rows 0..P-1 stay on the "
+                              "device across rounds",
+                    "copy_ms_per_step": ms_copy, "h2d_gbs": h2d / (ms_copy * 1e-3) / 1e9,
+                    "copy_probe_gbs": {w: probe_bytes / (best[w] * 1e-3) / 1e9 for w in best}},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }

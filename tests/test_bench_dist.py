@@ -134,3 +134,15 @@ def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
     s.start()
     assert s.tmp is None  # the sample file is not left behind
     assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_cpu_baseline_runs_the_oracle_on_every_host_core():
+    # The GPU arm's cpu_baseline leg: a subprocess (started before any GPU work) times the
+    # oracle with one single-threaded process per host core, then on one core.
+    sys.path.insert(0, ROOT)
+    import bench
+    cb = bench.run_oracle_subprocess(0.5, "tiny_fp32")
+    assert cb["kind"] == "oracle" and cb["unit"] == bench.UNIT and cb["value"] > 0
+    assert cb["cores"] == bench.host_cores()
+    assert cb["single_core"]["cores"] == 1 and cb["single_core"]["value"] > 0
+    assert "one per host core" in cb["sample"]
