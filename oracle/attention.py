@@ -15,6 +15,8 @@ Readings (not fixed by the pages)
   * Grouped-query attention: query head h reads KV head h // (Hq / Hkv).
   * Scale 1/sqrt(D) unless given; softmax over the visible keys only.
   * Node i's visible keys are rows [0, P) and {P + t : t in pi(i)}.
+  * Padding rows of a ragged batch (parent -1 after the last node, see tree.py) have no
+    output; their rows of the result stay zero.
 """
 from __future__ import annotations
 
@@ -22,7 +24,7 @@ import math
 
 import numpy as np
 
-from .tree import observable_set, root_path, validate
+from .tree import is_padding, observable_set, root_path, validate
 
 
 def _softmax_attend(qvec: np.ndarray, keys: np.ndarray, vals: np.ndarray, scale: float) -> np.ndarray:
@@ -54,6 +56,8 @@ def tree_attention(q, k_cache, v_cache, parent, prefix_len: int, scale: float | 
     for b in range(bsz):
         validate(parent[b])
         for i in (range(n) if nodes is None else nodes):
+            if is_padding(parent[b], i):
+                continue
             anc = sorted(observable_set(parent[b], i))
             rows = list(range(prefix_len)) + [prefix_len + t for t in anc]
             for h in (range(hq) if heads is None else heads):

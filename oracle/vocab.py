@@ -42,11 +42,13 @@ def vocab_stats(logits, temperature: float = 1.0):
 def drafted_token_prob(logits, lse, parent, tokens, temperature: float = 1.0) -> np.ndarray:
     """p_c = softmax(x[parent(c)] / T)[tok c] = exp(x[parent(c)][tok c] / T - lse[parent(c)]).
 
-    Entry 0 (the root, not a draft) is NaN.
+    Entry 0 (the root, not a draft) and padding rows (parent -1) are NaN.
     """
     n = len(parent)
     out = np.full(n, np.nan)
     for c in range(1, n):
         u = int(parent[c])
+        if u < 0:
+            continue
         out[c] = math.exp(float(logits[u][int(tokens[c])]) / temperature - float(lse[u]))
     return out

@@ -113,3 +113,21 @@ def test_dominant_key_selects_its_value():
     k[0, 0, p + 1, 0] = 400.0
     out2 = attention.tree_attention(q, k, v, par2, p, scale=1.0)
     assert not np.allclose(out2[0, 0, 2], v[0, 0, p + 1])
+
+
+def test_padded_rows_of_a_ragged_batch():
+    # a tree of n nodes padded with parent -1 rows to N: active rows equal the unpadded
+    # tree's attention (the padding keys at rows P + n.. are seen by nobody), padding
+    # rows stay zero; the per-node brute force agrees on the active rows
+    g = np.random.default_rng(77)
+    n, N, P, Hq, Hkv, D = 9, 14, 20, 4, 2, 16
+    par = np.array([-1] + [int(g.integers(i)) for i in range(1, n)], dtype=np.int32)
+    pad = np.concatenate([par, np.full(N - n, -1, np.int32)])[None]
+    q = g.standard_normal((1, Hq, N, D))
+    k = g.standard_normal((1, Hkv, P + N, D))
+    v = g.standard_normal((1, Hkv, P + N, D))
+    got = attention.tree_attention(q, k, v, pad, P)
+    ref = attention.tree_attention(q[:, :, :n], k[:, :, :P + n], v[:, :, :P + n], par[None], P)
+    assert np.allclose(got[:, :, :n], ref, atol=1e-12) and (got[:, :, n:] == 0).all()
+    for i in (0, n - 1):
+        assert np.allclose(got[0, 1, i], attention.per_node_bruteforce(q, k, v, pad, P, 0, 1, i), atol=1e-12)

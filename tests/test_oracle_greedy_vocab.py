@@ -79,3 +79,19 @@ def test_planted_argmax_is_found():
     for u in range(n):
         if fc[u] >= 0:
             assert am[u] == tok[fc[u]]
+
+
+def test_padded_rows_are_not_drafts():
+    # padding rows (parent -1 after the last node) are no drafts: NaN drafted-token
+    # probability, never walked; the walk equals that of the unpadded tree
+    par = [-1, 0, 0, 1]
+    tok = [5, 3, 4, 7]
+    pad = par + [-1, -1]
+    logits = np.zeros((6, 10))
+    logits[0, 3] = 4.0
+    logits[1, 7] = 4.0
+    _, lse, am = vocab.vocab_stats(logits)
+    p = vocab.drafted_token_prob(logits, lse, pad, tok + [0, 0])
+    assert np.isnan(p[4:]).all() and np.isnan(p[0])
+    assert np.allclose(p[1:4], vocab.drafted_token_prob(logits[:4], lse[:4], par, tok)[1:4])
+    assert greedy.greedy_walk(pad, tok + [3, 3], am) == greedy.greedy_walk(par, tok, am[:4]) == ([1, 3], int(am[3]))

@@ -200,3 +200,20 @@ def test_first_two_tokens_follow_the_target_joint():
     # ignores the first (every context's row replaced by the first context's row).
     wrong = n * np.outer(sp1, sampling.softmax_row(p2[0], 1.0))
     assert float(np.sum((hist - wrong) ** 2 / wrong)) > crit
+
+
+def test_padded_rows_are_never_tried():
+    # padding rows of a ragged batch are nobody's children: the walk, its draws and its
+    # output equal those of the unpadded tree
+    g = synth.rng(91)
+    V, n, N = 12, 7, 11
+    par = np.array([-1, 0, 0, 1, 1, 2, 3], dtype=np.int32)
+    tgt = g.standard_normal((N, V)) * 2
+    drf = tgt + g.standard_normal((N, V)) * 0.5
+    tok = synth.draw_children_from_draft(g, par, drf[:n], 1.0)
+    pad = np.concatenate([par, np.full(N - n, -1, np.int32)])
+    tokp = np.concatenate([tok, np.full(N - n, -1, np.int32)])
+    for seed in range(20):
+        a = sampling.sampling_walk(tgt, drf, pad, tokp, 1.0, seed, 3, 0)
+        b = sampling.sampling_walk(tgt[:n], drf[:n], par, tok, 1.0, seed, 3, 0)
+        assert a[0] == b[0] and a[1] == b[1]

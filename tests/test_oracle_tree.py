@@ -58,7 +58,33 @@ def test_children_csr():
     assert idx.tolist() == [1, 2, 3, 4, 5, 6]
 
 
-@pytest.mark.parametrize("bad", [[0, 0], [-1, 1], [-1, 0, 3, 1], [-1, -1], []])
+@pytest.mark.parametrize("bad", [[0, 0], [-1, 1], [-1, 0, 3, 1], [-1, -1, 0], [-1, 0, -1, 1], []])
 def test_rejects_malformed(bad):
+    # [-1, -1, 0] and [-1, 0, -1, 1]: an active row after a padding row
     with pytest.raises(ValueError):
         tree.validate(bad)
+
+
+def _padded(parent, n_total):
+    return np.concatenate([np.asarray(parent, dtype=np.int32), np.full(n_total - len(parent), -1, np.int32)])
+
+
+@pytest.mark.parametrize("n,n_total", [(1, 4), (10, 16), (33, 64), (40, 40)])
+def test_trailing_padding_rows_are_inactive(n, n_total):
+    # a ragged batch pads a sequence's tree with parent -1 rows: the active rows keep the
+    # unpadded tree's depth, positions, mask bits and children; padding rows get none
+    g = np.random.default_rng(n + n_total)
+    par = [-1] + [int(g.integers(i)) for i in range(1, n)]
+    pad = _padded(par, n_total)
+    tree.validate(pad)
+    assert tree.active_count(pad) == n
+    d0, dp = tree.depth(par), tree.depth(pad)
+    assert dp[:n].tolist() == d0.tolist() and (dp[n:] == -1).all()
+    pp = tree.position_ids(pad, 100)
+    assert pp[:n].tolist() == (100 + d0).tolist() and (pp[n:] == -1).all()
+    m0, mp = tree.packed_mask(par), tree.packed_mask(pad)
+    assert (mp[n:] == 0).all()
+    assert (mp[:n, :m0.shape[1]] == m0).all() and (mp[:n, m0.shape[1]:] == 0).all()
+    assert tree.children(pad)[:n] == tree.children(par) and all(not c for c in tree.children(pad)[n:])
+    off, idx = tree.child_csr(pad)
+    assert off[n:].tolist() == [n - 1] * (n_total + 1 - n) and idx.tolist() == tree.child_csr(par)[1].tolist()
