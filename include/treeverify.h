@@ -32,6 +32,15 @@
  *     committed token) and 0 <= parent[b][i] < i for i >= 1.  N counts all nodes,
  *     root included.  Row u of a logits block is the target (or draft) distribution of
  *     the token that follows node u, so draft node c is judged with row parent[c].
+ *   - Ragged batches (TAPS §4.1 stage 3: the selected subtree is large when the drafter
+ *     is confident and small otherwise, so one call's sequences hold different node
+ *     counts): rows after a sequence's last node hold parent -1 and are inactive
+ *     padding, as tv_select_subtree* writes them past n_nodes.  Padding is trailing:
+ *     sequence b's active rows are 0..n_b-1, n_b = the first row i >= 1 whose parent is
+ *     -1 (or N); a row with parent >= 0 after a padding row sets TV_DEV_BAD_TREE.  Padding
+ *     rows are no drafts: their tokens are not checked, they are nobody's children and
+ *     get no output (each call below says what it leaves in their output rows).  Their
+ *     logits and cache rows are still addressed as [B][N] blocks.
  *   - Logits / activations are row-major and contiguous.  bf16 is IEEE bfloat16.
  *   - The kernels of tv_select_subtree*, tv_tree_attention (tensor-core path) and
  *     tv_verify_* are launched with programmatic stream serialization: their CTAs may
@@ -164,6 +173,8 @@ TV_API tv_status tv_set_attention_splits(int splits);
  *   child_off  [B][N+1] int32 out, child_idx [B][N] int32 out: per sequence, the
  *              children of u are child_idx[child_off[u] .. child_off[u+1]) in
  *              ascending node index (child_idx[b][N-1] is unused)  (both or neither)
+ * Padding rows (ragged batches): depth and pos -1, an all-zero mask row, no children;
+ * child_idx holds -1 past the n_b - 1 edges and child_off[b][N] = n_b - 1.
  * Limits: 1 <= N <= 1024, B >= 1.  Launches one CTA per sequence.
  */
 TV_API tv_status tv_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* depth, int32_t* pos,
@@ -204,6 +215,8 @@ TV_API tv_status tv_prune_tree(const int32_t* parent, const float* conf, int B, 
  *                 keys are post-RoPE).  kv_stride_tokens >= P + N.
  *   parent        [B][N] int32
  *   scale         softmax scale (> 0); pass 0 for 1/sqrt(D).
+ * Padding rows of a ragged batch: their rows of out are not written (the active rows'
+ * results do not depend on the padding's q, k or v).
  * Precision: fp32 in/out with fp32 math, or bf16 in/out with fp32 softmax and fp32
  * accumulation.  Limits: 1 <= N <= 1024, 32 <= D <= 256 with D % 32 == 0, Hq % Hkv == 0.
  * bf16 with D in {64, 128}, G <= 16 and G * N >= 64 runs on the tensor cores; every
@@ -257,6 +270,8 @@ TV_API tv_status tv_tree_attention(const void* q, const void* k_cache, const voi
  *   p_draft       [B][N] float out (optional): softmax(x[parent(c)])[tokens[c]], NaN at c=0
  *   row_lse       [B][N] float out (optional): log-sum-exp of each row
  *   row_argmax    [B][N] int32 out (optional): argmax of each row
+ * Padding rows of a ragged batch: p_draft and row_lse NaN, row_argmax -1, never walked
+ * (their logits are still read by the streaming pass).
  * Limits: 1 <= N <= 1024, 1 <= V < 2^31 / N, B * N <= 131072.
  * Workspace: tv_verify_workspace_size().
  */
@@ -312,6 +327,7 @@ TV_API tv_status tv_verify_greedy_static(const void* logits, const int32_t* pare
  *   draft_row_lse [B][N] float out (optional, needs draft_logits): lse of the draft rows
  *   q_draft       [B][N] float out (optional, needs draft_logits): the same gather in the
  *                 draft rows
+ * Padding rows of a ragged batch: NaN lse and probabilities, argmax -1.
  * Limits as tv_verify_greedy.  Workspace: tv_verify_workspace_size(B, N, V, dtype,
  * draft_logits != NULL), zero-filled once; the call leaves it ready for the next one.
  * Errors: draft outputs without draft_logits -> TV_ERR_NULL; temperature <= 0 or not
@@ -338,6 +354,7 @@ TV_API tv_status tv_vocab_stats(const void* logits, const void* draft_logits, co
  *   target_logits, draft_logits [B][N][V] dtype
  *   accepted_nodes [B][N], accept_len [B], out_token [B] int32 out
  *   p_draft, q_draft [B][N] float out (optional): p_{parent(c)}(t_c), q_{parent(c)}(t_c)
+ * Padding rows of a ragged batch: p_draft and q_draft NaN, never tried.
  * Limits as tv_verify_greedy; temperature > 0.  Workspace:
  * tv_verify_workspace_size(B, N, V, dtype, 1).
  */
@@ -442,13 +459,11 @@ TV_API tv_status tv_select_subtree(const float* marg, const int32_t* pool_tokens
  * against tree rows (any unit, same for both).  Rows past n* hold -1 (score 0) and
  * n_nodes[b] = n*.  Other arguments, limits and workspace as tv_select_subtree, except
  * that n_nodes is required.
- * Handing the tree on: tv_tree_prep, tv_tree_attention and tv_verify_* take one N for
- * every sequence of a call and flag a parent of -1 below row 0 as TV_DEV_BAD_TREE, so
- * the padded rows past n_nodes[b] are not passed on: call them with N = n_nodes[b].
- * A call for one sequence can pass the first N rows of its output rows directly; a call
- * for several sequences with equal n_nodes needs their first N rows packed with row
- * stride N.  The same holds for tv_select_subtree whenever the candidate tree holds
- * fewer than budget - 1 nodes.
+ * Handing the tree on: the rows past n_nodes[b] hold parent -1, the trailing padding
+ * of a ragged batch, so parent and tokens go straight into tv_tree_prep,
+ * tv_tree_attention, tv_verify_* and tv_vocab_stats with N = budget, every sequence
+ * keeping its own node count.  The same holds for tv_select_subtree whenever the
+ * candidate tree holds fewer than budget - 1 nodes.
  * Host errors: cost_base < 0, cost_per_row <= 0 or not finite -> TV_ERR_VALUE.
  */
 TV_API tv_status tv_select_subtree_adaptive(const float* marg, const int32_t* pool_tokens, int B, int d,

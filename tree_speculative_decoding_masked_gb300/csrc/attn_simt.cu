@@ -76,9 +76,12 @@ __global__ void __launch_bounds__(kSimtWarpsT * 32) attn_simt_kernel(const T* __
     for (int d = lane; d < kD; d += 32) s_q[rr][d] = live ? ldx(q, qoff + d) * scale : 0.f;
     for (int w = lane; w < W; w += 32) s_vis[rr][w] = 0u;
     __syncwarp();
-    if (lane == 0 && live) {
+    // a padding row of a ragged batch (parent -1 after the last node) has no output;
+    // an active row must not follow a padding row
+    const bool pad = live && i > 0 && s_par[i] == -1;
+    if (lane == 0 && live && !pad) {
       int a = i, guard = 0;
-      bool ok = true;
+      bool ok = !(i >= 2 && s_par[i - 1] == -1);
       while (a >= 0 && guard <= N) {
         s_vis[rr][a >> 5] |= 1u << (a & 31);
         const int pa = s_par[a];
@@ -176,6 +179,7 @@ __global__ void __launch_bounds__(kSimtWarpsT * 32) attn_simt_kernel(const T* __
     const int row = r0 + rr;
     if (row >= G * N) continue;
     const int g = row / N, i = row % N;
+    if (i > 0 && s_par[i] == -1) continue;  // padding row: nothing written
     const size_t ooff = (((size_t)b * Hq + kh * G + g) * N + i) * D;
     const float inv = l[rw] > 0.f ? 1.f / l[rw] : 0.f;
 #pragma unroll

@@ -213,7 +213,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = t; c < a.N; c += kThreads - 64) {
       const int p = a.parent[(size_t)b * a.N + c];
       s_par[c] = p;
-      if (!((c == 0) ? (p == -1) : (p >= 0 && p < c))) bad = 1;
+      // trailing padding rows of a ragged batch hold parent -1; an active row must not
+      // follow one
+      const bool prev_pad = c >= 2 && a.parent[(size_t)b * a.N + c - 1] == -1;
+      if (!((c == 0) ? (p == -1) : (p == -1 || (p >= 0 && p < c && !prev_pad)))) bad = 1;
     }
     if (bad) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);
     for (int r = rows_used + t; r < kRows; r += kThreads - 64)
@@ -344,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q4 * 32 + lane;
     const int g = r / a.NT, il = r % a.NT;
     const int node = i0 + il;
-    const bool valid = (g < a.G) && (node < a.N) && (r < rows_used);
+    const bool valid = (g < a.G) && (node < a.N) && (r < rows_used) && !(node > 0 && s_par[node] == -1);
     const int mnode = valid ? node : 0;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const int c_lo = h * (kBN / 2);  // this thread's key columns in a tile
@@ -511,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rr = r0 + item / kChunks;
         const int ch = item % kChunks;
         const int gg = rr / a.NT, ii = i0 + rr % a.NT;
-        if (gg >= a.G || ii >= a.N || rr >= rows_used) continue;
+        if (gg >= a.G || ii >= a.N || rr >= rows_used || (ii > 0 && s_par[ii] == -1)) continue;
         float2 mlv[kMaxSplits];
         float4 x[kMaxSplits];
         const uint32_t moff = (uint32_t)(rr * 8);
@@ -680,7 +683,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = t; c < a.N; c += kThreads - 64) {
       const int p = a.parent[(size_t)b * a.N + c];
       s_par[c] = p;
-      if (!((c == 0) ? (p == -1) : (p >= 0 && p < c))) bad = 1;
+      // trailing padding rows of a ragged batch hold parent -1; an active row must not
+      // follow one
+      const bool prev_pad = c >= 2 && a.parent[(size_t)b * a.N + c - 1] == -1;
+      if (!((c == 0) ? (p == -1) : (p == -1 || (p >= 0 && p < c && !prev_pad)))) bad = 1;
     }
     if (bad) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);
     for (int r = rows_used + t; r < 2 * kRows; r += kThreads - 64) {
@@ -824,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q4 * 32 + lane;
     const int g = r / a.NT, il = r % a.NT;
     const int node = i0[x] + il;
-    const bool valid = (g < a.G) && (node < a.N) && (r < rows_used);
+    const bool valid = (g < a.G) && (node < a.N) && (r < rows_used) && !(node > 0 && s_par[node] == -1);
     const int mnode = valid ? node : 0;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const uint32_t colS = tmem + lane_base + x * kBN;
@@ -989,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ch = item % kChunks;
         const int xx = rr >= kRows ? 1 : 0, rt = rr - xx * kRows;
         const int gg = rt / a.NT, ii = i0[xx] + rt % a.NT;
-        if (gg >= a.G || ii >= a.N || rt >= rows_used) continue;
+        if (gg >= a.G || ii >= a.N || rt >= rows_used || (ii > 0 && s_par[ii] == -1)) continue;
         float2 mlv[kMaxSplits];
         float4 xv[kMaxSplits];
         const uint32_t moff = (uint32_t)(rr * 8);
@@ -1151,7 +1157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = t; c < a.N; c += kThreads - 64) {
       const int p = a.parent[(size_t)b * a.N + c];
       s_par[c] = p;
-      if (!((c == 0) ? (p == -1) : (p >= 0 && p < c))) bad = 1;
+      // trailing padding rows of a ragged batch hold parent -1; an active row must not
+      // follow one
+      const bool prev_pad = c >= 2 && a.parent[(size_t)b * a.N + c - 1] == -1;
+      if (!((c == 0) ? (p == -1) : (p == -1 || (p >= 0 && p < c && !prev_pad)))) bad = 1;
     }
     if (bad) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);
     for (int r = rows_used + t; r < 2 * kRows; r += kThreads - 64) {
@@ -1294,7 +1303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q4 * 32 + lane;
     const int g = r / a.NT, il = r % a.NT;
     const int node = i0[x] + il;
-    const bool valid = (g < a.G) && (node < a.N) && (r < rows_used);
+    const bool valid = (g < a.G) && (node < a.N) && (r < rows_used) && !(node > 0 && s_par[node] == -1);
     const int mnode = valid ? node : 0;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const uint32_t colS = tmem + lane_base + x * kRows;
@@ -1430,7 +1439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ch = item % kChunks;
         const int xx = rr >= kRows ? 1 : 0, rt = rr - xx * kRows;
         const int gg = rt / a.NT, ii = i0[xx] + rt % a.NT;
-        if (gg >= a.G || ii >= a.N || rt >= rows_used) continue;
+        if (gg >= a.G || ii >= a.N || rt >= rows_used || (ii > 0 && s_par[ii] == -1)) continue;
         float2 mlv[kMaxSplits];
         float4 xv[kMaxSplits];
         const uint32_t moff = (uint32_t)(rr * 8);

@@ -156,10 +156,14 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
     s_qc[c] = a.qc[(size_t)b * N + c];
     s_l2p[c] = a.lse2[(size_t)b * N + c];
     s_l2q[c] = a.lse2_q[(size_t)b * N + c];
-    const bool ok = (c == 0) ? (p == -1) : (p >= 0 && p < c);
+    // padding rows of a ragged batch (parent -1 after the last node) are no drafts
+    const bool ok = (c == 0) ? (p == -1) : (p == -1 || (p >= 0 && p < c));
     if (!ok) atomicOr(&s_bad, TV_DEV_BAD_TREE);
-    if (c > 0 && (t < 0 || t >= V)) atomicOr(&s_bad, TV_DEV_BAD_TOKEN);
+    if (c > 0 && p != -1 && (t < 0 || t >= V)) atomicOr(&s_bad, TV_DEV_BAD_TOKEN);
   }
+  __syncthreads();
+  for (int c = 2 + tid; c < N; c += blockDim.x)  // no active row after a padding row
+    if (s_par[c] != -1 && s_par[c - 1] == -1) atomicOr(&s_bad, TV_DEV_BAD_TREE);
   __syncthreads();
   if (s_bad) {
     if (crank == 0) {

@@ -3,6 +3,8 @@
 // PTD (Progressive Tree Drafting) §3.1 "tree construction": node v may attend only to
 // its observable prefix set pi(v) = {v} U pi(P(v)); its position encoding is fixed by
 // |pi(v)|.  One CTA of 1024 threads per sequence; parent[] lives in shared memory.
+// Ragged batches: rows after a sequence's last node hold parent -1 (trailing padding);
+// they get depth and position -1, an all-zero mask row and no place in the child lists.
 #include "philox.cuh"
 #include "tv_kernels.cuh"
 #include "tv_ptx.cuh"
@@ -16,16 +18,26 @@ __global__ void __launch_bounds__(1024) tree_prep_kernel(const int32_t* __restri
   __shared__ int s_par[kMaxNodes];
   __shared__ int s_cnt[kMaxNodes + 1];
   __shared__ int s_wsum[32];
-  __shared__ int s_bad;
+  __shared__ int s_bad, s_nact;
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int W = (N + 31) / 32;
-  if (tid == 0) s_bad = 0;
+  if (tid == 0) {
+    s_bad = 0;
+    s_nact = N;
+  }
   __syncthreads();
   for (int i = tid; i < N; i += blockDim.x) {
     const int p = parent[(size_t)b * N + i];
     s_par[i] = p;
     s_cnt[i] = 0;
-    if (!((i == 0) ? (p == -1) : (p >= 0 && p < i))) atomicOr(&s_bad, TV_DEV_BAD_TREE);
+    if (i >= 1 && p == -1) atomicMin(&s_nact, i);  // the first padding row
+  }
+  __syncthreads();
+  const int n = s_nact;  // active rows 0..n-1
+  for (int i = tid; i < N; i += blockDim.x) {
+    const int p = s_par[i];
+    const bool ok = (i == 0) ? (p == -1) : (i < n ? (p >= 0 && p < i) : (p == -1));
+    if (!ok) atomicOr(&s_bad, TV_DEV_BAD_TREE);
   }
   __syncthreads();
   if (s_bad) {
@@ -33,11 +45,18 @@ __global__ void __launch_bounds__(1024) tree_prep_kernel(const int32_t* __restri
     return;
   }
   for (int i = tid; i < N; i += blockDim.x) {
+    uint32_t* row = anc_mask ? anc_mask + ((size_t)b * N + i) * W : nullptr;
+    if (i >= n) {  // padding row
+      if (row)
+        for (int w = 0; w < W; ++w) row[w] = 0u;
+      if (depth) depth[(size_t)b * N + i] = -1;
+      if (pos) pos[(size_t)b * N + i] = -1;
+      continue;
+    }
     // walk i, parent(i), ..., root: indices strictly decrease, so words are visited
     // from high to low and each mask word is written exactly once
     int a = i, d = -1, cw = W - 1;
     uint32_t bits = 0;
-    uint32_t* row = anc_mask ? anc_mask + ((size_t)b * N + i) * W : nullptr;
     while (a >= 0) {
       const int w = a >> 5;
       while (cw > w) {
@@ -87,18 +106,16 @@ __global__ void __launch_bounds__(1024) tree_prep_kernel(const int32_t* __restri
     s_cnt[tid] = excl;
     child_off[(size_t)b * (N + 1) + tid] = excl;
   }
-  if (tid == 0) child_off[(size_t)b * (N + 1) + N] = N - 1;
+  if (tid == 0) child_off[(size_t)b * (N + 1) + N] = n - 1;
   __syncthreads();
-  for (int c = tid + 1; c < N; c += blockDim.x) {
-    if (c >= N) break;
+  for (int c = tid + 1; c < n; c += blockDim.x) {
     const int u = s_par[c];
     int rank = 0;
     for (int j = u + 1; j < c; ++j) rank += (s_par[j] == u);
     child_idx[(size_t)b * N + s_cnt[u] + rank] = c;
   }
-  if (tid == 0 && N >= 1) child_idx[(size_t)b * N + N - 1] = -1;
-  // (slot N-1 is only used when N-1 children exist; a tree has N-1 edges, so the
-  // list fills slots 0..N-2 and the last slot is padding)
+  // n active nodes have n - 1 edges: the list fills slots 0..n-2, the rest hold -1
+  for (int j = n - 1 + tid; j < N; j += blockDim.x) child_idx[(size_t)b * N + j] = -1;
 }
 
 cudaError_t launch_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* depth, int32_t* pos,

@@ -314,9 +314,11 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) 
       sm.xc[c] = x;
       if (a.sampling) sm.yc[c] = y;
       else sm.match[c] = 0x7fffffff;
-      const bool ok = (c == 0) ? (p == -1) : (p >= 0 && p < c);
+      // a padding row of a ragged batch (parent -1 after the last node) is no draft:
+      // its token is not checked; the rule that padding is trailing is checked below
+      const bool ok = (c == 0) ? (p == -1) : (p == -1 || (p >= 0 && p < c));
       if (!ok) atomicOr(&s_bad, TV_DEV_BAD_TREE);
-      if (c > 0 && (t < 0 || t >= V)) atomicOr(&s_bad, TV_DEV_BAD_TOKEN);
+      if (c > 0 && p != -1 && (t < 0 || t >= V)) atomicOr(&s_bad, TV_DEV_BAD_TOKEN);
     }
     if (stage_item) sm.stage[c] = v;
   }
@@ -328,6 +330,8 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) 
     __syncthreads();
     for (int u = tid; u < N; u += blockDim.x) {
       const long long ug = r0 + u;
+      const bool pad = u > 0 && sm.par[u] == -1;
+      if (pass == 0 && u >= 2 && !pad && sm.par[u - 1] == -1) atomicOr(&s_bad, TV_DEV_BAD_TREE);
       const int cover = (int)(c_last(ug, a) - c_first(ug, a) + 1);
       VocabPartial r = none;
       for (int k = 0; k < cover; ++k) {
@@ -340,12 +344,12 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) 
         sm.lse2[u] = l2;
         sm.am[u] = r.ai;
         if (a.sampling) a.lse2[ug] = l2;  // the sampling walk kernel reads these
-        if (a.row_lse) a.row_lse[ug] = l2 * kLn2;
-        if (a.row_argmax) a.row_argmax[ug] = r.ai;
+        if (a.row_lse) a.row_lse[ug] = pad ? __int_as_float(0x7fc00000) : l2 * kLn2;  // NaN: no row
+        if (a.row_argmax) a.row_argmax[ug] = pad ? -1 : r.ai;
       } else {
         sm.lse2q[u] = l2;
         a.lse2_q[ug] = l2;
-        if (a.row_lse_q) a.row_lse_q[ug] = l2 * kLn2;
+        if (a.row_lse_q) a.row_lse_q[ug] = pad ? __int_as_float(0x7fc00000) : l2 * kLn2;
       }
     }
     __syncthreads();
@@ -357,7 +361,7 @@ __device__ void sequence_epilogue(const VocabArgs& a, int b, const EpiSmem& sm) 
   // (lowest index if several)
   for (int c = tid; c < N; c += blockDim.x) {
     float pv = __int_as_float(0x7fc00000), qv = pv;
-    if (c > 0 && !bad) {
+    if (c > 0 && !bad && sm.par[c] >= 0) {
       const int u = sm.par[c];
       pv = ptx::ex2(fmaf(sm.xc[c], a.c2, -sm.lse2[u]));
       if (a.sampling)
