@@ -690,6 +690,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
       }
     }
   };
+  // a capture is retired once taken, so that the next piece to stop at is the earliest
+  // of the captures still pending (a thread owns two children when N > 513)
   auto capture = [&](int pc, int bs, const unsigned char* stage) {
 #pragma unroll
     for (int k = 0; k < 2; ++k)
@@ -697,6 +699,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) vocab_pass_tma_kernel(VocabArg
         const size_t c = (size_t)bs * a.N + 1 + tid + k * kTmaThreads;
         a.xc[c] = to_f32(reinterpret_cast<const T*>(stage)[cap_off[k]]);
         if (kArrays == 2) a.yc[c] = to_f32(reinterpret_cast<const T*>(stage + kPieceBytes)[cap_off[k]]);
+        cap_pc[k] = -1;
       }
   };
   fetch_tree(b_first);  // issued ahead of the bulk copies, so that it does not queue behind them
