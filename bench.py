@@ -696,8 +696,11 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         g_all = capture(lambda: [step(s) for s in sets])          # one step per input set
         g_one = [capture(lambda s=s: step(s)) for s in sets]
-        # one graph per kernel family covering every input set (launch overhead amortised
-        # the same way as in the step graph)
+    # one graph per kernel family covering every input set (launch overhead amortised the
+    # same way as in the step graph), each kernel alone on the whole device: the SM split
+    # above is for running attention and verify side by side
+    tv.set_sm_partition(0, 0)
+    with torch.cuda.stream(stream):
         fam_graphs = {"attention": capture(lambda: [k_attn(s) for s in sets]),
                       "verify": capture(lambda: [k_verify(s) for s in sets]),
                       "vocab": capture(lambda: [k_vocab(s) for s in sets]),
@@ -709,6 +712,7 @@ def run_ours(args):
             fam_graphs["select"] = capture(lambda: [k_select(s) for s in sets])
             fam_graphs["select_adaptive"] = capture(lambda: [k_select_adaptive(s) for s in sets])
     torch.cuda.synchronize()
+    tv.set_sm_partition(*sm_partition)
 
     def timed(fn, reps):
         ev0 = torch.cuda.Event(enable_timing=True)
@@ -787,6 +791,9 @@ def run_ours(args):
     # (written into cache rows P..P+N-1), the target (and draft) logits and the
     # candidate pool.  Those are copied in from pinned host memory every step, and the
     # accept outcome is copied back.
+    # Two device input sets alternate: the copies of round i + 1 run on a copy stream while
+    # round i computes (each round's copies finish before its compute starts, and a set
+    # is refilled only after the round that read it has finished).
     round_in = {"q": (host["q"], lambda d: d["q"]),
                 "k_tree": (np.ascontiguousarray(host["k"][:, :, P:P + N]), lambda d: d["k"][:, :, P:P + N]),
                 "v_tree": (np.ascontiguousarray(host["v"][:, :, P:P + N]), lambda d: d["v"][:, :, P:P + N]),
@@ -798,35 +805,56 @@ def run_ours(args):
         round_in["ptok"] = (host["ptok"], lambda d: d["ptok"])
     pinned = {kk: ((to_dev(vv) if kk not in ("marg", "ptok") else torch.from_numpy(vv)).cpu().pin_memory(), where)
               for kk, (vv, where) in round_in.items()}
-    res_host = {kk: torch.empty_like(ver_out[kk], device="cpu").pin_memory()
-                for kk in (("accepted_nodes", "accept_len", "out_token") if sampling_mode else
-                           ("accepted_nodes", "accept_len", "bonus_token"))}
+    res_host = [{kk: torch.empty_like(ver_out[kk], device="cpu").pin_memory()
+                 for kk in (("accepted_nodes", "accept_len", "out_token") if sampling_mode else
+                            ("accepted_nodes", "accept_len", "bonus_token"))} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t, _ in pinned.values())
-    d2h = sum(t.numel() * t.element_size() for t in res_host.values())
-    dst = sets[0]
-    dst_views = {kk: where(dst) for kk, (_, where) in pinned.items()}
+    d2h = sum(t.numel() * t.element_size() for t in res_host[0].values())
+    dsts = sets[:2] if n_sets >= 2 else [sets[0], {kk: t.clone() for kk, t in sets[0].items()}]
+    dst_views = [{kk: where(d) for kk, (_, where) in pinned.items()} for d in dsts]
     e2e_steps = max(20, min(2000, args.steps // 20))
+    copy_stream = torch.cuda.Stream(device=dev)
 
-    def copies_in():
+    def copies_in(j):
         for kk, (t, _) in pinned.items():
-            dst_views[kk].copy_(t, non_blocking=True)
+            dst_views[j][kk].copy_(t, non_blocking=True)
 
-    def copies_out():
-        for kk, t in res_host.items():
+    def copies_out(j):
+        for kk, t in res_host[j].items():
             t.copy_(ver_out[kk], non_blocking=True)
 
     def e2e(k):
-        with torch.cuda.stream(stream):
-            for _ in range(k):
-                copies_in()
-                step(dst)
-                copies_out()
+        # copy stream: inputs of round i into set i % 2; compute stream: round i, then its
+        # outcome back to the host
+        done = [None, None]
+        ready = torch.cuda.Event()
+        copy_stream.wait_stream(stream)  # after the timed region's start event
+        with torch.cuda.stream(copy_stream):
+            copies_in(0)
+            ready.record()
+        for i in range(k):
+            j = i % 2
+            stream.wait_event(ready)
+            if i + 1 < k:
+                with torch.cuda.stream(copy_stream):
+                    if done[1 - j] is not None:
+                        copy_stream.wait_event(done[1 - j])
+                    copies_in(1 - j)
+                    ready = torch.cuda.Event()
+                    ready.record()
+            with torch.cuda.stream(stream):
+                step(dsts[j])
+                copies_out(j)
+                ev = torch.cuda.Event()
+                ev.record()
+                done[j] = ev
+        stream.wait_stream(copy_stream)
 
     def copies_only(k):
         with torch.cuda.stream(stream):
-            for _ in range(k):
-                copies_in()
-                copies_out()
+            for i in range(k):
+                copies_in(i % 2)
+                copies_out(i % 2)
 
     e2e(3)
     ms_e2e = max_over_ranks(timed(e2e, e2e_steps), world, dev)
@@ -876,7 +904,8 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps, "ms_per_step": ms_e2e / e2e_steps,
                     "copied": "per round: " + ", ".join(pinned) + "; the prefix KV cache rows 0..P-1 stay on the "
-                              "device across rounds",
+                              "device across rounds; the next round's copies overlap this round's compute "
+                              "(two device input sets)",
                     "copy_ms_per_step": ms_copy, "h2d_gbs": h2d / (ms_copy * 1e-3) / 1e9,
                     "copy_probe_gbs": {w: probe_bytes / (best[w] * 1e-3) / 1e9 for w in best}},
             "gpu_launches": launches_per_step * args.steps,
