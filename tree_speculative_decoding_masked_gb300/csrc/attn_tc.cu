@@ -173,13 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int mt = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
   const int hk = blockIdx.y, b = blockIdx.z;
   const int i0 = mt * a.NT;
-  const int nodes_hi = min(a.N, i0 + a.NT);
-  const int ltot = a.P + nodes_hi;
-  const int t_all = (ltot + kBN - 1) / kBN;
-  const int tps = (t_all + a.splits - 1) / a.splits;
-  const int t_begin = split * tps;
-  const int nt = max(0, min(t_all, t_begin + tps) - t_begin);
   const int rows_used = a.G * a.NT;
+  __shared__ int s_wfirst[kThreads / 32];  // per warp: first padding row it saw (or N)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->q_full, 1);
@@ -209,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 2) {
     // parent array for the mask; zero the Q rows that no TMA box fills
     const int t = threadIdx.x - 64;
-    int bad = 0;
+    int bad = 0, first_pad = a.N;
     for (int c = t; c < a.N; c += kThreads - 64) {
       const int p = a.parent[(size_t)b * a.N + c];
       s_par[c] = p;
@@ -217,7 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // follow one
       const bool prev_pad = c >= 2 && a.parent[(size_t)b * a.N + c - 1] == -1;
       if (!((c == 0) ? (p == -1) : (p == -1 || (p >= 0 && p < c && !prev_pad)))) bad = 1;
+      if (c > 0 && p == -1) first_pad = min(first_pad, c);
     }
+    first_pad = __reduce_min_sync(0xffffffffu, first_pad);
+    if (lane == 0) s_wfirst[warp] = first_pad;
     if (bad) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);
     for (int r = rows_used + t; r < kRows; r += kThreads - 64)
       for (int db = 0; db < C::kDB; ++db) {
@@ -231,6 +229,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // active rows 0..n_act-1 (a ragged batch pads with parent -1): keys and row tiles past
+  // them are never needed
+  int n_act = a.N;
+#pragma unroll
+  for (int w = 2; w < kThreads / 32; ++w) n_act = min(n_act, s_wfirst[w]);
+  const int nodes_hi = min(n_act, i0 + a.NT);
+  const int t_all = i0 < n_act ? (a.P + nodes_hi + kBN - 1) / kBN : 0;
+  const int tps = (t_all + a.splits - 1) / a.splits;
+  const int t_begin = split * tps;
+  const int nt = max(0, min(t_all, t_begin + tps) - t_begin);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producers
@@ -1113,20 +1121,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mp = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
   const int hk = blockIdx.y, b = blockIdx.z;
-  int i0[2], t_allx[2];
+  int i0[2];
 #pragma unroll
-  for (int x = 0; x < 2; ++x) {
-    i0[x] = (2 * mp + x) * a.NT;
-    t_allx[x] = i0[x] < a.N ? (a.P + min(a.N, i0[x] + a.NT) + kBN2 - 1) / kBN2 : 0;
-  }
-  const int t_all = max(t_allx[0], t_allx[1]);
-  const int tps = (t_all + a.splits - 1) / a.splits;
-  const int t_begin = split * tps;
-  int ntx[2];
-#pragma unroll
-  for (int x = 0; x < 2; ++x) ntx[x] = max(0, min(t_allx[x], t_begin + tps) - t_begin);
-  const int nt = max(ntx[0], ntx[1]);
+  for (int x = 0; x < 2; ++x) i0[x] = (2 * mp + x) * a.NT;
   const int rows_used = a.G * a.NT;
+  __shared__ int s_wfirst[kThreads / 32];  // per warp: first padding row it saw (or N)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->q_full, 1);
@@ -1153,7 +1152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp >= 2) {
     const int t = threadIdx.x - 64;
-    int bad = 0;
+    int bad = 0, first_pad = a.N;
     for (int c = t; c < a.N; c += kThreads - 64) {
       const int p = a.parent[(size_t)b * a.N + c];
       s_par[c] = p;
@@ -1161,7 +1160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // follow one
       const bool prev_pad = c >= 2 && a.parent[(size_t)b * a.N + c - 1] == -1;
       if (!((c == 0) ? (p == -1) : (p == -1 || (p >= 0 && p < c && !prev_pad)))) bad = 1;
+      if (c > 0 && p == -1) first_pad = min(first_pad, c);
     }
+    first_pad = __reduce_min_sync(0xffffffffu, first_pad);
+    if (lane == 0) s_wfirst[warp] = first_pad;
     if (bad) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);
     for (int r = rows_used + t; r < 2 * kRows; r += kThreads - 64) {
       const int x = r >= kRows ? 1 : 0, rr = r - x * kRows;
@@ -1178,6 +1180,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // active rows 0..n_act-1 (a ragged batch pads with parent -1): keys and row tiles past
+  // them are never needed
+  int n_act = a.N;
+#pragma unroll
+  for (int w = 2; w < kThreads / 32; ++w) n_act = min(n_act, s_wfirst[w]);
+  int t_allx[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) t_allx[x] = i0[x] < n_act ? (a.P + min(n_act, i0[x] + a.NT) + kBN2 - 1) / kBN2 : 0;
+  const int t_all = max(t_allx[0], t_allx[1]);
+  const int tps = (t_all + a.splits - 1) / a.splits;
+  const int t_begin = split * tps;
+  int ntx[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) ntx[x] = max(0, min(t_allx[x], t_begin + tps) - t_begin);
+  const int nt = max(ntx[0], ntx[1]);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producers
