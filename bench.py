@@ -657,7 +657,7 @@ def run_ours(args):
         nt = (128 // G) // 8 * 8
         mtiles = -(-N // nt)
         ctas = B * Hkv * (-(-mtiles // 2) if kern >= 2 else mtiles) * spl
-        if kern and ctas < n_sm:
+        if kern in (1, 2, 3) and ctas < n_sm:  # the persistent grid (4) fills the device
             parts.append((n_sm - ctas, ctas))
     candidates = [(part, vm) for part in parts for vm in (False, True)]
     trial, trial_reps = {}, {}
@@ -772,8 +772,11 @@ def run_ours(args):
     visible = int(B * N * P + (depth + 1).sum())
     flops_alg = 4 * Hq * D * visible
     flops_dense = 4 * B * Hq * N * (P + N) * D
+    tv.set_sm_partition(0, 0)  # the plan of the attention family, timed on the whole device
     attn_kernel, attn_splits = tv.tree_attention_plan(B, Hq, Hkv, D, P, N, tdt)
-    attn_name = ("attn_simt_kernel", "attn_tc_kernel", "attn_pair_kernel", "attn_pair2_kernel")[attn_kernel]
+    tv.set_sm_partition(*sm_partition)
+    attn_name = ("attn_simt_kernel", "attn_tc_kernel", "attn_pair_kernel", "attn_pair2_kernel",
+                 "attn_stream_kernel")[attn_kernel]
     rooflines = {
         attn_name: roofline_entry(attn_name, bytes_attn, flops_alg if bf16 else 0, br["attention"] * 1e-6,
                                   args.workload),

@@ -145,9 +145,17 @@ TV_API tv_status tv_set_sm_partition(int verify_sms, int attention_sms);
  *   2  paired row tiles: one CTA streams the KV range once for two 128-row tiles
  *   3  paired row tiles with 64-key KV tiles and two S buffers per row tile, so S of
  *      the next KV tile is computed while the softmax of the current one runs
- * Both compute the same result (up to fp32 summation order); the switch exists to
+ *   4  variant 3's pipeline on a persistent grid of one CTA per SM (of the attention's
+ *      share): the 64-key steps of all tile pairs are cut into equal contiguous ranges,
+ *      one per CTA, so that the device stays busy when the tile pairs do not fill a
+ *      whole number of waves; a tile pair cut between CTAs is merged through the
+ *      workspace by the CTA that finishes its last piece.  Needs the workspace; shapes
+ *      whose ranges would hold more than 8 pieces run variant 3.  Measured 3-6 %
+ *      slower than variant 3 on the long-context shapes, which run at the GB300's power
+ *      limit (more busy SMs lower the clock), so the automatic choice never takes it.
+ * All compute the same result (up to fp32 summation order); the switch exists to
  * compare and test them.  Process-wide, host-side; affects launches made after the call.
- * Errors: a value outside 0..3 -> TV_ERR_VALUE.
+ * Errors: a value outside 0..4 -> TV_ERR_VALUE.
  */
 TV_API tv_status tv_set_attention_variant(int variant);
 
@@ -222,13 +230,18 @@ TV_API tv_status tv_prune_tree(const int32_t* parent, const float* conf, int B, 
  * bf16 with D in {64, 128}, G <= 16 and G * N >= 64 runs on the tensor cores; every
  * other case (fp32, other D, small trees) runs on the CUDA-core kernel.
  * Alignment: q, k_cache, v_cache, out 16-byte aligned.
- * Workspace: tv_tree_attention_workspace_size(...) bytes; that is 0 for every shape the
- * library takes today (split-KV partials are merged through the thread-block cluster's
- * distributed shared memory), and workspace may then be NULL.
+ * Workspace (optional): tv_tree_attention_workspace_size(...) bytes, 16-byte aligned,
+ * owned by the caller, device memory, no initial contents required.  It is nonzero only
+ * where the plan is the persistent schedule (variant 4 of tv_set_attention_variant),
+ * whose CTAs park partial rows of the units they share there; with a NULL or smaller
+ * workspace that call runs the paired 64-key kernel (variant 3) unsplit instead, with
+ * the same results up to fp32 summation order.  Split-KV partials of the other variants are merged through the
+ * thread-block cluster's distributed shared memory.  Calls that share a workspace must
+ * be ordered (one stream, or events).
  * Errors: NULL pointers -> TV_ERR_NULL; dtype -> TV_ERR_DTYPE; sizes, B * Hkv or the
  * grid outside the launch limits -> TV_ERR_SHAPE; scale < 0, NaN or infinite ->
- * TV_ERR_VALUE; misaligned pointers -> TV_ERR_ALIGN; a workspace smaller than the
- * query -> TV_ERR_WORKSPACE; a failed launch -> TV_ERR_CUDA.  Tree structure problems
+ * TV_ERR_VALUE; misaligned pointers (workspace included) -> TV_ERR_ALIGN; a failed
+ * launch -> TV_ERR_CUDA.  Tree structure problems
  * found on the device (node 0 not a root, or a parent index not below its node) and a
  * bounded wait that ran out are written to *dev_status.
  */
@@ -239,12 +252,13 @@ TV_API size_t tv_tree_attention_workspace_size(int B, int Hq, int Hkv, int D, in
  * (tv_set_attention_variant, tv_set_attention_splits, tv_set_sm_partition):
  *   *kernel  0 CUDA-core kernel (fp32, or shapes the tensor-core kernels do not take),
  *            1 tensor-core kernel with one 128-row tile per CTA, 2 paired row tiles,
- *            3 paired row tiles with 64-key KV tiles and double-buffered S
- *   *splits  KV ranges per tile group, merged in one thread-block cluster
+ *            3 paired row tiles with 64-key KV tiles and double-buffered S,
+ *            4 variant 3 on a persistent grid (given the queried workspace)
+ *   *splits  KV ranges per tile group, merged in one thread-block cluster (1 for 4)
  * Automatic choice: the variant and split count that minimise a wave model of the run
  * time (waves of resident clusters x (KV tiles per CTA + fixed per-CTA and merge costs))
- * fitted to GB300 measurements.  Queries the device's cluster occupancy (needs a
- * current CUDA device); launches nothing.
+ * fitted to GB300 measurements.  Queries the device's cluster occupancy
+ * (needs a current CUDA device); launches nothing.
  * Errors: NULL outputs -> TV_ERR_NULL; bad dtype -> TV_ERR_DTYPE; sizes -> TV_ERR_SHAPE.
  */
 TV_API tv_status tv_tree_attention_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype,

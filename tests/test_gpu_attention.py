@@ -232,7 +232,8 @@ def test_bad_tree_flagged():
         assert int(st.item()) & tv.TV_DEV_BAD_TREE
 
 
-@pytest.fixture(params=[1, 2, 3], ids=["one_tile_per_cta", "paired_tiles", "paired_tiles_64key_double_s"])
+@pytest.fixture(params=[1, 2, 3, 4],
+                ids=["one_tile_per_cta", "paired_tiles", "paired_tiles_64key_double_s", "persistent_grid"])
 def variant(request):
     tv.set_attention_variant(request.param)
     yield request.param
@@ -296,6 +297,55 @@ def test_workloads_sampled_64key_double_s(name):
         tv.set_attention_variant(0)
 
 
+@pytest.mark.parametrize("name", ["long_context", "sampling", "budget_sweep"])
+def test_workloads_sampled_persistent_grid(name):
+    tv.set_attention_variant(4)
+    try:
+        _sampled_rows(name, 24, seed_extra=7)
+    finally:
+        tv.set_attention_variant(0)
+
+
+@pytest.mark.parametrize("share", [16, 40, 0])
+def test_persistent_grid_many_pieces_per_cta(share):
+    # four tile pairs per (sequence, KV head) of 1..4 64-key steps, 80 steps in all: on
+    # 16 SMs a CTA's range of 5 steps holds up to seven pieces (whole units between a
+    # partial one at each end), on 40 up to four, on the whole device (80 CTAs) one step
+    # each, a 4-step unit merged from four CTAs; every cut matches the oracle
+    B, Hq, Hkv, D, P, N = 4, 8, 2, 64, 0, 256
+    g = synth.rng(41 + share)
+    par, _ = W.trees(g, B, N, 9, 100)
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, True)
+    tv.set_attention_variant(4)
+    tv.set_sm_partition(0, share)
+    try:
+        assert tv.tree_attention_plan(B, Hq, Hkv, D, P, N, torch.bfloat16) == (4, 1)
+        _check_all(q, k, v, par, P, True)
+    finally:
+        tv.set_attention_variant(0)
+        tv.set_sm_partition(0, 0)
+
+
+def test_persistent_grid_without_workspace_runs_paired_kernel():
+    # a workspace smaller than the query: the same result through the unsplit paired kernel
+    B, Hq, Hkv, D, P, N = 2, 8, 2, 128, 3000, 64
+    g = synth.rng(44)
+    par, _ = W.trees(g, B, N, 6, 100)
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, True)
+    tv.set_attention_variant(4)
+    try:
+        assert tv.tree_attention_workspace_size(B, Hq, Hkv, D, P, N, torch.bfloat16) > 0
+        st = torch.zeros(1, dtype=torch.int32, device=dev())
+        out = tv.tree_attention(to_dev(q, True), to_dev(k, True), to_dev(v, True), i32(par), P,
+                                workspace=torch.zeros(256, dtype=torch.uint8, device=dev()), dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        ref = attention.tree_attention(q, k, v, par, P)
+        assert np.max(np.abs(host(out) - ref)) < 2e-2
+    finally:
+        tv.set_attention_variant(0)
+
+
 @pytest.mark.parametrize("splits", [1, 3, 8])
 def test_forced_splits_both_variants(variant, splits):
     # every split count merges to the same result, including more splits than a short
@@ -326,7 +376,7 @@ def test_attention_plan_query_and_overrides():
     # for fp32; forced variants and split counts are what the query then reports
     assert tv.tree_attention_plan(1, 4, 1, 64, 128, 16, torch.float32) == (0, 1)
     k, s = tv.tree_attention_plan(8, 32, 8, 128, 32768, 128, torch.bfloat16)
-    assert k in (1, 3) and 1 <= s <= 8
+    assert k in (1, 3, 4) and 1 <= s <= 8
     try:
         tv.set_attention_variant(1)
         tv.set_attention_splits(3)
@@ -336,6 +386,10 @@ def test_attention_plan_query_and_overrides():
         assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16)[0] == 2
         tv.set_attention_variant(3)
         assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16)[0] == 3
+        tv.set_attention_variant(4)
+        assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16) == (4, 1)
+        tv.set_attention_splits(3)  # a forced split count: the paired kernel with splits
+        assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16) == (3, 3)
     finally:
         tv.set_attention_variant(0)
         tv.set_attention_splits(0)

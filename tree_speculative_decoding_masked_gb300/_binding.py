@@ -292,7 +292,7 @@ def tree_attention_workspace_size(B, Hq, Hkv, D, P, N, dtype) -> int:
 def tree_attention_plan(B, Hq, Hkv, D, P, N, dtype):
     """(kernel, splits) that tree_attention would launch: kernel 0 CUDA cores, 1 one
     128-row tile per CTA, 2 paired row tiles, 3 paired row tiles with 64-key KV tiles and
-    double-buffered S (tensor cores)."""
+    double-buffered S, 4 variant 3 on a persistent grid (tensor cores)."""
     code = TV_BF16 if dtype == torch.bfloat16 else TV_F32
     kern, spl = ctypes.c_int(0), ctypes.c_int(0)
     _check("tv_tree_attention_plan", load_library().tv_tree_attention_plan(
@@ -303,7 +303,9 @@ def tree_attention_plan(B, Hq, Hkv, D, P, N, dtype):
 def tree_attention(q, k_cache, v_cache, parent, prefix_len: int, *, scale: float = 0.0, out=None, workspace=None,
                    dev_status=None):
     """Tree-masked GQA attention.  q [B][Hq][N][D]; k_cache, v_cache [B][Hkv][S][D] with
-    S >= prefix_len + N; parent int32 [B][N]."""
+    S >= prefix_len + N; parent int32 [B][N].  workspace: uint8 device tensor of
+    tree_attention_workspace_size bytes for the persistent schedule (allocated here when
+    omitted; a smaller one runs the paired kernel unsplit)."""
     dev = _need_cuda(q=q, k_cache=k_cache, v_cache=v_cache, parent=parent, out=out)
     _ndim("q", q, 4)
     _ndim("k_cache", k_cache, 4)
@@ -321,8 +323,9 @@ def tree_attention(q, k_cache, v_cache, parent, prefix_len: int, *, scale: float
         out = torch.empty_like(q)
     elif out.dtype != q.dtype or out.shape != q.shape:
         raise ValueError("out must have q's shape and dtype")
+    # the workspace is optional here: a smaller one runs the plan that needs none
     ws_need = tree_attention_workspace_size(B, Hq, Hkv, D, prefix_len, N, q.dtype)
-    ws = _workspace(ws_need, dev, workspace)
+    ws = _workspace(0 if workspace is not None else ws_need, dev, workspace)
     st = _status_tensor(dev_status, dev)
     with _on(dev):
         _check("tv_tree_attention",

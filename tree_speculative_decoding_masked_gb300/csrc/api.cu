@@ -13,7 +13,8 @@ using namespace tv;
 // SM shares for running the vocab pass and the tree attention concurrently (0 = all SMs)
 static std::atomic<int> g_sm_verify{0}, g_sm_attention{0};
 // tensor-core attention kernel: 0 automatic, 1 one row tile per CTA, 2 paired row tiles,
-// 3 paired row tiles with 64-key KV tiles and double-buffered S
+// 3 paired row tiles with 64-key KV tiles and double-buffered S, 4 variant 3 on a
+// persistent grid
 static std::atomic<int> g_attn_variant{0};
 // KV splits per tensor-core attention CTA group: 0 automatic, else forced (capped at the
 // KV tile count and the cluster limit)
@@ -85,7 +86,7 @@ tv_status tv_set_sm_partition(int verify_sms, int attention_sms) {
 }
 
 tv_status tv_set_attention_variant(int variant) {
-  if (variant < 0 || variant > 3) return TV_ERR_VALUE;
+  if (variant < 0 || variant > 4) return TV_ERR_VALUE;
   g_attn_variant.store(variant, std::memory_order_relaxed);
   return TV_OK;
 }
@@ -136,10 +137,10 @@ tv_status tv_tree_attention(const void* q, const void* k_cache, const void* v_ca
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return TV_ERR_ALIGN;
   AttnPlan p = attn_plan(B, Hq, Hkv, D, P, N, dtype);
   if (p.tc) {
-    if (p.total > 0 && (!workspace || ws_bytes < p.total)) return TV_ERR_WORKSPACE;
     if (B > 65535 || Hkv > 65535) return TV_ERR_SHAPE;
+    if (workspace && !aligned16(workspace)) return TV_ERR_ALIGN;
     return cuda_status(launch_attn_tc(q, k_cache, v_cache, out, parent, B, Hq, Hkv, D, P, N, kv_stride_tokens, scale,
-                                      p, reinterpret_cast<char*>(workspace), dev_status, st(stream)));
+                                      p, reinterpret_cast<char*>(workspace), ws_bytes, dev_status, st(stream)));
   }
   if ((long long)B * Hq * N / 4 + 1 > 0x7fffffffLL) return TV_ERR_SHAPE;
   return cuda_status(launch_attn_simt(q, k_cache, v_cache, out, parent, B, Hq, Hkv, D, P, N, kv_stride_tokens, scale,

@@ -1505,6 +1505,510 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------
+// attn_stream_kernel: the paired 64-key pipeline of attn_pair2_kernel under a persistent
+// schedule.  The work of a launch is the list of all (tile pair, 64-key KV tile) steps,
+// unit by unit (a unit = one tile pair of one (sequence, KV head)); every CTA of the
+// grid (one per SM of its share) takes an equal contiguous range of it, so that 128
+// units on 152 SMs keep every SM busy instead of leaving 24 idle.  A range covers whole
+// units and at most one partial unit at each end.  A partial unit's pieces write their
+// unnormalised O and (m, l) rows to the workspace; one acquire-release atomic per unit
+// counts them and the CTA that adds the last piece merges the rows and writes the output
+// (no CTA ever waits for another).  Per piece, the Q tiles are reloaded once the S
+// products of the previous piece are done (q_empty), and the first PV product of a piece
+// waits until the softmax warps have read the previous piece's O (o_free).
+constexpr int kMaxMP = 64;      // tile pairs per (sequence, KV head): N = 1024 rows at G = 16
+constexpr int kMaxPieces = 8;   // units one persistent CTA may touch (the plan keeps below it)
+
+struct StreamArgs {
+  long long W;          // 64-key steps of the whole launch
+  int C;                // CTAs
+  int MP;               // tile pairs per (sequence, KV head)
+  int Tg;               // steps per (sequence, KV head) = pre[MP]
+  int pre[kMaxMP + 1];  // prefix sums of the tile pairs' step counts
+  float* ws_o;          // [2C][256][D] unnormalised partial O rows
+  float2* ws_ml;        // [2C][256] (running max in log2 units, sum)
+  unsigned* cnt;        // [B * Hkv * MP] pieces of each unit finished
+};
+
+struct StreamPiece {
+  int g, mp, ta, tb;  // unit (g = sequence * Hkv + KV head, tile pair mp), steps [ta, tb)
+  int slot;           // workspace slot of a partial piece; -1 when the piece is its whole unit
+};
+
+struct StreamBars {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kPair2Slots];
+  uint64_t k_empty[kPair2Slots];
+  uint64_t v_full[kPair2Slots];
+  uint64_t v_empty[kPair2Slots];
+  uint64_t s_full[2][2];
+  uint64_t p_full[2][2];
+  uint64_t pv_done[2][2];
+  uint64_t o_done, o_free, s_done;
+  uint32_t tmem_base;
+  int abort;
+  int npiece;
+  int last;  // this CTA adds the last piece of the current unit
+  StreamPiece piece[kMaxPieces];
+};
+
+// the CTA whose range holds step w: the largest c with floor(c W / C) <= w
+__device__ __forceinline__ int stream_owner(long long w, const StreamArgs& s) {
+  return (int)((w * s.C + s.C - 1) / s.W);
+}
+__device__ __forceinline__ long long stream_start(int c, const StreamArgs& s) { return (long long)c * s.W / s.C; }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_stream_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, TcArgs a, const __grid_constant__ StreamArgs sa) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();  // before any global read or write
+  using C = Pair2Cfg<D>;
+  static_assert(sizeof(StreamBars) <= 512, "stream barriers fit the barrier region");
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t mis = ptx::smem_addr(smem_raw) & 1023u;
+  unsigned char* sm = smem_raw + ((1024u - mis) & 1023u);
+  unsigned char* sQ = sm + C::kOffQ;
+  unsigned char* sK = sm + C::kOffK;
+  unsigned char* sV = sm + C::kOffV;
+  int* s_par = reinterpret_cast<int*>(sm + C::kOffPar);
+  StreamBars* bars = reinterpret_cast<StreamBars*>(sm + C::kOffBar);
+  volatile int* abort_flag = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x;
+  const int rows_used = a.G * a.NT;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bars->q_full, 1);
+    ptx::mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < kPair2Slots; ++s) {
+      ptx::mbar_init(&bars->k_full[s], 1);
+      ptx::mbar_init(&bars->k_empty[s], 1);
+      ptx::mbar_init(&bars->v_full[s], 1);
+      ptx::mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x)
+      for (int u = 0; u < 2; ++u) {
+        ptx::mbar_init(&bars->s_full[x][u], 1);
+        ptx::mbar_init(&bars->p_full[x][u], 4);
+        ptx::mbar_init(&bars->pv_done[x][u], 1);
+      }
+    ptx::mbar_init(&bars->o_done, 1);
+    ptx::mbar_init(&bars->o_free, 8);
+    ptx::mbar_init(&bars->s_done, 1);
+    bars->abort = 0;
+    // this CTA's pieces: its range [start(c), start(c + 1)) cut at unit boundaries
+    const long long w0 = stream_start(cta, sa), w1 = stream_start(cta + 1, sa);
+    int np = 0;
+    for (long long w = w0; w < w1 && np < kMaxPieces; ++np) {
+      const int g = (int)(w / sa.Tg);
+      const int rr = (int)(w - (long long)g * sa.Tg);
+      int mp = 0;
+      while (sa.pre[mp + 1] <= rr) ++mp;
+      const int tmp = sa.pre[mp + 1] - sa.pre[mp];
+      const int ta = rr - sa.pre[mp];
+      const int tb = (int)min((long long)tmp, ta + (w1 - w));
+      StreamPiece pc{g, mp, ta, tb, -1};
+      if (ta > 0 || tb < tmp) pc.slot = 2 * cta + (w > w0 ? 1 : 0);  // first or last piece of the range
+      bars->piece[np] = pc;
+      w += tb - ta;
+    }
+    bars->npiece = np;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp >= 2) {
+    // zero the Q rows that no TMA box fills (the same rows in every unit)
+    const int t = threadIdx.x - 64;
+    for (int r = rows_used + t; r < 2 * kRows; r += kThreads - 64) {
+      const int x = r >= kRows ? 1 : 0, rr = r - x * kRows;
+      if (rr < rows_used) continue;
+      for (int db = 0; db < C::kDB; ++db) {
+        uint4* row = reinterpret_cast<uint4*>(sQ + x * C::kQTile + db * C::kQBlock + rr * 128);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) row[k] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int np = bars->npiece;
+
+  // per-piece geometry, identical in every role
+  auto geom = [&](const StreamPiece& pc, int* i0, int* ntx) {
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      i0[x] = (2 * pc.mp + x) * a.NT;
+      const int tall = i0[x] < a.N ? (a.P + min(a.N, i0[x] + a.NT) + kBN2 - 1) / kBN2 : 0;
+      ntx[x] = max(0, min(tall, pc.tb) - pc.ta);
+    }
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producers
+    if (lane == 0) {
+      int issued[kPair2Slots] = {0, 0, 0, 0};
+      long long gk = 0;
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmK);
+      for (int p = 0; p < np && !*abort_flag; ++p) {
+        const StreamPiece pc = bars->piece[p];
+        int i0[2], ntx[2];
+        geom(pc, i0, ntx);
+        const int b = pc.g / a.Hkv, hk = pc.g % a.Hkv;
+        const int nt = max(ntx[0], ntx[1]);
+        // Q of this unit once the S products of the previous piece are done
+        if (p > 0 && !ptx::mbar_wait(&bars->q_empty, (p - 1) & 1, abort_flag)) break;
+        uint32_t qbytes = 0;
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+          if (ntx[x] > 0) qbytes += (uint32_t)(rows_used * 128 * C::kDB);
+        ptx::mbar_arrive_expect_tx(&bars->q_full, qbytes);
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+          if (ntx[x] > 0)
+            for (int g = 0; g < a.G; ++g)
+              for (int db = 0; db < C::kDB; ++db)
+                ptx::tma_load_3d(sQ + x * C::kQTile + db * C::kQBlock + g * a.NT * 128, &tmQ, &bars->q_full,
+                                 db * 64, i0[x], b * a.Hq + hk * a.G + g);
+        for (int t = 0; t < nt; ++t, ++gk) {
+          const int ks = (int)(gk % kPair2Slots);
+          if (gk >= kPair2Slots &&
+              !ptx::mbar_wait(&bars->k_empty[ks], (uint32_t)((gk / kPair2Slots) - 1) & 1, abort_flag))
+            break;
+          unsigned char* dst = sK + ks * C::kTileBytes;
+          ptx::mbar_arrive_expect_tx(&bars->k_full[ks], (uint32_t)C::kTileBytes);
+          for (int db = 0; db < C::kDB; ++db)
+            ptx::tma_load_3d(dst + db * C::kKVBlock, &tmK, &bars->k_full[ks], db * 64, (pc.ta + t) * kBN2,
+                             b * a.Hkv + hk);
+          ++issued[ks];
+        }
+      }
+      if (np > 0) ptx::mbar_wait(&bars->q_full, (np - 1) & 1, abort_flag);
+      for (int s = 0; s < kPair2Slots; ++s)
+        if (issued[s]) ptx::mbar_wait(&bars->k_full[s], (issued[s] - 1) & 1, abort_flag);
+    } else if (lane == 1) {
+      int issued[kPair2Slots] = {0, 0, 0, 0};
+      long long gv = 0;
+      ptx::prefetch_tmap(&tmV);
+      for (int p = 0; p < np && !*abort_flag; ++p) {
+        const StreamPiece pc = bars->piece[p];
+        int i0[2], ntx[2];
+        geom(pc, i0, ntx);
+        const int b = pc.g / a.Hkv, hk = pc.g % a.Hkv;
+        const int nt = max(ntx[0], ntx[1]);
+        for (int t = 0; t < nt; ++t, ++gv) {
+          const int vs = (int)(gv % kPair2Slots);
+          if (gv >= kPair2Slots &&
+              !ptx::mbar_wait(&bars->v_empty[vs], (uint32_t)((gv / kPair2Slots) - 1) & 1, abort_flag))
+            break;
+          unsigned char* dst = sV + vs * C::kTileBytes;
+          ptx::mbar_arrive_expect_tx(&bars->v_full[vs], (uint32_t)C::kTileBytes);
+          for (int db = 0; db < C::kDB; ++db)
+            ptx::tma_load_3d(dst + db * C::kKVBlock, &tmV, &bars->v_full[vs], db * 64, (pc.ta + t) * kBN2,
+                             b * a.Hkv + hk);
+          ++issued[vs];
+        }
+      }
+      for (int s = 0; s < kPair2Slots; ++s)
+        if (issued[s]) ptx::mbar_wait(&bars->v_full[s], (issued[s] - 1) & 1, abort_flag);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ S issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = ptx::idesc_bf16(kRows, kBN2, false, false);
+      long long gk = 0;
+      int cs[2] = {0, 0};  // S products issued so far per row tile (buffer = cs & 1)
+      bool ok = true;
+      for (int p = 0; ok && p < np; ++p) {
+        const StreamPiece pc = bars->piece[p];
+        int i0[2], ntx[2];
+        geom(pc, i0, ntx);
+        const int nt = max(ntx[0], ntx[1]);
+        if (!ptx::mbar_wait(&bars->q_full, p & 1, abort_flag)) break;
+        for (int t = 0; ok && t < nt; ++t, ++gk) {
+          const int ks = (int)(gk % kPair2Slots);
+          if (!ptx::mbar_wait(&bars->k_full[ks], (uint32_t)(gk / kPair2Slots) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t kaddr = ptx::smem_addr(sK + ks * C::kTileBytes);
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (t >= ntx[x]) continue;
+            const int buf = cs[x] & 1;
+            // S overwrites the P of two products back in this buffer: wait for its PV
+            if (cs[x] >= 2 && !ptx::mbar_wait(&bars->pv_done[x][buf], ((cs[x] - 2) >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t qaddr = ptx::smem_addr(sQ + x * C::kQTile);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk & 3) * 32;
+              const uint64_t ad = ptx::sdesc_sw128(qaddr + (kk >> 2) * C::kQBlock + off, 16, 1024);
+              const uint64_t bd = ptx::sdesc_sw128(kaddr + (kk >> 2) * C::kKVBlock + off, 16, 1024);
+              ptx::mma_bf16_ss(tmem + x * kRows + buf * kBN2, ad, bd, idS, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(&bars->s_full[x][buf]);
+            ++cs[x];
+          }
+          if (ok) ptx::mma_commit(&bars->k_empty[ks]);
+        }
+        if (ok) ptx::mma_commit(&bars->q_empty);  // the Q tiles are free once these S products are done
+      }
+      ptx::mma_commit(&bars->s_done);
+      ptx::mbar_wait(&bars->s_done, 0, abort_flag);
+    }
+    __syncwarp();
+  } else if (warp == kThreads / 32 - 1) {
+    // ------------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t idO = ptx::idesc_bf16(kRows, D, false, true);
+      long long gv = 0;
+      int cp[2] = {0, 0};
+      bool ok = true;
+      for (int p = 0; ok && p < np; ++p) {
+        const StreamPiece pc = bars->piece[p];
+        int i0[2], ntx[2];
+        geom(pc, i0, ntx);
+        const int nt = max(ntx[0], ntx[1]);
+        // the first PV of a piece overwrites O: the softmax warps have read the last one
+        if (p > 0 && !ptx::mbar_wait(&bars->o_free, (p - 1) & 1, abort_flag)) break;
+        for (int t = 0; ok && t < nt; ++t, ++gv) {
+          const int vs = (int)(gv % kPair2Slots);
+          if (!ptx::mbar_wait(&bars->v_full[vs], (uint32_t)(gv / kPair2Slots) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t vaddr = ptx::smem_addr(sV + vs * C::kTileBytes);
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (t >= ntx[x]) continue;
+            const int buf = cp[x] & 1;
+            if (!ptx::mbar_wait(&bars->p_full[x][buf], (cp[x] >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t pcol = tmem + x * kRows + buf * kBN2;
+#pragma unroll
+            for (int kk = 0; kk < kBN2 / 16; ++kk) {
+              const uint64_t bd = ptx::sdesc_sw128(vaddr + kk * 16 * 128, C::kKVBlock, 1024);
+              ptx::mma_bf16_ts(tmem + C::kColO + x * kRows, pcol + kk * 8, bd, idO, (t > 0 || kk > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(&bars->pv_done[x][buf]);
+            ++cp[x];
+          }
+          if (ok) ptx::mma_commit(&bars->v_empty[vs]);
+        }
+        ptx::mma_commit(&bars->o_done);  // every product of this piece (phase p)
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax rows
+    const int x = (warp - 2) >> 2;
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int R = x * kRows + r;  // row of the pair (workspace row)
+    const int g = r / a.NT, il = r % a.NT;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const uint32_t colS = tmem + lane_base + x * kRows;
+    const uint32_t colO = tmem + lane_base + C::kColO + x * kRows;
+    const int st = threadIdx.x - 64;  // 0..255 over the softmax warps
+    int cs = 0;
+    int cur_b = -1;
+    bool ok = true;
+    for (int p = 0; p < np; ++p) {
+      const StreamPiece pc = bars->piece[p];
+      int i0[2], ntx[2];
+      geom(pc, i0, ntx);
+      const int b = pc.g / a.Hkv, hk = pc.g % a.Hkv;
+      if (b != cur_b) {  // the parent array of this piece's sequence
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        int bad = 0;
+        for (int c = st; c < a.N; c += 256) {
+          const int pr = a.parent[(size_t)b * a.N + c];
+          s_par[c] = pr;
+          const bool prev_pad = c >= 2 && a.parent[(size_t)b * a.N + c - 1] == -1;
+          if (!((c == 0) ? (pr == -1) : (pr == -1 || (pr >= 0 && pr < c && !prev_pad)))) bad = 1;
+        }
+        if (bad) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        cur_b = b;
+      }
+      const int node = i0[x] + il;
+      const bool valid = (g < a.G) && (node < a.N) && (r < rows_used) && !(node > 0 && s_par[node] == -1);
+      const int mnode = valid ? node : 0;
+      const int ntm = ntx[x];
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int t = 0; ok && t < ntm; ++t, ++cs) {
+        const int buf = cs & 1;
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->s_full[x][buf], (cs >> 1) & 1, abort_flag));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint64_t vis = key_mask((pc.ta + t) * kBN2, a.P, a.N, mnode, s_par);
+        float sv[64];
+        ptx::tmem_ld32(colS + buf * kBN2, sv);
+        ptx::tmem_ld32(colS + buf * kBN2 + 32, sv + 32);
+        ptx::tmem_wait_ld();
+        if (vis != ~0ull) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (!((vis >> j) & 1ull)) sv[j] = -INFINITY;
+        }
+        const float tms = max64(sv, -INFINITY) * a.c;
+        float alpha = 1.f;
+        bool need = false;
+        if (tms > m_run + kRescaleLog2) {
+          if (m_run != -INFINITY) {
+            alpha = ptx::ex2(m_run - tms);
+            need = true;
+          }
+          m_run = tms;
+        }
+        uint32_t pw[32];
+        const float lsum = exp_p64(sv, a.c, m_run, pw);
+        ptx::tmem_st32u(colS + buf * kBN2, pw);
+        if (__any_sync(0xffffffffu, need) && t > 0) {
+          ok = __all_sync(0xffffffffu,
+                          ptx::mbar_wait(&bars->pv_done[x][(cs - 1) & 1], ((cs - 1) >> 1) & 1, abort_flag));
+          if (!ok) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float ov[32];
+            ptx::tmem_ld32(colO + c0, ov);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) ov[k] *= alpha;
+            ptx::tmem_st32(colO + c0, ov);
+          }
+        }
+        l_run = l_run * alpha + lsum;
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->p_full[x][buf]);
+      }
+      // ---- epilogue of the piece: every product of it is complete at o_done (phase p)
+      const bool done = __all_sync(0xffffffffu, ptx::mbar_wait(&bars->o_done, p & 1, abort_flag));
+      if (done) ptx::tc_fence_after();
+      const bool have_o = done && ok && ntm > 0;
+      const size_t orow = (((size_t)b * a.Hq + hk * a.G + g) * a.N + node) * D;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      float4* wrow = reinterpret_cast<float4*>(sa.ws_o + ((size_t)max(pc.slot, 0) * 2 * kRows + R) * D);
+      // O in 32-column chunks: the output row (whole unit) or the parked partial row
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float ov[32];
+        if (have_o) {
+          ptx::tmem_ld32(colO + c0, ov);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] = 0.f;
+        }
+        if (pc.slot >= 0) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) wrow[c0 / 4 + k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+        } else if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow + c0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 u;
+            u.x = ptx::cvt_bf16x2(ov[8 * k + 0] * inv, ov[8 * k + 1] * inv);
+            u.y = ptx::cvt_bf16x2(ov[8 * k + 2] * inv, ov[8 * k + 3] * inv);
+            u.z = ptx::cvt_bf16x2(ov[8 * k + 4] * inv, ov[8 * k + 5] * inv);
+            u.w = ptx::cvt_bf16x2(ov[8 * k + 6] * inv, ov[8 * k + 7] * inv);
+            dst[k] = u;
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->o_free);  // O may be overwritten by the next piece
+      if (pc.slot < 0) continue;
+      // partial piece: count it; the CTA adding the last piece of the unit merges
+      sa.ws_ml[(size_t)pc.slot * 2 * kRows + R] = make_float2(have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
+      const int unit = pc.g * sa.MP + pc.mp;
+      const long long U0 = (long long)pc.g * sa.Tg + sa.pre[pc.mp];
+      const long long U1 = U0 + (sa.pre[pc.mp + 1] - sa.pre[pc.mp]);
+      const int c_lo = stream_owner(U0, sa), c_hi = stream_owner(U1 - 1, sa);
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (st == 0) {
+        const unsigned prev = ptx::atom_add_acq_rel_gpu(sa.cnt + unit, 1u);
+        bars->last = prev + 1 == (unsigned)(c_hi - c_lo + 1);
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (!bars->last) continue;
+      if (st == 0) sa.cnt[unit] = 0;  // ready for the next launch
+      if (!valid) continue;
+      // merge this row over the unit's pieces (CTAs c_lo..c_hi), 32 columns at a time
+      float M = -INFINITY;
+      for (int c = c_lo; c <= c_hi; ++c) {
+        const int slot = 2 * c + ((c == c_lo && U0 > stream_start(c, sa)) ? 1 : 0);
+        M = fmaxf(M, __ldcg(&sa.ws_ml[(size_t)slot * 2 * kRows + R]).x);
+      }
+      float L = 0.f;
+      for (int c = c_lo; c <= c_hi; ++c) {
+        const int slot = 2 * c + ((c == c_lo && U0 > stream_start(c, sa)) ? 1 : 0);
+        const float2 ml = __ldcg(&sa.ws_ml[(size_t)slot * 2 * kRows + R]);
+        if (ml.x != -INFINITY) L = fmaf(ml.y, ptx::ex2(ml.x - M), L);
+      }
+      const float minv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float ov[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) ov[k] = 0.f;
+        for (int c = c_lo; c <= c_hi; ++c) {
+          const int slot = 2 * c + ((c == c_lo && U0 > stream_start(c, sa)) ? 1 : 0);
+          const float2 ml = __ldcg(&sa.ws_ml[(size_t)slot * 2 * kRows + R]);
+          if (ml.x == -INFINITY) continue;
+          const float w = ptx::ex2(ml.x - M);
+          const float4* src = reinterpret_cast<const float4*>(sa.ws_o + ((size_t)slot * 2 * kRows + R) * D + c0);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 v = __ldcg(src + k);
+            ov[4 * k] = fmaf(w, v.x, ov[4 * k]);
+            ov[4 * k + 1] = fmaf(w, v.y, ov[4 * k + 1]);
+            ov[4 * k + 2] = fmaf(w, v.z, ov[4 * k + 2]);
+            ov[4 * k + 3] = fmaf(w, v.w, ov[4 * k + 3]);
+          }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow + c0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 u;
+          u.x = ptx::cvt_bf16x2(ov[8 * k + 0] * minv, ov[8 * k + 1] * minv);
+          u.y = ptx::cvt_bf16x2(ov[8 * k + 2] * minv, ov[8 * k + 3] * minv);
+          u.z = ptx::cvt_bf16x2(ov[8 * k + 4] * minv, ov[8 * k + 5] * minv);
+          u.w = ptx::cvt_bf16x2(ov[8 * k + 6] * minv, ov[8 * k + 7] * minv);
+          dst[k] = u;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && bars->abort) set_dev_status(a.dev_status, TV_DEV_TIMEOUT);
+}
+
+// ------------------------------------------------------------------------------------
 // host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1539,32 +2043,68 @@ static bool encode_3d(CUtensorMap* m, const void* base, int D, int rows, long lo
   return r == CUDA_SUCCESS;
 }
 
-AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) {
-  AttnPlan p{};
-  const int G = Hkv > 0 ? Hq / Hkv : 0;
-  p.tc = dtype == TV_BF16 && (D == 64 || D == 128) && G >= 1 && G <= 16 && (long long)G * N >= 64;
-  if (!p.tc) return p;
-  p.nt = (kRows / G) / 8 * 8;
-  p.mtiles = (N + p.nt - 1) / p.nt;
-  // the kernel variant and the KV splits are chosen at launch (choose_plan)
-  p.total = 0;   // split partials stay in the cluster's shared memory
-  return p;
+static int device_sms() {
+  static std::atomic<int> cache[64];  // 0 = not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (!n) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+// Work geometry of the persistent schedule: per tile pair mp of a (sequence, KV head), its
+// 64-key step count max over its two row tiles of ceil((P + last node + 1) / 64); prefix
+// sums in sa->pre.  Returns false when the shape has more tile pairs than the kernel
+// takes.  *tmin: the smallest unit.
+static bool stream_geometry(int B, int Hkv, int NT, int mtiles, int P, int N, StreamArgs* sa, int* tmin) {
+  const int MP = (mtiles + 1) / 2;
+  if (MP < 1 || MP > kMaxMP) return false;
+  sa->MP = MP;
+  sa->pre[0] = 0;
+  int lo = 1 << 30;
+  for (int mp = 0; mp < MP; ++mp) {
+    int tu = 0;
+    for (int x = 0; x < 2; ++x) {
+      const int i0 = (2 * mp + x) * NT;
+      if (i0 < N) tu = std::max(tu, (P + std::min(N, i0 + NT) + kBN2 - 1) / kBN2);
+    }
+    sa->pre[mp + 1] = sa->pre[mp] + tu;
+    lo = std::min(lo, tu);
+  }
+  sa->Tg = sa->pre[MP];
+  sa->W = (long long)B * Hkv * sa->Tg;
+  *tmin = lo;
+  return true;
+}
+
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// workspace of the persistent schedule on C CTAs: two partial slots per CTA (its first
+// and last piece) of 256 rows x D fp32 plus (m, l), and one counter per unit
+static size_t stream_ws_bytes(int C, int D, long long units) {
+  return align256((size_t)2 * C * 2 * kRows * D * 4) + align256((size_t)2 * C * 2 * kRows * 8) +
+         align256((size_t)units * 4);
 }
 
 // Kernel variants: 1 attn_tc_kernel (one 128-row tile per CTA, 128-key KV tiles),
 // 2 attn_pair_kernel (two row tiles, 128-key KV tiles), 3 attn_pair2_kernel (two row
-// tiles, 64-key KV tiles, two S buffers per row tile).
+// tiles, 64-key KV tiles, two S buffers per row tile), 4 attn_stream_kernel (variant 3's
+// pipeline on a persistent grid, equal work per SM).
 template <int D, int kVar>
 static const void* tc_kernel_fn() {
   if constexpr (kVar == 1) return reinterpret_cast<const void*>(attn_tc_kernel<D>);
   else if constexpr (kVar == 2) return reinterpret_cast<const void*>(attn_pair_kernel<D>);
-  else return reinterpret_cast<const void*>(attn_pair2_kernel<D>);
+  else if constexpr (kVar == 3) return reinterpret_cast<const void*>(attn_pair2_kernel<D>);
+  else return reinterpret_cast<const void*>(attn_stream_kernel<D>);
 }
 template <int D, int kVar>
 static constexpr int tc_smem() {
   return kVar == 1 ? TcCfg<D>::kSmemAlloc : kVar == 2 ? PairCfg<D>::kSmemAlloc : Pair2Cfg<D>::kSmemAlloc;
 }
-constexpr int tc_keys(int var) { return var == 3 ? kBN2 : kBN; }  // keys per KV tile
+constexpr int tc_keys(int var) { return var >= 3 ? kBN2 : kBN; }  // keys per KV tile
 
 // How many clusters of `s` CTAs of variant kVar can be resident at once on the current
 // device (cached per device, variant and s).
@@ -1611,32 +2151,44 @@ constexpr double kMergeTiles = 4.4;
 constexpr double kPairTileCost = 1.85;
 constexpr double kPair2TileCost = 1.78;
 
+// SMs the attention may use (its share when one is set)
+static int attention_sms() {
+  const int nsm = device_sms();
+  const int share = sm_share_attention();
+  return share > 0 && share < nsm ? share : nsm;
+}
+
 template <int D, int kVar>
 static double plan_cost(long long units, int t_all128, int s) {
-  const int share = sm_share_attention();  // an SM share set for concurrent kernels
-  int nsm = 152, dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const int nsm = device_sms();
   int act = max_active_clusters<D, kVar>(s);
   if (act <= 0) return 1e300;
-  if (share > 0 && share < nsm) act = std::max(1, (int)((long long)act * share / nsm));
+  const int use = attention_sms();
+  if (use < nsm) act = std::max(1, (int)((long long)act * use / nsm));
   const long long waves = (units + act - 1) / act;
   const double tile = kVar == 1 ? 1.0 : kVar == 2 ? kPairTileCost : kPair2TileCost;
   return (double)waves * ((t_all128 + s - 1) / s + kFixedTiles + (s > 1 ? kMergeTiles : 0.0)) * tile;
 }
 
-// *var: 1, 2 or 3 (see tc_kernel_fn).  The automatic choice considers variants 1 and 3:
-// variant 3 was faster than variant 2 on every workload measured (3-8 %); 2 stays
-// available when forced.
+// *var: 1, 2, 3 or 4 (see tc_kernel_fn).  The automatic choice considers variants 1 and
+// 3: variant 3 was faster than variant 2 on every workload measured (3-8 %), and the
+// persistent grid (4) slower than variant 3 on every one (3-6 % on long context, 28 % on
+// sampling): these shapes run at the GB300's power limit, where 24 more busy SMs lower
+// the SM clock instead of finishing sooner and the extra pieces and merges cost energy.
+// 2 and 4 stay available when forced.  Variant 4 needs a workspace of
+// stream_ws_bytes(C, ...) and a shape whose CTA ranges touch at most kMaxPieces units;
+// *sa is filled when it is chosen.
 template <int D>
-static void choose_plan(int B, int Hkv, int mtiles, int P, int N, int* var, int* splits) {
+static void choose_plan(int B, int Hkv, int NT, int mtiles, int P, int N, int* var, int* splits, StreamArgs* sa) {
   const int variant = attention_variant();
   const int forced = attention_splits();
   const int t_all128 = (P + N + kBN - 1) / kBN;
+  const int fixed = variant == 4 ? 3 : variant;  // variant 4 falls back to 3 where it cannot run
   double best_cost = 1e300;
   *var = 1;
   *splits = 1;
   for (int v = 1; v <= 3; ++v) {
-    if (variant != 0 && v != variant) continue;
+    if (fixed != 0 && v != fixed) continue;
     if (variant == 0 && (v == 2 || (v == 3 && mtiles < 2))) continue;
     const long long units = (long long)B * Hkv * (v >= 2 ? (mtiles + 1) / 2 : mtiles);
     const int t_all = (P + N + tc_keys(v) - 1) / tc_keys(v);
@@ -1652,6 +2204,43 @@ static void choose_plan(int B, int Hkv, int mtiles, int P, int N, int* var, int*
       }
     }
   }
+  if (variant == 4 && forced <= 1 && max_active_clusters<D, 3>(1) > 0) {
+    StreamArgs g{};
+    int tmin = 0;
+    if (stream_geometry(B, Hkv, NT, mtiles, P, N, &g, &tmin) && tmin > 0) {
+      const int C = (int)std::min<long long>(attention_sms(), g.W);
+      const long long per = (g.W + C - 1) / C;  // steps per CTA
+      // a range of `per` steps holds at most per / tmin whole units and a partial one at
+      // each end
+      if (per / tmin + 2 <= kMaxPieces) {
+        *var = 4;
+        *splits = 1;
+        g.C = C;
+        *sa = g;
+      }
+    }
+  }
+}
+
+AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype) {
+  AttnPlan p{};
+  const int G = Hkv > 0 ? Hq / Hkv : 0;
+  p.tc = dtype == TV_BF16 && (D == 64 || D == 128) && G >= 1 && G <= 16 && (long long)G * N >= 64;
+  if (!p.tc) return p;
+  p.nt = (kRows / G) / 8 * 8;
+  p.mtiles = (N + p.nt - 1) / p.nt;
+  // the kernel variant and the KV splits are chosen at launch (choose_plan); split
+  // partials stay in the cluster's shared memory, the persistent schedule's in the
+  // workspace, sized for the whole device
+  p.total = 0;
+  int var = 1, spl = 1;
+  StreamArgs sa{};
+  if (D == 64)
+    choose_plan<64>(B, Hkv, p.nt, p.mtiles, P, N, &var, &spl, &sa);
+  else
+    choose_plan<128>(B, Hkv, p.nt, p.mtiles, P, N, &var, &spl, &sa);
+  if (var == 4) p.total = stream_ws_bytes(device_sms(), D, (long long)B * Hkv * sa.MP);
+  return p;
 }
 
 template <int D, int kVar>
@@ -1677,16 +2266,33 @@ static cudaError_t launch_tc_d(const CUtensorMap& mq, const CUtensorMap& mk, con
   return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t launch_stream_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                                   const TcArgs& a, const StreamArgs& sa, cudaStream_t stream) {
+  constexpr int smem = Pair2Cfg<D>::kSmemAlloc;
+  cudaError_t e = cudaFuncSetAttribute(attn_stream_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // the per-unit piece counters start at zero whatever an earlier (or aborted) call left
+  const size_t units = (size_t)(sa.W / sa.Tg) * sa.MP;
+  e = cudaMemsetAsync(sa.cnt, 0, units * sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(attn_stream_kernel<D>, dim3((unsigned)sa.C), dim3(kThreads), smem, stream, nullptr, 0, mq, mk, mv, a,
+                 sa);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 void attn_tc_choice(int B, int Hkv, int D, int P, int N, const AttnPlan& plan, int* var, int* splits) {
+  StreamArgs sa{};
   if (D == 64)
-    choose_plan<64>(B, Hkv, plan.mtiles, P, N, var, splits);
+    choose_plan<64>(B, Hkv, plan.nt, plan.mtiles, P, N, var, splits, &sa);
   else
-    choose_plan<128>(B, Hkv, plan.mtiles, P, N, var, splits);
+    choose_plan<128>(B, Hkv, plan.nt, plan.mtiles, P, N, var, splits, &sa);
 }
 
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* out, const int32_t* parent, int B,
                            int Hq, int Hkv, int D, int P, int N, int S, float scale, const AttnPlan& plan, char* ws,
-                           int32_t* dev_status, cudaStream_t stream) {
+                           size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
   TcArgs a;
   a.out = out;
   a.parent = parent;
@@ -1701,7 +2307,25 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* ou
   a.c = scale * kLog2e;
   a.dev_status = dev_status;
   int var = 1;
-  attn_tc_choice(B, Hkv, D, P, N, plan, &var, &a.splits);
+  StreamArgs sa{};
+  if (D == 64)
+    choose_plan<64>(B, Hkv, plan.nt, plan.mtiles, P, N, &var, &a.splits, &sa);
+  else
+    choose_plan<128>(B, Hkv, plan.nt, plan.mtiles, P, N, &var, &a.splits, &sa);
+  if (var == 4) {
+    // the persistent schedule needs its partial slots; with a smaller workspace (one
+    // sized under other settings) the unsplit paired kernel computes the same result
+    const long long units = (long long)B * Hkv * sa.MP;
+    if (!ws || ws_bytes < stream_ws_bytes(sa.C, D, units)) {
+      var = 3;
+      a.splits = 1;
+    } else {
+      sa.ws_o = reinterpret_cast<float*>(ws);
+      sa.ws_ml = reinterpret_cast<float2*>(ws + align256((size_t)2 * sa.C * 2 * kRows * D * 4));
+      sa.cnt = reinterpret_cast<unsigned*>(ws + align256((size_t)2 * sa.C * 2 * kRows * D * 4) +
+                                           align256((size_t)2 * sa.C * 2 * kRows * 8));
+    }
+  }
   const int keys = tc_keys(var);  // KV tile rows of the chosen variant
   CUtensorMap mq, mk, mv;
   if (!encode_3d(&mq, q, D, N, (long long)B * Hq, D, (long long)N * D, plan.nt)) return cudaErrorInvalidValue;
@@ -1710,10 +2334,12 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* ou
   if (D == 64) {
     if (var == 1) return launch_tc_d<64, 1>(mq, mk, mv, a, B, Hkv, stream);
     if (var == 2) return launch_tc_d<64, 2>(mq, mk, mv, a, B, Hkv, stream);
+    if (var == 4) return launch_stream_d<64>(mq, mk, mv, a, sa, stream);
     return launch_tc_d<64, 3>(mq, mk, mv, a, B, Hkv, stream);
   }
   if (var == 1) return launch_tc_d<128, 1>(mq, mk, mv, a, B, Hkv, stream);
   if (var == 2) return launch_tc_d<128, 2>(mq, mk, mv, a, B, Hkv, stream);
+  if (var == 4) return launch_stream_d<128>(mq, mk, mv, a, sa, stream);
   return launch_tc_d<128, 3>(mq, mk, mv, a, B, Hkv, stream);
 }
 

@@ -79,17 +79,17 @@ struct AttnPlan {
   bool tc;        // tensor-core (tcgen05) kernel
   int nt;         // nodes per 128-row tile (tc)
   int mtiles;     // row tiles per (b, kv head)
-  size_t total;   // workspace bytes (0: partials stay in the cluster's shared memory)
+  size_t total;   // workspace bytes (the persistent schedule's partials; 0 for the others)
 };
 AttnPlan attn_plan(int B, int Hq, int Hkv, int D, int P, int N, tv_dtype dtype);
 cudaError_t launch_attn_simt(const void* q, const void* k, const void* v, void* out, const int32_t* parent,
                              int B, int Hq, int Hkv, int D, int P, int N, int S, float scale, tv_dtype dtype,
                              int32_t* dev_status, cudaStream_t stream);
-// kernel variant (1 attn_tc_kernel, 2 attn_pair_kernel, 3 attn_pair2_kernel) and KV
-// splits the next launch would use
+// kernel variant (1 attn_tc_kernel, 2 attn_pair_kernel, 3 attn_pair2_kernel, 4
+// attn_stream_kernel) and KV splits the next launch would use
 void attn_tc_choice(int B, int Hkv, int D, int P, int N, const AttnPlan& plan, int* var, int* splits);
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* out, const int32_t* parent,
                            int B, int Hq, int Hkv, int D, int P, int N, int S, float scale, const AttnPlan& plan,
-                           char* ws, int32_t* dev_status, cudaStream_t stream);
+                           char* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream);
 
 }  // namespace tv
