@@ -889,12 +889,16 @@ def run_ours(args):
             "config": dict(workload_config(args.workload, cfg), N=N,
                            l2=f"inputs rotate over {n_sets} device copies, {n_sets * bytes_set / 1e6:.0f} MB "
                               f"> 2 x L2 ({l2 / 1e6:.0f} MB)",
-                           step="select_subtree, then tree_attention || " +
+                           step=("select_subtree, then " if use_pool else "given trees: ") + "tree_attention || " +
                                 ("verify_sample" if sampling_mode else "verify_greedy") +
                                 " (two streams; " + ("verify" if verify_on_main else "attention") +
-                                " on selection's stream with programmatic dependent launch)",
+                                (" on selection's stream with programmatic dependent launch)" if use_pool
+                                 else " on the main stream)"),
                            parallelism=f"replicas x{world}",
                            sm_partition={"verify": sm_partition[0] or n_sm, "attention": sm_partition[1] or n_sm},
+                           sm_partition_trials_us={
+                               f"verify {v or n_sm} / attention {a or n_sm}, {'verify' if vm else 'attention'} "
+                               f"on main": round(t * 1e3 / n_sets, 2) for ((v, a), vm), t in sorted(trial.items())},
                            attention_kernel=attn_name, attention_kv_splits=attn_splits),
             "path_gbs": bytes_set / (ms_per_step * 1e-3) / 1e9,
             "breakdown_us": br,
