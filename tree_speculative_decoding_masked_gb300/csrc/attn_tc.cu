@@ -154,7 +154,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, TcArgs a) {
   ptx::griddep_launch_dependents();
-  ptx::griddep_wait();  // before any global read or write
   using C = TcCfg<D>;
   extern __shared__ unsigned char smem_raw[];
   __shared__ float s_xmax[2][2][kRows];  // [tile parity][half][row] partial row maxima
@@ -201,6 +200,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(&bars->tmem_base, C::kTmemCols);
     ptx::tmem_relinquish();
   }
+  if (warp == 0 && lane == 0) {  // kernel parameters: safe before the wait
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+  }
+  // the set-up above touches only shared memory, TMEM and parameters, so it overlaps the
+  // previous kernel's tail (programmatic dependent launch); global memory after this
+  ptx::griddep_wait();
   if (warp >= 2) {
     // parent array for the mask; zero the Q rows that no TMA box fills
     const int t = threadIdx.x - 64;
@@ -247,8 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued[kKSlots];
 #pragma unroll
       for (int s = 0; s < kKSlots; ++s) issued[s] = 0;
-      ptx::prefetch_tmap(&tmQ);
-      ptx::prefetch_tmap(&tmK);
       ptx::mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(rows_used * 128 * C::kDB));
       for (int g = 0; g < a.G; ++g)
         for (int db = 0; db < C::kDB; ++db)
@@ -273,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued[kVSlots];
 #pragma unroll
       for (int s = 0; s < kVSlots; ++s) issued[s] = 0;
-      ptx::prefetch_tmap(&tmV);
       for (int t = 0; t < nt; ++t) {
         const int vs = t % kVSlots;
         if (t >= kVSlots && !ptx::mbar_wait(&bars->v_empty[vs], ((t / kVSlots) - 1) & 1, abort_flag)) break;
@@ -631,7 +635,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, TcArgs a) {
   ptx::griddep_launch_dependents();
-  ptx::griddep_wait();  // before any global read or write
   using C = PairCfg<D>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t mis = ptx::smem_addr(smem_raw) & 1023u;
@@ -684,6 +687,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(&bars->tmem_base, C::kTmemCols);
     ptx::tmem_relinquish();
   }
+  if (warp == 0 && lane == 0) {  // kernel parameters: safe before the wait
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+  }
+  // the set-up above touches only shared memory, TMEM and parameters, so it overlaps the
+  // previous kernel's tail (programmatic dependent launch); global memory after this
+  ptx::griddep_wait();
   if (warp >= 2) {
     // parent array for the mask; zero the Q rows that no TMA box fills
     const int t = threadIdx.x - 64;
@@ -717,8 +728,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ producers
     if (lane == 0 && nt > 0) {
       int issued[kPairSlots] = {0, 0};
-      ptx::prefetch_tmap(&tmQ);
-      ptx::prefetch_tmap(&tmK);
       uint32_t qbytes = 0;
 #pragma unroll
       for (int x = 0; x < 2; ++x)
@@ -747,7 +756,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued[s]) ptx::mbar_wait(&bars->k_full[s], (issued[s] - 1) & 1, abort_flag);
     } else if (lane == 1 && nt > 0) {
       int issued[kPairSlots] = {0, 0};
-      ptx::prefetch_tmap(&tmV);
       for (int t = 0; t < nt; ++t) {
         const int vs = t % kPairSlots;
         if (t >= kPairSlots && !ptx::mbar_wait(&bars->v_empty[vs], ((t / kPairSlots) - 1) & 1, abort_flag)) break;
@@ -1106,7 +1114,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_pair2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, TcArgs a) {
   ptx::griddep_launch_dependents();
-  ptx::griddep_wait();  // before any global read or write
   using C = Pair2Cfg<D>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t mis = ptx::smem_addr(smem_raw) & 1023u;
@@ -1150,6 +1157,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(&bars->tmem_base, C::kTmemCols);
     ptx::tmem_relinquish();
   }
+  if (warp == 0 && lane == 0) {  // kernel parameters: safe before the wait
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+  }
+  // the set-up above touches only shared memory, TMEM and parameters, so it overlaps the
+  // previous kernel's tail (programmatic dependent launch); global memory after this
+  ptx::griddep_wait();
   if (warp >= 2) {
     const int t = threadIdx.x - 64;
     int bad = 0, first_pad = a.N;
@@ -1200,8 +1215,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ producers
     if (lane == 0 && nt > 0) {
       int issued[kPair2Slots] = {0, 0, 0, 0};
-      ptx::prefetch_tmap(&tmQ);
-      ptx::prefetch_tmap(&tmK);
       uint32_t qbytes = 0;
 #pragma unroll
       for (int x = 0; x < 2; ++x)
@@ -1230,7 +1243,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued[s]) ptx::mbar_wait(&bars->k_full[s], (issued[s] - 1) & 1, abort_flag);
     } else if (lane == 1 && nt > 0) {
       int issued[kPair2Slots] = {0, 0, 0, 0};
-      ptx::prefetch_tmap(&tmV);
       for (int t = 0; t < nt; ++t) {
         const int vs = t % kPair2Slots;
         if (t >= kPair2Slots && !ptx::mbar_wait(&bars->v_empty[vs], ((t / kPair2Slots) - 1) & 1, abort_flag))
@@ -1563,7 +1575,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_stream_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, TcArgs a, const __grid_constant__ StreamArgs sa) {
   ptx::griddep_launch_dependents();
-  ptx::griddep_wait();  // before any global read or write
   using C = Pair2Cfg<D>;
   static_assert(sizeof(StreamBars) <= 512, "stream barriers fit the barrier region");
   extern __shared__ unsigned char smem_raw[];
@@ -1621,6 +1632,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(&bars->tmem_base, C::kTmemCols);
     ptx::tmem_relinquish();
   }
+  if (warp == 0 && lane == 0) {  // kernel parameters: safe before the wait
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+  }
+  // the set-up above touches only shared memory, TMEM and parameters, so it overlaps the
+  // previous kernel's tail (programmatic dependent launch); global memory after this
+  ptx::griddep_wait();
   if (warp >= 2) {
     // zero the Q rows that no TMA box fills (the same rows in every unit)
     const int t = threadIdx.x - 64;
@@ -1656,8 +1675,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int issued[kPair2Slots] = {0, 0, 0, 0};
       long long gk = 0;
-      ptx::prefetch_tmap(&tmQ);
-      ptx::prefetch_tmap(&tmK);
       for (int p = 0; p < np && !*abort_flag; ++p) {
         const StreamPiece pc = bars->piece[p];
         int i0[2], ntx[2];
@@ -1697,7 +1714,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (lane == 1) {
       int issued[kPair2Slots] = {0, 0, 0, 0};
       long long gv = 0;
-      ptx::prefetch_tmap(&tmV);
       for (int p = 0; p < np && !*abort_flag; ++p) {
         const StreamPiece pc = bars->piece[p];
         int i0[2], ntx[2];
