@@ -4,6 +4,8 @@
 
 #include <atomic>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "tv_kernels.cuh"
 
 using namespace tv;
@@ -33,6 +35,16 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline bool valid_dtype(tv_dtype d) { return d == TV_F32 || d == TV_BF16; }
 inline tv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TV_OK : TV_ERR_CUDA; }
 inline cudaStream_t st(tv_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// One NVTX range per entry point that launches work, named after the entry point, so
+// that a profiler's timeline groups each call's kernels.  NVTX is header-only: without an
+// attached tool a push or pop is one pointer check.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 }  // namespace
 
@@ -66,6 +78,7 @@ const char* tv_status_string(int s) {
 int tv_version(void) { return (1 << 16) | 0; }
 
 tv_status tv_philox4x32_10(uint64_t seed, const uint32_t* counters, int n, uint32_t* out, tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_philox4x32_10");
   if (n < 0) return TV_ERR_SHAPE;
   if (n > 0 && (!counters || !out)) return TV_ERR_NULL;
   if (!aligned16(counters) || !aligned16(out)) return TV_ERR_ALIGN;
@@ -73,6 +86,7 @@ tv_status tv_philox4x32_10(uint64_t seed, const uint32_t* counters, int n, uint3
 }
 
 tv_status tv_selftest_bounded_wait(int wait_us, int32_t* dev_status, tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_selftest_bounded_wait");
   if (!dev_status) return TV_ERR_NULL;
   if (wait_us < 1 || wait_us > 1000000) return TV_ERR_VALUE;
   return cuda_status(launch_wait_selftest((uint64_t)wait_us * 1000ull, dev_status, st(stream)));
@@ -99,6 +113,7 @@ tv_status tv_set_attention_splits(int splits) {
 
 tv_status tv_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* depth, int32_t* pos, uint32_t* anc_mask,
                        int32_t* child_off, int32_t* child_idx, int32_t* dev_status, tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_tree_prep");
   if (!parent) return TV_ERR_NULL;
   if (B < 1 || N < 1 || N > kMaxNodes || P < 0) return TV_ERR_SHAPE;
   if ((child_off == nullptr) != (child_idx == nullptr)) return TV_ERR_NULL;
@@ -109,6 +124,7 @@ tv_status tv_tree_prep(const int32_t* parent, int B, int N, int P, int32_t* dept
 tv_status tv_prune_tree(const int32_t* parent, const float* conf, int B, int N, int max_children, int depth_limit,
                         int32_t* old_to_new, int32_t* new_parent, int32_t* n_kept, int32_t* new_root,
                         int32_t* dev_status, tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_prune_tree");
   if (!parent || !conf || !old_to_new || !new_parent || !n_kept || !new_root) return TV_ERR_NULL;
   if (B < 1 || N < 1 || N > kMaxNodes) return TV_ERR_SHAPE;
   if (max_children < 1 || depth_limit < 1) return TV_ERR_VALUE;
@@ -126,6 +142,7 @@ tv_status tv_tree_attention(const void* q, const void* k_cache, const void* v_ca
                             const int32_t* parent, int B, int Hq, int Hkv, int D, int P, int N, int kv_stride_tokens,
                             float scale, tv_dtype dtype, void* workspace, size_t ws_bytes, int32_t* dev_status,
                             tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_tree_attention");
   if (!q || !k_cache || !v_cache || !out || !parent) return TV_ERR_NULL;
   if (!valid_dtype(dtype)) return TV_ERR_DTYPE;
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || N < 1 || N > kMaxNodes || P < 0) return TV_ERR_SHAPE;
@@ -184,6 +201,7 @@ tv_status tv_verify_greedy(const void* logits, const int32_t* parent, const int3
                            tv_dtype dtype, int32_t* accepted_nodes, int32_t* accept_len, int32_t* bonus_token,
                            float* p_draft, float* row_lse, int32_t* row_argmax, void* workspace, size_t ws_bytes,
                            int32_t* dev_status, tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_verify_greedy");
   if (!accepted_nodes || !accept_len || !bonus_token) return TV_ERR_NULL;
   tv_status s = verify_common_checks(logits, parent, tokens, B, N, V, dtype, workspace, ws_bytes, 0);
   if (s != TV_OK) return s;
@@ -199,6 +217,7 @@ tv_status tv_vocab_stats(const void* logits, const void* draft_logits, const int
                          const int32_t* tokens, int B, int N, int V, float temperature, tv_dtype dtype,
                          float* row_lse, int32_t* row_argmax, float* p_draft, float* draft_row_lse, float* q_draft,
                          void* workspace, size_t ws_bytes, int32_t* dev_status, tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_vocab_stats");
   if (!draft_logits && (draft_row_lse || q_draft)) return TV_ERR_NULL;
   if (!(temperature > 0.f) || isinf(temperature)) return TV_ERR_VALUE;
   const int two = draft_logits ? 1 : 0;
@@ -216,6 +235,7 @@ tv_status tv_verify_sample(const void* target_logits, const void* draft_logits, 
                            uint64_t round, tv_dtype dtype, int32_t* accepted_nodes, int32_t* accept_len,
                            int32_t* out_token, float* p_draft, float* q_draft, void* workspace, size_t ws_bytes,
                            int32_t* dev_status, tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_verify_sample");
   if (!draft_logits || !accepted_nodes || !accept_len || !out_token) return TV_ERR_NULL;
   if (!(temperature > 0.f) || isinf(temperature)) return TV_ERR_VALUE;
   tv_status s = verify_common_checks(target_logits, parent, tokens, B, N, V, dtype, workspace, ws_bytes, 1);
@@ -235,6 +255,7 @@ tv_status tv_verify_sample(const void* target_logits, const void* draft_logits, 
 tv_status tv_commit_accepted_kv(void* k_cache, void* v_cache, const int32_t* accepted_nodes,
                                 const int32_t* accept_len, int B, int Hkv, int D, int P, int N, int kv_stride_tokens,
                                 tv_dtype dtype, int32_t* dev_status, tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_commit_accepted_kv");
   if (!k_cache || !v_cache || !accepted_nodes || !accept_len) return TV_ERR_NULL;
   if (!valid_dtype(dtype)) return TV_ERR_DTYPE;
   if (B < 1 || Hkv < 1 || D < 1 || P < 0 || N < 1 || N > kMaxNodes) return TV_ERR_SHAPE;
@@ -249,6 +270,7 @@ tv_status tv_commit_accepted_kv(void* k_cache, void* v_cache, const int32_t* acc
 
 tv_status tv_frontier_topw(const float* scores, const int32_t* count, int B, int C, int W, int32_t* out_idx,
                            int32_t* dev_status, tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_frontier_topw");
   if (!scores || !count || !out_idx) return TV_ERR_NULL;
   if (B < 1 || C < 1 || C > 4096 || W < 1 || W > C) return TV_ERR_SHAPE;
   return cuda_status(launch_frontier_topw(scores, count, B, C, W, out_idx, dev_status, st(stream)));
@@ -260,6 +282,7 @@ tv_status tv_expand_children(const void* draft_logits, const float* parent_score
                              float temperature, tv_dtype dtype, int32_t* child_token, float* child_p,
                              float* child_score, void* workspace, size_t ws_bytes, int32_t* dev_status,
                              tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_expand_children");
   if (!draft_logits || !parent_score || !child_token || !child_p || !child_score) return TV_ERR_NULL;
   if (!valid_dtype(dtype)) return TV_ERR_DTYPE;
   if (R < 1 || V < 1 || m < 1 || m > 32) return TV_ERR_SHAPE;
@@ -277,6 +300,7 @@ tv_status tv_select_subtree(const float* marg, const int32_t* pool_tokens, int B
                             const int32_t* root_token, int32_t* parent, int32_t* tokens, int32_t* depth, float* score,
                             int32_t* n_nodes, void* workspace, size_t ws_bytes, int32_t* dev_status,
                             tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_select_subtree");
   if (!marg || !pool_tokens || !parent || !tokens || !depth || !score) return TV_ERR_NULL;
   if (B < 1 || d < 1 || d > kMaxDepth || K < 1 || K > kMaxRank || budget < 1 || budget > kMaxBudget)
     return TV_ERR_SHAPE;
@@ -289,6 +313,7 @@ tv_status tv_select_subtree_adaptive(const float* marg, const int32_t* pool_toke
                                      float cost_base, float cost_per_row, const int32_t* root_token, int32_t* parent,
                                      int32_t* tokens, int32_t* depth, float* score, int32_t* n_nodes,
                                      void* workspace, size_t ws_bytes, int32_t* dev_status, tv_stream_t stream) {
+  NvtxRange nvtx_range("tv_select_subtree_adaptive");
   if (!marg || !pool_tokens || !parent || !tokens || !depth || !score || !n_nodes) return TV_ERR_NULL;
   if (B < 1 || d < 1 || d > kMaxDepth || K < 1 || K > kMaxRank || budget < 1 || budget > kMaxBudget)
     return TV_ERR_SHAPE;
