@@ -1066,11 +1066,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // computed while the softmax of tile t runs, and the tensor core no longer waits for the
 // serial S -> softmax -> PV chain of each tile.  P_X(t) (bf16, 32 columns) is written over
 // the first half of its own S buffer by its row's thread; S_X(t + 2) reuses that buffer
-// once PV_X(t) has completed.
+// once PV_X(t) has completed.  Each row tile has its own S issuing thread: one thread
+// issues an N = 64 product with both operands in shared memory only every ~100 cycles
+// (37 cycles of tensor work), so a single issuer for both tiles left the tensor core
+// waiting; two issuers took the long-context attention from 475 to 407 us.
 // TMEM columns: S_A[0] 0..63, S_A[1] 64..127, S_B[0] 128..191, S_B[1] 192..255,
 // O_A 256.., O_B 384...
+// Warps: 0 TMA producers (lane 0 Q and K, lane 1 V), 1 S issuer of tile A and TMEM owner,
+// 2-9 softmax (four per tile, one thread per row), 10 PV issuer, 11 S issuer of tile B.
 constexpr int kBN2 = 64;       // keys per KV tile
 constexpr int kPair2Slots = 4; // K ring and V ring depth
+constexpr int kP2Threads = 384;  // 12 warps
 
 template <int D>
 struct Pair2Cfg {
@@ -1104,13 +1110,13 @@ struct Pair2Bars {
   uint64_t p_full[2][2];   // P_X(t) written (4 warps)
   uint64_t pv_done[2][2];  // PV_X(t) complete
   uint64_t o_done;
-  uint64_t s_done;
+  uint64_t s_done[2];
   uint32_t tmem_base;
   int abort;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kP2Threads, 1)
     attn_pair2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, TcArgs a) {
   ptx::griddep_launch_dependents();
@@ -1132,13 +1138,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int x = 0; x < 2; ++x) i0[x] = (2 * mp + x) * a.NT;
   const int rows_used = a.G * a.NT;
-  __shared__ int s_wfirst[kThreads / 32];  // per warp: first padding row it saw (or N)
+  __shared__ int s_wfirst[kP2Threads / 32];  // per warp: first padding row it saw (or N)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kPair2Slots; ++s) {
       ptx::mbar_init(&bars->k_full[s], 1);
-      ptx::mbar_init(&bars->k_empty[s], 1);
+      ptx::mbar_init(&bars->k_empty[s], 2);  // both S issuers
       ptx::mbar_init(&bars->v_full[s], 1);
       ptx::mbar_init(&bars->v_empty[s], 1);
     }
@@ -1149,7 +1155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(&bars->pv_done[x][u], 1);
       }
     ptx::mbar_init(&bars->o_done, 1);
-    ptx::mbar_init(&bars->s_done, 1);
+    ptx::mbar_init(&bars->s_done[0], 1);
+    ptx::mbar_init(&bars->s_done[1], 1);
     bars->abort = 0;
     ptx::fence_mbar_init();
   }
@@ -1168,7 +1175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 2) {
     const int t = threadIdx.x - 64;
     int bad = 0, first_pad = a.N;
-    for (int c = t; c < a.N; c += kThreads - 64) {
+    for (int c = t; c < a.N; c += kP2Threads - 64) {
       const int p = a.parent[(size_t)b * a.N + c];
       s_par[c] = p;
       // trailing padding rows of a ragged batch hold parent -1; an active row must not
@@ -1180,7 +1187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     first_pad = __reduce_min_sync(0xffffffffu, first_pad);
     if (lane == 0) s_wfirst[warp] = first_pad;
     if (bad) set_dev_status(a.dev_status, TV_DEV_BAD_TREE);
-    for (int r = rows_used + t; r < 2 * kRows; r += kThreads - 64) {
+    for (int r = rows_used + t; r < 2 * kRows; r += kP2Threads - 64) {
       const int x = r >= kRows ? 1 : 0, rr = r - x * kRows;
       if (rr < rows_used) continue;
       for (int db = 0; db < C::kDB; ++db) {
@@ -1199,7 +1206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // them are never needed
   int n_act = a.N;
 #pragma unroll
-  for (int w = 2; w < kThreads / 32; ++w) n_act = min(n_act, s_wfirst[w]);
+  for (int w = 2; w < kP2Threads / 32; ++w) n_act = min(n_act, s_wfirst[w]);
   int t_allx[2];
 #pragma unroll
   for (int x = 0; x < 2; ++x) t_allx[x] = i0[x] < n_act ? (a.P + min(n_act, i0[x] + a.NT) + kBN2 - 1) / kBN2 : 0;
@@ -1258,26 +1265,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued[s]) ptx::mbar_wait(&bars->v_full[s], (issued[s] - 1) & 1, abort_flag);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ S issuer
+  } else if (warp == 1 || warp == kP2Threads / 32 - 1) {
+    // ------------------------------------------------------------------ S issuer of tile x
+    // one issuing thread per row tile: the short (N = 64) S products of the two tiles are
+    // issued in parallel
+    const int x = warp == 1 ? 0 : 1;
     if (lane == 0) {
       if (nt > 0 && ptx::mbar_wait(&bars->q_full, 0, abort_flag)) {
         constexpr uint32_t idS = ptx::idesc_bf16(kRows, kBN2, false, false);
-        bool ok = true;
-        for (int t = 0; ok && t < nt; ++t) {
+        const uint32_t qaddr = ptx::smem_addr(sQ + x * C::kQTile);
+        for (int t = 0; t < nt; ++t) {
           const int ks = t % kPair2Slots, buf = t & 1;
           if (!ptx::mbar_wait(&bars->k_full[ks], (t / kPair2Slots) & 1, abort_flag)) break;
-          const uint32_t kaddr = ptx::smem_addr(sK + ks * C::kTileBytes);
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (t >= ntx[x]) continue;
+          if (t < ntx[x]) {
             // S_X(t) overwrites P_X(t - 2) in this buffer: wait for PV_X(t - 2)
-            if (t >= 2 && !ptx::mbar_wait(&bars->pv_done[x][buf], ((t - 2) >> 1) & 1, abort_flag)) {
-              ok = false;
-              break;
-            }
+            if (t >= 2 && !ptx::mbar_wait(&bars->pv_done[x][buf], ((t - 2) >> 1) & 1, abort_flag)) break;
             ptx::tc_fence_after();
-            const uint32_t qaddr = ptx::smem_addr(sQ + x * C::kQTile);
+            const uint32_t kaddr = ptx::smem_addr(sK + ks * C::kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk & 3) * 32;  // 16-element K step inside a 128-byte row
@@ -1287,14 +1291,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::mma_commit(&bars->s_full[x][buf]);
           }
-          if (ok) ptx::mma_commit(&bars->k_empty[ks]);
+          ptx::mma_commit(&bars->k_empty[ks]);  // this tile is done with the K slot
         }
       }
-      ptx::mma_commit(&bars->s_done);
-      ptx::mbar_wait(&bars->s_done, 0, abort_flag);
+      ptx::mma_commit(&bars->s_done[x]);
+      ptx::mbar_wait(&bars->s_done[x], 0, abort_flag);
     }
     __syncwarp();
-  } else if (warp == kThreads / 32 - 1) {
+  } else if (warp == kP2Threads / 32 - 2) {
     // ------------------------------------------------------------------ PV issuer
     if (lane == 0) {
       constexpr uint32_t idO = ptx::idesc_bf16(kRows, D, false, true);
@@ -1463,7 +1467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kChunks = D / 4;
       const uint32_t part_local = ptx::smem_addr(sK);
       const uint32_t ml_local = ptx::smem_addr(sQ);
-      for (int item = threadIdx.x; item < nrows * kChunks; item += kThreads) {
+      for (int item = threadIdx.x; item < nrows * kChunks; item += kP2Threads) {
         const int rr = r0 + item / kChunks;
         const int ch = item % kChunks;
         const int xx = rr >= kRows ? 1 : 0, rt = rr - xx * kRows;
@@ -2120,6 +2124,7 @@ template <int D, int kVar>
 static constexpr int tc_smem() {
   return kVar == 1 ? TcCfg<D>::kSmemAlloc : kVar == 2 ? PairCfg<D>::kSmemAlloc : Pair2Cfg<D>::kSmemAlloc;
 }
+constexpr int tc_threads(int var) { return var == 3 ? kP2Threads : kThreads; }
 constexpr int tc_keys(int var) { return var >= 3 ? kBN2 : kBN; }  // keys per KV tile
 
 // How many clusters of `s` CTAs of variant kVar can be resident at once on the current
@@ -2139,7 +2144,7 @@ static int max_active_clusters(int s) {
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(s * 64, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(tc_threads(kVar), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -2160,12 +2165,12 @@ static int max_active_clusters(int s) {
 // constants are fitted to GB300 measurements over the qwen3 layer, sampling,
 // long-context and budget-sweep shapes (every split count of both kernels): a CTA's
 // set-up, pipeline fill and epilogue cost about 6 tiles, a cluster merge about 4.4, and
-// 128 keys of a tile pair about 1.85 single tiles for attn_pair_kernel and 1.78 for
-// attn_pair2_kernel (1.69-1.83 over the workloads).
+// 128 keys of a tile pair about 1.85 single tiles for attn_pair_kernel and 1.55 for
+// attn_pair2_kernel (1.50-1.59 over the long-context, sampling and budget-sweep shapes).
 constexpr double kFixedTiles = 6.0;
 constexpr double kMergeTiles = 4.4;
 constexpr double kPairTileCost = 1.85;
-constexpr double kPair2TileCost = 1.78;
+constexpr double kPair2TileCost = 1.55;
 
 // SMs the attention may use (its share when one is set)
 static int attention_sms() {
@@ -2187,7 +2192,8 @@ static double plan_cost(long long units, int t_all128, int s) {
 }
 
 // *var: 1, 2, 3 or 4 (see tc_kernel_fn).  The automatic choice considers variants 1 and
-// 3: variant 3 was faster than variant 2 on every workload measured (3-8 %), and the
+// 3: variant 3 was faster than variant 2 on every workload measured (3-8 % before it had
+// one S issuer per row tile, 10-16 % since), and the
 // persistent grid (4) slower than variant 3 on every one (3-6 % on long context, 28 % on
 // sampling): these shapes run at the GB300's power limit, where 24 more busy SMs lower
 // the SM clock instead of finishing sooner and the extra pieces and merges cost energy.
@@ -2266,7 +2272,7 @@ static cudaError_t launch_tc_d(const CUtensorMap& mq, const CUtensorMap& mk, con
   cudaError_t e = cudaFuncSetAttribute(tc_kernel_fn<D, kVar>(), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int units = kVar >= 2 ? (a.MT + 1) / 2 : a.MT;  // CTAs per (b, kv head) and split
-  const dim3 grid(units * a.splits, Hkv, B), block(kThreads, 1, 1);
+  const dim3 grid(units * a.splits, Hkv, B), block(tc_threads(kVar), 1, 1);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)a.splits;
