@@ -44,6 +44,7 @@ constexpr int kKSlots = 3;     // K ring depth (tiles of 128 keys)
 constexpr int kVSlots = 2;     // V ring depth
 constexpr int kThreads = 352;  // 11 warps: TMA producers, S issuer, 8 softmax warps, PV issuer
 constexpr float kRescaleLog2 = 8.f;
+constexpr float kRescaleSum = 256.f;  // 2^kRescaleLog2
 constexpr int kMaxSplits = 8;  // KV splits of a row tile = one portable-size cluster
 
 template <int D>
@@ -1360,18 +1361,31 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         for (int j = 0; j < 64; ++j)
           if (!((vis >> j) & 1ull)) sv[j] = -INFINITY;
       }
-      const float tms = max64(sv, -INFINITY) * a.c;
+      // P = 2^(S c - m_run) against the running reference m_run, which moves (and O is
+      // rescaled) only when a score exceeds it by more than 2^8.  Such a score makes its P
+      // exceed 2^8 and so the tile's sum of P reach 2^8: the row maximum is taken only for
+      // those tiles (and for the first tile with a visible key), and a moved reference
+      // redoes the exponentials.  The decisions are those of taking the maximum of every
+      // tile first.
       float alpha = 1.f;
       bool need = false;
-      if (tms > m_run + kRescaleLog2) {
-        if (m_run != -INFINITY) {
-          alpha = ptx::ex2(m_run - tms);
-          need = true;
-        }
-        m_run = tms;
+      bool checked = false;
+      if (m_run == -INFINITY) {
+        m_run = max64(sv, -INFINITY) * a.c;  // stays -inf while no key is visible
+        checked = true;
       }
       uint32_t pw[32];
-      const float lsum = exp_p64(sv, a.c, m_run, pw);
+      float lsum;
+      for (;;) {
+        lsum = exp_p64(sv, a.c, m_run, pw);
+        if (checked || lsum < kRescaleSum) break;
+        checked = true;
+        const float tms = max64(sv, -INFINITY) * a.c;
+        if (!(tms > m_run + kRescaleLog2)) break;
+        alpha = ptx::ex2(m_run - tms);
+        need = true;
+        m_run = tms;
+      }
       ptx::tmem_st32u(colS + buf * kBN2, pw);  // P over the first half of this S buffer
       if (__any_sync(0xffffffffu, need) && t > 0) {
         // O_X must hold all of PV_X(t - 1) before it is rescaled (S_X(t) may have been
