@@ -1366,7 +1366,8 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       // exceed 2^8 and so the tile's sum of P reach 2^8: the row maximum is taken only for
       // those tiles (and for the first tile with a visible key), and a moved reference
       // redoes the exponentials.  The decisions are those of taking the maximum of every
-      // tile first.
+      // tile first, up to rounding of a score within an ulp of the 2^8 boundary (either
+      // choice gives the same softmax).
       float alpha = 1.f;
       bool need = false;
       bool checked = false;
