@@ -145,14 +145,16 @@ TV_API tv_status tv_set_sm_partition(int verify_sms, int attention_sms);
  *   2  paired row tiles: one CTA streams the KV range once for two 128-row tiles
  *   3  paired row tiles with 64-key KV tiles and two S buffers per row tile, so S of
  *      the next KV tile is computed while the softmax of the current one runs
- *   4  variant 3's pipeline on a persistent grid of one CTA per SM (of the attention's
+ *   4  variant 3's pipeline (in its earlier form with one S issuing thread for both row
+ *      tiles) on a persistent grid of one CTA per SM (of the attention's
  *      share): the 64-key steps of all tile pairs are cut into equal contiguous ranges,
  *      one per CTA, so that the device stays busy when the tile pairs do not fill a
  *      whole number of waves; a tile pair cut between CTAs is merged through the
  *      workspace by the CTA that finishes its last piece.  Needs the workspace; shapes
  *      whose ranges would hold more than 8 pieces run variant 3.  Measured 3-6 %
- *      slower than variant 3 on the long-context shapes, which run at the GB300's power
- *      limit (more busy SMs lower the clock), so the automatic choice never takes it.
+ *      slower than that single-issuer variant 3 on the long-context shapes, which run
+ *      at the GB300's power limit (more busy SMs lower the clock), so the automatic
+ *      choice never takes it.
  * All compute the same result (up to fp32 summation order); the switch exists to
  * compare and test them.  Process-wide, host-side; affects launches made after the call.
  * Errors: a value outside 0..4 -> TV_ERR_VALUE.

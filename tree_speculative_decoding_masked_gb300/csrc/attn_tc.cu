@@ -1536,8 +1536,8 @@ __global__ void __launch_bounds__(kP2Threads, 1)
 }
 
 // ------------------------------------------------------------------------------------
-// attn_stream_kernel: the paired 64-key pipeline of attn_pair2_kernel under a persistent
-// schedule.  The work of a launch is the list of all (tile pair, 64-key KV tile) steps,
+// attn_stream_kernel: the paired 64-key pipeline of attn_pair2_kernel (in its earlier form,
+// one S issuing thread for both row tiles) under a persistent schedule.  The work of a launch is the list of all (tile pair, 64-key KV tile) steps,
 // unit by unit (a unit = one tile pair of one (sequence, KV head)); every CTA of the
 // grid (one per SM of its share) takes an equal contiguous range of it, so that 128
 // units on 152 SMs keep every SM busy instead of leaving 24 idle.  A range covers whole
