@@ -11,7 +11,11 @@
 //
 // Every CTA of the cluster runs the same control flow (same tree, same Philox draws, same
 // sums, hence the same decisions) and takes an equal share of the vocabulary in each
-// pass.
+// pass.  Where its share fits in shared memory, a CTA loads the node's target and draft
+// rows once, as p(v) and q(v), at the node's first full pass and keeps the residual
+// P_n(v) there, updated in place after each rejection with the same float operations as
+// replaying the recursion from p and q (a rejected token is removed by zeroing its q);
+// otherwise every pass reads the rows again and replays the recursion.
 // Sums are exact: each term in [0, 1] is rounded once to a multiple of 2^-56 and added as
 // a 64-bit integer, so a total does not depend on the order of the additions and every
 // CTA, after reading the others' partial sums through distributed shared memory, holds
@@ -43,7 +47,8 @@ struct WalkArgs {
   int32_t* accept_len;
   int32_t* out_token;
   int32_t* dev_status;
-  int csize;  // CTAs per cluster (one cluster per sequence)
+  int csize;   // CTAs per cluster (one cluster per sequence)
+  int cached;  // the share of a row fits the dynamic shared memory (p, q as fp32)
 };
 
 template <typename T>
@@ -77,6 +82,7 @@ __device__ __forceinline__ void eval_pq(const Residual& r, int v, float p, float
 constexpr int kWalkClusterMax = 16;  // CTAs per sequence where the device allows it, else 8
 constexpr int kBatch = 5;            // vocabulary elements per thread whose loads are issued together
 constexpr float kFixScale = 72057594037927936.0f;  // 2^56
+constexpr int kWalkDynCap = 180 * 1024;  // dynamic shared memory for the cached rows
 
 __device__ __forceinline__ unsigned long long to_fix(float x) { return __float2ull_rn(x * kFixScale); }
 
@@ -116,6 +122,14 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
   const int span = (V + csize - 1) / csize;
   const int vlo = min(V, (int)crank * span), vhi = min(V, vlo + span);
   int npass = 0;
+  // cached rows: sP[i] = P_n(vlo + i) at the current node, sQ[i] = q(vlo + i) (0 once the
+  // token was rejected there)
+  extern __shared__ __align__(16) float walk_dyn[];
+  float* sP = walk_dyn;
+  float* sQ = walk_dyn + ((span + 3) & ~3);
+  const bool cached = a.cached != 0;
+  int loaded_u = -1;   // node whose p (and q) are in sP / sQ
+  bool loaded_q = false;
   // Sum of `mine` over the cluster: every CTA gets the same total; *below = the sum over
   // the lower-ranked CTAs
   auto cluster_total = [&](unsigned long long mine, unsigned long long* below) {
@@ -143,6 +157,32 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
     __syncthreads();
     ++npass;
     return tot;
+  };
+  // p(v) (and q(v) when `with_q`) of this CTA's share of node u's rows into sP / sQ
+  auto load_rows = [&](int node, bool with_q) {
+    const size_t row = ((size_t)b * N + node) * (size_t)V;
+    const float l2p = s_l2p[node], l2q = s_l2q[node];
+    const int n = vhi - vlo;
+    for (int i0 = tid; i0 < n; i0 += 4 * (int)blockDim.x) {
+      float xs[4], ys[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = i0 + k * (int)blockDim.x;
+        xs[k] = i < n ? ld_logit<T>(a.target, row + vlo + i) : 0.f;
+        ys[k] = (with_q && i < n) ? ld_logit<T>(a.draft, row + vlo + i) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = i0 + k * (int)blockDim.x;
+        if (i < n) {
+          sP[i] = ptx::ex2(fmaf(xs[k], a.c2, -l2p));
+          if (with_q) sQ[i] = ptx::ex2(fmaf(ys[k], a.c2, -l2q));
+        }
+      }
+    }
+    __syncthreads();
+    loaded_u = node;
+    loaded_q = with_q;
   };
   if (tid == 0) s_bad = 0;
   __syncthreads();
@@ -250,6 +290,11 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
       }
       // rejection of t_k: Z = sum_v (P(v) - Q(v))+ with the current (P, Q)
       unsigned long long zs = 0;
+      if (cached) {
+        if (loaded_u != u || !loaded_q) load_rows(u, true);
+        const float invd_n = res.invd[res.nrej];
+        for (int i = tid; i < vhi - vlo; i += blockDim.x) zs += to_fix(fmaxf(sP[i] - sQ[i] * invd_n, 0.f));
+      } else
       for (int vb = vlo + tid; vb < vhi; vb += kBatch * blockDim.x) {
         float xs[kBatch], ys[kBatch];  // all loads of a batch in flight together
 #pragma unroll
@@ -284,6 +329,17 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
         res.nrej = j + 1;
       }
       __syncthreads();
+      if (cached) {
+        // P_{n+1} = (P_n - Q_n)+ / Z_n where Z_n > 0 (else P stays), then t_k leaves Q
+        const int j = res.nrej - 1;
+        const float invz = res.invz[j], invd_j = res.invd[j];
+        if (invz > 0.f)
+          for (int i = tid; i < vhi - vlo; i += blockDim.x) sP[i] = fmaxf(sP[i] - sQ[i] * invd_j, 0.f) * invz;
+        __syncthreads();
+        const int t = res.tok[j];
+        if (tid == 0 && t >= vlo && t < vhi) sQ[t - vlo] = 0.f;
+        __syncthreads();
+      }
     }
     if (s_found >= 0) {
       const int c = s_found;
@@ -298,7 +354,16 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
     const int per = (vhi - vlo + (int)blockDim.x - 1) / (int)blockDim.x;
     const int v0 = min(vhi, vlo + tid * per), v1 = min(vhi, v0 + per);
     // fixed-point terms P(v) of v0 + i, i < kBatch (below v1), loads issued together
+    if (cached && loaded_u != u) load_rows(u, false);  // no rejection here: P = p
     auto terms = [&](int vb, unsigned long long* out) {
+      if (cached) {
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int v = vb + i;
+          out[i] = v < v1 ? to_fix(sP[v - vlo]) : 0ull;
+        }
+        return;
+      }
       float xs[kBatch], ys[kBatch];
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
@@ -418,6 +483,18 @@ cudaError_t launch_sample_walk(const void* target, const void* draft, const int3
     if (dev >= 0 && dev < 64) csize_cache[dev][ti].store(csize, std::memory_order_release);
   }
   a.csize = csize;
+  const int span = (V + csize - 1) / csize;
+  const size_t dyn = (size_t)((span + 3) & ~3) * 2 * sizeof(float);
+  a.cached = dyn <= (size_t)kWalkDynCap ? 1 : 0;
+  const size_t dsmem = a.cached ? dyn : 0;
+  if (a.cached) {
+    cudaError_t ea = dtype == TV_BF16
+                         ? cudaFuncSetAttribute(sample_walk_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)dsmem)
+                         : cudaFuncSetAttribute(sample_walk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)dsmem);
+    if (ea != cudaSuccess) return ea;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)B * csize);
   cfg.blockDim = dim3(kWalkThreads);
@@ -429,8 +506,8 @@ cudaError_t launch_sample_walk(const void* target, const void* draft, const int3
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaError_t e = dtype == TV_BF16
-                      ? launch_pdl(sample_walk_kernel<uint16_t>, cfg.gridDim, cfg.blockDim, 0, stream, attr, 1, a)
-                      : launch_pdl(sample_walk_kernel<float>, cfg.gridDim, cfg.blockDim, 0, stream, attr, 1, a);
+                      ? launch_pdl(sample_walk_kernel<uint16_t>, cfg.gridDim, cfg.blockDim, dsmem, stream, attr, 1, a)
+                      : launch_pdl(sample_walk_kernel<float>, cfg.gridDim, cfg.blockDim, dsmem, stream, attr, 1, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
