@@ -81,10 +81,24 @@ __device__ __forceinline__ void eval_pq(const Residual& r, int v, float p, float
 
 constexpr int kWalkClusterMax = 16;  // CTAs per sequence where the device allows it, else 8
 constexpr int kBatch = 5;            // vocabulary elements per thread whose loads are issued together
-constexpr float kFixScale = 72057594037927936.0f;  // 2^56
 constexpr int kWalkDynCap = 180 * 1024;  // dynamic shared memory for the cached rows
 
-__device__ __forceinline__ unsigned long long to_fix(float x) { return __float2ull_rn(x * kFixScale); }
+// x * 2^56 rounded to the nearest integer (ties to even), for x in [0, 1], in 32-bit
+// integer arithmetic: x = m * 2^(e - 150) with the 24-bit significand m, so x * 2^56 =
+// m * 2^(e - 94), a left shift or a right shift with rounding.  (The float to 64-bit
+// integer conversion instruction is slow on this part; this form gives the same value for
+// every float in [0, 1].)
+__device__ __forceinline__ unsigned long long to_fix(float x) {
+  const uint32_t u = __float_as_uint(x);
+  const int e = (int)((u >> 23) & 0xFFu);
+  const uint32_t m = e ? ((u & 0x7FFFFFu) | 0x800000u) : (u & 0x7FFFFFu);
+  const int sh = (e ? e : 1) - 94;
+  if (sh >= 0) return (unsigned long long)m << sh;
+  const int k = -sh;
+  if (k > 24) return 0ull;
+  const uint32_t q = m >> k, rem = m & ((1u << k) - 1u), half = 1u << (k - 1);
+  return (unsigned long long)(q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u));
+}
 
 __device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t addr) {
   unsigned long long v;
@@ -130,6 +144,11 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
   const bool cached = a.cached != 0;
   int loaded_u = -1;   // node whose p (and q) are in sP / sQ
   bool loaded_q = false;
+  // the last rejection's update of sP / sQ, applied by the next sweep over them:
+  // P = (P - q / D_j)+ / Z_j where Z_j > 0, then q(t_j) = 0
+  bool pend = false;
+  float pend_invz = 0.f, pend_invd = 0.f;
+  int pend_tok = -1;
   // Sum of `mine` over the cluster: every CTA gets the same total; *below = the sum over
   // the lower-ranked CTAs
   auto cluster_total = [&](unsigned long long mine, unsigned long long* below) {
@@ -158,31 +177,71 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
     ++npass;
     return tot;
   };
-  // p(v) (and q(v) when `with_q`) of this CTA's share of node u's rows into sP / sQ
+  // p(v) (and q(v) when `with_q`) of this CTA's share of node u's rows into sP / sQ:
+  // 16-byte loads, two per array and thread in flight, where the share is 16-byte aligned
+  // (else element loads)
   auto load_rows = [&](int node, bool with_q) {
     const size_t row = ((size_t)b * N + node) * (size_t)V;
     const float l2p = s_l2p[node], l2q = s_l2q[node];
     const int n = vhi - vlo;
-    for (int i0 = tid; i0 < n; i0 += 4 * (int)blockDim.x) {
-      float xs[4], ys[4];
+    constexpr int kE = 16 / (int)sizeof(T);  // elements per 16-byte vector
+    const bool vec = (row + (size_t)vlo) % kE == 0 &&
+                     ((reinterpret_cast<uintptr_t>(a.target) | reinterpret_cast<uintptr_t>(a.draft)) & 15u) == 0;
+    int start = 0;
+    if (vec) {
+      const int nv = n / kE;
+      const uint4* X = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.target) + row + vlo);
+      const uint4* Y = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.draft) + row + vlo);
+      for (int j0 = tid; j0 < nv; j0 += 2 * (int)blockDim.x) {
+        uint4 xv[2], yv[2];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = i0 + k * (int)blockDim.x;
-        xs[k] = i < n ? ld_logit<T>(a.target, row + vlo + i) : 0.f;
-        ys[k] = (with_q && i < n) ? ld_logit<T>(a.draft, row + vlo + i) : 0.f;
-      }
+        for (int k = 0; k < 2; ++k) {
+          const int j = j0 + k * (int)blockDim.x;
+          xv[k] = j < nv ? __ldg(X + j) : make_uint4(0u, 0u, 0u, 0u);
+          yv[k] = (with_q && j < nv) ? __ldg(Y + j) : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = i0 + k * (int)blockDim.x;
-        if (i < n) {
-          sP[i] = ptx::ex2(fmaf(xs[k], a.c2, -l2p));
-          if (with_q) sQ[i] = ptx::ex2(fmaf(ys[k], a.c2, -l2q));
+        for (int k = 0; k < 2; ++k) {
+          const int j = j0 + k * (int)blockDim.x;
+          if (j >= nv) continue;
+          const uint32_t xw[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
+          const uint32_t yw[4] = {yv[k].x, yv[k].y, yv[k].z, yv[k].w};
+#pragma unroll
+          for (int e = 0; e < kE; ++e) {
+            float xf, yf;
+            if constexpr (sizeof(T) == 2) {  // element e: half e & 1 of word e / 2, low half first
+              xf = __uint_as_float((e & 1) ? (xw[e >> 1] & 0xFFFF0000u) : (xw[e >> 1] << 16));
+              yf = __uint_as_float((e & 1) ? (yw[e >> 1] & 0xFFFF0000u) : (yw[e >> 1] << 16));
+            } else {
+              xf = __uint_as_float(xw[e]);
+              yf = __uint_as_float(yw[e]);
+            }
+            sP[j * kE + e] = ptx::ex2(fmaf(xf, a.c2, -l2p));
+            if (with_q) sQ[j * kE + e] = ptx::ex2(fmaf(yf, a.c2, -l2q));
+          }
         }
       }
+      start = nv * kE;
+    }
+    for (int i = start + tid; i < n; i += blockDim.x) {
+      sP[i] = ptx::ex2(fmaf(ld_logit<T>(a.target, row + vlo + i), a.c2, -l2p));
+      if (with_q) sQ[i] = ptx::ex2(fmaf(ld_logit<T>(a.draft, row + vlo + i), a.c2, -l2q));
     }
     __syncthreads();
     loaded_u = node;
     loaded_q = with_q;
+    pend = false;
+  };
+  // element i of the cached rows with the pending update applied (and stored back)
+  auto cur_pq = [&](int i, float& P, float& q) {
+    P = sP[i];
+    q = sQ[i];
+    if (pend) {
+      if (pend_invz > 0.f) P = fmaxf(P - q * pend_invd, 0.f) * pend_invz;
+      if (vlo + i == pend_tok) q = 0.f;
+      sP[i] = P;
+      sQ[i] = q;
+    }
   };
   if (tid == 0) s_bad = 0;
   __syncthreads();
@@ -293,7 +352,12 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
       if (cached) {
         if (loaded_u != u || !loaded_q) load_rows(u, true);
         const float invd_n = res.invd[res.nrej];
-        for (int i = tid; i < vhi - vlo; i += blockDim.x) zs += to_fix(fmaxf(sP[i] - sQ[i] * invd_n, 0.f));
+        for (int i = tid; i < vhi - vlo; i += blockDim.x) {
+          float P, q;
+          cur_pq(i, P, q);
+          zs += to_fix(fmaxf(P - q * invd_n, 0.f));
+        }
+        pend = false;
       } else
       for (int vb = vlo + tid; vb < vhi; vb += kBatch * blockDim.x) {
         float xs[kBatch], ys[kBatch];  // all loads of a batch in flight together
@@ -330,15 +394,14 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
       }
       __syncthreads();
       if (cached) {
-        // P_{n+1} = (P_n - Q_n)+ / Z_n where Z_n > 0 (else P stays), then t_k leaves Q
+        // P_{n+1} = (P_n - Q_n)+ / Z_n where Z_n > 0 (else P stays), then t_k leaves Q:
+        // applied element by element by the next sweep (each element is read and written
+        // by the same thread)
         const int j = res.nrej - 1;
-        const float invz = res.invz[j], invd_j = res.invd[j];
-        if (invz > 0.f)
-          for (int i = tid; i < vhi - vlo; i += blockDim.x) sP[i] = fmaxf(sP[i] - sQ[i] * invd_j, 0.f) * invz;
-        __syncthreads();
-        const int t = res.tok[j];
-        if (tid == 0 && t >= vlo && t < vhi) sQ[t - vlo] = 0.f;
-        __syncthreads();
+        pend = true;
+        pend_invz = res.invz[j];
+        pend_invd = res.invd[j];
+        pend_tok = res.tok[j];
       }
     }
     if (s_found >= 0) {
@@ -355,6 +418,14 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(WalkArgs a) {
     const int v0 = min(vhi, vlo + tid * per), v1 = min(vhi, v0 + per);
     // fixed-point terms P(v) of v0 + i, i < kBatch (below v1), loads issued together
     if (cached && loaded_u != u) load_rows(u, false);  // no rejection here: P = p
+    if (cached && pend) {  // the last rejection's update, before P is read
+      for (int i = tid; i < vhi - vlo; i += blockDim.x) {
+        float P, q;
+        cur_pq(i, P, q);
+      }
+      pend = false;
+      __syncthreads();
+    }
     auto terms = [&](int vb, unsigned long long* out) {
       if (cached) {
 #pragma unroll
