@@ -83,21 +83,16 @@ constexpr int kWalkClusterMax = 16;  // CTAs per sequence where the device allow
 constexpr int kBatch = 5;            // vocabulary elements per thread whose loads are issued together
 constexpr int kWalkDynCap = 180 * 1024;  // dynamic shared memory for the cached rows
 
-// x * 2^56 rounded to the nearest integer (ties to even), for x in [0, 1], in 32-bit
-// integer arithmetic: x = m * 2^(e - 150) with the 24-bit significand m, so x * 2^56 =
-// m * 2^(e - 94), a left shift or a right shift with rounding.  (The float to 64-bit
-// integer conversion instruction is slow on this part; this form gives the same value for
-// every float in [0, 1].)
+// x * 2^56 rounded to the nearest integer (ties to even), for x in [0, 1], with two
+// 32-bit conversions: t = x * 2^24 and its integer part h are exact, so x * 2^56 =
+// h * 2^32 + (t - h) * 2^32 and only the second term needs rounding.  (The float to
+// 64-bit integer conversion instruction is slow on this part; this form gives the same
+// value for every float in [0, 1].)
 __device__ __forceinline__ unsigned long long to_fix(float x) {
-  const uint32_t u = __float_as_uint(x);
-  const int e = (int)((u >> 23) & 0xFFu);
-  const uint32_t m = e ? ((u & 0x7FFFFFu) | 0x800000u) : (u & 0x7FFFFFu);
-  const int sh = (e ? e : 1) - 94;
-  if (sh >= 0) return (unsigned long long)m << sh;
-  const int k = -sh;
-  if (k > 24) return 0ull;
-  const uint32_t q = m >> k, rem = m & ((1u << k) - 1u), half = 1u << (k - 1);
-  return (unsigned long long)(q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u));
+  const float t = __fmul_rn(x, 0x1p24f);
+  const float h = floorf(t);
+  const uint32_t lo = __float2uint_rn(__fmul_rn(__fsub_rn(t, h), 0x1p32f));
+  return ((unsigned long long)__float2uint_rz(h) << 32) + lo;
 }
 
 __device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t addr) {
