@@ -93,6 +93,23 @@ def test_sampling_workload_full_vocab():
     assert _compare(tgt, drf, par, tok, got, True, cfg["temperature"], cfg["seed"], 0) <= 1
 
 
+@pytest.mark.parametrize("bf16", [False, True])
+def test_vocab_too_large_for_the_cached_rows(bf16):
+    # V = 400,000: a CTA's share of a row (25,000 elements as fp32 p and q, 200 KB at 16
+    # CTAs per sequence) exceeds the walk's shared-memory budget, so every pass reads the
+    # rows from global memory and replays the residual recursion (the path large
+    # vocabularies take); decisions must match the oracle as on the cached path
+    g = synth.rng(400 + int(bf16))
+    B, N, V, T = 3, 24, 400_000, 1.0
+    par, _ = W.trees(g, B, N, 6, V)
+    tgt, drf, tok = W.sampling_logits(g, par, V, bf16, T, noise=1.0)
+    close = 0
+    for rnd in range(2):
+        got = _run(tgt, drf, par, tok, bf16, T, 77, rnd)
+        close += _compare(tgt, drf, par, tok, got, bf16, T, 77, rnd)
+    assert close <= 1
+
+
 def test_identical_distributions_accept_everything():
     g = synth.rng(3)
     N, V = 12, 2048
