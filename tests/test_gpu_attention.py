@@ -346,6 +346,37 @@ def test_persistent_grid_without_workspace_runs_paired_kernel():
         tv.set_attention_variant(0)
 
 
+@pytest.mark.parametrize("n_active", [128, 100, 50])
+def test_kv_multicast_tile_pairs(n_active):
+    # a prefix of at least 64 N keys: the paired 64-key kernel runs its tile pairs in
+    # clusters of two that share each K/V tile (each CTA loads half of its rows into both
+    # rings).  Ragged rows: with 50 active nodes sequence 1's second tile pair has no
+    # active row and only streams the tiles its partner needs; with 100 the two pairs'
+    # key ranges differ.
+    B, Hq, Hkv, D, P, N = 2, 4, 1, 128, 8192, 128
+    g = synth.rng(45 + n_active)
+    par, _ = W.trees(g, B, N, 9, 100)
+    par[1, n_active:] = -1
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, True)
+    out = torch.full((B, Hq, N, D), 7.0, dtype=torch.bfloat16, device=dev())
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    tv.set_attention_variant(3)  # this small grid would otherwise run split single tiles
+    tv.set_attention_splits(1)
+    try:
+        assert tv.tree_attention_plan(B, Hq, Hkv, D, P, N, torch.bfloat16) == (3, 1)
+        tv.tree_attention(to_dev(q, True), to_dev(k, True), to_dev(v, True), i32(par), P, out=out, dev_status=st)
+        torch.cuda.synchronize()
+    finally:
+        tv.set_attention_variant(0)
+        tv.set_attention_splits(0)
+    assert int(st.item()) == 0
+    got = host(out)
+    ref = attention.tree_attention(q, k, v, par, P)
+    assert np.max(np.abs(got[0] - ref[0])) < 2e-2
+    assert np.max(np.abs(got[1, :, :n_active] - ref[1, :, :n_active])) < 2e-2
+    assert (got[1, :, n_active:] == 7.0).all()
+
+
 @pytest.mark.parametrize("splits", [1, 3, 8])
 def test_forced_splits_both_variants(variant, splits):
     # every split count merges to the same result, including more splits than a short

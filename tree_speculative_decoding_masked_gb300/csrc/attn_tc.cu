@@ -72,6 +72,7 @@ struct TcArgs {
   void* out;
   const int32_t* parent;
   int B, Hq, Hkv, N, P, G, NT, MT, splits;
+  int mcast;  // attn_pair2_kernel: tile pairs 2c and 2c + 1 form a cluster sharing each K/V tile
   float c;  // softmax scale * log2(e)
   int32_t* dev_status;
 };
@@ -1135,6 +1136,11 @@ __global__ void __launch_bounds__(kP2Threads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mp = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
   const int hk = blockIdx.y, b = blockIdx.z;
+  // K/V multicast: the two tile pairs of a cluster each load half of every K and V tile
+  // (32 of its 64 rows) into both CTAs' rings; a slot is refilled once both CTAs' products
+  // are done with it (their commits arrive on both CTAs' empty barriers)
+  const bool mc = a.mcast != 0;
+  const uint32_t crank = mc ? (blockIdx.x & 1u) : 0u;
   int i0[2];
 #pragma unroll
   for (int x = 0; x < 2; ++x) i0[x] = (2 * mp + x) * a.NT;
@@ -1145,9 +1151,9 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     ptx::mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kPair2Slots; ++s) {
       ptx::mbar_init(&bars->k_full[s], 1);
-      ptx::mbar_init(&bars->k_empty[s], 2);  // both S issuers
+      ptx::mbar_init(&bars->k_empty[s], mc ? 4 : 2);  // both S issuers (of both CTAs)
       ptx::mbar_init(&bars->v_full[s], 1);
-      ptx::mbar_init(&bars->v_empty[s], 1);
+      ptx::mbar_init(&bars->v_empty[s], mc ? 2 : 1);
     }
     for (int x = 0; x < 2; ++x)
       for (int u = 0; u < 2; ++u) {
@@ -1200,7 +1206,10 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     ptx::fence_proxy_async_smem();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if (mc)
+    ptx::cluster_sync();  // the peer's barriers are initialised before anything arrives on them
+  else
+    __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   // active rows 0..n_act-1 (a ragged batch pads with parent -1): keys and row tiles past
@@ -1218,10 +1227,21 @@ __global__ void __launch_bounds__(kP2Threads, 1)
 #pragma unroll
   for (int x = 0; x < 2; ++x) ntx[x] = max(0, min(t_allx[x], t_begin + tps) - t_begin);
   const int nt = max(ntx[0], ntx[1]);
+  // K/V tiles streamed: with multicast both CTAs of the cluster stream the longer of their
+  // two ranges (the other one's extra tiles are loaded and released, never computed)
+  int nts = nt;
+  if (mc) {
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int i0p = (2 * (mp ^ 1) + x) * a.NT;
+      if (i0p < n_act) nts = max(nts, (a.P + min(n_act, i0p + a.NT) + kBN2 - 1) / kBN2);
+    }
+  }
+  constexpr uint16_t kPairMask = 0x3;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producers
-    if (lane == 0 && nt > 0) {
+    if (lane == 0 && nts > 0) {
       int issued[kPair2Slots] = {0, 0, 0, 0};
       uint32_t qbytes = 0;
 #pragma unroll
@@ -1235,31 +1255,41 @@ __global__ void __launch_bounds__(kP2Threads, 1)
             for (int db = 0; db < C::kDB; ++db)
               ptx::tma_load_3d(sQ + x * C::kQTile + db * C::kQBlock + g * a.NT * 128, &tmQ, &bars->q_full, db * 64,
                                i0[x], b * a.Hq + hk * a.G + g);
-      for (int t = 0; t < nt; ++t) {
+      for (int t = 0; t < nts; ++t) {
         const int ks = t % kPair2Slots;
         if (t >= kPair2Slots && !ptx::mbar_wait(&bars->k_empty[ks], ((t / kPair2Slots) - 1) & 1, abort_flag))
           break;
         unsigned char* dst = sK + ks * C::kTileBytes;
         const int j0 = (t_begin + t) * kBN2;
         ptx::mbar_arrive_expect_tx(&bars->k_full[ks], (uint32_t)C::kTileBytes);
-        for (int db = 0; db < C::kDB; ++db)
-          ptx::tma_load_3d(dst + db * C::kKVBlock, &tmK, &bars->k_full[ks], db * 64, j0, b * a.Hkv + hk);
+        for (int db = 0; db < C::kDB; ++db) {
+          if (mc)
+            ptx::tma_load_3d_mc(dst + db * C::kKVBlock + crank * (kBN2 / 2) * 128, &tmK, &bars->k_full[ks], db * 64,
+                                j0 + (int)crank * (kBN2 / 2), b * a.Hkv + hk, kPairMask);
+          else
+            ptx::tma_load_3d(dst + db * C::kKVBlock, &tmK, &bars->k_full[ks], db * 64, j0, b * a.Hkv + hk);
+        }
         ++issued[ks];
       }
       ptx::mbar_wait(&bars->q_full, 0, abort_flag);
       for (int s = 0; s < kPair2Slots; ++s)
         if (issued[s]) ptx::mbar_wait(&bars->k_full[s], (issued[s] - 1) & 1, abort_flag);
-    } else if (lane == 1 && nt > 0) {
+    } else if (lane == 1 && nts > 0) {
       int issued[kPair2Slots] = {0, 0, 0, 0};
-      for (int t = 0; t < nt; ++t) {
+      for (int t = 0; t < nts; ++t) {
         const int vs = t % kPair2Slots;
         if (t >= kPair2Slots && !ptx::mbar_wait(&bars->v_empty[vs], ((t / kPair2Slots) - 1) & 1, abort_flag))
           break;
         unsigned char* dst = sV + vs * C::kTileBytes;
         const int j0 = (t_begin + t) * kBN2;
         ptx::mbar_arrive_expect_tx(&bars->v_full[vs], (uint32_t)C::kTileBytes);
-        for (int db = 0; db < C::kDB; ++db)
-          ptx::tma_load_3d(dst + db * C::kKVBlock, &tmV, &bars->v_full[vs], db * 64, j0, b * a.Hkv + hk);
+        for (int db = 0; db < C::kDB; ++db) {
+          if (mc)
+            ptx::tma_load_3d_mc(dst + db * C::kKVBlock + crank * (kBN2 / 2) * 128, &tmV, &bars->v_full[vs], db * 64,
+                                j0 + (int)crank * (kBN2 / 2), b * a.Hkv + hk, kPairMask);
+          else
+            ptx::tma_load_3d(dst + db * C::kKVBlock, &tmV, &bars->v_full[vs], db * 64, j0, b * a.Hkv + hk);
+        }
         ++issued[vs];
       }
       for (int s = 0; s < kPair2Slots; ++s)
@@ -1272,10 +1302,10 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     // issued in parallel
     const int x = warp == 1 ? 0 : 1;
     if (lane == 0) {
-      if (nt > 0 && ptx::mbar_wait(&bars->q_full, 0, abort_flag)) {
+      if (nts > 0 && ptx::mbar_wait(&bars->q_full, 0, abort_flag)) {
         constexpr uint32_t idS = ptx::idesc_bf16(kRows, kBN2, false, false);
         const uint32_t qaddr = ptx::smem_addr(sQ + x * C::kQTile);
-        for (int t = 0; t < nt; ++t) {
+        for (int t = 0; t < nts; ++t) {
           const int ks = t % kPair2Slots, buf = t & 1;
           if (!ptx::mbar_wait(&bars->k_full[ks], (t / kPair2Slots) & 1, abort_flag)) break;
           if (t < ntx[x]) {
@@ -1292,7 +1322,10 @@ __global__ void __launch_bounds__(kP2Threads, 1)
             }
             ptx::mma_commit(&bars->s_full[x][buf]);
           }
-          ptx::mma_commit(&bars->k_empty[ks]);  // this tile is done with the K slot
+          if (mc)  // this tile is done with the K slot (in both CTAs' rings)
+            ptx::mma_commit_mc(&bars->k_empty[ks], kPairMask);
+          else
+            ptx::mma_commit(&bars->k_empty[ks]);
         }
       }
       ptx::mma_commit(&bars->s_done[x]);
@@ -1304,7 +1337,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     if (lane == 0) {
       constexpr uint32_t idO = ptx::idesc_bf16(kRows, D, false, true);
       bool ok = true;
-      for (int t = 0; ok && t < nt; ++t) {
+      for (int t = 0; ok && t < nts; ++t) {
         const int vs = t % kPair2Slots, buf = t & 1;
         if (!ptx::mbar_wait(&bars->v_full[vs], (t / kPair2Slots) & 1, abort_flag)) break;
         const uint32_t vaddr = ptx::smem_addr(sV + vs * C::kTileBytes);
@@ -1324,7 +1357,12 @@ __global__ void __launch_bounds__(kP2Threads, 1)
           }
           ptx::mma_commit(&bars->pv_done[x][buf]);
         }
-        if (ok) ptx::mma_commit(&bars->v_empty[vs]);
+        if (ok) {
+          if (mc)
+            ptx::mma_commit_mc(&bars->v_empty[vs], kPairMask);
+          else
+            ptx::mma_commit(&bars->v_empty[vs]);
+        }
       }
       ptx::mma_commit(&bars->o_done);
       ptx::mbar_wait(&bars->o_done, 0, abort_flag);
@@ -1528,6 +1566,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     ptx::cluster_sync();
   }
   __syncthreads();
+  if (mc) ptx::cluster_sync();  // the peer's multicasts and commit arrivals into this CTA are done
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);
@@ -2290,7 +2329,7 @@ static cudaError_t launch_tc_d(const CUtensorMap& mq, const CUtensorMap& mk, con
   const dim3 grid(units * a.splits, Hkv, B), block(tc_threads(kVar), 1, 1);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)a.splits;
+  attr[0].val.clusterDim.x = a.mcast ? 2u : (unsigned)a.splits;  // K/V-sharing tile pairs, or KV splits
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   if constexpr (kVar == 1)
@@ -2343,6 +2382,7 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* ou
   a.MT = plan.mtiles;
   a.c = scale * kLog2e;
   a.dev_status = dev_status;
+  a.mcast = 0;
   int var = 1;
   StreamArgs sa{};
   if (D == 64)
@@ -2363,7 +2403,16 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* ou
                                            align256((size_t)2 * sa.C * 2 * kRows * 8));
     }
   }
-  const int keys = tc_keys(var);  // KV tile rows of the chosen variant
+  // the paired 64-key kernel without KV splits shares each K/V tile between the two tile
+  // pairs of a cluster (each loads half of its rows, multicast to both) where the tile
+  // pairs of a (sequence, KV head) come in twos and the prefix dominates the key range:
+  // half the L2-to-SM traffic lowers power at the power limit (long-context attention
+  // 427.7 -> 417.7 us in a long loop, SM clock 1905 -> 1972 MHz), while with short
+  // prefixes the two CTAs' lockstep and the pair's extra tile cost more (budget-sweep
+  // trees with P = 4 N: +2.5 %)
+  const int pairs = (plan.mtiles + 1) / 2;
+  a.mcast = (var == 3 && a.splits == 1 && pairs % 2 == 0 && (long long)P >= 64LL * N) ? 1 : 0;
+  const int keys = a.mcast ? kBN2 / 2 : tc_keys(var);  // rows of one K/V box
   CUtensorMap mq, mk, mv;
   if (!encode_3d(&mq, q, D, N, (long long)B * Hq, D, (long long)N * D, plan.nt)) return cudaErrorInvalidValue;
   if (!encode_3d(&mk, k, D, P + N, (long long)B * Hkv, D, (long long)S * D, keys)) return cudaErrorInvalidValue;
