@@ -144,7 +144,9 @@ TV_API tv_status tv_set_sm_partition(int verify_sms, int attention_sms);
  *   1  one 128-row tile per CTA
  *   2  paired row tiles: one CTA streams the KV range once for two 128-row tiles
  *   3  paired row tiles with 64-key KV tiles and two S buffers per row tile, so S of
- *      the next KV tile is computed while the softmax of the current one runs
+ *      the next KV tile is computed while the softmax of the current one runs; without
+ *      KV splits and with a prefix of at least 64 N keys, the tile pairs of a KV head run
+ *      as 2-CTA clusters that share each K/V tile (TMA multicast)
  *   4  variant 3's pipeline (in its earlier form with one S issuing thread for both row
  *      tiles) on a persistent grid of one CTA per SM (of the attention's
  *      share): the 64-key steps of all tile pairs are cut into equal contiguous ranges,
