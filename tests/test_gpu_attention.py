@@ -346,15 +346,15 @@ def test_persistent_grid_without_workspace_runs_paired_kernel():
         tv.set_attention_variant(0)
 
 
-@pytest.mark.parametrize("n_active", [128, 100, 50])
-def test_kv_multicast_tile_pairs(n_active):
+@pytest.mark.parametrize("n_active,D", [(128, 128), (100, 128), (50, 128), (100, 64)])
+def test_kv_multicast_tile_pairs(n_active, D):
     # a prefix of at least 64 N keys: the paired 64-key kernel runs its tile pairs in
     # clusters of two that share each K/V tile (each CTA loads half of its rows into both
     # rings).  Ragged rows: with 50 active nodes sequence 1's second tile pair has no
     # active row and only streams the tiles its partner needs; with 100 the two pairs'
     # key ranges differ.
-    B, Hq, Hkv, D, P, N = 2, 4, 1, 128, 8192, 128
-    g = synth.rng(45 + n_active)
+    B, Hq, Hkv, P, N = 2, 4, 1, 8192, 128
+    g = synth.rng(45 + n_active + D)
     par, _ = W.trees(g, B, N, 9, 100)
     par[1, n_active:] = -1
     q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, True)
