@@ -670,7 +670,7 @@ def run_ours(args):
         nt = (128 // G) // 8 * 8
         mtiles = -(-N // nt)
         ctas = B * Hkv * (-(-mtiles // 2) if kern >= 2 else mtiles) * spl
-        if kern in (1, 2, 3) and ctas < n_sm:  # the persistent grid (4) fills the device
+        if kern in (1, 2, 3, 5) and ctas < n_sm:  # the persistent grid (4) fills the device
             parts.append((n_sm - ctas, ctas))
     candidates = [(part, vm) for part in parts for vm in (False, True)]
     trial, trial_reps = {}, {}
@@ -789,7 +789,7 @@ def run_ours(args):
     attn_kernel, attn_splits = tv.tree_attention_plan(B, Hq, Hkv, D, P, N, tdt)
     tv.set_sm_partition(*sm_partition)
     attn_name = ("attn_simt_kernel", "attn_tc_kernel", "attn_pair_kernel", "attn_pair2_kernel",
-                 "attn_stream_kernel")[attn_kernel]
+                 "attn_stream_kernel", "attn_pair2_kernel")[attn_kernel]
     rooflines = {
         attn_name: roofline_entry(attn_name, bytes_attn, flops_alg if bf16 else 0, br["attention"] * 1e-6,
                                   args.workload),

@@ -157,9 +157,17 @@ TV_API tv_status tv_set_sm_partition(int verify_sms, int attention_sms);
  *      slower than that single-issuer variant 3 on the long-context shapes, which run
  *      at the GB300's power limit (more busy SMs lower the clock), so the automatic
  *      choice never takes it.
+ *   5  variant 3 on SM pairs (tcgen05 cta_group::2): the two CTAs of a cluster hold the
+ *      four row tiles of a KV head, and every S and PV product is one M = 256 MMA over
+ *      a row tile of each, issued by the even CTA; each CTA loads half of every K tile
+ *      (32 of its 64 keys) and of every V tile (64 of the 128 value columns).  D = 128
+ *      only, without KV splits, where the tile pairs of a KV head come in twos; other
+ *      shapes run variant 3.  Measured equal to variant 3 on the long-context shape
+ *      (at a higher SM clock under the power limit) and 3-7 % slower on budget-sweep
+ *      trees, so the automatic choice never takes it.
  * All compute the same result (up to fp32 summation order); the switch exists to
  * compare and test them.  Process-wide, host-side; affects launches made after the call.
- * Errors: a value outside 0..4 -> TV_ERR_VALUE.
+ * Errors: a value outside 0..5 -> TV_ERR_VALUE.
  */
 TV_API tv_status tv_set_attention_variant(int variant);
 
@@ -257,7 +265,8 @@ TV_API size_t tv_tree_attention_workspace_size(int B, int Hq, int Hkv, int D, in
  *   *kernel  0 CUDA-core kernel (fp32, or shapes the tensor-core kernels do not take),
  *            1 tensor-core kernel with one 128-row tile per CTA, 2 paired row tiles,
  *            3 paired row tiles with 64-key KV tiles and double-buffered S,
- *            4 variant 3 on a persistent grid (given the queried workspace)
+ *            4 variant 3 on a persistent grid (given the queried workspace),
+ *            5 variant 3 on SM pairs
  *   *splits  KV ranges per tile group, merged in one thread-block cluster (1 for 4)
  * Automatic choice: the variant and split count that minimise a wave model of the run
  * time (waves of resident clusters x (KV tiles per CTA + fixed per-CTA and merge costs))

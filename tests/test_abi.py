@@ -112,11 +112,11 @@ def test_binding_has_no_cpu_fallback(monkeypatch):
 
 def test_settings_and_utility_host_validation(lib):
     # process-wide settings: out-of-range values are refused, valid ones accepted
-    assert lib.tv_set_attention_variant(5) == -8
+    assert lib.tv_set_attention_variant(6) == -8
     assert lib.tv_set_attention_variant(-1) == -8
     assert lib.tv_set_attention_splits(9) == -8
     assert lib.tv_set_sm_partition(-1, 0) == -8
-    for v in (4, 3, 0):
+    for v in (5, 4, 3, 0):
         assert lib.tv_set_attention_variant(v) == 0
     assert lib.tv_set_attention_splits(0) == 0
     # the attention plan query checks its arguments before asking the device anything

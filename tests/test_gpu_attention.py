@@ -232,8 +232,8 @@ def test_bad_tree_flagged():
         assert int(st.item()) & tv.TV_DEV_BAD_TREE
 
 
-@pytest.fixture(params=[1, 2, 3, 4],
-                ids=["one_tile_per_cta", "paired_tiles", "paired_tiles_64key_double_s", "persistent_grid"])
+@pytest.fixture(params=[1, 2, 3, 4, 5],
+                ids=["one_tile_per_cta", "paired_tiles", "paired_tiles_64key_double_s", "persistent_grid", "sm_pairs"])
 def variant(request):
     tv.set_attention_variant(request.param)
     yield request.param
@@ -295,6 +295,56 @@ def test_workloads_sampled_64key_double_s(name):
         _sampled_rows(name, 24, seed_extra=6)
     finally:
         tv.set_attention_variant(0)
+
+
+@pytest.mark.parametrize("name", ["long_context", "sampling", "budget_sweep"])
+def test_workloads_sampled_sm_pairs(name):
+    # every product of the paired 64-key kernel as one M = 256 MMA over the row tiles of
+    # two CTAs (an SM pair), each CTA holding half of every K and V tile
+    tv.set_attention_variant(5)
+    try:
+        cfg = W.WORKLOADS[name]
+        assert tv.tree_attention_plan(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["P"], cfg.get("N", 1024),
+                                      torch.bfloat16) == (5, 1)
+        _sampled_rows(name, 24, seed_extra=7)
+    finally:
+        tv.set_attention_variant(0)
+
+
+@pytest.mark.parametrize("name", ["long_context", "budget_sweep"])
+def test_full_size_tree_dominated_sm_pairs(name):
+    tv.set_attention_variant(5)
+    try:
+        _sampled_rows(name, 32, seed_extra=10, tree_dominated=True)
+    finally:
+        tv.set_attention_variant(0)
+
+
+@pytest.mark.parametrize("n_active", [128, 100, 50, 20])
+def test_sm_pairs_ragged_rows(n_active):
+    # SM pairs over ragged rows: with 50 active nodes sequence 1's second CTA of the pair
+    # has no active row but still holds half of every product; with 20 only the first
+    # row tile of the first CTA is active
+    B, Hq, Hkv, D, P, N = 2, 4, 1, 128, 2000, 128
+    g = synth.rng(61 + n_active)
+    par, _ = W.trees(g, B, N, 9, 100)
+    par[1, n_active:] = -1
+    q, k, v = W.qkv_host(g, B, Hq, Hkv, D, P, N, True)
+    out = torch.full((B, Hq, N, D), 7.0, dtype=torch.bfloat16, device=dev())
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    tv.set_attention_variant(5)
+    try:
+        assert tv.tree_attention_plan(B, Hq, Hkv, D, P, N, torch.bfloat16) == (5, 1)
+        tv.tree_attention(to_dev(q, True), to_dev(k, True), to_dev(v, True), i32(par), P, out=out, dev_status=st)
+        torch.cuda.synchronize()
+    finally:
+        tv.set_attention_variant(0)
+    assert int(st.item()) == 0
+    got = host(out)
+    ref = attention.tree_attention(q, k, v, par, P)
+    assert np.max(np.abs(got[0] - ref[0])) < 2e-2
+    assert np.max(np.abs(got[1, :, :n_active] - ref[1, :, :n_active])) < 2e-2
+    assert (got[1, :, n_active:] == 7.0).all()
 
 
 @pytest.mark.parametrize("name", ["long_context", "sampling", "budget_sweep"])
@@ -421,6 +471,12 @@ def test_attention_plan_query_and_overrides():
         assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16) == (4, 1)
         tv.set_attention_splits(3)  # a forced split count: the paired kernel with splits
         assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16) == (3, 3)
+        tv.set_attention_variant(5)  # SM pairs: D = 128, no splits, tile pairs in twos
+        assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16) == (3, 3)
+        tv.set_attention_splits(0)
+        assert tv.tree_attention_plan(2, 8, 2, 128, 1000, 70, torch.bfloat16) == (5, 1)
+        assert tv.tree_attention_plan(2, 8, 2, 64, 1000, 70, torch.bfloat16)[0] == 3
+        assert tv.tree_attention_plan(2, 8, 2, 128, 96, 64, torch.bfloat16)[0] == 3  # one tile pair
     finally:
         tv.set_attention_variant(0)
         tv.set_attention_splits(0)

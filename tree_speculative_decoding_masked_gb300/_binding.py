@@ -233,7 +233,8 @@ def selftest_bounded_wait(wait_us: int, dev_status):
 
 def set_attention_variant(variant: int):
     """Tensor-core attention kernel: 0 automatic, 1 one 128-row tile per CTA, 2 paired tiles,
-    3 paired tiles with 64-key KV tiles and double-buffered S."""
+    3 paired tiles with 64-key KV tiles and double-buffered S, 4 variant 3 on a persistent
+    grid, 5 variant 3 on SM pairs (M = 256 products over two CTAs; D = 128)."""
     _check("tv_set_attention_variant", load_library().tv_set_attention_variant(int(variant)))
 
 
@@ -292,7 +293,8 @@ def tree_attention_workspace_size(B, Hq, Hkv, D, P, N, dtype) -> int:
 def tree_attention_plan(B, Hq, Hkv, D, P, N, dtype):
     """(kernel, splits) that tree_attention would launch: kernel 0 CUDA cores, 1 one
     128-row tile per CTA, 2 paired row tiles, 3 paired row tiles with 64-key KV tiles and
-    double-buffered S, 4 variant 3 on a persistent grid (tensor cores)."""
+    double-buffered S, 4 variant 3 on a persistent grid, 5 variant 3 on SM pairs (tensor
+    cores)."""
     code = TV_BF16 if dtype == torch.bfloat16 else TV_F32
     kern, spl = ctypes.c_int(0), ctypes.c_int(0)
     _check("tv_tree_attention_plan", load_library().tv_tree_attention_plan(

@@ -100,7 +100,7 @@ tv_status tv_set_sm_partition(int verify_sms, int attention_sms) {
 }
 
 tv_status tv_set_attention_variant(int variant) {
-  if (variant < 0 || variant > 4) return TV_ERR_VALUE;
+  if (variant < 0 || variant > 5) return TV_ERR_VALUE;
   g_attn_variant.store(variant, std::memory_order_relaxed);
   return TV_OK;
 }

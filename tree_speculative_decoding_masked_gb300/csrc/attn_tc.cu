@@ -1117,10 +1117,11 @@ struct Pair2Bars {
   int abort;
 };
 
-template <int D>
+template <int D, bool kPair>
 __global__ void __launch_bounds__(kP2Threads, 1)
     attn_pair2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, TcArgs a) {
+  static_assert(!kPair || D == 128, "the SM-pair form splits V into two 64-column blocks");
   ptx::griddep_launch_dependents();
   using C = Pair2Cfg<D>;
   extern __shared__ unsigned char smem_raw[];
@@ -1139,8 +1140,15 @@ __global__ void __launch_bounds__(kP2Threads, 1)
   // K/V multicast: the two tile pairs of a cluster each load half of every K and V tile
   // (32 of its 64 rows) into both CTAs' rings; a slot is refilled once both CTAs' products
   // are done with it (their commits arrive on both CTAs' empty barriers)
-  const bool mc = a.mcast != 0;
-  const uint32_t crank = mc ? (blockIdx.x & 1u) : 0u;
+  const bool mc = !kPair && a.mcast != 0;
+  // SM pair (kPair): the two CTAs of a cluster (tile pairs 2c and 2c + 1, one KV head)
+  // compute every product as one M = 256 MMA issued by the even CTA: the 128 rows of
+  // each CTA's row tile X form half of product X.  Each CTA loads its half of every K tile
+  // (32 of the 64 keys, both column blocks) and of every V tile (64 of the 128 value
+  // columns); the copies complete on the even CTA's barriers, the MMAs' commits arrive on
+  // both CTAs' barriers, and both CTAs' softmax warps report P on the even CTA's barrier.
+  const uint32_t crank = (mc || kPair) ? (blockIdx.x & 1u) : 0u;
+  const bool issuer_cta = !kPair || crank == 0;
   int i0[2];
 #pragma unroll
   for (int x = 0; x < 2; ++x) i0[x] = (2 * mp + x) * a.NT;
@@ -1158,7 +1166,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     for (int x = 0; x < 2; ++x)
       for (int u = 0; u < 2; ++u) {
         ptx::mbar_init(&bars->s_full[x][u], 1);
-        ptx::mbar_init(&bars->p_full[x][u], 4);
+        ptx::mbar_init(&bars->p_full[x][u], kPair ? 8 : 4);  // the softmax warps of tile X (of both CTAs)
         ptx::mbar_init(&bars->pv_done[x][u], 1);
       }
     ptx::mbar_init(&bars->o_done, 1);
@@ -1168,8 +1176,13 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&bars->tmem_base, C::kTmemCols);
-    ptx::tmem_relinquish();
+    if constexpr (kPair) {
+      ptx::tmem_alloc_pair(&bars->tmem_base, C::kTmemCols);  // with the peer CTA's warp 1
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(&bars->tmem_base, C::kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {  // kernel parameters: safe before the wait
     ptx::prefetch_tmap(&tmQ);
@@ -1206,7 +1219,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     ptx::fence_proxy_async_smem();
   }
   ptx::tc_fence_before();
-  if (mc)
+  if (mc || kPair)
     ptx::cluster_sync();  // the peer's barriers are initialised before anything arrives on them
   else
     __syncthreads();
@@ -1219,7 +1232,13 @@ __global__ void __launch_bounds__(kP2Threads, 1)
   for (int w = 2; w < kP2Threads / 32; ++w) n_act = min(n_act, s_wfirst[w]);
   int t_allx[2];
 #pragma unroll
-  for (int x = 0; x < 2; ++x) t_allx[x] = i0[x] < n_act ? (a.P + min(n_act, i0[x] + a.NT) + kBN2 - 1) / kBN2 : 0;
+  for (int x = 0; x < 2; ++x) {
+    t_allx[x] = i0[x] < n_act ? (a.P + min(n_act, i0[x] + a.NT) + kBN2 - 1) / kBN2 : 0;
+    if constexpr (kPair) {  // product X covers row tile X of both CTAs (no KV splits)
+      const int i0p = (2 * (mp ^ 1) + x) * a.NT;
+      if (i0p < n_act) t_allx[x] = max(t_allx[x], (a.P + min(n_act, i0p + a.NT) + kBN2 - 1) / kBN2);
+    }
+  }
   const int t_all = max(t_allx[0], t_allx[1]);
   const int tps = (t_all + a.splits - 1) / a.splits;
   const int t_begin = split * tps;
@@ -1247,20 +1266,37 @@ __global__ void __launch_bounds__(kP2Threads, 1)
 #pragma unroll
       for (int x = 0; x < 2; ++x)
         if (ntx[x] > 0) qbytes += (uint32_t)(rows_used * 128 * C::kDB);
-      ptx::mbar_arrive_expect_tx(&bars->q_full, qbytes);
+      // SM pair: both CTAs' Q tiles complete on the even CTA's barrier
+      const uint32_t qf = kPair ? ptx::map_cluster(ptx::smem_addr(&bars->q_full), 0) : 0u;
+      if (crank == 0 || !kPair) ptx::mbar_arrive_expect_tx(&bars->q_full, kPair ? 2 * qbytes : qbytes);
 #pragma unroll
       for (int x = 0; x < 2; ++x)
         if (ntx[x] > 0)
           for (int g = 0; g < a.G; ++g)
-            for (int db = 0; db < C::kDB; ++db)
-              ptx::tma_load_3d(sQ + x * C::kQTile + db * C::kQBlock + g * a.NT * 128, &tmQ, &bars->q_full, db * 64,
-                               i0[x], b * a.Hq + hk * a.G + g);
+            for (int db = 0; db < C::kDB; ++db) {
+              unsigned char* dq = sQ + x * C::kQTile + db * C::kQBlock + g * a.NT * 128;
+              if constexpr (kPair)
+                ptx::tma_load_3d_pair(dq, &tmQ, qf, db * 64, i0[x], b * a.Hq + hk * a.G + g);
+              else
+                ptx::tma_load_3d(dq, &tmQ, &bars->q_full, db * 64, i0[x], b * a.Hq + hk * a.G + g);
+            }
       for (int t = 0; t < nts; ++t) {
         const int ks = t % kPair2Slots;
         if (t >= kPair2Slots && !ptx::mbar_wait(&bars->k_empty[ks], ((t / kPair2Slots) - 1) & 1, abort_flag))
           break;
         unsigned char* dst = sK + ks * C::kTileBytes;
         const int j0 = (t_begin + t) * kBN2;
+        if constexpr (kPair) {
+          // this CTA's 32 keys of the tile, both column blocks (4 KB each); the even CTA
+          // expects both halves
+          if (crank == 0) ptx::mbar_arrive_expect_tx(&bars->k_full[ks], (uint32_t)C::kTileBytes);
+          const uint32_t kf = ptx::map_cluster(ptx::smem_addr(&bars->k_full[ks]), 0);
+          for (int db = 0; db < C::kDB; ++db)
+            ptx::tma_load_3d_pair(dst + db * (C::kKVBlock / 2), &tmK, kf, db * 64, j0 + (int)crank * (kBN2 / 2),
+                                  b * a.Hkv + hk);
+          ++issued[ks];
+          continue;
+        }
         ptx::mbar_arrive_expect_tx(&bars->k_full[ks], (uint32_t)C::kTileBytes);
         for (int db = 0; db < C::kDB; ++db) {
           if (mc)
@@ -1271,9 +1307,17 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         }
         ++issued[ks];
       }
-      ptx::mbar_wait(&bars->q_full, 0, abort_flag);
-      for (int s = 0; s < kPair2Slots; ++s)
-        if (issued[s]) ptx::mbar_wait(&bars->k_full[s], (issued[s] - 1) & 1, abort_flag);
+      if constexpr (kPair) {
+        // the copies completed on the even CTA's barriers: wait until the products have
+        // released the last ones (so that none is in flight at exit); the Q tiles were
+        // read by those products
+        for (int s = 0; s < kPair2Slots; ++s)
+          if (issued[s]) ptx::mbar_wait(&bars->k_empty[s], (issued[s] - 1) & 1, abort_flag);
+      } else {
+        ptx::mbar_wait(&bars->q_full, 0, abort_flag);
+        for (int s = 0; s < kPair2Slots; ++s)
+          if (issued[s]) ptx::mbar_wait(&bars->k_full[s], (issued[s] - 1) & 1, abort_flag);
+      }
     } else if (lane == 1 && nts > 0) {
       int issued[kPair2Slots] = {0, 0, 0, 0};
       for (int t = 0; t < nts; ++t) {
@@ -1282,6 +1326,14 @@ __global__ void __launch_bounds__(kP2Threads, 1)
           break;
         unsigned char* dst = sV + vs * C::kTileBytes;
         const int j0 = (t_begin + t) * kBN2;
+        if constexpr (kPair) {
+          // all 64 keys of the tile, this CTA's 64 value columns (one column block)
+          if (crank == 0) ptx::mbar_arrive_expect_tx(&bars->v_full[vs], (uint32_t)C::kTileBytes);
+          ptx::tma_load_3d_pair(dst, &tmV, ptx::map_cluster(ptx::smem_addr(&bars->v_full[vs]), 0), (int)crank * 64, j0,
+                                b * a.Hkv + hk);
+          ++issued[vs];
+          continue;
+        }
         ptx::mbar_arrive_expect_tx(&bars->v_full[vs], (uint32_t)C::kTileBytes);
         for (int db = 0; db < C::kDB; ++db) {
           if (mc)
@@ -1293,7 +1345,8 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         ++issued[vs];
       }
       for (int s = 0; s < kPair2Slots; ++s)
-        if (issued[s]) ptx::mbar_wait(&bars->v_full[s], (issued[s] - 1) & 1, abort_flag);
+        if (issued[s])
+          ptx::mbar_wait(kPair ? &bars->v_empty[s] : &bars->v_full[s], (issued[s] - 1) & 1, abort_flag);
     }
     __syncwarp();
   } else if (warp == 1 || warp == kP2Threads / 32 - 1) {
@@ -1301,9 +1354,9 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     // one issuing thread per row tile: the short (N = 64) S products of the two tiles are
     // issued in parallel
     const int x = warp == 1 ? 0 : 1;
-    if (lane == 0) {
+    if (lane == 0 && issuer_cta) {
       if (nts > 0 && ptx::mbar_wait(&bars->q_full, 0, abort_flag)) {
-        constexpr uint32_t idS = ptx::idesc_bf16(kRows, kBN2, false, false);
+        constexpr uint32_t idS = ptx::idesc_bf16(kPair ? 2 * kRows : kRows, kBN2, false, false);
         const uint32_t qaddr = ptx::smem_addr(sQ + x * C::kQTile);
         for (int t = 0; t < nts; ++t) {
           const int ks = t % kPair2Slots, buf = t & 1;
@@ -1317,25 +1370,38 @@ __global__ void __launch_bounds__(kP2Threads, 1)
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk & 3) * 32;  // 16-element K step inside a 128-byte row
               const uint64_t ad = ptx::sdesc_sw128(qaddr + (kk >> 2) * C::kQBlock + off, 16, 1024);
-              const uint64_t bd = ptx::sdesc_sw128(kaddr + (kk >> 2) * C::kKVBlock + off, 16, 1024);
-              ptx::mma_bf16_ss(tmem + x * kRows + buf * kBN2, ad, bd, idS, kk > 0 ? 1u : 0u);
+              if constexpr (kPair) {  // 32 keys per CTA: column blocks of 4 KB
+                const uint64_t bd = ptx::sdesc_sw128(kaddr + (kk >> 2) * (C::kKVBlock / 2) + off, 16, 1024);
+                ptx::mma_bf16_ss_pair(tmem + x * kRows + buf * kBN2, ad, bd, idS, kk > 0 ? 1u : 0u);
+              } else {
+                const uint64_t bd = ptx::sdesc_sw128(kaddr + (kk >> 2) * C::kKVBlock + off, 16, 1024);
+                ptx::mma_bf16_ss(tmem + x * kRows + buf * kBN2, ad, bd, idS, kk > 0 ? 1u : 0u);
+              }
             }
-            ptx::mma_commit(&bars->s_full[x][buf]);
+            if constexpr (kPair)
+              ptx::mma_commit_pair_mc(&bars->s_full[x][buf], kPairMask);
+            else
+              ptx::mma_commit(&bars->s_full[x][buf]);
           }
-          if (mc)  // this tile is done with the K slot (in both CTAs' rings)
+          if constexpr (kPair)
+            ptx::mma_commit_pair_mc(&bars->k_empty[ks], kPairMask);
+          else if (mc)  // this tile is done with the K slot (in both CTAs' rings)
             ptx::mma_commit_mc(&bars->k_empty[ks], kPairMask);
           else
             ptx::mma_commit(&bars->k_empty[ks]);
         }
       }
-      ptx::mma_commit(&bars->s_done[x]);
+      if constexpr (kPair)
+        ptx::mma_commit_pair(&bars->s_done[x]);
+      else
+        ptx::mma_commit(&bars->s_done[x]);
       ptx::mbar_wait(&bars->s_done[x], 0, abort_flag);
     }
     __syncwarp();
   } else if (warp == kP2Threads / 32 - 2) {
     // ------------------------------------------------------------------ PV issuer
-    if (lane == 0) {
-      constexpr uint32_t idO = ptx::idesc_bf16(kRows, D, false, true);
+    if (lane == 0 && issuer_cta) {
+      constexpr uint32_t idO = ptx::idesc_bf16(kPair ? 2 * kRows : kRows, D, false, true);
       bool ok = true;
       for (int t = 0; ok && t < nts; ++t) {
         const int vs = t % kPair2Slots, buf = t & 1;
@@ -1344,7 +1410,8 @@ __global__ void __launch_bounds__(kP2Threads, 1)
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           if (t >= ntx[x]) continue;
-          if (!ptx::mbar_wait(&bars->p_full[x][buf], (t >> 1) & 1, abort_flag)) {
+          if (!(kPair ? ptx::mbar_wait_cluster(&bars->p_full[x][buf], (t >> 1) & 1, abort_flag)
+                      : ptx::mbar_wait(&bars->p_full[x][buf], (t >> 1) & 1, abort_flag))) {
             ok = false;
             break;
           }
@@ -1353,18 +1420,29 @@ __global__ void __launch_bounds__(kP2Threads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBN2 / 16; ++kk) {
             const uint64_t bd = ptx::sdesc_sw128(vaddr + kk * 16 * 128, C::kKVBlock, 1024);
-            ptx::mma_bf16_ts(tmem + C::kColO + x * kRows, pcol + kk * 8, bd, idO, (t > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (kPair)  // this CTA's 64 value columns of the 128
+              ptx::mma_bf16_ts_pair(tmem + C::kColO + x * kRows, pcol + kk * 8, bd, idO, (t > 0 || kk > 0) ? 1u : 0u);
+            else
+              ptx::mma_bf16_ts(tmem + C::kColO + x * kRows, pcol + kk * 8, bd, idO, (t > 0 || kk > 0) ? 1u : 0u);
           }
-          ptx::mma_commit(&bars->pv_done[x][buf]);
+          if constexpr (kPair)
+            ptx::mma_commit_pair_mc(&bars->pv_done[x][buf], kPairMask);
+          else
+            ptx::mma_commit(&bars->pv_done[x][buf]);
         }
         if (ok) {
-          if (mc)
+          if constexpr (kPair)
+            ptx::mma_commit_pair_mc(&bars->v_empty[vs], kPairMask);
+          else if (mc)
             ptx::mma_commit_mc(&bars->v_empty[vs], kPairMask);
           else
             ptx::mma_commit(&bars->v_empty[vs]);
         }
       }
-      ptx::mma_commit(&bars->o_done);
+      if constexpr (kPair)
+        ptx::mma_commit_pair_mc(&bars->o_done, kPairMask);
+      else
+        ptx::mma_commit(&bars->o_done);
       ptx::mbar_wait(&bars->o_done, 0, abort_flag);
     }
     __syncwarp();
@@ -1447,7 +1525,14 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->p_full[x][buf]);
+      if (lane == 0) {
+        // SM pair: the odd CTA's warps arrive on the even (issuing) CTA's barrier; P is in
+        // TMEM, ordered by the tcgen05 wait and fence above, so no release is needed
+        if (kPair && crank != 0)
+          ptx::mbar_arrive_cluster_relaxed(ptx::map_cluster(ptx::smem_addr(&bars->p_full[x][buf]), 0));
+        else
+          ptx::mbar_arrive(&bars->p_full[x][buf]);
+      }
     }
     // ---- epilogue (as in attn_pair_kernel): every MMA is complete at o_done
     bool have_o = false;
@@ -1566,10 +1651,15 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     ptx::cluster_sync();
   }
   __syncthreads();
-  if (mc) ptx::cluster_sync();  // the peer's multicasts and commit arrivals into this CTA are done
+  // the peer's multicasts and commit arrivals into this CTA are done (SM pair: and the
+  // pair's MMAs, which read and write both CTAs)
+  if (mc || kPair) ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, C::kTmemCols);
+    if constexpr (kPair)
+      ptx::tmem_dealloc_pair(tmem, C::kTmemCols);
+    else
+      ptx::tmem_dealloc(tmem, C::kTmemCols);
   }
   if (threadIdx.x == 0 && bars->abort) set_dev_status(a.dev_status, TV_DEV_TIMEOUT);
 }
@@ -2166,19 +2256,21 @@ static size_t stream_ws_bytes(int C, int D, long long units) {
 // Kernel variants: 1 attn_tc_kernel (one 128-row tile per CTA, 128-key KV tiles),
 // 2 attn_pair_kernel (two row tiles, 128-key KV tiles), 3 attn_pair2_kernel (two row
 // tiles, 64-key KV tiles, two S buffers per row tile), 4 attn_stream_kernel (variant 3's
-// pipeline on a persistent grid, equal work per SM).
+// pipeline on a persistent grid, equal work per SM), 5 attn_pair2_kernel on SM pairs
+// (variant 3 with every product an M = 256 MMA over two CTAs' row tiles; D = 128).
 template <int D, int kVar>
 static const void* tc_kernel_fn() {
   if constexpr (kVar == 1) return reinterpret_cast<const void*>(attn_tc_kernel<D>);
   else if constexpr (kVar == 2) return reinterpret_cast<const void*>(attn_pair_kernel<D>);
-  else if constexpr (kVar == 3) return reinterpret_cast<const void*>(attn_pair2_kernel<D>);
+  else if constexpr (kVar == 3) return reinterpret_cast<const void*>(attn_pair2_kernel<D, false>);
+  else if constexpr (kVar == 5) return reinterpret_cast<const void*>(attn_pair2_kernel<D, true>);
   else return reinterpret_cast<const void*>(attn_stream_kernel<D>);
 }
 template <int D, int kVar>
 static constexpr int tc_smem() {
   return kVar == 1 ? TcCfg<D>::kSmemAlloc : kVar == 2 ? PairCfg<D>::kSmemAlloc : Pair2Cfg<D>::kSmemAlloc;
 }
-constexpr int tc_threads(int var) { return var == 3 ? kP2Threads : kThreads; }
+constexpr int tc_threads(int var) { return var == 3 || var == 5 ? kP2Threads : kThreads; }
 constexpr int tc_keys(int var) { return var >= 3 ? kBN2 : kBN; }  // keys per KV tile
 
 // How many clusters of `s` CTAs of variant kVar can be resident at once on the current
@@ -2259,7 +2351,7 @@ static void choose_plan(int B, int Hkv, int NT, int mtiles, int P, int N, int* v
   const int variant = attention_variant();
   const int forced = attention_splits();
   const int t_all128 = (P + N + kBN - 1) / kBN;
-  const int fixed = variant == 4 ? 3 : variant;  // variant 4 falls back to 3 where it cannot run
+  const int fixed = variant >= 4 ? 3 : variant;  // variants 4 and 5 fall back to 3 where they cannot run
   double best_cost = 1e300;
   *var = 1;
   *splits = 1;
@@ -2278,6 +2370,18 @@ static void choose_plan(int B, int Hkv, int NT, int mtiles, int P, int N, int* v
         *var = v;
         *splits = s;
       }
+    }
+  }
+  if constexpr (D == 128) {
+    // the SM-pair form (forced only): no KV splits, the tile pairs of a (sequence, KV
+    // head) in twos.  It ties variant 3 on the long-context shape (402 us; 420 us in a
+    // power-capped loop at a higher SM clock) and is 3-7 % slower on budget-sweep trees:
+    // each SM's tensor pipe still runs 24 MMAs per 64-key step, the number that sets the
+    // pace of variant 3
+    const int pairs = (mtiles + 1) / 2;
+    if (variant == 5 && forced <= 1 && pairs % 2 == 0 && max_active_clusters<D, 5>(1) > 0) {
+      *var = 5;
+      *splits = 1;
     }
   }
   if (variant == 4 && forced <= 1 && max_active_clusters<D, 3>(1) > 0) {
@@ -2329,15 +2433,18 @@ static cudaError_t launch_tc_d(const CUtensorMap& mq, const CUtensorMap& mk, con
   const dim3 grid(units * a.splits, Hkv, B), block(tc_threads(kVar), 1, 1);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.mcast ? 2u : (unsigned)a.splits;  // K/V-sharing tile pairs, or KV splits
+  // SM pairs, K/V-sharing tile pairs, or KV splits
+  attr[0].val.clusterDim.x = (kVar == 5 || a.mcast) ? 2u : (unsigned)a.splits;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   if constexpr (kVar == 1)
     e = launch_pdl(attn_tc_kernel<D>, grid, block, smem, stream, attr, 1, mq, mk, mv, a);
   else if constexpr (kVar == 2)
     e = launch_pdl(attn_pair_kernel<D>, grid, block, smem, stream, attr, 1, mq, mk, mv, a);
+  else if constexpr (kVar == 3)
+    e = launch_pdl(attn_pair2_kernel<D, false>, grid, block, smem, stream, attr, 1, mq, mk, mv, a);
   else
-    e = launch_pdl(attn_pair2_kernel<D>, grid, block, smem, stream, attr, 1, mq, mk, mv, a);
+    e = launch_pdl(attn_pair2_kernel<D, true>, grid, block, smem, stream, attr, 1, mq, mk, mv, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -2412,11 +2519,14 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* ou
   // trees with P = 4 N: +2.5 %)
   const int pairs = (plan.mtiles + 1) / 2;
   a.mcast = (var == 3 && a.splits == 1 && pairs % 2 == 0 && (long long)P >= 64LL * N) ? 1 : 0;
-  const int keys = a.mcast ? kBN2 / 2 : tc_keys(var);  // rows of one K/V box
+  // rows of one K / V box: each CTA of an SM pair loads 32 keys of a K tile and all 64
+  // keys of its half of a V tile
+  const int kkeys = (var == 5 || a.mcast) ? kBN2 / 2 : tc_keys(var);
+  const int vkeys = var == 5 ? kBN2 : kkeys;
   CUtensorMap mq, mk, mv;
   if (!encode_3d(&mq, q, D, N, (long long)B * Hq, D, (long long)N * D, plan.nt)) return cudaErrorInvalidValue;
-  if (!encode_3d(&mk, k, D, P + N, (long long)B * Hkv, D, (long long)S * D, keys)) return cudaErrorInvalidValue;
-  if (!encode_3d(&mv, v, D, P + N, (long long)B * Hkv, D, (long long)S * D, keys)) return cudaErrorInvalidValue;
+  if (!encode_3d(&mk, k, D, P + N, (long long)B * Hkv, D, (long long)S * D, kkeys)) return cudaErrorInvalidValue;
+  if (!encode_3d(&mv, v, D, P + N, (long long)B * Hkv, D, (long long)S * D, vkeys)) return cudaErrorInvalidValue;
   if (D == 64) {
     if (var == 1) return launch_tc_d<64, 1>(mq, mk, mv, a, B, Hkv, stream);
     if (var == 2) return launch_tc_d<64, 2>(mq, mk, mv, a, B, Hkv, stream);
@@ -2426,6 +2536,7 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* ou
   if (var == 1) return launch_tc_d<128, 1>(mq, mk, mv, a, B, Hkv, stream);
   if (var == 2) return launch_tc_d<128, 2>(mq, mk, mv, a, B, Hkv, stream);
   if (var == 4) return launch_stream_d<128>(mq, mk, mv, a, sa, stream);
+  if (var == 5) return launch_tc_d<128, 5>(mq, mk, mv, a, B, Hkv, stream);
   return launch_tc_d<128, 3>(mq, mk, mv, a, B, Hkv, stream);
 }
 

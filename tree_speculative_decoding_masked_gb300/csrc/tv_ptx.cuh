@@ -59,6 +59,44 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   return mbar_wait_limit(bar, parity, abort, TV_WAIT_NS);
 }
 
+// arrive on an mbarrier of any CTA of the cluster (shared::cluster address) without
+// releasing this thread's generic-memory writes: for hand-offs of TMEM data, which
+// tcgen05.wait::st and tcgen05.fence::before_thread_sync order before the arrival (a
+// cluster-scope release costs ~1000 cycles per arrival on this part)
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait for a phase completed by arrivals from other CTAs of the cluster (acquire at
+// cluster scope); the same limit and abort flag
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > TV_WAIT_NS) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Device-scope fetch-and-add with acquire-release semantics: after a CTA barrier, one
 // thread's call publishes the CTA's earlier writes and, if it observes the other CTAs'
 // contributions, makes their writes visible to the CTA after the next barrier.
@@ -96,6 +134,17 @@ __device__ __forceinline__ void tma_load_3d_mc(void* dst, const void* tmap, uint
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
       "[%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "h"(mask)
+      : "memory");
+}
+// SM-pair form (tcgen05 cta_group::2): the box lands in this CTA's shared memory and its
+// bytes complete on the mbarrier at shared::cluster address `bar_cluster`, which may be
+// the peer CTA's (the one issuing the pair's MMAs)
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const void* tmap, uint32_t bar_cluster, int x, int y,
+                                                 int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
       : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
@@ -188,6 +237,52 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 // the same, arriving on the mbarrier at this offset in each CTA of the cluster in `mask`
 __device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_addr(bar)),
+               "h"(mask)
+               : "memory");
+}
+
+// ---- the SM-pair forms (cta_group::2): two CTAs of a cluster (ranks 2c, 2c + 1) hold one
+// M = 256 product, 128 rows each, in the same TMEM columns.  One warp of each CTA
+// allocates and frees the columns together; the even CTA issues the MMAs, whose A rows
+// and half of whose B columns (N / 2 each, the even CTA's first) sit at the same
+// shared-memory offsets in both CTAs.  A kernel uses either these forms or the ones above.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrives on the mbarrier at this offset in this CTA once this thread's pair MMAs are done
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+// the same, on the mbarrier at this offset in each CTA of `mask`
+__device__ __forceinline__ void mma_commit_pair_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
                    smem_addr(bar)),
                "h"(mask)
                : "memory");
