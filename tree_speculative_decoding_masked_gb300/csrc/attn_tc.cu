@@ -1117,6 +1117,43 @@ struct Pair2Bars {
   int abort;
 };
 
+// One S product of attn_pair2_kernel (D = 128): the 8 MMAs of K = 16 each from one asm
+// block, the first overwriting S.  A descriptors come precomputed (the Q tile's never
+// change); the K tile's follow from its first one by constant steps in 16-byte units:
+// 32 bytes per K step inside a 128-byte row, 8 KB to the second column block.  Issuing
+// threads share their SM sub-partitions with softmax warps, so fewer instructions per MMA
+// issue the short (N = 64) products sooner.
+__device__ __forceinline__ void s_product_d128(uint32_t d, const uint64_t (&ad)[8], uint64_t bd0, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b32 z;\n\tmov.b32 z, 0;\n\tsetp.ne.b32 p0, z, 0;\n\tsetp.eq.b32 p1, z, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, p0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, p1;\n\t}" ::"r"(d),
+      "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]), "l"(ad[4]), "l"(ad[5]), "l"(ad[6]), "l"(ad[7]),
+      "l"(bd0), "l"(bd0 + 2), "l"(bd0 + 4), "l"(bd0 + 6), "l"(bd0 + 512), "l"(bd0 + 514), "l"(bd0 + 516),
+      "l"(bd0 + 518), "r"(idesc)
+      : "memory");
+}
+// One PV product (D = 128, 64 keys): 4 MMAs of K = 16 with P read from TMEM (8 columns per
+// 16 keys) and V tile rows 16 apart (2 KB = 128 descriptor units); the first accumulates
+// only when acc0 != 0.
+__device__ __forceinline__ void pv_product_d128(uint32_t d, uint32_t a, uint64_t vd0, uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b32 z;\n\tmov.b32 z, 0;\n\tsetp.ne.b32 p0, %10, 0;\n\tsetp.eq.b32 p1, z, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %9, p0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %9, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %9, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %9, p1;\n\t}" ::"r"(d),
+      "r"(a), "r"(a + 8), "r"(a + 16), "r"(a + 24), "l"(vd0), "l"(vd0 + 128), "l"(vd0 + 256), "l"(vd0 + 384),
+      "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
 template <int D, bool kPair>
 __global__ void __launch_bounds__(kP2Threads, 1)
     attn_pair2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -1358,6 +1395,10 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       if (nts > 0 && ptx::mbar_wait(&bars->q_full, 0, abort_flag)) {
         constexpr uint32_t idS = ptx::idesc_bf16(kPair ? 2 * kRows : kRows, kBN2, false, false);
         const uint32_t qaddr = ptx::smem_addr(sQ + x * C::kQTile);
+        uint64_t adq[8];  // the Q tile's A descriptors, one per 16-element K step
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          adq[kk] = ptx::sdesc_sw128(qaddr + (kk >> 2) * C::kQBlock + (kk & 3) * 32, 16, 1024);
         for (int t = 0; t < nts; ++t) {
           const int ks = t % kPair2Slots, buf = t & 1;
           if (!ptx::mbar_wait(&bars->k_full[ks], (t / kPair2Slots) & 1, abort_flag)) break;
@@ -1366,6 +1407,9 @@ __global__ void __launch_bounds__(kP2Threads, 1)
             if (t >= 2 && !ptx::mbar_wait(&bars->pv_done[x][buf], ((t - 2) >> 1) & 1, abort_flag)) break;
             ptx::tc_fence_after();
             const uint32_t kaddr = ptx::smem_addr(sK + ks * C::kTileBytes);
+            if constexpr (!kPair && D == 128) {
+              s_product_d128(tmem + x * kRows + buf * kBN2, adq, ptx::sdesc_sw128(kaddr, 16, 1024), idS);
+            } else
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk & 3) * 32;  // 16-element K step inside a 128-byte row
@@ -1417,6 +1461,10 @@ __global__ void __launch_bounds__(kP2Threads, 1)
           }
           ptx::tc_fence_after();
           const uint32_t pcol = tmem + x * kRows + buf * kBN2;  // P: 8 columns per 16 keys
+          if constexpr (!kPair && D == 128) {
+            pv_product_d128(tmem + C::kColO + x * kRows, pcol, ptx::sdesc_sw128(vaddr, C::kKVBlock, 1024), idO,
+                            t > 0 ? 1u : 0u);
+          } else
 #pragma unroll
           for (int kk = 0; kk < kBN2 / 16; ++kk) {
             const uint64_t bd = ptx::sdesc_sw128(vaddr + kk * 16 * 128, C::kKVBlock, 1024);
